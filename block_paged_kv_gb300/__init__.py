@@ -1,0 +1,314 @@
+"""GB300-native block-paged KV attention: Python binding of ``libpkv.so``.
+
+The functions here only marshal arguments (torch tensors -> device pointers,
+sizes and the current CUDA stream) into the C ABI declared in
+``include/pkv.h``; every step of the computation runs in the library's
+CUDA kernels.  There is no fallback: if the library is missing, importing
+this package raises.
+
+Layouts (see ``include/pkv.h``): pools ``[num_blocks, num_kv_heads,
+block_size, head_dim]``; ``q``/``out`` ``[batch, num_q_heads, head_dim]``
+(prefill: ``[sum C, num_q_heads, head_dim]``); block tables int32
+``[batch, max_blocks_per_seq]``; ``seq_lens`` int32 ``[batch]`` counting the
+tokens appended this step.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional, Tuple
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpkv.so")
+
+PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA, PKV_ERR_WORKSPACE = range(5)
+PKV_F32, PKV_BF16 = 0, 1
+DEV_BAD_BLOCK, DEV_BAD_SLOT, DEV_BAD_LEN, DEV_BAD_PREFIX, DEV_TIMEOUT = 1, 2, 4, 8, 16
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is missing: build it first "
+                      "(python -c 'import __graft_entry__ as g; g.build()')")
+_lib = ctypes.CDLL(LIB_PATH)
+
+
+class _Pool(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("num_blocks", ctypes.c_int32),
+                ("block_size", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("dtype", ctypes.c_int)]
+
+
+class _Prefix(ctypes.Structure):
+    _fields_ = [("num_groups", ctypes.c_int32), ("max_group_rows", ctypes.c_int32),
+                ("max_prefix_blocks", ctypes.c_int32), ("group_of_row", ctypes.c_void_p),
+                ("prefix_blocks", ctypes.c_void_p)]
+
+
+_vp, _i32, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+_PP, _XP = ctypes.POINTER(_Pool), ctypes.POINTER(_Prefix)
+
+_lib.paged_kv_append.argtypes = [_PP, _vp, _i32, _vp, _vp, _vp, _vp]
+_lib.paged_kv_append.restype = ctypes.c_int
+_lib.paged_decode_workspace_size.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32, _i32, _XP]
+_lib.paged_decode_workspace_size.restype = _sz
+_lib.paged_decode_attention.argtypes = [_vp, _i32, _PP, _vp, _i32, _vp, _i32, _i32, _i32,
+                                        ctypes.c_float, _vp, _vp, _sz, _XP, _vp, _vp]
+_lib.paged_decode_attention.restype = ctypes.c_int
+_lib.paged_prefill_workspace_size.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32]
+_lib.paged_prefill_workspace_size.restype = _sz
+_lib.paged_prefill_chunk_attention.argtypes = [_vp, _vp, _i32, _PP, _vp, _i32, _vp, _i32, _i32,
+                                               _i32, _i32, ctypes.c_float, _vp, _vp, _sz, _vp, _vp]
+_lib.paged_prefill_chunk_attention.restype = ctypes.c_int
+_lib.pkv_status_string.argtypes = [ctypes.c_int]
+_lib.pkv_status_string.restype = ctypes.c_char_p
+_lib.pkv_slot_mapping_host.argtypes = [_vp, _i32, _i32, _i32, _vp, _vp, _i32, _i32, _vp]
+_lib.pkv_slot_mapping_host.restype = ctypes.c_int
+_lib.pkv_prefix_groups_host.argtypes = [_vp, _i32, _vp, _i32, _i32, _vp, _vp]
+_lib.pkv_prefix_groups_host.restype = _i32
+_lib.pkv_set_decode_split_blocks.argtypes = [_i32]
+_lib.pkv_set_decode_split_blocks.restype = _i32
+_lib.pkv_decode_plan.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32, _i32,
+                                 ctypes.POINTER(_i32)]
+_lib.pkv_decode_plan.restype = _i32
+_lib.pkv_version.restype = ctypes.c_char_p
+
+EXPORTED = ["paged_kv_append", "paged_decode_workspace_size", "paged_decode_attention",
+            "paged_prefill_workspace_size", "paged_prefill_chunk_attention", "pkv_status_string",
+            "pkv_slot_mapping_host", "pkv_prefix_groups_host", "pkv_set_decode_split_blocks",
+            "pkv_decode_plan", "pkv_version"]
+
+
+class PkvError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn}: {_lib.pkv_status_string(code).decode()} (status {code})")
+        self.code = code
+
+
+def _check(fn: str, code: int) -> None:
+    if code != PKV_OK:
+        raise PkvError(fn, code)
+
+
+def _dtype_code(t: torch.dtype) -> int:
+    if t == torch.float32:
+        return PKV_F32
+    if t == torch.bfloat16:
+        return PKV_BF16
+    raise TypeError(f"unsupported dtype {t}: the pools hold float32 or bfloat16")
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(device: torch.device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _require(cond: bool, msg: str) -> None:
+    if not cond:
+        raise ValueError(msg)
+
+
+def _pool(k_pool: torch.Tensor, v_pool: torch.Tensor) -> _Pool:
+    _require(k_pool.dim() == 4 and k_pool.shape == v_pool.shape,
+             "pools are [num_blocks, num_kv_heads, block_size, head_dim] and K/V match")
+    _require(k_pool.dtype == v_pool.dtype, "K and V pools share a dtype")
+    _require(k_pool.is_cuda and v_pool.is_cuda, "pools live on the GPU")
+    _require(k_pool.is_contiguous() and v_pool.is_contiguous(), "pools are contiguous")
+    nb, hkv, bs, d = k_pool.shape
+    return _Pool(k_pool.data_ptr(), v_pool.data_ptr(), nb, bs, hkv, d, _dtype_code(k_pool.dtype))
+
+
+def _i32_dev(t: torch.Tensor, name: str, device) -> torch.Tensor:
+    _require(t.dtype == torch.int32 and t.is_contiguous() and t.device == device,
+             f"{name} is a contiguous int32 tensor on {device}")
+    return t
+
+
+@dataclass
+class PrefixDesc:
+    """Shared-prefix descriptor: device arrays plus the host-side bounds."""
+    num_groups: int
+    max_group_rows: int
+    max_prefix_blocks: int
+    group_of_row: torch.Tensor   # int32 [batch] on the device
+    prefix_blocks: torch.Tensor  # int32 [num_groups] (at least 1 element) on the device
+
+    def _c(self) -> _Prefix:
+        return _Prefix(self.num_groups, self.max_group_rows, self.max_prefix_blocks,
+                       self.group_of_row.data_ptr(), self.prefix_blocks.data_ptr())
+
+
+def prefix_groups_host(block_tables: np.ndarray, seq_lens: np.ndarray,
+                       block_size: int) -> Tuple[np.ndarray, np.ndarray]:
+    """Shared-prefix groups of host block tables (library helper)."""
+    t = np.ascontiguousarray(block_tables, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    B = t.shape[0]
+    gor = np.empty(B, dtype=np.int32)
+    pb = np.zeros(max(B, 1), dtype=np.int32)
+    n = _lib.pkv_prefix_groups_host(t.ctypes.data, t.shape[1], sl.ctypes.data, B, block_size,
+                                    gor.ctypes.data, pb.ctypes.data)
+    if n < 0:
+        raise ValueError("pkv_prefix_groups_host: invalid arguments")
+    return gor, pb[:n].copy()
+
+
+def make_prefix_desc(block_tables: np.ndarray, seq_lens: np.ndarray, block_size: int,
+                     device) -> Optional[PrefixDesc]:
+    """Derive the groups on the host and upload them; None when no rows share."""
+    gor, pb = prefix_groups_host(block_tables, seq_lens, block_size)
+    if len(pb) == 0:
+        return None
+    counts = np.bincount(gor[gor >= 0], minlength=len(pb))
+    return PrefixDesc(len(pb), int(counts.max()), int(pb.max()),
+                      torch.from_numpy(gor).to(device), torch.from_numpy(pb).to(device))
+
+
+def slot_mapping_host(block_tables: np.ndarray, num_blocks: int, rows: np.ndarray,
+                      positions: np.ndarray, block_size: int) -> np.ndarray:
+    """slot = table[row][pos // bs] * bs + pos % bs (library helper); raises on a missing entry."""
+    t = np.ascontiguousarray(block_tables, dtype=np.int32)
+    r = np.ascontiguousarray(rows, dtype=np.int32)
+    p = np.ascontiguousarray(positions, dtype=np.int32)
+    out = np.empty(r.shape[0], dtype=np.int32)
+    code = _lib.pkv_slot_mapping_host(t.ctypes.data, t.shape[1], t.shape[0], num_blocks,
+                                      r.ctypes.data, p.ctypes.data, r.shape[0], block_size,
+                                      out.ctypes.data)
+    _check("pkv_slot_mapping_host", code)
+    return out
+
+
+def paged_kv_append(k_pool: torch.Tensor, v_pool: torch.Tensor, slot_mapping: torch.Tensor,
+                    k_new: torch.Tensor, v_new: torch.Tensor,
+                    status: Optional[torch.Tensor] = None) -> None:
+    """Write ``k_new``/``v_new`` [T, Hkv, D] into the pools at ``slot_mapping`` [T]."""
+    pool = _pool(k_pool, v_pool)
+    dev = k_pool.device
+    _i32_dev(slot_mapping, "slot_mapping", dev)
+    _require(k_new.shape == v_new.shape and k_new.dim() == 3 and
+             k_new.shape[1:] == (pool.num_kv_heads, pool.head_dim),
+             "k_new/v_new are [T, num_kv_heads, head_dim]")
+    _require(k_new.dtype == k_pool.dtype and v_new.dtype == k_pool.dtype, "new rows match the pool dtype")
+    _require(k_new.is_contiguous() and v_new.is_contiguous(), "new rows are contiguous")
+    _require(slot_mapping.shape[0] == k_new.shape[0], "one slot per new token")
+    _check("paged_kv_append", _lib.paged_kv_append(
+        ctypes.byref(pool), slot_mapping.data_ptr(), k_new.shape[0], k_new.data_ptr(),
+        v_new.data_ptr(), _ptr(status), _stream(dev)))
+
+
+def decode_workspace_size(batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                          block_size: int, max_seq_len: int, window: int = 0,
+                          prefix: Optional[PrefixDesc] = None) -> int:
+    px = ctypes.byref(prefix._c()) if prefix is not None else None
+    return int(_lib.paged_decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim,
+                                                block_size, max_seq_len, window, px))
+
+
+def alloc_workspace(nbytes: int, device) -> torch.Tensor:
+    """A 256-byte-aligned device buffer (torch allocations are)."""
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def paged_decode_attention(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                           block_tables: torch.Tensor, seq_lens: torch.Tensor, window: int,
+                           scale: float, out: Optional[torch.Tensor] = None,
+                           workspace: Optional[torch.Tensor] = None,
+                           max_seq_len: Optional[int] = None,
+                           prefix: Optional[PrefixDesc] = None,
+                           status: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Batched paged decode attention; returns ``out`` [B, Hq, D].
+
+    ``max_seq_len`` is a host bound on ``seq_lens`` (default: the block-table
+    capacity); ``workspace`` defaults to a fresh buffer of the queried size.
+    """
+    pool = _pool(k_pool, v_pool)
+    dev = k_pool.device
+    _require(q.dim() == 3 and q.shape[2] == pool.head_dim and q.dtype == k_pool.dtype and
+             q.is_contiguous() and q.device == dev, "q is [B, Hq, D], contiguous, pool dtype")
+    B, hq, D = q.shape
+    _i32_dev(block_tables, "block_tables", dev)
+    _i32_dev(seq_lens, "seq_lens", dev)
+    _require(block_tables.dim() == 2 and block_tables.shape[0] == B and seq_lens.shape == (B,),
+             "block_tables [B, max_blocks], seq_lens [B]")
+    width = block_tables.shape[1]
+    if max_seq_len is None:
+        max_seq_len = width * pool.block_size
+    if out is None:
+        out = torch.empty_like(q)
+    _require(out.shape == q.shape and out.dtype == q.dtype and out.is_contiguous(), "out matches q")
+    need = decode_workspace_size(B, hq, pool.num_kv_heads, D, pool.block_size, max_seq_len, window,
+                                 prefix)
+    if workspace is None:
+        workspace = alloc_workspace(need, dev)
+    px = ctypes.byref(prefix._c()) if prefix is not None else None
+    _check("paged_decode_attention", _lib.paged_decode_attention(
+        q.data_ptr(), hq, ctypes.byref(pool), block_tables.data_ptr(), width, seq_lens.data_ptr(),
+        B, max_seq_len, window, float(scale), out.data_ptr(), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), px, _ptr(status), _stream(dev)))
+    return out
+
+
+def prefill_workspace_size(batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                           block_size: int, max_q_len: int, max_seq_len: int,
+                           window: int = 0) -> int:
+    return int(_lib.paged_prefill_workspace_size(batch, num_q_heads, num_kv_heads, head_dim,
+                                                 block_size, max_q_len, max_seq_len, window))
+
+
+def paged_prefill_chunk_attention(q: torch.Tensor, cu_q_lens: torch.Tensor, k_pool: torch.Tensor,
+                                  v_pool: torch.Tensor, block_tables: torch.Tensor,
+                                  seq_lens: torch.Tensor, max_q_len: int, window: int,
+                                  scale: float, out: Optional[torch.Tensor] = None,
+                                  workspace: Optional[torch.Tensor] = None,
+                                  max_seq_len: Optional[int] = None,
+                                  status: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Chunked prefill against the paged prefix; returns ``out`` [sum C, Hq, D]."""
+    pool = _pool(k_pool, v_pool)
+    dev = k_pool.device
+    _require(q.dim() == 3 and q.shape[2] == pool.head_dim and q.dtype == k_pool.dtype and
+             q.is_contiguous() and q.device == dev, "q is [sum C, Hq, D], contiguous, pool dtype")
+    _i32_dev(cu_q_lens, "cu_q_lens", dev)
+    _i32_dev(block_tables, "block_tables", dev)
+    _i32_dev(seq_lens, "seq_lens", dev)
+    B = seq_lens.shape[0]
+    _require(cu_q_lens.shape == (B + 1,) and block_tables.shape[0] == B,
+             "cu_q_lens [B+1], block_tables [B, max_blocks]")
+    width = block_tables.shape[1]
+    if max_seq_len is None:
+        max_seq_len = width * pool.block_size
+    if out is None:
+        out = torch.empty_like(q)
+    hq = q.shape[1]
+    need = prefill_workspace_size(B, hq, pool.num_kv_heads, pool.head_dim, pool.block_size,
+                                  max_q_len, max_seq_len, window)
+    if workspace is None:
+        workspace = alloc_workspace(need, dev)
+    _check("paged_prefill_chunk_attention", _lib.paged_prefill_chunk_attention(
+        q.data_ptr(), cu_q_lens.data_ptr(), hq, ctypes.byref(pool), block_tables.data_ptr(),
+        width, seq_lens.data_ptr(), B, max_q_len, max_seq_len, window, float(scale),
+        out.data_ptr(), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+        _ptr(status), _stream(dev)))
+    return out
+
+
+def set_decode_split_blocks(n: int) -> int:
+    """Diagnostic split-size override (0 = automatic); returns the previous value."""
+    return int(_lib.pkv_set_decode_split_blocks(n))
+
+
+def decode_plan(batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int, block_size: int,
+                max_seq_len: int, window: int = 0) -> Tuple[int, int]:
+    """(splits per row, blocks per split) of the automatic plan on the current device."""
+    c = ctypes.c_int32(0)
+    n = _lib.pkv_decode_plan(batch, num_q_heads, num_kv_heads, head_dim, block_size, max_seq_len,
+                             window, ctypes.byref(c))
+    return int(n), int(c.value)
+
+
+def version() -> str:
+    return _lib.pkv_version().decode()

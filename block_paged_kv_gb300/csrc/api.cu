@@ -1,0 +1,366 @@
+// C ABI entry points: argument checks, the split plan, TMA descriptors and
+// kernel launches.  Everything here runs on the host; nothing allocates
+// device memory and nothing synchronises the stream.
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "pkv.h"
+#include "pkv_internal.h"
+
+namespace pkv {
+size_t f32_smem_bytes(int D, int bs);
+cudaError_t launch_prefill(const void *q, const int32_t *cu_q_lens, int32_t hq, const pkv_pool &pool,
+                           const int32_t *tables, int32_t width, const int32_t *seq_lens,
+                           int32_t batch, int32_t max_q_len, int32_t max_len, int32_t window,
+                           float scale, void *out, void *ws, size_t ws_bytes, int32_t *status,
+                           cudaStream_t stream, int *unsupported);
+size_t prefill_workspace_bytes(int32_t batch, int32_t hq, int32_t hkv, int32_t D, int32_t bs,
+                               int32_t max_q_len, int32_t max_len, int32_t window, pkv_dtype dtype);
+}  // namespace pkv
+
+using namespace pkv;
+
+namespace {
+
+std::atomic<int32_t> g_split_override{0};
+
+int num_sms_current()
+{
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 64) cache[dev] = n;
+    return n;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+bool valid_pool(const pkv_pool *pool)
+{
+    if (pool == nullptr || pool->k == nullptr || pool->v == nullptr) return false;
+    if (pool->num_blocks <= 0 || pool->block_size <= 0 || pool->num_kv_heads <= 0 ||
+        pool->head_dim <= 0)
+        return false;
+    if (pool->dtype != PKV_F32 && pool->dtype != PKV_BF16) return false;
+    return aligned16(pool->k) && aligned16(pool->v);
+}
+
+int elem_bytes(pkv_dtype t) { return t == PKV_BF16 ? 2 : 4; }
+
+// Which decode shapes are built.
+bool decode_shape_built(pkv_dtype dtype, int32_t D, int32_t bs, int32_t G)
+{
+    if (G < 1 || G > 16) return false;
+    if (dtype == PKV_BF16) return bs == 16 && (D == 64 || D == 128 || D == 256);
+    return (D == 32 || D == 64 || D == 128 || D == 256) && bs <= 64 && bs * D <= 4096;
+}
+
+// The split plan: a pure function of the sizes and the SM count.
+DecodePlan make_plan(int32_t batch, int32_t hq, int32_t hkv, int32_t D, int32_t bs,
+                     int32_t max_len, int32_t window, const pkv_prefix_desc *prefix,
+                     pkv_dtype dtype, int num_sms)
+{
+    DecodePlan pl{};
+    const int32_t G = hq / hkv;
+    int64_t nblk_max = ceil_div64(max_len, bs);
+    if (window > 0) nblk_max = std::min<int64_t>(nblk_max, ceil_div64(window, bs) + 1);
+    nblk_max = std::max<int64_t>(nblk_max, 1);
+    const int64_t tiles_ub = static_cast<int64_t>(batch) * nblk_max * hkv;
+    // about four waves of two resident CTAs per SM over the upper bound of
+    // (block, kv head) tiles; at least 8 blocks per split, a multiple of the
+    // consumer warp count
+    const int64_t target = static_cast<int64_t>(std::max(num_sms, 1)) * 2 * 4;
+    int64_t C = ceil_div64(tiles_ub, target);
+    C = std::max<int64_t>(C, 8);
+    C = ceil_div64(C, kDecodeWarps) * kDecodeWarps;
+    const int32_t ov = g_split_override.load();
+    if (ov > 0) C = ov;
+    pl.split_blocks = static_cast<int32_t>(C);
+    pl.n_suffix_splits = static_cast<int32_t>(ceil_div64(nblk_max, C));
+    pl.prefix_split_blocks = 8;
+    pl.n_prefix_splits = 0;
+    pl.prefix_chunks = 0;
+    pl.n_prefix_ctas = 0;
+    if (prefix != nullptr && prefix->num_groups > 0 && prefix->max_prefix_blocks > 0) {
+        // The prefix cut aims at about one CTA per SM for the bf16 kernel (128
+        // (row, head) pairs per CTA); it does not depend on the dtype, so the
+        // workspace size does not either.  The f32 kernel takes 16 pairs per CTA.
+        const int64_t rows_pairs = static_cast<int64_t>(prefix->max_group_rows) * G;
+        const int64_t chunks_bf16 = ceil_div64(rows_pairs, kPrefixWarps * 16);
+        int64_t Cp = ceil_div64(static_cast<int64_t>(prefix->max_prefix_blocks) * hkv *
+                                    prefix->num_groups * chunks_bf16,
+                                std::max(num_sms, 1));
+        Cp = std::min<int64_t>(std::max<int64_t>(Cp, 4), 64);
+        const int64_t chunks = dtype == PKV_BF16 ? chunks_bf16 : ceil_div64(rows_pairs, kF32Rows);
+        pl.prefix_split_blocks = static_cast<int32_t>(Cp);
+        pl.n_prefix_splits = static_cast<int32_t>(ceil_div64(prefix->max_prefix_blocks, Cp));
+        pl.prefix_chunks = static_cast<int32_t>(chunks);
+        pl.prefix_max = prefix->max_prefix_blocks;
+        pl.n_prefix_ctas = static_cast<int64_t>(pl.n_prefix_splits) * hkv * prefix->num_groups * chunks;
+    }
+    pl.nslot = pl.n_prefix_splits + pl.n_suffix_splits;
+    pl.n_suffix_ctas = static_cast<int64_t>(pl.n_suffix_splits) * hkv * batch;
+    return pl;
+}
+
+size_t ws_o_bytes(int32_t batch, int32_t hq, int32_t D, const DecodePlan &pl)
+{
+    const size_t b = static_cast<size_t>(batch) * hq * pl.nslot * D * sizeof(float);
+    return (b + 255) & ~static_cast<size_t>(255);
+}
+
+size_t ws_total_bytes(int32_t batch, int32_t hq, int32_t D, const DecodePlan &pl)
+{
+    return ws_o_bytes(batch, hq, D, pl) + static_cast<size_t>(batch) * hq * pl.nslot * 2 * sizeof(float);
+}
+
+bool valid_prefix(const pkv_prefix_desc *prefix, int32_t batch, int32_t width)
+{
+    if (prefix == nullptr || prefix->num_groups == 0) return true;
+    if (prefix->num_groups < 0 || prefix->num_groups > batch) return false;
+    if (prefix->group_of_row == nullptr || prefix->prefix_blocks == nullptr) return false;
+    if (prefix->max_group_rows < 1 || prefix->max_group_rows > batch) return false;
+    if (prefix->max_prefix_blocks < 0 || prefix->max_prefix_blocks > width) return false;
+    return true;
+}
+
+// ---------------------------------------------------------------------------
+// TMA descriptors
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool encode_fn_ready()
+{
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode != nullptr;
+}
+
+// 4-D map over a bf16 pool [num_blocks][hkv][bs][D], box 64 dims x bs slots,
+// 128-byte swizzle.
+bool encode_pool_map(CUtensorMap *map, void *base, const pkv_pool &pool)
+{
+    const cuuint64_t D = pool.head_dim, bs = pool.block_size, hkv = pool.num_kv_heads;
+    cuuint64_t dims[4] = {D, bs, hkv, static_cast<cuuint64_t>(pool.num_blocks)};
+    cuuint64_t strides[3] = {D * 2, bs * D * 2, hkv * bs * D * 2};
+    cuuint32_t box[4] = {64, static_cast<cuuint32_t>(bs), 1, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box,
+                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *pkv_version(void) { return "pkv 0.1 (sm_103a)"; }
+
+const char *pkv_status_string(pkv_status s)
+{
+    switch (s) {
+    case PKV_OK: return "ok";
+    case PKV_ERR_INVALID_ARG: return "invalid argument";
+    case PKV_ERR_UNSUPPORTED: return "unsupported dtype/shape combination";
+    case PKV_ERR_CUDA: return "CUDA error";
+    case PKV_ERR_WORKSPACE: return "workspace too small or misaligned";
+    }
+    return "unknown status";
+}
+
+int32_t pkv_set_decode_split_blocks(int32_t blocks_per_split)
+{
+    return g_split_override.exchange(blocks_per_split > 0 ? blocks_per_split : 0);
+}
+
+pkv_status paged_kv_append(const pkv_pool *pool, const int32_t *slot_mapping, int32_t num_tokens,
+                           const void *k_new, const void *v_new, int32_t *dev_status,
+                           pkv_stream_t stream)
+{
+    if (!valid_pool(pool) || num_tokens < 0) return PKV_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PKV_OK;
+    if (slot_mapping == nullptr || k_new == nullptr || v_new == nullptr) return PKV_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new)) return PKV_ERR_INVALID_ARG;
+    const int64_t row_bytes = static_cast<int64_t>(pool->head_dim) * elem_bytes(pool->dtype);
+    if (row_bytes % 16 != 0) return PKV_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(pool->num_blocks) * pool->block_size > INT32_MAX)
+        return PKV_ERR_UNSUPPORTED;
+    AppendParams p{};
+    p.k_pool = pool->k;
+    p.v_pool = pool->v;
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.slot_mapping = slot_mapping;
+    p.status = dev_status;
+    p.num_tokens = num_tokens;
+    p.hkv = pool->num_kv_heads;
+    p.block_size = pool->block_size;
+    p.vecs_per_row = static_cast<int32_t>(row_bytes / 16);
+    p.num_slots = pool->num_blocks * pool->block_size;
+    return launch_append(p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK
+                                                                                  : PKV_ERR_CUDA;
+}
+
+int32_t pkv_decode_plan(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                        int32_t block_size, int32_t max_seq_len, int32_t window,
+                        int32_t *blocks_per_split_out)
+{
+    if (batch < 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 || head_dim <= 0 ||
+        block_size <= 0 || max_seq_len < 0 || window < 0)
+        return -1;
+    const DecodePlan pl = make_plan(batch, num_q_heads, num_kv_heads, head_dim, block_size,
+                                    max_seq_len, window, nullptr, PKV_BF16, num_sms_current());
+    if (blocks_per_split_out) *blocks_per_split_out = pl.split_blocks;
+    return pl.n_suffix_splits;
+}
+
+size_t paged_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                   int32_t head_dim, int32_t block_size, int32_t max_seq_len,
+                                   int32_t window, const pkv_prefix_desc *prefix)
+{
+    if (batch < 0 || num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads != 0 ||
+        head_dim <= 0 || block_size <= 0 || max_seq_len < 0 || window < 0)
+        return 0;
+    // the f32 and bf16 plans differ only in how many CTAs cover a group's
+    // rows, which does not change the slot count
+    const DecodePlan pl = make_plan(batch, num_q_heads, num_kv_heads, head_dim, block_size,
+                                    max_seq_len, window, prefix, PKV_BF16, num_sms_current());
+    return ws_total_bytes(batch, num_q_heads, head_dim, pl);
+}
+
+pkv_status paged_decode_attention(const void *q, int32_t num_q_heads, const pkv_pool *pool,
+                                  const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                  const int32_t *seq_lens, int32_t batch, int32_t max_seq_len,
+                                  int32_t window, float scale, void *out, void *workspace,
+                                  size_t ws_bytes, const pkv_prefix_desc *prefix,
+                                  int32_t *dev_status, pkv_stream_t stream)
+{
+    if (!valid_pool(pool) || batch < 0 || num_q_heads <= 0 || max_seq_len < 0 || window < 0 ||
+        !std::isfinite(scale))
+        return PKV_ERR_INVALID_ARG;
+    if (num_q_heads % pool->num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+    if (batch == 0) return PKV_OK;
+    if (q == nullptr || out == nullptr || block_tables == nullptr || seq_lens == nullptr ||
+        max_blocks_per_seq <= 0 || !aligned16(q) || !aligned16(out))
+        return PKV_ERR_INVALID_ARG;
+    if (!valid_prefix(prefix, batch, max_blocks_per_seq)) return PKV_ERR_INVALID_ARG;
+    const bool use_prefix = prefix != nullptr && prefix->num_groups > 0;
+    if (use_prefix && window != 0) return PKV_ERR_UNSUPPORTED;
+    const int32_t G = num_q_heads / pool->num_kv_heads;
+    if (!decode_shape_built(pool->dtype, pool->head_dim, pool->block_size, G))
+        return PKV_ERR_UNSUPPORTED;
+    const int64_t cap = static_cast<int64_t>(max_blocks_per_seq) * pool->block_size;
+    const int32_t max_len = static_cast<int32_t>(std::min<int64_t>(max_seq_len, cap));
+
+    const DecodePlan pl = make_plan(batch, num_q_heads, pool->num_kv_heads, pool->head_dim,
+                                    pool->block_size, max_len, window,
+                                    use_prefix ? prefix : nullptr, pool->dtype, num_sms_current());
+    if (pl.n_suffix_ctas > INT32_MAX || pl.n_prefix_ctas > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+    const size_t need = ws_total_bytes(batch, num_q_heads, pool->head_dim, pl);
+    if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+        ws_bytes < need)
+        return PKV_ERR_WORKSPACE;
+
+    DecodeParams p{};
+    p.q = q;
+    p.out = out;
+    p.k_pool = pool->k;
+    p.v_pool = pool->v;
+    p.tables = block_tables;
+    p.seq_lens = seq_lens;
+    p.group_of_row = use_prefix ? prefix->group_of_row : nullptr;
+    p.prefix_blocks = use_prefix ? prefix->prefix_blocks : nullptr;
+    p.num_groups = use_prefix ? prefix->num_groups : 0;
+    p.ws_o = static_cast<float *>(workspace);
+    p.ws_ml = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                        ws_o_bytes(batch, num_q_heads, pool->head_dim, pl));
+    p.status = dev_status;
+    p.batch = batch;
+    p.hq = num_q_heads;
+    p.hkv = pool->num_kv_heads;
+    p.group = G;
+    p.head_dim = pool->head_dim;
+    p.block_size = pool->block_size;
+    p.width = max_blocks_per_seq;
+    p.num_blocks = pool->num_blocks;
+    p.max_len = max_len;
+    p.window = window;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.plan = pl;
+
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t err;
+    if (pool->dtype == PKV_BF16) {
+        if (!encode_fn_ready()) return PKV_ERR_CUDA;
+        CUtensorMap kmap, vmap;
+        if (!encode_pool_map(&kmap, pool->k, *pool) || !encode_pool_map(&vmap, pool->v, *pool))
+            return PKV_ERR_UNSUPPORTED;
+        err = launch_decode_bf16(p, kmap, vmap, st);
+    } else {
+        err = launch_decode_f32(p, st);
+    }
+    if (err != cudaSuccess) return PKV_ERR_CUDA;
+    err = launch_decode_combine(p, pool->dtype, st);
+    return err == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+size_t paged_prefill_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                    int32_t head_dim, int32_t block_size, int32_t max_q_len,
+                                    int32_t max_seq_len, int32_t window)
+{
+    if (batch < 0 || num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads != 0 ||
+        head_dim <= 0 || block_size <= 0 || max_q_len < 0 || max_seq_len < 0 || window < 0)
+        return 0;
+    return prefill_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim, block_size,
+                                   max_q_len, max_seq_len, window, PKV_BF16);
+}
+
+pkv_status paged_prefill_chunk_attention(const void *q, const int32_t *cu_q_lens,
+                                         int32_t num_q_heads, const pkv_pool *pool,
+                                         const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                         const int32_t *seq_lens, int32_t batch, int32_t max_q_len,
+                                         int32_t max_seq_len, int32_t window, float scale,
+                                         void *out, void *workspace, size_t ws_bytes,
+                                         int32_t *dev_status, pkv_stream_t stream)
+{
+    if (!valid_pool(pool) || batch < 0 || num_q_heads <= 0 || max_q_len < 0 || max_seq_len < 0 ||
+        window < 0 || !std::isfinite(scale))
+        return PKV_ERR_INVALID_ARG;
+    if (num_q_heads % pool->num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+    if (batch == 0 || max_q_len == 0) return PKV_OK;
+    if (q == nullptr || out == nullptr || cu_q_lens == nullptr || block_tables == nullptr ||
+        seq_lens == nullptr || max_blocks_per_seq <= 0 || !aligned16(q) || !aligned16(out))
+        return PKV_ERR_INVALID_ARG;
+    const int64_t cap = static_cast<int64_t>(max_blocks_per_seq) * pool->block_size;
+    const int32_t max_len = static_cast<int32_t>(std::min<int64_t>(max_seq_len, cap));
+    if (workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return PKV_ERR_WORKSPACE;
+    int unsupported = 0;
+    const cudaError_t err = launch_prefill(q, cu_q_lens, num_q_heads, *pool, block_tables,
+                                           max_blocks_per_seq, seq_lens, batch, max_q_len, max_len,
+                                           window, scale, out, workspace, ws_bytes, dev_status,
+                                           reinterpret_cast<cudaStream_t>(stream), &unsupported);
+    if (unsupported == 1) return PKV_ERR_UNSUPPORTED;
+    if (unsupported == 2) return PKV_ERR_WORKSPACE;
+    return err == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+}  // extern "C"

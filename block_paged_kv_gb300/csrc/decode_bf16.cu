@@ -1,0 +1,500 @@
+// Split-KV paged decode attention for bf16 pools ("perf.md": the paged decode
+// reads the pages through the block table and splits each row into partitions
+// whose online-softmax partials a reducer merges; all q heads of a GQA group
+// share each block load, as the pages' grouped decode kernels do).
+//
+// One CTA = one work item:
+//   suffix item (TILES == 1): row r, kv head g, split s -> blocks
+//       b_first + s*C .. ; its 16-row query tile holds the G q heads of (r, g);
+//   prefix item (TILES == NW): group, kv head g, row chunk, prefix split s ->
+//       prefix blocks s*Cp ..; NW query tiles hold (row, head) pairs of the
+//       group, so every shared block is read once for all of them.
+// A producer warp streams (block, kv head) K and V tiles with TMA tensor loads
+// (4-D maps over [block][kv head][slot][dim], 64-dim boxes, 128-byte swizzle)
+// into a ring of STAGES shared-memory slots guarded by mbarriers.  Consumer
+// warps compute S = Q K^T and O += P V with mma.sync m16n8k16 (bf16 in, fp32
+// accumulate): M = 16 query rows, N = 8 tokens or 8 dims.  The online softmax
+// runs on the accumulator fragments with quad shuffles; P is rounded to bf16
+// for the P.V product and the row sums use the rounded values.  Each tile's
+// partial (max in log2 units, sum, unnormalised O) goes to the workspace.
+#include "decode_common.cuh"
+
+namespace pkv {
+
+template <int D>
+struct Bf16Cfg {
+    static constexpr int kTok = 16;                       // block_size
+    static constexpr int kTileBytes = kTok * D * 2;       // one (block, kv head) tile of K or V
+    static constexpr int kStageBytes = 2 * kTileBytes;    // K + V
+    static constexpr int kStages = (64 * 1024) / kStageBytes;
+    static constexpr int kRegions = D / 64;               // 64-dim swizzled regions per tile
+    static constexpr int kRegionBytes = kTok * 128;
+    static constexpr int kQStride = (D + 8) * 2;          // padded query row (bytes)
+    static constexpr int kQTileBytes = 16 * kQStride;
+    static constexpr bool kQInRegs = D <= 128;
+    static constexpr int kNT = D / 8;                     // 8-dim output n-tiles
+    static constexpr int kKS = D / 16;                    // 16-dim k-steps of Q K^T
+};
+
+template <int D, int NW, int TILES>
+struct Bf16Smem {
+    using C = Bf16Cfg<D>;
+    static constexpr int kStageOff = 0;
+    static constexpr int kQOff = C::kStages * C::kStageBytes;
+    static constexpr int kBarOff = kQOff + TILES * C::kQTileBytes;
+    static constexpr int kOkOff = kBarOff + 2 * C::kStages * 8;
+    static constexpr int kPairOff = kOkOff + C::kStages * 4;
+    static constexpr int kMiscOff = kPairOff + 3 * TILES * 16 * 4;
+    static constexpr int kBytes = kMiscOff + 16;
+    static constexpr int kLaunchBytes = kBytes + 1024;  // room to align the base to 1024
+};
+
+// Swizzled shared address of the 16-byte chunk holding dims d0..d0+7 of token
+// `tok` in a K/V tile (TMA SWIZZLE_128B: chunk index XOR (line % 8)).
+template <int D>
+__device__ __forceinline__ uint32_t kv_chunk_addr(uint32_t tile, int tok, int d0)
+{
+    return tile + (d0 >> 6) * Bf16Cfg<D>::kRegionBytes + tok * 128 +
+           ((((d0 & 63) >> 3) ^ (tok & 7)) << 4);
+}
+
+__device__ __forceinline__ void consumer_bar_sync(int nthreads)
+{
+    asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+}
+
+template <int D, int NW, int TILES>
+__global__ void __launch_bounds__((NW + 1) * 32, TILES == 1 ? 2 : 1)
+    decode_bf16_kernel(const __grid_constant__ CUtensorMap kmap,
+                       const __grid_constant__ CUtensorMap vmap, const DecodeParams p)
+{
+    using C = Bf16Cfg<D>;
+    using SM = Bf16Smem<D, NW, TILES>;
+    constexpr int WPT = NW / TILES;  // consumer warps per query tile
+    constexpr int STAGES = C::kStages;
+    static_assert(NW % TILES == 0, "tiles split the consumer warps evenly");
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *stage_mem = smem + SM::kStageOff;
+    uint8_t *q_mem = smem + SM::kQOff;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + SM::kBarOff);
+    uint64_t *empty = full + STAGES;
+    int32_t *stage_ok = reinterpret_cast<int32_t *>(smem + SM::kOkOff);
+    int32_t *pair_row = reinterpret_cast<int32_t *>(smem + SM::kPairOff);
+    int32_t *pair_head = pair_row + TILES * 16;
+    int32_t *pair_len = pair_head + TILES * 16;
+    int32_t *misc = reinterpret_cast<int32_t *>(smem + SM::kMiscOff);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int G = p.group;
+    const int bs = C::kTok;
+
+    // ---------------------------------------------------------------- work item
+    int32_t b0, nblk, slot, tab_row, g, lo_all, hi_all;
+    int32_t row_r = 0;  // suffix item only
+    if constexpr (TILES == 1) {
+        int64_t bid = blockIdx.x;
+        const int32_t s = static_cast<int32_t>(bid % p.plan.n_suffix_splits);
+        bid /= p.plan.n_suffix_splits;
+        g = static_cast<int32_t>(bid % p.hkv);
+        row_r = static_cast<int32_t>(bid / p.hkv);
+        const RowRange rr = row_range(p, row_r, s == 0 && g == 0);
+        b0 = rr.b_first + s * p.plan.split_blocks;
+        const int32_t b1 = min(b0 + p.plan.split_blocks, rr.b_end);
+        if (b0 >= b1) return;
+        nblk = b1 - b0;
+        slot = p.plan.n_prefix_splits + s;
+        tab_row = row_r;
+        lo_all = rr.lo;
+        hi_all = rr.L;
+    } else {
+        int64_t bid = blockIdx.x;
+        const int32_t s = static_cast<int32_t>(bid % p.plan.n_prefix_splits);
+        bid /= p.plan.n_prefix_splits;
+        g = static_cast<int32_t>(bid % p.hkv);
+        bid /= p.hkv;
+        const int32_t chunk = static_cast<int32_t>(bid % p.plan.prefix_chunks);
+        const int32_t grp = static_cast<int32_t>(bid / p.plan.prefix_chunks);
+        int32_t P = __ldg(p.prefix_blocks + grp);
+        const int32_t pmax = p.plan.prefix_max;
+        P = P < 0 ? 0 : (P > pmax ? pmax : P);
+        b0 = s * p.plan.prefix_split_blocks;
+        const int32_t b1 = min(b0 + p.plan.prefix_split_blocks, P);
+        if (b0 >= b1) return;
+        nblk = b1 - b0;
+        slot = s;
+        for (int i = threadIdx.x; i < TILES * 16; i += blockDim.x) pair_row[i] = -1;
+        __syncthreads();
+        if (warp == 0) {
+            // rows of the group in ascending order; pair k = rank * G + j
+            const int32_t kbase = chunk * TILES * 16;
+            int32_t cnt = 0, leader = -1, hmax = 0;
+            for (int32_t base = 0; base < p.batch; base += 32) {
+                const int32_t r = base + lane;
+                const bool in = r < p.batch && __ldg(p.group_of_row + r) == grp;
+                const uint32_t m = __ballot_sync(0xffffffffu, in);
+                if (in) {
+                    const int32_t rank = cnt + __popc(m & ((1u << lane) - 1u));
+                    if (rank == 0) leader = r;
+                    int32_t L = __ldg(p.seq_lens + r);
+                    L = L < 0 ? 0 : (L > p.max_len ? p.max_len : L);
+                    if (L < P * bs) report(p.status, PKV_DEV_BAD_PREFIX);
+                    if ((rank + 1) * G > p.plan.prefix_chunks * TILES * 16)
+                        report(p.status, PKV_DEV_BAD_PREFIX);  // more rows than max_group_rows
+                    for (int j = 0; j < G; ++j) {
+                        const int32_t k = rank * G + j - kbase;
+                        if (k >= 0 && k < TILES * 16) {
+                            pair_row[k] = r;
+                            pair_head[k] = g * G + j;
+                            pair_len[k] = L;
+                            hmax = max(hmax, L);
+                        }
+                    }
+                }
+                cnt += __popc(m);
+            }
+            leader = __reduce_max_sync(0xffffffffu, leader);
+            hmax = __reduce_max_sync(0xffffffffu, hmax);
+            if (lane == 0) {
+                misc[0] = leader;
+                misc[1] = hmax;
+            }
+        }
+        __syncthreads();
+        if (pair_row[0] < 0) return;  // this chunk lies past the group's rows
+        tab_row = misc[0];
+        lo_all = 0;
+        hi_all = misc[1];
+        // every row of the chunk must hold the leader's blocks in this range
+        for (int i = threadIdx.x; i < TILES * 16 * nblk; i += blockDim.x) {
+            const int k = i / nblk, b = b0 + i % nblk;
+            const int32_t pr = pair_row[k];
+            if (pr >= 0 && (k % G) == 0 &&
+                __ldg(p.tables + static_cast<int64_t>(pr) * p.width + b) !=
+                    __ldg(p.tables + static_cast<int64_t>(tab_row) * p.width + b))
+                report(p.status, PKV_DEV_BAD_PREFIX);
+        }
+    }
+
+    // ------------------------------------------------- query tiles + barriers
+    {
+        const int nthr = blockDim.x;
+        constexpr int kVec = D / 8;  // 16-byte vectors per row
+        for (int i = threadIdx.x; i < TILES * 16 * kVec; i += nthr) {
+            const int row = i / kVec, v = i % kVec;
+            int32_t qr = -1, qh = 0;
+            if constexpr (TILES == 1) {
+                if (row < G) {
+                    qr = row_r;
+                    qh = g * G + row;
+                }
+            } else {
+                qr = pair_row[row];
+                qh = pair_head[row];
+            }
+            uint4 val = make_uint4(0, 0, 0, 0);
+            if (qr >= 0)
+                val = __ldg(reinterpret_cast<const uint4 *>(p.q) +
+                            ((static_cast<int64_t>(qr) * p.hq + qh) * D) / 8 + v);
+            *reinterpret_cast<uint4 *>(q_mem + (row / 16) * C::kQTileBytes +
+                                       (row % 16) * C::kQStride + v * 16) = val;
+        }
+        if (threadIdx.x == 0) {
+            for (int s = 0; s < STAGES; ++s) {
+                mbar_init(&full[s], 1);
+                mbar_init(&empty[s], TILES);
+            }
+            fence_mbar_init();
+        }
+        __syncthreads();
+    }
+
+    // ---------------------------------------------------------------- producer
+    if (warp == NW) {
+        if (lane == 0) {
+            tma_prefetch_desc(&kmap);
+            tma_prefetch_desc(&vmap);
+        }
+        const uint64_t policy = l2_evict_first_policy();
+        bool abort = false;
+        for (int base = 0; base < nblk && !abort; base += 32) {
+            int32_t blk = -1;
+            if (base + lane < nblk)
+                blk = __ldg(p.tables + static_cast<int64_t>(tab_row) * p.width + b0 + base + lane);
+            const int cnt = min(32, nblk - base);
+            for (int j = 0; j < cnt; ++j) {
+                const int32_t bj = __shfl_sync(0xffffffffu, blk, j);
+                if (lane == 0) {
+                    const int i = base + j;
+                    const int st = i % STAGES;
+                    if (i >= STAGES && !mbar_wait(&empty[st], ((i / STAGES) + 1) & 1)) {
+                        report(p.status, PKV_DEV_TIMEOUT);
+                        abort = true;
+                    }
+                    if (!abort) {
+                        const bool ok = static_cast<uint32_t>(bj) < static_cast<uint32_t>(p.num_blocks);
+                        stage_ok[st] = ok ? 1 : 0;
+                        if (ok) {
+                            mbar_arrive_expect_tx(&full[st], C::kStageBytes);
+                            uint8_t *kdst = stage_mem + st * C::kStageBytes;
+                            uint8_t *vdst = kdst + C::kTileBytes;
+#pragma unroll
+                            for (int reg = 0; reg < C::kRegions; ++reg) {
+                                tma_load_4d(kdst + reg * C::kRegionBytes, &kmap, &full[st], reg * 64,
+                                            0, g, bj, policy);
+                                tma_load_4d(vdst + reg * C::kRegionBytes, &vmap, &full[st], reg * 64,
+                                            0, g, bj, policy);
+                            }
+                        } else {
+                            report(p.status, PKV_DEV_BAD_BLOCK);
+                            mbar_arrive(&full[st]);
+                        }
+                    }
+                }
+                abort = __shfl_sync(0xffffffffu, abort, 0);
+                if (abort) break;
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    const int tile = warp / WPT;
+    const int sub = warp % WPT;
+    const int qd = lane >> 2;        // fragment rows qd and qd + 8
+    const int c2 = 2 * (lane & 3);   // fragment columns c2, c2 + 1
+    int lo0, hi0, lo1, hi1;
+    if constexpr (TILES == 1) {
+        lo0 = lo1 = lo_all;
+        hi0 = hi1 = hi_all;
+    } else {
+        lo0 = lo1 = 0;
+        const int k0 = tile * 16 + qd;
+        hi0 = pair_row[k0] >= 0 ? pair_len[k0] : 0;
+        hi1 = pair_row[k0 + 8] >= 0 ? pair_len[k0 + 8] : 0;
+    }
+
+    const uint32_t q_tile = smem_u32(q_mem + tile * C::kQTileBytes);
+    const uint32_t q_lane = q_tile + (((lane >> 3) & 1) * 8 + (lane & 7)) * C::kQStride +
+                            (lane >> 4) * 16;
+    uint32_t qf[C::kQInRegs ? C::kKS : 1][4];
+    if constexpr (C::kQInRegs) {
+#pragma unroll
+        for (int kk = 0; kk < C::kKS; ++kk)
+            ldsm_x4(q_lane + kk * 32, qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3]);
+    }
+
+    float o[C::kNT][4];
+#pragma unroll
+    for (int nt = 0; nt < C::kNT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    bool timed_out = false;
+
+    // lane-constant parts of the ldmatrix addresses
+    const int k_tok = (lane >> 4) * 8 + (lane & 7);
+    const int k_dof = ((lane >> 3) & 1) * 8;
+    const int v_tok = ((lane >> 3) & 1) * 8 + (lane & 7);
+    const int v_dof = (lane >> 4) * 8;
+
+    for (int i = sub; i < nblk; i += WPT) {
+        const int st = i % STAGES;
+        const bool got = mbar_wait(&full[st], (i / STAGES) & 1);
+        if (__any_sync(0xffffffffu, !got)) {
+            if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
+            timed_out = true;
+            break;
+        }
+        const bool ok = stage_ok[st] != 0;
+        const uint32_t kt = smem_u32(stage_mem + st * C::kStageBytes);
+        const uint32_t vt = kt + C::kTileBytes;
+        const int base_tok = (b0 + i) * bs;
+
+        // S = Q K^T  (16 rows x 16 tokens)
+        float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+        for (int kk = 0; kk < C::kKS; ++kk) {
+            uint32_t a[4];
+            if constexpr (C::kQInRegs) {
+                a[0] = qf[kk][0]; a[1] = qf[kk][1]; a[2] = qf[kk][2]; a[3] = qf[kk][3];
+            } else {
+                ldsm_x4(q_lane + kk * 32, a[0], a[1], a[2], a[3]);
+            }
+            uint32_t k0, k1, k2, k3;
+            ldsm_x4(kv_chunk_addr<D>(kt, k_tok, kk * 16 + k_dof), k0, k1, k2, k3);
+            mma_16816(sacc[0], a, k0, k1);
+            mma_16816(sacc[1], a, k2, k3);
+        }
+
+        // mask, scale to log2 units, online softmax over the quad's row
+        float s[2][4];
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int pos = base_tok + j * 8 + c2 + (e & 1);
+                const int lo = e < 2 ? lo0 : lo1, hi = e < 2 ? hi0 : hi1;
+                s[j][e] = (ok && pos >= lo && pos < hi) ? sacc[j][e] * p.scale_log2 : -INFINITY;
+            }
+        float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
+        float mx1 = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
+        const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
+        const float al0 = fast_exp2(m0 - mu0), al1 = fast_exp2(m1 - mu1);
+        m0 = mn0;
+        m1 = mn1;
+        uint32_t pa[4];
+        pa[0] = pack_bf16x2(fast_exp2(s[0][0] - mu0), fast_exp2(s[0][1] - mu0));
+        pa[1] = pack_bf16x2(fast_exp2(s[0][2] - mu1), fast_exp2(s[0][3] - mu1));
+        pa[2] = pack_bf16x2(fast_exp2(s[1][0] - mu0), fast_exp2(s[1][1] - mu0));
+        pa[3] = pack_bf16x2(fast_exp2(s[1][2] - mu1), fast_exp2(s[1][3] - mu1));
+        l0 = l0 * al0 + ((bf16lo_to_f32(pa[0]) + bf16hi_to_f32(pa[0])) +
+                         (bf16lo_to_f32(pa[2]) + bf16hi_to_f32(pa[2])));
+        l1 = l1 * al1 + ((bf16lo_to_f32(pa[1]) + bf16hi_to_f32(pa[1])) +
+                         (bf16lo_to_f32(pa[3]) + bf16hi_to_f32(pa[3])));
+#pragma unroll
+        for (int nt = 0; nt < C::kNT; ++nt) {
+            o[nt][0] *= al0;
+            o[nt][1] *= al0;
+            o[nt][2] *= al1;
+            o[nt][3] *= al1;
+        }
+
+        // O += P V  (values of tokens outside every row's range are zeroed:
+        // stale slots may hold anything, including NaN)
+        if (ok) {
+            uint32_t mk0 = 0xffffffffu, mk1 = 0xffffffffu;
+            if (base_tok < lo_all || base_tok + bs > hi_all) {
+                auto live = [&](int t) {
+                    return base_tok + t >= lo_all && base_tok + t < hi_all;
+                };
+                mk0 = (live(c2) ? 0x0000ffffu : 0u) | (live(c2 + 1) ? 0xffff0000u : 0u);
+                mk1 = (live(c2 + 8) ? 0x0000ffffu : 0u) | (live(c2 + 9) ? 0xffff0000u : 0u);
+            }
+#pragma unroll
+            for (int np = 0; np < C::kNT / 2; ++np) {
+                uint32_t v0, v1, v2, v3;
+                ldsm_x4_trans(kv_chunk_addr<D>(vt, v_tok, np * 16 + v_dof), v0, v1, v2, v3);
+                v0 &= mk0; v1 &= mk1; v2 &= mk0; v3 &= mk1;
+                mma_16816(o[2 * np], pa, v0, v1);
+                mma_16816(o[2 * np + 1], pa, v2, v3);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+    }
+
+    // row sums: the quad's four partial sums
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+
+    if constexpr (WPT == 1) {
+        // prefix item: every warp owns its tile; write its rows directly
+        if (timed_out) return;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const int k = tile * 16 + qd + half * 8;
+            const int32_t pr = pair_row[k];
+            if (pr < 0) continue;
+            const size_t pi = partial_index(p, pr, pair_head[k], slot);
+            float *dst = p.ws_o + pi * D;
+#pragma unroll
+            for (int nt = 0; nt < C::kNT; ++nt)
+                *reinterpret_cast<float2 *>(dst + nt * 8 + c2) =
+                    make_float2(o[nt][2 * half], o[nt][2 * half + 1]);
+            if ((lane & 3) == 0)
+                *reinterpret_cast<float2 *>(p.ws_ml + pi * 2) =
+                    make_float2(half ? m1 : m0, half ? l1 : l0);
+        }
+    } else {
+        // suffix item: merge the NW warps' partials of the one tile
+        float *mbuf = reinterpret_cast<float *>(stage_mem);           // [WPT][G][D]
+        float *mlbuf = mbuf + WPT * G * D;                             // [WPT][G][2]
+        consumer_bar_sync(NW * 32);  // every warp is done with the stage ring
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const int row = qd + half * 8;
+            if (row >= G) continue;
+            float *dst = mbuf + (sub * G + row) * D;
+#pragma unroll
+            for (int nt = 0; nt < C::kNT; ++nt)
+                *reinterpret_cast<float2 *>(dst + nt * 8 + c2) =
+                    make_float2(o[nt][2 * half], o[nt][2 * half + 1]);
+            if ((lane & 3) == 0) {
+                mlbuf[(sub * G + row) * 2] = half ? m1 : m0;
+                mlbuf[(sub * G + row) * 2 + 1] = half ? l1 : l0;
+            }
+        }
+        consumer_bar_sync(NW * 32);
+        for (int idx = threadIdx.x; idx < G * D; idx += NW * 32) {
+            const int row = idx / D, d = idx % D;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < WPT; ++w) M = fmaxf(M, mlbuf[(w * G + row) * 2]);
+            float acc = 0.f, lsum = 0.f;
+            if (M != -INFINITY) {
+#pragma unroll
+                for (int w = 0; w < WPT; ++w) {
+                    const float wgt = fast_exp2(mlbuf[(w * G + row) * 2] - M);
+                    acc += wgt * mbuf[(w * G + row) * D + d];
+                    lsum += wgt * mlbuf[(w * G + row) * 2 + 1];
+                }
+            }
+            const size_t pi = partial_index(p, row_r, g * G + row, slot);
+            p.ws_o[pi * D + d] = acc;
+            if (d == 0) *reinterpret_cast<float2 *>(p.ws_ml + pi * 2) = make_float2(M, lsum);
+        }
+    }
+}
+
+template <typename K>
+static cudaError_t prepare(K kernel, int smem_bytes)
+{
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+}
+
+template <int D>
+static cudaError_t launch_d(const DecodeParams &p, const CUtensorMap &kmap, const CUtensorMap &vmap,
+                            cudaStream_t stream)
+{
+    constexpr int NW = kDecodeWarps;
+    constexpr int NWP = kPrefixWarps;
+    cudaError_t err;
+    if (p.plan.n_prefix_ctas > 0) {
+        auto kern = decode_bf16_kernel<D, NWP, NWP>;
+        const int smem = Bf16Smem<D, NWP, NWP>::kLaunchBytes;
+        if ((err = prepare(kern, smem)) != cudaSuccess) return err;
+        kern<<<static_cast<unsigned>(p.plan.n_prefix_ctas), (NWP + 1) * 32, smem, stream>>>(kmap, vmap, p);
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    }
+    if (p.plan.n_suffix_ctas > 0) {
+        auto kern = decode_bf16_kernel<D, NW, 1>;
+        const int smem = Bf16Smem<D, NW, 1>::kLaunchBytes;
+        if ((err = prepare(kern, smem)) != cudaSuccess) return err;
+        kern<<<static_cast<unsigned>(p.plan.n_suffix_ctas), (NW + 1) * 32, smem, stream>>>(kmap, vmap, p);
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    }
+    return cudaSuccess;
+}
+
+cudaError_t launch_decode_bf16(const DecodeParams &p, const CUtensorMap &kmap,
+                               const CUtensorMap &vmap, cudaStream_t stream)
+{
+    switch (p.head_dim) {
+    case 64: return launch_d<64>(p, kmap, vmap, stream);
+    case 128: return launch_d<128>(p, kmap, vmap, stream);
+    case 256: return launch_d<256>(p, kmap, vmap, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace pkv

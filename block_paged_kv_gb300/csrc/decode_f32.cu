@@ -1,0 +1,297 @@
+// Split-KV paged decode for f32 pools (CUDA cores) and the log-sum-exp merge
+// of split partials used by every decode path ("perf.md", partition-rule
+// paragraphs: each partition keeps online-softmax partials that a reducer
+// merges; an empty partition contributes exact zeros).
+//
+// The f32 kernel follows the same work items and partial layout as the bf16
+// kernel: a CTA takes up to 16 (row, q head) pairs of one kv head (the G heads
+// of a row, or pairs of a shared-prefix group) and a run of blocks; each block
+// tile is staged in shared memory and scores, softmax and values are
+// accumulated in fp32.
+#include "decode_common.cuh"
+
+namespace pkv {
+
+constexpr int kF32Threads = 128;
+
+__global__ void __launch_bounds__(kF32Threads)
+    decode_f32_kernel(const DecodeParams p, int prefix_mode)
+{
+    constexpr int NQ = kF32Rows;
+    extern __shared__ float fsm[];
+    const int D = p.head_dim, bs = p.block_size;
+    float *qs = fsm;                   // [NQ][D]
+    float *os = qs + NQ * D;           // [NQ][D]
+    float *ks = os + NQ * D;           // [bs][D]
+    float *vs = ks + bs * D;           // [bs][D]
+    float *sc = vs + bs * D;           // [NQ][bs]
+    float *mrow = sc + NQ * bs;        // [NQ]
+    float *lrow = mrow + NQ;           // [NQ]
+    float *alpha = lrow + NQ;          // [NQ]
+    int32_t *prow = reinterpret_cast<int32_t *>(alpha + NQ);  // [NQ] row, -1 = unused
+    int32_t *phead = prow + NQ;        // [NQ]
+    int32_t *plo = phead + NQ;         // [NQ]
+    int32_t *phi = plo + NQ;           // [NQ]
+    int32_t *misc = phi + NQ;          // [0] = table row
+
+    const int tid = threadIdx.x;
+    const int G = p.group;
+    int32_t b0, nblk, slot, g;
+    if (!prefix_mode) {
+        int64_t bid = blockIdx.x;
+        const int32_t s = static_cast<int32_t>(bid % p.plan.n_suffix_splits);
+        bid /= p.plan.n_suffix_splits;
+        g = static_cast<int32_t>(bid % p.hkv);
+        const int32_t r = static_cast<int32_t>(bid / p.hkv);
+        const RowRange rr = row_range(p, r, s == 0 && g == 0);
+        b0 = rr.b_first + s * p.plan.split_blocks;
+        const int32_t b1 = min(b0 + p.plan.split_blocks, rr.b_end);
+        if (b0 >= b1) return;
+        nblk = b1 - b0;
+        slot = p.plan.n_prefix_splits + s;
+        if (tid < NQ) {
+            prow[tid] = tid < G ? r : -1;
+            phead[tid] = g * G + tid;
+            plo[tid] = rr.lo;
+            phi[tid] = rr.L;
+        }
+        if (tid == 0) misc[0] = r;
+    } else {
+        int64_t bid = blockIdx.x;
+        const int32_t s = static_cast<int32_t>(bid % p.plan.n_prefix_splits);
+        bid /= p.plan.n_prefix_splits;
+        g = static_cast<int32_t>(bid % p.hkv);
+        bid /= p.hkv;
+        const int32_t chunk = static_cast<int32_t>(bid % p.plan.prefix_chunks);
+        const int32_t grp = static_cast<int32_t>(bid / p.plan.prefix_chunks);
+        int32_t P = __ldg(p.prefix_blocks + grp);
+        const int32_t pmax = p.plan.prefix_max;
+        P = P < 0 ? 0 : (P > pmax ? pmax : P);
+        b0 = s * p.plan.prefix_split_blocks;
+        const int32_t b1 = min(b0 + p.plan.prefix_split_blocks, P);
+        if (b0 >= b1) return;
+        nblk = b1 - b0;
+        slot = s;
+        if (tid < NQ) prow[tid] = -1;
+        __syncthreads();
+        if (tid < 32) {
+            const int lane = tid;
+            int32_t cnt = 0, leader = -1;
+            for (int32_t base = 0; base < p.batch; base += 32) {
+                const int32_t r = base + lane;
+                const bool in = r < p.batch && __ldg(p.group_of_row + r) == grp;
+                const uint32_t m = __ballot_sync(0xffffffffu, in);
+                if (in) {
+                    const int32_t rank = cnt + __popc(m & ((1u << lane) - 1u));
+                    if (rank == 0) leader = r;
+                    int32_t L = __ldg(p.seq_lens + r);
+                    L = L < 0 ? 0 : (L > p.max_len ? p.max_len : L);
+                    if (L < P * bs) report(p.status, PKV_DEV_BAD_PREFIX);
+                    if ((rank + 1) * G > p.plan.prefix_chunks * NQ)
+                        report(p.status, PKV_DEV_BAD_PREFIX);  // more rows than max_group_rows
+                    for (int j = 0; j < G; ++j) {
+                        const int32_t k = rank * G + j - chunk * NQ;
+                        if (k >= 0 && k < NQ) {
+                            prow[k] = r;
+                            phead[k] = g * G + j;
+                            plo[k] = 0;
+                            phi[k] = L;
+                        }
+                    }
+                }
+                cnt += __popc(m);
+            }
+            leader = __reduce_max_sync(0xffffffffu, leader);
+            if (lane == 0) misc[0] = leader;
+        }
+    }
+    __syncthreads();
+    if (prow[0] < 0) return;
+    const int32_t tab_row = misc[0];
+    if (prefix_mode) {
+        for (int i = tid; i < NQ * nblk; i += kF32Threads) {
+            const int k = i / nblk, b = b0 + i % nblk;
+            const int32_t pr = prow[k];
+            if (pr >= 0 && (k % G) == 0 &&
+                __ldg(p.tables + static_cast<int64_t>(pr) * p.width + b) !=
+                    __ldg(p.tables + static_cast<int64_t>(tab_row) * p.width + b))
+                report(p.status, PKV_DEV_BAD_PREFIX);
+        }
+    }
+    const float *qg = static_cast<const float *>(p.q);
+    for (int i = tid; i < NQ * D; i += kF32Threads) {
+        const int k = i / D, d = i % D;
+        qs[i] = prow[k] >= 0 ? qg[(static_cast<int64_t>(prow[k]) * p.hq + phead[k]) * D + d] : 0.f;
+        os[i] = 0.f;
+    }
+    if (tid < NQ) {
+        mrow[tid] = -INFINITY;
+        lrow[tid] = 0.f;
+    }
+    __syncthreads();
+
+    const float *kpool = static_cast<const float *>(p.k_pool);
+    const float *vpool = static_cast<const float *>(p.v_pool);
+    for (int i = 0; i < nblk; ++i) {
+        const int32_t b = b0 + i;
+        const int32_t blk = __ldg(p.tables + static_cast<int64_t>(tab_row) * p.width + b);
+        const bool ok = static_cast<uint32_t>(blk) < static_cast<uint32_t>(p.num_blocks);
+        if (!ok && tid == 0) report(p.status, PKV_DEV_BAD_BLOCK);
+        if (ok) {
+            const int64_t base = (static_cast<int64_t>(blk) * p.hkv + g) * bs * D;
+            for (int j = tid; j < bs * D; j += kF32Threads) {
+                ks[j] = __ldg(kpool + base + j);
+                vs[j] = __ldg(vpool + base + j);
+            }
+        }
+        __syncthreads();
+        for (int j = tid; j < NQ * bs; j += kF32Threads) {
+            const int k = j / bs, t = j % bs;
+            const int pos = b * bs + t;
+            float sv = -INFINITY;
+            if (ok && prow[k] >= 0 && pos >= plo[k] && pos < phi[k]) {
+                float acc = 0.f;
+                for (int d = 0; d < D; ++d) acc = fmaf(qs[k * D + d], ks[t * D + d], acc);
+                sv = acc * p.scale_log2;
+            }
+            sc[j] = sv;
+        }
+        __syncthreads();
+        if (tid < NQ) {
+            float mx = -INFINITY;
+            for (int t = 0; t < bs; ++t) mx = fmaxf(mx, sc[tid * bs + t]);
+            const float mn = fmaxf(mrow[tid], mx);
+            const float mu = mn == -INFINITY ? 0.f : mn;
+            const float al = fast_exp2(mrow[tid] - mu);
+            float sum = 0.f;
+            for (int t = 0; t < bs; ++t) {
+                const float e = fast_exp2(sc[tid * bs + t] - mu);
+                sc[tid * bs + t] = e;
+                sum += e;
+            }
+            lrow[tid] = lrow[tid] * al + sum;
+            mrow[tid] = mn;
+            alpha[tid] = al;
+        }
+        __syncthreads();
+        for (int j = tid; j < NQ * D; j += kF32Threads) {
+            const int k = j / D, d = j % D;
+            float acc = os[j] * alpha[k];
+            for (int t = 0; t < bs; ++t) {
+                const float w = sc[k * bs + t];
+                if (w != 0.f) acc = fmaf(w, vs[t * D + d], acc);  // masked slots may hold NaN
+            }
+            os[j] = acc;
+        }
+        __syncthreads();
+    }
+    for (int j = tid; j < NQ * D; j += kF32Threads) {
+        const int k = j / D, d = j % D;
+        if (prow[k] < 0) continue;
+        const size_t pi = partial_index(p, prow[k], phead[k], slot);
+        p.ws_o[pi * D + d] = os[j];
+        if (d == 0) {
+            p.ws_ml[pi * 2] = mrow[k];
+            p.ws_ml[pi * 2 + 1] = lrow[k];
+        }
+    }
+}
+
+size_t f32_smem_bytes(int D, int bs)
+{
+    return sizeof(float) * (2 * kF32Rows * D + 2 * bs * D + kF32Rows * bs + 3 * kF32Rows) +
+           sizeof(int32_t) * (4 * kF32Rows + 4);
+}
+
+cudaError_t launch_decode_f32(const DecodeParams &p, cudaStream_t stream)
+{
+    const size_t smem = f32_smem_bytes(p.head_dim, p.block_size);
+    cudaError_t err = cudaFuncSetAttribute(decode_f32_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+    if (p.plan.n_prefix_ctas > 0) {
+        decode_f32_kernel<<<static_cast<unsigned>(p.plan.n_prefix_ctas), kF32Threads, smem, stream>>>(p, 1);
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    }
+    if (p.plan.n_suffix_ctas > 0) {
+        decode_f32_kernel<<<static_cast<unsigned>(p.plan.n_suffix_ctas), kF32Threads, smem, stream>>>(p, 0);
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    }
+    return cudaSuccess;
+}
+
+// ---------------------------------------------------------------------------
+// Merge: one warp per (row, q head).  M = max of the partial maxima; each
+// partial is weighted by 2^(m_s - M); out = sum w_s O_s / sum w_s l_s.  Rows
+// with no partial (an empty key range) get zeros.
+// ---------------------------------------------------------------------------
+template <typename OutT>
+__device__ __forceinline__ OutT to_out(float x);
+template <>
+__device__ __forceinline__ float to_out<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 to_out<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+template <typename OutT, int D>
+__global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams p)
+{
+    constexpr int PER = D / 32;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t idx = static_cast<int64_t>(blockIdx.x) * 4 + warp;
+    if (idx >= static_cast<int64_t>(p.batch) * p.hq) return;
+    const int32_t r = static_cast<int32_t>(idx / p.hq), h = static_cast<int32_t>(idx % p.hq);
+    const RowRange rr = row_range(p, r, false);
+    const int32_t npre = row_prefix_splits(p, rr);
+    const int32_t n = npre + row_suffix_splits(p, rr);
+    const size_t base = partial_index(p, r, h, 0);
+    auto slot_of = [&](int32_t k) { return k < npre ? k : p.plan.n_prefix_splits + (k - npre); };
+
+    float M = -INFINITY;
+    for (int32_t k = lane; k < n; k += 32) M = fmaxf(M, p.ws_ml[(base + slot_of(k)) * 2]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+
+    float acc[PER];
+#pragma unroll
+    for (int j = 0; j < PER; ++j) acc[j] = 0.f;
+    float lsum = 0.f;
+    if (M != -INFINITY) {
+        for (int32_t k = 0; k < n; ++k) {
+            const size_t pi = base + slot_of(k);
+            const float2 ml = *reinterpret_cast<const float2 *>(p.ws_ml + pi * 2);
+            const float w = fast_exp2(ml.x - M);
+            lsum = fmaf(w, ml.y, lsum);
+#pragma unroll
+            for (int j = 0; j < PER; ++j) acc[j] = fmaf(w, p.ws_o[pi * D + lane + 32 * j], acc[j]);
+        }
+    }
+    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+    OutT *out = static_cast<OutT *>(p.out) + idx * D;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) out[lane + 32 * j] = to_out<OutT>(acc[j] * inv);
+}
+
+template <typename OutT>
+static cudaError_t launch_combine_t(const DecodeParams &p, cudaStream_t stream)
+{
+    const int64_t pairs = static_cast<int64_t>(p.batch) * p.hq;
+    if (pairs == 0) return cudaSuccess;
+    const unsigned grid = static_cast<unsigned>((pairs + 3) / 4);
+    switch (p.head_dim) {
+    case 32: decode_combine_kernel<OutT, 32><<<grid, 128, 0, stream>>>(p); break;
+    case 64: decode_combine_kernel<OutT, 64><<<grid, 128, 0, stream>>>(p); break;
+    case 128: decode_combine_kernel<OutT, 128><<<grid, 128, 0, stream>>>(p); break;
+    case 256: decode_combine_kernel<OutT, 256><<<grid, 128, 0, stream>>>(p); break;
+    default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_decode_combine(const DecodeParams &p, pkv_dtype dtype, cudaStream_t stream)
+{
+    return dtype == PKV_BF16 ? launch_combine_t<__nv_bfloat16>(p, stream)
+                             : launch_combine_t<float>(p, stream);
+}
+
+}  // namespace pkv

@@ -1,0 +1,83 @@
+// Internal host/device interface between the C ABI layer (api.cu) and the
+// kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pkv.h"
+
+namespace pkv {
+
+struct AppendParams {
+    void *k_pool;
+    void *v_pool;
+    const void *k_new;
+    const void *v_new;
+    const int32_t *slot_mapping;
+    int32_t *status;
+    int32_t num_tokens;
+    int32_t hkv;
+    int32_t block_size;
+    int32_t vecs_per_row;  // head_dim * elem_bytes / 16
+    int32_t num_slots;     // num_blocks * block_size
+};
+
+// Split plan of one decode call.  A row's key range [lo, L) covers the blocks
+// b_first .. b_end-1; split s of the row's suffix covers blocks
+// b_first + s*split_blocks .. (capped at b_end).  Rows of a shared-prefix
+// group start their suffix at the group's prefix_blocks, and the prefix is cut
+// into runs of prefix_split_blocks read once for the whole group.
+struct DecodePlan {
+    int32_t split_blocks;         // C
+    int32_t n_suffix_splits;      // splits per row (upper bound)
+    int32_t prefix_split_blocks;  // Cp
+    int32_t n_prefix_splits;      // prefix splits per group (upper bound); 0 = no prefix path
+    int32_t nslot;                // partial slots per (row, q head) = n_prefix + n_suffix
+    int32_t prefix_chunks;        // CTAs per (group, kv head, prefix split) over its rows
+    int32_t prefix_max;           // prefix lengths are clamped to this (<= table width)
+    int64_t n_prefix_ctas;
+    int64_t n_suffix_ctas;
+};
+
+struct DecodeParams {
+    const void *q;
+    void *out;
+    const void *k_pool;  // used by the CUDA-core (f32) kernel; the bf16 kernel reads via TMA
+    const void *v_pool;
+    const int32_t *tables;
+    const int32_t *seq_lens;
+    const int32_t *group_of_row;   // nullptr when there is no prefix path
+    const int32_t *prefix_blocks;
+    float *ws_o;   // [batch][hq][nslot][head_dim] unnormalised weighted values
+    float *ws_ml;  // [batch][hq][nslot][2]: running max (log2 units) and weight sum
+    int32_t *status;
+    int32_t batch, hq, hkv, group, head_dim, block_size, width, num_blocks;
+    int32_t max_len;   // min(max_seq_len, width * block_size): lengths are clamped to it
+    int32_t window;
+    int32_t num_groups;
+    float scale_log2;  // scale * log2(e): scores are kept in base-2 units
+    DecodePlan plan;
+};
+
+cudaError_t launch_append(const AppendParams &p, cudaStream_t stream);
+
+// bf16 pools: TMA + mbarrier pipeline, mma.sync tiles.  kmap/vmap: 4-D tensor
+// maps (head_dim, block_size, kv head, block) with 64-element boxes, 128B swizzle.
+cudaError_t launch_decode_bf16(const DecodeParams &p, const CUtensorMap &kmap,
+                               const CUtensorMap &vmap, cudaStream_t stream);
+// f32 pools: CUDA-core kernel.
+cudaError_t launch_decode_f32(const DecodeParams &p, cudaStream_t stream);
+// merge of the split partials into out (dtype of q)
+cudaError_t launch_decode_combine(const DecodeParams &p, pkv_dtype dtype, cudaStream_t stream);
+
+// Consumer warps per decode CTA (plus one producer warp for bf16): a suffix
+// CTA's warps share one 16-row query tile and split its blocks; a prefix CTA's
+// warps each own a tile of (row, head) pairs and all read every block.
+constexpr int kDecodeWarps = 4;
+constexpr int kPrefixWarps = 8;
+// query rows per CTA of the f32 kernel
+constexpr int kF32Rows = 16;
+
+}  // namespace pkv

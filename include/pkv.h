@@ -1,0 +1,226 @@
+/*
+ * pkv.h -- C ABI of the GB300 (sm_103a) block-paged KV attention library.
+ *
+ * The operations are those of a vLLM-style block-paged KV cache as the page
+ * "paged-cache.md" (mlx-node docs) describes it: each request keeps its keys and
+ * values in fixed-size blocks of a per-layer pool (LayerKVPool row of the type
+ * table), reached through a per-request block table, and requests that share a
+ * prompt prefix point at the same refcounted blocks.  The page "perf.md"
+ * (mlx-node docs, paged knob table) names the three steps on the hot path: the
+ * graph-native K/V write into pool slots (MLX_PAGED_NATIVE_KV_WRITE), the paged
+ * decode that reads the pages through the table, split into partitions whose
+ * softmax partials a reducer merges (MLX_PAGED_GRAPH_DECODE_GATHER and the
+ * partition-rule paragraphs), and a prefill chunk attending a paged prefix
+ * (gather_kv_for_prefill_chunk).
+ *
+ * Conventions (the plainest reading where the pages are silent):
+ *   - pool layout [num_blocks][num_kv_heads][block_size][head_dim], row major,
+ *     element type pkv_dtype; the K and V pools share the shape;
+ *   - slot = block_id * block_size + offset;  a negative slot is skipped;
+ *   - block tables: int32 [batch][max_blocks_per_seq]; entry j of row r is the
+ *     physical block of the row's positions j*block_size .. +block_size-1;
+ *     -1 is the null sentinel of expired sliding blocks (never read);
+ *   - seq_lens[r] counts every token of row r including those appended this
+ *     step; the decode query of row r sits at position seq_lens[r] - 1;
+ *   - grouped-query attention: q head h reads kv head h / (Hq / Hkv);
+ *   - window W > 0: a query at absolute position p attends positions
+ *     max(0, p - W + 1) .. p; W = 0 is full attention;
+ *   - an empty key range (seq_len 0) yields an all-zero output row;
+ *   - softmax scores are scale * (q . k); accumulation is fp32.
+ *
+ * Ownership and errors.  Every pointer named "device" is device memory owned
+ * by the caller; the library allocates no device memory.  All calls are
+ * asynchronous on the caller's stream.  Arguments are checked on the host
+ * before anything is launched and a bad one returns PKV_ERR_INVALID_ARG (a
+ * combination that is not built returns PKV_ERR_UNSUPPORTED) with nothing
+ * enqueued.  Faults that only the device can see (an out-of-pool block id, a
+ * slot past the pool, a length past the table) never trap: the element is
+ * skipped or masked and a bit is OR-ed into *dev_status (device int32, may be
+ * NULL), see PKV_DEV_*.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *pkv_stream_t;
+
+typedef enum {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = 1,
+    PKV_ERR_UNSUPPORTED = 2,
+    PKV_ERR_CUDA = 3,
+    PKV_ERR_WORKSPACE = 4
+} pkv_status;
+
+typedef enum { PKV_F32 = 0, PKV_BF16 = 1 } pkv_dtype;
+
+/* Bits OR-ed into *dev_status by the kernels. */
+#define PKV_DEV_BAD_BLOCK 1  /* a table entry inside a row's key range is < 0 or >= num_blocks:
+                                that block is treated as fully masked */
+#define PKV_DEV_BAD_SLOT 2   /* an append slot >= num_blocks * block_size: token skipped */
+#define PKV_DEV_BAD_LEN 4    /* seq_len < 0, > max_blocks_per_seq * block_size or > max_seq_len,
+                                or a prefill chunk longer than its row: the row is clamped */
+#define PKV_DEV_BAD_PREFIX 8 /* a row of a shared-prefix group does not hold the group's
+                                prefix blocks, or is shorter than the prefix */
+#define PKV_DEV_TIMEOUT 16   /* a pipeline wait gave up after its time limit; the outputs of
+                                that call are not valid */
+
+/* One layer's K/V block pool (device pointers, 16-byte aligned). */
+typedef struct {
+    void *k;
+    void *v;
+    int32_t num_blocks;
+    int32_t block_size;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    pkv_dtype dtype;
+} pkv_pool;
+
+/*
+ * Shared-prefix descriptor ("paged-cache.md": requests share refcounted blocks
+ * for a common prompt prefix).  Rows of one group hold the same physical
+ * blocks in their first prefix_blocks[group] table entries; the decode reads
+ * those blocks once for all rows of the group.  pkv_prefix_groups_host derives
+ * the device arrays from the block tables.
+ */
+typedef struct {
+    int32_t num_groups;            /* host: number of groups (0 = none) */
+    int32_t max_group_rows;        /* host: upper bound on the rows of any group */
+    int32_t max_prefix_blocks;     /* host: upper bound on prefix_blocks[] */
+    const int32_t *group_of_row;   /* device int32 [batch]: group of each row, -1 = none */
+    const int32_t *prefix_blocks;  /* device int32 [num_groups]: shared leading blocks */
+} pkv_prefix_desc;
+
+/*
+ * Append ("perf.md", paged knob table, MLX_PAGED_NATIVE_KV_WRITE: new K/V rows
+ * are written into their pool slots).  For token t with slot s >= 0:
+ *   pool.k[s / bs][h][s % bs][:] = k_new[t][h][:]   for every kv head h (same for v).
+ * k_new, v_new: device [num_tokens][num_kv_heads][head_dim] of pool.dtype.
+ * slot_mapping: device int32 [num_tokens].  Bit-exact copy.  Two tokens naming
+ * one slot race (the caller must not do that).
+ */
+pkv_status paged_kv_append(const pkv_pool *pool, const int32_t *slot_mapping, int32_t num_tokens,
+                           const void *k_new, const void *v_new, int32_t *dev_status,
+                           pkv_stream_t stream);
+
+/*
+ * Bytes of device workspace paged_decode_attention needs for these sizes on the
+ * current device (the split plan depends on its SM count).  prefix may be NULL.
+ * Returns 0 for invalid sizes.
+ */
+size_t paged_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                   int32_t head_dim, int32_t block_size, int32_t max_seq_len,
+                                   int32_t window, const pkv_prefix_desc *prefix);
+
+/*
+ * Batched paged decode attention ("perf.md", MLX_PAGED_GRAPH_DECODE_GATHER and
+ * the partition-rule paragraphs; "paged-cache.md", Gemma4 coordinator section
+ * for sliding groups).  For every row r and q head h:
+ *   out[r][h][:] = softmax_p(scale * q[r][h] . K_p) . V_p
+ * over the positions p of row r in its key range (see the conventions above),
+ * K_p/V_p read through block_tables from kv head h / (Hq / Hkv).
+ *   q, out:        device [batch][num_q_heads][head_dim], pool.dtype
+ *   block_tables:  device int32 [batch][max_blocks_per_seq]
+ *   seq_lens:      device int32 [batch]
+ *   max_seq_len:   host upper bound on seq_lens (sizes the split plan)
+ *   workspace:     device, >= paged_decode_workspace_size(...) bytes, 256-byte aligned
+ *   prefix:        NULL, or a shared-prefix descriptor (window must be 0)
+ * Split-KV: each row's key range is cut into fixed-size runs of blocks; every
+ * run yields fp32 (max, sum, weighted values) partials that a second kernel
+ * merges.  The cut depends only on the sizes and the SM count, so a call is
+ * bit-reproducible.  Built: f32 and bf16; block_size 16 for bf16 (any
+ * block_size <= 64 for f32); head_dim 64, 128, 256; Hq / Hkv <= 16.
+ */
+pkv_status paged_decode_attention(const void *q, int32_t num_q_heads, const pkv_pool *pool,
+                                  const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                  const int32_t *seq_lens, int32_t batch, int32_t max_seq_len,
+                                  int32_t window, float scale, void *out, void *workspace,
+                                  size_t ws_bytes, const pkv_prefix_desc *prefix,
+                                  int32_t *dev_status, pkv_stream_t stream);
+
+/* Bytes of device workspace paged_prefill_chunk_attention needs. */
+size_t paged_prefill_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                    int32_t head_dim, int32_t block_size, int32_t max_q_len,
+                                    int32_t max_seq_len, int32_t window);
+
+/*
+ * Chunked prefill against a paged prefix ("perf.md", gather_kv_for_prefill_chunk:
+ * a prefill chunk attends the cached prefix through the pages; "paged-cache.md",
+ * chunked prefill whose boundaries change the reduction order but not the
+ * result).  Row r owns the packed queries cu_q_lens[r] .. cu_q_lens[r+1]-1
+ * (C_r of them); its chunk's K/V must already be in the pool (paged_kv_append).
+ * Query i of row r sits at p = seq_lens[r] - C_r + i and attends the positions
+ * max(0, p - W + 1) .. p (W = 0: 0 .. p), i.e. the whole prefix and the chunk
+ * causally.
+ *   q, out:      device [cu_q_lens[batch]][num_q_heads][head_dim], pool.dtype
+ *   cu_q_lens:   device int32 [batch + 1], non-decreasing, cu_q_lens[0] = 0
+ *   max_q_len:   host upper bound on C_r;  max_seq_len: host bound on seq_lens
+ * Built: bf16, block_size 16, head_dim 128, Hq / Hkv <= 16 (tcgen05 tensor
+ * cores, fp32 accumulation in tensor memory; probabilities rounded to bf16
+ * before the P.V product); f32 pools run a CUDA-core kernel.
+ */
+pkv_status paged_prefill_chunk_attention(const void *q, const int32_t *cu_q_lens,
+                                         int32_t num_q_heads, const pkv_pool *pool,
+                                         const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                         const int32_t *seq_lens, int32_t batch, int32_t max_q_len,
+                                         int32_t max_seq_len, int32_t window, float scale,
+                                         void *out, void *workspace, size_t ws_bytes,
+                                         int32_t *dev_status, pkv_stream_t stream);
+
+/* Static text for a status code. */
+const char *pkv_status_string(pkv_status status);
+
+/*
+ * Host helper: slot of each (row, position) pair, slot = table[row][pos / bs] * bs
+ * + pos % bs.  Pairs whose table entry is missing (-1, past the table, or past
+ * the pool) get -1 and make the call return PKV_ERR_INVALID_ARG after filling
+ * every slot.  All arrays are host memory.
+ */
+pkv_status pkv_slot_mapping_host(const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                 int32_t batch, int32_t num_blocks, const int32_t *rows,
+                                 const int32_t *positions, int32_t n, int32_t block_size,
+                                 int32_t *slots_out);
+
+/*
+ * Host helper: shared-prefix groups read off the block tables (host arrays).
+ * Rows whose first entry is the same physical block form a group when there
+ * are at least two of them; the group's prefix is the longest run of leading
+ * entries common to all its rows, cut to blocks that are full in every row
+ * (prefix_blocks * block_size <= seq_len: only full blocks are shared).  Groups
+ * are numbered by their lowest row.  Writes group_of_row[batch] (-1 = none) and
+ * prefix_blocks[0 .. num_groups-1] (capacity batch); returns num_groups, or -1
+ * on invalid arguments.
+ */
+int32_t pkv_prefix_groups_host(const int32_t *block_tables, int32_t max_blocks_per_seq,
+                               const int32_t *seq_lens, int32_t batch, int32_t block_size,
+                               int32_t *group_of_row, int32_t *prefix_blocks);
+
+/*
+ * Diagnostic: force the decode split size to this many blocks per split
+ * (0 = the automatic plan).  Process-wide; for tests of split invariance, in
+ * the spirit of the pages' partition-override knob ("perf.md",
+ * MLX_PAGED_GROUPED_D512_STRIPES).  Returns the previous value.
+ */
+int32_t pkv_set_decode_split_blocks(int32_t blocks_per_split);
+
+/* Number of splits per row and blocks per split the automatic plan picks for
+ * these sizes on the current device (diagnostic; -1 on invalid sizes). */
+int32_t pkv_decode_plan(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                        int32_t head_dim, int32_t block_size, int32_t max_seq_len, int32_t window,
+                        int32_t *blocks_per_split_out);
+
+/* Library version string. */
+const char *pkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */
