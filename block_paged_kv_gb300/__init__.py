@@ -74,11 +74,19 @@ _lib.pkv_decode_plan.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32, _i32,
                                  ctypes.POINTER(_i32)]
 _lib.pkv_decode_plan.restype = _i32
 _lib.pkv_version.restype = ctypes.c_char_p
+_lib.pkv_profile_enable.argtypes = [ctypes.c_uint32]
+_lib.pkv_profile_enable.restype = ctypes.c_int
+_lib.pkv_profile_read.argtypes = [_i32, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_double)]
+_lib.pkv_profile_read.restype = ctypes.c_int
+_lib.pkv_launch_count.restype = ctypes.c_int64
+
+KERNEL_APPEND, KERNEL_DECODE_PREFIX, KERNEL_DECODE_SPLIT, KERNEL_DECODE_COMBINE, KERNEL_PREFILL = range(5)
 
 EXPORTED = ["paged_kv_append", "paged_decode_workspace_size", "paged_decode_attention",
             "paged_prefill_workspace_size", "paged_prefill_chunk_attention", "pkv_status_string",
             "pkv_slot_mapping_host", "pkv_prefix_groups_host", "pkv_set_decode_split_blocks",
-            "pkv_decode_plan", "pkv_version"]
+            "pkv_decode_plan", "pkv_version", "pkv_profile_enable", "pkv_profile_read",
+            "pkv_launch_count"]
 
 
 class PkvError(RuntimeError):
@@ -312,3 +320,24 @@ def decode_plan(batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int, 
 
 def version() -> str:
     return _lib.pkv_version().decode()
+
+
+def profile_enable(kinds=()) -> None:
+    """Time every launch of the given kernel kinds with CUDA events on its stream."""
+    mask = 0
+    for k in kinds:
+        mask |= 1 << k
+    _check("pkv_profile_enable", _lib.pkv_profile_enable(mask))
+
+
+def profile_read(kind: int) -> Tuple[int, float]:
+    """(launches, summed device milliseconds) recorded for a kernel kind."""
+    n = ctypes.c_int64(0)
+    ms = ctypes.c_double(0.0)
+    _check("pkv_profile_read", _lib.pkv_profile_read(kind, ctypes.byref(n), ctypes.byref(ms)))
+    return int(n.value), float(ms.value)
+
+
+def launch_count() -> int:
+    """Kernels launched through the library by this process."""
+    return int(_lib.pkv_launch_count())

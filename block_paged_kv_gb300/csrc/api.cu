@@ -5,6 +5,7 @@
 #include <cmath>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include <cudaTypedefs.h>
 
@@ -27,6 +28,33 @@ using namespace pkv;
 namespace {
 
 std::atomic<int32_t> g_split_override{0};
+
+// ---------------------------------------------------------------------------
+// launch counting and optional per-kind event timing
+// ---------------------------------------------------------------------------
+std::atomic<int64_t> g_launches{0};
+std::atomic<uint32_t> g_prof_mask{0};
+struct ProfRecord {
+    int kind;
+    cudaEvent_t start, stop;
+};
+std::mutex g_prof_mu;
+std::vector<ProfRecord> g_prof_records;
+std::vector<cudaEvent_t> g_prof_free;
+cudaEvent_t g_prof_pending[PKV_KERNEL_KINDS] = {};
+constexpr size_t kMaxProfRecords = 65536;
+
+cudaEvent_t take_event()
+{
+    if (!g_prof_free.empty()) {
+        cudaEvent_t e = g_prof_free.back();
+        g_prof_free.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+}
 
 int num_sms_current()
 {
@@ -170,7 +198,75 @@ bool encode_pool_map(CUtensorMap *map, void *base, const pkv_pool &pool)
 
 }  // namespace
 
+namespace pkv {
+
+void prof_begin(int kind, cudaStream_t stream)
+{
+    g_launches.fetch_add(1);
+    if (!(g_prof_mask.load() & (1u << kind))) return;
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    if (g_prof_records.size() >= kMaxProfRecords) return;
+    cudaEvent_t e = take_event();
+    if (e != nullptr && cudaEventRecord(e, stream) == cudaSuccess) g_prof_pending[kind] = e;
+}
+
+void prof_end(int kind, cudaStream_t stream)
+{
+    if (!(g_prof_mask.load() & (1u << kind))) return;
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    cudaEvent_t s = g_prof_pending[kind];
+    g_prof_pending[kind] = nullptr;
+    if (s == nullptr) return;
+    cudaEvent_t e = take_event();
+    if (e != nullptr && cudaEventRecord(e, stream) == cudaSuccess)
+        g_prof_records.push_back({kind, s, e});
+    else
+        g_prof_free.push_back(s);
+}
+
+}  // namespace pkv
+
 extern "C" {
+
+pkv_status pkv_profile_enable(uint32_t kind_mask)
+{
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    for (auto &r : g_prof_records) {
+        g_prof_free.push_back(r.start);
+        g_prof_free.push_back(r.stop);
+    }
+    g_prof_records.clear();
+    for (auto &e : g_prof_pending) {
+        if (e != nullptr) g_prof_free.push_back(e);
+        e = nullptr;
+    }
+    g_prof_mask.store(kind_mask);
+    return PKV_OK;
+}
+
+pkv_status pkv_profile_read(int32_t kind, int64_t *launches, double *total_ms)
+{
+    if (kind < 0 || kind >= PKV_KERNEL_KINDS || launches == nullptr || total_ms == nullptr)
+        return PKV_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    int64_t n = 0;
+    double ms = 0.0;
+    for (const auto &r : g_prof_records) {
+        if (r.kind != kind) continue;
+        float t = 0.f;
+        if (cudaEventSynchronize(r.stop) != cudaSuccess ||
+            cudaEventElapsedTime(&t, r.start, r.stop) != cudaSuccess)
+            return PKV_ERR_CUDA;
+        ++n;
+        ms += t;
+    }
+    *launches = n;
+    *total_ms = ms;
+    return PKV_OK;
+}
+
+int64_t pkv_launch_count(void) { return g_launches.load(); }
+
 
 const char *pkv_version(void) { return "pkv 0.1 (sm_103a)"; }
 

@@ -50,7 +50,9 @@ cudaError_t launch_append(const AppendParams &p, cudaStream_t stream)
     if (total == 0) return cudaSuccess;
     constexpr int kVpt = 2;
     const int64_t blocks = (total + kVpt * 256 - 1) / (kVpt * 256);
+    prof_begin(PKV_KERNEL_APPEND, stream);
     append_kernel<kVpt><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
+    prof_end(PKV_KERNEL_APPEND, stream);
     return cudaGetLastError();
 }
 

@@ -473,14 +473,18 @@ static cudaError_t launch_d(const DecodeParams &p, const CUtensorMap &kmap, cons
         auto kern = decode_bf16_kernel<D, NWP, NWP>;
         const int smem = Bf16Smem<D, NWP, NWP>::kLaunchBytes;
         if ((err = prepare(kern, smem)) != cudaSuccess) return err;
+        prof_begin(PKV_KERNEL_DECODE_PREFIX, stream);
         kern<<<static_cast<unsigned>(p.plan.n_prefix_ctas), (NWP + 1) * 32, smem, stream>>>(kmap, vmap, p);
+        prof_end(PKV_KERNEL_DECODE_PREFIX, stream);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
     if (p.plan.n_suffix_ctas > 0) {
         auto kern = decode_bf16_kernel<D, NW, 1>;
         const int smem = Bf16Smem<D, NW, 1>::kLaunchBytes;
         if ((err = prepare(kern, smem)) != cudaSuccess) return err;
+        prof_begin(PKV_KERNEL_DECODE_SPLIT, stream);
         kern<<<static_cast<unsigned>(p.plan.n_suffix_ctas), (NW + 1) * 32, smem, stream>>>(kmap, vmap, p);
+        prof_end(PKV_KERNEL_DECODE_SPLIT, stream);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
     return cudaSuccess;

@@ -211,11 +211,15 @@ cudaError_t launch_decode_f32(const DecodeParams &p, cudaStream_t stream)
                                            static_cast<int>(smem));
     if (err != cudaSuccess) return err;
     if (p.plan.n_prefix_ctas > 0) {
+        prof_begin(PKV_KERNEL_DECODE_PREFIX, stream);
         decode_f32_kernel<<<static_cast<unsigned>(p.plan.n_prefix_ctas), kF32Threads, smem, stream>>>(p, 1);
+        prof_end(PKV_KERNEL_DECODE_PREFIX, stream);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
     if (p.plan.n_suffix_ctas > 0) {
+        prof_begin(PKV_KERNEL_DECODE_SPLIT, stream);
         decode_f32_kernel<<<static_cast<unsigned>(p.plan.n_suffix_ctas), kF32Threads, smem, stream>>>(p, 0);
+        prof_end(PKV_KERNEL_DECODE_SPLIT, stream);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
     return cudaSuccess;
@@ -278,6 +282,7 @@ static cudaError_t launch_combine_t(const DecodeParams &p, cudaStream_t stream)
     const int64_t pairs = static_cast<int64_t>(p.batch) * p.hq;
     if (pairs == 0) return cudaSuccess;
     const unsigned grid = static_cast<unsigned>((pairs + 3) / 4);
+    prof_begin(PKV_KERNEL_DECODE_COMBINE, stream);
     switch (p.head_dim) {
     case 32: decode_combine_kernel<OutT, 32><<<grid, 128, 0, stream>>>(p); break;
     case 64: decode_combine_kernel<OutT, 64><<<grid, 128, 0, stream>>>(p); break;
@@ -285,6 +290,7 @@ static cudaError_t launch_combine_t(const DecodeParams &p, cudaStream_t stream)
     case 256: decode_combine_kernel<OutT, 256><<<grid, 128, 0, stream>>>(p); break;
     default: return cudaErrorInvalidValue;
     }
+    prof_end(PKV_KERNEL_DECODE_COMBINE, stream);
     return cudaGetLastError();
 }
 

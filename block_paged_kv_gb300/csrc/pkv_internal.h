@@ -61,6 +61,11 @@ struct DecodeParams {
     DecodePlan plan;
 };
 
+// Launch bookkeeping (api.cu): every kernel launch is counted; launches of
+// kinds enabled by pkv_profile_enable are bracketed by CUDA events.
+void prof_begin(int kind, cudaStream_t stream);
+void prof_end(int kind, cudaStream_t stream);
+
 cudaError_t launch_append(const AppendParams &p, cudaStream_t stream);
 
 // bf16 pools: TMA + mbarrier pipeline, mma.sync tiles.  kmap/vmap: 4-D tensor

@@ -216,6 +216,31 @@ int32_t pkv_decode_plan(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads
                         int32_t head_dim, int32_t block_size, int32_t max_seq_len, int32_t window,
                         int32_t *blocks_per_split_out);
 
+/*
+ * Diagnostic kernel timing and launch counting (no counterpart on the pages:
+ * measurement plumbing).  Kernel kinds: */
+typedef enum {
+    PKV_KERNEL_APPEND = 0,
+    PKV_KERNEL_DECODE_PREFIX = 1, /* shared-prefix read-once decode */
+    PKV_KERNEL_DECODE_SPLIT = 2,  /* per-row split-KV decode */
+    PKV_KERNEL_DECODE_COMBINE = 3,
+    PKV_KERNEL_PREFILL = 4,
+    PKV_KERNEL_KINDS = 5
+} pkv_kernel_kind;
+
+/* Bit k of kind_mask enables timing of kernel kind k: each such launch is
+ * bracketed by two CUDA events recorded on its stream (the events are host
+ * objects; no device memory is allocated).  Resets the accumulated records.
+ * Up to 65536 launches are recorded.  Not for use inside stream capture. */
+pkv_status pkv_profile_enable(uint32_t kind_mask);
+
+/* Launches recorded for a kind and their summed device time in milliseconds.
+ * Waits for the recorded events. */
+pkv_status pkv_profile_read(int32_t kind, int64_t *launches, double *total_ms);
+
+/* Number of kernels this process has launched through the library. */
+int64_t pkv_launch_count(void);
+
 /* Library version string. */
 const char *pkv_version(void);
 
