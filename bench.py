@@ -1,0 +1,462 @@
+#!/usr/bin/env python
+"""Benchmark of the paged-KV decode step on one GB300 (per rank).
+
+A step is one pass of the decode hot path over the batch-32 mixed-length
+workload: append one new token per row into its pool slot
+(paged_kv_append), then batched paged decode attention of every row's query
+over its block table, with the 1024-token shared prefix read once for all 32
+rows (paged_decode_attention).  Workload: bf16, 32 q / 8 kv heads, head_dim
+128, block size 16, suffixes uniform on 0..7168 (seed 1002), block ids
+shuffled.  The K/V read per step (about 0.47 GB) is larger than L2, so no
+flush is needed between steps.
+
+value    = unique K/V bytes the step attends (the prefix once, every row's own
+           tokens) / device time per step, in GB/s (whole job: all ranks).
+e2e      = the same metric with the step's inputs (q, new K/V, slots, lengths)
+           copied from pinned host memory and the output copied back inside
+           the timed region.
+roofline = the dominant kernel (split-KV decode) timed with CUDA events on its
+           own stream during the timed region; its algorithmic bytes are the
+           K/V tiles of the tokens it covers (512 B per token and kv head).
+
+``--impl reference`` times the CPU oracle (single thread) on a bounded sample
+of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import pkv_inputs as gen  # noqa: E402
+
+METRIC = "paged decode KV GB/s (% of 8 TB/s) and decode tok/s at batch 32, 1×GB300"
+NOMINAL_HBM_GBS = 8000.0
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def workload_bytes(w: gen.Workload):
+    """Unique K/V bytes a decode step attends and the split kernel's share."""
+    D, hkv, eb = w.head_dim, w.num_kv_heads, w.elem_bytes
+    per_token = 2 * hkv * D * eb  # K and V, every kv head
+    P = w.shared_prefix_tokens
+    unique_tokens = P + int(np.sum(w.seq_lens.astype(np.int64) - P))
+    suffix_tokens = int(np.sum(w.seq_lens.astype(np.int64) - P))
+    return unique_tokens * per_token, suffix_tokens * per_token
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled with nvidia-smi during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu=timestamp,{self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-i", str(self.index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.2)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = []
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != 7:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[3:]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        # samples from the loaded part of the run: SM clock above idle
+        load = [r for r in rows if r[0] > 0.5 * r[1]] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in load for i, v in enumerate(r[2]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in load), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(load)}
+
+
+# ---------------------------------------------------------------------------
+# the library arm
+# ---------------------------------------------------------------------------
+def kernel_source_sha():
+    h = hashlib.sha256()
+    for f in ("decode_bf16.cu", "decode_common.cuh", "pkv_device.cuh"):
+        with open(os.path.join(ROOT, "block_paged_kv_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(sha):
+    path = os.path.join(ROOT, "profiles", "decode_split_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    if d.get("source_sha") != sha:
+        return None
+    return d.get("dram_bytes_per_launch_full_workload")
+
+
+def run_pkv(args, rank, world, local):
+    import torch
+    import block_paged_kv_gb300 as pkv
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    w = gen.shared_prefix_b32()
+    bytes_step, bytes_split = workload_bytes(w)
+
+    def up(a):
+        if w.dtype == "bf16":
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    k_pool, v_pool = up(w.k_pool), up(w.v_pool)
+    q, k_new, v_new = up(w.q), up(w.k_new), up(w.v_new)
+    tables = torch.from_numpy(w.block_tables).to(dev)
+    lens = torch.from_numpy(w.seq_lens).to(dev)
+    slots_h = pkv.slot_mapping_host(w.block_tables, w.num_blocks, w.new_rows, w.new_pos,
+                                    w.block_size)
+    slots = torch.from_numpy(slots_h).to(dev)
+    desc = pkv.make_prefix_desc(w.block_tables, w.seq_lens, w.block_size, dev)
+    max_len = int(w.seq_lens.max())
+    ws = pkv.alloc_workspace(pkv.decode_workspace_size(w.batch, w.num_q_heads, w.num_kv_heads,
+                                                       w.head_dim, w.block_size, max_len, 0, desc), dev)
+    out = torch.empty_like(q)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step(qx=q, kx=k_new, vx=v_new, sx=slots, lx=lens, ox=out):
+        pkv.paged_kv_append(k_pool, v_pool, sx, kx, vx, status=status)
+        pkv.paged_decode_attention(qx, k_pool, v_pool, tables, lx, 0, w.scale, out=ox,
+                                   workspace=ws, max_seq_len=max_len, prefix=desc, status=status)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def max_over_ranks(x):
+        if world == 1:
+            return x
+        import torch.distributed as dist
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    clocks = ClockSampler(local)
+    if rank == 0:
+        clocks.start()
+    stream = torch.cuda.current_stream(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    pkv.profile_enable([pkv.KERNEL_DECODE_SPLIT])
+    n0 = pkv.launch_count()
+    barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    launches = pkv.launch_count() - n0
+    ms = max_over_ranks(e0.elapsed_time(e1))
+    nsplit, split_ms = pkv.profile_read(pkv.KERNEL_DECODE_SPLIT)
+    pkv.profile_enable([])
+    clk = clocks.stop() if rank == 0 else None
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+
+    # end to end: inputs from pinned host memory, output back, every step
+    q_h = q.cpu().pin_memory()
+    kn_h, vn_h = k_new.cpu().pin_memory(), v_new.cpu().pin_memory()
+    sl_h, ln_h = slots.cpu().pin_memory(), lens.cpu().pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    q_d, kn_d, vn_d = torch.empty_like(q), torch.empty_like(k_new), torch.empty_like(v_new)
+    sl_d, ln_d = torch.empty_like(slots), torch.empty_like(lens)
+    h2d = sum(t.numel() * t.element_size() for t in (q_h, kn_h, vn_h, sl_h, ln_h))
+    d2h = out_h.numel() * out_h.element_size()
+    e2e_steps = max(1, min(args.steps, 1000))
+
+    def e2e_step():
+        q_d.copy_(q_h, non_blocking=True)
+        kn_d.copy_(kn_h, non_blocking=True)
+        vn_d.copy_(vn_h, non_blocking=True)
+        sl_d.copy_(sl_h, non_blocking=True)
+        ln_d.copy_(ln_h, non_blocking=True)
+        step(q_d, kn_d, vn_d, sl_d, ln_d, out)
+        out_h.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1))
+
+    secondary = secondary_measurements(args, pkv, torch, dev) if (rank == 0 and args.secondary) else None
+
+    if rank != 0:
+        return
+    peak, peak_kind = peaks()
+    t_step = ms / args.steps / 1e3
+    value = world * bytes_step / t_step / 1e9
+    split_avg_s = split_ms / max(nsplit, 1) / 1e3
+    achieved = bytes_split / split_avg_s / 1e9
+    sha = kernel_source_sha()
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) cast to bf16; shuffled block ids)",
+        "config": {"workload": w.name, "batch": w.batch, "q_heads": w.num_q_heads,
+                   "kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
+                   "shared_prefix_tokens": w.shared_prefix_tokens, "suffix_tokens": "uniform 0..7168",
+                   "step": "append 1 token/row + shared-prefix paged decode",
+                   "kv_bytes_per_step": bytes_step, "parallelism": f"replicas x{world} (rows shard)",
+                   "l2": "no flush: 0.47 GB of K/V per step exceeds the 129 MB L2"},
+        "pct_of_8TBps": round(100 * value / world / NOMINAL_HBM_GBS, 1),
+        "tok_per_s": round(world * w.batch / t_step, 1),
+        "clocks": clk,
+        "e2e": {"value": round(world * bytes_step / (e2e_ms / e2e_steps / 1e3) / 1e9, 1), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_ms / e2e_steps, 5)},
+        "gpu_launches": int(launches),
+        "roofline": {"kernel": "decode_bf16_kernel<128,4,1> (split-KV decode)", "bound": "hbm",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 3), "peak_source": f"{peak_kind} hbm_gbs",
+                     "traffic": committed_traffic(sha), "algorithmic_bytes_per_launch": bytes_split,
+                     "avg_launch_us": round(split_avg_s * 1e6, 2), "launches_timed": nsplit,
+                     "source_sha": sha},
+    }
+    if secondary is not None:
+        line["secondary"] = secondary
+    if args.cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+
+
+def time_loop(torch, fn, steps, warmup, flush=None):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    total = 0.0
+    for _ in range(steps):
+        if flush is not None:
+            flush()
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        total += e0.elapsed_time(e1)
+    return total / steps / 1e3
+
+
+def secondary_measurements(args, pkv, torch, dev):
+    """The other workloads, shorter runs: dense decode (L2 flushed), long
+    context full + sliding, bulk append of a whole context."""
+    res = {}
+    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def flush():
+        flush_buf.add_(1)
+
+    def up(w, a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    # dense decode (33.5 MB of K/V: L2-sized, so L2 is flushed before each step)
+    w = gen.dense_bf16()
+    kp, vp, q = up(w, w.k_pool), up(w, w.v_pool), up(w, w.q)
+    t = torch.from_numpy(w.block_tables).to(dev)
+    sl = torch.from_numpy(w.seq_lens).to(dev)
+    out = torch.empty_like(q)
+    ws = pkv.alloc_workspace(pkv.decode_workspace_size(w.batch, w.num_q_heads, w.num_kv_heads,
+                                                       w.head_dim, 16, 2048, 0), dev)
+    s = time_loop(torch, lambda: pkv.paged_decode_attention(q, kp, vp, t, sl, 0, w.scale, out=out,
+                                                            workspace=ws, max_seq_len=2048),
+                  200, 10, flush)
+    b = workload_bytes(w)[0]
+    res["dense_bf16_decode"] = {"us": round(s * 1e6, 2), "GB/s": round(b / s / 1e9, 1),
+                                "kv_bytes": b, "l2": "flushed before each step"}
+    del kp, vp
+    # long context: full group and sliding group, one call each
+    full, sliding = gen.long_two_groups()
+    for name, w in (("long_full_bf16_decode", full), ("long_sliding_bf16_decode", sliding)):
+        kp, vp, q = up(w, w.k_pool), up(w, w.v_pool), up(w, w.q)
+        t = torch.from_numpy(w.block_tables).to(dev)
+        sl = torch.from_numpy(w.seq_lens).to(dev)
+        out = torch.empty_like(q)
+        ml = int(w.seq_lens.max())
+        ws = pkv.alloc_workspace(pkv.decode_workspace_size(w.batch, w.num_q_heads, w.num_kv_heads,
+                                                           w.head_dim, 16, ml, w.window), dev)
+        s = time_loop(torch, lambda: pkv.paged_decode_attention(q, kp, vp, t, sl, w.window, w.scale,
+                                                                out=out, workspace=ws, max_seq_len=ml),
+                      100, 5, flush)
+        if w.window:
+            b = w.batch * min(w.window, ml) * 2 * w.num_kv_heads * w.head_dim * 2
+        else:
+            b = workload_bytes(w)[0]
+        res[name] = {"us": round(s * 1e6, 2), "GB/s": round(b / s / 1e9, 1), "kv_bytes": b}
+        del kp, vp
+    # bulk append: every token of the batch-32 workload's private suffixes
+    w = gen.shared_prefix_b32()
+    n = int(np.sum(w.seq_lens - 1024))
+    kp = torch.empty((w.num_blocks, 8, 16, 128), dtype=torch.bfloat16, device=dev)
+    vp = torch.empty_like(kp)
+    rows = np.repeat(np.arange(w.batch), w.seq_lens - 1024).astype(np.int32)
+    pos = np.concatenate([np.arange(1024, L) for L in w.seq_lens]).astype(np.int32)
+    slots = torch.from_numpy(pkv.slot_mapping_host(w.block_tables, w.num_blocks, rows, pos, 16)).to(dev)
+    kn = torch.randn((n, 8, 128), dtype=torch.bfloat16, device=dev)
+    vn = torch.randn_like(kn)
+    s = time_loop(torch, lambda: pkv.paged_kv_append(kp, vp, slots, kn, vn), 50, 5)
+    b = 2 * 2 * n * 8 * 128 * 2 + 4 * n
+    res["bulk_append"] = {"tokens": n, "us": round(s * 1e6, 2), "GB/s": round(b / s / 1e9, 1),
+                          "bytes": b}
+    return res
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (the reference arm and the cpu_baseline field)
+# ---------------------------------------------------------------------------
+def _oracle_setup(w):
+    import oracle
+    orc = oracle.load()
+    slots, bad = orc.slot_mapping(w.block_tables, w.num_blocks, w.new_rows, w.new_pos, w.block_size)
+    kp, vp = w.k_pool.copy(), w.v_pool.copy()
+    orc.append(kp, vp, w.dtype, slots, w.k_new, w.v_new)
+    return orc, kp, vp
+
+
+def _oracle_rate(w, orc, kp, vp, budget_s, rows_order):
+    """Oracle time for sampled rows (all q heads each) until about budget_s;
+    the full step's time is extrapolated by attended keys."""
+    bytes_step, _ = workload_bytes(w)
+    full_keys = float(np.sum(w.seq_lens.astype(np.int64))) * w.num_q_heads
+    done_keys, spent, rows = 0.0, 0.0, []
+    for r in rows_order:
+        pairs = np.array([[r, h] for h in range(w.num_q_heads)], dtype=np.int32)
+        t0 = time.perf_counter()
+        orc.decode(w.q, kp, vp, w.dtype, w.block_tables, w.seq_lens, w.window, w.scale, pairs=pairs)
+        spent += time.perf_counter() - t0
+        done_keys += float(w.seq_lens[r]) * w.num_q_heads
+        rows.append(int(r))
+        if spent >= budget_s:
+            break
+    t_full = spent * full_keys / done_keys
+    return bytes_step / t_full / 1e9, rows, spent
+
+
+def cpu_baseline(w, budget_s=10.0):
+    orc, kp, vp = _oracle_setup(w)
+    order = gen.permutation(77, "cpu_rows", w.batch)
+    value, rows, spent = _oracle_rate(w, orc, kp, vp, budget_s, order)
+    return {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"decode of rows {rows} (all 32 q heads each, {spent:.1f} s single-threaded); "
+                      "full-step time extrapolated by attended keys"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    w = gen.shared_prefix_b32()
+    orc, kp, vp = _oracle_setup(w)
+    order = gen.permutation(77, "cpu_rows", w.batch)
+    total_steps = args.steps + args.warmup
+    per_step = max(0.05, min(5.0, 120.0 / max(total_steps, 1)))
+    vals = []
+    for i in range(total_steps):
+        rot = np.roll(order, -i)
+        v, rows, spent = _oracle_rate(w, orc, kp, vp, per_step, rot)
+        if i >= args.warmup:
+            vals.append((v, spent, rows))
+    value = statistics.median(v for v, _, _ in vals)
+    ms_step = 1e3 * workload_bytes(w)[0] / (value * 1e9)
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms_step, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "batch": w.batch, "q_heads": w.num_q_heads,
+                       "kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
+                       "step": "oracle decode (CPU, IEEE double), bounded sample per step"},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"each step: whole rows (all q heads) for about {per_step:.2f} s; "
+                                       "full-step time extrapolated by attended keys"},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["pkv", "reference"], default="pkv")
+    ap.add_argument("--no-secondary", dest="secondary", action="store_false")
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_pkv(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -14,8 +14,9 @@
 // into a ring of STAGES shared-memory slots guarded by mbarriers.  Consumer
 // warps compute S = Q K^T and O += P V with mma.sync m16n8k16 (bf16 in, fp32
 // accumulate): M = 16 query rows, N = 8 tokens or 8 dims.  The online softmax
-// runs on the accumulator fragments with quad shuffles; P is rounded to bf16
-// for the P.V product and the row sums use the rounded values.  Each tile's
+// runs on the accumulator fragments with quad shuffles; P enters the P.V
+// product as two bf16 terms (hi + lo) so that its rounding stays far below
+// the output's own bf16 rounding.  Each tile's
 // partial (max in log2 units, sum, unnormalised O) goes to the workspace.
 #include "decode_common.cuh"
 
@@ -350,15 +351,28 @@ __global__ void __launch_bounds__((NW + 1) * 32, TILES == 1 ? 2 : 1)
         const float al0 = fast_exp2(m0 - mu0), al1 = fast_exp2(m1 - mu1);
         m0 = mn0;
         m1 = mn1;
-        uint32_t pa[4];
-        pa[0] = pack_bf16x2(fast_exp2(s[0][0] - mu0), fast_exp2(s[0][1] - mu0));
-        pa[1] = pack_bf16x2(fast_exp2(s[0][2] - mu1), fast_exp2(s[0][3] - mu1));
-        pa[2] = pack_bf16x2(fast_exp2(s[1][0] - mu0), fast_exp2(s[1][1] - mu0));
-        pa[3] = pack_bf16x2(fast_exp2(s[1][2] - mu1), fast_exp2(s[1][3] - mu1));
-        l0 = l0 * al0 + ((bf16lo_to_f32(pa[0]) + bf16hi_to_f32(pa[0])) +
-                         (bf16lo_to_f32(pa[2]) + bf16hi_to_f32(pa[2])));
-        l1 = l1 * al1 + ((bf16lo_to_f32(pa[1]) + bf16hi_to_f32(pa[1])) +
-                         (bf16lo_to_f32(pa[3]) + bf16hi_to_f32(pa[3])));
+        // P = 2^(s - m) as a bf16 pair hi + lo (lo = bf16(P - hi)): the P.V
+        // product then carries P to about 2^-17 relative instead of the 2^-9
+        // of a single bf16 rounding
+        float pf[2][4];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            pf[j][0] = fast_exp2(s[j][0] - mu0);
+            pf[j][1] = fast_exp2(s[j][1] - mu0);
+            pf[j][2] = fast_exp2(s[j][2] - mu1);
+            pf[j][3] = fast_exp2(s[j][3] - mu1);
+        }
+        uint32_t pa[4], pl[4];
+        pa[0] = pack_bf16x2(pf[0][0], pf[0][1]);
+        pa[1] = pack_bf16x2(pf[0][2], pf[0][3]);
+        pa[2] = pack_bf16x2(pf[1][0], pf[1][1]);
+        pa[3] = pack_bf16x2(pf[1][2], pf[1][3]);
+        pl[0] = pack_bf16x2(pf[0][0] - bf16lo_to_f32(pa[0]), pf[0][1] - bf16hi_to_f32(pa[0]));
+        pl[1] = pack_bf16x2(pf[0][2] - bf16lo_to_f32(pa[1]), pf[0][3] - bf16hi_to_f32(pa[1]));
+        pl[2] = pack_bf16x2(pf[1][0] - bf16lo_to_f32(pa[2]), pf[1][1] - bf16hi_to_f32(pa[2]));
+        pl[3] = pack_bf16x2(pf[1][2] - bf16lo_to_f32(pa[3]), pf[1][3] - bf16hi_to_f32(pa[3]));
+        l0 = l0 * al0 + ((pf[0][0] + pf[0][1]) + (pf[1][0] + pf[1][1]));
+        l1 = l1 * al1 + ((pf[0][2] + pf[0][3]) + (pf[1][2] + pf[1][3]));
 #pragma unroll
         for (int nt = 0; nt < C::kNT; ++nt) {
             o[nt][0] *= al0;
@@ -385,6 +399,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, TILES == 1 ? 2 : 1)
                 v0 &= mk0; v1 &= mk1; v2 &= mk0; v3 &= mk1;
                 mma_16816(o[2 * np], pa, v0, v1);
                 mma_16816(o[2 * np + 1], pa, v2, v3);
+                mma_16816(o[2 * np], pl, v0, v1);
+                mma_16816(o[2 * np + 1], pl, v2, v3);
             }
         }
         __syncwarp();

@@ -45,8 +45,7 @@ def test_bad_slot_sets_status(pkv, dtype):
     pkv.paged_kv_append(d.k_pool, d.v_pool, slots, d.k_new, d.v_new, status=d.status)
     torch.cuda.synchronize()
     assert int(d.status.item()) == pkv.DEV_BAD_SLOT
-    assert torch.equal(before.view(torch.uint8) if dtype == "bf16" else before,
-                       d.k_pool.view(torch.uint8) if dtype == "bf16" else d.k_pool)
+    assert torch.equal(before.view(torch.uint8), d.k_pool.view(torch.uint8))
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
