@@ -15,9 +15,10 @@ value    = unique K/V bytes the step attends (the prefix once, every row's own
 e2e      = the same metric with the step's inputs (q, new K/V, slots, lengths)
            copied from pinned host memory and the output copied back inside
            the timed region.
-roofline = the dominant kernel (split-KV decode) timed with CUDA events on its
-           own stream during the timed region; its algorithmic bytes are the
-           K/V tiles of the tokens it covers (512 B per token and kv head).
+roofline = the dominant kernel (the decode kernel: shared-prefix and split-KV
+           CTAs in one launch) timed with CUDA events on its own stream during
+           the timed region; its algorithmic bytes are the unique K/V tiles it
+           reads (512 B per token and kv head; the prefix once).
 
 ``--impl reference`` times the CPU oracle (single thread) on a bounded sample
 of the same workload instead.
@@ -252,7 +253,7 @@ def run_pkv(args, rank, world, local):
     t_step = ms / args.steps / 1e3
     value = world * bytes_step / t_step / 1e9
     split_avg_s = split_ms / max(nsplit, 1) / 1e3
-    achieved = bytes_split / split_avg_s / 1e9
+    achieved = bytes_step / split_avg_s / 1e9
     sha = kernel_source_sha()
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
@@ -272,10 +273,11 @@ def run_pkv(args, rank, world, local):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms / e2e_steps, 5)},
         "gpu_launches": int(launches),
-        "roofline": {"kernel": "decode_bf16_kernel<128,4,1> (split-KV decode)", "bound": "hbm",
+        "roofline": {"kernel": "decode_bf16_kernel<128> (shared-prefix + split-KV decode, one launch)",
+                     "bound": "hbm",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 3), "peak_source": f"{peak_kind} hbm_gbs",
-                     "traffic": committed_traffic(sha), "algorithmic_bytes_per_launch": bytes_split,
+                     "traffic": committed_traffic(sha), "algorithmic_bytes_per_launch": bytes_step,
                      "avg_launch_us": round(split_avg_s * 1e6, 2), "launches_timed": nsplit,
                      "source_sha": sha},
     }

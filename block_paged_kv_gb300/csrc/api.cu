@@ -119,11 +119,13 @@ DecodePlan make_plan(int32_t batch, int32_t hq, int32_t hkv, int32_t D, int32_t 
     pl.prefix_chunks = 0;
     pl.n_prefix_ctas = 0;
     if (prefix != nullptr && prefix->num_groups > 0 && prefix->max_prefix_blocks > 0) {
-        // The prefix cut aims at about one CTA per SM for the bf16 kernel (128
-        // (row, head) pairs per CTA); it does not depend on the dtype, so the
-        // workspace size does not either.  The f32 kernel takes 16 pairs per CTA.
+        // The prefix cut aims at about one CTA per SM for the bf16 kernel (64
+        // (row, head) pairs per CTA, 32 at head_dim 256); it does not depend
+        // on the dtype, so the workspace size does not either.  The f32 kernel
+        // takes 16 pairs per CTA.
         const int64_t rows_pairs = static_cast<int64_t>(prefix->max_group_rows) * G;
-        const int64_t chunks_bf16 = ceil_div64(rows_pairs, kPrefixWarps * 16);
+        const int64_t pairs_bf16 = D == 256 ? kPrefixPairsPerCta / 2 : kPrefixPairsPerCta;
+        const int64_t chunks_bf16 = ceil_div64(rows_pairs, pairs_bf16);
         int64_t Cp = ceil_div64(static_cast<int64_t>(prefix->max_prefix_blocks) * hkv *
                                     prefix->num_groups * chunks_bf16,
                                 std::max(num_sms, 1));

@@ -15,6 +15,8 @@ template <int VPT>
 __global__ void __launch_bounds__(256) append_kernel(AppendParams p)
 {
     // vector v of row (t, h):  idx = (t * hkv + h) * vecs_per_row + v
+    pdl_wait();
+    pdl_trigger();
     const int64_t total = static_cast<int64_t>(p.num_tokens) * p.hkv * p.vecs_per_row;
     // each block covers VPT * blockDim consecutive vectors, one warp-wide
     // contiguous run per unrolled step
@@ -51,9 +53,10 @@ cudaError_t launch_append(const AppendParams &p, cudaStream_t stream)
     constexpr int kVpt = 2;
     const int64_t blocks = (total + kVpt * 256 - 1) / (kVpt * 256);
     prof_begin(PKV_KERNEL_APPEND, stream);
-    append_kernel<kVpt><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
+    const cudaError_t err = launch_pdl(append_kernel<kVpt>, dim3(static_cast<unsigned>(blocks)),
+                                       dim3(256), 0, stream, p);
     prof_end(PKV_KERNEL_APPEND, stream);
-    return cudaGetLastError();
+    return err;
 }
 
 }  // namespace pkv

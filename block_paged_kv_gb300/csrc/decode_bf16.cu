@@ -3,12 +3,13 @@
 // whose online-softmax partials a reducer merges; all q heads of a GQA group
 // share each block load, as the pages' grouped decode kernels do).
 //
-// One CTA = one work item:
-//   suffix item (TILES == 1): row r, kv head g, split s -> blocks
-//       b_first + s*C .. ; its 16-row query tile holds the G q heads of (r, g);
-//   prefix item (TILES == NW): group, kv head g, row chunk, prefix split s ->
-//       prefix blocks s*Cp ..; NW query tiles hold (row, head) pairs of the
-//       group, so every shared block is read once for all of them.
+// One launch carries two kinds of CTA, one work item each:
+//   prefix item (the first n_prefix_ctas CTAs): group, kv head g, row chunk,
+//       prefix split s -> prefix blocks s*Cp ..; its query tiles hold (row,
+//       head) pairs of the group's rows, so every shared block is read once
+//       for all of them;
+//   split item: row r, kv head g, split s -> blocks b_first + s*C .. ; its one
+//       16-row query tile holds the G q heads of (r, g).
 // A producer warp streams (block, kv head) K and V tiles with TMA tensor loads
 // (4-D maps over [block][kv head][slot][dim], 64-dim boxes, 128-byte swizzle)
 // into a ring of STAGES shared-memory slots guarded by mbarriers.  Consumer
@@ -27,27 +28,32 @@ struct Bf16Cfg {
     static constexpr int kTok = 16;                       // block_size
     static constexpr int kTileBytes = kTok * D * 2;       // one (block, kv head) tile of K or V
     static constexpr int kStageBytes = 2 * kTileBytes;    // K + V
-    static constexpr int kStages = (64 * 1024) / kStageBytes;
+    // ring sized so that two CTAs fit on an SM next to their query tiles
+    static constexpr int kRingBytes = (D == 256 ? 80 : 88) * 1024;
+    static constexpr int kStages = kRingBytes / kStageBytes;
     static constexpr int kRegions = D / 64;               // 64-dim swizzled regions per tile
     static constexpr int kRegionBytes = kTok * 128;
     static constexpr int kQStride = (D + 8) * 2;          // padded query row (bytes)
     static constexpr int kQTileBytes = 16 * kQStride;
+    static constexpr int kPrefixTiles = (D == 256 ? kPrefixPairsPerCta / 2 : kPrefixPairsPerCta) / 16;
     static constexpr bool kQInRegs = D <= 128;
     static constexpr int kNT = D / 8;                     // 8-dim output n-tiles
     static constexpr int kKS = D / 16;                    // 16-dim k-steps of Q K^T
 };
 
-template <int D, int NW, int TILES>
+template <int D>
 struct Bf16Smem {
     using C = Bf16Cfg<D>;
     static constexpr int kStageOff = 0;
     static constexpr int kQOff = C::kStages * C::kStageBytes;
-    static constexpr int kBarOff = kQOff + TILES * C::kQTileBytes;
+    static constexpr int kBarOff = kQOff + C::kPrefixTiles * C::kQTileBytes;
     static constexpr int kOkOff = kBarOff + 2 * C::kStages * 8;
     static constexpr int kPairOff = kOkOff + C::kStages * 4;
-    static constexpr int kMiscOff = kPairOff + 3 * TILES * 16 * 4;
+    static constexpr int kMiscOff = kPairOff + 3 * C::kPrefixTiles * 16 * 4;
     static constexpr int kBytes = kMiscOff + 16;
     static constexpr int kLaunchBytes = kBytes + 1024;  // room to align the base to 1024
+    static_assert(kDecodeWarps * 16 * D * 4 + kDecodeWarps * 16 * 8 <= kQOff + C::kPrefixTiles * C::kQTileBytes,
+                  "the merge buffers fit in the ring and query tiles");
 };
 
 // Swizzled shared address of the 16-byte chunk holding dims d0..d0+7 of token
@@ -64,16 +70,15 @@ __device__ __forceinline__ void consumer_bar_sync(int nthreads)
     asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
 }
 
-template <int D, int NW, int TILES>
-__global__ void __launch_bounds__((NW + 1) * 32, TILES == 1 ? 2 : 1)
+template <int D>
+__global__ void __launch_bounds__((kDecodeWarps + 1) * 32, D == 256 ? 2 : 1)
     decode_bf16_kernel(const __grid_constant__ CUtensorMap kmap,
                        const __grid_constant__ CUtensorMap vmap, const DecodeParams p)
 {
     using C = Bf16Cfg<D>;
-    using SM = Bf16Smem<D, NW, TILES>;
-    constexpr int WPT = NW / TILES;  // consumer warps per query tile
+    using SM = Bf16Smem<D>;
+    constexpr int NW = kDecodeWarps;
     constexpr int STAGES = C::kStages;
-    static_assert(NW % TILES == 0, "tiles split the consumer warps evenly");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -84,8 +89,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, TILES == 1 ? 2 : 1)
     uint64_t *empty = full + STAGES;
     int32_t *stage_ok = reinterpret_cast<int32_t *>(smem + SM::kOkOff);
     int32_t *pair_row = reinterpret_cast<int32_t *>(smem + SM::kPairOff);
-    int32_t *pair_head = pair_row + TILES * 16;
-    int32_t *pair_len = pair_head + TILES * 16;
+    int32_t *pair_head = pair_row + C::kPrefixTiles * 16;
+    int32_t *pair_len = pair_head + C::kPrefixTiles * 16;
     int32_t *misc = reinterpret_cast<int32_t *>(smem + SM::kMiscOff);
 
     const int warp = threadIdx.x >> 5;
@@ -93,11 +98,19 @@ __global__ void __launch_bounds__((NW + 1) * 32, TILES == 1 ? 2 : 1)
     const int G = p.group;
     const int bs = C::kTok;
 
+    if (warp == NW && lane == 0) {
+        tma_prefetch_desc(&kmap);
+        tma_prefetch_desc(&vmap);
+    }
+    pdl_wait();     // inputs may come from the previous kernel on the stream
+    pdl_trigger();  // the merge kernel may be scheduled now; it waits for us
+
     // ---------------------------------------------------------------- work item
-    int32_t b0, nblk, slot, tab_row, g, lo_all, hi_all;
-    int32_t row_r = 0;  // suffix item only
-    if constexpr (TILES == 1) {
-        int64_t bid = blockIdx.x;
+    const bool prefix_item = static_cast<int64_t>(blockIdx.x) < p.plan.n_prefix_ctas;
+    int32_t b0, nblk, slot, tab_row, g, lo_all, hi_all, tiles;
+    int32_t row_r = 0;  // split item only
+    if (!prefix_item) {
+        int64_t bid = static_cast<int64_t>(blockIdx.x) - p.plan.n_prefix_ctas;
         const int32_t s = static_cast<int32_t>(bid % p.plan.n_suffix_splits);
         bid /= p.plan.n_suffix_splits;
         g = static_cast<int32_t>(bid % p.hkv);
@@ -111,7 +124,9 @@ __global__ void __launch_bounds__((NW + 1) * 32, TILES == 1 ? 2 : 1)
         tab_row = row_r;
         lo_all = rr.lo;
         hi_all = rr.L;
+        tiles = 1;
     } else {
+        tiles = C::kPrefixTiles;
         int64_t bid = blockIdx.x;
         const int32_t s = static_cast<int32_t>(bid % p.plan.n_prefix_splits);
         bid /= p.plan.n_prefix_splits;
@@ -127,11 +142,12 @@ __global__ void __launch_bounds__((NW + 1) * 32, TILES == 1 ? 2 : 1)
         if (b0 >= b1) return;
         nblk = b1 - b0;
         slot = s;
-        for (int i = threadIdx.x; i < TILES * 16; i += blockDim.x) pair_row[i] = -1;
+        for (int i = threadIdx.x; i < tiles * 16; i += blockDim.x) pair_row[i] = -1;
         __syncthreads();
         if (warp == 0) {
             // rows of the group in ascending order; pair k = rank * G + j
-            const int32_t kbase = chunk * TILES * 16;
+            const int32_t per_cta = tiles * 16;
+            const int32_t kbase = chunk * per_cta;
             int32_t cnt = 0, leader = -1, hmax = 0;
             for (int32_t base = 0; base < p.batch; base += 32) {
                 const int32_t r = base + lane;
@@ -143,11 +159,11 @@ __global__ void __launch_bounds__((NW + 1) * 32, TILES == 1 ? 2 : 1)
                     int32_t L = __ldg(p.seq_lens + r);
                     L = L < 0 ? 0 : (L > p.max_len ? p.max_len : L);
                     if (L < P * bs) report(p.status, PKV_DEV_BAD_PREFIX);
-                    if ((rank + 1) * G > p.plan.prefix_chunks * TILES * 16)
+                    if ((rank + 1) * G > p.plan.prefix_chunks * per_cta)
                         report(p.status, PKV_DEV_BAD_PREFIX);  // more rows than max_group_rows
                     for (int j = 0; j < G; ++j) {
                         const int32_t k = rank * G + j - kbase;
-                        if (k >= 0 && k < TILES * 16) {
+                        if (k >= 0 && k < per_cta) {
                             pair_row[k] = r;
                             pair_head[k] = g * G + j;
                             pair_len[k] = L;
@@ -170,7 +186,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, TILES == 1 ? 2 : 1)
         lo_all = 0;
         hi_all = misc[1];
         // every row of the chunk must hold the leader's blocks in this range
-        for (int i = threadIdx.x; i < TILES * 16 * nblk; i += blockDim.x) {
+        for (int i = threadIdx.x; i < tiles * 16 * nblk; i += blockDim.x) {
             const int k = i / nblk, b = b0 + i % nblk;
             const int32_t pr = pair_row[k];
             if (pr >= 0 && (k % G) == 0 &&
@@ -179,15 +195,15 @@ __global__ void __launch_bounds__((NW + 1) * 32, TILES == 1 ? 2 : 1)
                 report(p.status, PKV_DEV_BAD_PREFIX);
         }
     }
+    const int WPT = NW / tiles;  // consumer warps per query tile
 
     // ------------------------------------------------- query tiles + barriers
     {
-        const int nthr = blockDim.x;
         constexpr int kVec = D / 8;  // 16-byte vectors per row
-        for (int i = threadIdx.x; i < TILES * 16 * kVec; i += nthr) {
+        for (int i = threadIdx.x; i < tiles * 16 * kVec; i += blockDim.x) {
             const int row = i / kVec, v = i % kVec;
             int32_t qr = -1, qh = 0;
-            if constexpr (TILES == 1) {
+            if (!prefix_item) {
                 if (row < G) {
                     qr = row_r;
                     qh = g * G + row;
@@ -206,7 +222,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, TILES == 1 ? 2 : 1)
         if (threadIdx.x == 0) {
             for (int s = 0; s < STAGES; ++s) {
                 mbar_init(&full[s], 1);
-                mbar_init(&empty[s], TILES);
+                mbar_init(&empty[s], tiles);
             }
             fence_mbar_init();
         }
@@ -215,10 +231,6 @@ __global__ void __launch_bounds__((NW + 1) * 32, TILES == 1 ? 2 : 1)
 
     // ---------------------------------------------------------------- producer
     if (warp == NW) {
-        if (lane == 0) {
-            tma_prefetch_desc(&kmap);
-            tma_prefetch_desc(&vmap);
-        }
         const uint64_t policy = l2_evict_first_policy();
         bool abort = false;
         for (int base = 0; base < nblk && !abort; base += 32) {
@@ -268,7 +280,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, TILES == 1 ? 2 : 1)
     const int qd = lane >> 2;        // fragment rows qd and qd + 8
     const int c2 = 2 * (lane & 3);   // fragment columns c2, c2 + 1
     int lo0, hi0, lo1, hi1;
-    if constexpr (TILES == 1) {
+    if (!prefix_item) {
         lo0 = lo1 = lo_all;
         hi0 = hi1 = hi_all;
     } else {
@@ -292,7 +304,6 @@ __global__ void __launch_bounds__((NW + 1) * 32, TILES == 1 ? 2 : 1)
 #pragma unroll
     for (int nt = 0; nt < C::kNT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    bool timed_out = false;
 
     // lane-constant parts of the ldmatrix addresses
     const int k_tok = (lane >> 4) * 8 + (lane & 7);
@@ -305,7 +316,6 @@ __global__ void __launch_bounds__((NW + 1) * 32, TILES == 1 ? 2 : 1)
         const bool got = mbar_wait(&full[st], (i / STAGES) & 1);
         if (__any_sync(0xffffffffu, !got)) {
             if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
-            timed_out = true;
             break;
         }
         const bool ok = stage_ok[st] != 0;
@@ -413,97 +423,65 @@ __global__ void __launch_bounds__((NW + 1) * 32, TILES == 1 ? 2 : 1)
     l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
 
-    if constexpr (WPT == 1) {
-        // prefix item: every warp owns its tile; write its rows directly
-        if (timed_out) return;
+    // merge the WPT warps of each tile through shared memory (the ring and
+    // query tiles are free once every consumer is past its last block)
+    float *mbuf = reinterpret_cast<float *>(stage_mem);         // [NW * 16][D]
+    float *mlbuf = mbuf + NW * 16 * D;                           // [NW * 16][2]
+    auto row_valid = [&](int t, int row) {
+        return prefix_item ? pair_row[t * 16 + row] >= 0 : row < G;
+    };
+    consumer_bar_sync(NW * 32);
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            const int k = tile * 16 + qd + half * 8;
-            const int32_t pr = pair_row[k];
-            if (pr < 0) continue;
-            const size_t pi = partial_index(p, pr, pair_head[k], slot);
-            float *dst = p.ws_o + pi * D;
+    for (int half = 0; half < 2; ++half) {
+        const int row = qd + half * 8;
+        if (!row_valid(tile, row)) continue;
+        const int mrow = warp * 16 + row;  // warp = tile * WPT + sub
+        float *dst = mbuf + mrow * D;
 #pragma unroll
-            for (int nt = 0; nt < C::kNT; ++nt)
-                *reinterpret_cast<float2 *>(dst + nt * 8 + c2) =
-                    make_float2(o[nt][2 * half], o[nt][2 * half + 1]);
-            if ((lane & 3) == 0)
-                *reinterpret_cast<float2 *>(p.ws_ml + pi * 2) =
-                    make_float2(half ? m1 : m0, half ? l1 : l0);
-        }
-    } else {
-        // suffix item: merge the NW warps' partials of the one tile
-        float *mbuf = reinterpret_cast<float *>(stage_mem);           // [WPT][G][D]
-        float *mlbuf = mbuf + WPT * G * D;                             // [WPT][G][2]
-        consumer_bar_sync(NW * 32);  // every warp is done with the stage ring
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            const int row = qd + half * 8;
-            if (row >= G) continue;
-            float *dst = mbuf + (sub * G + row) * D;
-#pragma unroll
-            for (int nt = 0; nt < C::kNT; ++nt)
-                *reinterpret_cast<float2 *>(dst + nt * 8 + c2) =
-                    make_float2(o[nt][2 * half], o[nt][2 * half + 1]);
-            if ((lane & 3) == 0) {
-                mlbuf[(sub * G + row) * 2] = half ? m1 : m0;
-                mlbuf[(sub * G + row) * 2 + 1] = half ? l1 : l0;
-            }
-        }
-        consumer_bar_sync(NW * 32);
-        for (int idx = threadIdx.x; idx < G * D; idx += NW * 32) {
-            const int row = idx / D, d = idx % D;
-            float M = -INFINITY;
-#pragma unroll
-            for (int w = 0; w < WPT; ++w) M = fmaxf(M, mlbuf[(w * G + row) * 2]);
-            float acc = 0.f, lsum = 0.f;
-            if (M != -INFINITY) {
-#pragma unroll
-                for (int w = 0; w < WPT; ++w) {
-                    const float wgt = fast_exp2(mlbuf[(w * G + row) * 2] - M);
-                    acc += wgt * mbuf[(w * G + row) * D + d];
-                    lsum += wgt * mlbuf[(w * G + row) * 2 + 1];
-                }
-            }
-            const size_t pi = partial_index(p, row_r, g * G + row, slot);
-            p.ws_o[pi * D + d] = acc;
-            if (d == 0) *reinterpret_cast<float2 *>(p.ws_ml + pi * 2) = make_float2(M, lsum);
-        }
+        for (int nt = 0; nt < C::kNT; ++nt)
+            *reinterpret_cast<float2 *>(dst + nt * 8 + c2) =
+                make_float2(o[nt][2 * half], o[nt][2 * half + 1]);
+        if ((lane & 3) == 0)
+            *reinterpret_cast<float2 *>(mlbuf + mrow * 2) = make_float2(half ? m1 : m0, half ? l1 : l0);
     }
-}
-
-template <typename K>
-static cudaError_t prepare(K kernel, int smem_bytes)
-{
-    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    consumer_bar_sync(NW * 32);
+    for (int idx = threadIdx.x; idx < tiles * 16 * D; idx += NW * 32) {
+        const int t = idx / (16 * D), row = (idx / D) % 16, d = idx % D;
+        if (!row_valid(t, row)) continue;
+        float M = -INFINITY;
+        for (int w = 0; w < WPT; ++w) M = fmaxf(M, mlbuf[((t * WPT + w) * 16 + row) * 2]);
+        float acc = 0.f, lsum = 0.f;
+        if (M != -INFINITY) {
+            for (int w = 0; w < WPT; ++w) {
+                const int mrow = (t * WPT + w) * 16 + row;
+                const float wgt = fast_exp2(mlbuf[mrow * 2] - M);
+                acc += wgt * mbuf[mrow * D + d];
+                lsum += wgt * mlbuf[mrow * 2 + 1];
+            }
+        }
+        const int32_t rr = prefix_item ? pair_row[t * 16 + row] : row_r;
+        const int32_t hh = prefix_item ? pair_head[t * 16 + row] : g * G + row;
+        const size_t pi = partial_index(p, rr, hh, slot);
+        p.ws_o[pi * D + d] = acc;
+        if (d == 0) *reinterpret_cast<float2 *>(p.ws_ml + pi * 2) = make_float2(M, lsum);
+    }
 }
 
 template <int D>
 static cudaError_t launch_d(const DecodeParams &p, const CUtensorMap &kmap, const CUtensorMap &vmap,
                             cudaStream_t stream)
 {
-    constexpr int NW = kDecodeWarps;
-    constexpr int NWP = kPrefixWarps;
-    cudaError_t err;
-    if (p.plan.n_prefix_ctas > 0) {
-        auto kern = decode_bf16_kernel<D, NWP, NWP>;
-        const int smem = Bf16Smem<D, NWP, NWP>::kLaunchBytes;
-        if ((err = prepare(kern, smem)) != cudaSuccess) return err;
-        prof_begin(PKV_KERNEL_DECODE_PREFIX, stream);
-        kern<<<static_cast<unsigned>(p.plan.n_prefix_ctas), (NWP + 1) * 32, smem, stream>>>(kmap, vmap, p);
-        prof_end(PKV_KERNEL_DECODE_PREFIX, stream);
-        if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    }
-    if (p.plan.n_suffix_ctas > 0) {
-        auto kern = decode_bf16_kernel<D, NW, 1>;
-        const int smem = Bf16Smem<D, NW, 1>::kLaunchBytes;
-        if ((err = prepare(kern, smem)) != cudaSuccess) return err;
-        prof_begin(PKV_KERNEL_DECODE_SPLIT, stream);
-        kern<<<static_cast<unsigned>(p.plan.n_suffix_ctas), (NW + 1) * 32, smem, stream>>>(kmap, vmap, p);
-        prof_end(PKV_KERNEL_DECODE_SPLIT, stream);
-        if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    }
-    return cudaSuccess;
+    const int64_t ctas = p.plan.n_prefix_ctas + p.plan.n_suffix_ctas;
+    if (ctas == 0) return cudaSuccess;
+    auto kern = decode_bf16_kernel<D>;
+    const int smem = Bf16Smem<D>::kLaunchBytes;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return err;
+    prof_begin(PKV_KERNEL_DECODE_SPLIT, stream);
+    err = launch_pdl(kern, dim3(static_cast<unsigned>(ctas)), dim3((kDecodeWarps + 1) * 32), smem,
+                     stream, kmap, vmap, p);
+    prof_end(PKV_KERNEL_DECODE_SPLIT, stream);
+    return err;
 }
 
 cudaError_t launch_decode_bf16(const DecodeParams &p, const CUtensorMap &kmap,

@@ -36,6 +36,8 @@ __global__ void __launch_bounds__(kF32Threads)
 
     const int tid = threadIdx.x;
     const int G = p.group;
+    pdl_wait();
+    pdl_trigger();
     int32_t b0, nblk, slot, g;
     if (!prefix_mode) {
         int64_t bid = blockIdx.x;
@@ -212,15 +214,17 @@ cudaError_t launch_decode_f32(const DecodeParams &p, cudaStream_t stream)
     if (err != cudaSuccess) return err;
     if (p.plan.n_prefix_ctas > 0) {
         prof_begin(PKV_KERNEL_DECODE_PREFIX, stream);
-        decode_f32_kernel<<<static_cast<unsigned>(p.plan.n_prefix_ctas), kF32Threads, smem, stream>>>(p, 1);
+        err = launch_pdl(decode_f32_kernel, dim3(static_cast<unsigned>(p.plan.n_prefix_ctas)),
+                         dim3(kF32Threads), smem, stream, p, 1);
         prof_end(PKV_KERNEL_DECODE_PREFIX, stream);
-        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+        if (err != cudaSuccess) return err;
     }
     if (p.plan.n_suffix_ctas > 0) {
         prof_begin(PKV_KERNEL_DECODE_SPLIT, stream);
-        decode_f32_kernel<<<static_cast<unsigned>(p.plan.n_suffix_ctas), kF32Threads, smem, stream>>>(p, 0);
+        err = launch_pdl(decode_f32_kernel, dim3(static_cast<unsigned>(p.plan.n_suffix_ctas)),
+                         dim3(kF32Threads), smem, stream, p, 0);
         prof_end(PKV_KERNEL_DECODE_SPLIT, stream);
-        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+        if (err != cudaSuccess) return err;
     }
     return cudaSuccess;
 }
@@ -238,9 +242,10 @@ template <>
 __device__ __forceinline__ __nv_bfloat16 to_out<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
 
 template <typename OutT, int D>
-__global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams p)
+__global__ void __launch_bounds__(128, 1) decode_combine_kernel(const DecodeParams p)
 {
     constexpr int PER = D / 32;
+    pdl_wait();  // the partials come from the decode kernel just before
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t idx = static_cast<int64_t>(blockIdx.x) * 4 + warp;
     if (idx >= static_cast<int64_t>(p.batch) * p.hq) return;
@@ -249,10 +254,13 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams 
     const int32_t npre = row_prefix_splits(p, rr);
     const int32_t n = npre + row_suffix_splits(p, rr);
     const size_t base = partial_index(p, r, h, 0);
-    auto slot_of = [&](int32_t k) { return k < npre ? k : p.plan.n_prefix_splits + (k - npre); };
 
+    // weights of every partial: lanes take partials k = lane, lane + 32, ...
     float M = -INFINITY;
-    for (int32_t k = lane; k < n; k += 32) M = fmaxf(M, p.ws_ml[(base + slot_of(k)) * 2]);
+    for (int32_t k = lane; k < n; k += 32) {
+        const int32_t slot = k < npre ? k : p.plan.n_prefix_splits + (k - npre);
+        M = fmaxf(M, p.ws_ml[(base + slot) * 2]);
+    }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
 
@@ -261,19 +269,35 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams 
     for (int j = 0; j < PER; ++j) acc[j] = 0.f;
     float lsum = 0.f;
     if (M != -INFINITY) {
-        for (int32_t k = 0; k < n; ++k) {
-            const size_t pi = base + slot_of(k);
-            const float2 ml = *reinterpret_cast<const float2 *>(p.ws_ml + pi * 2);
-            const float w = fast_exp2(ml.x - M);
-            lsum = fmaf(w, ml.y, lsum);
+        for (int32_t k0 = 0; k0 < n; k0 += 32) {
+            const int32_t k = k0 + lane;
+            int32_t my_slot = 0;
+            float my_w = 0.f;
+            if (k < n) {
+                my_slot = k < npre ? k : p.plan.n_prefix_splits + (k - npre);
+                const float2 ml = *reinterpret_cast<const float2 *>(p.ws_ml + (base + my_slot) * 2);
+                my_w = fast_exp2(ml.x - M);
+                lsum = fmaf(my_w, ml.y, lsum);
+            }
+            const int cnt = min(32, n - k0);
+            // weighted sum of the partials' values; the loads of several
+            // partials are independent, so unrolling keeps them in flight
+#pragma unroll 8
+            for (int j = 0; j < cnt; ++j) {
+                const float w = __shfl_sync(0xffffffffu, my_w, j);
+                const int32_t slot = __shfl_sync(0xffffffffu, my_slot, j);
+                const float *src = p.ws_o + (base + slot) * D + lane;
 #pragma unroll
-            for (int j = 0; j < PER; ++j) acc[j] = fmaf(w, p.ws_o[pi * D + lane + 32 * j], acc[j]);
+                for (int e = 0; e < PER; ++e) acc[e] = fmaf(w, src[32 * e], acc[e]);
+            }
         }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
     }
     const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
     OutT *out = static_cast<OutT *>(p.out) + idx * D;
 #pragma unroll
-    for (int j = 0; j < PER; ++j) out[lane + 32 * j] = to_out<OutT>(acc[j] * inv);
+    for (int e = 0; e < PER; ++e) out[lane + 32 * e] = to_out<OutT>(acc[e] * inv);
 }
 
 template <typename OutT>
@@ -281,17 +305,18 @@ static cudaError_t launch_combine_t(const DecodeParams &p, cudaStream_t stream)
 {
     const int64_t pairs = static_cast<int64_t>(p.batch) * p.hq;
     if (pairs == 0) return cudaSuccess;
-    const unsigned grid = static_cast<unsigned>((pairs + 3) / 4);
+    const dim3 grid(static_cast<unsigned>((pairs + 3) / 4)), block(128);
+    cudaError_t err;
     prof_begin(PKV_KERNEL_DECODE_COMBINE, stream);
     switch (p.head_dim) {
-    case 32: decode_combine_kernel<OutT, 32><<<grid, 128, 0, stream>>>(p); break;
-    case 64: decode_combine_kernel<OutT, 64><<<grid, 128, 0, stream>>>(p); break;
-    case 128: decode_combine_kernel<OutT, 128><<<grid, 128, 0, stream>>>(p); break;
-    case 256: decode_combine_kernel<OutT, 256><<<grid, 128, 0, stream>>>(p); break;
-    default: return cudaErrorInvalidValue;
+    case 32: err = launch_pdl(decode_combine_kernel<OutT, 32>, grid, block, 0, stream, p); break;
+    case 64: err = launch_pdl(decode_combine_kernel<OutT, 64>, grid, block, 0, stream, p); break;
+    case 128: err = launch_pdl(decode_combine_kernel<OutT, 128>, grid, block, 0, stream, p); break;
+    case 256: err = launch_pdl(decode_combine_kernel<OutT, 256>, grid, block, 0, stream, p); break;
+    default: err = cudaErrorInvalidValue; break;
     }
     prof_end(PKV_KERNEL_DECODE_COMBINE, stream);
-    return cudaGetLastError();
+    return err;
 }
 
 cudaError_t launch_decode_combine(const DecodeParams &p, pkv_dtype dtype, cudaStream_t stream)

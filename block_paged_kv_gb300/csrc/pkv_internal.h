@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "pkv.h"
 
 namespace pkv {
@@ -61,6 +63,26 @@ struct DecodeParams {
     DecodePlan plan;
 };
 
+// Launch with programmatic stream serialization (PDL): the kernel may be
+// scheduled while the previous kernel on the stream drains; it calls
+// pdl_wait() before touching global memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args &&...args)
+{
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // Launch bookkeeping (api.cu): every kernel launch is counted; launches of
 // kinds enabled by pkv_profile_enable are bracketed by CUDA events.
 void prof_begin(int kind, cudaStream_t stream);
@@ -77,11 +99,12 @@ cudaError_t launch_decode_f32(const DecodeParams &p, cudaStream_t stream);
 // merge of the split partials into out (dtype of q)
 cudaError_t launch_decode_combine(const DecodeParams &p, pkv_dtype dtype, cudaStream_t stream);
 
-// Consumer warps per decode CTA (plus one producer warp for bf16): a suffix
-// CTA's warps share one 16-row query tile and split its blocks; a prefix CTA's
-// warps each own a tile of (row, head) pairs and all read every block.
+// Consumer warps per decode CTA (plus one producer warp for bf16): a split
+// CTA's warps share one 16-row query tile and take its blocks in turn; a
+// shared-prefix CTA holds several tiles of (row, head) pairs (64 pairs for
+// head_dim <= 128, 32 for 256), each read by NW / tiles warps.
 constexpr int kDecodeWarps = 4;
-constexpr int kPrefixWarps = 8;
+constexpr int kPrefixPairsPerCta = 64;  // head_dim <= 128 (32 for head_dim 256)
 // query rows per CTA of the f32 kernel
 constexpr int kF32Rows = 16;
 
