@@ -28,15 +28,23 @@ struct Bf16Cfg {
     static constexpr int kTok = 16;                       // block_size
     static constexpr int kTileBytes = kTok * D * 2;       // one (block, kv head) tile of K or V
     static constexpr int kStageBytes = 2 * kTileBytes;    // K + V
-    // ring sized so that two CTAs fit on an SM next to their query tiles
-    static constexpr int kRingBytes = (D == 256 ? 80 : 88) * 1024;
+    // query fragments stay in registers for head_dim <= 128; there the query
+    // tiles are staged through the ring before the first load, otherwise they
+    // keep a region of their own
+    static constexpr bool kQInRegs = D <= 128;
+    // ring sized so that two CTAs fit on an SM
+    static constexpr int kRingBytes = (D == 256 ? 64 : 96) * 1024;
     static constexpr int kStages = kRingBytes / kStageBytes;
+    // A stage must always be consumed by the same warp of a tile: with the
+    // warps of a tile taking blocks in turn, a stage count that is not a
+    // multiple of the warps per tile would let one warp run a full ring ahead
+    // of another and wait on an mbarrier phase of the wrong parity.
+    static_assert(kStages % kDecodeWarps == 0, "stages must be a multiple of the warps per tile");
     static constexpr int kRegions = D / 64;               // 64-dim swizzled regions per tile
     static constexpr int kRegionBytes = kTok * 128;
     static constexpr int kQStride = (D + 8) * 2;          // padded query row (bytes)
     static constexpr int kQTileBytes = 16 * kQStride;
     static constexpr int kPrefixTiles = (D == 256 ? kPrefixPairsPerCta / 2 : kPrefixPairsPerCta) / 16;
-    static constexpr bool kQInRegs = D <= 128;
     static constexpr int kNT = D / 8;                     // 8-dim output n-tiles
     static constexpr int kKS = D / 16;                    // 16-dim k-steps of Q K^T
 };
@@ -45,15 +53,18 @@ template <int D>
 struct Bf16Smem {
     using C = Bf16Cfg<D>;
     static constexpr int kStageOff = 0;
-    static constexpr int kQOff = C::kStages * C::kStageBytes;
-    static constexpr int kBarOff = kQOff + C::kPrefixTiles * C::kQTileBytes;
+    static constexpr int kQOff = C::kQInRegs ? 0 : C::kRingBytes;
+    static constexpr int kBarOff =
+        C::kQInRegs ? C::kRingBytes : C::kRingBytes + C::kPrefixTiles * C::kQTileBytes;
     static constexpr int kOkOff = kBarOff + 2 * C::kStages * 8;
     static constexpr int kPairOff = kOkOff + C::kStages * 4;
     static constexpr int kMiscOff = kPairOff + 3 * C::kPrefixTiles * 16 * 4;
     static constexpr int kBytes = kMiscOff + 16;
     static constexpr int kLaunchBytes = kBytes + 1024;  // room to align the base to 1024
-    static_assert(kDecodeWarps * 16 * D * 4 + kDecodeWarps * 16 * 8 <= kQOff + C::kPrefixTiles * C::kQTileBytes,
-                  "the merge buffers fit in the ring and query tiles");
+    static_assert(C::kPrefixTiles * C::kQTileBytes <= C::kRingBytes || !C::kQInRegs,
+                  "query tiles staged through the ring fit in it");
+    static_assert(kDecodeWarps * 16 * D * 4 + kDecodeWarps * 16 * 8 <= kBarOff,
+                  "the merge buffers fit below the barriers");
 };
 
 // Swizzled shared address of the 16-byte chunk holding dims d0..d0+7 of token
@@ -195,7 +206,7 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, D == 256 ? 2 : 1)
                 report(p.status, PKV_DEV_BAD_PREFIX);
         }
     }
-    const int WPT = NW / tiles;  // consumer warps per query tile
+    const int WPT = NW / tiles;  // consumer warps per query tile (divides STAGES)
 
     // ------------------------------------------------- query tiles + barriers
     {
@@ -226,6 +237,25 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, D == 256 ? 2 : 1)
             }
             fence_mbar_init();
         }
+        __syncthreads();
+    }
+
+    // ------------------------------------------- query fragments (consumers)
+    const int tile = warp / WPT;
+    const int sub = warp % WPT;
+    const uint32_t q_tile = smem_u32(q_mem + tile * C::kQTileBytes);
+    const uint32_t q_lane = q_tile + (((lane >> 3) & 1) * 8 + (lane & 7)) * C::kQStride +
+                            (lane >> 4) * 16;
+    uint32_t qf[C::kQInRegs ? C::kKS : 1][4];
+    if constexpr (C::kQInRegs) {
+        if (warp < NW) {
+#pragma unroll
+            for (int kk = 0; kk < C::kKS; ++kk)
+                ldsm_x4(q_lane + kk * 32, qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3]);
+        }
+        // the ring is about to be overwritten by TMA (async proxy) after these
+        // generic-proxy reads and writes of the staged query tiles
+        fence_proxy_async_smem();
         __syncthreads();
     }
 
@@ -275,8 +305,6 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, D == 256 ? 2 : 1)
     }
 
     // ---------------------------------------------------------------- consumers
-    const int tile = warp / WPT;
-    const int sub = warp % WPT;
     const int qd = lane >> 2;        // fragment rows qd and qd + 8
     const int c2 = 2 * (lane & 3);   // fragment columns c2, c2 + 1
     int lo0, hi0, lo1, hi1;
@@ -288,16 +316,6 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, D == 256 ? 2 : 1)
         const int k0 = tile * 16 + qd;
         hi0 = pair_row[k0] >= 0 ? pair_len[k0] : 0;
         hi1 = pair_row[k0 + 8] >= 0 ? pair_len[k0 + 8] : 0;
-    }
-
-    const uint32_t q_tile = smem_u32(q_mem + tile * C::kQTileBytes);
-    const uint32_t q_lane = q_tile + (((lane >> 3) & 1) * 8 + (lane & 7)) * C::kQStride +
-                            (lane >> 4) * 16;
-    uint32_t qf[C::kQInRegs ? C::kKS : 1][4];
-    if constexpr (C::kQInRegs) {
-#pragma unroll
-        for (int kk = 0; kk < C::kKS; ++kk)
-            ldsm_x4(q_lane + kk * 32, qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3]);
     }
 
     float o[C::kNT][4];
@@ -476,6 +494,10 @@ static cudaError_t launch_d(const DecodeParams &p, const CUtensorMap &kmap, cons
     auto kern = decode_bf16_kernel<D>;
     const int smem = Bf16Smem<D>::kLaunchBytes;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return err;
+    // the largest shared-memory carveout, so that two CTAs are resident per SM
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared);
     if (err != cudaSuccess) return err;
     prof_begin(PKV_KERNEL_DECODE_SPLIT, stream);
     err = launch_pdl(kern, dim3(static_cast<unsigned>(ctas)), dim3((kDecodeWarps + 1) * 32), smem,

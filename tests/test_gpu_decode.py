@@ -249,3 +249,23 @@ def test_shared_equals_private_copies(pkv, orc):
     private = _decode(pkv, d2, w)
     assert torch.equal(private, shared_off)  # the same blocks, relabelled
     assert_close(to_f64(shared_on), to_f64(private), "bf16", "read-once prefix vs private copies")
+
+
+@pytest.mark.parametrize("d,hq,hkv", [(64, 8, 2), (128, 32, 8), (256, 8, 1)])
+def test_repeated_calls_stable_across_split_sizes(pkv, d, hq, hkv):
+    # every split size gives a clean status and the same bits call after call
+    # (a pipeline that lets a consumer run a full ring ahead fails this)
+    w = gen.decode_workload(seed=17, dtype="bf16", num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
+                            context_lens=[4000, 1500, 30, 2900])
+    d_ = Dev(w)
+    append(pkv, d_)
+    try:
+        for C in (0, 4, 12, 20, 40, 100, 300):
+            pkv.set_decode_split_blocks(C)
+            ref = _decode(pkv, d_, w)
+            for _ in range(10):
+                out = _decode(pkv, d_, w)
+                assert torch.equal(out, ref), C
+            assert int(d_.status.item()) == 0, C
+    finally:
+        pkv.set_decode_split_blocks(0)
