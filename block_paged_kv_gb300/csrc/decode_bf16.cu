@@ -5,20 +5,25 @@
 //
 // One launch carries two kinds of CTA, one work item each:
 //   prefix item (the first n_prefix_ctas CTAs): group, kv head g, row chunk,
-//       prefix split s -> prefix blocks s*Cp ..; its query tiles hold (row,
-//       head) pairs of the group's rows, so every shared block is read once
-//       for all of them;
+//       prefix split s -> prefix blocks s*Cp ..; its four query tiles hold
+//       (row, head) pairs of the group's rows, so every shared block is read
+//       once for all of them;
 //   split item: row r, kv head g, split s -> blocks b_first + s*C .. ; its one
 //       16-row query tile holds the G q heads of (r, g).
-// A producer warp streams (block, kv head) K and V tiles with TMA tensor loads
-// (4-D maps over [block][kv head][slot][dim], 64-dim boxes, 128-byte swizzle)
-// into a ring of STAGES shared-memory slots guarded by mbarriers.  Consumer
-// warps compute S = Q K^T and O += P V with mma.sync m16n8k16 (bf16 in, fp32
+// K and V (block, kv head) tiles are brought into shared memory with TMA tensor
+// loads (4-D maps over [block][kv head][slot][dim], 64-dim boxes, 128-byte
+// swizzle) that complete on mbarriers.
+//   split item: each of the four warps takes every fourth block of the run and
+//       keeps its own ring of stages: it issues the loads of its next blocks
+//       itself as it frees a stage, so no warp ever waits behind another;
+//   prefix item: the four warps share one ring (each owns a query tile and
+//       reads every block); warp 0 refills a stage once all four released it.
+// Warps compute S = Q K^T and O += P V with mma.sync m16n8k16 (bf16 in, fp32
 // accumulate): M = 16 query rows, N = 8 tokens or 8 dims.  The online softmax
 // runs on the accumulator fragments with quad shuffles; P enters the P.V
-// product as two bf16 terms (hi + lo) so that its rounding stays far below
-// the output's own bf16 rounding.  Each tile's
-// partial (max in log2 units, sum, unnormalised O) goes to the workspace.
+// product as two bf16 terms (hi + lo) so that its rounding stays far below the
+// output's own bf16 rounding.  Each tile's partial (max in log2 units, sum,
+// unnormalised O) goes to the workspace.
 #include "decode_common.cuh"
 
 namespace pkv {
@@ -32,19 +37,16 @@ struct Bf16Cfg {
     // tiles are staged through the ring before the first load, otherwise they
     // keep a region of their own
     static constexpr bool kQInRegs = D <= 128;
+    static constexpr int kTiles = 4;                      // query tiles of a prefix item
     // ring sized so that two CTAs fit on an SM
     static constexpr int kRingBytes = (D == 256 ? 64 : 96) * 1024;
     static constexpr int kStages = kRingBytes / kStageBytes;
-    // A stage must always be consumed by the same warp of a tile: with the
-    // warps of a tile taking blocks in turn, a stage count that is not a
-    // multiple of the warps per tile would let one warp run a full ring ahead
-    // of another and wait on an mbarrier phase of the wrong parity.
-    static_assert(kStages % kDecodeWarps == 0, "stages must be a multiple of the warps per tile");
+    static constexpr int kStagesPerWarp = kStages / kDecodeWarps;  // split items
+    static_assert(kStages % kDecodeWarps == 0, "split items give each warp the same stages");
     static constexpr int kRegions = D / 64;               // 64-dim swizzled regions per tile
     static constexpr int kRegionBytes = kTok * 128;
     static constexpr int kQStride = (D + 8) * 2;          // padded query row (bytes)
     static constexpr int kQTileBytes = 16 * kQStride;
-    static constexpr int kPrefixTiles = (D == 256 ? kPrefixPairsPerCta / 2 : kPrefixPairsPerCta) / 16;
     static constexpr int kNT = D / 8;                     // 8-dim output n-tiles
     static constexpr int kKS = D / 16;                    // 16-dim k-steps of Q K^T
 };
@@ -55,13 +57,13 @@ struct Bf16Smem {
     static constexpr int kStageOff = 0;
     static constexpr int kQOff = C::kQInRegs ? 0 : C::kRingBytes;
     static constexpr int kBarOff =
-        C::kQInRegs ? C::kRingBytes : C::kRingBytes + C::kPrefixTiles * C::kQTileBytes;
+        C::kQInRegs ? C::kRingBytes : C::kRingBytes + C::kTiles * C::kQTileBytes;
     static constexpr int kOkOff = kBarOff + 2 * C::kStages * 8;
     static constexpr int kPairOff = kOkOff + C::kStages * 4;
-    static constexpr int kMiscOff = kPairOff + 3 * C::kPrefixTiles * 16 * 4;
+    static constexpr int kMiscOff = kPairOff + 3 * C::kTiles * 16 * 4;
     static constexpr int kBytes = kMiscOff + 16;
     static constexpr int kLaunchBytes = kBytes + 1024;  // room to align the base to 1024
-    static_assert(C::kPrefixTiles * C::kQTileBytes <= C::kRingBytes || !C::kQInRegs,
+    static_assert(C::kTiles * C::kQTileBytes <= C::kRingBytes || !C::kQInRegs,
                   "query tiles staged through the ring fit in it");
     static_assert(kDecodeWarps * 16 * D * 4 + kDecodeWarps * 16 * 8 <= kBarOff,
                   "the merge buffers fit below the barriers");
@@ -76,13 +78,42 @@ __device__ __forceinline__ uint32_t kv_chunk_addr(uint32_t tile, int tok, int d0
            ((((d0 & 63) >> 3) ^ (tok & 7)) << 4);
 }
 
-__device__ __forceinline__ void consumer_bar_sync(int nthreads)
-{
-    asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
-}
+// Block ids of a strided run, fetched 32 at a time ahead of use: index j of
+// the run is row[first + stride * j].  All lanes call next() with the same,
+// increasing j; the id comes back on every lane.
+struct BlockIds {
+    const int32_t *row;
+    int32_t first, stride, n, batch_no;
+    int32_t cur, nxt;
+    __device__ __forceinline__ int32_t fetch(int32_t j, int lane) const
+    {
+        const int32_t k = j + lane;
+        return k < n ? __ldg(row + first + stride * k) : -1;
+    }
+    __device__ __forceinline__ void init(const int32_t *r, int32_t f, int32_t s, int32_t count,
+                                         int lane)
+    {
+        row = r;
+        first = f;
+        stride = s;
+        n = count;
+        batch_no = 0;
+        cur = fetch(0, lane);
+        nxt = fetch(32, lane);
+    }
+    __device__ __forceinline__ int32_t next(int32_t j, int lane)
+    {
+        if ((j >> 5) != batch_no) {
+            cur = nxt;
+            ++batch_no;
+            nxt = fetch((batch_no + 1) * 32, lane);
+        }
+        return __shfl_sync(0xffffffffu, cur, j & 31);
+    }
+};
 
 template <int D>
-__global__ void __launch_bounds__((kDecodeWarps + 1) * 32, D == 256 ? 2 : 1)
+__global__ void __launch_bounds__(kDecodeWarps * 32, 2)
     decode_bf16_kernel(const __grid_constant__ CUtensorMap kmap,
                        const __grid_constant__ CUtensorMap vmap, const DecodeParams p)
 {
@@ -90,6 +121,7 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, D == 256 ? 2 : 1)
     using SM = Bf16Smem<D>;
     constexpr int NW = kDecodeWarps;
     constexpr int STAGES = C::kStages;
+    constexpr int SPW = C::kStagesPerWarp;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -100,8 +132,8 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, D == 256 ? 2 : 1)
     uint64_t *empty = full + STAGES;
     int32_t *stage_ok = reinterpret_cast<int32_t *>(smem + SM::kOkOff);
     int32_t *pair_row = reinterpret_cast<int32_t *>(smem + SM::kPairOff);
-    int32_t *pair_head = pair_row + C::kPrefixTiles * 16;
-    int32_t *pair_len = pair_head + C::kPrefixTiles * 16;
+    int32_t *pair_head = pair_row + C::kTiles * 16;
+    int32_t *pair_len = pair_head + C::kTiles * 16;
     int32_t *misc = reinterpret_cast<int32_t *>(smem + SM::kMiscOff);
 
     const int warp = threadIdx.x >> 5;
@@ -109,7 +141,7 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, D == 256 ? 2 : 1)
     const int G = p.group;
     const int bs = C::kTok;
 
-    if (warp == NW && lane == 0) {
+    if (threadIdx.x == 0) {
         tma_prefetch_desc(&kmap);
         tma_prefetch_desc(&vmap);
     }
@@ -137,7 +169,7 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, D == 256 ? 2 : 1)
         hi_all = rr.L;
         tiles = 1;
     } else {
-        tiles = C::kPrefixTiles;
+        tiles = C::kTiles;
         int64_t bid = blockIdx.x;
         const int32_t s = static_cast<int32_t>(bid % p.plan.n_prefix_splits);
         bid /= p.plan.n_prefix_splits;
@@ -206,7 +238,6 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, D == 256 ? 2 : 1)
                 report(p.status, PKV_DEV_BAD_PREFIX);
         }
     }
-    const int WPT = NW / tiles;  // consumer warps per query tile (divides STAGES)
 
     // ------------------------------------------------- query tiles + barriers
     {
@@ -233,78 +264,68 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, D == 256 ? 2 : 1)
         if (threadIdx.x == 0) {
             for (int s = 0; s < STAGES; ++s) {
                 mbar_init(&full[s], 1);
-                mbar_init(&empty[s], tiles);
+                mbar_init(&empty[s], NW);  // prefix items: every warp releases every stage
             }
             fence_mbar_init();
         }
         __syncthreads();
     }
 
-    // ------------------------------------------- query fragments (consumers)
-    const int tile = warp / WPT;
-    const int sub = warp % WPT;
-    const uint32_t q_tile = smem_u32(q_mem + tile * C::kQTileBytes);
-    const uint32_t q_lane = q_tile + (((lane >> 3) & 1) * 8 + (lane & 7)) * C::kQStride +
-                            (lane >> 4) * 16;
+    // a split item's warps all read query tile 0; a prefix item's warp w owns
+    // tile w
+    const int tile = prefix_item ? warp : 0;
+    const uint32_t q_lane = smem_u32(q_mem + tile * C::kQTileBytes) +
+                            (((lane >> 3) & 1) * 8 + (lane & 7)) * C::kQStride + (lane >> 4) * 16;
     uint32_t qf[C::kQInRegs ? C::kKS : 1][4];
     if constexpr (C::kQInRegs) {
-        if (warp < NW) {
 #pragma unroll
-            for (int kk = 0; kk < C::kKS; ++kk)
-                ldsm_x4(q_lane + kk * 32, qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3]);
-        }
+        for (int kk = 0; kk < C::kKS; ++kk)
+            ldsm_x4(q_lane + kk * 32, qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3]);
         // the ring is about to be overwritten by TMA (async proxy) after these
         // generic-proxy reads and writes of the staged query tiles
         fence_proxy_async_smem();
         __syncthreads();
     }
 
-    // ---------------------------------------------------------------- producer
-    if (warp == NW) {
-        const uint64_t policy = l2_evict_first_policy();
-        bool abort = false;
-        for (int base = 0; base < nblk && !abort; base += 32) {
-            int32_t blk = -1;
-            if (base + lane < nblk)
-                blk = __ldg(p.tables + static_cast<int64_t>(tab_row) * p.width + b0 + base + lane);
-            const int cnt = min(32, nblk - base);
-            for (int j = 0; j < cnt; ++j) {
-                const int32_t bj = __shfl_sync(0xffffffffu, blk, j);
-                if (lane == 0) {
-                    const int i = base + j;
-                    const int st = i % STAGES;
-                    if (i >= STAGES && !mbar_wait(&empty[st], ((i / STAGES) + 1) & 1)) {
-                        report(p.status, PKV_DEV_TIMEOUT);
-                        abort = true;
-                    }
-                    if (!abort) {
-                        const bool ok = static_cast<uint32_t>(bj) < static_cast<uint32_t>(p.num_blocks);
-                        stage_ok[st] = ok ? 1 : 0;
-                        if (ok) {
-                            mbar_arrive_expect_tx(&full[st], C::kStageBytes);
-                            uint8_t *kdst = stage_mem + st * C::kStageBytes;
-                            uint8_t *vdst = kdst + C::kTileBytes;
+    // ------------------------------------------------------------- loads
+    // split item: warp w's blocks are b0 + w + NW*k (k = 0 .. nk-1); its use k
+    // goes to stage w*SPW + k % SPW.  prefix item: block k to stage k % STAGES,
+    // loads issued by warp 0.
+    const uint64_t policy = l2_evict_first_policy();
+    const int32_t *table_row = p.tables + static_cast<int64_t>(tab_row) * p.width + b0;
+    const int32_t nk = prefix_item ? nblk : (nblk > warp ? (nblk - warp + NW - 1) / NW : 0);
+    const bool issuer = !prefix_item || warp == 0;
+    BlockIds ids;
+    if (issuer) ids.init(table_row, prefix_item ? 0 : warp, prefix_item ? 1 : NW, nk, lane);
+    auto stage_of = [&](int32_t k) { return prefix_item ? k % STAGES : warp * SPW + k % SPW; };
+    auto issue = [&](int32_t k) {  // whole warp; lane 0 issues
+        const int32_t bj = ids.next(k, lane);
+        if (lane == 0) {
+            const int st = stage_of(k);
+            const bool ok = static_cast<uint32_t>(bj) < static_cast<uint32_t>(p.num_blocks);
+            stage_ok[st] = ok ? 1 : 0;
+            if (ok) {
+                mbar_arrive_expect_tx(&full[st], C::kStageBytes);
+                uint8_t *kdst = stage_mem + st * C::kStageBytes;
+                uint8_t *vdst = kdst + C::kTileBytes;
 #pragma unroll
-                            for (int reg = 0; reg < C::kRegions; ++reg) {
-                                tma_load_4d(kdst + reg * C::kRegionBytes, &kmap, &full[st], reg * 64,
-                                            0, g, bj, policy);
-                                tma_load_4d(vdst + reg * C::kRegionBytes, &vmap, &full[st], reg * 64,
-                                            0, g, bj, policy);
-                            }
-                        } else {
-                            report(p.status, PKV_DEV_BAD_BLOCK);
-                            mbar_arrive(&full[st]);
-                        }
-                    }
+                for (int reg = 0; reg < C::kRegions; ++reg) {
+                    tma_load_4d(kdst + reg * C::kRegionBytes, &kmap, &full[st], reg * 64, 0, g, bj,
+                                policy);
+                    tma_load_4d(vdst + reg * C::kRegionBytes, &vmap, &full[st], reg * 64, 0, g, bj,
+                                policy);
                 }
-                abort = __shfl_sync(0xffffffffu, abort, 0);
-                if (abort) break;
+            } else {
+                report(p.status, PKV_DEV_BAD_BLOCK);
+                mbar_arrive(&full[st]);
             }
         }
-        return;
-    }
+    };
+    const int32_t depth = prefix_item ? STAGES : SPW;
+    if (issuer)
+        for (int32_t k = 0; k < min(depth, nk); ++k) issue(k);
 
-    // ---------------------------------------------------------------- consumers
+    // ---------------------------------------------------------------- compute
     const int qd = lane >> 2;        // fragment rows qd and qd + 8
     const int c2 = 2 * (lane & 3);   // fragment columns c2, c2 + 1
     int lo0, hi0, lo1, hi1;
@@ -329,9 +350,10 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, D == 256 ? 2 : 1)
     const int v_tok = ((lane >> 3) & 1) * 8 + (lane & 7);
     const int v_dof = (lane >> 4) * 8;
 
-    for (int i = sub; i < nblk; i += WPT) {
-        const int st = i % STAGES;
-        const bool got = mbar_wait(&full[st], (i / STAGES) & 1);
+    for (int32_t k = 0; k < nk; ++k) {
+        const int st = stage_of(k);
+        const int32_t use = prefix_item ? k / STAGES : k / SPW;
+        const bool got = mbar_wait(&full[st], use & 1);
         if (__any_sync(0xffffffffu, !got)) {
             if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
             break;
@@ -339,7 +361,7 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, D == 256 ? 2 : 1)
         const bool ok = stage_ok[st] != 0;
         const uint32_t kt = smem_u32(stage_mem + st * C::kStageBytes);
         const uint32_t vt = kt + C::kTileBytes;
-        const int base_tok = (b0 + i) * bs;
+        const int base_tok = (b0 + (prefix_item ? k : warp + NW * k)) * bs;
 
         // S = Q K^T  (16 rows x 16 tokens)
         float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -431,8 +453,26 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, D == 256 ? 2 : 1)
                 mma_16816(o[2 * np + 1], pl, v2, v3);
             }
         }
+
+        // release the stage: its generic-proxy reads come before the next
+        // TMA write into it
+        fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[st]);
+        if (!prefix_item) {
+            if (k + SPW < nk) issue(k + SPW);
+        } else {
+            if (lane == 0) mbar_arrive(&empty[st]);
+            if (warp == 0 && k + STAGES < nk) {
+                // every warp has released this stage before it is refilled
+                bool freed = true;
+                if (lane == 0) freed = mbar_wait(&empty[st], use & 1);
+                if (!__shfl_sync(0xffffffffu, freed, 0)) {
+                    if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
+                } else {
+                    issue(k + STAGES);
+                }
+            }
+        }
     }
 
     // row sums: the quad's four partial sums
@@ -441,45 +481,60 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32, D == 256 ? 2 : 1)
     l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
 
-    // merge the WPT warps of each tile through shared memory (the ring and
-    // query tiles are free once every consumer is past its last block)
-    float *mbuf = reinterpret_cast<float *>(stage_mem);         // [NW * 16][D]
-    float *mlbuf = mbuf + NW * 16 * D;                           // [NW * 16][2]
-    auto row_valid = [&](int t, int row) {
-        return prefix_item ? pair_row[t * 16 + row] >= 0 : row < G;
-    };
-    consumer_bar_sync(NW * 32);
+    if (prefix_item) {
+        // each warp owns its tile: write its rows directly
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const int k = tile * 16 + qd + half * 8;
+            const int32_t pr = pair_row[k];
+            if (pr < 0) continue;
+            const size_t pi = partial_index(p, pr, pair_head[k], slot);
+            float *dst = p.ws_o + pi * D;
+#pragma unroll
+            for (int nt = 0; nt < C::kNT; ++nt)
+                *reinterpret_cast<float2 *>(dst + nt * 8 + c2) =
+                    make_float2(o[nt][2 * half], o[nt][2 * half + 1]);
+            if ((lane & 3) == 0)
+                *reinterpret_cast<float2 *>(p.ws_ml + pi * 2) =
+                    make_float2(half ? m1 : m0, half ? l1 : l0);
+        }
+        return;
+    }
+
+    // split item: merge the four warps' partials of the one tile through
+    // shared memory (the ring is free once every warp is past its last block)
+    float *mbuf = reinterpret_cast<float *>(stage_mem);  // [NW][G][D]
+    float *mlbuf = mbuf + NW * 16 * D;                    // [NW][G][2]
+    __syncthreads();
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
         const int row = qd + half * 8;
-        if (!row_valid(tile, row)) continue;
-        const int mrow = warp * 16 + row;  // warp = tile * WPT + sub
-        float *dst = mbuf + mrow * D;
+        if (row >= G) continue;
+        float *dst = mbuf + (warp * G + row) * D;
 #pragma unroll
         for (int nt = 0; nt < C::kNT; ++nt)
             *reinterpret_cast<float2 *>(dst + nt * 8 + c2) =
                 make_float2(o[nt][2 * half], o[nt][2 * half + 1]);
         if ((lane & 3) == 0)
-            *reinterpret_cast<float2 *>(mlbuf + mrow * 2) = make_float2(half ? m1 : m0, half ? l1 : l0);
+            *reinterpret_cast<float2 *>(mlbuf + (warp * G + row) * 2) =
+                make_float2(half ? m1 : m0, half ? l1 : l0);
     }
-    consumer_bar_sync(NW * 32);
-    for (int idx = threadIdx.x; idx < tiles * 16 * D; idx += NW * 32) {
-        const int t = idx / (16 * D), row = (idx / D) % 16, d = idx % D;
-        if (!row_valid(t, row)) continue;
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < G * D; idx += NW * 32) {
+        const int row = idx / D, d = idx % D;
         float M = -INFINITY;
-        for (int w = 0; w < WPT; ++w) M = fmaxf(M, mlbuf[((t * WPT + w) * 16 + row) * 2]);
+#pragma unroll
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, mlbuf[(w * G + row) * 2]);
         float acc = 0.f, lsum = 0.f;
         if (M != -INFINITY) {
-            for (int w = 0; w < WPT; ++w) {
-                const int mrow = (t * WPT + w) * 16 + row;
-                const float wgt = fast_exp2(mlbuf[mrow * 2] - M);
-                acc += wgt * mbuf[mrow * D + d];
-                lsum += wgt * mlbuf[mrow * 2 + 1];
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                const float wgt = fast_exp2(mlbuf[(w * G + row) * 2] - M);
+                acc += wgt * mbuf[(w * G + row) * D + d];
+                lsum += wgt * mlbuf[(w * G + row) * 2 + 1];
             }
         }
-        const int32_t rr = prefix_item ? pair_row[t * 16 + row] : row_r;
-        const int32_t hh = prefix_item ? pair_head[t * 16 + row] : g * G + row;
-        const size_t pi = partial_index(p, rr, hh, slot);
+        const size_t pi = partial_index(p, row_r, g * G + row, slot);
         p.ws_o[pi * D + d] = acc;
         if (d == 0) *reinterpret_cast<float2 *>(p.ws_ml + pi * 2) = make_float2(M, lsum);
     }
@@ -500,7 +555,7 @@ static cudaError_t launch_d(const DecodeParams &p, const CUtensorMap &kmap, cons
                                cudaSharedmemCarveoutMaxShared);
     if (err != cudaSuccess) return err;
     prof_begin(PKV_KERNEL_DECODE_SPLIT, stream);
-    err = launch_pdl(kern, dim3(static_cast<unsigned>(ctas)), dim3((kDecodeWarps + 1) * 32), smem,
+    err = launch_pdl(kern, dim3(static_cast<unsigned>(ctas)), dim3(kDecodeWarps * 32), smem,
                      stream, kmap, vmap, p);
     prof_end(PKV_KERNEL_DECODE_SPLIT, stream);
     return err;
