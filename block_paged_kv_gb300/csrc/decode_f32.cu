@@ -245,22 +245,30 @@ template <typename OutT, int D>
 __global__ void __launch_bounds__(128, 1) decode_combine_kernel(const DecodeParams p)
 {
     constexpr int PER = D / 32;
-    pdl_wait();  // the partials come from the decode kernel just before
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t idx = static_cast<int64_t>(blockIdx.x) * 4 + warp;
-    if (idx >= static_cast<int64_t>(p.batch) * p.hq) return;
-    const int32_t r = static_cast<int32_t>(idx / p.hq), h = static_cast<int32_t>(idx % p.hq);
-    const RowRange rr = row_range(p, r, false);
-    const int32_t npre = row_prefix_splits(p, rr);
-    const int32_t n = npre + row_suffix_splits(p, rr);
-    const size_t base = partial_index(p, r, h, 0);
-
-    // weights of every partial: lanes take partials k = lane, lane + 32, ...
-    float M = -INFINITY;
-    for (int32_t k = lane; k < n; k += 32) {
-        const int32_t slot = k < npre ? k : p.plan.n_prefix_splits + (k - npre);
-        M = fmaxf(M, p.ws_ml[(base + slot) * 2]);
+    const bool live = idx < static_cast<int64_t>(p.batch) * p.hq;
+    // The row bookkeeping reads only call inputs: the decode kernel released
+    // this grid after its own wait on earlier work, so they are final already.
+    int32_t r = 0, h = 0, npre = 0, n = 0;
+    if (live) {
+        r = static_cast<int32_t>(idx / p.hq);
+        h = static_cast<int32_t>(idx % p.hq);
+        const RowRange rr = row_range(p, r, false);
+        npre = row_prefix_splits(p, rr);
+        n = npre + row_suffix_splits(p, rr);
     }
+    pdl_wait();  // the partials come from the decode kernel just before
+    if (!live) return;
+    const size_t base = partial_index(p, r, h, 0);
+    auto slot_of = [&](int32_t k) { return k < npre ? k : p.plan.n_prefix_splits + (k - npre); };
+
+    // lane k holds partial k's (max, sum) for the first 32 partials
+    float2 ml0 = make_float2(-INFINITY, 0.f);
+    if (lane < n) ml0 = *reinterpret_cast<const float2 *>(p.ws_ml + (base + slot_of(lane)) * 2);
+    float M = ml0.x;
+    for (int32_t k = 32 + lane; k < n; k += 32)
+        M = fmaxf(M, p.ws_ml[(base + slot_of(k)) * 2]);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
 
@@ -270,15 +278,15 @@ __global__ void __launch_bounds__(128, 1) decode_combine_kernel(const DecodePara
     float lsum = 0.f;
     if (M != -INFINITY) {
         for (int32_t k0 = 0; k0 < n; k0 += 32) {
-            const int32_t k = k0 + lane;
-            int32_t my_slot = 0;
-            float my_w = 0.f;
-            if (k < n) {
-                my_slot = k < npre ? k : p.plan.n_prefix_splits + (k - npre);
-                const float2 ml = *reinterpret_cast<const float2 *>(p.ws_ml + (base + my_slot) * 2);
-                my_w = fast_exp2(ml.x - M);
-                lsum = fmaf(my_w, ml.y, lsum);
+            float2 ml = ml0;
+            if (k0 > 0) {
+                ml = make_float2(-INFINITY, 0.f);
+                if (k0 + lane < n)
+                    ml = *reinterpret_cast<const float2 *>(p.ws_ml + (base + slot_of(k0 + lane)) * 2);
             }
+            const float my_w = fast_exp2(ml.x - M);  // 0 for absent partials
+            lsum = fmaf(my_w, ml.y, lsum);
+            const int32_t my_slot = k0 + lane < n ? slot_of(k0 + lane) : 0;
             const int cnt = min(32, n - k0);
             // weighted sum of the partials' values; the loads of several
             // partials are independent, so unrolling keeps them in flight
