@@ -12,16 +12,6 @@
 #include "pkv.h"
 #include "pkv_internal.h"
 
-namespace pkv {
-size_t f32_smem_bytes(int D, int bs);
-cudaError_t launch_prefill(const void *q, const int32_t *cu_q_lens, int32_t hq, const pkv_pool &pool,
-                           const int32_t *tables, int32_t width, const int32_t *seq_lens,
-                           int32_t batch, int32_t max_q_len, int32_t max_len, int32_t window,
-                           float scale, void *out, void *ws, size_t ws_bytes, int32_t *status,
-                           cudaStream_t stream, int *unsupported);
-size_t prefill_workspace_bytes(int32_t batch, int32_t hq, int32_t hkv, int32_t D, int32_t bs,
-                               int32_t max_q_len, int32_t max_len, int32_t window, pkv_dtype dtype);
-}  // namespace pkv
 
 using namespace pkv;
 
@@ -424,11 +414,9 @@ size_t paged_prefill_workspace_size(int32_t batch, int32_t num_q_heads, int32_t 
                                     int32_t head_dim, int32_t block_size, int32_t max_q_len,
                                     int32_t max_seq_len, int32_t window)
 {
-    if (batch < 0 || num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads != 0 ||
-        head_dim <= 0 || block_size <= 0 || max_q_len < 0 || max_seq_len < 0 || window < 0)
-        return 0;
-    return prefill_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim, block_size,
-                                   max_q_len, max_seq_len, window, PKV_BF16);
+    (void)batch; (void)num_q_heads; (void)num_kv_heads; (void)head_dim; (void)block_size;
+    (void)max_q_len; (void)max_seq_len; (void)window;
+    return 0;  // the prefill kernels need no scratch: no split of the key range
 }
 
 pkv_status paged_prefill_chunk_attention(const void *q, const int32_t *cu_q_lens,
@@ -439,6 +427,8 @@ pkv_status paged_prefill_chunk_attention(const void *q, const int32_t *cu_q_lens
                                          void *out, void *workspace, size_t ws_bytes,
                                          int32_t *dev_status, pkv_stream_t stream)
 {
+    (void)workspace;
+    (void)ws_bytes;
     if (!valid_pool(pool) || batch < 0 || num_q_heads <= 0 || max_q_len < 0 || max_seq_len < 0 ||
         window < 0 || !std::isfinite(scale))
         return PKV_ERR_INVALID_ARG;
@@ -447,17 +437,45 @@ pkv_status paged_prefill_chunk_attention(const void *q, const int32_t *cu_q_lens
     if (q == nullptr || out == nullptr || cu_q_lens == nullptr || block_tables == nullptr ||
         seq_lens == nullptr || max_blocks_per_seq <= 0 || !aligned16(q) || !aligned16(out))
         return PKV_ERR_INVALID_ARG;
+    const int32_t G = num_q_heads / pool->num_kv_heads;
+    if (!prefill_shape_built(pool->dtype, pool->head_dim, pool->block_size, G))
+        return PKV_ERR_UNSUPPORTED;
     const int64_t cap = static_cast<int64_t>(max_blocks_per_seq) * pool->block_size;
-    const int32_t max_len = static_cast<int32_t>(std::min<int64_t>(max_seq_len, cap));
-    if (workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
-        return PKV_ERR_WORKSPACE;
-    int unsupported = 0;
-    const cudaError_t err = launch_prefill(q, cu_q_lens, num_q_heads, *pool, block_tables,
-                                           max_blocks_per_seq, seq_lens, batch, max_q_len, max_len,
-                                           window, scale, out, workspace, ws_bytes, dev_status,
-                                           reinterpret_cast<cudaStream_t>(stream), &unsupported);
-    if (unsupported == 1) return PKV_ERR_UNSUPPORTED;
-    if (unsupported == 2) return PKV_ERR_WORKSPACE;
+    PrefillParams p{};
+    p.q = q;
+    p.out = out;
+    p.k_pool = pool->k;
+    p.v_pool = pool->v;
+    p.cu_q_lens = cu_q_lens;
+    p.tables = block_tables;
+    p.seq_lens = seq_lens;
+    p.status = dev_status;
+    p.batch = batch;
+    p.hq = num_q_heads;
+    p.hkv = pool->num_kv_heads;
+    p.group = G;
+    p.head_dim = pool->head_dim;
+    p.block_size = pool->block_size;
+    p.width = max_blocks_per_seq;
+    p.num_blocks = pool->num_blocks;
+    p.max_len = static_cast<int32_t>(std::min<int64_t>(max_seq_len, cap));
+    p.max_q_len = max_q_len;
+    p.window = window;
+    const int32_t qpt = prefill_queries_per_cta(pool->dtype, G);
+    p.q_tiles = static_cast<int32_t>(ceil_div64(max_q_len, qpt));
+    p.scale_log2 = scale * 1.4426950408889634f;
+    if (static_cast<int64_t>(batch) * p.hkv * p.q_tiles > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t err;
+    if (pool->dtype == PKV_BF16) {
+        if (!encode_fn_ready()) return PKV_ERR_CUDA;
+        CUtensorMap kmap, vmap;
+        if (!encode_pool_map(&kmap, pool->k, *pool) || !encode_pool_map(&vmap, pool->v, *pool))
+            return PKV_ERR_UNSUPPORTED;
+        err = launch_prefill_bf16(p, kmap, vmap, st);
+    } else {
+        err = launch_prefill_f32(p, st);
+    }
     return err == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

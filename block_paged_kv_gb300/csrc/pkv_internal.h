@@ -88,7 +88,29 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 void prof_begin(int kind, cudaStream_t stream);
 void prof_end(int kind, cudaStream_t stream);
 
+struct PrefillParams {
+    const void *q;
+    void *out;
+    const void *k_pool;  // used by the f32 kernel; the bf16 kernel reads via TMA
+    const void *v_pool;
+    const int32_t *cu_q_lens;
+    const int32_t *tables;
+    const int32_t *seq_lens;
+    int32_t *status;
+    int32_t batch, hq, hkv, group, head_dim, block_size, width, num_blocks;
+    int32_t max_len;    // min(max_seq_len, width * block_size)
+    int32_t max_q_len;
+    int32_t window;
+    int32_t q_tiles;    // CTAs per (row, kv head): ceil(max_q_len / queries per CTA)
+    float scale_log2;
+};
+
 cudaError_t launch_append(const AppendParams &p, cudaStream_t stream);
+bool prefill_shape_built(pkv_dtype dtype, int32_t D, int32_t bs, int32_t G);
+int32_t prefill_queries_per_cta(pkv_dtype dtype, int32_t G);
+cudaError_t launch_prefill_bf16(const PrefillParams &p, const CUtensorMap &kmap,
+                                const CUtensorMap &vmap, cudaStream_t stream);
+cudaError_t launch_prefill_f32(const PrefillParams &p, cudaStream_t stream);
 
 // bf16 pools: TMA + mbarrier pipeline, mma.sync tiles.  kmap/vmap: 4-D tensor
 // maps (head_dim, block_size, kv head, block) with 64-element boxes, 128B swizzle.

@@ -1,22 +1,557 @@
-// Chunked prefill against a paged prefix (placeholder until the tensor-core
-// kernel lands): reports every shape as not built.
-#include "pkv_internal.h"
+// Chunked prefill against a paged prefix ("perf.md", gather_kv_for_prefill_chunk:
+// a prefill chunk attends its cached prefix through the pages; "paged-cache.md":
+// chunk boundaries change the reduction order, not the result).  Query i of a
+// row's chunk sits at absolute position p = L - C + i and attends positions
+// max(0, p - W + 1) .. p: the whole prefix and the chunk causally.
+//
+// bf16 kernel, one CTA per (row, kv head, tile of 128/G queries).  The tile's
+// 128 M-rows are (query, head) pairs: all G q heads of the kv head, so each
+// K/V tile is loaded once for the whole GQA group.  QK^T and PV are dense
+// contractions and run on the 5th-generation tensor cores:
+//   warp 0    TMA producer: K and V tiles of 128 keys (8 paged blocks, 16
+//             tensor loads each) into a 2-stage ring;
+//   warp 1    allocates tensor memory and issues tcgen05.mma from one thread:
+//             S_j = Q K_j^T into a double-buffered S in tensor memory, then
+//             O += P_j V_j with P read from tensor memory (V MN-major);
+//   warps 2-5 softmax, one thread per M-row: S row from tensor memory, causal /
+//             window / range mask, running max kept within 2^8 of the true
+//             maximum (O in tensor memory is rescaled only when it moves
+//             further), P written back over S as bf16 hi + lo terms (the P.V
+//             product then carries P to ~2^-17 relative), and the epilogue
+//             O / l to global memory.
+// f32 kernel: CUDA cores, the same work split with 16 (query, head) pairs per
+// CTA, for the fp32 pools.
+#include "decode_common.cuh"
+#include "tcgen05.cuh"
 
 namespace pkv {
 
-size_t prefill_workspace_bytes(int32_t, int32_t, int32_t, int32_t, int32_t, int32_t, int32_t,
-                               int32_t, pkv_dtype)
+namespace pf {
+constexpr int kD = 128;
+constexpr int kRows = 128;                // M
+constexpr int kKeys = 128;                // keys per tile (8 blocks of 16)
+constexpr int kQBytes = 2 * kRows * 128;  // two 64-dim swizzled regions
+constexpr int kKVRegion = kKeys * 128;    // 16 KiB
+constexpr int kTileBytes = 2 * kKVRegion; // 32 KiB: K or V tile
+constexpr int kStageBytes = 2 * kTileBytes;
+constexpr int kStages = 2;
+constexpr int kQOff = 0;
+constexpr int kStageOff = kQOff + kQBytes;
+constexpr int kBarOff = kStageOff + kStages * kStageBytes;
+// barriers: kv_full[2], kv_empty[2], s_full[2], p_full[2], pv_done[2]
+constexpr int kMaskOff = kBarOff + 10 * 8;
+constexpr int kTmemOff = kMaskOff + kStages * 4;
+constexpr int kBytes = kTmemOff + 16;
+constexpr int kLaunchBytes = kBytes + 1024;
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;       // S0, S1, O (+ spare)
+constexpr uint32_t kRescaleLog2 = 8;      // O is rescaled only when the max grows past 2^8
+}  // namespace pf
+
+struct PrefillRowInfo {
+    int32_t r, g, i0, nq, L, C, kv_lo, kv_hi;
+};
+
+__device__ __forceinline__ bool prefill_item(const PrefillParams &p, int64_t bid, int qpt,
+                                             PrefillRowInfo &w)
 {
-    return 256;
+    const int32_t qt = static_cast<int32_t>(bid % p.q_tiles);
+    bid /= p.q_tiles;
+    w.g = static_cast<int32_t>(bid % p.hkv);
+    w.r = static_cast<int32_t>(bid / p.hkv);
+    const int32_t c0 = __ldg(p.cu_q_lens + w.r), c1 = __ldg(p.cu_q_lens + w.r + 1);
+    int32_t C = c1 - c0;
+    int32_t L = __ldg(p.seq_lens + w.r);
+    const bool report_bad = qt == 0 && w.g == 0;
+    if (L < 0 || L > p.max_len) {
+        if (report_bad) report(p.status, PKV_DEV_BAD_LEN);
+        L = L < 0 ? 0 : p.max_len;
+    }
+    if (c0 < 0 || C < 0 || C > p.max_q_len || C > L) {
+        if (report_bad) report(p.status, PKV_DEV_BAD_LEN);
+        C = c0 < 0 || C < 0 ? 0 : min(min(C, p.max_q_len), L);
+    }
+    w.C = C;
+    w.L = L;
+    w.i0 = qt * qpt;
+    if (w.i0 >= C) return false;
+    w.nq = min(qpt, C - w.i0);
+    const int32_t p_first = L - C + w.i0;
+    w.kv_hi = p_first + w.nq;
+    w.kv_lo = p.window > 0 ? max(0, p_first - p.window + 1) : 0;
+    return true;
 }
 
-cudaError_t launch_prefill(const void *, const int32_t *, int32_t, const pkv_pool &,
-                           const int32_t *, int32_t, const int32_t *, int32_t, int32_t, int32_t,
-                           int32_t, float, void *, void *, size_t, int32_t *, cudaStream_t,
-                           int *unsupported)
+// ---------------------------------------------------------------------------
+// bf16, tcgen05
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(pf::kThreads, 1)
+    prefill_bf16_kernel(const __grid_constant__ CUtensorMap kmap,
+                        const __grid_constant__ CUtensorMap vmap, const PrefillParams p)
 {
-    *unsupported = 1;
-    return cudaSuccess;
+    using namespace pf;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *q_s = smem + kQOff;
+    uint8_t *stage_s = smem + kStageOff;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kBarOff);
+    uint64_t *kv_full = bars, *kv_empty = bars + 2, *s_full = bars + 4, *p_full = bars + 6,
+             *pv_done = bars + 8;
+    uint32_t *stage_mask = reinterpret_cast<uint32_t *>(smem + kMaskOff);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kTmemOff);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = p.group;
+    const int qpt = kRows / G;
+
+    if (threadIdx.x == 0) {
+        tma_prefetch_desc(&kmap);
+        tma_prefetch_desc(&vmap);
+    }
+    pdl_wait();
+    pdl_trigger();
+
+    PrefillRowInfo w;
+    if (!prefill_item(p, blockIdx.x, qpt, w)) return;
+    const int32_t jt0 = w.kv_lo / kKeys;
+    const int32_t ntile = (w.kv_hi - 1) / kKeys - jt0 + 1;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&kv_full[i], 1);
+            mbar_init(&kv_empty[i], 1);
+            mbar_init(&s_full[i], 1);
+            mbar_init(&p_full[i], 4);
+            mbar_init(&pv_done[i], 1);
+        }
+        fence_mbar_init();
+    }
+    if (warp == 1) tc::alloc(tmem_slot, kTmemCols);
+
+    // query tile: row i = (query t = i / G, head h = i % G) of this kv head
+    if (warp >= 2) {
+        const int i = threadIdx.x - 64;
+        const int t = i / G, h = i % G;
+        const bool valid = i < qpt * G && t < w.nq;
+        const uint4 *src = reinterpret_cast<const uint4 *>(p.q) +
+                           ((static_cast<int64_t>(__ldg(p.cu_q_lens + w.r)) + w.i0 + t) * p.hq +
+                            w.g * G + h) * (kD / 8);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+            const uint4 v = valid ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4 *>(q_s + (c >> 3) * (kRows * 128) + i * 128 +
+                                       (((c & 7) ^ (i & 7)) << 4)) = v;
+        }
+        fence_proxy_async_smem();  // read by the tensor cores (async proxy)
+    }
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tS[2] = {tmem, tmem + 128};
+    const uint32_t tO = tmem + 256;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        const uint64_t policy = l2_evict_last_policy();  // K/V tiles are re-read by the row's other CTAs
+        const int32_t *trow = p.tables + static_cast<int64_t>(w.r) * p.width;
+        for (int32_t jj = 0; jj < ntile; ++jj) {
+            const int st = jj & 1;
+            if (jj >= 2) {
+                bool ok = true;
+                if (lane == 0) ok = mbar_wait(&kv_empty[st], ((jj >> 1) + 1) & 1);
+                if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                    if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
+                    break;
+                }
+            }
+            const int32_t kb = (jt0 + jj) * (kKeys / 16) + lane;  // logical block of lane < 8
+            const bool in_range = lane < 8 && kb < p.width && kb * 16 < w.kv_hi &&
+                                  (kb + 1) * 16 > w.kv_lo;
+            const int32_t id = in_range ? __ldg(trow + kb) : -1;
+            const bool good = in_range && static_cast<uint32_t>(id) < static_cast<uint32_t>(p.num_blocks);
+            if (in_range && !good) report(p.status, PKV_DEV_BAD_BLOCK);
+            const uint32_t mask = __ballot_sync(0xffffffffu, good) & 0xffu;
+            if (lane == 0) {
+                stage_mask[st] = mask;
+                if (mask == 0) {
+                    mbar_arrive(&kv_full[st]);
+                } else {
+                    mbar_arrive_expect_tx(&kv_full[st], __popc(mask) * 4 * 2048);
+                }
+            }
+            __syncwarp();
+            uint8_t *ks = stage_s + st * kStageBytes, *vs = ks + kTileBytes;
+            for (int b = 0; b < 8; ++b) {
+                const int32_t bid = __shfl_sync(0xffffffffu, id, b);
+                if (lane == 0 && ((mask >> b) & 1u)) {
+#pragma unroll
+                    for (int reg = 0; reg < 2; ++reg) {
+                        tma_load_4d(ks + reg * kKVRegion + b * 2048, &kmap, &kv_full[st], reg * 64, 0,
+                                    w.g, bid, policy);
+                        tma_load_4d(vs + reg * kKVRegion + b * 2048, &vmap, &kv_full[st], reg * 64, 0,
+                                    w.g, bid, policy);
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issue
+        constexpr uint32_t idS = tc::idesc_bf16(kRows, kKeys, 0, 0);
+        constexpr uint32_t idO = tc::idesc_bf16(kRows, kD, 0, 1);
+        const uint32_t q_addr = smem_u32(q_s);
+        bool abort = false;
+        auto pv = [&](int32_t x) {
+            const int sb = x & 1;
+            bool ok = true;
+            if (lane == 0) ok = mbar_wait(&p_full[sb], (x >> 1) & 1);
+            if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
+                abort = true;
+                return;
+            }
+            tc::fence_after();
+            if (lane == 0) {
+                const uint32_t v_addr = smem_u32(stage_s + sb * kStageBytes + kTileBytes);
+#pragma unroll
+                for (int part = 0; part < 2; ++part)      // P hi, then P lo
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint64_t bdesc = tc::smem_desc(v_addr + kk * 2048, kKVRegion, 1024);
+                        tc::mma_ts(tO, tS[sb] + part * 64 + kk * 8, bdesc, idO,
+                                   (x > 0 || part > 0 || kk > 0) ? 1u : 0u);
+                    }
+                tc::commit(&kv_empty[sb]);
+                tc::commit(&pv_done[sb]);
+            }
+            __syncwarp();
+        };
+        for (int32_t jj = 0; jj < ntile && !abort; ++jj) {
+            const int st = jj & 1;
+            bool ok = true;
+            if (lane == 0) ok = mbar_wait(&kv_full[st], (jj >> 1) & 1);
+            if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
+                break;
+            }
+            tc::fence_after();
+            if (lane == 0) {
+                const uint32_t k_addr = smem_u32(stage_s + st * kStageBytes);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t off = (kk >> 2) * kKVRegion + (kk & 3) * 32;
+                    tc::mma_ss(tS[st], tc::smem_desc(q_addr + off, 16, 1024),
+                               tc::smem_desc(k_addr + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
+                }
+                tc::commit(&s_full[st]);
+            }
+            __syncwarp();
+            if (jj >= 1) pv(jj - 1);
+        }
+        if (!abort) pv(ntile - 1);
+    } else {
+        // ------------------------------------------------------------ softmax
+        const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+        const int row = 32 * (warp & 3) + lane;  // tensor-memory lane of this thread
+        const int t = row / G, h = row % G;
+        const bool valid_row = row < qpt * G && t < w.nq;
+        const int32_t qpos = w.L - w.C + w.i0 + t;
+        const int32_t qlo = p.window > 0 ? max(0, qpos - p.window + 1) : 0;
+        float m_ref = -INFINITY, l = 0.f;
+        bool abort = false;
+        for (int32_t jj = 0; jj < ntile; ++jj) {
+            const int sb = jj & 1;
+            const bool got = mbar_wait(&s_full[sb], (jj >> 1) & 1);
+            if (__any_sync(0xffffffffu, !got)) {
+                if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
+                abort = true;
+                break;
+            }
+            tc::fence_after();
+            float s[kKeys];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t r32[32];
+                tc::ld32(tS[sb] + lane_base + c * 32, r32);
+                tc::wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(r32[e]);
+            }
+            const int32_t kbase = (jt0 + jj) * kKeys;
+            const uint32_t mask = stage_mask[sb];
+            const bool full_tile = mask == 0xffu && kbase >= qlo && kbase + kKeys - 1 <= qpos && valid_row;
+            float mt = -INFINITY;
+            if (full_tile) {
+#pragma unroll
+                for (int c = 0; c < kKeys; ++c) {
+                    s[c] *= p.scale_log2;
+                    mt = fmaxf(mt, s[c]);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < kKeys; ++c) {
+                    const int32_t kp = kbase + c;
+                    const bool ok = valid_row && kp >= qlo && kp <= qpos && ((mask >> (c >> 4)) & 1u);
+                    s[c] = ok ? s[c] * p.scale_log2 : -INFINITY;
+                    mt = fmaxf(mt, s[c]);
+                }
+            }
+            // keep the reference max within 2^8 of the running max
+            const float new_ref = (mt > m_ref + static_cast<float>(kRescaleLog2)) ? mt : m_ref;
+            const float alpha = fast_exp2(m_ref - new_ref);  // 0 from -inf, 1 if unchanged
+            const bool resc = new_ref != m_ref && m_ref != -INFINITY;
+            if (jj > 0 && __any_sync(0xffffffffu, resc)) {
+                // O holds the P.V products up to tile jj-1: wait for the last one
+                const bool done = mbar_wait(&pv_done[(jj - 1) & 1], ((jj - 1) >> 1) & 1);
+                if (__any_sync(0xffffffffu, !done)) {
+                    if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
+                    abort = true;
+                    break;
+                }
+                tc::fence_after();
+                const float f = resc ? alpha : 1.f;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t r32[32];
+                    tc::ld32(tO + lane_base + c * 32, r32);
+                    tc::wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) r32[e] = __float_as_uint(__uint_as_float(r32[e]) * f);
+                    tc::st32(tO + lane_base + c * 32, r32);
+                }
+                tc::wait_st();
+            }
+            m_ref = new_ref;
+            const float mu = new_ref == -INFINITY ? 0.f : new_ref;
+            float lsum = 0.f;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t hi[32], lo[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const float a = fast_exp2(s[half * 64 + 2 * e] - mu);
+                    const float b = fast_exp2(s[half * 64 + 2 * e + 1] - mu);
+                    lsum += a + b;
+                    hi[e] = pack_bf16x2(a, b);
+                    lo[e] = pack_bf16x2(a - bf16lo_to_f32(hi[e]), b - bf16hi_to_f32(hi[e]));
+                }
+                tc::st32(tS[sb] + lane_base + half * 32, hi);
+                tc::st32(tS[sb] + lane_base + 64 + half * 32, lo);
+            }
+            l = l * (resc ? alpha : 1.f) + lsum;  // l is 0 while nothing was attended
+            tc::wait_st();
+            // value rows of keys outside [kv_lo, kv_hi) or of blocks not loaded
+            // hold stale slots (possibly NaN): zero them before P.V reads them
+            const bool edge = mask != 0xffu || kbase < w.kv_lo || kbase + kKeys > w.kv_hi;
+            if (edge) {
+                const int kr = row;  // one key row per thread
+                const int32_t kp = kbase + kr;
+                if (!(kp >= w.kv_lo && kp < w.kv_hi && ((mask >> (kr >> 4)) & 1u))) {
+                    uint8_t *vs = stage_s + sb * kStageBytes + kTileBytes;
+#pragma unroll
+                    for (int reg = 0; reg < 2; ++reg)
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            *reinterpret_cast<uint4 *>(vs + reg * kKVRegion + kr * 128 + c * 16) =
+                                make_uint4(0, 0, 0, 0);
+                }
+                fence_proxy_async_smem();
+            }
+            tc::fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&p_full[sb]);
+        }
+        // epilogue: O / l once the last P.V product is in
+        if (!abort) {
+            const int32_t x = ntile - 1;
+            const bool done = mbar_wait(&pv_done[x & 1], (x >> 1) & 1);
+            if (__any_sync(0xffffffffu, !done)) {
+                if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
+            } else {
+                tc::fence_after();
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+                uint4 *dst = reinterpret_cast<uint4 *>(p.out) +
+                             ((static_cast<int64_t>(__ldg(p.cu_q_lens + w.r)) + w.i0 + t) * p.hq +
+                              w.g * G + h) * (kD / 8);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t r32[32];
+                    tc::ld32(tO + lane_base + c * 32, r32);
+                    tc::wait_ld();
+                    if (valid_row) {
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            uint4 o;
+                            o.x = pack_bf16x2(__uint_as_float(r32[8 * v + 0]) * inv, __uint_as_float(r32[8 * v + 1]) * inv);
+                            o.y = pack_bf16x2(__uint_as_float(r32[8 * v + 2]) * inv, __uint_as_float(r32[8 * v + 3]) * inv);
+                            o.z = pack_bf16x2(__uint_as_float(r32[8 * v + 4]) * inv, __uint_as_float(r32[8 * v + 5]) * inv);
+                            o.w = pack_bf16x2(__uint_as_float(r32[8 * v + 6]) * inv, __uint_as_float(r32[8 * v + 7]) * inv);
+                            dst[c * 4 + v] = o;
+                        }
+                    }
+                }
+            }
+        }
+    }
+    tc::fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after();
+        tc::dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// f32, CUDA cores: 16 (query, head) pairs per CTA
+// ---------------------------------------------------------------------------
+constexpr int kPf32Threads = 128;
+constexpr int kPf32Pairs = 16;
+
+__global__ void __launch_bounds__(kPf32Threads) prefill_f32_kernel(const PrefillParams p)
+{
+    constexpr int NQ = kPf32Pairs;
+    extern __shared__ float fsm[];
+    const int D = p.head_dim, bs = p.block_size, G = p.group;
+    const int qpt = NQ / G;
+    float *qs = fsm, *os = qs + NQ * D, *ks = os + NQ * D, *vs = ks + bs * D, *sc = vs + bs * D;
+    float *mrow = sc + NQ * bs, *lrow = mrow + NQ, *alpha = lrow + NQ;
+    int32_t *phi = reinterpret_cast<int32_t *>(alpha + NQ), *plo = phi + NQ;
+    const int tid = threadIdx.x;
+    pdl_wait();
+    pdl_trigger();
+    PrefillRowInfo w;
+    if (!prefill_item(p, blockIdx.x, qpt, w)) return;
+    const int32_t row0 = __ldg(p.cu_q_lens + w.r) + w.i0;
+    if (tid < NQ) {
+        const int t = tid / G;
+        const bool valid = tid < qpt * G && t < w.nq;
+        const int32_t qpos = w.L - w.C + w.i0 + t;
+        phi[tid] = valid ? qpos + 1 : 0;
+        plo[tid] = p.window > 0 ? max(0, qpos - p.window + 1) : 0;
+        mrow[tid] = -INFINITY;
+        lrow[tid] = 0.f;
+    }
+    const float *qg = static_cast<const float *>(p.q);
+    for (int i = tid; i < NQ * D; i += kPf32Threads) {
+        const int k = i / D, d = i % D, t = k / G, h = k % G;
+        const bool valid = k < qpt * G && t < w.nq;
+        qs[i] = valid ? qg[(static_cast<int64_t>(row0 + t) * p.hq + w.g * G + h) * D + d] : 0.f;
+        os[i] = 0.f;
+    }
+    __syncthreads();
+    const float *kpool = static_cast<const float *>(p.k_pool);
+    const float *vpool = static_cast<const float *>(p.v_pool);
+    const int32_t *trow = p.tables + static_cast<int64_t>(w.r) * p.width;
+    for (int32_t b = w.kv_lo / bs; b * bs < w.kv_hi; ++b) {
+        const int32_t blk = b < p.width ? __ldg(trow + b) : -1;
+        const bool ok = static_cast<uint32_t>(blk) < static_cast<uint32_t>(p.num_blocks);
+        if (!ok && tid == 0) report(p.status, PKV_DEV_BAD_BLOCK);
+        if (ok) {
+            const int64_t base = (static_cast<int64_t>(blk) * p.hkv + w.g) * bs * D;
+            for (int j = tid; j < bs * D; j += kPf32Threads) {
+                ks[j] = __ldg(kpool + base + j);
+                vs[j] = __ldg(vpool + base + j);
+            }
+        }
+        __syncthreads();
+        for (int j = tid; j < NQ * bs; j += kPf32Threads) {
+            const int k = j / bs, tt = j % bs;
+            const int pos = b * bs + tt;
+            float sv = -INFINITY;
+            if (ok && pos >= plo[k] && pos < phi[k]) {
+                float acc = 0.f;
+                for (int d = 0; d < D; ++d) acc = fmaf(qs[k * D + d], ks[tt * D + d], acc);
+                sv = acc * p.scale_log2;
+            }
+            sc[j] = sv;
+        }
+        __syncthreads();
+        if (tid < NQ) {
+            float mx = -INFINITY;
+            for (int tt = 0; tt < bs; ++tt) mx = fmaxf(mx, sc[tid * bs + tt]);
+            const float mn = fmaxf(mrow[tid], mx);
+            const float mu = mn == -INFINITY ? 0.f : mn;
+            const float al = fast_exp2(mrow[tid] - mu);
+            float sum = 0.f;
+            for (int tt = 0; tt < bs; ++tt) {
+                const float e = fast_exp2(sc[tid * bs + tt] - mu);
+                sc[tid * bs + tt] = e;
+                sum += e;
+            }
+            lrow[tid] = lrow[tid] * al + sum;
+            mrow[tid] = mn;
+            alpha[tid] = al;
+        }
+        __syncthreads();
+        for (int j = tid; j < NQ * D; j += kPf32Threads) {
+            const int k = j / D, d = j % D;
+            float acc = os[j] * alpha[k];
+            for (int tt = 0; tt < bs; ++tt) {
+                const float wv = sc[k * bs + tt];
+                if (wv != 0.f) acc = fmaf(wv, vs[tt * D + d], acc);  // masked slots may hold NaN
+            }
+            os[j] = acc;
+        }
+        __syncthreads();
+    }
+    float *og = static_cast<float *>(p.out);
+    for (int j = tid; j < NQ * D; j += kPf32Threads) {
+        const int k = j / D, d = j % D, t = k / G, h = k % G;
+        if (k >= qpt * G || t >= w.nq) continue;
+        const float l = lrow[k];
+        og[(static_cast<int64_t>(row0 + t) * p.hq + w.g * G + h) * D + d] = l > 0.f ? os[j] / l : 0.f;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+bool prefill_shape_built(pkv_dtype dtype, int32_t D, int32_t bs, int32_t G)
+{
+    if (G < 1 || G > 16) return false;
+    if (dtype == PKV_BF16) return D == pf::kD && bs == 16 && (pf::kRows % G) == 0;
+    return (D == 32 || D == 64 || D == 128 || D == 256) && bs <= 64 && bs * D <= 4096 &&
+           (kPf32Pairs % G) == 0;
+}
+
+int32_t prefill_queries_per_cta(pkv_dtype dtype, int32_t G)
+{
+    return dtype == PKV_BF16 ? pf::kRows / G : kPf32Pairs / G;
+}
+
+cudaError_t launch_prefill_bf16(const PrefillParams &p, const CUtensorMap &kmap,
+                                const CUtensorMap &vmap, cudaStream_t stream)
+{
+    const int64_t ctas = static_cast<int64_t>(p.batch) * p.hkv * p.q_tiles;
+    if (ctas == 0) return cudaSuccess;
+    cudaError_t err = cudaFuncSetAttribute(prefill_bf16_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           pf::kLaunchBytes);
+    if (err != cudaSuccess) return err;
+    prof_begin(PKV_KERNEL_PREFILL, stream);
+    err = launch_pdl(prefill_bf16_kernel, dim3(static_cast<unsigned>(ctas)), dim3(pf::kThreads),
+                     pf::kLaunchBytes, stream, kmap, vmap, p);
+    prof_end(PKV_KERNEL_PREFILL, stream);
+    return err;
+}
+
+cudaError_t launch_prefill_f32(const PrefillParams &p, cudaStream_t stream)
+{
+    const int64_t ctas = static_cast<int64_t>(p.batch) * p.hkv * p.q_tiles;
+    if (ctas == 0) return cudaSuccess;
+    const int D = p.head_dim, bs = p.block_size, NQ = kPf32Pairs;
+    const size_t smem = sizeof(float) * (2 * NQ * D + 2 * bs * D + NQ * bs + 3 * NQ) +
+                        sizeof(int32_t) * 2 * NQ;
+    cudaError_t err = cudaFuncSetAttribute(prefill_f32_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+    prof_begin(PKV_KERNEL_PREFILL, stream);
+    err = launch_pdl(prefill_f32_kernel, dim3(static_cast<unsigned>(ctas)), dim3(kPf32Threads),
+                     smem, stream, p);
+    prof_end(PKV_KERNEL_PREFILL, stream);
+    return err;
 }
 
 }  // namespace pkv

@@ -1,0 +1,132 @@
+"""GPU parity of the chunked prefill against the oracle (through the C ABI).
+
+The chunk's K/V is appended first (paged_kv_append), then every query of the
+chunk attends the paged prefix and the chunk causally.  Tolerances as for
+decode: bf16 |gpu - ref| <= 2e-3 + 1e-2 |ref|; f32 1e-5 + 1e-5 |ref|.
+"""
+import numpy as np
+import pytest
+
+import pkv_inputs as gen
+from gpu_util import Dev, append, assert_close, oracle_pools, storage_bytes, to_f64
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import block_paged_kv_gb300 as m
+    return m
+
+
+def run_prefill(pkv, orc, w, samples=None, check_pool=True):
+    d = Dev(w)
+    slots = append(pkv, d)
+    or_slots, kp, vp = oracle_pools(orc, w)
+    assert np.array_equal(slots, or_slots)
+    if check_pool:
+        assert storage_bytes(d.k_pool) == kp.tobytes() and storage_bytes(d.v_pool) == vp.tobytes()
+    max_q = int(np.max(np.diff(w.cu_q_lens)))
+    out = pkv.paged_prefill_chunk_attention(d.q, d.cu, d.k_pool, d.v_pool, d.tables, d.seq_lens,
+                                            max_q, w.window, w.scale,
+                                            max_seq_len=int(w.seq_lens.max()), status=d.status)
+    torch.cuda.synchronize()
+    assert int(d.status.item()) == 0, int(d.status.item())
+    got = to_f64(out)
+    if samples is None:
+        ref = orc.prefill(w.q, w.cu_q_lens, kp, vp, w.dtype, w.block_tables, w.seq_lens, w.window,
+                          w.scale)
+        return got, ref, d
+    ref = orc.prefill(w.q, w.cu_q_lens, kp, vp, w.dtype, w.block_tables, w.seq_lens, w.window,
+                      w.scale, samples=samples)
+    rows = w.cu_q_lens[samples[:, 0]] + samples[:, 1]
+    return got[rows, samples[:, 2]], ref, d
+
+
+def test_chunked_prefill_full_size(pkv, orc):
+    w = gen.chunked_prefill()
+    u = gen.uniform_ints(5, "samples", 3 * 160, 0, 1 << 30)
+    C = int(w.cu_q_lens[1] - w.cu_q_lens[0])
+    samples = [[r, i, h] for r in range(w.batch) for i in (0, 1, 31, 32, C - 1)
+               for h in (0, w.num_q_heads - 1)]
+    samples += [[int(u[3 * k]) % w.batch, int(u[3 * k + 1]) % C, int(u[3 * k + 2]) % w.num_q_heads]
+                for k in range(160)]
+    samples = np.array(samples, dtype=np.int32)
+    got, ref, _ = run_prefill(pkv, orc, w, samples=samples, check_pool=False)
+    assert_close(got, ref, "bf16", "chunked prefill 4 x 512 vs 16384 prefix")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("hq,hkv", [(4, 4), (8, 4), (16, 4), (32, 4), (16, 1)])
+@pytest.mark.parametrize("window", [0, 50])
+def test_ragged_shapes(pkv, orc, dtype, hq, hkv, window):
+    w = gen.prefill_workload(seed=40 + hq + hkv + window, dtype=dtype, num_q_heads=hq,
+                             num_kv_heads=hkv, head_dim=128,
+                             prefix_lens=[0, 5, 130, 300], chunk_lens=[1, 47, 200, 129],
+                             window=window)
+    got, ref, _ = run_prefill(pkv, orc, w)
+    assert_close(got, ref, dtype, f"{dtype} prefill {hq}/{hkv} w{window}")
+
+
+@pytest.mark.parametrize("d", [64, 256])
+def test_f32_other_head_dims(pkv, orc, d):
+    w = gen.prefill_workload(seed=60 + d, dtype="f32", num_q_heads=8, num_kv_heads=2, head_dim=d,
+                             prefix_lens=[17, 64], chunk_lens=[9, 20], window=0)
+    got, ref, _ = run_prefill(pkv, orc, w)
+    assert_close(got, ref, "f32", f"f32 prefill d{d}")
+
+
+def test_prefill_with_one_query_equals_decode(pkv):
+    w = gen.prefill_workload(seed=70, dtype="bf16", num_q_heads=16, num_kv_heads=4, head_dim=128,
+                             prefix_lens=[300, 1000, 31], chunk_lens=[1, 1, 1])
+    d = Dev(w)
+    append(pkv, d)
+    pre = pkv.paged_prefill_chunk_attention(d.q, d.cu, d.k_pool, d.v_pool, d.tables, d.seq_lens, 1,
+                                            0, w.scale)
+    dec = pkv.paged_decode_attention(d.q, d.k_pool, d.v_pool, d.tables, d.seq_lens, 0, w.scale)
+    torch.cuda.synchronize()
+    assert_close(to_f64(pre), to_f64(dec), "bf16", "prefill C=1 vs decode")
+
+
+def test_two_chunks_equal_one_chunk(pkv, orc):
+    # the chunk of 200 queries prefilled at once, or as 120 then 80
+    w = gen.prefill_workload(seed=71, dtype="bf16", num_q_heads=8, num_kv_heads=2, head_dim=128,
+                             prefix_lens=[500], chunk_lens=[200])
+    d = Dev(w)
+    append(pkv, d)
+    one = pkv.paged_prefill_chunk_attention(d.q, d.cu, d.k_pool, d.v_pool, d.tables, d.seq_lens, 200,
+                                            0, w.scale)
+    first = pkv.paged_prefill_chunk_attention(
+        d.q[:120].contiguous(), torch.tensor([0, 120], dtype=torch.int32, device="cuda"), d.k_pool,
+        d.v_pool, d.tables, torch.tensor([620], dtype=torch.int32, device="cuda"), 120, 0, w.scale)
+    second = pkv.paged_prefill_chunk_attention(
+        d.q[120:].contiguous(), torch.tensor([0, 80], dtype=torch.int32, device="cuda"), d.k_pool,
+        d.v_pool, d.tables, d.seq_lens, 80, 0, w.scale)
+    torch.cuda.synchronize()
+    assert_close(to_f64(torch.cat([first, second])), to_f64(one), "bf16", "two chunks vs one")
+
+
+def test_deterministic(pkv):
+    w = gen.prefill_workload(seed=72, dtype="bf16", num_q_heads=32, num_kv_heads=8, head_dim=128,
+                             prefix_lens=[2000, 700], chunk_lens=[300, 128])
+    d = Dev(w)
+    append(pkv, d)
+    a = pkv.paged_prefill_chunk_attention(d.q, d.cu, d.k_pool, d.v_pool, d.tables, d.seq_lens, 300,
+                                          0, w.scale).clone()
+    b = pkv.paged_prefill_chunk_attention(d.q, d.cu, d.k_pool, d.v_pool, d.tables, d.seq_lens, 300,
+                                          0, w.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b) and int(d.status.item()) == 0
+
+
+def test_unsupported_shape_reported(pkv):
+    w = gen.prefill_workload(seed=73, dtype="bf16", num_q_heads=6, num_kv_heads=2, head_dim=64,
+                             prefix_lens=[10], chunk_lens=[4])
+    d = Dev(w)
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.paged_prefill_chunk_attention(d.q, d.cu, d.k_pool, d.v_pool, d.tables, d.seq_lens, 4, 0,
+                                          w.scale)
+    assert e.value.code == pkv.PKV_ERR_UNSUPPORTED
