@@ -54,6 +54,14 @@ def peaks():
     return 6800.0, "fallback"
 
 
+def bf16_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"])
+    return 1900.0
+
+
 def workload_bytes(w: gen.Workload):
     """Unique K/V bytes a decode step attends and the split kernel's share."""
     D, hkv, eb = w.head_dim, w.num_kv_heads, w.elem_bytes
@@ -351,6 +359,28 @@ def secondary_measurements(args, pkv, torch, dev):
             b = workload_bytes(w)[0]
         res[name] = {"us": round(s * 1e6, 2), "GB/s": round(b / s / 1e9, 1), "kv_bytes": b}
         del kp, vp
+    # chunked prefill: 4 rows x 512 queries against a 16384-token paged prefix
+    w = gen.chunked_prefill()
+    kp, vp, q = up(w, w.k_pool), up(w, w.v_pool), up(w, w.q)
+    kn, vn = up(w, w.k_new), up(w, w.v_new)
+    t = torch.from_numpy(w.block_tables).to(dev)
+    sl = torch.from_numpy(w.seq_lens).to(dev)
+    cu = torch.from_numpy(w.cu_q_lens).to(dev)
+    slots = torch.from_numpy(pkv.slot_mapping_host(w.block_tables, w.num_blocks, w.new_rows,
+                                                   w.new_pos, 16)).to(dev)
+    pkv.paged_kv_append(kp, vp, slots, kn, vn)
+    out = torch.empty_like(q)
+    C = int(w.cu_q_lens[1] - w.cu_q_lens[0])
+    ml = int(w.seq_lens.max())
+    s = time_loop(torch, lambda: pkv.paged_prefill_chunk_attention(q, cu, kp, vp, t, sl, C, 0, w.scale,
+                                                                   out=out, max_seq_len=ml),
+                  30, 5, flush)
+    keys = sum(int(L) - C + i + 1 for L in w.seq_lens for i in range(C))
+    flops = 4 * w.head_dim * keys * w.num_q_heads
+    res["chunked_prefill"] = {"us": round(s * 1e6, 2), "TFLOP/s": round(flops / s / 1e12, 1),
+                              "flop": flops, "frac_of_bf16_peak": round(flops / s / 1e12 / bf16_peak(), 3),
+                              "peak": "measured bf16_tflops (burst)", "l2": "flushed before each call"}
+    del kp, vp
     # bulk append: every token of the batch-32 workload's private suffixes
     w = gen.shared_prefix_b32()
     n = int(np.sum(w.seq_lens - 1024))
