@@ -8,8 +8,9 @@
 // 128 M-rows are (query, head) pairs: all G q heads of the kv head, so each
 // K/V tile is loaded once for the whole GQA group.  QK^T and PV are dense
 // contractions and run on the 5th-generation tensor cores:
-//   warp 0    TMA producer: K and V tiles of 128 keys (8 paged blocks, 16
-//             tensor loads each) into a 2-stage ring;
+//   warps 0/6 TMA producers: K and V tiles of 128 keys (8 paged blocks, 16
+//             tensor loads each) into rings of 3 K and 2 V stages; a K stage
+//             is freed once S is computed, a V stage once P.V is;
 //   warp 1    allocates tensor memory and issues tcgen05.mma from one thread:
 //             S_j = Q K_j^T into a double-buffered S in tensor memory, then
 //             O += P_j V_j with P read from tensor memory (V MN-major);
@@ -32,18 +33,20 @@ constexpr int kRows = 128;                // M
 constexpr int kKeys = 128;                // keys per tile (8 blocks of 16)
 constexpr int kQBytes = 2 * kRows * 128;  // two 64-dim swizzled regions
 constexpr int kKVRegion = kKeys * 128;    // 16 KiB
-constexpr int kTileBytes = 2 * kKVRegion; // 32 KiB: K or V tile
-constexpr int kStageBytes = 2 * kTileBytes;
-constexpr int kStages = 2;
+constexpr int kTileBytes = 2 * kKVRegion; // 32 KiB: a K or a V tile
+constexpr int kKStages = 3;               // K is released as soon as S is computed
+constexpr int kVStages = 2;               // V only once P.V is done
 constexpr int kQOff = 0;
-constexpr int kStageOff = kQOff + kQBytes;
-constexpr int kBarOff = kStageOff + kStages * kStageBytes;
-// barriers: kv_full[2], kv_empty[2], s_full[2], p_full[2], pv_done[2]
-constexpr int kMaskOff = kBarOff + 10 * 8;
-constexpr int kTmemOff = kMaskOff + kStages * 4;
+constexpr int kKOff = kQOff + kQBytes;
+constexpr int kVOff = kKOff + kKStages * kTileBytes;
+constexpr int kBarOff = kVOff + kVStages * kTileBytes;
+// barriers: k_full[3], k_empty[3], v_full[2], v_empty[2], s_full[2], p_full[2], pv_done[2]
+constexpr int kNumBars = 16;
+constexpr int kMaskOff = kBarOff + kNumBars * 8;
+constexpr int kTmemOff = kMaskOff + kKStages * 4;
 constexpr int kBytes = kTmemOff + 16;
 constexpr int kLaunchBytes = kBytes + 1024;
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;             // K producer, MMA, 4 softmax warps, V producer
 constexpr uint32_t kTmemCols = 512;       // S0, S1, O (+ spare)
 constexpr uint32_t kRescaleLog2 = 8;      // O is rescaled only when the max grows past 2^8
 }  // namespace pf
@@ -82,6 +85,16 @@ __device__ __forceinline__ bool prefill_item(const PrefillParams &p, int64_t bid
     return true;
 }
 
+// Wait by one lane, result broadcast to the warp; reports a timeout.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, int lane, int32_t *status)
+{
+    bool ok = true;
+    if (lane == 0) ok = mbar_wait(bar, parity);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok && lane == 0) report(status, PKV_DEV_TIMEOUT);
+    return ok;
+}
+
 // ---------------------------------------------------------------------------
 // bf16, tcgen05
 // ---------------------------------------------------------------------------
@@ -94,11 +107,12 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t *q_s = smem + kQOff;
-    uint8_t *stage_s = smem + kStageOff;
+    uint8_t *k_s = smem + kKOff;
+    uint8_t *v_s = smem + kVOff;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kBarOff);
-    uint64_t *kv_full = bars, *kv_empty = bars + 2, *s_full = bars + 4, *p_full = bars + 6,
-             *pv_done = bars + 8;
-    uint32_t *stage_mask = reinterpret_cast<uint32_t *>(smem + kMaskOff);
+    uint64_t *k_full = bars, *k_empty = bars + 3, *v_full = bars + 6, *v_empty = bars + 8,
+             *s_full = bars + 10, *p_full = bars + 12, *pv_done = bars + 14;
+    uint32_t *kmask = reinterpret_cast<uint32_t *>(smem + kMaskOff);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kTmemOff);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -118,9 +132,13 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
     const int32_t ntile = (w.kv_hi - 1) / kKeys - jt0 + 1;
 
     if (threadIdx.x == 0) {
+        for (int i = 0; i < kKStages; ++i) {
+            mbar_init(&k_full[i], 1);
+            mbar_init(&k_empty[i], 1 + 4);  // the S product, and the softmax warps' read of kmask
+        }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&kv_full[i], 1);
-            mbar_init(&kv_empty[i], 1);
+            mbar_init(&v_full[i], 1);
+            mbar_init(&v_empty[i], 1);
             mbar_init(&s_full[i], 1);
             mbar_init(&p_full[i], 4);
             mbar_init(&pv_done[i], 1);
@@ -130,7 +148,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
     if (warp == 1) tc::alloc(tmem_slot, kTmemCols);
 
     // query tile: row i = (query t = i / G, head h = i % G) of this kv head
-    if (warp >= 2) {
+    if (warp >= 2 && warp < 6) {
         const int i = threadIdx.x - 64;
         const int t = i / G, h = i % G;
         const bool valid = i < qpt * G && t < w.nq;
@@ -152,47 +170,41 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
     const uint32_t tS[2] = {tmem, tmem + 128};
     const uint32_t tO = tmem + 256;
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
-        const uint64_t policy = l2_evict_last_policy();  // K/V tiles are re-read by the row's other CTAs
+    if (warp == 0 || warp == 6) {
+        // --------------------------------------------- K (warp 0) / V (warp 6) producer
+        const bool is_k = warp == 0;
+        const CUtensorMap *map = is_k ? &kmap : &vmap;
+        uint8_t *ring = is_k ? k_s : v_s;
+        const int stages = is_k ? kKStages : kVStages;
+        uint64_t *full = is_k ? k_full : v_full;
+        uint64_t *empty = is_k ? k_empty : v_empty;
+        const uint64_t policy = l2_evict_last_policy();  // re-read by the row's other CTAs
         const int32_t *trow = p.tables + static_cast<int64_t>(w.r) * p.width;
         for (int32_t jj = 0; jj < ntile; ++jj) {
-            const int st = jj & 1;
-            if (jj >= 2) {
-                bool ok = true;
-                if (lane == 0) ok = mbar_wait(&kv_empty[st], ((jj >> 1) + 1) & 1);
-                if (!__shfl_sync(0xffffffffu, ok, 0)) {
-                    if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
-                    break;
-                }
-            }
+            const int st = jj % stages;
+            if (jj >= stages && !warp_wait(&empty[st], ((jj / stages) + 1) & 1, lane, p.status))
+                break;
             const int32_t kb = (jt0 + jj) * (kKeys / 16) + lane;  // logical block of lane < 8
             const bool in_range = lane < 8 && kb < p.width && kb * 16 < w.kv_hi &&
                                   (kb + 1) * 16 > w.kv_lo;
             const int32_t id = in_range ? __ldg(trow + kb) : -1;
             const bool good = in_range && static_cast<uint32_t>(id) < static_cast<uint32_t>(p.num_blocks);
-            if (in_range && !good) report(p.status, PKV_DEV_BAD_BLOCK);
+            if (is_k && in_range && !good) report(p.status, PKV_DEV_BAD_BLOCK);
             const uint32_t mask = __ballot_sync(0xffffffffu, good) & 0xffu;
             if (lane == 0) {
-                stage_mask[st] = mask;
-                if (mask == 0) {
-                    mbar_arrive(&kv_full[st]);
-                } else {
-                    mbar_arrive_expect_tx(&kv_full[st], __popc(mask) * 4 * 2048);
-                }
+                if (is_k) kmask[st] = mask;
+                if (mask == 0)
+                    mbar_arrive(&full[st]);
+                else
+                    mbar_arrive_expect_tx(&full[st], __popc(mask) * 2 * 2048);
             }
             __syncwarp();
-            uint8_t *ks = stage_s + st * kStageBytes, *vs = ks + kTileBytes;
+            uint8_t *dst = ring + st * kTileBytes;
             for (int b = 0; b < 8; ++b) {
                 const int32_t bid = __shfl_sync(0xffffffffu, id, b);
                 if (lane == 0 && ((mask >> b) & 1u)) {
-#pragma unroll
-                    for (int reg = 0; reg < 2; ++reg) {
-                        tma_load_4d(ks + reg * kKVRegion + b * 2048, &kmap, &kv_full[st], reg * 64, 0,
-                                    w.g, bid, policy);
-                        tma_load_4d(vs + reg * kKVRegion + b * 2048, &vmap, &kv_full[st], reg * 64, 0,
-                                    w.g, bid, policy);
-                    }
+                    tma_load_4d(dst + b * 2048, map, &full[st], 0, 0, w.g, bid, policy);
+                    tma_load_4d(dst + kKVRegion + b * 2048, map, &full[st], 64, 0, w.g, bid, policy);
                 }
             }
         }
@@ -204,16 +216,14 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         bool abort = false;
         auto pv = [&](int32_t x) {
             const int sb = x & 1;
-            bool ok = true;
-            if (lane == 0) ok = mbar_wait(&p_full[sb], (x >> 1) & 1);
-            if (!__shfl_sync(0xffffffffu, ok, 0)) {
-                if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
+            if (!warp_wait(&p_full[sb], (x >> 1) & 1, lane, p.status) ||
+                !warp_wait(&v_full[sb], (x >> 1) & 1, lane, p.status)) {
                 abort = true;
                 return;
             }
             tc::fence_after();
             if (lane == 0) {
-                const uint32_t v_addr = smem_u32(stage_s + sb * kStageBytes + kTileBytes);
+                const uint32_t v_addr = smem_u32(v_s + sb * kTileBytes);
 #pragma unroll
                 for (int part = 0; part < 2; ++part)      // P hi, then P lo
 #pragma unroll
@@ -222,29 +232,25 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
                         tc::mma_ts(tO, tS[sb] + part * 64 + kk * 8, bdesc, idO,
                                    (x > 0 || part > 0 || kk > 0) ? 1u : 0u);
                     }
-                tc::commit(&kv_empty[sb]);
+                tc::commit(&v_empty[sb]);
                 tc::commit(&pv_done[sb]);
             }
             __syncwarp();
         };
         for (int32_t jj = 0; jj < ntile && !abort; ++jj) {
-            const int st = jj & 1;
-            bool ok = true;
-            if (lane == 0) ok = mbar_wait(&kv_full[st], (jj >> 1) & 1);
-            if (!__shfl_sync(0xffffffffu, ok, 0)) {
-                if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
-                break;
-            }
+            const int ks = jj % kKStages, sb = jj & 1;
+            if (!warp_wait(&k_full[ks], (jj / kKStages) & 1, lane, p.status)) break;
             tc::fence_after();
             if (lane == 0) {
-                const uint32_t k_addr = smem_u32(stage_s + st * kStageBytes);
+                const uint32_t k_addr = smem_u32(k_s + ks * kTileBytes);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint32_t off = (kk >> 2) * kKVRegion + (kk & 3) * 32;
-                    tc::mma_ss(tS[st], tc::smem_desc(q_addr + off, 16, 1024),
+                    tc::mma_ss(tS[sb], tc::smem_desc(q_addr + off, 16, 1024),
                                tc::smem_desc(k_addr + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
                 }
-                tc::commit(&s_full[st]);
+                tc::commit(&s_full[sb]);
+                tc::commit(&k_empty[ks]);
             }
             __syncwarp();
             if (jj >= 1) pv(jj - 1);
@@ -253,7 +259,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
     } else {
         // ------------------------------------------------------------ softmax
         const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-        const int row = 32 * (warp & 3) + lane;  // tensor-memory lane of this thread
+        const int row = 32 * (warp & 3) + lane;  // tensor-memory lane of this thread = M-row
         const int t = row / G, h = row % G;
         const bool valid_row = row < qpt * G && t < w.nq;
         const int32_t qpos = w.L - w.C + w.i0 + t;
@@ -261,25 +267,35 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         float m_ref = -INFINITY, l = 0.f;
         bool abort = false;
         for (int32_t jj = 0; jj < ntile; ++jj) {
-            const int sb = jj & 1;
-            const bool got = mbar_wait(&s_full[sb], (jj >> 1) & 1);
+            const int sb = jj & 1, ks = jj % kKStages;
+            bool got = mbar_wait(&s_full[sb], (jj >> 1) & 1);
+            got = got && mbar_wait(&k_full[ks], (jj / kKStages) & 1);  // for kmask
             if (__any_sync(0xffffffffu, !got)) {
                 if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
                 abort = true;
                 break;
             }
+            const uint32_t mask = kmask[ks];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&k_empty[ks]);
             tc::fence_after();
             float s[kKeys];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t r32[32];
-                tc::ld32(tS[sb] + lane_base + c * 32, r32);
+            {
+                uint32_t r0[32], r1[32], r2[32], r3[32];
+                tc::ld32(tS[sb] + lane_base + 0, r0);
+                tc::ld32(tS[sb] + lane_base + 32, r1);
+                tc::ld32(tS[sb] + lane_base + 64, r2);
+                tc::ld32(tS[sb] + lane_base + 96, r3);
                 tc::wait_ld();
 #pragma unroll
-                for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(r32[e]);
+                for (int e = 0; e < 32; ++e) {
+                    s[e] = __uint_as_float(r0[e]);
+                    s[32 + e] = __uint_as_float(r1[e]);
+                    s[64 + e] = __uint_as_float(r2[e]);
+                    s[96 + e] = __uint_as_float(r3[e]);
+                }
             }
             const int32_t kbase = (jt0 + jj) * kKeys;
-            const uint32_t mask = stage_mask[sb];
             const bool full_tile = mask == 0xffu && kbase >= qlo && kbase + kKeys - 1 <= qpos && valid_row;
             float mt = -INFINITY;
             if (full_tile) {
@@ -340,15 +356,20 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
                 tc::st32(tS[sb] + lane_base + 64 + half * 32, lo);
             }
             l = l * (resc ? alpha : 1.f) + lsum;  // l is 0 while nothing was attended
-            tc::wait_st();
             // value rows of keys outside [kv_lo, kv_hi) or of blocks not loaded
             // hold stale slots (possibly NaN): zero them before P.V reads them
             const bool edge = mask != 0xffu || kbase < w.kv_lo || kbase + kKeys > w.kv_hi;
             if (edge) {
+                const bool landed = mbar_wait(&v_full[sb], (jj >> 1) & 1);
+                if (__any_sync(0xffffffffu, !landed)) {
+                    if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
+                    abort = true;
+                    break;
+                }
                 const int kr = row;  // one key row per thread
                 const int32_t kp = kbase + kr;
                 if (!(kp >= w.kv_lo && kp < w.kv_hi && ((mask >> (kr >> 4)) & 1u))) {
-                    uint8_t *vs = stage_s + sb * kStageBytes + kTileBytes;
+                    uint8_t *vs = v_s + sb * kTileBytes;
 #pragma unroll
                     for (int reg = 0; reg < 2; ++reg)
 #pragma unroll
@@ -358,6 +379,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
                 }
                 fence_proxy_async_smem();
             }
+            tc::wait_st();
             tc::fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&p_full[sb]);
