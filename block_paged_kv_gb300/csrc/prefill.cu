@@ -14,9 +14,10 @@
 //   warp 1    allocates tensor memory and issues tcgen05.mma from one thread:
 //             S_j = Q K_j^T into a double-buffered S in tensor memory, then
 //             O += P_j V_j with P read from tensor memory (V MN-major);
-//   warps 2-5 softmax, one thread per M-row: S row from tensor memory, causal /
-//             window / range mask, running max kept within 2^8 of the true
-//             maximum (O in tensor memory is rescaled only when it moves
+//   warps 2-9 softmax, two threads per M-row (64 key columns each, row
+//             maxima exchanged through shared memory): S from tensor memory,
+//             causal / window / range mask, running max kept within 2^8 of the
+//             true maximum (O in tensor memory is rescaled only when it moves
 //             further), P written back over S as bf16 hi + lo terms (the P.V
 //             product then carries P to ~2^-17 relative), and the epilogue
 //             O / l to global memory.
@@ -43,10 +44,13 @@ constexpr int kBarOff = kVOff + kVStages * kTileBytes;
 // barriers: k_full[3], k_empty[3], v_full[2], v_empty[2], s_full[2], p_full[2], pv_done[2]
 constexpr int kNumBars = 16;
 constexpr int kMaskOff = kBarOff + kNumBars * 8;
-constexpr int kTmemOff = kMaskOff + kKStages * 4;
+constexpr int kXOff = kMaskOff + kKStages * 4;       // row maxima exchanged between halves: [2][2][128]
+constexpr int kTmemOff = kXOff + 2 * 2 * kRows * 4;
 constexpr int kBytes = kTmemOff + 16;
 constexpr int kLaunchBytes = kBytes + 1024;
-constexpr int kThreads = 224;             // K producer, MMA, 4 softmax warps, V producer
+constexpr int kSoftmaxWarps = 8;          // two per tensor-memory lane quarter: 64 key columns each
+constexpr int kVWarp = 2 + kSoftmaxWarps;
+constexpr int kThreads = 32 * (kVWarp + 1);  // K producer, MMA, 8 softmax warps, V producer
 constexpr uint32_t kTmemCols = 512;       // S0, S1, O (+ spare)
 constexpr uint32_t kRescaleLog2 = 8;      // O is rescaled only when the max grows past 2^8
 }  // namespace pf
@@ -113,6 +117,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
     uint64_t *k_full = bars, *k_empty = bars + 3, *v_full = bars + 6, *v_empty = bars + 8,
              *s_full = bars + 10, *p_full = bars + 12, *pv_done = bars + 14;
     uint32_t *kmask = reinterpret_cast<uint32_t *>(smem + kMaskOff);
+    float *xbuf = reinterpret_cast<float *>(smem + kXOff);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kTmemOff);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -134,13 +139,13 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < kKStages; ++i) {
             mbar_init(&k_full[i], 1);
-            mbar_init(&k_empty[i], 1 + 4);  // the S product, and the softmax warps' read of kmask
+            mbar_init(&k_empty[i], 1 + kSoftmaxWarps);  // the S product, and the softmax warps' read of kmask
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&v_full[i], 1);
             mbar_init(&v_empty[i], 1);
             mbar_init(&s_full[i], 1);
-            mbar_init(&p_full[i], 4);
+            mbar_init(&p_full[i], kSoftmaxWarps);
             mbar_init(&pv_done[i], 1);
         }
         fence_mbar_init();
@@ -149,7 +154,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
 
     // query tile: row i = (query t = i / G, head h = i % G) of this kv head
     if (warp >= 2 && warp < 6) {
-        const int i = threadIdx.x - 64;
+        const int i = threadIdx.x - 64;  // 128 threads, one row each
         const int t = i / G, h = i % G;
         const bool valid = i < qpt * G && t < w.nq;
         const uint4 *src = reinterpret_cast<const uint4 *>(p.q) +
@@ -170,8 +175,8 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
     const uint32_t tS[2] = {tmem, tmem + 128};
     const uint32_t tO = tmem + 256;
 
-    if (warp == 0 || warp == 6) {
-        // --------------------------------------------- K (warp 0) / V (warp 6) producer
+    if (warp == 0 || warp == kVWarp) {
+        // ---------------------------------------- K (warp 0) / V (last warp) producer
         const bool is_k = warp == 0;
         const CUtensorMap *map = is_k ? &kmap : &vmap;
         uint8_t *ring = is_k ? k_s : v_s;
@@ -224,13 +229,15 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             tc::fence_after();
             if (lane == 0) {
                 const uint32_t v_addr = smem_u32(v_s + sb * kTileBytes);
+                // keys 32c..32c+31 hold P hi in S columns 32c..32c+15 and P lo
+                // in 32c+16..32c+31 (bf16 pairs, 8 columns per 16 keys)
 #pragma unroll
                 for (int part = 0; part < 2; ++part)      // P hi, then P lo
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
                         const uint64_t bdesc = tc::smem_desc(v_addr + kk * 2048, kKVRegion, 1024);
-                        tc::mma_ts(tO, tS[sb] + part * 64 + kk * 8, bdesc, idO,
-                                   (x > 0 || part > 0 || kk > 0) ? 1u : 0u);
+                        tc::mma_ts(tO, tS[sb] + 32 * (kk >> 1) + 8 * (kk & 1) + 16 * part, bdesc,
+                                   idO, (x > 0 || part > 0 || kk > 0) ? 1u : 0u);
                     }
                 tc::commit(&v_empty[sb]);
                 tc::commit(&pv_done[sb]);
@@ -258,8 +265,12 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         if (!abort) pv(ntile - 1);
     } else {
         // ------------------------------------------------------------ softmax
+        // warps 2..9: lane quarter q = warp % 4 (rows 32q..32q+31), key half
+        // hf: columns 64hf..64hf+63 of S (and of O)
+        const int hf = (warp - 2) >> 2;
         const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
         const int row = 32 * (warp & 3) + lane;  // tensor-memory lane of this thread = M-row
+        const uint32_t col0 = 64 * hf;
         const int t = row / G, h = row % G;
         const bool valid_row = row < qpt * G && t < w.nq;
         const int32_t qpos = w.L - w.C + w.i0 + t;
@@ -279,40 +290,36 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&k_empty[ks]);
             tc::fence_after();
-            float s[kKeys];
+            float s[64];
             {
-                uint32_t r0[32], r1[32], r2[32], r3[32];
-                tc::ld32(tS[sb] + lane_base + 0, r0);
-                tc::ld32(tS[sb] + lane_base + 32, r1);
-                tc::ld32(tS[sb] + lane_base + 64, r2);
-                tc::ld32(tS[sb] + lane_base + 96, r3);
+                uint32_t r0[32], r1[32];
+                tc::ld32(tS[sb] + lane_base + col0, r0);
+                tc::ld32(tS[sb] + lane_base + col0 + 32, r1);
                 tc::wait_ld();
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
-                    s[e] = __uint_as_float(r0[e]);
-                    s[32 + e] = __uint_as_float(r1[e]);
-                    s[64 + e] = __uint_as_float(r2[e]);
-                    s[96 + e] = __uint_as_float(r3[e]);
+                    s[e] = __uint_as_float(r0[e]) * p.scale_log2;
+                    s[32 + e] = __uint_as_float(r1[e]) * p.scale_log2;
                 }
             }
-            const int32_t kbase = (jt0 + jj) * kKeys;
-            const bool full_tile = mask == 0xffu && kbase >= qlo && kbase + kKeys - 1 <= qpos && valid_row;
-            float mt = -INFINITY;
-            if (full_tile) {
+            const int32_t kbase = (jt0 + jj) * kKeys + static_cast<int32_t>(col0);
+            const uint32_t hmask = (mask >> (4 * hf)) & 0xfu;  // blocks of this half
+            const bool full = hmask == 0xfu && kbase >= qlo && kbase + 63 <= qpos && valid_row;
+            if (!full) {
 #pragma unroll
-                for (int c = 0; c < kKeys; ++c) {
-                    s[c] *= p.scale_log2;
-                    mt = fmaxf(mt, s[c]);
-                }
-            } else {
-#pragma unroll
-                for (int c = 0; c < kKeys; ++c) {
+                for (int c = 0; c < 64; ++c) {
                     const int32_t kp = kbase + c;
-                    const bool ok = valid_row && kp >= qlo && kp <= qpos && ((mask >> (c >> 4)) & 1u);
-                    s[c] = ok ? s[c] * p.scale_log2 : -INFINITY;
-                    mt = fmaxf(mt, s[c]);
+                    const bool ok = valid_row && kp >= qlo && kp <= qpos && ((hmask >> (c >> 4)) & 1u);
+                    if (!ok) s[c] = -INFINITY;
                 }
             }
+            float mt = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 64; ++c) mt = fmaxf(mt, s[c]);
+            // row maximum over both halves
+            xbuf[(sb * 2 + hf) * kRows + row] = mt;
+            asm volatile("bar.sync 1, %0;" ::"r"(32 * kSoftmaxWarps) : "memory");
+            mt = fmaxf(mt, xbuf[(sb * 2 + (hf ^ 1)) * kRows + row]);
             // keep the reference max within 2^8 of the running max
             const float new_ref = (mt > m_ref + static_cast<float>(kRescaleLog2)) ? mt : m_ref;
             const float alpha = fast_exp2(m_ref - new_ref);  // 0 from -inf, 1 if unchanged
@@ -328,37 +335,39 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
                 tc::fence_after();
                 const float f = resc ? alpha : 1.f;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < 2; ++c) {
                     uint32_t r32[32];
-                    tc::ld32(tO + lane_base + c * 32, r32);
+                    tc::ld32(tO + lane_base + col0 + c * 32, r32);
                     tc::wait_ld();
 #pragma unroll
                     for (int e = 0; e < 32; ++e) r32[e] = __float_as_uint(__uint_as_float(r32[e]) * f);
-                    tc::st32(tO + lane_base + c * 32, r32);
+                    tc::st32(tO + lane_base + col0 + c * 32, r32);
                 }
                 tc::wait_st();
             }
             m_ref = new_ref;
             const float mu = new_ref == -INFINITY ? 0.f : new_ref;
             float lsum = 0.f;
+            // chunk c (32 keys) -> 16 columns of P hi then 16 of P lo, in place
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t hi[32], lo[32];
+            for (int c = 0; c < 2; ++c) {
+                uint32_t pk[32];
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const float a = fast_exp2(s[half * 64 + 2 * e] - mu);
-                    const float b = fast_exp2(s[half * 64 + 2 * e + 1] - mu);
+                for (int e = 0; e < 16; ++e) {
+                    const float a = fast_exp2(s[c * 32 + 2 * e] - mu);
+                    const float b = fast_exp2(s[c * 32 + 2 * e + 1] - mu);
                     lsum += a + b;
-                    hi[e] = pack_bf16x2(a, b);
-                    lo[e] = pack_bf16x2(a - bf16lo_to_f32(hi[e]), b - bf16hi_to_f32(hi[e]));
+                    const uint32_t hi = pack_bf16x2(a, b);
+                    pk[e] = hi;
+                    pk[16 + e] = pack_bf16x2(a - bf16lo_to_f32(hi), b - bf16hi_to_f32(hi));
                 }
-                tc::st32(tS[sb] + lane_base + half * 32, hi);
-                tc::st32(tS[sb] + lane_base + 64 + half * 32, lo);
+                tc::st32(tS[sb] + lane_base + col0 + c * 32, pk);
             }
             l = l * (resc ? alpha : 1.f) + lsum;  // l is 0 while nothing was attended
             // value rows of keys outside [kv_lo, kv_hi) or of blocks not loaded
             // hold stale slots (possibly NaN): zero them before P.V reads them
-            const bool edge = mask != 0xffu || kbase < w.kv_lo || kbase + kKeys > w.kv_hi;
+            const int32_t tbase = (jt0 + jj) * kKeys;
+            const bool edge = mask != 0xffu || tbase < w.kv_lo || tbase + kKeys > w.kv_hi;
             if (edge) {
                 const bool landed = mbar_wait(&v_full[sb], (jj >> 1) & 1);
                 if (__any_sync(0xffffffffu, !landed)) {
@@ -366,16 +375,13 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
                     abort = true;
                     break;
                 }
-                const int kr = row;  // one key row per thread
-                const int32_t kp = kbase + kr;
+                const int kr = row;  // key row; this half zeroes its 64-dim region
+                const int32_t kp = tbase + kr;
                 if (!(kp >= w.kv_lo && kp < w.kv_hi && ((mask >> (kr >> 4)) & 1u))) {
-                    uint8_t *vs = v_s + sb * kTileBytes;
+                    uint8_t *vs = v_s + sb * kTileBytes + hf * kKVRegion + kr * 128;
 #pragma unroll
-                    for (int reg = 0; reg < 2; ++reg)
-#pragma unroll
-                        for (int c = 0; c < 8; ++c)
-                            *reinterpret_cast<uint4 *>(vs + reg * kKVRegion + kr * 128 + c * 16) =
-                                make_uint4(0, 0, 0, 0);
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<uint4 *>(vs + c * 16) = make_uint4(0, 0, 0, 0);
                 }
                 fence_proxy_async_smem();
             }
@@ -384,8 +390,11 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&p_full[sb]);
         }
-        // epilogue: O / l once the last P.V product is in
+        // epilogue: O / l once the last P.V product is in (l summed over halves)
         if (!abort) {
+            xbuf[hf * kRows + row] = l;
+            asm volatile("bar.sync 1, %0;" ::"r"(32 * kSoftmaxWarps) : "memory");
+            l += xbuf[(hf ^ 1) * kRows + row];
             const int32_t x = ntile - 1;
             const bool done = mbar_wait(&pv_done[x & 1], (x >> 1) & 1);
             if (__any_sync(0xffffffffu, !done)) {
@@ -395,11 +404,11 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
                 const float inv = l > 0.f ? 1.f / l : 0.f;
                 uint4 *dst = reinterpret_cast<uint4 *>(p.out) +
                              ((static_cast<int64_t>(__ldg(p.cu_q_lens + w.r)) + w.i0 + t) * p.hq +
-                              w.g * G + h) * (kD / 8);
+                              w.g * G + h) * (kD / 8) + hf * 8;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < 2; ++c) {
                     uint32_t r32[32];
-                    tc::ld32(tO + lane_base + c * 32, r32);
+                    tc::ld32(tO + lane_base + col0 + c * 32, r32);
                     tc::wait_ld();
                     if (valid_row) {
 #pragma unroll
