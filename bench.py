@@ -469,6 +469,36 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def run_prefill_case(args, local):
+    """Chunked prefill (4 x 512 queries vs a 16384-token prefix) timed alone."""
+    import torch
+    import block_paged_kv_gb300 as pkv
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = gen.chunked_prefill()
+
+    def up(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    kp, vp, q, kn, vn = up(w.k_pool), up(w.v_pool), up(w.q), up(w.k_new), up(w.v_new)
+    t = torch.from_numpy(w.block_tables).to(dev)
+    sl = torch.from_numpy(w.seq_lens).to(dev)
+    cu = torch.from_numpy(w.cu_q_lens).to(dev)
+    slots = torch.from_numpy(pkv.slot_mapping_host(w.block_tables, w.num_blocks, w.new_rows,
+                                                   w.new_pos, 16)).to(dev)
+    pkv.paged_kv_append(kp, vp, slots, kn, vn)
+    out = torch.empty_like(q)
+    C = int(w.cu_q_lens[1] - w.cu_q_lens[0])
+    s = time_loop(torch, lambda: pkv.paged_prefill_chunk_attention(q, cu, kp, vp, t, sl, C, 0, w.scale,
+                                                                   out=out),
+                  args.steps, args.warmup)
+    keys = sum(int(L) - C + i + 1 for L in w.seq_lens for i in range(C))
+    flops = 4 * w.head_dim * keys * w.num_q_heads
+    print(json.dumps({"case": "chunked_prefill", "workload": w.name, "us": round(s * 1e6, 2),
+                      "TFLOP/s": round(flops / s / 1e12, 1),
+                      "frac_of_bf16_peak": round(flops / s / 1e12 / bf16_peak(), 3)}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -478,6 +508,9 @@ def main():
     ap.add_argument("--no-secondary", dest="secondary", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--case", choices=["step", "prefill"], default="step",
+                    help="step: the decode step (the contract line); prefill: time the chunked "
+                         "prefill kernel alone (for profiling)")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -486,6 +519,8 @@ def main():
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         run_reference(args, rank, world)
+    elif args.case == "prefill":
+        run_prefill_case(args, local)
     else:
         run_pkv(args, rank, world, local)
 
