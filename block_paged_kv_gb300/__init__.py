@@ -79,6 +79,10 @@ _lib.pkv_profile_enable.restype = ctypes.c_int
 _lib.pkv_profile_read.argtypes = [_i32, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_double)]
 _lib.pkv_profile_read.restype = ctypes.c_int
 _lib.pkv_launch_count.restype = ctypes.c_int64
+_lib.paged_decode_attention_no_alloc.argtypes = [_vp, _i32, _PP, _vp, _i32, _vp, _i32, _i32, _i32,
+                                                 ctypes.c_float, _vp, _XP, _vp, _vp]
+_lib.paged_decode_attention_no_alloc.restype = ctypes.c_int
+NO_ALLOC_SCRATCH_BYTES = 16 << 20
 
 KERNEL_APPEND, KERNEL_DECODE_PREFIX, KERNEL_DECODE_SPLIT, KERNEL_DECODE_COMBINE, KERNEL_PREFILL = range(5)
 
@@ -86,7 +90,7 @@ EXPORTED = ["paged_kv_append", "paged_decode_workspace_size", "paged_decode_atte
             "paged_prefill_workspace_size", "paged_prefill_chunk_attention", "pkv_status_string",
             "pkv_slot_mapping_host", "pkv_prefix_groups_host", "pkv_set_decode_split_blocks",
             "pkv_decode_plan", "pkv_version", "pkv_profile_enable", "pkv_profile_read",
-            "pkv_launch_count"]
+            "pkv_launch_count", "paged_decode_attention_no_alloc"]
 
 
 class PkvError(RuntimeError):
@@ -341,3 +345,41 @@ def profile_read(kind: int) -> Tuple[int, float]:
 def launch_count() -> int:
     """Kernels launched through the library by this process."""
     return int(_lib.pkv_launch_count())
+
+
+def paged_decode_attention_no_alloc(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                                    block_tables: torch.Tensor, seq_lens: torch.Tensor,
+                                    window: int, scale: float, out: torch.Tensor,
+                                    max_seq_len: Optional[int] = None,
+                                    prefix: Optional[PrefixDesc] = None,
+                                    status: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """paged_decode_attention for callers that cannot allocate device memory.
+
+    No workspace is passed and nothing is allocated: the library's fixed
+    device scratch (``NO_ALLOC_SCRATCH_BYTES`` per GPU) is used, and ``out``
+    must be given.  Calls on one device share that scratch, so calls that may
+    overlap on the GPU must be ordered.  Sizes that need more scratch raise
+    PkvError with PKV_ERR_WORKSPACE.
+    """
+    pool = _pool(k_pool, v_pool)
+    dev = k_pool.device
+    _require(q.dim() == 3 and q.shape[2] == pool.head_dim and q.dtype == k_pool.dtype and
+             q.is_contiguous() and q.device == dev, "q is [B, Hq, D], contiguous, pool dtype")
+    B, hq, _ = q.shape
+    _i32_dev(block_tables, "block_tables", dev)
+    _i32_dev(seq_lens, "seq_lens", dev)
+    _require(block_tables.dim() == 2 and block_tables.shape[0] == B and seq_lens.shape == (B,),
+             "block_tables [B, max_blocks], seq_lens [B]")
+    _require(out.shape == q.shape and out.dtype == q.dtype and out.is_contiguous(), "out matches q")
+    width = block_tables.shape[1]
+    if max_seq_len is None:
+        max_seq_len = width * pool.block_size
+    px = ctypes.byref(prefix._c()) if prefix is not None else None
+    code = _lib.paged_decode_attention_no_alloc(
+        q.data_ptr(), hq, ctypes.byref(pool), block_tables.data_ptr(), width, seq_lens.data_ptr(),
+        B, max_seq_len, window, float(scale), out.data_ptr(), px, _ptr(status), _stream(dev))
+    if code == PKV_ERR_WORKSPACE:
+        raise PkvError("paged_decode_attention_no_alloc (request exceeds the "
+                       f"{NO_ALLOC_SCRATCH_BYTES >> 20} MiB static scratch)", code)
+    _check("paged_decode_attention_no_alloc", code)
+    return out

@@ -145,6 +145,36 @@ pkv_status paged_decode_attention(const void *q, int32_t num_q_heads, const pkv_
                                   size_t ws_bytes, const pkv_prefix_desc *prefix,
                                   int32_t *dev_status, pkv_stream_t stream);
 
+/*
+ * Allocation-free decode.  The pages have no counterpart: this entry point
+ * exists for callers that cannot allocate device memory where they call the
+ * library (a plug-in inside a framework that owns all device memory, a serving
+ * loop that bans cudaMalloc on its hot path) and so have no workspace to pass.
+ * It is paged_decode_attention with its scratch taken from a fixed array in
+ * the library's device image, PKV_NO_ALLOC_SCRATCH_BYTES long, which every GPU
+ * that loads the library holds until the process exits.
+ *   - It allocates nothing: no cudaMalloc, no cudaFree, no allocating library
+ *     routine.
+ *   - The first call on a device, with that device current, looks up the
+ *     array's device address (cudaGetSymbolAddress) and keeps it; make that
+ *     first call before any stream capture.
+ *   - Sizes whose workspace (paged_decode_workspace_size) exceeds
+ *     PKV_NO_ALLOC_SCRATCH_BYTES return PKV_ERR_WORKSPACE, nothing enqueued.
+ *   - Every call on a device shares the one array and leaves its contents
+ *     behind (nothing in it has to start at zero).  Calls that overlap on the
+ *     GPU (different streams, or different host threads without ordering)
+ *     race on it: order them.
+ * Arguments, results and the other errors are those of paged_decode_attention.
+ */
+#define PKV_NO_ALLOC_SCRATCH_BYTES (16u << 20)
+
+pkv_status paged_decode_attention_no_alloc(const void *q, int32_t num_q_heads,
+                                           const pkv_pool *pool, const int32_t *block_tables,
+                                           int32_t max_blocks_per_seq, const int32_t *seq_lens,
+                                           int32_t batch, int32_t max_seq_len, int32_t window,
+                                           float scale, void *out, const pkv_prefix_desc *prefix,
+                                           int32_t *dev_status, pkv_stream_t stream);
+
 /* Bytes of device workspace paged_prefill_chunk_attention needs. */
 size_t paged_prefill_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                     int32_t head_dim, int32_t block_size, int32_t max_q_len,
