@@ -188,6 +188,25 @@ bool encode_pool_map(CUtensorMap *map, void *base, const pkv_pool &pool)
     return r == CUDA_SUCCESS;
 }
 
+// 5-D view of the same pool for whole-tile boxes: (64 dims, slot, 64-dim
+// region, kv head, block), box (64, bs, D/64, 1, 1).  The region stride (128 B)
+// is smaller than the slot stride: the box walks dims, then slots, then
+// regions, so a (block, kv head) tile lands region by region, each region
+// [bs][64] with the 128-byte swizzle, in one load.
+bool encode_pool_map_tile(CUtensorMap *map, void *base, const pkv_pool &pool)
+{
+    const cuuint64_t D = pool.head_dim, bs = pool.block_size, hkv = pool.num_kv_heads;
+    cuuint64_t dims[5] = {64, bs, D / 64, hkv, static_cast<cuuint64_t>(pool.num_blocks)};
+    cuuint64_t strides[4] = {D * 2, 128, bs * D * 2, hkv * bs * D * 2};
+    cuuint32_t box[5] = {64, static_cast<cuuint32_t>(bs), static_cast<cuuint32_t>(D / 64), 1, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, base, dims, strides, box,
+                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 namespace pkv {
@@ -399,7 +418,8 @@ pkv_status paged_decode_attention(const void *q, int32_t num_q_heads, const pkv_
     if (pool->dtype == PKV_BF16) {
         if (!encode_fn_ready()) return PKV_ERR_CUDA;
         CUtensorMap kmap, vmap;
-        if (!encode_pool_map(&kmap, pool->k, *pool) || !encode_pool_map(&vmap, pool->v, *pool))
+        if (!encode_pool_map_tile(&kmap, pool->k, *pool) ||
+            !encode_pool_map_tile(&vmap, pool->v, *pool))
             return PKV_ERR_UNSUPPORTED;
         err = launch_decode_bf16(p, kmap, vmap, st);
     } else {

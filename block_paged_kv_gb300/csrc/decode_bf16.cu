@@ -10,9 +10,10 @@
 //       once for all of them;
 //   split item: row r, kv head g, split s -> blocks b_first + s*C .. ; its one
 //       16-row query tile holds the G q heads of (r, g).
-// K and V (block, kv head) tiles are brought into shared memory with TMA tensor
-// loads (4-D maps over [block][kv head][slot][dim], 64-dim boxes, 128-byte
-// swizzle) that complete on mbarriers.
+// K and V (block, kv head) tiles are brought into shared memory with one TMA
+// tensor load each (5-D maps viewing [block][kv head][slot][dim] as
+// (64 dims, slot, 64-dim region, kv head, block), 128-byte swizzle, so a tile
+// lands as one 2 KiB swizzled region per 64 dims) that completes on an mbarrier.
 //   split item: each of the four warps takes every fourth block of the run and
 //       keeps its own ring of stages: it issues the loads of its next blocks
 //       itself as it frees a stage, so no warp ever waits behind another;
@@ -308,13 +309,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
                 mbar_arrive_expect_tx(&full[st], C::kStageBytes);
                 uint8_t *kdst = stage_mem + st * C::kStageBytes;
                 uint8_t *vdst = kdst + C::kTileBytes;
-#pragma unroll
-                for (int reg = 0; reg < C::kRegions; ++reg) {
-                    tma_load_4d(kdst + reg * C::kRegionBytes, &kmap, &full[st], reg * 64, 0, g, bj,
-                                policy);
-                    tma_load_4d(vdst + reg * C::kRegionBytes, &vmap, &full[st], reg * 64, 0, g, bj,
-                                policy);
-                }
+                // one box per (block, kv head) tile: every 64-dim region at once
+                tma_load_5d(kdst, &kmap, &full[st], 0, 0, 0, g, bj, policy);
+                tma_load_5d(vdst, &vmap, &full[st], 0, 0, 0, g, bj, policy);
             } else {
                 report(p.status, PKV_DEV_BAD_BLOCK);
                 mbar_arrive(&full[st]);

@@ -112,8 +112,8 @@ cudaError_t launch_prefill_bf16(const PrefillParams &p, const CUtensorMap &kmap,
                                 const CUtensorMap &vmap, cudaStream_t stream);
 cudaError_t launch_prefill_f32(const PrefillParams &p, cudaStream_t stream);
 
-// bf16 pools: TMA + mbarrier pipeline, mma.sync tiles.  kmap/vmap: 4-D tensor
-// maps (head_dim, block_size, kv head, block) with 64-element boxes, 128B swizzle.
+// bf16 pools: TMA + mbarrier pipeline, mma.sync tiles.  kmap/vmap: 5-D tensor
+// maps (64 dims, slot, 64-dim region, kv head, block), whole-tile boxes, 128B swizzle.
 cudaError_t launch_decode_bf16(const DecodeParams &p, const CUtensorMap &kmap,
                                const CUtensorMap &vmap, cudaStream_t stream);
 // f32 pools: CUDA-core kernel.
