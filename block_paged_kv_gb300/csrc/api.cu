@@ -489,8 +489,8 @@ pkv_status paged_prefill_chunk_attention(const void *q, const int32_t *cu_q_lens
     cudaError_t err;
     if (pool->dtype == PKV_BF16) {
         if (!encode_fn_ready()) return PKV_ERR_CUDA;
-        CUtensorMap kmap, vmap;  // K: 64-dim boxes; V: whole-block boxes
-        if (!encode_pool_map(&kmap, pool->k, *pool) || !encode_pool_map_tile(&vmap, pool->v, *pool))
+        CUtensorMap kmap, vmap;
+        if (!encode_pool_map(&kmap, pool->k, *pool) || !encode_pool_map(&vmap, pool->v, *pool))
             return PKV_ERR_UNSUPPORTED;
         err = launch_prefill_bf16(p, kmap, vmap, st);
     } else {

@@ -8,10 +8,9 @@
 // 128 M-rows are (query, head) pairs: all G q heads of the kv head, so each
 // K/V tile is loaded once for the whole GQA group.  QK^T and PV are dense
 // contractions and run on the 5th-generation tensor cores:
-//   warps 0/10 TMA producers: K and V tiles of 128 keys (8 paged blocks;
-//             K as two 64-dim boxes per block, V as one whole-block box) into
-//             rings of 3 K and 2 V stages; a K stage is freed once S is
-//             computed, a V stage once P.V is;
+//   warps 0/6 TMA producers: K and V tiles of 128 keys (8 paged blocks, 16
+//             tensor loads each) into rings of 3 K and 2 V stages; a K stage
+//             is freed once S is computed, a V stage once P.V is;
 //   warp 1    allocates tensor memory and issues tcgen05.mma from one thread:
 //             S_j = Q K_j^T into a double-buffered S in tensor memory, then
 //             O += P_j V_j with P read from tensor memory (V MN-major);
@@ -209,17 +208,8 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             for (int b = 0; b < 8; ++b) {
                 const int32_t bid = __shfl_sync(0xffffffffu, id, b);
                 if (lane == 0 && ((mask >> b) & 1u)) {
-                    if (is_k) {
-                        // K: [64-dim half][128 keys][64] so that the S product's N
-                        // (keys) runs over uniform 8-row atoms
-                        tma_load_4d(dst + b * 2048, map, &full[st], 0, 0, w.g, bid, policy);
-                        tma_load_4d(dst + kKVRegion + b * 2048, map, &full[st], 64, 0, w.g, bid,
-                                    policy);
-                    } else {
-                        // V: one whole-block box, [block][64-dim half][16 keys][64]: each
-                        // 16-key step of P.V reads exactly one block
-                        tma_load_5d(dst + b * 4096, &vmap, &full[st], 0, 0, 0, w.g, bid, policy);
-                    }
+                    tma_load_4d(dst + b * 2048, map, &full[st], 0, 0, w.g, bid, policy);
+                    tma_load_4d(dst + kKVRegion + b * 2048, map, &full[st], 64, 0, w.g, bid, policy);
                 }
             }
         }
@@ -245,8 +235,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
                 for (int part = 0; part < 2; ++part)      // P hi, then P lo
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
-                        // block kk: halves 2 KiB apart (LBO), 8-key groups 1 KiB (SBO)
-                        const uint64_t bdesc = tc::smem_desc(v_addr + kk * 4096, 2048, 1024);
+                        const uint64_t bdesc = tc::smem_desc(v_addr + kk * 2048, kKVRegion, 1024);
                         tc::mma_ts(tO, tS[sb] + 32 * (kk >> 1) + 8 * (kk & 1) + 16 * part, bdesc,
                                    idO, (x > 0 || part > 0 || kk > 0) ? 1u : 0u);
                     }
@@ -389,7 +378,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
                 const int kr = row;  // key row; this half zeroes its 64-dim region
                 const int32_t kp = tbase + kr;
                 if (!(kp >= w.kv_lo && kp < w.kv_hi && ((mask >> (kr >> 4)) & 1u))) {
-                    uint8_t *vs = v_s + sb * kTileBytes + (kr >> 4) * 4096 + hf * 2048 + (kr & 15) * 128;
+                    uint8_t *vs = v_s + sb * kTileBytes + hf * kKVRegion + kr * 128;
 #pragma unroll
                     for (int c = 0; c < 8; ++c)
                         *reinterpret_cast<uint4 *>(vs + c * 16) = make_uint4(0, 0, 0, 0);
