@@ -4,23 +4,25 @@
 // row's chunk sits at absolute position p = L - C + i and attends positions
 // max(0, p - W + 1) .. p: the whole prefix and the chunk causally.
 //
-// bf16 kernel, one CTA per (row, kv head, tile of 128/G queries).  The tile's
-// 128 M-rows are (query, head) pairs: all G q heads of the kv head, so each
-// K/V tile is loaded once for the whole GQA group.  QK^T and PV are dense
-// contractions and run on the 5th-generation tensor cores:
-//   warps 0/6 TMA producers: K and V tiles of 128 keys (8 paged blocks, 16
-//             tensor loads each) into rings of 3 K and 2 V stages; a K stage
-//             is freed once S is computed, a V stage once P.V is;
+// bf16 kernel, one CTA per (row, kv head, two tiles of 128/G queries).  A
+// tile's 128 M-rows are (query, head) pairs of all G q heads of the kv head,
+// and both tiles share every K/V tile, so K/V are loaded once per 256 query
+// rows.  QK^T and PV are dense contractions and run on the 5th-generation
+// tensor cores:
+//   warps 0/10 TMA producers: K and V tiles of 128 keys (8 paged blocks, two
+//             64-dim boxes each) into 2-stage rings; a K stage is freed once
+//             both S products are computed, a V stage once both P.V are;
 //   warp 1    allocates tensor memory and issues tcgen05.mma from one thread:
-//             S_j = Q K_j^T into a double-buffered S in tensor memory, then
-//             O += P_j V_j with P read from tensor memory (V MN-major);
-//   warps 2-9 softmax, two threads per M-row (64 key columns each, row
-//             maxima exchanged through shared memory): S from tensor memory,
-//             causal / window / range mask, running max kept within 2^8 of the
-//             true maximum (O in tensor memory is rescaled only when it moves
-//             further), P written back over S as bf16 hi + lo terms (the P.V
-//             product then carries P to ~2^-17 relative), and the epilogue
-//             O / l to global memory.
+//             S_x = Q_x K^T into tensor memory (both operands K-major, 128-byte
+//             swizzle), then O_x += P_x V with P read from tensor memory (V
+//             MN-major), in the order PV_A(j), S_A(j+1), PV_B(j), S_B(j+1):
+//             each tile's softmax overlaps the other tile's products;
+//   warps 2-5 / 6-9 softmax of tile A / B, one thread per M-row: S from tensor
+//             memory in 32-column chunks, causal / window / range mask,
+//             running max kept within 2^8 of the true maximum (O is rescaled
+//             in tensor memory only when it moves further), P written back over
+//             S as bf16 hi + lo terms (the P.V product then carries P to
+//             ~2^-17 relative), and the epilogue O / l to global memory.
 // f32 kernel: CUDA cores, the same work split with 16 (query, head) pairs per
 // CTA, for the fp32 pools.
 #include "decode_common.cuh"
@@ -30,28 +32,28 @@ namespace pkv {
 
 namespace pf {
 constexpr int kD = 128;
-constexpr int kRows = 128;                // M
-constexpr int kKeys = 128;                // keys per tile (8 blocks of 16)
-constexpr int kQBytes = 2 * kRows * 128;  // two 64-dim swizzled regions
+constexpr int kRows = 128;                // M of one query tile
+constexpr int kQTiles = 2;                // query tiles per CTA, sharing every K/V tile
+constexpr int kKeys = 128;                // keys per K/V tile (8 blocks of 16)
+constexpr int kQBytes = kRows * 2 * 128;  // one query tile: two 64-dim swizzled regions
 constexpr int kKVRegion = kKeys * 128;    // 16 KiB
 constexpr int kTileBytes = 2 * kKVRegion; // 32 KiB: a K or a V tile
-constexpr int kKStages = 3;               // K is released as soon as S is computed
-constexpr int kVStages = 2;               // V only once P.V is done
+constexpr int kKStages = 2;
+constexpr int kVStages = 2;
 constexpr int kQOff = 0;
-constexpr int kKOff = kQOff + kQBytes;
+constexpr int kKOff = kQOff + kQTiles * kQBytes;
 constexpr int kVOff = kKOff + kKStages * kTileBytes;
 constexpr int kBarOff = kVOff + kVStages * kTileBytes;
-// barriers: k_full[3], k_empty[3], v_full[2], v_empty[2], s_full[2], p_full[2], pv_done[2]
-constexpr int kNumBars = 16;
+// barriers: k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[A,B], p_full[A,B], pv_done[A,B]
+constexpr int kNumBars = 14;
 constexpr int kMaskOff = kBarOff + kNumBars * 8;
-constexpr int kXOff = kMaskOff + kKStages * 4;       // row maxima exchanged between halves: [2][2][128]
-constexpr int kTmemOff = kXOff + 2 * 2 * kRows * 4;
+constexpr int kTmemOff = kMaskOff + kKStages * 4;
 constexpr int kBytes = kTmemOff + 16;
 constexpr int kLaunchBytes = kBytes + 1024;
-constexpr int kSoftmaxWarps = 8;          // two per tensor-memory lane quarter: 64 key columns each
-constexpr int kVWarp = 2 + kSoftmaxWarps;
-constexpr int kThreads = 32 * (kVWarp + 1);  // K producer, MMA, 8 softmax warps, V producer
-constexpr uint32_t kTmemCols = 512;       // S0, S1, O (+ spare)
+constexpr int kWGWarps = 4;               // one softmax warpgroup per query tile
+constexpr int kVWarp = 2 + kQTiles * kWGWarps;
+constexpr int kThreads = 32 * (kVWarp + 1);  // K producer, MMA, 2 softmax warpgroups, V producer
+constexpr uint32_t kTmemCols = 512;       // S_A, S_B, O_A, O_B
 constexpr uint32_t kRescaleLog2 = 8;      // O is rescaled only when the max grows past 2^8
 }  // namespace pf
 
@@ -59,7 +61,7 @@ struct PrefillRowInfo {
     int32_t r, g, i0, nq, L, C, kv_lo, kv_hi;
 };
 
-__device__ __forceinline__ bool prefill_item(const PrefillParams &p, int64_t bid, int qpt,
+__device__ __forceinline__ bool prefill_item(const PrefillParams &p, int64_t bid, int qpc,
                                              PrefillRowInfo &w)
 {
     const int32_t qt = static_cast<int32_t>(bid % p.q_tiles);
@@ -80,9 +82,9 @@ __device__ __forceinline__ bool prefill_item(const PrefillParams &p, int64_t bid
     }
     w.C = C;
     w.L = L;
-    w.i0 = qt * qpt;
+    w.i0 = qt * qpc;
     if (w.i0 >= C) return false;
-    w.nq = min(qpt, C - w.i0);
+    w.nq = min(qpc, C - w.i0);
     const int32_t p_first = L - C + w.i0;
     w.kv_hi = p_first + w.nq;
     w.kv_lo = p.window > 0 ? max(0, p_first - p.window + 1) : 0;
@@ -114,15 +116,14 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
     uint8_t *k_s = smem + kKOff;
     uint8_t *v_s = smem + kVOff;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kBarOff);
-    uint64_t *k_full = bars, *k_empty = bars + 3, *v_full = bars + 6, *v_empty = bars + 8,
-             *s_full = bars + 10, *p_full = bars + 12, *pv_done = bars + 14;
+    uint64_t *k_full = bars, *k_empty = bars + 2, *v_full = bars + 4, *v_empty = bars + 6,
+             *s_full = bars + 8, *p_full = bars + 10, *pv_done = bars + 12;
     uint32_t *kmask = reinterpret_cast<uint32_t *>(smem + kMaskOff);
-    float *xbuf = reinterpret_cast<float *>(smem + kXOff);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kTmemOff);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = p.group;
-    const int qpt = kRows / G;
+    const int qpt = kRows / G;  // queries per query tile
 
     if (threadIdx.x == 0) {
         tma_prefetch_desc(&kmap);
@@ -132,38 +133,38 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
     pdl_trigger();
 
     PrefillRowInfo w;
-    if (!prefill_item(p, blockIdx.x, qpt, w)) return;
+    if (!prefill_item(p, blockIdx.x, kQTiles * qpt, w)) return;
     const int32_t jt0 = w.kv_lo / kKeys;
     const int32_t ntile = (w.kv_hi - 1) / kKeys - jt0 + 1;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kKStages; ++i) {
-            mbar_init(&k_full[i], 1);
-            mbar_init(&k_empty[i], 1 + kSoftmaxWarps);  // the S product, and the softmax warps' read of kmask
-        }
         for (int i = 0; i < 2; ++i) {
+            mbar_init(&k_full[i], 1);
+            mbar_init(&k_empty[i], 1 + kQTiles * kWGWarps);  // both S products + the kmask reads
             mbar_init(&v_full[i], 1);
             mbar_init(&v_empty[i], 1);
             mbar_init(&s_full[i], 1);
-            mbar_init(&p_full[i], kSoftmaxWarps);
+            mbar_init(&p_full[i], kWGWarps);
             mbar_init(&pv_done[i], 1);
         }
         fence_mbar_init();
     }
     if (warp == 1) tc::alloc(tmem_slot, kTmemCols);
 
-    // query tile: row i = (query t = i / G, head h = i % G) of this kv head
-    if (warp >= 2 && warp < 6) {
-        const int i = threadIdx.x - 64;  // 128 threads, one row each
-        const int t = i / G, h = i % G;
+    // query tiles: tile x row i = (query t = x * qpt + i / G, head h = i % G)
+    if (warp >= 2 && warp < kVWarp) {
+        const int x = (warp - 2) / kWGWarps;
+        const int i = threadIdx.x - 64 - x * kRows;
+        const int t = x * qpt + i / G, h = i % G;
         const bool valid = i < qpt * G && t < w.nq;
         const uint4 *src = reinterpret_cast<const uint4 *>(p.q) +
                            ((static_cast<int64_t>(__ldg(p.cu_q_lens + w.r)) + w.i0 + t) * p.hq +
                             w.g * G + h) * (kD / 8);
+        uint8_t *qt_s = q_s + x * kQBytes;
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
             const uint4 v = valid ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4 *>(q_s + (c >> 3) * (kRows * 128) + i * 128 +
+            *reinterpret_cast<uint4 *>(qt_s + (c >> 3) * (kRows * 128) + i * 128 +
                                        (((c & 7) ^ (i & 7)) << 4)) = v;
         }
         fence_proxy_async_smem();  // read by the tensor cores (async proxy)
@@ -173,22 +174,20 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
     tc::fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t tS[2] = {tmem, tmem + 128};
-    const uint32_t tO = tmem + 256;
+    const uint32_t tO[2] = {tmem + 256, tmem + 384};
 
     if (warp == 0 || warp == kVWarp) {
         // ---------------------------------------- K (warp 0) / V (last warp) producer
         const bool is_k = warp == 0;
         const CUtensorMap *map = is_k ? &kmap : &vmap;
         uint8_t *ring = is_k ? k_s : v_s;
-        const int stages = is_k ? kKStages : kVStages;
         uint64_t *full = is_k ? k_full : v_full;
         uint64_t *empty = is_k ? k_empty : v_empty;
         const uint64_t policy = l2_evict_last_policy();  // re-read by the row's other CTAs
         const int32_t *trow = p.tables + static_cast<int64_t>(w.r) * p.width;
         for (int32_t jj = 0; jj < ntile; ++jj) {
-            const int st = jj % stages;
-            if (jj >= stages && !warp_wait(&empty[st], ((jj / stages) + 1) & 1, lane, p.status))
-                break;
+            const int st = jj & 1;
+            if (jj >= 2 && !warp_wait(&empty[st], ((jj >> 1) + 1) & 1, lane, p.status)) break;
             const int32_t kb = (jt0 + jj) * (kKeys / 16) + lane;  // logical block of lane < 8
             const bool in_range = lane < 8 && kb < p.width && kb * 16 < w.kv_hi &&
                                   (kb + 1) * 16 > w.kv_lo;
@@ -215,72 +214,93 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issue
+        // Order per K/V tile j: PV_A(j), S_A(j+1), PV_B(j), S_B(j+1).  Each
+        // warpgroup's softmax of tile j+1 runs while the tensor cores work on
+        // the other tile; the tensor cores execute in issue order, so S_x(j+1)
+        // completing also means PV_x(j) is done.
         constexpr uint32_t idS = tc::idesc_bf16(kRows, kKeys, 0, 0);
         constexpr uint32_t idO = tc::idesc_bf16(kRows, kD, 0, 1);
         const uint32_t q_addr = smem_u32(q_s);
-        bool abort = false;
-        auto pv = [&](int32_t x) {
-            const int sb = x & 1;
-            if (!warp_wait(&p_full[sb], (x >> 1) & 1, lane, p.status) ||
-                !warp_wait(&v_full[sb], (x >> 1) & 1, lane, p.status)) {
-                abort = true;
-                return;
-            }
-            tc::fence_after();
-            if (lane == 0) {
-                const uint32_t v_addr = smem_u32(v_s + sb * kTileBytes);
-                // keys 32c..32c+31 hold P hi in S columns 32c..32c+15 and P lo
-                // in 32c+16..32c+31 (bf16 pairs, 8 columns per 16 keys)
+        auto s_mma = [&](int x, int32_t jj) {  // lane 0
+            const uint32_t k_addr = smem_u32(k_s + (jj & 1) * kTileBytes);
+            const uint32_t qa = q_addr + x * kQBytes;
 #pragma unroll
-                for (int part = 0; part < 2; ++part)      // P hi, then P lo
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint64_t bdesc = tc::smem_desc(v_addr + kk * 2048, kKVRegion, 1024);
-                        tc::mma_ts(tO, tS[sb] + 32 * (kk >> 1) + 8 * (kk & 1) + 16 * part, bdesc,
-                                   idO, (x > 0 || part > 0 || kk > 0) ? 1u : 0u);
-                    }
-                tc::commit(&v_empty[sb]);
-                tc::commit(&pv_done[sb]);
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t off = (kk >> 2) * kKVRegion + (kk & 3) * 32;
+                tc::mma_ss(tS[x], tc::smem_desc(qa + off, 16, 1024),
+                           tc::smem_desc(k_addr + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
             }
-            __syncwarp();
+            tc::commit(&s_full[x]);
         };
-        for (int32_t jj = 0; jj < ntile && !abort; ++jj) {
-            const int ks = jj % kKStages, sb = jj & 1;
-            if (!warp_wait(&k_full[ks], (jj / kKStages) & 1, lane, p.status)) break;
-            tc::fence_after();
-            if (lane == 0) {
-                const uint32_t k_addr = smem_u32(k_s + ks * kTileBytes);
+        auto pv_mma = [&](int x, int32_t jj) {  // lane 0
+            const uint32_t v_addr = smem_u32(v_s + (jj & 1) * kTileBytes);
+            // keys 32c..32c+31 hold P hi in S columns 32c..32c+15 and P lo in
+            // 32c+16..32c+31 (bf16 pairs, 8 columns per 16 keys)
+#pragma unroll
+            for (int part = 0; part < 2; ++part)
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t off = (kk >> 2) * kKVRegion + (kk & 3) * 32;
-                    tc::mma_ss(tS[sb], tc::smem_desc(q_addr + off, 16, 1024),
-                               tc::smem_desc(k_addr + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
+                    const uint64_t bdesc = tc::smem_desc(v_addr + kk * 2048, kKVRegion, 1024);
+                    tc::mma_ts(tO[x], tS[x] + 32 * (kk >> 1) + 8 * (kk & 1) + 16 * part, bdesc,
+                               idO, (jj > 0 || part > 0 || kk > 0) ? 1u : 0u);
                 }
-                tc::commit(&s_full[sb]);
-                tc::commit(&k_empty[ks]);
+            tc::commit(&pv_done[x]);
+        };
+        bool ok = warp_wait(&k_full[0], 0, lane, p.status);
+        if (ok) {
+            tc::fence_after();
+            if (lane == 0) {
+                s_mma(0, 0);
+                s_mma(1, 0);
+                tc::commit(&k_empty[0]);
             }
             __syncwarp();
-            if (jj >= 1) pv(jj - 1);
         }
-        if (!abort) pv(ntile - 1);
+        for (int32_t jj = 0; jj < ntile && ok; ++jj) {
+            const bool more = jj + 1 < ntile;
+            ok = warp_wait(&p_full[0], jj & 1, lane, p.status) &&
+                 warp_wait(&v_full[jj & 1], (jj >> 1) & 1, lane, p.status);
+            if (!ok) break;
+            tc::fence_after();
+            if (lane == 0) pv_mma(0, jj);
+            __syncwarp();
+            if (more) {
+                ok = warp_wait(&k_full[(jj + 1) & 1], ((jj + 1) >> 1) & 1, lane, p.status);
+                if (!ok) break;
+                tc::fence_after();
+                if (lane == 0) s_mma(0, jj + 1);
+                __syncwarp();
+            }
+            ok = warp_wait(&p_full[1], jj & 1, lane, p.status);
+            if (!ok) break;
+            tc::fence_after();
+            if (lane == 0) {
+                pv_mma(1, jj);
+                tc::commit(&v_empty[jj & 1]);
+                if (more) {
+                    s_mma(1, jj + 1);
+                    tc::commit(&k_empty[(jj + 1) & 1]);
+                }
+            }
+            __syncwarp();
+        }
     } else {
         // ------------------------------------------------------------ softmax
-        // warps 2..9: lane quarter q = warp % 4 (rows 32q..32q+31), key half
-        // hf: columns 64hf..64hf+63 of S (and of O)
-        const int hf = (warp - 2) >> 2;
+        // warpgroup x = query tile x; warp w%4 = lane quarter (rows 32q..32q+31)
+        const int x = (warp - 2) / kWGWarps;
         const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
         const int row = 32 * (warp & 3) + lane;  // tensor-memory lane of this thread = M-row
-        const uint32_t col0 = 64 * hf;
-        const int t = row / G, h = row % G;
+        const int t = x * qpt + row / G, h = row % G;
         const bool valid_row = row < qpt * G && t < w.nq;
         const int32_t qpos = w.L - w.C + w.i0 + t;
         const int32_t qlo = p.window > 0 ? max(0, qpos - p.window + 1) : 0;
+        const uint32_t sx = tS[x] + lane_base, ox = tO[x] + lane_base;
         float m_ref = -INFINITY, l = 0.f;
         bool abort = false;
         for (int32_t jj = 0; jj < ntile; ++jj) {
-            const int sb = jj & 1, ks = jj % kKStages;
-            bool got = mbar_wait(&s_full[sb], (jj >> 1) & 1);
-            got = got && mbar_wait(&k_full[ks], (jj / kKStages) & 1);  // for kmask
+            const int ks = jj & 1;
+            bool got = mbar_wait(&s_full[x], jj & 1);
+            got = got && mbar_wait(&k_full[ks], (jj >> 1) & 1);  // for kmask
             if (__any_sync(0xffffffffu, !got)) {
                 if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
                 abort = true;
@@ -290,113 +310,103 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&k_empty[ks]);
             tc::fence_after();
-            float s[64];
-            {
-                uint32_t r0[32], r1[32];
-                tc::ld32(tS[sb] + lane_base + col0, r0);
-                tc::ld32(tS[sb] + lane_base + col0 + 32, r1);
+            const int32_t kbase = (jt0 + jj) * kKeys;
+            const bool full = mask == 0xffu && kbase >= qlo && kbase + kKeys - 1 <= qpos && valid_row;
+            // pass 1: the tile's row maximum (scaled, masked)
+            float mt = -INFINITY;
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t r32[32];
+                tc::ld32(sx + c * 32, r32);
                 tc::wait_ld();
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
-                    s[e] = __uint_as_float(r0[e]) * p.scale_log2;
-                    s[32 + e] = __uint_as_float(r1[e]) * p.scale_log2;
+                    const int32_t kp = kbase + c * 32 + e;
+                    const bool ok = full || (valid_row && kp >= qlo && kp <= qpos &&
+                                             ((mask >> ((c * 32 + e) >> 4)) & 1u));
+                    if (ok) mt = fmaxf(mt, __uint_as_float(r32[e]) * p.scale_log2);
                 }
             }
-            const int32_t kbase = (jt0 + jj) * kKeys + static_cast<int32_t>(col0);
-            const uint32_t hmask = (mask >> (4 * hf)) & 0xfu;  // blocks of this half
-            const bool full = hmask == 0xfu && kbase >= qlo && kbase + 63 <= qpos && valid_row;
-            if (!full) {
-#pragma unroll
-                for (int c = 0; c < 64; ++c) {
-                    const int32_t kp = kbase + c;
-                    const bool ok = valid_row && kp >= qlo && kp <= qpos && ((hmask >> (c >> 4)) & 1u);
-                    if (!ok) s[c] = -INFINITY;
-                }
-            }
-            float mt = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < 64; ++c) mt = fmaxf(mt, s[c]);
-            // row maximum over both halves
-            xbuf[(sb * 2 + hf) * kRows + row] = mt;
-            asm volatile("bar.sync 1, %0;" ::"r"(32 * kSoftmaxWarps) : "memory");
-            mt = fmaxf(mt, xbuf[(sb * 2 + (hf ^ 1)) * kRows + row]);
             // keep the reference max within 2^8 of the running max
             const float new_ref = (mt > m_ref + static_cast<float>(kRescaleLog2)) ? mt : m_ref;
             const float alpha = fast_exp2(m_ref - new_ref);  // 0 from -inf, 1 if unchanged
             const bool resc = new_ref != m_ref && m_ref != -INFINITY;
-            if (jj > 0 && __any_sync(0xffffffffu, resc)) {
-                // O holds the P.V products up to tile jj-1: wait for the last one
-                const bool done = mbar_wait(&pv_done[(jj - 1) & 1], ((jj - 1) >> 1) & 1);
-                if (__any_sync(0xffffffffu, !done)) {
-                    if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
-                    abort = true;
-                    break;
-                }
-                tc::fence_after();
+            if (__any_sync(0xffffffffu, resc)) {
+                // O_x holds the products up to tile jj-1; S_x(jj) was issued after
+                // them, so they are complete
                 const float f = resc ? alpha : 1.f;
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
                     uint32_t r32[32];
-                    tc::ld32(tO + lane_base + col0 + c * 32, r32);
+                    tc::ld32(ox + c * 32, r32);
                     tc::wait_ld();
 #pragma unroll
                     for (int e = 0; e < 32; ++e) r32[e] = __float_as_uint(__uint_as_float(r32[e]) * f);
-                    tc::st32(tO + lane_base + col0 + c * 32, r32);
+                    tc::st32(ox + c * 32, r32);
                 }
                 tc::wait_st();
             }
             m_ref = new_ref;
             const float mu = new_ref == -INFINITY ? 0.f : new_ref;
+            // pass 2: P = 2^(s - m) as bf16 hi + lo, written over S chunk by chunk
             float lsum = 0.f;
-            // chunk c (32 keys) -> 16 columns of P hi then 16 of P lo, in place
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t r32[32];
+                tc::ld32(sx + c * 32, r32);
+                tc::wait_ld();
                 uint32_t pk[32];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    const float a = fast_exp2(s[c * 32 + 2 * e] - mu);
-                    const float b = fast_exp2(s[c * 32 + 2 * e + 1] - mu);
+                    float a = 0.f, b = 0.f;
+                    const int32_t kp = kbase + c * 32 + 2 * e;
+                    const bool ok0 = full || (valid_row && kp >= qlo && kp <= qpos &&
+                                              ((mask >> ((c * 32 + 2 * e) >> 4)) & 1u));
+                    const bool ok1 = full || (valid_row && kp + 1 >= qlo && kp + 1 <= qpos &&
+                                              ((mask >> ((c * 32 + 2 * e + 1) >> 4)) & 1u));
+                    if (ok0) a = fast_exp2(fmaf(__uint_as_float(r32[2 * e]), p.scale_log2, -mu));
+                    if (ok1) b = fast_exp2(fmaf(__uint_as_float(r32[2 * e + 1]), p.scale_log2, -mu));
                     lsum += a + b;
                     const uint32_t hi = pack_bf16x2(a, b);
                     pk[e] = hi;
                     pk[16 + e] = pack_bf16x2(a - bf16lo_to_f32(hi), b - bf16hi_to_f32(hi));
                 }
-                tc::st32(tS[sb] + lane_base + col0 + c * 32, pk);
+                tc::st32(sx + c * 32, pk);
             }
             l = l * (resc ? alpha : 1.f) + lsum;  // l is 0 while nothing was attended
             // value rows of keys outside [kv_lo, kv_hi) or of blocks not loaded
-            // hold stale slots (possibly NaN): zero them before P.V reads them
-            const int32_t tbase = (jt0 + jj) * kKeys;
-            const bool edge = mask != 0xffu || tbase < w.kv_lo || tbase + kKeys > w.kv_hi;
-            if (edge) {
-                const bool landed = mbar_wait(&v_full[sb], (jj >> 1) & 1);
+            // hold stale slots (possibly NaN): warpgroup A zeroes them before
+            // either P.V product reads them
+            const bool edge = mask != 0xffu || kbase < w.kv_lo || kbase + kKeys > w.kv_hi;
+            if (x == 0 && edge) {
+                const bool landed = mbar_wait(&v_full[ks], (jj >> 1) & 1);
                 if (__any_sync(0xffffffffu, !landed)) {
                     if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
                     abort = true;
                     break;
                 }
-                const int kr = row;  // key row; this half zeroes its 64-dim region
-                const int32_t kp = tbase + kr;
+                const int kr = row;  // one key row per thread
+                const int32_t kp = kbase + kr;
                 if (!(kp >= w.kv_lo && kp < w.kv_hi && ((mask >> (kr >> 4)) & 1u))) {
-                    uint8_t *vs = v_s + sb * kTileBytes + hf * kKVRegion + kr * 128;
+                    uint8_t *vs = v_s + ks * kTileBytes + kr * 128;
 #pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        *reinterpret_cast<uint4 *>(vs + c * 16) = make_uint4(0, 0, 0, 0);
+                    for (int reg = 0; reg < 2; ++reg)
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            *reinterpret_cast<uint4 *>(vs + reg * kKVRegion + c * 16) =
+                                make_uint4(0, 0, 0, 0);
                 }
                 fence_proxy_async_smem();
             }
             tc::wait_st();
             tc::fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&p_full[sb]);
+            if (lane == 0) mbar_arrive(&p_full[x]);
         }
-        // epilogue: O / l once the last P.V product is in (l summed over halves)
+        // epilogue: O / l once the last P.V product of this tile is in
         if (!abort) {
-            xbuf[hf * kRows + row] = l;
-            asm volatile("bar.sync 1, %0;" ::"r"(32 * kSoftmaxWarps) : "memory");
-            l += xbuf[(hf ^ 1) * kRows + row];
-            const int32_t x = ntile - 1;
-            const bool done = mbar_wait(&pv_done[x & 1], (x >> 1) & 1);
+            const int32_t last = ntile - 1;
+            const bool done = mbar_wait(&pv_done[x], last & 1);
             if (__any_sync(0xffffffffu, !done)) {
                 if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
             } else {
@@ -404,11 +414,11 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
                 const float inv = l > 0.f ? 1.f / l : 0.f;
                 uint4 *dst = reinterpret_cast<uint4 *>(p.out) +
                              ((static_cast<int64_t>(__ldg(p.cu_q_lens + w.r)) + w.i0 + t) * p.hq +
-                              w.g * G + h) * (kD / 8) + hf * 8;
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {
+                              w.g * G + h) * (kD / 8);
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
                     uint32_t r32[32];
-                    tc::ld32(tO + lane_base + col0 + c * 32, r32);
+                    tc::ld32(ox + c * 32, r32);
                     tc::wait_ld();
                     if (valid_row) {
 #pragma unroll
@@ -548,7 +558,7 @@ bool prefill_shape_built(pkv_dtype dtype, int32_t D, int32_t bs, int32_t G)
 
 int32_t prefill_queries_per_cta(pkv_dtype dtype, int32_t G)
 {
-    return dtype == PKV_BF16 ? pf::kRows / G : kPf32Pairs / G;
+    return dtype == PKV_BF16 ? pf::kQTiles * (pf::kRows / G) : kPf32Pairs / G;
 }
 
 cudaError_t launch_prefill_bf16(const PrefillParams &p, const CUtensorMap &kmap,
