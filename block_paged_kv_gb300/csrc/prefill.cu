@@ -17,8 +17,9 @@
 //             swizzle), then O_x += P_x V with P read from tensor memory (V
 //             MN-major), in the order PV_A(j), S_A(j+1), PV_B(j), S_B(j+1):
 //             each tile's softmax overlaps the other tile's products;
-//   warps 2-5 / 6-9 softmax of tile A / B, one thread per M-row: S from tensor
-//             memory in 32-column chunks, causal / window / range mask,
+//   warps 2-9 softmax, tile A then tile B of every K/V tile, two threads per
+//             M-row (64 key columns each, row maxima exchanged through shared
+//             memory): S from tensor memory, causal / window / range mask,
 //             running max kept within 2^8 of the true maximum (O is rescaled
 //             in tensor memory only when it moves further), P written back over
 //             S as bf16 hi + lo terms (the P.V product then carries P to
@@ -47,12 +48,13 @@ constexpr int kBarOff = kVOff + kVStages * kTileBytes;
 // barriers: k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[A,B], p_full[A,B], pv_done[A,B]
 constexpr int kNumBars = 14;
 constexpr int kMaskOff = kBarOff + kNumBars * 8;
-constexpr int kTmemOff = kMaskOff + kKStages * 4;
+constexpr int kXOff = kMaskOff + kKStages * 4;  // row maxima exchanged between halves: [2][2][128]
+constexpr int kTmemOff = kXOff + 2 * 2 * kRows * 4;
 constexpr int kBytes = kTmemOff + 16;
 constexpr int kLaunchBytes = kBytes + 1024;
-constexpr int kWGWarps = 4;               // one softmax warpgroup per query tile
-constexpr int kVWarp = 2 + kQTiles * kWGWarps;
-constexpr int kThreads = 32 * (kVWarp + 1);  // K producer, MMA, 2 softmax warpgroups, V producer
+constexpr int kSoftmaxWarps = 8;          // two per tensor-memory lane quarter: 64 columns each
+constexpr int kVWarp = 2 + kSoftmaxWarps;
+constexpr int kThreads = 32 * (kVWarp + 1);  // K producer, MMA, 8 softmax warps, V producer
 constexpr uint32_t kTmemCols = 512;       // S_A, S_B, O_A, O_B
 constexpr uint32_t kRescaleLog2 = 8;      // O is rescaled only when the max grows past 2^8
 }  // namespace pf
@@ -119,6 +121,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
     uint64_t *k_full = bars, *k_empty = bars + 2, *v_full = bars + 4, *v_empty = bars + 6,
              *s_full = bars + 8, *p_full = bars + 10, *pv_done = bars + 12;
     uint32_t *kmask = reinterpret_cast<uint32_t *>(smem + kMaskOff);
+    float *xbuf = reinterpret_cast<float *>(smem + kXOff);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kTmemOff);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -140,21 +143,22 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < 2; ++i) {
             mbar_init(&k_full[i], 1);
-            mbar_init(&k_empty[i], 1 + kQTiles * kWGWarps);  // both S products + the kmask reads
+            mbar_init(&k_empty[i], 1 + kSoftmaxWarps);  // both S products + the kmask reads
             mbar_init(&v_full[i], 1);
             mbar_init(&v_empty[i], 1);
             mbar_init(&s_full[i], 1);
-            mbar_init(&p_full[i], kWGWarps);
+            mbar_init(&p_full[i], kSoftmaxWarps);
             mbar_init(&pv_done[i], 1);
         }
         fence_mbar_init();
     }
     if (warp == 1) tc::alloc(tmem_slot, kTmemCols);
 
-    // query tiles: tile x row i = (query t = x * qpt + i / G, head h = i % G)
+    // query tiles: tile x row i = (query t = x * qpt + i / G, head h = i % G);
+    // the 256 softmax threads load one row each
     if (warp >= 2 && warp < kVWarp) {
-        const int x = (warp - 2) / kWGWarps;
-        const int i = threadIdx.x - 64 - x * kRows;
+        const int ii = threadIdx.x - 64;
+        const int x = ii / kRows, i = ii % kRows;
         const int t = x * qpt + i / G, h = i % G;
         const bool valid = i < qpt * G && t < w.nq;
         const uint4 *src = reinterpret_cast<const uint4 *>(p.q) +
@@ -173,8 +177,9 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tS[2] = {tmem, tmem + 128};
-    const uint32_t tO[2] = {tmem + 256, tmem + 384};
+    // tensor memory: S_x at columns 128x, O_x at 256 + 128x
+    auto tS = [&](int x) { return tmem + 128u * static_cast<uint32_t>(x); };
+    auto tO = [&](int x) { return tmem + 256u + 128u * static_cast<uint32_t>(x); };
 
     if (warp == 0 || warp == kVWarp) {
         // ---------------------------------------- K (warp 0) / V (last warp) producer
@@ -227,7 +232,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
                 const uint32_t off = (kk >> 2) * kKVRegion + (kk & 3) * 32;
-                tc::mma_ss(tS[x], tc::smem_desc(qa + off, 16, 1024),
+                tc::mma_ss(tS(x), tc::smem_desc(qa + off, 16, 1024),
                            tc::smem_desc(k_addr + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
             }
             tc::commit(&s_full[x]);
@@ -241,7 +246,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint64_t bdesc = tc::smem_desc(v_addr + kk * 2048, kKVRegion, 1024);
-                    tc::mma_ts(tO[x], tS[x] + 32 * (kk >> 1) + 8 * (kk & 1) + 16 * part, bdesc,
+                    tc::mma_ts(tO(x), tS(x) + 32 * (kk >> 1) + 8 * (kk & 1) + 16 * part, bdesc,
                                idO, (jj > 0 || part > 0 || kk > 0) ? 1u : 0u);
                 }
             tc::commit(&pv_done[x]);
@@ -286,150 +291,177 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ softmax
-        // warpgroup x = query tile x; warp w%4 = lane quarter (rows 32q..32q+31)
-        const int x = (warp - 2) / kWGWarps;
+        // warps 2..9, for tile A then tile B of every K/V tile: lane quarter
+        // q = warp % 4 (rows 32q..32q+31), key half hf = columns 64hf..64hf+63
+        // of S (and of O); the two halves of a row exchange maxima in smem
+        const int hf = (warp - 2) >> 2;
         const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
         const int row = 32 * (warp & 3) + lane;  // tensor-memory lane of this thread = M-row
-        const int t = x * qpt + row / G, h = row % G;
-        const bool valid_row = row < qpt * G && t < w.nq;
-        const int32_t qpos = w.L - w.C + w.i0 + t;
-        const int32_t qlo = p.window > 0 ? max(0, qpos - p.window + 1) : 0;
-        const uint32_t sx = tS[x] + lane_base, ox = tO[x] + lane_base;
-        float m_ref = -INFINITY, l = 0.f;
+        const uint32_t col0 = 64 * hf;
+        // per-tile row state kept in scalars (selected by tile, no local arrays)
+        const int t0 = row / G, t1 = qpt + row / G;
+        const bool vr0 = row < qpt * G && t0 < w.nq, vr1 = row < qpt * G && t1 < w.nq;
+        const int32_t qp0 = w.L - w.C + w.i0 + t0, qp1 = w.L - w.C + w.i0 + t1;
+        const int32_t ql0 = p.window > 0 ? max(0, qp0 - p.window + 1) : 0;
+        const int32_t ql1 = p.window > 0 ? max(0, qp1 - p.window + 1) : 0;
+        float mr0 = -INFINITY, mr1 = -INFINITY, l0 = 0.f, l1 = 0.f;
         bool abort = false;
-        for (int32_t jj = 0; jj < ntile; ++jj) {
+        for (int32_t jj = 0; jj < ntile && !abort; ++jj) {
             const int ks = jj & 1;
-            bool got = mbar_wait(&s_full[x], jj & 1);
-            got = got && mbar_wait(&k_full[ks], (jj >> 1) & 1);  // for kmask
-            if (__any_sync(0xffffffffu, !got)) {
-                if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
-                abort = true;
-                break;
-            }
-            const uint32_t mask = kmask[ks];
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&k_empty[ks]);
-            tc::fence_after();
-            const int32_t kbase = (jt0 + jj) * kKeys;
-            const bool full = mask == 0xffu && kbase >= qlo && kbase + kKeys - 1 <= qpos && valid_row;
-            // pass 1: the tile's row maximum (scaled, masked)
-            float mt = -INFINITY;
+            const int32_t tbase = (jt0 + jj) * kKeys;
+            const int32_t kbase = tbase + static_cast<int32_t>(col0);
+            uint32_t mask = 0;
 #pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-                uint32_t r32[32];
-                tc::ld32(sx + c * 32, r32);
-                tc::wait_ld();
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int32_t kp = kbase + c * 32 + e;
-                    const bool ok = full || (valid_row && kp >= qlo && kp <= qpos &&
-                                             ((mask >> ((c * 32 + e) >> 4)) & 1u));
-                    if (ok) mt = fmaxf(mt, __uint_as_float(r32[e]) * p.scale_log2);
-                }
-            }
-            // keep the reference max within 2^8 of the running max
-            const float new_ref = (mt > m_ref + static_cast<float>(kRescaleLog2)) ? mt : m_ref;
-            const float alpha = fast_exp2(m_ref - new_ref);  // 0 from -inf, 1 if unchanged
-            const bool resc = new_ref != m_ref && m_ref != -INFINITY;
-            if (__any_sync(0xffffffffu, resc)) {
-                // O_x holds the products up to tile jj-1; S_x(jj) was issued after
-                // them, so they are complete
-                const float f = resc ? alpha : 1.f;
-#pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t r32[32];
-                    tc::ld32(ox + c * 32, r32);
-                    tc::wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) r32[e] = __float_as_uint(__uint_as_float(r32[e]) * f);
-                    tc::st32(ox + c * 32, r32);
-                }
-                tc::wait_st();
-            }
-            m_ref = new_ref;
-            const float mu = new_ref == -INFINITY ? 0.f : new_ref;
-            // pass 2: P = 2^(s - m) as bf16 hi + lo, written over S chunk by chunk
-            float lsum = 0.f;
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-                uint32_t r32[32];
-                tc::ld32(sx + c * 32, r32);
-                tc::wait_ld();
-                uint32_t pk[32];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    float a = 0.f, b = 0.f;
-                    const int32_t kp = kbase + c * 32 + 2 * e;
-                    const bool ok0 = full || (valid_row && kp >= qlo && kp <= qpos &&
-                                              ((mask >> ((c * 32 + 2 * e) >> 4)) & 1u));
-                    const bool ok1 = full || (valid_row && kp + 1 >= qlo && kp + 1 <= qpos &&
-                                              ((mask >> ((c * 32 + 2 * e + 1) >> 4)) & 1u));
-                    if (ok0) a = fast_exp2(fmaf(__uint_as_float(r32[2 * e]), p.scale_log2, -mu));
-                    if (ok1) b = fast_exp2(fmaf(__uint_as_float(r32[2 * e + 1]), p.scale_log2, -mu));
-                    lsum += a + b;
-                    const uint32_t hi = pack_bf16x2(a, b);
-                    pk[e] = hi;
-                    pk[16 + e] = pack_bf16x2(a - bf16lo_to_f32(hi), b - bf16hi_to_f32(hi));
-                }
-                tc::st32(sx + c * 32, pk);
-            }
-            l = l * (resc ? alpha : 1.f) + lsum;  // l is 0 while nothing was attended
-            // value rows of keys outside [kv_lo, kv_hi) or of blocks not loaded
-            // hold stale slots (possibly NaN): warpgroup A zeroes them before
-            // either P.V product reads them
-            const bool edge = mask != 0xffu || kbase < w.kv_lo || kbase + kKeys > w.kv_hi;
-            if (x == 0 && edge) {
-                const bool landed = mbar_wait(&v_full[ks], (jj >> 1) & 1);
-                if (__any_sync(0xffffffffu, !landed)) {
+            for (int x = 0; x < kQTiles; ++x) {
+                bool got = mbar_wait(&s_full[x], jj & 1);
+                if (x == 0) got = got && mbar_wait(&k_full[ks], (jj >> 1) & 1);  // for kmask
+                if (__any_sync(0xffffffffu, !got)) {
                     if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
                     abort = true;
                     break;
                 }
-                const int kr = row;  // one key row per thread
-                const int32_t kp = kbase + kr;
-                if (!(kp >= w.kv_lo && kp < w.kv_hi && ((mask >> (kr >> 4)) & 1u))) {
-                    uint8_t *vs = v_s + ks * kTileBytes + kr * 128;
+                if (x == 0) {
+                    mask = kmask[ks];
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&k_empty[ks]);
+                }
+                tc::fence_after();
+                const uint32_t sx = tS(x) + lane_base + col0, ox = tO(x) + lane_base + col0;
+                const bool valid_row = x ? vr1 : vr0;
+                const int32_t qpos = x ? qp1 : qp0, qlo = x ? ql1 : ql0;
+                const float m_ref = x ? mr1 : mr0;
+                float s[64];
+                {
+                    uint32_t r0[32], r1[32];
+                    tc::ld32(sx, r0);
+                    tc::ld32(sx + 32, r1);
+                    tc::wait_ld();
 #pragma unroll
-                    for (int reg = 0; reg < 2; ++reg)
+                    for (int e = 0; e < 32; ++e) {
+                        s[e] = __uint_as_float(r0[e]) * p.scale_log2;
+                        s[32 + e] = __uint_as_float(r1[e]) * p.scale_log2;
+                    }
+                }
+                const uint32_t hmask = (mask >> (4 * hf)) & 0xfu;  // blocks of this half
+                const bool full = hmask == 0xfu && kbase >= qlo && kbase + 63 <= qpos && valid_row;
+                if (!full) {
+#pragma unroll
+                    for (int c = 0; c < 64; ++c) {
+                        const int32_t kp = kbase + c;
+                        const bool ok = valid_row && kp >= qlo && kp <= qpos &&
+                                        ((hmask >> (c >> 4)) & 1u);
+                        if (!ok) s[c] = -INFINITY;
+                    }
+                }
+                float mt = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < 64; ++c) mt = fmaxf(mt, s[c]);
+                // row maximum over both halves (double-buffered by tile parity)
+                const int xb = (jj & 1) * 2 + x;
+                xbuf[(xb * 2 + hf) * kRows + row] = mt;
+                asm volatile("bar.sync 1, %0;" ::"r"(32 * kSoftmaxWarps) : "memory");
+                mt = fmaxf(mt, xbuf[(xb * 2 + (hf ^ 1)) * kRows + row]);
+                // keep the reference max within 2^8 of the running max
+                const float new_ref = (mt > m_ref + static_cast<float>(kRescaleLog2)) ? mt : m_ref;
+                const float alpha = fast_exp2(m_ref - new_ref);  // 0 from -inf, 1 if unchanged
+                const bool resc = new_ref != m_ref && m_ref != -INFINITY;
+                if (__any_sync(0xffffffffu, resc)) {
+                    // O_x holds the products up to tile jj-1; S_x(jj) was issued
+                    // after them, so they are complete
+                    const float f = resc ? alpha : 1.f;
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        uint32_t r32[32];
+                        tc::ld32(ox + c * 32, r32);
+                        tc::wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) r32[e] = __float_as_uint(__uint_as_float(r32[e]) * f);
+                        tc::st32(ox + c * 32, r32);
+                    }
+                    tc::wait_st();
+                }
+                if (x) mr1 = new_ref; else mr0 = new_ref;
+                const float mu = new_ref == -INFINITY ? 0.f : new_ref;
+                float lsum = 0.f;
+                // chunk c (32 keys) -> 16 columns of P hi then 16 of P lo, in place
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const float a = fast_exp2(s[c * 32 + 2 * e] - mu);
+                        const float b = fast_exp2(s[c * 32 + 2 * e + 1] - mu);
+                        lsum += a + b;
+                        const uint32_t hi = pack_bf16x2(a, b);
+                        pk[e] = hi;
+                        pk[16 + e] = pack_bf16x2(a - bf16lo_to_f32(hi), b - bf16hi_to_f32(hi));
+                    }
+                    tc::st32(sx + c * 32, pk);
+                }
+                const float lnew = (x ? l1 : l0) * (resc ? alpha : 1.f) + lsum;  // 0 while nothing attended
+                if (x) l1 = lnew; else l0 = lnew;
+                // value rows of keys outside [kv_lo, kv_hi) or of blocks not
+                // loaded hold stale slots (possibly NaN): zero them during tile
+                // A, before either P.V product reads them
+                const bool edge = mask != 0xffu || tbase < w.kv_lo || tbase + kKeys > w.kv_hi;
+                if (x == 0 && edge) {
+                    const bool landed = mbar_wait(&v_full[ks], (jj >> 1) & 1);
+                    if (__any_sync(0xffffffffu, !landed)) {
+                        if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
+                        abort = true;
+                        break;
+                    }
+                    const int kr = row;  // key row; this half zeroes its 64-dim region
+                    const int32_t kp = tbase + kr;
+                    if (!(kp >= w.kv_lo && kp < w.kv_hi && ((mask >> (kr >> 4)) & 1u))) {
+                        uint8_t *vs = v_s + ks * kTileBytes + hf * kKVRegion + kr * 128;
 #pragma unroll
                         for (int c = 0; c < 8; ++c)
-                            *reinterpret_cast<uint4 *>(vs + reg * kKVRegion + c * 16) =
-                                make_uint4(0, 0, 0, 0);
+                            *reinterpret_cast<uint4 *>(vs + c * 16) = make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
                 }
-                fence_proxy_async_smem();
+                tc::wait_st();
+                tc::fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&p_full[x]);
             }
-            tc::wait_st();
-            tc::fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&p_full[x]);
         }
-        // epilogue: O / l once the last P.V product of this tile is in
-        if (!abort) {
+        // epilogue per tile: O / l once its last P.V product is in (l summed
+        // over the two halves)
+#pragma unroll 1
+        for (int x = 0; x < kQTiles && !abort; ++x) {
+            const float lx = x ? l1 : l0;
+            xbuf[(x * 2 + hf) * kRows + row] = lx;
+            asm volatile("bar.sync 1, %0;" ::"r"(32 * kSoftmaxWarps) : "memory");
+            const float lt = lx + xbuf[(x * 2 + (hf ^ 1)) * kRows + row];
             const int32_t last = ntile - 1;
             const bool done = mbar_wait(&pv_done[x], last & 1);
             if (__any_sync(0xffffffffu, !done)) {
                 if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
-            } else {
-                tc::fence_after();
-                const float inv = l > 0.f ? 1.f / l : 0.f;
-                uint4 *dst = reinterpret_cast<uint4 *>(p.out) +
-                             ((static_cast<int64_t>(__ldg(p.cu_q_lens + w.r)) + w.i0 + t) * p.hq +
-                              w.g * G + h) * (kD / 8);
-#pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t r32[32];
-                    tc::ld32(ox + c * 32, r32);
-                    tc::wait_ld();
-                    if (valid_row) {
+                continue;
+            }
+            tc::fence_after();
+            const float inv = lt > 0.f ? 1.f / lt : 0.f;
+            const int t = x * qpt + row / G, h = row % G;
+            uint4 *dst = reinterpret_cast<uint4 *>(p.out) +
+                         ((static_cast<int64_t>(__ldg(p.cu_q_lens + w.r)) + w.i0 + t) * p.hq +
+                          w.g * G + h) * (kD / 8) + hf * 8;
+            const uint32_t ox = tO(x) + lane_base + col0;
 #pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            uint4 o;
-                            o.x = pack_bf16x2(__uint_as_float(r32[8 * v + 0]) * inv, __uint_as_float(r32[8 * v + 1]) * inv);
-                            o.y = pack_bf16x2(__uint_as_float(r32[8 * v + 2]) * inv, __uint_as_float(r32[8 * v + 3]) * inv);
-                            o.z = pack_bf16x2(__uint_as_float(r32[8 * v + 4]) * inv, __uint_as_float(r32[8 * v + 5]) * inv);
-                            o.w = pack_bf16x2(__uint_as_float(r32[8 * v + 6]) * inv, __uint_as_float(r32[8 * v + 7]) * inv);
-                            dst[c * 4 + v] = o;
-                        }
+            for (int c = 0; c < 2; ++c) {
+                uint32_t r32[32];
+                tc::ld32(ox + c * 32, r32);
+                tc::wait_ld();
+                if (x ? vr1 : vr0) {
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        uint4 o;
+                        o.x = pack_bf16x2(__uint_as_float(r32[8 * v + 0]) * inv, __uint_as_float(r32[8 * v + 1]) * inv);
+                        o.y = pack_bf16x2(__uint_as_float(r32[8 * v + 2]) * inv, __uint_as_float(r32[8 * v + 3]) * inv);
+                        o.z = pack_bf16x2(__uint_as_float(r32[8 * v + 4]) * inv, __uint_as_float(r32[8 * v + 5]) * inv);
+                        o.w = pack_bf16x2(__uint_as_float(r32[8 * v + 6]) * inv, __uint_as_float(r32[8 * v + 7]) * inv);
+                        dst[c * 4 + v] = o;
                     }
                 }
             }
