@@ -48,8 +48,11 @@ constexpr int kBarOff = kVOff + kVStages * kTileBytes;
 // barriers: k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[A,B], p_full[A,B], pv_done[A,B]
 constexpr int kNumBars = 14;
 constexpr int kMaskOff = kBarOff + kNumBars * 8;
-constexpr int kXOff = kMaskOff + kKStages * 4;  // row maxima exchanged between halves: [2][2][128]
-constexpr int kTmemOff = kXOff + 2 * 2 * kRows * 4;
+// row maxima / sums exchanged between the two column halves of a row:
+// [tile parity][query tile][half][row] floats
+constexpr int kXFloats = 2 * kQTiles * 2 * kRows;
+constexpr int kXOff = kMaskOff + kKStages * 4;
+constexpr int kTmemOff = kXOff + kXFloats * 4;
 constexpr int kBytes = kTmemOff + 16;
 constexpr int kLaunchBytes = kBytes + 1024;
 constexpr int kSoftmaxWarps = 8;          // two per tensor-memory lane quarter: 64 columns each
@@ -57,6 +60,7 @@ constexpr int kVWarp = 2 + kSoftmaxWarps;
 constexpr int kThreads = 32 * (kVWarp + 1);  // K producer, MMA, 8 softmax warps, V producer
 constexpr uint32_t kTmemCols = 512;       // S_A, S_B, O_A, O_B
 constexpr uint32_t kRescaleLog2 = 8;      // O is rescaled only when the max grows past 2^8
+static_assert(kLaunchBytes <= 227 * 1024, "shared memory of one CTA");
 }  // namespace pf
 
 struct PrefillRowInfo {
@@ -357,7 +361,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
 #pragma unroll
                 for (int c = 0; c < 64; ++c) mt = fmaxf(mt, s[c]);
                 // row maximum over both halves (double-buffered by tile parity)
-                const int xb = (jj & 1) * 2 + x;
+                const int xb = (jj & 1) * kQTiles + x;  // < 2 * kQTiles: kXFloats covers it
                 xbuf[(xb * 2 + hf) * kRows + row] = mt;
                 asm volatile("bar.sync 1, %0;" ::"r"(32 * kSoftmaxWarps) : "memory");
                 mt = fmaxf(mt, xbuf[(xb * 2 + (hf ^ 1)) * kRows + row]);
