@@ -229,30 +229,40 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         // completing also means PV_x(j) is done.
         constexpr uint32_t idS = tc::idesc_bf16(kRows, kKeys, 0, 0);
         constexpr uint32_t idO = tc::idesc_bf16(kRows, kD, 0, 1);
-        const uint32_t q_addr = smem_u32(q_s);
+        // Descriptors are built once: a single issuing thread that rebuilds
+        // them per instruction spends longer than the tensor cores take for
+        // an N=128 product.  Moving along K (or to the next 16 keys of V)
+        // adds the byte offset / 16 to the start-address field, which cannot
+        // carry out of it inside shared memory.
+        const uint64_t dq0 = tc::smem_desc(smem_u32(q_s), 16, 1024);
+        const uint64_t dq1 = tc::smem_desc(smem_u32(q_s + kQBytes), 16, 1024);
+        const uint64_t dk0 = tc::smem_desc(smem_u32(k_s), 16, 1024);
+        const uint64_t dk1 = tc::smem_desc(smem_u32(k_s + kTileBytes), 16, 1024);
+        const uint64_t dv0 = tc::smem_desc(smem_u32(v_s), kKVRegion, 1024);
+        const uint64_t dv1 = tc::smem_desc(smem_u32(v_s + kTileBytes), kKVRegion, 1024);
         auto s_mma = [&](int x, int32_t jj) {  // lane 0
-            const uint32_t k_addr = smem_u32(k_s + (jj & 1) * kTileBytes);
-            const uint32_t qa = q_addr + x * kQBytes;
+            const uint64_t qd = x ? dq1 : dq0, kd = (jj & 1) ? dk1 : dk0;
+            const uint32_t d = tS(x);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t off = (kk >> 2) * kKVRegion + (kk & 3) * 32;
-                tc::mma_ss(tS(x), tc::smem_desc(qa + off, 16, 1024),
-                           tc::smem_desc(k_addr + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
+                const uint64_t off = static_cast<uint64_t>(((kk >> 2) * kKVRegion + (kk & 3) * 32) >> 4);
+                tc::mma_ss(d, qd + off, kd + off, idS, kk > 0 ? 1u : 0u);
             }
             tc::commit(&s_full[x]);
         };
         auto pv_mma = [&](int x, int32_t jj) {  // lane 0
-            const uint32_t v_addr = smem_u32(v_s + (jj & 1) * kTileBytes);
+            const uint64_t vd = (jj & 1) ? dv1 : dv0;
+            const uint32_t d = tO(x), a = tS(x);
+            const uint32_t first = jj > 0 ? 1u : 0u;
             // keys 32c..32c+31 hold P hi in S columns 32c..32c+15 and P lo in
             // 32c+16..32c+31 (bf16 pairs, 8 columns per 16 keys)
 #pragma unroll
             for (int part = 0; part < 2; ++part)
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t bdesc = tc::smem_desc(v_addr + kk * 2048, kKVRegion, 1024);
-                    tc::mma_ts(tO(x), tS(x) + 32 * (kk >> 1) + 8 * (kk & 1) + 16 * part, bdesc,
-                               idO, (jj > 0 || part > 0 || kk > 0) ? 1u : 0u);
-                }
+                for (int kk = 0; kk < 8; ++kk)
+                    tc::mma_ts(d, a + 32 * (kk >> 1) + 8 * (kk & 1) + 16 * part,
+                               vd + static_cast<uint64_t>(kk * 2048 >> 4), idO,
+                               (part > 0 || kk > 0) ? 1u : first);
             tc::commit(&pv_done[x]);
         };
         bool ok = warp_wait(&k_full[0], 0, lane, p.status);
