@@ -39,6 +39,18 @@ __device__ __forceinline__ unsigned long long globaltimer()
 // reading anything the predecessor (or earlier work) wrote.  Both are no-ops
 // for a normal launch.
 // ---------------------------------------------------------------------------
+// True in one lane of the converged warp (the lowest active lane, so every
+// call with the full warp present elects the same thread).  Issuing a
+// single-thread instruction under it keeps the surrounding loop warp-uniform.
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
+
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger()
 {

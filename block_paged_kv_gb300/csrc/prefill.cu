@@ -9,21 +9,22 @@
 // and both tiles share every K/V tile, so K/V are loaded once per 256 query
 // rows.  QK^T and PV are dense contractions and run on the 5th-generation
 // tensor cores:
-//   warps 0/10 TMA producers: K and V tiles of 128 keys (8 paged blocks, two
+//   warps 0/2 TMA producers: K and V tiles of 128 keys (8 paged blocks, two
 //             64-dim boxes each) into 2-stage rings; a K stage is freed once
 //             both S products are computed, a V stage once both P.V are;
-//   warp 1    allocates tensor memory and issues tcgen05.mma from one thread:
-//             S_x = Q_x K^T into tensor memory (both operands K-major, 128-byte
-//             swizzle), then O_x += P_x V with P read from tensor memory (V
-//             MN-major), in the order PV_A(j), S_A(j+1), PV_B(j), S_B(j+1):
-//             each tile's softmax overlaps the other tile's products;
-//   warps 2-9 softmax, tile A then tile B of every K/V tile, two threads per
-//             M-row (64 key columns each, row maxima exchanged through shared
-//             memory): S from tensor memory, causal / window / range mask,
+//   warp 1    allocates tensor memory and issues tcgen05.mma from one elected
+//             lane: S_x = Q_x K^T into tensor memory (both operands K-major,
+//             128-byte swizzle), then O_x += P_x V with P read from tensor
+//             memory (V MN-major), in the order PV_A(j), S_A(j+1), PV_B(j),
+//             S_B(j+1);
+//   warps 4-7 / 8-11  softmax of tile A / tile B, concurrently, one M-row per
+//             thread: S from tensor memory, causal / window / range mask,
 //             running max kept within 2^8 of the true maximum (O is rescaled
 //             in tensor memory only when it moves further), P written back over
-//             S as bf16 hi + lo terms (the P.V product then carries P to
+//             S as bf16 hi + lo terms, 8 columns each per 16 keys (P.V then carries P to
 //             ~2^-17 relative), and the epilogue O / l to global memory.
+//             S is read twice from tensor memory (row maximum, then P), which
+//             keeps a thread's live scores to 32 at a time.
 // f32 kernel: CUDA cores, the same work split with 16 (query, head) pairs per
 // CTA, for the fp32 pools.
 #include "decode_common.cuh"
@@ -48,16 +49,13 @@ constexpr int kBarOff = kVOff + kVStages * kTileBytes;
 // barriers: k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[A,B], p_full[A,B], pv_done[A,B]
 constexpr int kNumBars = 14;
 constexpr int kMaskOff = kBarOff + kNumBars * 8;
-// row maxima / sums exchanged between the two column halves of a row:
-// [tile parity][query tile][half][row] floats
-constexpr int kXFloats = 2 * kQTiles * 2 * kRows;
-constexpr int kXOff = kMaskOff + kKStages * 4;
-constexpr int kTmemOff = kXOff + kXFloats * 4;
+constexpr int kTmemOff = kMaskOff + kKStages * 4;
 constexpr int kBytes = kTmemOff + 16;
 constexpr int kLaunchBytes = kBytes + 1024;
-constexpr int kSoftmaxWarps = 8;          // two per tensor-memory lane quarter: 64 columns each
-constexpr int kVWarp = 2 + kSoftmaxWarps;
-constexpr int kThreads = 32 * (kVWarp + 1);  // K producer, MMA, 8 softmax warps, V producer
+// warps: 0 K producer, 1 MMA issue, 2 V producer, 3 idle (warpgroup 0);
+// 4-7 softmax of query tile A, 8-11 of tile B (one M-row per thread)
+constexpr int kSoftmaxWarps = 8;
+constexpr int kThreads = 384;
 constexpr uint32_t kTmemCols = 512;       // S_A, S_B, O_A, O_B
 constexpr uint32_t kRescaleLog2 = 8;      // O is rescaled only when the max grows past 2^8
 static_assert(kLaunchBytes <= 227 * 1024, "shared memory of one CTA");
@@ -125,9 +123,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
     uint64_t *k_full = bars, *k_empty = bars + 2, *v_full = bars + 4, *v_empty = bars + 6,
              *s_full = bars + 8, *p_full = bars + 10, *pv_done = bars + 12;
     uint32_t *kmask = reinterpret_cast<uint32_t *>(smem + kMaskOff);
-    float *xbuf = reinterpret_cast<float *>(smem + kXOff);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kTmemOff);
-
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = p.group;
     const int qpt = kRows / G;  // queries per query tile
@@ -151,7 +147,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             mbar_init(&v_full[i], 1);
             mbar_init(&v_empty[i], 1);
             mbar_init(&s_full[i], 1);
-            mbar_init(&p_full[i], kSoftmaxWarps);
+            mbar_init(&p_full[i], kSoftmaxWarps / kQTiles);
             mbar_init(&pv_done[i], 1);
         }
         fence_mbar_init();
@@ -160,8 +156,8 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
 
     // query tiles: tile x row i = (query t = x * qpt + i / G, head h = i % G);
     // the 256 softmax threads load one row each
-    if (warp >= 2 && warp < kVWarp) {
-        const int ii = threadIdx.x - 64;
+    if (warp >= 4) {
+        const int ii = threadIdx.x - 128;
         const int x = ii / kRows, i = ii % kRows;
         const int t = x * qpt + i / G, h = i % G;
         const bool valid = i < qpt * G && t < w.nq;
@@ -169,9 +165,16 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
                            ((static_cast<int64_t>(__ldg(p.cu_q_lens + w.r)) + w.i0 + t) * p.hq +
                             w.g * G + h) * (kD / 8);
         uint8_t *qt_s = q_s + x * kQBytes;
+        // a negative scale: stage -q (sign bits flipped, exact), so that the
+        // scores the tensor cores produce always take a positive factor
+        const uint32_t flip = p.scale_log2 < 0.f ? 0x80008000u : 0u;
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-            const uint4 v = valid ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+            uint4 v = valid ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+            v.x ^= flip;
+            v.y ^= flip;
+            v.z ^= flip;
+            v.w ^= flip;
             *reinterpret_cast<uint4 *>(qt_s + (c >> 3) * (kRows * 128) + i * 128 +
                                        (((c & 7) ^ (i & 7)) << 4)) = v;
         }
@@ -185,8 +188,9 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
     auto tS = [&](int x) { return tmem + 128u * static_cast<uint32_t>(x); };
     auto tO = [&](int x) { return tmem + 256u + 128u * static_cast<uint32_t>(x); };
 
-    if (warp == 0 || warp == kVWarp) {
-        // ---------------------------------------- K (warp 0) / V (last warp) producer
+    if (warp < 4) {
+      if (warp == 0 || warp == 2) {
+        // ------------------------------------------ K (warp 0) / V (warp 2) producer
         const bool is_k = warp == 0;
         const CUtensorMap *map = is_k ? &kmap : &vmap;
         uint8_t *ring = is_k ? k_s : v_s;
@@ -215,17 +219,17 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             uint8_t *dst = ring + st * kTileBytes;
             for (int b = 0; b < 8; ++b) {
                 const int32_t bid = __shfl_sync(0xffffffffu, id, b);
-                if (lane == 0 && ((mask >> b) & 1u)) {
+                if (((mask >> b) & 1u) && elect_one()) {
                     tma_load_4d(dst + b * 2048, map, &full[st], 0, 0, w.g, bid, policy);
                     tma_load_4d(dst + kKVRegion + b * 2048, map, &full[st], 64, 0, w.g, bid, policy);
                 }
             }
         }
-    } else if (warp == 1) {
+      } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issue
-        // Order per K/V tile j: PV_A(j), S_A(j+1), PV_B(j), S_B(j+1).  Each
-        // warpgroup's softmax of tile j+1 runs while the tensor cores work on
-        // the other tile; the tensor cores execute in issue order, so S_x(j+1)
+        // Order per K/V tile j: PV_A(j), S_A(j+1), PV_B(j), S_B(j+1): while
+        // one tile's warpgroup turns S into P the tensor cores work for the
+        // other.  The tensor cores execute in issue order, so S_x(j+1)
         // completing also means PV_x(j) is done.
         constexpr uint32_t idS = tc::idesc_bf16(kRows, kKeys, 0, 0);
         constexpr uint32_t idO = tc::idesc_bf16(kRows, kD, 0, 1);
@@ -240,39 +244,43 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         const uint64_t dk1 = tc::smem_desc(smem_u32(k_s + kTileBytes), 16, 1024);
         const uint64_t dv0 = tc::smem_desc(smem_u32(v_s), kKVRegion, 1024);
         const uint64_t dv1 = tc::smem_desc(smem_u32(v_s + kTileBytes), kKVRegion, 1024);
-        auto s_mma = [&](int x, int32_t jj) {  // lane 0
+        // The whole warp runs these; one elected lane issues each product
+        // and the commits (an issuing thread inside a lane-0 branch is
+        // measurably slower to issue).
+        auto s_mma = [&](int x, int32_t jj) {
             const uint64_t qd = x ? dq1 : dq0, kd = (jj & 1) ? dk1 : dk0;
             const uint32_t d = tS(x);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
                 const uint64_t off = static_cast<uint64_t>(((kk >> 2) * kKVRegion + (kk & 3) * 32) >> 4);
-                tc::mma_ss(d, qd + off, kd + off, idS, kk > 0 ? 1u : 0u);
+                if (elect_one()) tc::mma_ss(d, qd + off, kd + off, idS, kk > 0 ? 1u : 0u);
             }
-            tc::commit(&s_full[x]);
+            if (elect_one()) tc::commit(&s_full[x]);
+            __syncwarp();
         };
-        auto pv_mma = [&](int x, int32_t jj) {  // lane 0
+        auto pv_mma = [&](int x, int32_t jj) {
             const uint64_t vd = (jj & 1) ? dv1 : dv0;
             const uint32_t d = tO(x), a = tS(x);
             const uint32_t first = jj > 0 ? 1u : 0u;
-            // keys 32c..32c+31 hold P hi in S columns 32c..32c+15 and P lo in
-            // 32c+16..32c+31 (bf16 pairs, 8 columns per 16 keys)
+            // keys 16g..16g+15 hold P hi in S columns 16g..16g+7 and P lo in
+            // 16g+8..16g+15 (bf16 pairs)
 #pragma unroll
             for (int part = 0; part < 2; ++part)
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    tc::mma_ts(d, a + 32 * (kk >> 1) + 8 * (kk & 1) + 16 * part,
-                               vd + static_cast<uint64_t>(kk * 2048 >> 4), idO,
-                               (part > 0 || kk > 0) ? 1u : first);
-            tc::commit(&pv_done[x]);
+                    if (elect_one())
+                        tc::mma_ts(d, a + 16 * kk + 8 * part,
+                                   vd + static_cast<uint64_t>(kk * 2048 >> 4), idO,
+                                   (part > 0 || kk > 0) ? 1u : first);
+            if (elect_one()) tc::commit(&pv_done[x]);
+            __syncwarp();
         };
         bool ok = warp_wait(&k_full[0], 0, lane, p.status);
         if (ok) {
             tc::fence_after();
-            if (lane == 0) {
-                s_mma(0, 0);
-                s_mma(1, 0);
-                tc::commit(&k_empty[0]);
-            }
+            s_mma(0, 0);
+            s_mma(1, 0);
+            if (elect_one()) tc::commit(&k_empty[0]);
             __syncwarp();
         }
         for (int32_t jj = 0; jj < ntile && ok; ++jj) {
@@ -281,201 +289,209 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
                  warp_wait(&v_full[jj & 1], (jj >> 1) & 1, lane, p.status);
             if (!ok) break;
             tc::fence_after();
-            if (lane == 0) pv_mma(0, jj);
-            __syncwarp();
+            pv_mma(0, jj);
             if (more) {
                 ok = warp_wait(&k_full[(jj + 1) & 1], ((jj + 1) >> 1) & 1, lane, p.status);
                 if (!ok) break;
                 tc::fence_after();
-                if (lane == 0) s_mma(0, jj + 1);
-                __syncwarp();
+                s_mma(0, jj + 1);
             }
             ok = warp_wait(&p_full[1], jj & 1, lane, p.status);
             if (!ok) break;
             tc::fence_after();
-            if (lane == 0) {
-                pv_mma(1, jj);
-                tc::commit(&v_empty[jj & 1]);
-                if (more) {
-                    s_mma(1, jj + 1);
-                    tc::commit(&k_empty[(jj + 1) & 1]);
-                }
-            }
+            pv_mma(1, jj);
+            if (elect_one()) tc::commit(&v_empty[jj & 1]);
             __syncwarp();
+            if (more) {
+                s_mma(1, jj + 1);
+                if (elect_one()) tc::commit(&k_empty[(jj + 1) & 1]);
+                __syncwarp();
+            }
         }
+      }
     } else {
         // ------------------------------------------------------------ softmax
-        // warps 2..9, for tile A then tile B of every K/V tile: lane quarter
-        // q = warp % 4 (rows 32q..32q+31), key half hf = columns 64hf..64hf+63
-        // of S (and of O); the two halves of a row exchange maxima in smem
-        const int hf = (warp - 2) >> 2;
+        // warpgroup x (warps 4-7: tile A, 8-11: tile B), one M-row per thread:
+        // tensor-memory lane quarter warp % 4, all 128 key columns of S
+        const int x = (warp >> 2) - 1;
         const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-        const int row = 32 * (warp & 3) + lane;  // tensor-memory lane of this thread = M-row
-        const uint32_t col0 = 64 * hf;
-        // per-tile row state kept in scalars (selected by tile, no local arrays)
-        const int t0 = row / G, t1 = qpt + row / G;
-        const bool vr0 = row < qpt * G && t0 < w.nq, vr1 = row < qpt * G && t1 < w.nq;
-        const int32_t qp0 = w.L - w.C + w.i0 + t0, qp1 = w.L - w.C + w.i0 + t1;
-        const int32_t ql0 = p.window > 0 ? max(0, qp0 - p.window + 1) : 0;
-        const int32_t ql1 = p.window > 0 ? max(0, qp1 - p.window + 1) : 0;
-        float mr0 = -INFINITY, mr1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+        const int row = 32 * (warp & 3) + lane;
+        const int t = x * qpt + row / G;
+        const bool valid_row = row < qpt * G && t < w.nq;
+        const int32_t qpos = w.L - w.C + w.i0 + t;
+        const int32_t qlo = p.window > 0 ? max(0, qpos - p.window + 1) : 0;
+        const uint32_t sx = tS(x) + lane_base, ox = tO(x) + lane_base;
+        // |scale| * log2(e) (q was staged negated for a negative scale), kept
+        // away from 0 so that a masked score (-inf) never meets a zero factor
+        const float sl = fmaxf(fabsf(p.scale_log2), 1e-30f);
+        float m_ref = -INFINITY, l = 0.f;
         bool abort = false;
-        for (int32_t jj = 0; jj < ntile && !abort; ++jj) {
+        for (int32_t jj = 0; jj < ntile; ++jj) {
             const int ks = jj & 1;
             const int32_t tbase = (jt0 + jj) * kKeys;
-            const int32_t kbase = tbase + static_cast<int32_t>(col0);
-            uint32_t mask = 0;
+            bool got = mbar_wait(&s_full[x], jj & 1);
+            got = got && mbar_wait(&k_full[ks], (jj >> 1) & 1);  // for kmask
+            if (__any_sync(0xffffffffu, !got)) {
+                if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
+                abort = true;
+                break;
+            }
+            const uint32_t mask = kmask[ks];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&k_empty[ks]);
+            tc::fence_after();
+            // pass 1: row maximum of the raw scores, 64 columns at a time; a
+            // tile with any key outside this row's range takes the masked path
+            const bool full = mask == 0xffu && tbase >= qlo && tbase + kKeys - 1 <= qpos && valid_row;
+            // key column e of chunk c is attended iff e - lo_c is in [0, hi_c - lo_c]
+            // and its block was loaded
+            auto mask_chunk = [&](int c, float (&v)[32]) {
+                const int32_t lo_c = qlo - (tbase + 32 * c);
+                const uint32_t span = static_cast<uint32_t>(qpos - qlo);  // qlo <= qpos
+                const uint32_t bm = valid_row ? (mask >> (2 * c)) & 3u : 0u;
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const bool ok = static_cast<uint32_t>(e - lo_c) <= span && ((bm >> (e >> 4)) & 1u);
+                    v[e] = ok ? v[e] : -INFINITY;
+                }
+            };
+            float mt = -INFINITY;
 #pragma unroll 1
-            for (int x = 0; x < kQTiles; ++x) {
-                bool got = mbar_wait(&s_full[x], jj & 1);
-                if (x == 0) got = got && mbar_wait(&k_full[ks], (jj >> 1) & 1);  // for kmask
-                if (__any_sync(0xffffffffu, !got)) {
+            for (int c2 = 0; c2 < 2; ++c2) {
+                float v0[32], v1[32];
+                {
+                    uint32_t r0[32], r1[32];
+                    tc::ld32(sx + 64 * c2, r0);
+                    tc::ld32(sx + 64 * c2 + 32, r1);
+                    tc::wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        v0[e] = __uint_as_float(r0[e]);
+                        v1[e] = __uint_as_float(r1[e]);
+                    }
+                }
+                if (!full) {
+                    mask_chunk(2 * c2, v0);
+                    mask_chunk(2 * c2 + 1, v1);
+                }
+                float m8[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) m8[e] = fmaxf(fmaxf(v0[e], v0[8 + e]), fmaxf(v1[e], v1[8 + e]));
+#pragma unroll
+                for (int c = 2; c < 4; ++c)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        m8[e] = fmaxf(m8[e], fmaxf(v0[8 * c + e], v1[8 * c + e]));
+                mt = fmaxf(mt, fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                     fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))));
+            }
+            mt *= sl;
+            // keep the reference max within 2^8 of the running max
+            const float new_ref = (mt > m_ref + static_cast<float>(kRescaleLog2)) ? mt : m_ref;
+            const float alpha = fast_exp2(m_ref - new_ref);  // 0 from -inf, 1 if unchanged
+            const bool resc = new_ref != m_ref && m_ref != -INFINITY;
+            if (__any_sync(0xffffffffu, resc)) {
+                // O_x holds the products up to tile jj-1; S_x(jj) was issued
+                // after them, so they are complete
+                const float f = resc ? alpha : 1.f;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t r32[32];
+                    tc::ld32(ox + c * 32, r32);
+                    tc::wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) r32[e] = __float_as_uint(__uint_as_float(r32[e]) * f);
+                    tc::st32(ox + c * 32, r32);
+                }
+                tc::wait_st();
+            }
+            m_ref = new_ref;
+            const float nmu = new_ref == -INFINITY ? 0.f : -new_ref;
+            float ls[4] = {0.f, 0.f, 0.f, 0.f};
+            // pass 2: P = 2^(s * scale - max), 32 columns at a time; group g
+            // (16 keys) -> 8 columns of P hi then 8 of P lo, in place
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                float v[32];
+                {
+                    uint32_t r[32];
+                    tc::ld32(sx + 32 * c, r);
+                    tc::wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]);
+                }
+                if (!full) mask_chunk(c, v);
+#pragma unroll
+                for (int g = 0; g < 2; ++g) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float a = fast_exp2(fmaf(v[16 * g + 2 * e], sl, nmu));
+                        const float b = fast_exp2(fmaf(v[16 * g + 2 * e + 1], sl, nmu));
+                        ls[e & 3] += a + b;
+                        const uint32_t hi = pack_bf16x2(a, b);
+                        pk[e] = hi;
+                        pk[8 + e] = pack_bf16x2(a - bf16lo_to_f32(hi), b - bf16hi_to_f32(hi));
+                    }
+                    tc::st16(sx + 32 * c + 16 * g, pk);
+                }
+            }
+            l = l * (resc ? alpha : 1.f) + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
+            // value rows of keys outside [kv_lo, kv_hi) or of blocks not
+            // loaded hold stale slots (possibly NaN): tile A's warpgroup zeroes
+            // them before either P.V product reads them
+            const bool edge = mask != 0xffu || tbase < w.kv_lo || tbase + kKeys > w.kv_hi;
+            if (x == 0 && edge) {
+                const bool landed = mbar_wait(&v_full[ks], (jj >> 1) & 1);
+                if (__any_sync(0xffffffffu, !landed)) {
                     if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
                     abort = true;
                     break;
                 }
-                if (x == 0) {
-                    mask = kmask[ks];
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&k_empty[ks]);
-                }
-                tc::fence_after();
-                const uint32_t sx = tS(x) + lane_base + col0, ox = tO(x) + lane_base + col0;
-                const bool valid_row = x ? vr1 : vr0;
-                const int32_t qpos = x ? qp1 : qp0, qlo = x ? ql1 : ql0;
-                const float m_ref = x ? mr1 : mr0;
-                float s[64];
-                {
-                    uint32_t r0[32], r1[32];
-                    tc::ld32(sx, r0);
-                    tc::ld32(sx + 32, r1);
-                    tc::wait_ld();
+                const int kr = row;  // key row of this thread
+                const int32_t kp = tbase + kr;
+                if (!(kp >= w.kv_lo && kp < w.kv_hi && ((mask >> (kr >> 4)) & 1u))) {
+                    uint8_t *vs = v_s + ks * kTileBytes + kr * 128;
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        s[e] = __uint_as_float(r0[e]) * p.scale_log2;
-                        s[32 + e] = __uint_as_float(r1[e]) * p.scale_log2;
+                    for (int c = 0; c < 8; ++c) {
+                        *reinterpret_cast<uint4 *>(vs + c * 16) = make_uint4(0, 0, 0, 0);
+                        *reinterpret_cast<uint4 *>(vs + kKVRegion + c * 16) = make_uint4(0, 0, 0, 0);
                     }
                 }
-                const uint32_t hmask = (mask >> (4 * hf)) & 0xfu;  // blocks of this half
-                const bool full = hmask == 0xfu && kbase >= qlo && kbase + 63 <= qpos && valid_row;
-                if (!full) {
-#pragma unroll
-                    for (int c = 0; c < 64; ++c) {
-                        const int32_t kp = kbase + c;
-                        const bool ok = valid_row && kp >= qlo && kp <= qpos &&
-                                        ((hmask >> (c >> 4)) & 1u);
-                        if (!ok) s[c] = -INFINITY;
-                    }
-                }
-                float mt = -INFINITY;
-#pragma unroll
-                for (int c = 0; c < 64; ++c) mt = fmaxf(mt, s[c]);
-                // row maximum over both halves (double-buffered by tile parity)
-                const int xb = (jj & 1) * kQTiles + x;  // < 2 * kQTiles: kXFloats covers it
-                xbuf[(xb * 2 + hf) * kRows + row] = mt;
-                asm volatile("bar.sync 1, %0;" ::"r"(32 * kSoftmaxWarps) : "memory");
-                mt = fmaxf(mt, xbuf[(xb * 2 + (hf ^ 1)) * kRows + row]);
-                // keep the reference max within 2^8 of the running max
-                const float new_ref = (mt > m_ref + static_cast<float>(kRescaleLog2)) ? mt : m_ref;
-                const float alpha = fast_exp2(m_ref - new_ref);  // 0 from -inf, 1 if unchanged
-                const bool resc = new_ref != m_ref && m_ref != -INFINITY;
-                if (__any_sync(0xffffffffu, resc)) {
-                    // O_x holds the products up to tile jj-1; S_x(jj) was issued
-                    // after them, so they are complete
-                    const float f = resc ? alpha : 1.f;
-#pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        uint32_t r32[32];
-                        tc::ld32(ox + c * 32, r32);
-                        tc::wait_ld();
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) r32[e] = __float_as_uint(__uint_as_float(r32[e]) * f);
-                        tc::st32(ox + c * 32, r32);
-                    }
-                    tc::wait_st();
-                }
-                if (x) mr1 = new_ref; else mr0 = new_ref;
-                const float mu = new_ref == -INFINITY ? 0.f : new_ref;
-                float lsum = 0.f;
-                // chunk c (32 keys) -> 16 columns of P hi then 16 of P lo, in place
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    uint32_t pk[32];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const float a = fast_exp2(s[c * 32 + 2 * e] - mu);
-                        const float b = fast_exp2(s[c * 32 + 2 * e + 1] - mu);
-                        lsum += a + b;
-                        const uint32_t hi = pack_bf16x2(a, b);
-                        pk[e] = hi;
-                        pk[16 + e] = pack_bf16x2(a - bf16lo_to_f32(hi), b - bf16hi_to_f32(hi));
-                    }
-                    tc::st32(sx + c * 32, pk);
-                }
-                const float lnew = (x ? l1 : l0) * (resc ? alpha : 1.f) + lsum;  // 0 while nothing attended
-                if (x) l1 = lnew; else l0 = lnew;
-                // value rows of keys outside [kv_lo, kv_hi) or of blocks not
-                // loaded hold stale slots (possibly NaN): zero them during tile
-                // A, before either P.V product reads them
-                const bool edge = mask != 0xffu || tbase < w.kv_lo || tbase + kKeys > w.kv_hi;
-                if (x == 0 && edge) {
-                    const bool landed = mbar_wait(&v_full[ks], (jj >> 1) & 1);
-                    if (__any_sync(0xffffffffu, !landed)) {
-                        if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
-                        abort = true;
-                        break;
-                    }
-                    const int kr = row;  // key row; this half zeroes its 64-dim region
-                    const int32_t kp = tbase + kr;
-                    if (!(kp >= w.kv_lo && kp < w.kv_hi && ((mask >> (kr >> 4)) & 1u))) {
-                        uint8_t *vs = v_s + ks * kTileBytes + hf * kKVRegion + kr * 128;
-#pragma unroll
-                        for (int c = 0; c < 8; ++c)
-                            *reinterpret_cast<uint4 *>(vs + c * 16) = make_uint4(0, 0, 0, 0);
-                    }
-                    fence_proxy_async_smem();
-                }
-                tc::wait_st();
-                tc::fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&p_full[x]);
+                fence_proxy_async_smem();
             }
+            tc::wait_st();
+            tc::fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&p_full[x]);
         }
-        // epilogue per tile: O / l once its last P.V product is in (l summed
-        // over the two halves)
-#pragma unroll 1
-        for (int x = 0; x < kQTiles && !abort; ++x) {
-            const float lx = x ? l1 : l0;
-            xbuf[(x * 2 + hf) * kRows + row] = lx;
-            asm volatile("bar.sync 1, %0;" ::"r"(32 * kSoftmaxWarps) : "memory");
-            const float lt = lx + xbuf[(x * 2 + (hf ^ 1)) * kRows + row];
-            const int32_t last = ntile - 1;
-            const bool done = mbar_wait(&pv_done[x], last & 1);
+        // epilogue: O / l once the tile's last P.V product is in
+        if (!abort) {
+            const bool done = mbar_wait(&pv_done[x], (ntile - 1) & 1);
             if (__any_sync(0xffffffffu, !done)) {
                 if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
-                continue;
-            }
-            tc::fence_after();
-            const float inv = lt > 0.f ? 1.f / lt : 0.f;
-            const int t = x * qpt + row / G, h = row % G;
-            uint4 *dst = reinterpret_cast<uint4 *>(p.out) +
-                         ((static_cast<int64_t>(__ldg(p.cu_q_lens + w.r)) + w.i0 + t) * p.hq +
-                          w.g * G + h) * (kD / 8) + hf * 8;
-            const uint32_t ox = tO(x) + lane_base + col0;
+            } else {
+                tc::fence_after();
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+                const int h = row % G;
+                uint4 *dst = reinterpret_cast<uint4 *>(p.out) +
+                             ((static_cast<int64_t>(__ldg(p.cu_q_lens + w.r)) + w.i0 + t) * p.hq +
+                              w.g * G + h) * (kD / 8);
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                uint32_t r32[32];
-                tc::ld32(ox + c * 32, r32);
-                tc::wait_ld();
-                if (x ? vr1 : vr0) {
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t r32[32];
+                    tc::ld32(ox + c * 32, r32);
+                    tc::wait_ld();
+                    if (valid_row) {
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        uint4 o;
-                        o.x = pack_bf16x2(__uint_as_float(r32[8 * v + 0]) * inv, __uint_as_float(r32[8 * v + 1]) * inv);
-                        o.y = pack_bf16x2(__uint_as_float(r32[8 * v + 2]) * inv, __uint_as_float(r32[8 * v + 3]) * inv);
-                        o.z = pack_bf16x2(__uint_as_float(r32[8 * v + 4]) * inv, __uint_as_float(r32[8 * v + 5]) * inv);
-                        o.w = pack_bf16x2(__uint_as_float(r32[8 * v + 6]) * inv, __uint_as_float(r32[8 * v + 7]) * inv);
-                        dst[c * 4 + v] = o;
+                        for (int v = 0; v < 4; ++v) {
+                            uint4 o;
+                            o.x = pack_bf16x2(__uint_as_float(r32[8 * v + 0]) * inv, __uint_as_float(r32[8 * v + 1]) * inv);
+                            o.y = pack_bf16x2(__uint_as_float(r32[8 * v + 2]) * inv, __uint_as_float(r32[8 * v + 3]) * inv);
+                            o.z = pack_bf16x2(__uint_as_float(r32[8 * v + 4]) * inv, __uint_as_float(r32[8 * v + 5]) * inv);
+                            o.w = pack_bf16x2(__uint_as_float(r32[8 * v + 6]) * inv, __uint_as_float(r32[8 * v + 7]) * inv);
+                            dst[c * 4 + v] = o;
+                        }
                     }
                 }
             }
