@@ -36,27 +36,30 @@ namespace pf {
 constexpr int kD = 128;
 constexpr int kRows = 128;                // M of one query tile
 constexpr int kQTiles = 2;                // query tiles per CTA, sharing every K/V tile
-constexpr int kKeys = 128;                // keys per K/V tile (8 blocks of 16)
+constexpr int kKeys = 64;                 // keys per K/V tile (4 blocks of 16)
+constexpr int kBlocks = kKeys / 16;
 constexpr int kQBytes = kRows * 2 * 128;  // one query tile: two 64-dim swizzled regions
-constexpr int kKVRegion = kKeys * 128;    // 16 KiB
-constexpr int kTileBytes = 2 * kKVRegion; // 32 KiB: a K or a V tile
-constexpr int kKStages = 2;
-constexpr int kVStages = 2;
+constexpr int kKVRegion = kKeys * 128;    // 8 KiB: one 64-dim half of a K/V tile
+constexpr int kTileBytes = 2 * kKVRegion; // 16 KiB: a K or a V tile
+constexpr int kStages = 4;                // K ring and V ring depth
 constexpr int kQOff = 0;
 constexpr int kKOff = kQOff + kQTiles * kQBytes;
-constexpr int kVOff = kKOff + kKStages * kTileBytes;
-constexpr int kBarOff = kVOff + kVStages * kTileBytes;
-// barriers: k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[A,B], p_full[A,B], pv_done[A,B]
-constexpr int kNumBars = 14;
+constexpr int kVOff = kKOff + kStages * kTileBytes;
+constexpr int kBarOff = kVOff + kStages * kTileBytes;
+// barriers: k_full[4], k_empty[4], v_full[4], v_empty[4], s_full[tile][buf],
+// p_full[tile][buf], pv_done[tile]
+constexpr int kNumBars = 4 * kStages + 4 + 4 + 2;
 constexpr int kMaskOff = kBarOff + kNumBars * 8;
-constexpr int kTmemOff = kMaskOff + kKStages * 4;
+constexpr int kTmemOff = kMaskOff + kStages * 4;
 constexpr int kBytes = kTmemOff + 16;
 constexpr int kLaunchBytes = kBytes + 1024;
-// warps: 0 K producer, 1 MMA issue, 2 V producer, 3 idle (warpgroup 0);
+// warps: 0 K producer, 1 MMA issue for tile A, 2 V producer, 3 MMA issue for
+// tile B;
 // 4-7 softmax of query tile A, 8-11 of tile B (one M-row per thread)
 constexpr int kSoftmaxWarps = 8;
 constexpr int kThreads = 384;
-constexpr uint32_t kTmemCols = 512;       // S_A, S_B, O_A, O_B
+// tensor memory: S_x[buf] (64 columns each) at 128x + 64buf, O_x at 256 + 128x
+constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kRescaleLog2 = 8;      // O is rescaled only when the max grows past 2^8
 static_assert(kLaunchBytes <= 227 * 1024, "shared memory of one CTA");
 }  // namespace pf
@@ -120,8 +123,11 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
     uint8_t *k_s = smem + kKOff;
     uint8_t *v_s = smem + kVOff;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kBarOff);
-    uint64_t *k_full = bars, *k_empty = bars + 2, *v_full = bars + 4, *v_empty = bars + 6,
-             *s_full = bars + 8, *p_full = bars + 10, *pv_done = bars + 12;
+    uint64_t *k_full = bars, *k_empty = bars + kStages, *v_full = bars + 2 * kStages,
+             *v_empty = bars + 3 * kStages;
+    uint64_t *s_full = bars + 4 * kStages;      // [tile * 2 + buf]
+    uint64_t *p_full = bars + 4 * kStages + 4;  // [tile * 2 + buf]
+    uint64_t *pv_done = bars + 4 * kStages + 8; // [tile]
     uint32_t *kmask = reinterpret_cast<uint32_t *>(smem + kMaskOff);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kTmemOff);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -141,15 +147,18 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
     const int32_t ntile = (w.kv_hi - 1) / kKeys - jt0 + 1;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kStages; ++i) {
             mbar_init(&k_full[i], 1);
-            mbar_init(&k_empty[i], 1 + kSoftmaxWarps);  // both S products + the kmask reads
+            mbar_init(&k_empty[i], kQTiles + kSoftmaxWarps);  // both S products + kmask reads
             mbar_init(&v_full[i], 1);
-            mbar_init(&v_empty[i], 1);
+            mbar_init(&v_empty[i], kQTiles);                  // both P.V products
+        }
+        for (int i = 0; i < 4; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&p_full[i], kSoftmaxWarps / kQTiles);
-            mbar_init(&pv_done[i], 1);
         }
+        mbar_init(&pv_done[0], 1);
+        mbar_init(&pv_done[1], 1);
         fence_mbar_init();
     }
     if (warp == 1) tc::alloc(tmem_slot, kTmemCols);
@@ -184,12 +193,10 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = *tmem_slot;
-    // tensor memory: S_x at columns 128x, O_x at 256 + 128x
-    auto tS = [&](int x) { return tmem + 128u * static_cast<uint32_t>(x); };
+    auto tS = [&](int x, int buf) { return tmem + 128u * static_cast<uint32_t>(x) + 64u * static_cast<uint32_t>(buf); };
     auto tO = [&](int x) { return tmem + 256u + 128u * static_cast<uint32_t>(x); };
 
-    if (warp < 4) {
-      if (warp == 0 || warp == 2) {
+    if (warp == 0 || warp == 2) {
         // ------------------------------------------ K (warp 0) / V (warp 2) producer
         const bool is_k = warp == 0;
         const CUtensorMap *map = is_k ? &kmap : &vmap;
@@ -199,15 +206,15 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         const uint64_t policy = l2_evict_last_policy();  // re-read by the row's other CTAs
         const int32_t *trow = p.tables + static_cast<int64_t>(w.r) * p.width;
         for (int32_t jj = 0; jj < ntile; ++jj) {
-            const int st = jj & 1;
-            if (jj >= 2 && !warp_wait(&empty[st], ((jj >> 1) + 1) & 1, lane, p.status)) break;
-            const int32_t kb = (jt0 + jj) * (kKeys / 16) + lane;  // logical block of lane < 8
-            const bool in_range = lane < 8 && kb < p.width && kb * 16 < w.kv_hi &&
+            const int st = jj % kStages;
+            if (jj >= kStages && !warp_wait(&empty[st], ((jj / kStages) + 1) & 1, lane, p.status)) break;
+            const int32_t kb = (jt0 + jj) * kBlocks + lane;  // logical block of lane < kBlocks
+            const bool in_range = lane < kBlocks && kb < p.width && kb * 16 < w.kv_hi &&
                                   (kb + 1) * 16 > w.kv_lo;
             const int32_t id = in_range ? __ldg(trow + kb) : -1;
             const bool good = in_range && static_cast<uint32_t>(id) < static_cast<uint32_t>(p.num_blocks);
             if (is_k && in_range && !good) report(p.status, PKV_DEV_BAD_BLOCK);
-            const uint32_t mask = __ballot_sync(0xffffffffu, good) & 0xffu;
+            const uint32_t mask = __ballot_sync(0xffffffffu, good) & ((1u << kBlocks) - 1u);
             if (lane == 0) {
                 if (is_k) kmask[st] = mask;
                 if (mask == 0)
@@ -217,7 +224,8 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             }
             __syncwarp();
             uint8_t *dst = ring + st * kTileBytes;
-            for (int b = 0; b < 8; ++b) {
+#pragma unroll
+            for (int b = 0; b < kBlocks; ++b) {
                 const int32_t bid = __shfl_sync(0xffffffffu, id, b);
                 if (((mask >> b) & 1u) && elect_one()) {
                     tma_load_4d(dst + b * 2048, map, &full[st], 0, 0, w.g, bid, policy);
@@ -225,94 +233,76 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
                 }
             }
         }
-      } else if (warp == 1) {
+    } else if (warp == 1 || warp == 3) {
         // ------------------------------------------------------------ MMA issue
-        // Order per K/V tile j: PV_A(j), S_A(j+1), PV_B(j), S_B(j+1): while
-        // one tile's warpgroup turns S into P the tensor cores work for the
-        // other.  The tensor cores execute in issue order, so S_x(j+1)
-        // completing also means PV_x(j) is done.
+        // Warp 1 issues tile A's products, warp 3 tile B's.  Per K/V tile j:
+        // P(j).V, then S(j+2) = Q K(j+2)^T into the S buffer that product just
+        // read.  With two S buffers a warpgroup finds S(j+1) computed when it
+        // finishes P(j).  One thread's products execute in issue order, so a
+        // product never overtakes an earlier read of the same columns.
+        const int x = warp >> 1;
         constexpr uint32_t idS = tc::idesc_bf16(kRows, kKeys, 0, 0);
         constexpr uint32_t idO = tc::idesc_bf16(kRows, kD, 0, 1);
-        // Descriptors are built once: a single issuing thread that rebuilds
-        // them per instruction spends longer than the tensor cores take for
-        // an N=128 product.  Moving along K (or to the next 16 keys of V)
-        // adds the byte offset / 16 to the start-address field, which cannot
-        // carry out of it inside shared memory.
-        const uint64_t dq0 = tc::smem_desc(smem_u32(q_s), 16, 1024);
-        const uint64_t dq1 = tc::smem_desc(smem_u32(q_s + kQBytes), 16, 1024);
-        const uint64_t dk0 = tc::smem_desc(smem_u32(k_s), 16, 1024);
-        const uint64_t dk1 = tc::smem_desc(smem_u32(k_s + kTileBytes), 16, 1024);
-        const uint64_t dv0 = tc::smem_desc(smem_u32(v_s), kKVRegion, 1024);
-        const uint64_t dv1 = tc::smem_desc(smem_u32(v_s + kTileBytes), kKVRegion, 1024);
+        // Descriptors are built once; moving along K (or to the next 16 keys
+        // of V) adds the byte offset / 16 to the start-address field, which
+        // cannot carry out of it inside shared memory.
+        const uint64_t dq = tc::smem_desc(smem_u32(q_s + x * kQBytes), 16, 1024);
+        const uint64_t dk = tc::smem_desc(smem_u32(k_s), 16, 1024);
+        const uint64_t dv = tc::smem_desc(smem_u32(v_s), kKVRegion, 1024);
+        constexpr uint64_t kStageStep = kTileBytes >> 4;
+        const uint32_t tO_x = tO(x);
         // The whole warp runs these; one elected lane issues each product
-        // and the commits (an issuing thread inside a lane-0 branch is
-        // measurably slower to issue).
-        auto s_mma = [&](int x, int32_t jj) {
-            const uint64_t qd = x ? dq1 : dq0, kd = (jj & 1) ? dk1 : dk0;
-            const uint32_t d = tS(x);
+        // and the commits.
+        auto s_mma = [&](int32_t jj) {  // once K(jj) has landed
+            if (!warp_wait(&k_full[jj % kStages], (jj / kStages) & 1, lane, p.status)) return false;
+            tc::fence_after();
+            const uint64_t kd = dk + static_cast<uint64_t>(jj % kStages) * kStageStep;
+            const uint32_t d = tS(x, jj & 1);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
-                const uint64_t off = static_cast<uint64_t>(((kk >> 2) * kKVRegion + (kk & 3) * 32) >> 4);
-                if (elect_one()) tc::mma_ss(d, qd + off, kd + off, idS, kk > 0 ? 1u : 0u);
+                const uint64_t qo = static_cast<uint64_t>(((kk >> 2) * (kRows * 128) + (kk & 3) * 32) >> 4);
+                const uint64_t ko = static_cast<uint64_t>(((kk >> 2) * kKVRegion + (kk & 3) * 32) >> 4);
+                if (elect_one()) tc::mma_ss(d, dq + qo, kd + ko, idS, kk > 0 ? 1u : 0u);
             }
-            if (elect_one()) tc::commit(&s_full[x]);
+            if (elect_one()) {
+                tc::commit(&s_full[x * 2 + (jj & 1)]);
+                tc::commit(&k_empty[jj % kStages]);
+            }
             __syncwarp();
+            return true;
         };
-        auto pv_mma = [&](int x, int32_t jj) {
-            const uint64_t vd = (jj & 1) ? dv1 : dv0;
-            const uint32_t d = tO(x), a = tS(x);
+        auto pv_mma = [&](int32_t jj) {  // V(jj) has landed: the warpgroup checked it
+            const uint64_t vd = dv + static_cast<uint64_t>(jj % kStages) * kStageStep;
+            const uint32_t a = tS(x, jj & 1);
             const uint32_t first = jj > 0 ? 1u : 0u;
             // keys 16g..16g+15 hold P hi in S columns 16g..16g+7 and P lo in
             // 16g+8..16g+15 (bf16 pairs)
 #pragma unroll
             for (int part = 0; part < 2; ++part)
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
+                for (int kk = 0; kk < kBlocks; ++kk)
                     if (elect_one())
-                        tc::mma_ts(d, a + 16 * kk + 8 * part,
+                        tc::mma_ts(tO_x, a + 16 * kk + 8 * part,
                                    vd + static_cast<uint64_t>(kk * 2048 >> 4), idO,
                                    (part > 0 || kk > 0) ? 1u : first);
-            if (elect_one()) tc::commit(&pv_done[x]);
+            if (elect_one()) {
+                tc::commit(&pv_done[x]);
+                tc::commit(&v_empty[jj % kStages]);
+            }
             __syncwarp();
         };
-        bool ok = warp_wait(&k_full[0], 0, lane, p.status);
-        if (ok) {
-            tc::fence_after();
-            s_mma(0, 0);
-            s_mma(1, 0);
-            if (elect_one()) tc::commit(&k_empty[0]);
-            __syncwarp();
-        }
+        bool ok = s_mma(0) && (ntile < 2 || s_mma(1));
         for (int32_t jj = 0; jj < ntile && ok; ++jj) {
-            const bool more = jj + 1 < ntile;
-            ok = warp_wait(&p_full[0], jj & 1, lane, p.status) &&
-                 warp_wait(&v_full[jj & 1], (jj >> 1) & 1, lane, p.status);
+            ok = warp_wait(&p_full[x * 2 + (jj & 1)], (jj >> 1) & 1, lane, p.status);
             if (!ok) break;
             tc::fence_after();
-            pv_mma(0, jj);
-            if (more) {
-                ok = warp_wait(&k_full[(jj + 1) & 1], ((jj + 1) >> 1) & 1, lane, p.status);
-                if (!ok) break;
-                tc::fence_after();
-                s_mma(0, jj + 1);
-            }
-            ok = warp_wait(&p_full[1], jj & 1, lane, p.status);
-            if (!ok) break;
-            tc::fence_after();
-            pv_mma(1, jj);
-            if (elect_one()) tc::commit(&v_empty[jj & 1]);
-            __syncwarp();
-            if (more) {
-                s_mma(1, jj + 1);
-                if (elect_one()) tc::commit(&k_empty[(jj + 1) & 1]);
-                __syncwarp();
-            }
+            pv_mma(jj);
+            if (jj + 2 < ntile) ok = s_mma(jj + 2);
         }
-      }
-    } else {
+    } else if (warp >= 4) {
         // ------------------------------------------------------------ softmax
         // warpgroup x (warps 4-7: tile A, 8-11: tile B), one M-row per thread:
-        // tensor-memory lane quarter warp % 4, all 128 key columns of S
+        // tensor-memory lane quarter warp % 4, the 64 key columns of S
         const int x = (warp >> 2) - 1;
         const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
         const int row = 32 * (warp & 3) + lane;
@@ -320,17 +310,18 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         const bool valid_row = row < qpt * G && t < w.nq;
         const int32_t qpos = w.L - w.C + w.i0 + t;
         const int32_t qlo = p.window > 0 ? max(0, qpos - p.window + 1) : 0;
-        const uint32_t sx = tS(x) + lane_base, ox = tO(x) + lane_base;
+        const uint32_t ox = tO(x) + lane_base;
         // |scale| * log2(e) (q was staged negated for a negative scale), kept
         // away from 0 so that a masked score (-inf) never meets a zero factor
         const float sl = fmaxf(fabsf(p.scale_log2), 1e-30f);
         float m_ref = -INFINITY, l = 0.f;
         bool abort = false;
         for (int32_t jj = 0; jj < ntile; ++jj) {
-            const int ks = jj & 1;
+            const int ks = jj % kStages, buf = jj & 1;
             const int32_t tbase = (jt0 + jj) * kKeys;
-            bool got = mbar_wait(&s_full[x], jj & 1);
-            got = got && mbar_wait(&k_full[ks], (jj >> 1) & 1);  // for kmask
+            const uint32_t sx = tS(x, buf) + lane_base;
+            bool got = mbar_wait(&s_full[x * 2 + buf], (jj >> 1) & 1);
+            got = got && mbar_wait(&k_full[ks], (jj / kStages) & 1);  // for kmask
             if (__any_sync(0xffffffffu, !got)) {
                 if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
                 abort = true;
@@ -340,59 +331,60 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&k_empty[ks]);
             tc::fence_after();
-            // pass 1: row maximum of the raw scores, 64 columns at a time; a
-            // tile with any key outside this row's range takes the masked path
-            const bool full = mask == 0xffu && tbase >= qlo && tbase + kKeys - 1 <= qpos && valid_row;
-            // key column e of chunk c is attended iff e - lo_c is in [0, hi_c - lo_c]
-            // and its block was loaded
-            auto mask_chunk = [&](int c, float (&v)[32]) {
-                const int32_t lo_c = qlo - (tbase + 32 * c);
-                const uint32_t span = static_cast<uint32_t>(qpos - qlo);  // qlo <= qpos
-                const uint32_t bm = valid_row ? (mask >> (2 * c)) & 3u : 0u;
+            float s[64];
+            {
+                uint32_t r0[32], r1[32];
+                tc::ld32(sx, r0);
+                tc::ld32(sx + 32, r1);
+                tc::wait_ld();
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
-                    const bool ok = static_cast<uint32_t>(e - lo_c) <= span && ((bm >> (e >> 4)) & 1u);
-                    v[e] = ok ? v[e] : -INFINITY;
+                    s[e] = __uint_as_float(r0[e]);
+                    s[32 + e] = __uint_as_float(r1[e]);
                 }
-            };
-            float mt = -INFINITY;
-#pragma unroll 1
-            for (int c2 = 0; c2 < 2; ++c2) {
-                float v0[32], v1[32];
-                {
-                    uint32_t r0[32], r1[32];
-                    tc::ld32(sx + 64 * c2, r0);
-                    tc::ld32(sx + 64 * c2 + 32, r1);
-                    tc::wait_ld();
+            }
+            // a tile with any key outside this row's range takes the masked
+            // path: key column e is attended iff e - lo is in [0, qpos - qlo]
+            // and its block was loaded
+            const bool full = mask == (1u << kBlocks) - 1u && tbase >= qlo &&
+                              tbase + kKeys - 1 <= qpos && valid_row;
+            if (!full) {
+                const int32_t lo = qlo - tbase;
+                const uint32_t span = static_cast<uint32_t>(qpos - qlo);  // qlo <= qpos
+                const uint32_t bm = valid_row ? mask : 0u;
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        v0[e] = __uint_as_float(r0[e]);
-                        v1[e] = __uint_as_float(r1[e]);
-                    }
+                for (int e = 0; e < 64; ++e) {
+                    const bool ok = static_cast<uint32_t>(e - lo) <= span && ((bm >> (e >> 4)) & 1u);
+                    s[e] = ok ? s[e] : -INFINITY;
                 }
-                if (!full) {
-                    mask_chunk(2 * c2, v0);
-                    mask_chunk(2 * c2 + 1, v1);
-                }
+            }
+            float mt;
+            {
                 float m8[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) m8[e] = fmaxf(fmaxf(v0[e], v0[8 + e]), fmaxf(v1[e], v1[8 + e]));
+                for (int e = 0; e < 8; ++e) m8[e] = fmaxf(s[e], s[8 + e]);
 #pragma unroll
-                for (int c = 2; c < 4; ++c)
+                for (int c = 2; c < 8; ++c)
 #pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        m8[e] = fmaxf(m8[e], fmaxf(v0[8 * c + e], v1[8 * c + e]));
-                mt = fmaxf(mt, fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                                     fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))));
+                    for (int e = 0; e < 8; ++e) m8[e] = fmaxf(m8[e], s[8 * c + e]);
+                mt = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                           fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * sl;
             }
-            mt *= sl;
             // keep the reference max within 2^8 of the running max
             const float new_ref = (mt > m_ref + static_cast<float>(kRescaleLog2)) ? mt : m_ref;
             const float alpha = fast_exp2(m_ref - new_ref);  // 0 from -inf, 1 if unchanged
             const bool resc = new_ref != m_ref && m_ref != -INFINITY;
             if (__any_sync(0xffffffffu, resc)) {
-                // O_x holds the products up to tile jj-1; S_x(jj) was issued
-                // after them, so they are complete
+                // O_x holds P.V up to tile jj-1 once that product completes
+                if (jj > 0) {
+                    const bool done = mbar_wait(&pv_done[x], (jj - 1) & 1);
+                    if (__any_sync(0xffffffffu, !done)) {
+                        if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
+                        abort = true;
+                        break;
+                    }
+                    tc::fence_after();
+                }
                 const float f = resc ? alpha : 1.f;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
@@ -408,66 +400,59 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             m_ref = new_ref;
             const float nmu = new_ref == -INFINITY ? 0.f : -new_ref;
             float ls[4] = {0.f, 0.f, 0.f, 0.f};
-            // pass 2: P = 2^(s * scale - max), 32 columns at a time; group g
-            // (16 keys) -> 8 columns of P hi then 8 of P lo, in place
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-                float v[32];
-                {
-                    uint32_t r[32];
-                    tc::ld32(sx + 32 * c, r);
-                    tc::wait_ld();
+            // group g (16 keys) -> 8 columns of P hi then 8 of P lo, in place
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]);
+            for (int g = 0; g < kBlocks; ++g) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float a = fast_exp2(fmaf(s[16 * g + 2 * e], sl, nmu));
+                    const float b = fast_exp2(fmaf(s[16 * g + 2 * e + 1], sl, nmu));
+                    ls[e & 3] += a + b;
+                    const uint32_t hi = pack_bf16x2(a, b);
+                    pk[e] = hi;
+                    pk[8 + e] = pack_bf16x2(a - bf16lo_to_f32(hi), b - bf16hi_to_f32(hi));
                 }
-                if (!full) mask_chunk(c, v);
-#pragma unroll
-                for (int g = 0; g < 2; ++g) {
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float a = fast_exp2(fmaf(v[16 * g + 2 * e], sl, nmu));
-                        const float b = fast_exp2(fmaf(v[16 * g + 2 * e + 1], sl, nmu));
-                        ls[e & 3] += a + b;
-                        const uint32_t hi = pack_bf16x2(a, b);
-                        pk[e] = hi;
-                        pk[8 + e] = pack_bf16x2(a - bf16lo_to_f32(hi), b - bf16hi_to_f32(hi));
-                    }
-                    tc::st16(sx + 32 * c + 16 * g, pk);
-                }
+                tc::st16(sx + 16 * g, pk);
             }
             l = l * (resc ? alpha : 1.f) + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
-            // value rows of keys outside [kv_lo, kv_hi) or of blocks not
-            // loaded hold stale slots (possibly NaN): tile A's warpgroup zeroes
-            // them before either P.V product reads them
-            const bool edge = mask != 0xffu || tbase < w.kv_lo || tbase + kKeys > w.kv_hi;
-            if (x == 0 && edge) {
-                const bool landed = mbar_wait(&v_full[ks], (jj >> 1) & 1);
-                if (__any_sync(0xffffffffu, !landed)) {
-                    if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
-                    abort = true;
-                    break;
-                }
-                const int kr = row;  // key row of this thread
+            // V(jj) must have landed before this tile's P.V is issued.  Value
+            // rows of keys outside [kv_lo, kv_hi) or of blocks not loaded hold
+            // stale slots (possibly NaN): each warpgroup zeroes them before its
+            // own P.V reads them (both write the same zeros, so whichever
+            // product runs first reads zeros)
+            const bool landed = mbar_wait(&v_full[ks], (jj / kStages) & 1);
+            if (__any_sync(0xffffffffu, !landed)) {
+                if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
+                abort = true;
+                break;
+            }
+            const bool edge = mask != (1u << kBlocks) - 1u || tbase < w.kv_lo || tbase + kKeys > w.kv_hi;
+            if (edge) {
+                // thread row r < 64 zeroes key row r's first 64 dims, r >= 64
+                // the second 64 dims of key row r - 64
+                const int kr = row & (kKeys - 1), half = row >> 6;
                 const int32_t kp = tbase + kr;
                 if (!(kp >= w.kv_lo && kp < w.kv_hi && ((mask >> (kr >> 4)) & 1u))) {
-                    uint8_t *vs = v_s + ks * kTileBytes + kr * 128;
+                    uint8_t *vs = v_s + ks * kTileBytes + half * kKVRegion + kr * 128;
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
+                    for (int c = 0; c < 8; ++c)
                         *reinterpret_cast<uint4 *>(vs + c * 16) = make_uint4(0, 0, 0, 0);
-                        *reinterpret_cast<uint4 *>(vs + kKVRegion + c * 16) = make_uint4(0, 0, 0, 0);
-                    }
                 }
                 fence_proxy_async_smem();
             }
             tc::wait_st();
             tc::fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&p_full[x]);
+            if (lane == 0) mbar_arrive(&p_full[x * 2 + buf]);
         }
-        // epilogue: O / l once the tile's last P.V product is in
+        // epilogue: O / l once the tile's last P.V product is in.  Phases up
+        // to ntile - 3 are known complete here (S(ntile-1) was issued after
+        // P(ntile-3).V), so wait for ntile - 2 first: a parity names one phase
+        // only when the one before it has completed
         if (!abort) {
-            const bool done = mbar_wait(&pv_done[x], (ntile - 1) & 1);
+            bool done = ntile < 2 || mbar_wait(&pv_done[x], (ntile - 2) & 1);
+            done = done && mbar_wait(&pv_done[x], (ntile - 1) & 1);
             if (__any_sync(0xffffffffu, !done)) {
                 if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
             } else {
