@@ -98,12 +98,11 @@ __device__ __forceinline__ bool prefill_item(const PrefillParams &p, int64_t bid
     return true;
 }
 
-// Wait by one lane, result broadcast to the warp; reports a timeout.
+// Wait by every lane of the warp (false in all lanes if any gave up); reports
+// a timeout.
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, int lane, int32_t *status)
 {
-    bool ok = true;
-    if (lane == 0) ok = mbar_wait(bar, parity);
-    ok = __shfl_sync(0xffffffffu, ok, 0);
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(bar, parity));
     if (!ok && lane == 0) report(status, PKV_DEV_TIMEOUT);
     return ok;
 }
@@ -251,20 +250,20 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         const uint64_t dv = tc::smem_desc(smem_u32(v_s), kKVRegion, 1024);
         constexpr uint64_t kStageStep = kTileBytes >> 4;
         const uint32_t tO_x = tO(x);
-        // The whole warp runs these; one elected lane issues each product
-        // and the commits.
+        // The whole warp runs these; one elected lane issues a group's
+        // products and commits from one straight-line block.
         auto s_mma = [&](int32_t jj) {  // once K(jj) has landed
             if (!warp_wait(&k_full[jj % kStages], (jj / kStages) & 1, lane, p.status)) return false;
             tc::fence_after();
             const uint64_t kd = dk + static_cast<uint64_t>(jj % kStages) * kStageStep;
             const uint32_t d = tS(x, jj & 1);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint64_t qo = static_cast<uint64_t>(((kk >> 2) * (kRows * 128) + (kk & 3) * 32) >> 4);
-                const uint64_t ko = static_cast<uint64_t>(((kk >> 2) * kKVRegion + (kk & 3) * 32) >> 4);
-                if (elect_one()) tc::mma_ss(d, dq + qo, kd + ko, idS, kk > 0 ? 1u : 0u);
-            }
             if (elect_one()) {
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint64_t qo = static_cast<uint64_t>(((kk >> 2) * (kRows * 128) + (kk & 3) * 32) >> 4);
+                    const uint64_t ko = static_cast<uint64_t>(((kk >> 2) * kKVRegion + (kk & 3) * 32) >> 4);
+                    tc::mma_ss(d, dq + qo, kd + ko, idS, kk > 0 ? 1u : 0u);
+                }
                 tc::commit(&s_full[x * 2 + (jj & 1)]);
                 tc::commit(&k_empty[jj % kStages]);
             }
@@ -277,15 +276,14 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             const uint32_t first = jj > 0 ? 1u : 0u;
             // keys 16g..16g+15 hold P hi in S columns 16g..16g+7 and P lo in
             // 16g+8..16g+15 (bf16 pairs)
+            if (elect_one()) {
 #pragma unroll
-            for (int part = 0; part < 2; ++part)
+                for (int part = 0; part < 2; ++part)
 #pragma unroll
-                for (int kk = 0; kk < kBlocks; ++kk)
-                    if (elect_one())
+                    for (int kk = 0; kk < kBlocks; ++kk)
                         tc::mma_ts(tO_x, a + 16 * kk + 8 * part,
                                    vd + static_cast<uint64_t>(kk * 2048 >> 4), idO,
                                    (part > 0 || kk > 0) ? 1u : first);
-            if (elect_one()) {
                 tc::commit(&pv_done[x]);
                 tc::commit(&v_empty[jj % kStages]);
             }
