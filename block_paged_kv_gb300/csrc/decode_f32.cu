@@ -230,9 +230,14 @@ cudaError_t launch_decode_f32(const DecodeParams &p, cudaStream_t stream)
 }
 
 // ---------------------------------------------------------------------------
-// Merge: one warp per (row, q head).  M = max of the partial maxima; each
-// partial is weighted by 2^(m_s - M); out = sum w_s O_s / sum w_s l_s.  Rows
-// with no partial (an empty key range) get zeros.
+// Merge of the split partials.  With W = 1 (rows with few partials) an item is
+// a (row, q head) and a warp takes it whole; with W = 8 an item is a (row,
+// q head, chunk of up to 64 dims) shared by the CTA's 8 warps: warp w takes partials w, w+W, ...  M = max of the
+// partial maxima; each partial is weighted by 2^(m_s - M); out = sum w_s O_s /
+// sum w_s l_s.  Each warp first reduces its own partials against its own
+// maximum and the warp results are merged through shared memory, so a row with
+// many partials keeps many loads in flight.  Rows with no partial (an empty
+// key range) get zeros.
 // ---------------------------------------------------------------------------
 template <typename OutT>
 __device__ __forceinline__ OutT to_out(float x);
@@ -241,88 +246,124 @@ __device__ __forceinline__ float to_out<float>(float x) { return x; }
 template <>
 __device__ __forceinline__ __nv_bfloat16 to_out<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
 
-template <typename OutT, int D>
-__global__ void __launch_bounds__(128, 1) decode_combine_kernel(const DecodeParams p)
+constexpr int kCombineWarps = 8;
+
+template <typename OutT, int D, int W>
+__global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(const DecodeParams p)
 {
-    constexpr int PER = D / 32;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t idx = static_cast<int64_t>(blockIdx.x) * 4 + warp;
-    const bool live = idx < static_cast<int64_t>(p.batch) * p.hq;
+    constexpr int CH = (W == 1 || D < 64) ? D : 64;  // dims per item
+    constexpr int PER = CH / 32;                     // dims per lane
+    constexpr int NCH = D / CH;
+    constexpr int IPC = kCombineWarps / W;  // items per CTA
+    __shared__ float sm_m[kCombineWarps], sm_l[kCombineWarps];
+    __shared__ float sm_acc[kCombineWarps][CH];
+    const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int warp = wid % W, sub = wid / W;  // warp within the item, item within the CTA
+    const int64_t item = static_cast<int64_t>(blockIdx.x) * IPC + sub;
+    const bool live = item < static_cast<int64_t>(p.batch) * p.hq * NCH;
+    const int64_t idx = live ? item / NCH : 0;  // (row, q head)
+    const int ch = static_cast<int>(item % NCH);
     // The row bookkeeping reads only call inputs: the decode kernel released
     // this grid after its own wait on earlier work, so they are final already.
-    int32_t r = 0, h = 0, npre = 0, n = 0;
-    if (live) {
-        r = static_cast<int32_t>(idx / p.hq);
-        h = static_cast<int32_t>(idx % p.hq);
-        const RowRange rr = row_range(p, r, false);
-        npre = row_prefix_splits(p, rr);
-        n = npre + row_suffix_splits(p, rr);
-    }
+    const int32_t r = static_cast<int32_t>(idx / p.hq);
+    const int32_t h = static_cast<int32_t>(idx % p.hq);
+    const RowRange rr = row_range(p, r, false);
+    const int32_t npre = row_prefix_splits(p, rr);
+    const int32_t n = npre + row_suffix_splits(p, rr);
     pdl_wait();  // the partials come from the decode kernel just before
-    if (!live) return;
     const size_t base = partial_index(p, r, h, 0);
     auto slot_of = [&](int32_t k) { return k < npre ? k : p.plan.n_prefix_splits + (k - npre); };
 
-    // lane k holds partial k's (max, sum) for the first 32 partials
-    float2 ml0 = make_float2(-INFINITY, 0.f);
-    if (lane < n) ml0 = *reinterpret_cast<const float2 *>(p.ws_ml + (base + slot_of(lane)) * 2);
-    float M = ml0.x;
-    for (int32_t k = 32 + lane; k < n; k += 32)
-        M = fmaxf(M, p.ws_ml[(base + slot_of(k)) * 2]);
+    // this warp's maximum over its partials k = warp + W * i
+    float Mw = -INFINITY;
+    for (int32_t k = warp + W * lane; k < n; k += W * 32)
+        Mw = fmaxf(Mw, p.ws_ml[(base + slot_of(k)) * 2]);
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-
+    for (int off = 16; off > 0; off >>= 1) Mw = fmaxf(Mw, __shfl_xor_sync(0xffffffffu, Mw, off));
     float acc[PER];
 #pragma unroll
-    for (int j = 0; j < PER; ++j) acc[j] = 0.f;
-    float lsum = 0.f;
-    if (M != -INFINITY) {
-        for (int32_t k0 = 0; k0 < n; k0 += 32) {
-            float2 ml = ml0;
-            if (k0 > 0) {
-                ml = make_float2(-INFINITY, 0.f);
-                if (k0 + lane < n)
-                    ml = *reinterpret_cast<const float2 *>(p.ws_ml + (base + slot_of(k0 + lane)) * 2);
-            }
-            const float my_w = fast_exp2(ml.x - M);  // 0 for absent partials
-            lsum = fmaf(my_w, ml.y, lsum);
-            const int32_t my_slot = k0 + lane < n ? slot_of(k0 + lane) : 0;
-            const int cnt = min(32, n - k0);
-            // weighted sum of the partials' values; the loads of several
-            // partials are independent, so unrolling keeps them in flight
+    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+    float lw = 0.f;
+    if (Mw != -INFINITY) {
+        // the partials' loads are independent: unrolling keeps several in flight
 #pragma unroll 8
-            for (int j = 0; j < cnt; ++j) {
-                const float w = __shfl_sync(0xffffffffu, my_w, j);
-                const int32_t slot = __shfl_sync(0xffffffffu, my_slot, j);
-                const float *src = p.ws_o + (base + slot) * D + lane;
+        for (int32_t k = warp; k < n; k += W) {
+            const size_t slot = base + slot_of(k);
+            const float2 ml = *reinterpret_cast<const float2 *>(p.ws_ml + slot * 2);
+            const float wgt = fast_exp2(ml.x - Mw);  // 0 for an empty partial
+            lw = fmaf(wgt, ml.y, lw);
+            const float *src = p.ws_o + slot * D + ch * CH + (W == 1 ? lane : lane * PER);
+            if constexpr (W == 1) {
+                // lane owns dims lane + 32 e: each load instruction is coalesced
 #pragma unroll
-                for (int e = 0; e < PER; ++e) acc[e] = fmaf(w, src[32 * e], acc[e]);
+                for (int e = 0; e < PER; ++e) acc[e] = fmaf(wgt, src[32 * e], acc[e]);
+            } else if constexpr (PER == 2) {
+                const float2 v = *reinterpret_cast<const float2 *>(src);
+                acc[0] = fmaf(wgt, v.x, acc[0]);
+                acc[1] = fmaf(wgt, v.y, acc[1]);
+            } else {
+                acc[0] = fmaf(wgt, src[0], acc[0]);
             }
         }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
     }
-    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-    OutT *out = static_cast<OutT *>(p.out) + idx * D;
+    if constexpr (W == 1) {
+        // one warp per item: every lane already holds the item's sum
+        if (!live) return;
+        const float inv = lw > 0.f ? 1.f / lw : 0.f;
+        OutT *out = static_cast<OutT *>(p.out) + idx * D + lane;
 #pragma unroll
-    for (int e = 0; e < PER; ++e) out[lane + 32 * e] = to_out<OutT>(acc[e] * inv);
+        for (int e = 0; e < PER; ++e) out[32 * e] = to_out<OutT>(acc[e] * inv);
+    } else {
+        if (lane == 0) {
+            sm_m[wid] = Mw;
+            sm_l[wid] = lw;
+        }
+#pragma unroll
+        for (int e = 0; e < PER; ++e) sm_acc[wid][lane * PER + e] = acc[e];
+        __syncthreads();
+        if (live && threadIdx.x < CH) {
+            float M = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < W; ++i) M = fmaxf(M, sm_m[i]);
+            float L = 0.f, o = 0.f;
+            if (M != -INFINITY) {
+#pragma unroll
+                for (int i = 0; i < W; ++i) {
+                    const float f = fast_exp2(sm_m[i] - M);  // 0 for a warp without partials
+                    L = fmaf(f, sm_l[i], L);
+                    o = fmaf(f, sm_acc[i][threadIdx.x], o);
+                }
+            }
+            const float inv = L > 0.f ? 1.f / L : 0.f;
+            static_cast<OutT *>(p.out)[idx * D + ch * CH + threadIdx.x] = to_out<OutT>(o * inv);
+        }
+    }
+}
+
+template <typename OutT, int W>
+static cudaError_t launch_combine_w(const DecodeParams &p, cudaStream_t stream)
+{
+    const int64_t chunks = (W == 1 || p.head_dim < 64) ? 1 : p.head_dim / 64;
+    const int64_t items = static_cast<int64_t>(p.batch) * p.hq * chunks;
+    const int64_t ipc = kCombineWarps / W;
+    const dim3 grid(static_cast<unsigned>((items + ipc - 1) / ipc)), block(kCombineWarps * 32);
+    switch (p.head_dim) {
+    case 32: return launch_pdl(decode_combine_kernel<OutT, 32, W>, grid, block, 0, stream, p);
+    case 64: return launch_pdl(decode_combine_kernel<OutT, 64, W>, grid, block, 0, stream, p);
+    case 128: return launch_pdl(decode_combine_kernel<OutT, 128, W>, grid, block, 0, stream, p);
+    case 256: return launch_pdl(decode_combine_kernel<OutT, 256, W>, grid, block, 0, stream, p);
+    default: return cudaErrorInvalidValue;
+    }
 }
 
 template <typename OutT>
 static cudaError_t launch_combine_t(const DecodeParams &p, cudaStream_t stream)
 {
-    const int64_t pairs = static_cast<int64_t>(p.batch) * p.hq;
-    if (pairs == 0) return cudaSuccess;
-    const dim3 grid(static_cast<unsigned>((pairs + 3) / 4)), block(128);
-    cudaError_t err;
+    if (static_cast<int64_t>(p.batch) * p.hq == 0) return cudaSuccess;
     prof_begin(PKV_KERNEL_DECODE_COMBINE, stream);
-    switch (p.head_dim) {
-    case 32: err = launch_pdl(decode_combine_kernel<OutT, 32>, grid, block, 0, stream, p); break;
-    case 64: err = launch_pdl(decode_combine_kernel<OutT, 64>, grid, block, 0, stream, p); break;
-    case 128: err = launch_pdl(decode_combine_kernel<OutT, 128>, grid, block, 0, stream, p); break;
-    case 256: err = launch_pdl(decode_combine_kernel<OutT, 256>, grid, block, 0, stream, p); break;
-    default: err = cudaErrorInvalidValue; break;
-    }
+    // a warp per item while rows have few partials, eight when they have many
+    const cudaError_t err = p.plan.nslot > 16 ? launch_combine_w<OutT, kCombineWarps>(p, stream)
+                                             : launch_combine_w<OutT, 1>(p, stream);
     prof_end(PKV_KERNEL_DECODE_COMBINE, stream);
     return err;
 }
