@@ -145,6 +145,32 @@ def committed_traffic(sha):
     return d.get("dram_bytes_per_launch_full_workload")
 
 
+def barrier(world):
+    """All ranks meet (no-op for one rank)."""
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world, dev):
+    """The largest of the ranks' values of x (a time): the job is as slow as
+    its slowest rank."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank_step, world, ms, steps):
+    """Whole-job throughput: every rank processes units_per_rank_step per step
+    (replicas over disjoint row batches, no exchange), and the job takes the
+    max-over-ranks time ms for `steps` steps.  Units per second."""
+    return world * units_per_rank_step / (ms / steps / 1e3)
+
+
 def run_pkv(args, rank, world, local):
     import torch
     import block_paged_kv_gb300 as pkv
@@ -186,19 +212,6 @@ def run_pkv(args, rank, world, local):
         step()
     torch.cuda.synchronize()
 
-    def barrier():
-        if world > 1:
-            import torch.distributed as dist
-            dist.barrier()
-
-    def max_over_ranks(x):
-        if world == 1:
-            return x
-        import torch.distributed as dist
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
-
     clocks = ClockSampler(local)
     if rank == 0:
         clocks.start()
@@ -206,16 +219,16 @@ def run_pkv(args, rank, world, local):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     pkv.profile_enable([pkv.KERNEL_DECODE_SPLIT])
     n0 = pkv.launch_count()
-    barrier()
+    barrier(world)
     torch.cuda.synchronize()
     e0.record(stream)
     for _ in range(args.steps):
         step()
     e1.record(stream)
     torch.cuda.synchronize()
-    barrier()
+    barrier(world)
     launches = pkv.launch_count() - n0
-    ms = max_over_ranks(e0.elapsed_time(e1))
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     nsplit, split_ms = pkv.profile_read(pkv.KERNEL_DECODE_SPLIT)
     pkv.profile_enable([])
     clk = clocks.stop() if rank == 0 else None
@@ -244,14 +257,14 @@ def run_pkv(args, rank, world, local):
     for _ in range(3):
         e2e_step()
     torch.cuda.synchronize()
-    barrier()
+    barrier(world)
     e0.record(stream)
     for _ in range(e2e_steps):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    barrier()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1))
+    barrier(world)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
 
     secondary = secondary_measurements(args, pkv, torch, dev) if (rank == 0 and args.secondary) else None
 
@@ -259,7 +272,7 @@ def run_pkv(args, rank, world, local):
         return
     peak, peak_kind = peaks()
     t_step = ms / args.steps / 1e3
-    value = world * bytes_step / t_step / 1e9
+    value = job_rate(bytes_step, world, ms, args.steps) / 1e9
     split_avg_s = split_ms / max(nsplit, 1) / 1e3
     achieved = bytes_step / split_avg_s / 1e9
     sha = kernel_source_sha()
@@ -275,9 +288,9 @@ def run_pkv(args, rank, world, local):
                    "kv_bytes_per_step": bytes_step, "parallelism": f"replicas x{world} (rows shard)",
                    "l2": "no flush: 0.47 GB of K/V per step exceeds the 129 MB L2"},
         "pct_of_8TBps": round(100 * value / world / NOMINAL_HBM_GBS, 1),
-        "tok_per_s": round(world * w.batch / t_step, 1),
+        "tok_per_s": round(job_rate(w.batch, world, ms, args.steps), 1),
         "clocks": clk,
-        "e2e": {"value": round(world * bytes_step / (e2e_ms / e2e_steps / 1e3) / 1e9, 1), "unit": "GB/s",
+        "e2e": {"value": round(job_rate(bytes_step, world, e2e_ms, e2e_steps) / 1e9, 1), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms / e2e_steps, 5)},
         "gpu_launches": int(launches),
