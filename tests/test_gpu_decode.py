@@ -95,6 +95,17 @@ def test_shapes_windows_ragged(pkv, orc, dtype, d, hq, hkv, window):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("scale", [-0.3, 0.0])
+def test_scale_sign_and_zero(pkv, orc, dtype, scale):
+    import dataclasses
+    w = gen.decode_workload(seed=9, dtype=dtype, num_q_heads=8, num_kv_heads=2, head_dim=128,
+                            context_lens=[1, 30, 300, 1000])
+    w = dataclasses.replace(w, scale=scale)
+    got, ref, _ = run_step(pkv, orc, w)
+    assert_close(got, ref, dtype, f"{dtype} decode scale {scale}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_sliding_null_sentinel(pkv, orc, dtype):
     w = gen.decode_workload(seed=7, dtype=dtype, num_q_heads=8, num_kv_heads=2, head_dim=128,
                             context_lens=[40, 500, 1000, 63], window=48, sliding_live_only=True)

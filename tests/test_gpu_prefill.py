@@ -130,3 +130,14 @@ def test_unsupported_shape_reported(pkv):
         pkv.paged_prefill_chunk_attention(d.q, d.cu, d.k_pool, d.v_pool, d.tables, d.seq_lens, 4, 0,
                                           w.scale)
     assert e.value.code == pkv.PKV_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("scale", [-0.3, 0.0, 0.5])
+def test_scale_sign_and_zero(pkv, orc, scale):
+    # a negative scale is staged as -q (exact), a zero scale attends uniformly
+    import dataclasses
+    w = gen.prefill_workload(seed=74, dtype="bf16", num_q_heads=8, num_kv_heads=2, head_dim=128,
+                             prefix_lens=[0, 90, 300], chunk_lens=[37, 64, 130])
+    w = dataclasses.replace(w, scale=scale)
+    got, ref, _ = run_prefill(pkv, orc, w)
+    assert_close(got, ref, "bf16", f"prefill scale {scale}")
