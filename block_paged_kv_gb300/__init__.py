@@ -76,6 +76,8 @@ _lib.pkv_decode_plan.restype = _i32
 _lib.pkv_version.restype = ctypes.c_char_p
 _lib.pkv_profile_enable.argtypes = [ctypes.c_uint32]
 _lib.pkv_profile_enable.restype = ctypes.c_int
+_lib.pkv_profile_mask.argtypes = [ctypes.c_uint32]
+_lib.pkv_profile_mask.restype = ctypes.c_int
 _lib.pkv_profile_read.argtypes = [_i32, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_double)]
 _lib.pkv_profile_read.restype = ctypes.c_int
 _lib.pkv_launch_count.restype = ctypes.c_int64
@@ -89,7 +91,7 @@ KERNEL_APPEND, KERNEL_DECODE_PREFIX, KERNEL_DECODE_SPLIT, KERNEL_DECODE_COMBINE,
 EXPORTED = ["paged_kv_append", "paged_decode_workspace_size", "paged_decode_attention",
             "paged_prefill_workspace_size", "paged_prefill_chunk_attention", "pkv_status_string",
             "pkv_slot_mapping_host", "pkv_prefix_groups_host", "pkv_set_decode_split_blocks",
-            "pkv_decode_plan", "pkv_version", "pkv_profile_enable", "pkv_profile_read",
+            "pkv_decode_plan", "pkv_version", "pkv_profile_enable", "pkv_profile_mask", "pkv_profile_read",
             "pkv_launch_count", "paged_decode_attention_no_alloc"]
 
 
@@ -332,6 +334,14 @@ def profile_enable(kinds=()) -> None:
     for k in kinds:
         mask |= 1 << k
     _check("pkv_profile_enable", _lib.pkv_profile_enable(mask))
+
+
+def profile_mask(kinds=()) -> None:
+    """Change which kernel kinds are timed, keeping the records so far."""
+    mask = 0
+    for k in kinds:
+        mask |= 1 << k
+    _check("pkv_profile_mask", _lib.pkv_profile_mask(mask))
 
 
 def profile_read(kind: int) -> Tuple[int, float]:

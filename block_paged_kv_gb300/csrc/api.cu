@@ -260,6 +260,12 @@ pkv_status pkv_profile_enable(uint32_t kind_mask)
     return PKV_OK;
 }
 
+pkv_status pkv_profile_mask(uint32_t kind_mask)
+{
+    g_prof_mask.store(kind_mask);
+    return PKV_OK;
+}
+
 pkv_status pkv_profile_read(int32_t kind, int64_t *launches, double *total_ms)
 {
     if (kind < 0 || kind >= PKV_KERNEL_KINDS || launches == nullptr || total_ms == nullptr)

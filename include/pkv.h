@@ -264,6 +264,11 @@ typedef enum {
  * Up to 65536 launches are recorded.  Not for use inside stream capture. */
 pkv_status pkv_profile_enable(uint32_t kind_mask);
 
+/* Changes which kinds are timed without resetting the records: timing only
+ * some launches (one in N, say) keeps the events, which end the overlap of a
+ * launch with its neighbours, off the other launches. */
+pkv_status pkv_profile_mask(uint32_t kind_mask);
+
 /* Launches recorded for a kind and their summed device time in milliseconds.
  * Waits for the recorded events. */
 pkv_status pkv_profile_read(int32_t kind, int64_t *launches, double *total_ms);
