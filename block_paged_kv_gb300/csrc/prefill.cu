@@ -144,13 +144,17 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
     if (!prefill_item(p, blockIdx.x, kQTiles * qpt, w)) return;
     const int32_t jt0 = w.kv_lo / kKeys;
     const int32_t ntile = (w.kv_hi - 1) / kKeys - jt0 + 1;
+    // query tiles with queries in them: a short chunk (a verify step of a few
+    // queries) fills tile A only, and tile B's warps then stay idle
+    const int nqt = w.nq > qpt ? 2 : 1;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&k_full[i], 1);
-            mbar_init(&k_empty[i], kQTiles + kSoftmaxWarps);  // both S products + kmask reads
+            // the S products of the live tiles + their warpgroups' kmask reads
+            mbar_init(&k_empty[i], nqt + nqt * (kSoftmaxWarps / kQTiles));
             mbar_init(&v_full[i], 1);
-            mbar_init(&v_empty[i], kQTiles);                  // both P.V products
+            mbar_init(&v_empty[i], nqt);  // the live tiles' P.V products
         }
         for (int i = 0; i < 4; ++i) {
             mbar_init(&s_full[i], 1);
@@ -232,7 +236,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
                 }
             }
         }
-    } else if (warp == 1 || warp == 3) {
+    } else if (warp == 1 || (warp == 3 && nqt == 2)) {
         // ------------------------------------------------------------ MMA issue
         // Warp 1 issues tile A's products, warp 3 tile B's.  Per K/V tile j:
         // P(j).V, then S(j+2) = Q K(j+2)^T into the S buffer that product just
@@ -297,7 +301,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             pv_mma(jj);
             if (jj + 2 < ntile) ok = s_mma(jj + 2);
         }
-    } else if (warp >= 4) {
+    } else if (warp >= 4 && (warp < 8 || nqt == 2)) {
         // ------------------------------------------------------------ softmax
         // warpgroup x (warps 4-7: tile A, 8-11: tile B), one M-row per thread:
         // tensor-memory lane quarter warp % 4, the 64 key columns of S

@@ -141,3 +141,16 @@ def test_scale_sign_and_zero(pkv, orc, scale):
     w = dataclasses.replace(w, scale=scale)
     got, ref, _ = run_prefill(pkv, orc, w)
     assert_close(got, ref, "bf16", f"prefill scale {scale}")
+
+
+@pytest.mark.parametrize("hq,hkv", [(32, 8), (8, 1), (16, 16)])
+@pytest.mark.parametrize("window", [0, 64])
+def test_verify_steps(pkv, orc, hq, hkv, window):
+    # speculative-verify shape: a few queries per row over a long paged
+    # context; the chunk fits the first query tile, the second stays idle
+    w = gen.prefill_workload(seed=80 + hq + hkv + window, dtype="bf16", num_q_heads=hq,
+                             num_kv_heads=hkv, head_dim=128,
+                             prefix_lens=[100, 1000, 3000, 17, 0], chunk_lens=[4, 4, 2, 8, 3],
+                             window=window)
+    got, ref, _ = run_prefill(pkv, orc, w)
+    assert_close(got, ref, "bf16", f"verify {hq}/{hkv} w{window}")
