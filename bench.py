@@ -405,6 +405,27 @@ def secondary_measurements(args, pkv, torch, dev):
                               "flop": flops, "frac_of_bf16_peak": round(flops / s / 1e12 / bf16_peak(), 3),
                               "peak": "measured bf16_tflops (burst)", "l2": "flushed before each call"}
     del kp, vp
+    # speculative verify: 32 rows x 4 queries over 1024..8192-token contexts
+    w = gen.verify_steps()
+    kp, vp, q = up(w, w.k_pool), up(w, w.v_pool), up(w, w.q)
+    kn, vn = up(w, w.k_new), up(w, w.v_new)
+    t = torch.from_numpy(w.block_tables).to(dev)
+    sl = torch.from_numpy(w.seq_lens).to(dev)
+    cu = torch.from_numpy(w.cu_q_lens).to(dev)
+    slots = torch.from_numpy(pkv.slot_mapping_host(w.block_tables, w.num_blocks, w.new_rows,
+                                                   w.new_pos, 16)).to(dev)
+    pkv.paged_kv_append(kp, vp, slots, kn, vn)
+    out = torch.empty_like(q)
+    C = int(w.cu_q_lens[1] - w.cu_q_lens[0])
+    ml = int(w.seq_lens.max())
+    s = time_loop(torch, lambda: pkv.paged_prefill_chunk_attention(q, cu, kp, vp, t, sl, C, 0, w.scale,
+                                                                   out=out, max_seq_len=ml),
+                  50, 5, flush)
+    b = int(np.sum(w.seq_lens)) * 2 * w.num_kv_heads * w.head_dim * 2
+    res["verify_4q"] = {"workload": w.name, "us": round(s * 1e6, 2), "GB/s": round(b / s / 1e9, 1),
+                        "kv_bytes": b, "queries_per_s": round(w.batch * C / s, 1),
+                        "l2": "flushed before each call"}
+    del kp, vp
     # bulk append: every token of the batch-32 workload's private suffixes
     w = gen.shared_prefix_b32()
     n = int(np.sum(w.seq_lens - 1024))

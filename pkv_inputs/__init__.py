@@ -341,6 +341,16 @@ def long_two_groups(batch: int = 4, context: int = 32768, window: int = 512):
     return full, sliding
 
 
+def verify_steps(batch: int = 32, q_len: int = 4, min_ctx: int = 1024,
+                 max_ctx: int = 8192) -> Workload:
+    """bf16, 32 rows, each a speculative-verify step of 4 queries after a paged
+    context uniform on 1024..8192 tokens, 32 q / 8 kv heads, head_dim 128."""
+    ctx = [int(x) for x in uniform_ints(1005, "verify_ctx", batch, min_ctx, max_ctx)]
+    return prefill_workload(seed=1005, dtype="bf16", num_q_heads=32, num_kv_heads=8,
+                            head_dim=128, prefix_lens=ctx, chunk_lens=[q_len] * batch,
+                            name=f"verify_bf16_b{batch}_q{q_len}_ctx{min_ctx}-{max_ctx}_h32x8_d128")
+
+
 def chunked_prefill(batch: int = 4, chunk: int = 512, prefix: int = 16384) -> Workload:
     """bf16, 4 rows, a 512-query chunk each after a 16384-token paged prefix,
     32 q / 8 kv heads, head_dim 128, causal within the chunk."""
