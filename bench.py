@@ -426,6 +426,32 @@ def secondary_measurements(args, pkv, torch, dev):
                         "kv_bytes": b, "queries_per_s": round(w.batch * C / s, 1),
                         "l2": "flushed before each call"}
     del kp, vp
+    # host block allocator: the batch-32 workload's requests (a 1024-token
+    # shared prompt + private suffixes) through find / reserve / publish /
+    # release, timed on the host
+    alloc = pkv.BlockAllocator(16, 1024, 1 << 20)
+    wl = gen.shared_prefix_b32()
+    prompts = [np.concatenate([np.arange(1024, dtype=np.int32),
+                               np.arange(int(L) - 1024, dtype=np.int32) + 10**6 * (i + 1)])
+               for i, L in enumerate(wl.seq_lens)]
+    t0 = time.perf_counter()
+    rounds = 20
+    for _ in range(rounds):
+        ids = []
+        for ptoks in prompts:
+            r = alloc.begin()
+            alloc.find_cached_prefix(r, ptoks)
+            alloc.reserve(r, len(ptoks) + 1)
+            alloc.publish(r, ptoks)
+            ids.append(r)
+        for r in ids:
+            alloc.release(r)
+    dt = time.perf_counter() - t0
+    res["block_allocator"] = {"requests_per_s": round(rounds * len(prompts) / dt, 1),
+                              "us_per_batch32": round(dt / rounds * 1e6, 1),
+                              "tokens_per_batch": int(sum(len(x) for x in prompts)),
+                              "pool_blocks": alloc.stats()[0],
+                              "note": "host, single thread, via the Python binding"}
     # bulk append: every token of the batch-32 workload's private suffixes
     w = gen.shared_prefix_b32()
     n = int(np.sum(w.seq_lens - 1024))

@@ -25,7 +25,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libpkv.so")
 
-PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA, PKV_ERR_WORKSPACE = range(5)
+PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA, PKV_ERR_WORKSPACE, PKV_ERR_OUT_OF_BLOCKS = range(6)
 PKV_F32, PKV_BF16 = 0, 1
 DEV_BAD_BLOCK, DEV_BAD_SLOT, DEV_BAD_LEN, DEV_BAD_PREFIX, DEV_TIMEOUT = 1, 2, 4, 8, 16
 
@@ -85,6 +85,28 @@ _lib.paged_decode_attention_no_alloc.argtypes = [_vp, _i32, _PP, _vp, _i32, _vp,
                                                  ctypes.c_float, _vp, _XP, _vp, _vp]
 _lib.paged_decode_attention_no_alloc.restype = ctypes.c_int
 NO_ALLOC_SCRATCH_BYTES = 16 << 20
+_u64p = ctypes.POINTER(ctypes.c_uint64)
+_i32p = ctypes.POINTER(ctypes.c_int32)
+_lib.pkv_allocator_create.argtypes = [_i32, _i32, _i32]
+_lib.pkv_allocator_create.restype = _vp
+_lib.pkv_allocator_destroy.argtypes = [_vp]
+_lib.pkv_allocator_destroy.restype = None
+_lib.pkv_allocator_begin.argtypes = [_vp]
+_lib.pkv_allocator_begin.restype = _i32
+_lib.pkv_allocator_find_cached_prefix.argtypes = [_vp, _i32, _vp, _i32, _vp, _i32p]
+_lib.pkv_allocator_find_cached_prefix.restype = ctypes.c_int
+_lib.pkv_allocator_reserve.argtypes = [_vp, _i32, _i32]
+_lib.pkv_allocator_reserve.restype = ctypes.c_int
+_lib.pkv_allocator_publish.argtypes = [_vp, _i32, _vp, _i32, _vp]
+_lib.pkv_allocator_publish.restype = ctypes.c_int
+_lib.pkv_allocator_release.argtypes = [_vp, _i32]
+_lib.pkv_allocator_release.restype = ctypes.c_int
+_lib.pkv_allocator_table.argtypes = [_vp, _i32, _vp, _i32, _i32p]
+_lib.pkv_allocator_table.restype = ctypes.c_int
+_lib.pkv_allocator_refcount.argtypes = [_vp, _i32]
+_lib.pkv_allocator_refcount.restype = _i32
+_lib.pkv_allocator_stats.argtypes = [_vp, _i32p, _i32p, _i32p, _i32p]
+_lib.pkv_allocator_stats.restype = ctypes.c_int
 
 KERNEL_APPEND, KERNEL_DECODE_PREFIX, KERNEL_DECODE_SPLIT, KERNEL_DECODE_COMBINE, KERNEL_PREFILL = range(5)
 
@@ -92,7 +114,10 @@ EXPORTED = ["paged_kv_append", "paged_decode_workspace_size", "paged_decode_atte
             "paged_prefill_workspace_size", "paged_prefill_chunk_attention", "pkv_status_string",
             "pkv_slot_mapping_host", "pkv_prefix_groups_host", "pkv_set_decode_split_blocks",
             "pkv_decode_plan", "pkv_version", "pkv_profile_enable", "pkv_profile_mask", "pkv_profile_read",
-            "pkv_launch_count", "paged_decode_attention_no_alloc"]
+            "pkv_launch_count", "paged_decode_attention_no_alloc", "pkv_allocator_create",
+            "pkv_allocator_destroy", "pkv_allocator_begin", "pkv_allocator_find_cached_prefix",
+            "pkv_allocator_reserve", "pkv_allocator_publish", "pkv_allocator_release",
+            "pkv_allocator_table", "pkv_allocator_refcount", "pkv_allocator_stats"]
 
 
 class PkvError(RuntimeError):
@@ -393,3 +418,76 @@ def paged_decode_attention_no_alloc(q: torch.Tensor, k_pool: torch.Tensor, v_poo
                        f"{NO_ALLOC_SCRATCH_BYTES >> 20} MiB static scratch)", code)
     _check("paged_decode_attention_no_alloc", code)
     return out
+
+
+# ---------------------------------------------------------------------------
+# host block allocator
+# ---------------------------------------------------------------------------
+class BlockAllocator:
+    """The library's host block allocator (see ``include/pkv.h``): block ids of
+    a pool of ``block_size``-token blocks, shared across requests by prefix
+    hash, refcounted, with LRU eviction of cache-only blocks and
+    grow-on-demand up to ``max_blocks``.  Token lists are int32 sequences."""
+
+    def __init__(self, block_size: int, initial_blocks: int, max_blocks: int):
+        self._a = _lib.pkv_allocator_create(block_size, initial_blocks, max_blocks)
+        _require(bool(self._a), "block_size > 0 and 0 <= initial_blocks <= max_blocks")
+        self.block_size = block_size
+
+    def __del__(self):
+        a = getattr(self, "_a", None)
+        if a:
+            _lib.pkv_allocator_destroy(a)
+            self._a = None
+
+    @staticmethod
+    def _tokens(tokens):
+        arr = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+        return arr, (arr.ctypes.data if arr.size else None)
+
+    @staticmethod
+    def _keys(extra_keys):
+        if extra_keys is None:
+            return None, None
+        arr = np.ascontiguousarray(np.asarray(extra_keys, dtype=np.uint64))
+        return arr, arr.ctypes.data
+
+    def begin(self) -> int:
+        return int(_lib.pkv_allocator_begin(self._a))
+
+    def find_cached_prefix(self, req: int, tokens, extra_keys=None) -> int:
+        t, tp = self._tokens(tokens)
+        k, kp = self._keys(extra_keys)
+        n = ctypes.c_int32(0)
+        _check("pkv_allocator_find_cached_prefix",
+               _lib.pkv_allocator_find_cached_prefix(self._a, req, tp, t.size, kp, ctypes.byref(n)))
+        return int(n.value)
+
+    def reserve(self, req: int, n_tokens: int) -> None:
+        _check("pkv_allocator_reserve", _lib.pkv_allocator_reserve(self._a, req, int(n_tokens)))
+
+    def publish(self, req: int, tokens, extra_keys=None) -> None:
+        t, tp = self._tokens(tokens)
+        k, kp = self._keys(extra_keys)
+        _check("pkv_allocator_publish", _lib.pkv_allocator_publish(self._a, req, tp, t.size, kp))
+
+    def release(self, req: int) -> None:
+        _check("pkv_allocator_release", _lib.pkv_allocator_release(self._a, req))
+
+    def table(self, req: int) -> np.ndarray:
+        n = ctypes.c_int32(0)
+        _check("pkv_allocator_table", _lib.pkv_allocator_table(self._a, req, None, 0, ctypes.byref(n)))
+        out = np.empty(n.value, dtype=np.int32)
+        if n.value:
+            _check("pkv_allocator_table", _lib.pkv_allocator_table(
+                self._a, req, out.ctypes.data, n.value, ctypes.byref(n)))
+        return out
+
+    def refcount(self, block: int) -> int:
+        return int(_lib.pkv_allocator_refcount(self._a, block))
+
+    def stats(self):
+        """(num_blocks, free_blocks, cached_blocks, grows)."""
+        v = [ctypes.c_int32(0) for _ in range(4)]
+        _check("pkv_allocator_stats", _lib.pkv_allocator_stats(self._a, *[ctypes.byref(x) for x in v]))
+        return tuple(int(x.value) for x in v)

@@ -300,6 +300,7 @@ const char *pkv_status_string(pkv_status s)
     case PKV_ERR_UNSUPPORTED: return "unsupported dtype/shape combination";
     case PKV_ERR_CUDA: return "CUDA error";
     case PKV_ERR_WORKSPACE: return "workspace too small or misaligned";
+    case PKV_ERR_OUT_OF_BLOCKS: return "block pool exhausted at its maximum size";
     }
     return "unknown status";
 }

@@ -56,7 +56,8 @@ typedef enum {
     PKV_ERR_INVALID_ARG = 1,
     PKV_ERR_UNSUPPORTED = 2,
     PKV_ERR_CUDA = 3,
-    PKV_ERR_WORKSPACE = 4
+    PKV_ERR_WORKSPACE = 4,
+    PKV_ERR_OUT_OF_BLOCKS = 5 /* block allocator: the pool (at its maximum) cannot hold the request */
 } pkv_status;
 
 typedef enum { PKV_F32 = 0, PKV_BF16 = 1 } pkv_dtype;
@@ -278,6 +279,83 @@ int64_t pkv_launch_count(void);
 
 /* Library version string. */
 const char *pkv_version(void);
+
+/* ========================================================================
+ * Host block allocator ("paged-cache.md": the BlockAllocator row of the
+ * component table - per-block refcounts, LRU eviction, a prefix-hash table for
+ * reuse across requests; the PagedKVCacheAdapter per-request lifecycle; the
+ * grow-on-demand rule of the pool-sizing passage; a block enters the prefix
+ * table only once it is full).  Host memory only, single-threaded (callers serialise).  It
+ * hands out block ids of the caller's device pools; when it grows, the caller
+ * grows the pools to pkv_allocator_stats' num_blocks before using new ids.
+ *
+ * Block identity: a full block's hash is FNV-1a (64-bit) over the
+ * little-endian bytes of its parent's hash (0 for the first block), its
+ * block_size token ids (int32) and one 64-bit extra key (0 for text-only
+ * blocks; image digests and similar go there), so a block's identity carries
+ * its whole prefix.  Equal hashes are taken as equal blocks.
+ *
+ * Block states: free (lowest id handed out first); in use (refcount = the
+ * requests whose table holds it); cache-only (published, refcount 0, on an LRU
+ * list ordered by release time).  A reservation that needs k new blocks when
+ * fewer than k are free:
+ *   - if free + cache-only blocks cannot cover k and the pool is below its
+ *     maximum, the pool grows once first, to
+ *       min(max_blocks, max(2 * current, current + (k - free)));
+ *   - then cache-only blocks are evicted, least recently released first
+ *     (they leave the prefix table);
+ *   - if k blocks are still not there, PKV_ERR_OUT_OF_BLOCKS and nothing
+ *     changes.
+ * ======================================================================== */
+typedef struct pkv_allocator pkv_allocator;
+
+/* block_size tokens per block; the pool starts at initial_blocks and grows up
+ * to max_blocks (initial_blocks <= max_blocks).  NULL on invalid sizes. */
+pkv_allocator *pkv_allocator_create(int32_t block_size, int32_t initial_blocks,
+                                    int32_t max_blocks);
+void pkv_allocator_destroy(pkv_allocator *a);
+
+/* A new request (reset_for_new_request): its id, >= 0, with an empty table. */
+int32_t pkv_allocator_begin(pkv_allocator *a);
+
+/* find_cached_prefix: for a fresh request with prompt tokens[0..n_tokens),
+ * walk the prompt's full blocks in order, hashing each on its parent, and take
+ * every block found in the prefix table until the first miss (refcount + 1; a
+ * cache-only block leaves the LRU).  extra_keys: NULL, or one key per full
+ * block.  *cached_tokens = the tokens covered (a multiple of block_size). */
+pkv_status pkv_allocator_find_cached_prefix(pkv_allocator *a, int32_t req,
+                                            const int32_t *tokens, int32_t n_tokens,
+                                            const uint64_t *extra_keys,
+                                            int32_t *cached_tokens);
+
+/* allocate_suffix_blocks: extend the request's table with new blocks until it
+ * covers n_tokens tokens (grow / evict as above).  PKV_ERR_OUT_OF_BLOCKS
+ * leaves the table as it was. */
+pkv_status pkv_allocator_reserve(pkv_allocator *a, int32_t req, int32_t n_tokens);
+
+/* record_tokens + register_full_blocks_for_reuse: tokens[0..n_tokens) are the
+ * request's tokens so far (n_tokens <= its table's capacity).  Each full block
+ * of the table not yet published is hashed and published, unless the prefix
+ * table already holds that hash under another block (this block then stays
+ * private to the request).  extra_keys as above. */
+pkv_status pkv_allocator_publish(pkv_allocator *a, int32_t req, const int32_t *tokens,
+                                 int32_t n_tokens, const uint64_t *extra_keys);
+
+/* release_request: every block of the table loses a reference; a published
+ * block at refcount 0 becomes cache-only (LRU tail), an unpublished one free.
+ * The id is retired. */
+pkv_status pkv_allocator_release(pkv_allocator *a, int32_t req);
+
+/* The request's block table: min(cap, n) ids into out (host), n into *n_blocks. */
+pkv_status pkv_allocator_table(const pkv_allocator *a, int32_t req, int32_t *out, int32_t cap,
+                               int32_t *n_blocks);
+
+/* Refcount of one block (-1 for an id outside the pool). */
+int32_t pkv_allocator_refcount(const pkv_allocator *a, int32_t block);
+
+/* Pool counters: current block count, free, cache-only, grows so far. */
+pkv_status pkv_allocator_stats(const pkv_allocator *a, int32_t *num_blocks, int32_t *free_blocks,
+                               int32_t *cached_blocks, int32_t *grows);
 
 #ifdef __cplusplus
 }
