@@ -446,9 +446,13 @@ size_t paged_prefill_workspace_size(int32_t batch, int32_t num_q_heads, int32_t 
                                     int32_t head_dim, int32_t block_size, int32_t max_q_len,
                                     int32_t max_seq_len, int32_t window)
 {
-    (void)batch; (void)num_q_heads; (void)num_kv_heads; (void)head_dim; (void)block_size;
-    (void)max_q_len; (void)max_seq_len; (void)window;
-    return 0;  // the prefill kernels need no scratch: no split of the key range
+    if (batch <= 0 || num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads != 0 ||
+        max_q_len <= 0 || max_seq_len < 0 || window < 0)
+        return 0;
+    // scratch only for the key-range runs of short bf16 chunks
+    const PrefillSplit sp = prefill_split_plan(batch, num_q_heads, num_kv_heads, head_dim, block_size,
+                                               max_q_len, max_seq_len, window, num_sms_current());
+    return prefill_split_ws_bytes(batch, num_q_heads, max_q_len, sp);
 }
 
 pkv_status paged_prefill_chunk_attention(const void *q, const int32_t *cu_q_lens,
@@ -459,8 +463,6 @@ pkv_status paged_prefill_chunk_attention(const void *q, const int32_t *cu_q_lens
                                          void *out, void *workspace, size_t ws_bytes,
                                          int32_t *dev_status, pkv_stream_t stream)
 {
-    (void)workspace;
-    (void)ws_bytes;
     if (!valid_pool(pool) || batch < 0 || num_q_heads <= 0 || max_q_len < 0 || max_seq_len < 0 ||
         window < 0 || !std::isfinite(scale))
         return PKV_ERR_INVALID_ARG;
@@ -495,8 +497,29 @@ pkv_status paged_prefill_chunk_attention(const void *q, const int32_t *cu_q_lens
     p.window = window;
     const int32_t qpt = prefill_queries_per_cta(pool->dtype, G);
     p.q_tiles = static_cast<int32_t>(ceil_div64(max_q_len, qpt));
+    p.kv_splits = 1;
+    p.split_tiles = 0;
+    if (pool->dtype == PKV_BF16) {
+        const PrefillSplit sp = prefill_split_plan(batch, num_q_heads, pool->num_kv_heads,
+                                                   pool->head_dim, pool->block_size, max_q_len,
+                                                   p.max_len, window, num_sms_current());
+        if (sp.splits > 1) {
+            const size_t need = prefill_split_ws_bytes(batch, num_q_heads, max_q_len, sp);
+            if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+                ws_bytes < need)
+                return PKV_ERR_WORKSPACE;
+            p.kv_splits = sp.splits;
+            p.split_tiles = sp.tiles;
+            const size_t n = static_cast<size_t>(batch) * max_q_len * num_q_heads * sp.splits;
+            p.ws_o = static_cast<float *>(workspace);
+            p.ws_ml = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                                ((n * pool->head_dim * sizeof(float) + 255) &
+                                                 ~static_cast<size_t>(255)));
+        }
+    }
     p.scale_log2 = scale * 1.4426950408889634f;
-    if (static_cast<int64_t>(batch) * p.hkv * p.q_tiles > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(batch) * p.hkv * p.q_tiles * p.kv_splits > INT32_MAX)
+        return PKV_ERR_UNSUPPORTED;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t err;
     if (pool->dtype == PKV_BF16) {

@@ -102,12 +102,29 @@ struct PrefillParams {
     int32_t max_q_len;
     int32_t window;
     int32_t q_tiles;    // CTAs per (row, kv head): ceil(max_q_len / queries per CTA)
+    // key-range split (bf16, short chunks only; 1 = none): each (row, kv head,
+    // query tile) is cut into kv_splits runs of split_tiles 64-key tiles whose
+    // fp32 partials a merge kernel combines
+    int32_t kv_splits;
+    int32_t split_tiles;
+    float *ws_o;   // [batch][max_q_len][hq][kv_splits][128] unnormalised weighted values
+    float *ws_ml;  // [batch][max_q_len][hq][kv_splits][2]: reference max (log2 units), weight sum
     float scale_log2;
 };
 
 cudaError_t launch_append(const AppendParams &p, cudaStream_t stream);
 bool prefill_shape_built(pkv_dtype dtype, int32_t D, int32_t bs, int32_t G);
 int32_t prefill_queries_per_cta(pkv_dtype dtype, int32_t G);
+// Key-range split of the bf16 prefill for short chunks (all of a row's
+// queries in one query tile) on grids too small to fill the GPU: runs per
+// (row, kv head) and 64-key tiles per run; {1, 0} = no split.
+struct PrefillSplit {
+    int32_t splits, tiles;
+};
+PrefillSplit prefill_split_plan(int32_t batch, int32_t hq, int32_t hkv, int32_t D, int32_t bs,
+                                int32_t max_q_len, int32_t max_seq_len, int32_t window,
+                                int num_sms);
+size_t prefill_split_ws_bytes(int32_t batch, int32_t hq, int32_t max_q_len, const PrefillSplit &sp);
 cudaError_t launch_prefill_bf16(const PrefillParams &p, const CUtensorMap &kmap,
                                 const CUtensorMap &vmap, cudaStream_t stream);
 cudaError_t launch_prefill_f32(const PrefillParams &p, cudaStream_t stream);

@@ -27,6 +27,8 @@
 //             keeps a thread's live scores to 32 at a time.
 // f32 kernel: CUDA cores, the same work split with 16 (query, head) pairs per
 // CTA, for the fp32 pools.
+#include <algorithm>
+
 #include "decode_common.cuh"
 #include "tcgen05.cuh"
 
@@ -65,12 +67,14 @@ static_assert(kLaunchBytes <= 227 * 1024, "shared memory of one CTA");
 }  // namespace pf
 
 struct PrefillRowInfo {
-    int32_t r, g, i0, nq, L, C, kv_lo, kv_hi;
+    int32_t r, g, i0, nq, L, C, kv_lo, kv_hi, s;
 };
 
 __device__ __forceinline__ bool prefill_item(const PrefillParams &p, int64_t bid, int qpc,
                                              PrefillRowInfo &w)
 {
+    w.s = static_cast<int32_t>(bid % p.kv_splits);
+    bid /= p.kv_splits;
     const int32_t qt = static_cast<int32_t>(bid % p.q_tiles);
     bid /= p.q_tiles;
     w.g = static_cast<int32_t>(bid % p.hkv);
@@ -142,8 +146,28 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
 
     PrefillRowInfo w;
     if (!prefill_item(p, blockIdx.x, kQTiles * qpt, w)) return;
-    const int32_t jt0 = w.kv_lo / kKeys;
-    const int32_t ntile = (w.kv_hi - 1) / kKeys - jt0 + 1;
+    int32_t jt0 = w.kv_lo / kKeys;
+    int32_t ntile = (w.kv_hi - 1) / kKeys - jt0 + 1;
+    const bool split = p.kv_splits > 1;
+    if (split) {
+        // this CTA's run of the key range
+        const int32_t tb = w.s * p.split_tiles;
+        ntile = min(ntile, tb + p.split_tiles) - tb;
+        jt0 += tb;
+        if (ntile <= 0) {
+            // an empty run: an empty partial (no weight) for every live row
+            if (warp >= 4) {
+                const int x = (warp >> 2) - 1, row = 32 * (warp & 3) + lane;
+                const int t = x * qpt + row / G;
+                if (row < qpt * G && t < w.nq) {
+                    const size_t pi = ((static_cast<size_t>(w.r) * p.max_q_len + w.i0 + t) * p.hq +
+                                       w.g * G + row % G) * p.kv_splits + w.s;
+                    *reinterpret_cast<float2 *>(p.ws_ml + pi * 2) = make_float2(-INFINITY, 0.f);
+                }
+            }
+            return;
+        }
+    }
     // query tiles with queries in them: a short chunk (a verify step of a few
     // queries) fills tile A only, and tile B's warps then stay idle
     const int nqt = w.nq > qpt ? 2 : 1;
@@ -318,6 +342,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         const float sl = fmaxf(fabsf(p.scale_log2), 1e-30f);
         float m_ref = -INFINITY, l = 0.f;
         bool abort = false;
+        const bool warp_live = __any_sync(0xffffffffu, valid_row);
         for (int32_t jj = 0; jj < ntile; ++jj) {
             const int ks = jj % kStages, buf = jj & 1;
             const int32_t tbase = (jt0 + jj) * kKeys;
@@ -333,6 +358,10 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&k_empty[ks]);
             tc::fence_after();
+            // a warp whose 32 rows hold no query (a short chunk fills only the
+            // first rows of the tile) leaves its S rows alone: the P.V product
+            // then writes only O rows that are never stored
+            if (warp_live) {
             float s[64];
             {
                 uint32_t r0[32], r1[32];
@@ -418,6 +447,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
                 tc::st16(sx + 16 * g, pk);
             }
             l = l * (resc ? alpha : 1.f) + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
+            }
             // V(jj) must have landed before this tile's P.V is issued.  Value
             // rows of keys outside [kv_lo, kv_hi) or of blocks not loaded hold
             // stale slots (possibly NaN): each warpgroup zeroes them before its
@@ -457,6 +487,25 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             done = done && mbar_wait(&pv_done[x], (ntile - 1) & 1);
             if (__any_sync(0xffffffffu, !done)) {
                 if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
+            } else if (split) {
+                // a partial: O unnormalised with its reference max and sum
+                tc::fence_after();
+                const size_t pi = ((static_cast<size_t>(w.r) * p.max_q_len + w.i0 + t) * p.hq +
+                                   w.g * G + row % G) * p.kv_splits + w.s;
+                float4 *dst = reinterpret_cast<float4 *>(p.ws_o + pi * kD);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t r32[32];
+                    tc::ld32(ox + c * 32, r32);
+                    tc::wait_ld();
+                    if (valid_row) {
+#pragma unroll
+                        for (int v = 0; v < 8; ++v)
+                            dst[c * 8 + v] = make_float4(__uint_as_float(r32[4 * v]), __uint_as_float(r32[4 * v + 1]),
+                                                         __uint_as_float(r32[4 * v + 2]), __uint_as_float(r32[4 * v + 3]));
+                    }
+                }
+                if (valid_row) *reinterpret_cast<float2 *>(p.ws_ml + pi * 2) = make_float2(m_ref, l);
             } else {
                 tc::fence_after();
                 const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -595,6 +644,59 @@ __global__ void __launch_bounds__(kPf32Threads) prefill_f32_kernel(const Prefill
 }
 
 // ---------------------------------------------------------------------------
+// merge of the key-range runs (bf16, short chunks): one warp per (row, query
+// of the chunk, q head).  M = max of the runs' reference maxima; each run is
+// weighted by 2^(m_s - M); out = sum w_s O_s / sum w_s l_s.
+// ---------------------------------------------------------------------------
+constexpr int kMergeWarps = 8;
+
+__global__ void __launch_bounds__(kMergeWarps * 32) prefill_merge_kernel(const PrefillParams p)
+{
+    constexpr int D = pf::kD;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t item = static_cast<int64_t>(blockIdx.x) * kMergeWarps + warp;
+    const int64_t total = static_cast<int64_t>(p.batch) * p.max_q_len * p.hq;
+    if (item >= total) return;
+    const int32_t h = static_cast<int32_t>(item % p.hq);
+    const int64_t ri = item / p.hq;
+    const int32_t i = static_cast<int32_t>(ri % p.max_q_len);
+    const int32_t r = static_cast<int32_t>(ri / p.max_q_len);
+    // the chunk length as the prefill kernel clamps it (call inputs: final
+    // before the wait, as the prefill kernel waited on earlier work itself)
+    const int32_t c0 = __ldg(p.cu_q_lens + r), c1 = __ldg(p.cu_q_lens + r + 1);
+    int32_t C = c1 - c0;
+    int32_t L = __ldg(p.seq_lens + r);
+    L = L < 0 ? 0 : (L > p.max_len ? p.max_len : L);
+    if (c0 < 0 || C < 0 || C > p.max_q_len || C > L)
+        C = c0 < 0 || C < 0 ? 0 : min(min(C, p.max_q_len), L);
+    if (i >= C) return;
+    pdl_wait();  // the partials come from the prefill kernel just before
+    const size_t base = ((static_cast<size_t>(r) * p.max_q_len + i) * p.hq + h) * p.kv_splits;
+    float M = -INFINITY;
+    for (int32_t s = 0; s < p.kv_splits; ++s) M = fmaxf(M, p.ws_ml[(base + s) * 2]);
+    float acc[D / 32];
+#pragma unroll
+    for (int e = 0; e < D / 32; ++e) acc[e] = 0.f;
+    float lsum = 0.f;
+    if (M != -INFINITY) {
+        for (int32_t s = 0; s < p.kv_splits; ++s) {
+            const float2 ml = *reinterpret_cast<const float2 *>(p.ws_ml + (base + s) * 2);
+            if (ml.x == -INFINITY) continue;  // an empty run wrote no values
+            const float wgt = fast_exp2(ml.x - M);
+            lsum = fmaf(wgt, ml.y, lsum);
+            const float *src = p.ws_o + (base + s) * D + lane;
+#pragma unroll
+            for (int e = 0; e < D / 32; ++e) acc[e] = fmaf(wgt, src[32 * e], acc[e]);
+        }
+    }
+    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out) +
+                         (static_cast<size_t>(c0 + i) * p.hq + h) * D + lane;
+#pragma unroll
+    for (int e = 0; e < D / 32; ++e) out[32 * e] = __float2bfloat16_rn(acc[e] * inv);
+}
+
+// ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
 bool prefill_shape_built(pkv_dtype dtype, int32_t D, int32_t bs, int32_t G)
@@ -610,10 +712,41 @@ int32_t prefill_queries_per_cta(pkv_dtype dtype, int32_t G)
     return dtype == PKV_BF16 ? pf::kQTiles * (pf::kRows / G) : kPf32Pairs / G;
 }
 
+PrefillSplit prefill_split_plan(int32_t batch, int32_t hq, int32_t hkv, int32_t D, int32_t bs,
+                                int32_t max_q_len, int32_t max_seq_len, int32_t window, int num_sms)
+{
+    PrefillSplit sp{1, 0};
+    if (hkv <= 0 || hq % hkv != 0 || batch <= 0 || max_q_len <= 0) return sp;
+    const int32_t G = hq / hkv;
+    if (D != pf::kD || bs != 16 || G < 1 || pf::kRows % G != 0) return sp;
+    if (max_q_len > pf::kRows / G) return sp;  // chunks that need both query tiles: no split
+    const int64_t ctas = static_cast<int64_t>(batch) * hkv;
+    const int64_t keys = window > 0 ? std::min<int64_t>(max_seq_len, static_cast<int64_t>(window) + max_q_len)
+                                    : max_seq_len;
+    // +1: a CTA's range may start inside a tile
+    const int64_t tiles = (keys + pf::kKeys - 1) / pf::kKeys + 1;
+    // about four CTAs per SM over the grid, at least 8 tiles (512 keys) per run
+    int64_t s = (4ll * std::max(num_sms, 1) + ctas - 1) / ctas;
+    s = std::min<int64_t>(s, tiles / 8);
+    s = std::max<int64_t>(1, std::min<int64_t>(s, 32));
+    if (s == 1) return sp;
+    sp.splits = static_cast<int32_t>(s);
+    sp.tiles = static_cast<int32_t>((tiles + s - 1) / s);
+    return sp;
+}
+
+size_t prefill_split_ws_bytes(int32_t batch, int32_t hq, int32_t max_q_len, const PrefillSplit &sp)
+{
+    if (sp.splits <= 1) return 0;
+    const size_t n = static_cast<size_t>(batch) * max_q_len * hq * sp.splits;
+    const size_t o = (n * pf::kD * sizeof(float) + 255) & ~static_cast<size_t>(255);
+    return o + n * 2 * sizeof(float);
+}
+
 cudaError_t launch_prefill_bf16(const PrefillParams &p, const CUtensorMap &kmap,
                                 const CUtensorMap &vmap, cudaStream_t stream)
 {
-    const int64_t ctas = static_cast<int64_t>(p.batch) * p.hkv * p.q_tiles;
+    const int64_t ctas = static_cast<int64_t>(p.batch) * p.hkv * p.q_tiles * p.kv_splits;
     if (ctas == 0) return cudaSuccess;
     cudaError_t err = cudaFuncSetAttribute(prefill_bf16_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -622,6 +755,12 @@ cudaError_t launch_prefill_bf16(const PrefillParams &p, const CUtensorMap &kmap,
     prof_begin(PKV_KERNEL_PREFILL, stream);
     err = launch_pdl(prefill_bf16_kernel, dim3(static_cast<unsigned>(ctas)), dim3(pf::kThreads),
                      pf::kLaunchBytes, stream, kmap, vmap, p);
+    if (err == cudaSuccess && p.kv_splits > 1) {
+        const int64_t items = static_cast<int64_t>(p.batch) * p.max_q_len * p.hq;
+        err = launch_pdl(prefill_merge_kernel,
+                         dim3(static_cast<unsigned>((items + kMergeWarps - 1) / kMergeWarps)),
+                         dim3(kMergeWarps * 32), 0, stream, p);
+    }
     prof_end(PKV_KERNEL_PREFILL, stream);
     return err;
 }

@@ -176,7 +176,11 @@ pkv_status paged_decode_attention_no_alloc(const void *q, int32_t num_q_heads,
                                            float scale, void *out, const pkv_prefix_desc *prefix,
                                            int32_t *dev_status, pkv_stream_t stream);
 
-/* Bytes of device workspace paged_prefill_chunk_attention needs. */
+/* Bytes of device workspace paged_prefill_chunk_attention needs on the
+ * current device: 0, except for short bf16 chunks (every C_r <= 128 / (Hq /
+ * Hkv), a speculative-verify step, say) on grids too small to fill the GPU,
+ * whose key ranges are then cut into runs whose fp32 partials a second kernel
+ * merges.  The cut depends only on the sizes and the SM count. */
 size_t paged_prefill_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                     int32_t head_dim, int32_t block_size, int32_t max_q_len,
                                     int32_t max_seq_len, int32_t window);
@@ -193,9 +197,11 @@ size_t paged_prefill_workspace_size(int32_t batch, int32_t num_q_heads, int32_t 
  *   q, out:      device [cu_q_lens[batch]][num_q_heads][head_dim], pool.dtype
  *   cu_q_lens:   device int32 [batch + 1], non-decreasing, cu_q_lens[0] = 0
  *   max_q_len:   host upper bound on C_r;  max_seq_len: host bound on seq_lens
+ *   workspace:   device, >= paged_prefill_workspace_size(...) bytes, 256-byte
+ *                aligned (NULL when that size is 0)
  * Built: bf16, block_size 16, head_dim 128, Hq / Hkv <= 16 (tcgen05 tensor
- * cores, fp32 accumulation in tensor memory; probabilities rounded to bf16
- * before the P.V product); f32 pools run a CUDA-core kernel.
+ * cores, fp32 accumulation in tensor memory; probabilities enter the P.V
+ * product as bf16 hi + lo terms); f32 pools run a CUDA-core kernel.
  */
 pkv_status paged_prefill_chunk_attention(const void *q, const int32_t *cu_q_lens,
                                          int32_t num_q_heads, const pkv_pool *pool,
