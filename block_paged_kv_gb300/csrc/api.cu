@@ -412,6 +412,8 @@ pkv_status paged_decode_attention(const void *q, int32_t num_q_heads, const pkv_
     p.ws_ml = reinterpret_cast<float *>(static_cast<char *>(workspace) +
                                         ws_o_bytes(batch, num_q_heads, pool->head_dim, pl));
     p.status = dev_status;
+    p.cu_q_lens = nullptr;  // one query per row
+    p.max_q = 1;
     p.batch = batch;
     p.hq = num_q_heads;
     p.hkv = pool->num_kv_heads;
@@ -442,6 +444,31 @@ pkv_status paged_decode_attention(const void *q, int32_t num_q_heads, const pkv_
     return err == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
+}  // extern "C"
+
+namespace {
+
+// Chunks whose (query, head) pairs of a kv head fit one 16-row decode tile
+// (verify steps of a few queries) run on the split-KV decode kernel.
+bool verify_on_decode(int32_t G, int32_t D, int32_t bs, int32_t max_q_len)
+{
+    return max_q_len >= 1 && static_cast<int64_t>(G) * max_q_len <= 16 &&
+           decode_shape_built(PKV_BF16, D, bs, G);
+}
+
+// The decode plan for a verify step: the key range of a row spans its
+// queries' windows.
+DecodePlan verify_plan(int32_t batch, int32_t hq, int32_t hkv, int32_t D, int32_t bs,
+                       int32_t max_len, int32_t window, int32_t max_q_len)
+{
+    return make_plan(batch, hq, hkv, D, bs, max_len, window > 0 ? window + max_q_len - 1 : 0,
+                     nullptr, PKV_BF16, num_sms_current());
+}
+
+}  // namespace
+
+extern "C" {
+
 size_t paged_prefill_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                     int32_t head_dim, int32_t block_size, int32_t max_q_len,
                                     int32_t max_seq_len, int32_t window)
@@ -449,7 +476,14 @@ size_t paged_prefill_workspace_size(int32_t batch, int32_t num_q_heads, int32_t 
     if (batch <= 0 || num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads != 0 ||
         max_q_len <= 0 || max_seq_len < 0 || window < 0)
         return 0;
-    // scratch only for the key-range runs of short bf16 chunks
+    // scratch only for short bf16 chunks: the decode kernel's split partials
+    // (a few queries per row), or the prefill kernel's key-range runs
+    const int32_t G = num_q_heads / num_kv_heads;
+    if (verify_on_decode(G, head_dim, block_size, max_q_len)) {
+        const DecodePlan pl = verify_plan(batch, num_q_heads, num_kv_heads, head_dim, block_size,
+                                          max_seq_len, window, max_q_len);
+        return ws_total_bytes(batch * max_q_len, num_q_heads, head_dim, pl);
+    }
     const PrefillSplit sp = prefill_split_plan(batch, num_q_heads, num_kv_heads, head_dim, block_size,
                                                max_q_len, max_seq_len, window, num_sms_current());
     return prefill_split_ws_bytes(batch, num_q_heads, max_q_len, sp);
@@ -472,9 +506,60 @@ pkv_status paged_prefill_chunk_attention(const void *q, const int32_t *cu_q_lens
         seq_lens == nullptr || max_blocks_per_seq <= 0 || !aligned16(q) || !aligned16(out))
         return PKV_ERR_INVALID_ARG;
     const int32_t G = num_q_heads / pool->num_kv_heads;
+    const int64_t cap = static_cast<int64_t>(max_blocks_per_seq) * pool->block_size;
+    if (pool->dtype == PKV_BF16 &&
+        verify_on_decode(G, pool->head_dim, pool->block_size, max_q_len)) {
+        // a few queries per row: the split-KV decode kernel with (query, head)
+        // M-rows, then its merge
+        const int32_t max_len = static_cast<int32_t>(std::min<int64_t>(max_seq_len, cap));
+        const DecodePlan pl = verify_plan(batch, num_q_heads, pool->num_kv_heads, pool->head_dim,
+                                          pool->block_size, max_len, window, max_q_len);
+        if (pl.n_suffix_ctas > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+        const int32_t prow = batch * max_q_len;
+        const size_t need = ws_total_bytes(prow, num_q_heads, pool->head_dim, pl);
+        if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+            ws_bytes < need)
+            return PKV_ERR_WORKSPACE;
+        DecodeParams d{};
+        d.q = q;
+        d.out = out;
+        d.k_pool = pool->k;
+        d.v_pool = pool->v;
+        d.tables = block_tables;
+        d.seq_lens = seq_lens;
+        d.group_of_row = nullptr;
+        d.prefix_blocks = nullptr;
+        d.num_groups = 0;
+        d.ws_o = static_cast<float *>(workspace);
+        d.ws_ml = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                            ws_o_bytes(prow, num_q_heads, pool->head_dim, pl));
+        d.status = dev_status;
+        d.cu_q_lens = cu_q_lens;
+        d.max_q = max_q_len;
+        d.batch = batch;
+        d.hq = num_q_heads;
+        d.hkv = pool->num_kv_heads;
+        d.group = G;
+        d.head_dim = pool->head_dim;
+        d.block_size = pool->block_size;
+        d.width = max_blocks_per_seq;
+        d.num_blocks = pool->num_blocks;
+        d.max_len = max_len;
+        d.window = window;
+        d.scale_log2 = scale * 1.4426950408889634f;
+        d.plan = pl;
+        if (!encode_fn_ready()) return PKV_ERR_CUDA;
+        CUtensorMap kmap, vmap;
+        if (!encode_pool_map_tile(&kmap, pool->k, *pool) ||
+            !encode_pool_map_tile(&vmap, pool->v, *pool))
+            return PKV_ERR_UNSUPPORTED;
+        cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+        cudaError_t err = launch_decode_bf16(d, kmap, vmap, st);
+        if (err == cudaSuccess) err = launch_decode_combine(d, pool->dtype, st);
+        return err == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    }
     if (!prefill_shape_built(pool->dtype, pool->head_dim, pool->block_size, G))
         return PKV_ERR_UNSUPPORTED;
-    const int64_t cap = static_cast<int64_t>(max_blocks_per_seq) * pool->block_size;
     PrefillParams p{};
     p.q = q;
     p.out = out;

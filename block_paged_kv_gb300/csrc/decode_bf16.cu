@@ -113,7 +113,7 @@ struct BlockIds {
     }
 };
 
-template <int D>
+template <int D, bool kMQ>
 __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
     decode_bf16_kernel(const __grid_constant__ CUtensorMap kmap,
                        const __grid_constant__ CUtensorMap vmap, const DecodeParams p)
@@ -152,7 +152,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
     // ---------------------------------------------------------------- work item
     const bool prefix_item = static_cast<int64_t>(blockIdx.x) < p.plan.n_prefix_ctas;
     int32_t b0, nblk, slot, tab_row, g, lo_all, hi_all, tiles;
-    int32_t row_r = 0;  // split item only
+    // split item only: the row, its query count and first packed query
+    int32_t row_r = 0, row_C = 1, row_q0 = 0;
+    // M-rows of a split item: the G heads of one query (decode), or (query,
+    // head) pairs of a row's few queries (kMQ: a verify step)
+    const int R = kMQ ? G * p.max_q : G;
     if (!prefix_item) {
         int64_t bid = static_cast<int64_t>(blockIdx.x) - p.plan.n_prefix_ctas;
         const int32_t s = static_cast<int32_t>(bid % p.plan.n_suffix_splits);
@@ -168,6 +172,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
         tab_row = row_r;
         lo_all = rr.lo;
         hi_all = rr.L;
+        row_C = rr.C;
+        row_q0 = rr.q0;
         tiles = 1;
     } else {
         tiles = C::kTiles;
@@ -247,7 +253,12 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
             const int row = i / kVec, v = i % kVec;
             int32_t qr = -1, qh = 0;
             if (!prefix_item) {
-                if (row < G) {
+                if constexpr (kMQ) {
+                    if (row < R && row / G < row_C) {
+                        qr = row_q0 + row / G;
+                        qh = g * G + row % G;
+                    }
+                } else if (row < G) {
                     qr = row_r;
                     qh = g * G + row;
                 }
@@ -327,8 +338,19 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
     const int c2 = 2 * (lane & 3);   // fragment columns c2, c2 + 1
     int lo0, hi0, lo1, hi1;
     if (!prefix_item) {
-        lo0 = lo1 = lo_all;
-        hi0 = hi1 = hi_all;
+        if constexpr (kMQ) {
+            // query t of the row sits at L - C + t: causal limit hi, window start lo
+            auto limits = [&](int row, int &lo, int &hi) {
+                const int t = row / G;
+                hi = (row < R && t < row_C) ? hi_all - row_C + t + 1 : 0;
+                lo = (p.window > 0 && hi > 0) ? max(0, hi - p.window) : 0;
+            };
+            limits(qd, lo0, hi0);
+            limits(qd + 8, lo1, hi1);
+        } else {
+            lo0 = lo1 = lo_all;
+            hi0 = hi1 = hi_all;
+        }
     } else {
         lo0 = lo1 = 0;
         const int k0 = tile * 16 + qd;
@@ -500,50 +522,52 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
 
     // split item: merge the four warps' partials of the one tile through
     // shared memory (the ring is free once every warp is past its last block)
-    float *mbuf = reinterpret_cast<float *>(stage_mem);  // [NW][G][D]
-    float *mlbuf = mbuf + NW * 16 * D;                    // [NW][G][2]
+    float *mbuf = reinterpret_cast<float *>(stage_mem);  // [NW][R][D]
+    float *mlbuf = mbuf + NW * 16 * D;                    // [NW][R][2], R <= 16
     __syncthreads();
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
         const int row = qd + half * 8;
-        if (row >= G) continue;
-        float *dst = mbuf + (warp * G + row) * D;
+        if (row >= R) continue;
+        float *dst = mbuf + (warp * R + row) * D;
 #pragma unroll
         for (int nt = 0; nt < C::kNT; ++nt)
             *reinterpret_cast<float2 *>(dst + nt * 8 + c2) =
                 make_float2(o[nt][2 * half], o[nt][2 * half + 1]);
         if ((lane & 3) == 0)
-            *reinterpret_cast<float2 *>(mlbuf + (warp * G + row) * 2) =
+            *reinterpret_cast<float2 *>(mlbuf + (warp * R + row) * 2) =
                 make_float2(half ? m1 : m0, half ? l1 : l0);
     }
     __syncthreads();
-    for (int idx = threadIdx.x; idx < G * D; idx += NW * 32) {
+    for (int idx = threadIdx.x; idx < R * D; idx += NW * 32) {
         const int row = idx / D, d = idx % D;
+        if (kMQ && row / G >= row_C) continue;  // no such query in this row
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < NW; ++w) M = fmaxf(M, mlbuf[(w * G + row) * 2]);
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, mlbuf[(w * R + row) * 2]);
         float acc = 0.f, lsum = 0.f;
         if (M != -INFINITY) {
 #pragma unroll
             for (int w = 0; w < NW; ++w) {
-                const float wgt = fast_exp2(mlbuf[(w * G + row) * 2] - M);
-                acc += wgt * mbuf[(w * G + row) * D + d];
-                lsum += wgt * mlbuf[(w * G + row) * 2 + 1];
+                const float wgt = fast_exp2(mlbuf[(w * R + row) * 2] - M);
+                acc += wgt * mbuf[(w * R + row) * D + d];
+                lsum += wgt * mlbuf[(w * R + row) * 2 + 1];
             }
         }
-        const size_t pi = partial_index(p, row_r, g * G + row, slot);
+        const size_t pi = kMQ ? partial_index(p, row_r, g * G + row % G, slot, row / G)
+                              : partial_index(p, row_r, g * G + row, slot);
         p.ws_o[pi * D + d] = acc;
         if (d == 0) *reinterpret_cast<float2 *>(p.ws_ml + pi * 2) = make_float2(M, lsum);
     }
 }
 
-template <int D>
+template <int D, bool kMQ>
 static cudaError_t launch_d(const DecodeParams &p, const CUtensorMap &kmap, const CUtensorMap &vmap,
                             cudaStream_t stream)
 {
     const int64_t ctas = p.plan.n_prefix_ctas + p.plan.n_suffix_ctas;
     if (ctas == 0) return cudaSuccess;
-    auto kern = decode_bf16_kernel<D>;
+    auto kern = decode_bf16_kernel<D, kMQ>;
     const int smem = Bf16Smem<D>::kLaunchBytes;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
@@ -561,10 +585,11 @@ static cudaError_t launch_d(const DecodeParams &p, const CUtensorMap &kmap, cons
 cudaError_t launch_decode_bf16(const DecodeParams &p, const CUtensorMap &kmap,
                                const CUtensorMap &vmap, cudaStream_t stream)
 {
+    const bool mq = p.cu_q_lens != nullptr;  // several queries per row
     switch (p.head_dim) {
-    case 64: return launch_d<64>(p, kmap, vmap, stream);
-    case 128: return launch_d<128>(p, kmap, vmap, stream);
-    case 256: return launch_d<256>(p, kmap, vmap, stream);
+    case 64: return mq ? launch_d<64, true>(p, kmap, vmap, stream) : launch_d<64, false>(p, kmap, vmap, stream);
+    case 128: return mq ? launch_d<128, true>(p, kmap, vmap, stream) : launch_d<128, false>(p, kmap, vmap, stream);
+    case 256: return mq ? launch_d<256, true>(p, kmap, vmap, stream) : launch_d<256, false>(p, kmap, vmap, stream);
     default: return cudaErrorInvalidValue;
     }
 }

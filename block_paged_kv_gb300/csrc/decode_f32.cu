@@ -260,18 +260,21 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
     const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int warp = wid % W, sub = wid / W;  // warp within the item, item within the CTA
     const int64_t item = static_cast<int64_t>(blockIdx.x) * IPC + sub;
-    const bool live = item < static_cast<int64_t>(p.batch) * p.hq * NCH;
-    const int64_t idx = live ? item / NCH : 0;  // (row, q head)
+    bool live = item < static_cast<int64_t>(p.batch) * p.max_q * p.hq * NCH;
+    const int64_t idx = live ? item / NCH : 0;  // ((row, query), q head)
     const int ch = static_cast<int>(item % NCH);
     // The row bookkeeping reads only call inputs: the decode kernel released
     // this grid after its own wait on earlier work, so they are final already.
-    const int32_t r = static_cast<int32_t>(idx / p.hq);
     const int32_t h = static_cast<int32_t>(idx % p.hq);
+    const int32_t r = static_cast<int32_t>(idx / p.hq / p.max_q);
+    const int32_t t = static_cast<int32_t>((idx / p.hq) % p.max_q);
     const RowRange rr = row_range(p, r, false);
+    live = live && t < rr.C;  // a row with fewer queries than max_q
     const int32_t npre = row_prefix_splits(p, rr);
-    const int32_t n = npre + row_suffix_splits(p, rr);
+    const int32_t n = live ? npre + row_suffix_splits(p, rr) : 0;
+    const int64_t out_row = static_cast<int64_t>(rr.q0) + t;  // packed query index
     pdl_wait();  // the partials come from the decode kernel just before
-    const size_t base = partial_index(p, r, h, 0);
+    const size_t base = partial_index(p, r, h, 0, t);
     auto slot_of = [&](int32_t k) { return k < npre ? k : p.plan.n_prefix_splits + (k - npre); };
 
     // this warp's maximum over its partials k = warp + W * i
@@ -310,7 +313,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
         // one warp per item: every lane already holds the item's sum
         if (!live) return;
         const float inv = lw > 0.f ? 1.f / lw : 0.f;
-        OutT *out = static_cast<OutT *>(p.out) + idx * D + lane;
+        OutT *out = static_cast<OutT *>(p.out) + (out_row * p.hq + h) * D + lane;
 #pragma unroll
         for (int e = 0; e < PER; ++e) out[32 * e] = to_out<OutT>(acc[e] * inv);
     } else {
@@ -335,7 +338,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
                 }
             }
             const float inv = L > 0.f ? 1.f / L : 0.f;
-            static_cast<OutT *>(p.out)[idx * D + ch * CH + threadIdx.x] = to_out<OutT>(o * inv);
+            static_cast<OutT *>(p.out)[(out_row * p.hq + h) * D + ch * CH + threadIdx.x] = to_out<OutT>(o * inv);
         }
     }
 }
@@ -344,7 +347,7 @@ template <typename OutT, int W>
 static cudaError_t launch_combine_w(const DecodeParams &p, cudaStream_t stream)
 {
     const int64_t chunks = (W == 1 || p.head_dim < 64) ? 1 : p.head_dim / 64;
-    const int64_t items = static_cast<int64_t>(p.batch) * p.hq * chunks;
+    const int64_t items = static_cast<int64_t>(p.batch) * p.max_q * p.hq * chunks;
     const int64_t ipc = kCombineWarps / W;
     const dim3 grid(static_cast<unsigned>((items + ipc - 1) / ipc)), block(kCombineWarps * 32);
     switch (p.head_dim) {

@@ -52,9 +52,14 @@ struct DecodeParams {
     const int32_t *seq_lens;
     const int32_t *group_of_row;   // nullptr when there is no prefix path
     const int32_t *prefix_blocks;
-    float *ws_o;   // [batch][hq][nslot][head_dim] unnormalised weighted values
-    float *ws_ml;  // [batch][hq][nslot][2]: running max (log2 units) and weight sum
+    float *ws_o;   // [batch * max_q][hq][nslot][head_dim] unnormalised weighted values
+    float *ws_ml;  // [batch * max_q][hq][nslot][2]: running max (log2 units) and weight sum
     int32_t *status;
+    // several queries per row (a speculative-verify step; bf16 only): row r
+    // owns the packed queries cu_q_lens[r] .. cu_q_lens[r+1]-1 at the last
+    // positions of its length, causally.  nullptr: one query per row (decode)
+    const int32_t *cu_q_lens;
+    int32_t max_q;  // queries per row, upper bound (1 for decode)
     int32_t batch, hq, hkv, group, head_dim, block_size, width, num_blocks;
     int32_t max_len;   // min(max_seq_len, width * block_size): lengths are clamped to it
     int32_t window;

@@ -123,11 +123,13 @@ def test_deterministic(pkv):
 
 
 def test_unsupported_shape_reported(pkv):
+    # head_dim 64 runs only as a short chunk (on the decode kernel); 8 queries
+    # x 3 heads per kv head do not fit its 16-row tile
     w = gen.prefill_workload(seed=73, dtype="bf16", num_q_heads=6, num_kv_heads=2, head_dim=64,
-                             prefix_lens=[10], chunk_lens=[4])
+                             prefix_lens=[10], chunk_lens=[8])
     d = Dev(w)
     with pytest.raises(pkv.PkvError) as e:
-        pkv.paged_prefill_chunk_attention(d.q, d.cu, d.k_pool, d.v_pool, d.tables, d.seq_lens, 4, 0,
+        pkv.paged_prefill_chunk_attention(d.q, d.cu, d.k_pool, d.v_pool, d.tables, d.seq_lens, 8, 0,
                                           w.scale)
     assert e.value.code == pkv.PKV_ERR_UNSUPPORTED
 
@@ -154,3 +156,23 @@ def test_verify_steps(pkv, orc, hq, hkv, window):
                              window=window)
     got, ref, _ = run_prefill(pkv, orc, w)
     assert_close(got, ref, "bf16", f"verify {hq}/{hkv} w{window}")
+
+
+
+@pytest.mark.parametrize("d,hq,hkv,chunks", [
+    (128, 32, 8, [4, 4, 2, 1, 3]),    # 4 queries x 4 heads fill the 16-row tile
+    (128, 16, 16, [8, 16, 1, 5, 9]),  # one head per kv head: up to 16 queries
+    (64, 8, 2, [4, 2, 4, 1, 3]),
+    (256, 8, 1, [2, 1, 2, 2, 1]),
+    (128, 48, 16, [5, 1, 3, 5, 2]),   # 3 heads per kv head
+])
+@pytest.mark.parametrize("window", [0, 40])
+def test_verify_steps_on_decode_kernel(pkv, orc, d, hq, hkv, chunks, window):
+    # (query, head) pairs of a kv head within 16: the split-KV decode kernel
+    # serves the chunk, one row of M per pair, causal within the chunk
+    w = gen.prefill_workload(seed=90 + d + hq + window, dtype="bf16", num_q_heads=hq,
+                             num_kv_heads=hkv, head_dim=d,
+                             prefix_lens=[100, 1000, 3000, 17, 0], chunk_lens=chunks,
+                             window=window)
+    got, ref, _ = run_prefill(pkv, orc, w)
+    assert_close(got, ref, "bf16", f"verify on decode d{d} {hq}/{hkv} w{window}")
