@@ -201,7 +201,10 @@ size_t paged_prefill_workspace_size(int32_t batch, int32_t num_q_heads, int32_t 
  *                aligned (NULL when that size is 0)
  * Built: bf16, block_size 16, head_dim 128, Hq / Hkv <= 16 (tcgen05 tensor
  * cores, fp32 accumulation in tensor memory; probabilities enter the P.V
- * product as bf16 hi + lo terms); f32 pools run a CUDA-core kernel.
+ * product as bf16 hi + lo terms); f32 pools run a CUDA-core kernel.  bf16
+ * chunks with max_q_len * (Hq / Hkv) <= 16 (a speculative-verify step) run on
+ * the split-KV decode kernel instead, one M-row per (query, head) pair, for
+ * head_dim 64, 128 or 256.
  */
 pkv_status paged_prefill_chunk_attention(const void *q, const int32_t *cu_q_lens,
                                          int32_t num_q_heads, const pkv_pool *pool,
