@@ -99,6 +99,8 @@ _lib.pkv_allocator_reserve.argtypes = [_vp, _i32, _i32]
 _lib.pkv_allocator_reserve.restype = ctypes.c_int
 _lib.pkv_allocator_publish.argtypes = [_vp, _i32, _vp, _i32, _vp]
 _lib.pkv_allocator_publish.restype = ctypes.c_int
+_lib.pkv_allocator_expire.argtypes = [_vp, _i32, _i32]
+_lib.pkv_allocator_expire.restype = ctypes.c_int
 _lib.pkv_allocator_release.argtypes = [_vp, _i32]
 _lib.pkv_allocator_release.restype = ctypes.c_int
 _lib.pkv_allocator_table.argtypes = [_vp, _i32, _vp, _i32, _i32p]
@@ -116,7 +118,8 @@ EXPORTED = ["paged_kv_append", "paged_decode_workspace_size", "paged_decode_atte
             "pkv_decode_plan", "pkv_version", "pkv_profile_enable", "pkv_profile_mask", "pkv_profile_read",
             "pkv_launch_count", "paged_decode_attention_no_alloc", "pkv_allocator_create",
             "pkv_allocator_destroy", "pkv_allocator_begin", "pkv_allocator_find_cached_prefix",
-            "pkv_allocator_reserve", "pkv_allocator_publish", "pkv_allocator_release",
+            "pkv_allocator_reserve", "pkv_allocator_publish", "pkv_allocator_expire",
+            "pkv_allocator_release",
             "pkv_allocator_table", "pkv_allocator_refcount", "pkv_allocator_stats"]
 
 
@@ -470,6 +473,11 @@ class BlockAllocator:
         t, tp = self._tokens(tokens)
         k, kp = self._keys(extra_keys)
         _check("pkv_allocator_publish", _lib.pkv_allocator_publish(self._a, req, tp, t.size, kp))
+
+    def expire(self, req: int, first_live_token: int) -> None:
+        """Drop the blocks wholly before ``first_live_token`` (a sliding
+        window's start); their table entries become -1."""
+        _check("pkv_allocator_expire", _lib.pkv_allocator_expire(self._a, req, int(first_live_token)))
 
     def release(self, req: int) -> None:
         _check("pkv_allocator_release", _lib.pkv_allocator_release(self._a, req))

@@ -87,6 +87,20 @@ struct pkv_allocator {
         ++grows;
     }
 
+    // one reference less; at zero a published block becomes cache-only (LRU
+    // tail), any other block free
+    void drop_ref(int32_t b)
+    {
+        Block &blk = blocks[b];
+        if (--blk.refcount > 0) return;
+        if (blk.published) {
+            blk.cached = true;
+            blk.lru_it = lru.insert(lru.end(), b);
+        } else {
+            free_set.insert(b);
+        }
+    }
+
     void evict_one()
     {
         const int32_t b = lru.front();
@@ -212,7 +226,7 @@ pkv_status pkv_allocator_publish(pkv_allocator *a, int32_t req, const int32_t *t
                                       extra_keys ? extra_keys[i] : 0);
         r.hashes.push_back(h);
         const int32_t b = r.table[i];
-        if (a->table.find(h) == a->table.end()) {
+        if (b >= 0 && a->table.find(h) == a->table.end()) {  // an expired entry: chain only
             a->table.emplace(h, b);
             a->blocks[b].published = true;
             a->blocks[b].hash = h;
@@ -222,21 +236,28 @@ pkv_status pkv_allocator_publish(pkv_allocator *a, int32_t req, const int32_t *t
     return PKV_OK;
 }
 
+pkv_status pkv_allocator_expire(pkv_allocator *a, int32_t req, int32_t first_live_token)
+{
+    if (a == nullptr || first_live_token < 0) return PKV_ERR_INVALID_ARG;
+    auto it = a->reqs.find(req);
+    if (it == a->reqs.end()) return PKV_ERR_INVALID_ARG;
+    std::vector<int32_t> &t = it->second.table;
+    const int64_t n = std::min<int64_t>(first_live_token / a->bs, static_cast<int64_t>(t.size()));
+    for (int64_t i = 0; i < n; ++i) {
+        if (t[i] < 0) continue;
+        a->drop_ref(t[i]);
+        t[i] = -1;
+    }
+    return PKV_OK;
+}
+
 pkv_status pkv_allocator_release(pkv_allocator *a, int32_t req)
 {
     if (a == nullptr) return PKV_ERR_INVALID_ARG;
     auto it = a->reqs.find(req);
     if (it == a->reqs.end()) return PKV_ERR_INVALID_ARG;
-    for (const int32_t b : it->second.table) {
-        Block &blk = a->blocks[b];
-        if (--blk.refcount > 0) continue;
-        if (blk.published) {
-            blk.cached = true;
-            blk.lru_it = a->lru.insert(a->lru.end(), b);
-        } else {
-            a->free_set.insert(b);
-        }
-    }
+    for (const int32_t b : it->second.table)
+        if (b >= 0) a->drop_ref(b);
     a->reqs.erase(it);
     return PKV_OK;
 }

@@ -350,6 +350,13 @@ pkv_status pkv_allocator_reserve(pkv_allocator *a, int32_t req, int32_t n_tokens
 pkv_status pkv_allocator_publish(pkv_allocator *a, int32_t req, const int32_t *tokens,
                                  int32_t n_tokens, const uint64_t *extra_keys);
 
+/* Sliding-window groups ("paged-cache.md", Gemma4 row and coordinator
+ * passage: expired sliding blocks are replaced by a null sentinel): every
+ * block of the table that lies wholly before first_live_token loses the
+ * request's reference (as in release) and its table entry becomes -1, the
+ * sentinel the decode never reads.  Table positions are kept (absolute). */
+pkv_status pkv_allocator_expire(pkv_allocator *a, int32_t req, int32_t first_live_token);
+
 /* release_request: every block of the table loses a reference; a published
  * block at refcount 0 becomes cache-only (LRU tail), an unpublished one free.
  * The id is retired. */

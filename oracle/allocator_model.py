@@ -131,20 +131,33 @@ class AllocatorModel:
                            extra_keys[i] if extra_keys is not None else 0)
             self.chains[r].append(h)
             b = self.tables[r][i]
-            if h not in self.block_of_hash:
+            if b >= 0 and h not in self.block_of_hash:
                 self.block_of_hash[h] = b
                 self.hash_of_block[b] = h
         self.done[r] = max(self.done[r], nfull)
 
+    def _drop(self, b: int) -> None:
+        self.refcount[b] -= 1
+        if self.refcount[b] > 0:
+            return
+        if b in self.hash_of_block:
+            self.lru.append(b)
+        else:
+            self.free = sorted(self.free + [b])
+
+    def expire(self, r: int, first_live_token: int) -> None:
+        """A sliding window's expired blocks: those wholly before
+        first_live_token leave the table (entry -1, the null sentinel)."""
+        t = self.tables[r]
+        for i in range(min(first_live_token // self.bs, len(t))):
+            if t[i] >= 0:
+                self._drop(t[i])
+                t[i] = -1
+
     def release(self, r: int) -> None:
         for b in self.tables.pop(r):
-            self.refcount[b] -= 1
-            if self.refcount[b] > 0:
-                continue
-            if b in self.hash_of_block:
-                self.lru.append(b)
-            else:
-                self.free = sorted(self.free + [b])
+            if b >= 0:
+                self._drop(b)
         del self.chains[r], self.done[r], self.fresh[r]
 
     # -- views ---------------------------------------------------------------

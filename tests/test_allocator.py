@@ -90,6 +90,22 @@ def test_shared_prompt_lifecycle_by_hand():
     assert m.table(c) == [0, 1, 3] and m.lru == []
 
 
+def test_sliding_expiry_by_hand():
+    bs = 4
+    m = AllocatorModel(bs, 8, 8)
+    toks = list(range(18))                      # 5 blocks, the last partial
+    r = m.begin()
+    m.reserve(r, len(toks))
+    m.publish(r, toks)                          # blocks 0..3 published
+    m.expire(r, 9)                              # window starts at token 9: blocks 0, 1 expire
+    assert m.table(r) == [-1, -1, 2, 3, 4]
+    assert m.lru == [0, 1] and m.refcount[0] == 0
+    s = m.begin()                               # the expired blocks still serve as a prefix
+    assert m.find_cached_prefix(s, toks[:8]) == 8 and m.table(s) == [0, 1]
+    m.release(r)
+    assert m.lru == [2, 3] and 4 in m.free
+
+
 def test_lru_eviction_order():
     bs = 1
     m = AllocatorModel(bs, 3, 3)
@@ -113,7 +129,8 @@ def _invariants(m: AllocatorModel):
     held = {}
     for t in m.tables.values():
         for b in t:
-            held[b] = held.get(b, 0) + 1
+            if b >= 0:
+                held[b] = held.get(b, 0) + 1
     for b in range(m.num_blocks):
         assert m.refcount[b] == held.get(b, 0)
     states = [set(m.free), set(m.lru), set(held)]
@@ -179,6 +196,13 @@ def test_library_matches_model_on_random_lifecycles(pkv, seed):
                 m.publish(r, toks)
                 a.publish(q, toks)
                 live[r] = (q, toks)
+        elif op == 2 and rng.integers(0, 2) == 0:
+            # a sliding window moves: expire the blocks before it
+            r = list(live)[rng.integers(0, len(live))]
+            q, toks = live[r]
+            first = int(rng.integers(0, len(toks) + 1))
+            m.expire(r, first)
+            a.expire(q, first)
         else:
             r = list(live)[rng.integers(0, len(live))]
             q, _ = live.pop(r)

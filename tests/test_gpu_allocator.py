@@ -65,3 +65,40 @@ def test_allocator_tables_decode_matches_oracle(pkv, orc):
     assert int(d.status.item()) == 0
     assert_close(to_f64(plain), ref, "bf16", "allocator tables, split path")
     assert_close(to_f64(shared), ref, "bf16", "allocator tables, shared-prefix path")
+
+
+def test_sliding_group_with_expired_blocks(pkv, orc):
+    # a sliding-window group: the allocator drops the blocks the window has
+    # left (-1 sentinels in the tables) and decode reads only live blocks
+    bs, pool, W = 16, 256, 64
+    a = pkv.BlockAllocator(bs, 32, pool)
+    prompts = [list(range(500)), list(range(1000, 1333)), list(range(40)), list(range(2000, 2100))]
+    reqs, lens = [], []
+    for p in prompts:
+        r = a.begin()
+        a.find_cached_prefix(r, p)
+        a.reserve(r, len(p) + 1)
+        a.publish(r, p)
+        a.expire(r, max(0, len(p) + 1 - W))        # the window after this step's token
+        reqs.append(r)
+        lens.append(len(p))
+    width = max(len(a.table(r)) for r in reqs)
+    tables = np.full((len(reqs), width), -1, dtype=np.int32)
+    for i, r in enumerate(reqs):
+        t = a.table(r)
+        tables[i, :len(t)] = t
+    assert (tables[0, :27] == -1).all() and (tables[0, 27:] >= 0).all()   # 501 - 64 = 437 -> 27 blocks gone
+    w = gen.decode_workload(seed=91, dtype="bf16", num_q_heads=8, num_kv_heads=2, head_dim=128,
+                            context_lens=lens, window=W, pool_blocks=pool, table_width=width,
+                            poison=False)
+    w = dataclasses.replace(w, block_tables=tables)
+    d = Dev(w)
+    slots = append(pkv, d)
+    or_slots, kp, vp = oracle_pools(orc, w)
+    assert np.array_equal(slots, or_slots)
+    ref = orc.decode(w.q, kp, vp, w.dtype, w.block_tables, w.seq_lens, W, w.scale)
+    got = pkv.paged_decode_attention(d.q, d.k_pool, d.v_pool, d.tables, d.seq_lens, W, w.scale,
+                                     status=d.status)
+    torch.cuda.synchronize()
+    assert int(d.status.item()) == 0
+    assert_close(to_f64(got), ref, "bf16", "sliding group with expired blocks")
