@@ -9,22 +9,25 @@
 // and both tiles share every K/V tile, so K/V are loaded once per 256 query
 // rows.  QK^T and PV are dense contractions and run on the 5th-generation
 // tensor cores:
-//   warps 0/2 TMA producers: K and V tiles of 128 keys (8 paged blocks, two
-//             64-dim boxes each) into 2-stage rings; a K stage is freed once
-//             both S products are computed, a V stage once both P.V are;
-//   warp 1    allocates tensor memory and issues tcgen05.mma from one elected
-//             lane: S_x = Q_x K^T into tensor memory (both operands K-major,
-//             128-byte swizzle), then O_x += P_x V with P read from tensor
-//             memory (V MN-major), in the order PV_A(j), S_A(j+1), PV_B(j),
-//             S_B(j+1);
+//   warps 0/2 TMA producers: K and V tiles of 64 keys (4 paged blocks, two
+//             64-dim boxes each) into 4-stage rings; a K stage is freed once
+//             both S products are computed and the key masks read, a V stage
+//             once both P.V products are;
+//   warps 1/3 issue tile A's / tile B's tcgen05.mma from one elected lane:
+//             S = Q K^T into one of the tile's two S buffers in tensor memory
+//             (both operands K-major, 128-byte swizzle), O += P V with P read
+//             from tensor memory (V MN-major); per K/V tile j: P(j).V, then
+//             S(j+2) into the buffer that product just read.  Warp 1 also
+//             allocates the 512 tensor-memory columns;
 //   warps 4-7 / 8-11  softmax of tile A / tile B, concurrently, one M-row per
 //             thread: S from tensor memory, causal / window / range mask,
 //             running max kept within 2^8 of the true maximum (O is rescaled
-//             in tensor memory only when it moves further), P written back over
-//             S as bf16 hi + lo terms, 8 columns each per 16 keys (P.V then carries P to
-//             ~2^-17 relative), and the epilogue O / l to global memory.
-//             S is read twice from tensor memory (row maximum, then P), which
-//             keeps a thread's live scores to 32 at a time.
+//             in tensor memory only when it moves further), P written back
+//             over S as bf16 hi + lo terms, 8 columns each per 16 keys (P.V
+//             then carries P to ~2^-17 relative), and the epilogue O / l.
+// A short chunk fills tile A only (tile B's warps stay idle, warps whose rows
+// hold no query skip the softmax work); on a grid too small for the GPU its
+// key range is cut into runs whose fp32 partials prefill_merge_kernel merges.
 // f32 kernel: CUDA cores, the same work split with 16 (query, head) pairs per
 // CTA, for the fp32 pools.
 #include <algorithm>
@@ -362,91 +365,91 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             // first rows of the tile) leaves its S rows alone: the P.V product
             // then writes only O rows that are never stored
             if (warp_live) {
-            float s[64];
-            {
-                uint32_t r0[32], r1[32];
-                tc::ld32(sx, r0);
-                tc::ld32(sx + 32, r1);
-                tc::wait_ld();
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    s[e] = __uint_as_float(r0[e]);
-                    s[32 + e] = __uint_as_float(r1[e]);
-                }
-            }
-            // a tile with any key outside this row's range takes the masked
-            // path: key column e is attended iff e - lo is in [0, qpos - qlo]
-            // and its block was loaded
-            const bool full = mask == (1u << kBlocks) - 1u && tbase >= qlo &&
-                              tbase + kKeys - 1 <= qpos && valid_row;
-            if (!full) {
-                const int32_t lo = qlo - tbase;
-                const uint32_t span = static_cast<uint32_t>(qpos - qlo);  // qlo <= qpos
-                const uint32_t bm = valid_row ? mask : 0u;
-#pragma unroll
-                for (int e = 0; e < 64; ++e) {
-                    const bool ok = static_cast<uint32_t>(e - lo) <= span && ((bm >> (e >> 4)) & 1u);
-                    s[e] = ok ? s[e] : -INFINITY;
-                }
-            }
-            float mt;
-            {
-                float m8[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) m8[e] = fmaxf(s[e], s[8 + e]);
-#pragma unroll
-                for (int c = 2; c < 8; ++c)
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) m8[e] = fmaxf(m8[e], s[8 * c + e]);
-                mt = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                           fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * sl;
-            }
-            // keep the reference max within 2^8 of the running max
-            const float new_ref = (mt > m_ref + static_cast<float>(kRescaleLog2)) ? mt : m_ref;
-            const float alpha = fast_exp2(m_ref - new_ref);  // 0 from -inf, 1 if unchanged
-            const bool resc = new_ref != m_ref && m_ref != -INFINITY;
-            if (__any_sync(0xffffffffu, resc)) {
-                // O_x holds P.V up to tile jj-1 once that product completes
-                if (jj > 0) {
-                    const bool done = mbar_wait(&pv_done[x], (jj - 1) & 1);
-                    if (__any_sync(0xffffffffu, !done)) {
-                        if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
-                        abort = true;
-                        break;
-                    }
-                    tc::fence_after();
-                }
-                const float f = resc ? alpha : 1.f;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t r32[32];
-                    tc::ld32(ox + c * 32, r32);
+                float s[64];
+                {
+                    uint32_t r0[32], r1[32];
+                    tc::ld32(sx, r0);
+                    tc::ld32(sx + 32, r1);
                     tc::wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) r32[e] = __float_as_uint(__uint_as_float(r32[e]) * f);
-                    tc::st32(ox + c * 32, r32);
+    #pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        s[e] = __uint_as_float(r0[e]);
+                        s[32 + e] = __uint_as_float(r1[e]);
+                    }
                 }
-                tc::wait_st();
-            }
-            m_ref = new_ref;
-            const float nmu = new_ref == -INFINITY ? 0.f : -new_ref;
-            float ls[4] = {0.f, 0.f, 0.f, 0.f};
-            // group g (16 keys) -> 8 columns of P hi then 8 of P lo, in place
-#pragma unroll
-            for (int g = 0; g < kBlocks; ++g) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float a = fast_exp2(fmaf(s[16 * g + 2 * e], sl, nmu));
-                    const float b = fast_exp2(fmaf(s[16 * g + 2 * e + 1], sl, nmu));
-                    ls[e & 3] += a + b;
-                    const uint32_t hi = pack_bf16x2(a, b);
-                    pk[e] = hi;
-                    pk[8 + e] = pack_bf16x2(a - bf16lo_to_f32(hi), b - bf16hi_to_f32(hi));
+                // a tile with any key outside this row's range takes the masked
+                // path: key column e is attended iff e - lo is in [0, qpos - qlo]
+                // and its block was loaded
+                const bool full = mask == (1u << kBlocks) - 1u && tbase >= qlo &&
+                                  tbase + kKeys - 1 <= qpos && valid_row;
+                if (!full) {
+                    const int32_t lo = qlo - tbase;
+                    const uint32_t span = static_cast<uint32_t>(qpos - qlo);  // qlo <= qpos
+                    const uint32_t bm = valid_row ? mask : 0u;
+    #pragma unroll
+                    for (int e = 0; e < 64; ++e) {
+                        const bool ok = static_cast<uint32_t>(e - lo) <= span && ((bm >> (e >> 4)) & 1u);
+                        s[e] = ok ? s[e] : -INFINITY;
+                    }
                 }
-                tc::st16(sx + 16 * g, pk);
-            }
-            l = l * (resc ? alpha : 1.f) + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
+                float mt;
+                {
+                    float m8[8];
+    #pragma unroll
+                    for (int e = 0; e < 8; ++e) m8[e] = fmaxf(s[e], s[8 + e]);
+    #pragma unroll
+                    for (int c = 2; c < 8; ++c)
+    #pragma unroll
+                        for (int e = 0; e < 8; ++e) m8[e] = fmaxf(m8[e], s[8 * c + e]);
+                    mt = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * sl;
+                }
+                // keep the reference max within 2^8 of the running max
+                const float new_ref = (mt > m_ref + static_cast<float>(kRescaleLog2)) ? mt : m_ref;
+                const float alpha = fast_exp2(m_ref - new_ref);  // 0 from -inf, 1 if unchanged
+                const bool resc = new_ref != m_ref && m_ref != -INFINITY;
+                if (__any_sync(0xffffffffu, resc)) {
+                    // O_x holds P.V up to tile jj-1 once that product completes
+                    if (jj > 0) {
+                        const bool done = mbar_wait(&pv_done[x], (jj - 1) & 1);
+                        if (__any_sync(0xffffffffu, !done)) {
+                            if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
+                            abort = true;
+                            break;
+                        }
+                        tc::fence_after();
+                    }
+                    const float f = resc ? alpha : 1.f;
+    #pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t r32[32];
+                        tc::ld32(ox + c * 32, r32);
+                        tc::wait_ld();
+    #pragma unroll
+                        for (int e = 0; e < 32; ++e) r32[e] = __float_as_uint(__uint_as_float(r32[e]) * f);
+                        tc::st32(ox + c * 32, r32);
+                    }
+                    tc::wait_st();
+                }
+                m_ref = new_ref;
+                const float nmu = new_ref == -INFINITY ? 0.f : -new_ref;
+                float ls[4] = {0.f, 0.f, 0.f, 0.f};
+                // group g (16 keys) -> 8 columns of P hi then 8 of P lo, in place
+    #pragma unroll
+                for (int g = 0; g < kBlocks; ++g) {
+                    uint32_t pk[16];
+    #pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float a = fast_exp2(fmaf(s[16 * g + 2 * e], sl, nmu));
+                        const float b = fast_exp2(fmaf(s[16 * g + 2 * e + 1], sl, nmu));
+                        ls[e & 3] += a + b;
+                        const uint32_t hi = pack_bf16x2(a, b);
+                        pk[e] = hi;
+                        pk[8 + e] = pack_bf16x2(a - bf16lo_to_f32(hi), b - bf16hi_to_f32(hi));
+                    }
+                    tc::st16(sx + 16 * g, pk);
+                }
+                l = l * (resc ? alpha : 1.f) + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
             }
             // V(jj) must have landed before this tile's P.V is issued.  Value
             // rows of keys outside [kv_lo, kv_hi) or of blocks not loaded hold
