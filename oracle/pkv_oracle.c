@@ -5,8 +5,9 @@
  * table with the CUDA library.
  *
  * Plain loops, no blocking, no fusion.  Inputs are read exactly (float32, or
- * bf16 widened bit-for-bit) and every sum, max, exp and division is carried
- * out in IEEE double.
+ * bf16 widened bit-for-bit, E4M3 codes decoded exactly) and every sum, max,
+ * exp and division is carried out in IEEE double; the one float32 step is the
+ * FP8 append's quotient x / scale, whose rounding decides the stored code.
  *
  * What it follows (page titles as printed at the top of each page):
  *   "paged-cache.md" (mlx-node): requests keep K/V in fixed-size blocks of a
@@ -30,7 +31,16 @@
  *   - window W > 0: the query at absolute position p attends positions
  *     max(0, p - W + 1) .. p; W = 0 is full attention;
  *   - seq_lens count the tokens just appended; the decode query sits at L - 1;
- *   - an empty key range gives an all-zero output.
+ *   - an empty key range gives an all-zero output;
+ *   - FP8 pools ("perf.md" quantisation table: the paged adapter keeps an FP8
+ *     KV cache with per-layer scales): each K/V element is one E4M3 code c
+ *     holding the value e4m3(c) * scale, with one float32 scale for the K
+ *     pool and one for the V pool of the layer; the append stores
+ *     c = nearest E4M3 code to the float32 quotient x / scale (ties to the
+ *     even code, magnitudes past 448 saturate to +-448); queries and new rows
+ *     are bf16.  An FP8 block holds 16 tokens and head_dim is a multiple of
+ *     64; the bytes of a (block, kv head) tile follow the order given at
+ *     fp8_k_byte / fp8_v_byte below (a storage format of this library).
  *
  * PLANT_* macros compile deliberate mistakes; the pin tests build those
  * variants to show that each mistake is caught.  The normal build defines none.
@@ -42,6 +52,7 @@
 
 #define OR_F32 0
 #define OR_BF16 1
+#define OR_FP8 2 /* E4M3 pools, bf16 queries and new rows */
 
 static double ld(const void *base, int dtype, size_t i)
 {
@@ -55,6 +66,88 @@ static double ld(const void *base, int dtype, size_t i)
 }
 
 static size_t esize(int dtype) { return dtype == OR_BF16 ? 2 : 4; }
+
+/* ---------------------------------------------------------------------------
+ * E4M3 ("FP8 Formats for Deep Learning", Micikevicius et al. 2022, the E4M3
+ * column of its format table): sign bit, 4 exponent bits with bias 7, 3
+ * mantissa bits.  Exponent field 0 holds the subnormals m * 2^-9; the code
+ * S.1111.111 is NaN; there is no infinity, so the largest magnitude is
+ * 1.75 * 2^8 = 448.
+ * ------------------------------------------------------------------------- */
+static double e4m3_value(uint8_t c)
+{
+    int e = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0)
+        v = ldexp((double)m, -9);
+    else
+        v = ldexp(1.0 + m / 8.0, e - 7);
+    return (c & 0x80) ? -v : v;
+}
+
+/* Nearest finite E4M3 code to x by search over every positive code; a tie
+ * between two neighbours goes to the one with an even code (mantissa lsb 0).
+ * 448 is the nearest finite value to anything larger, so the search itself
+ * saturates.  The sign bit is x's own (so -0.0 and negative values that
+ * round to zero give 0x80).  NaN gives 0x7F. */
+static uint8_t e4m3_encode(float x)
+{
+    if (isnan(x)) return 0x7F;
+    double a = fabs((double)x);
+    int best = 0;
+    double bd = INFINITY;
+    for (int c = 0; c <= 0x7E; ++c) {
+        double d = fabs(e4m3_value((uint8_t)c) - a);
+#ifdef PLANT_E4M3_TIES
+        if (d < bd || (d == bd && 0)) { /* wrong: ties go to the smaller magnitude */
+#else
+        if (d < bd || (d == bd && (c & 1) == 0)) {
+#endif
+            bd = d;
+            best = c;
+        }
+    }
+    return (uint8_t)(signbit(x) ? (best | 0x80) : best);
+}
+
+void or_e4m3_decode(const uint8_t *codes, int32_t n, double *out)
+{
+    for (int32_t i = 0; i < n; ++i) out[i] = e4m3_value(codes[i]);
+}
+
+void or_e4m3_encode(const float *x, int32_t n, uint8_t *out)
+{
+    for (int32_t i = 0; i < n; ++i) out[i] = e4m3_encode(x[i]);
+}
+
+/* Byte of (token t, dim d) inside one (block, kv head) tile of an FP8 pool
+ * (16 tokens, dim a multiple of 64).  The order is the operand order of the
+ * m16n8k16 tensor-core product, so that each of 32 threads finds its operand
+ * values as 16 consecutive bytes:
+ *   K: per 64-dim group, two 512-byte halves (tokens 0-7, 8-15); inside a
+ *      half, 16 bytes per (token t%8, pair class c) holding, for each of the
+ *      four 16-dim steps kk, the dims kk*16 + {2c, 2c+1, 2c+8, 2c+9};
+ *   V: per 32-dim group of 512 bytes, 16 bytes per (dim d%8, pair class c)
+ *      holding, for each of the four 8-dim steps, that dim's tokens
+ *      {2c, 2c+1, 2c+8, 2c+9}. */
+static size_t fp8_k_byte(int32_t t, int32_t d)
+{
+    int32_t r = d % 64, kk = r / 16, kap = r % 16;
+    int32_t c = (kap % 8) / 2, j = (kap % 2) + 2 * (kap / 8);
+    return (size_t)(d / 64) * 1024 + (size_t)(t / 8) * 512 + (size_t)((t % 8) * 4 + c) * 16 +
+           (size_t)(kk * 4 + j);
+}
+
+static size_t fp8_v_byte(int32_t t, int32_t d)
+{
+#ifdef PLANT_FP8_VPERM
+    int32_t c = (t % 8) / 2, j = (t % 2) * 2 + (t / 8); /* wrong: token pair order swapped */
+#else
+    int32_t c = (t % 8) / 2, j = (t % 2) + 2 * (t / 8);
+#endif
+    return (size_t)(d / 32) * 512 + (size_t)((d % 8) * 4 + c) * 16 + (size_t)(((d % 32) / 8) * 4 + j);
+}
 
 /* Pool element (block b, kv head g, slot offset t, dim d). */
 static size_t pool_index(int32_t hkv, int32_t bs, int32_t dim, int32_t b, int32_t g, int32_t t,
@@ -95,15 +188,18 @@ int32_t or_slot_mapping(const int32_t *tables, int32_t width, int32_t batch, int
 
 /* ---------------------------------------------------------------------------
  * Append: copy token i's K and V rows for every kv head into its slot.
- * Storage is copied byte for byte.  Returns the number of tokens skipped for a
- * slot past the pool (negative slots are skipped silently).
+ * Storage is copied byte for byte; into an FP8 pool each bf16 element x is
+ * stored as the code e4m3_encode(float32(x) / scale) (float32 division), at
+ * its byte of the tile.  Returns the number of tokens skipped for a slot past
+ * the pool (negative slots are skipped silently).
  * ------------------------------------------------------------------------- */
 int32_t or_append(void *k_pool, void *v_pool, int32_t dtype, int32_t num_blocks, int32_t hkv,
                   int32_t bs, int32_t dim, const int32_t *slots, int32_t n, const void *k_new,
-                  const void *v_new)
+                  const void *v_new, float k_scale, float v_scale)
 {
     size_t es = esize(dtype), row = (size_t)dim * es;
     int32_t bad = 0;
+    if (dtype == OR_FP8 && (bs != 16 || dim % 64 != 0)) return -1;
     for (int32_t i = 0; i < n; ++i) {
         int32_t s = slots[i];
         if (s < 0) continue;
@@ -115,6 +211,18 @@ int32_t or_append(void *k_pool, void *v_pool, int32_t dtype, int32_t num_blocks,
 #else
             int32_t gs = g;
 #endif
+            if (dtype == OR_FP8) {
+                uint8_t *kt = (uint8_t *)k_pool + ((size_t)b * hkv + g) * (size_t)(bs * dim);
+                uint8_t *vt = (uint8_t *)v_pool + ((size_t)b * hkv + g) * (size_t)(bs * dim);
+                size_t src = ((size_t)i * hkv + gs) * (size_t)dim;
+                for (int32_t d = 0; d < dim; ++d) {
+                    float kx = (float)ld(k_new, OR_BF16, src + d);
+                    float vx = (float)ld(v_new, OR_BF16, src + d);
+                    kt[fp8_k_byte(t, d)] = e4m3_encode(kx / k_scale);
+                    vt[fp8_v_byte(t, d)] = e4m3_encode(vx / v_scale);
+                }
+                continue;
+            }
             size_t dst = pool_index(hkv, bs, dim, b, g, t, 0) * es;
             size_t src = ((size_t)i * hkv + gs) * row;
             memcpy((char *)k_pool + dst, (const char *)k_new + src, row);
@@ -136,7 +244,22 @@ struct view {
     int32_t dtype, num_blocks, hkv, bs, dim;
     const int32_t *tables;
     int32_t width;
+    double k_scale, v_scale; /* FP8 pools only */
 };
+
+/* The query's element type: bf16 beside FP8 pools, else the pools' own. */
+static int q_dtype(int32_t dtype) { return dtype == OR_FP8 ? OR_BF16 : dtype; }
+
+/* K (is_v = 0) or V (is_v = 1) element (block b, kv head g, slot t, dim d). */
+static double kv_ld(const struct view *w, int is_v, int32_t b, int32_t g, int32_t t, int32_t d)
+{
+    const void *pool = is_v ? w->v_pool : w->k_pool;
+    if (w->dtype != OR_FP8)
+        return ld(pool, w->dtype, pool_index(w->hkv, w->bs, w->dim, b, g, t, d));
+    size_t tile = ((size_t)b * w->hkv + g) * (size_t)(w->bs * w->dim);
+    size_t off = is_v ? fp8_v_byte(t, d) : fp8_k_byte(t, d);
+    return e4m3_value(((const uint8_t *)pool)[tile + off]) * (is_v ? w->v_scale : w->k_scale);
+}
 
 static int attend(const struct view *w, const void *q, size_t qoff, int32_t r, int32_t g,
                   int32_t lo, int32_t hi, double scale, double *out)
@@ -164,8 +287,7 @@ static int attend(const struct view *w, const void *q, size_t qoff, int32_t r, i
 #endif
         double acc = 0.0;
         for (int32_t d = 0; d < dim; ++d)
-            acc += ld(q, w->dtype, qoff + d) *
-                   ld(w->k_pool, w->dtype, pool_index(w->hkv, w->bs, dim, blk[j], g, t, d));
+            acc += ld(q, q_dtype(w->dtype), qoff + d) * kv_ld(w, 0, blk[j], g, t, d);
 #ifdef PLANT_NO_SCALE
         s[j] = acc;
 #else
@@ -182,7 +304,7 @@ static int attend(const struct view *w, const void *q, size_t qoff, int32_t r, i
         if (j == n - 1 && n > 1) continue; /* wrong: last value never accumulated */
 #endif
         for (int32_t d = 0; d < dim; ++d)
-            out[d] += e * ld(w->v_pool, w->dtype, pool_index(w->hkv, w->bs, dim, blk[j], g, t, d));
+            out[d] += e * kv_ld(w, 1, blk[j], g, t, d);
     }
     for (int32_t d = 0; d < dim; ++d) out[d] /= l;
     free(s);
@@ -228,9 +350,11 @@ static int decode_one(const struct view *w, const void *q, int32_t hq, const int
 int32_t or_decode(const void *q, const void *k_pool, const void *v_pool, int32_t dtype,
                   int32_t num_blocks, int32_t hq, int32_t hkv, int32_t bs, int32_t dim,
                   const int32_t *tables, int32_t width, const int32_t *seq_lens, int32_t batch,
-                  int32_t window, double scale, double *out)
+                  int32_t window, double scale, double k_scale, double v_scale, double *out)
 {
-    struct view w = {k_pool, v_pool, dtype, num_blocks, hkv, bs, dim, tables, width};
+    struct view w = {k_pool, v_pool, dtype, num_blocks, hkv, bs, dim, tables, width, k_scale,
+                     v_scale};
+    if (dtype == OR_FP8 && (bs != 16 || dim % 64 != 0)) return -1;
     int32_t bad = 0;
     for (int32_t r = 0; r < batch; ++r)
         for (int32_t h = 0; h < hq; ++h)
@@ -244,10 +368,12 @@ int32_t or_decode(const void *q, const void *k_pool, const void *v_pool, int32_t
 int32_t or_decode_pairs(const void *q, const void *k_pool, const void *v_pool, int32_t dtype,
                         int32_t num_blocks, int32_t hq, int32_t hkv, int32_t bs, int32_t dim,
                         const int32_t *tables, int32_t width, const int32_t *seq_lens,
-                        int32_t window, double scale, const int32_t *rows, const int32_t *heads,
-                        int32_t npairs, double *out)
+                        int32_t window, double scale, double k_scale, double v_scale,
+                        const int32_t *rows, const int32_t *heads, int32_t npairs, double *out)
 {
-    struct view w = {k_pool, v_pool, dtype, num_blocks, hkv, bs, dim, tables, width};
+    struct view w = {k_pool, v_pool, dtype, num_blocks, hkv, bs, dim, tables, width, k_scale,
+                     v_scale};
+    if (dtype == OR_FP8 && (bs != 16 || dim % 64 != 0)) return -1;
     int32_t bad = 0;
     for (int32_t i = 0; i < npairs; ++i)
         if (decode_one(&w, q, hq, seq_lens, window, scale, rows[i], heads[i],
@@ -281,9 +407,11 @@ int32_t or_prefill(const void *q, const int32_t *cu_q_lens, const void *k_pool,
                    const void *v_pool, int32_t dtype, int32_t num_blocks, int32_t hq, int32_t hkv,
                    int32_t bs, int32_t dim, const int32_t *tables, int32_t width,
                    const int32_t *seq_lens, int32_t batch, int32_t window, double scale,
-                   double *out)
+                   double k_scale, double v_scale, double *out)
 {
-    struct view w = {k_pool, v_pool, dtype, num_blocks, hkv, bs, dim, tables, width};
+    struct view w = {k_pool, v_pool, dtype, num_blocks, hkv, bs, dim, tables, width, k_scale,
+                     v_scale};
+    if (dtype == OR_FP8 && (bs != 16 || dim % 64 != 0)) return -1;
     int32_t bad = 0;
     for (int32_t r = 0; r < batch; ++r)
         for (int32_t i = 0; i < cu_q_lens[r + 1] - cu_q_lens[r]; ++i)
@@ -299,10 +427,12 @@ int32_t or_prefill_samples(const void *q, const int32_t *cu_q_lens, const void *
                            const void *v_pool, int32_t dtype, int32_t num_blocks, int32_t hq,
                            int32_t hkv, int32_t bs, int32_t dim, const int32_t *tables,
                            int32_t width, const int32_t *seq_lens, int32_t window, double scale,
-                           const int32_t *rows, const int32_t *qidx, const int32_t *heads,
-                           int32_t n, double *out)
+                           double k_scale, double v_scale, const int32_t *rows,
+                           const int32_t *qidx, const int32_t *heads, int32_t n, double *out)
 {
-    struct view w = {k_pool, v_pool, dtype, num_blocks, hkv, bs, dim, tables, width};
+    struct view w = {k_pool, v_pool, dtype, num_blocks, hkv, bs, dim, tables, width, k_scale,
+                     v_scale};
+    if (dtype == OR_FP8 && (bs != 16 || dim % 64 != 0)) return -1;
     int32_t bad = 0;
     for (int32_t k = 0; k < n; ++k)
         if (prefill_one(&w, q, hq, cu_q_lens, seq_lens, window, scale, rows[k], qidx[k], heads[k],

@@ -293,6 +293,38 @@ def prefill_workload(*, seed: int, dtype: str, num_q_heads: int, num_kv_heads: i
 
 
 # ---------------------------------------------------------------------------
+# FP8 pools
+# ---------------------------------------------------------------------------
+
+# per-layer scales of the FP8 K and V pools ("perf.md" quantisation table: the
+# paged adapter's FP8 KV cache keeps one scale per layer); deliberately not
+# powers of two, so that the quotient's rounding matters
+FP8_K_SCALE = np.float32(0.0123)
+FP8_V_SCALE = np.float32(0.0171)
+FP8_POISON = 0x7F   # the E4M3 NaN code: what an FP8 pool holds before any write
+
+
+def live_slots(w: Workload):
+    """Every pool slot that holds context in ``w`` (not poisoned, not one of
+    this step's append targets) with its K and V rows: ``(slots, k_rows,
+    v_rows)``, rows ``[n, Hkv, D]`` in storage form.  An FP8 pool is filled by
+    appending exactly these rows, so that it holds the same context as the
+    bf16 pool of the workload."""
+    live = ~np.isnan(as_f32(w.k_pool[:, 0, :, 0], w.dtype))
+    b, t = np.nonzero(live)
+    slots = (b * w.block_size + t).astype(np.int32)
+    return slots, np.ascontiguousarray(w.k_pool[b, :, t, :]), np.ascontiguousarray(w.v_pool[b, :, t, :])
+
+
+def fp8_empty_pools(w: Workload):
+    """Two FP8 pools for ``w`` (uint8 tile bytes ``[nb, Hkv, 16 * D]``), every
+    byte the poison code."""
+    assert w.block_size == 16
+    shape = (w.num_blocks, w.num_kv_heads, 16 * w.head_dim)
+    return np.full(shape, FP8_POISON, np.uint8), np.full(shape, FP8_POISON, np.uint8)
+
+
+# ---------------------------------------------------------------------------
 # The five workloads (seed = 1000 + index)
 # ---------------------------------------------------------------------------
 

@@ -16,6 +16,12 @@ What pins what:
                          (one key, zero query, equal keys, window 1, window
                          >= length, one dominant key); shared blocks == private
                          copies; physical block relabelling.
+  * E4M3 codec        -> the published format table's values, the grid's
+                         spacing, round trips, worked ties and saturation, a
+                         brute-force nearest search;
+  * FP8 tile layout   -> the PTX ISA's m16n8k16 B-fragment table;
+  * FP8 append/attend -> the codec on float32 quotients; dense attention on
+                         pools dequantized through the fragment table;
   * prefix groups     -> the pages' worked full-block example (a 1400-token
                          prompt at block size 16 has full blocks up to 1392,
                          "paged-cache.md" GDN ladder section) and the defining
@@ -374,6 +380,188 @@ def pin_prefix_groups_properties(orc):
             assert not same or all(gor[s] < 0 for s in same)
 
 
+# ---------------------------------------------------------------------------
+# FP8 (E4M3) pools
+# ---------------------------------------------------------------------------
+
+def pin_e4m3_published_values(orc):
+    # the E4M3 column of the format table in "FP8 Formats for Deep Learning"
+    # (Micikevicius et al. 2022): bias 7, max normal S.1111.110 = 448, min
+    # normal S.0001.000 = 2^-6, max subnormal S.0000.111 = 0.875 * 2^-6, min
+    # subnormal S.0000.001 = 2^-9, NaN S.1111.111, no infinities
+    codes = np.array([0x7E, 0x08, 0x07, 0x01, 0x38, 0xC0, 0x00], np.uint8)
+    want = [448.0, 2.0 ** -6, 0.875 * 2.0 ** -6, 2.0 ** -9, 1.0, -2.0, 0.0]
+    assert orc.e4m3_decode(codes).tolist() == want
+    assert np.isnan(orc.e4m3_decode(np.array([0x7F, 0xFF], np.uint8))).all()
+    negz = orc.e4m3_decode(np.array([0x80], np.uint8))[0]
+    assert negz == 0.0 and math.copysign(1.0, negz) < 0
+
+
+def pin_e4m3_grid_and_round_trip(orc):
+    v = orc.e4m3_decode(np.arange(0x7F, dtype=np.uint8))
+    # 3 mantissa bits: steps of 2^-9 through the subnormals and the first
+    # binade, then the step doubles with every binade
+    steps = np.diff(v)
+    for c in range(0x7E):
+        e = max(c >> 3, 1)   # binade of the lower code
+        assert steps[c] == 2.0 ** (e - 10), c
+    neg = orc.e4m3_decode(np.arange(0x80, 0xFF, dtype=np.uint8))
+    assert np.array_equal(neg, -v)
+    # every finite code is its own nearest code
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], np.uint8)
+    x = orc.e4m3_decode(codes).astype(np.float32)
+    x[codes == 0x80] = np.float32(-0.0)
+    assert np.array_equal(orc.e4m3_encode(x), codes)
+
+
+def pin_e4m3_rounding(orc):
+    # worked cases: ties go to the even code, magnitudes past 448 saturate
+    x = np.array([1.0625, 1.1875, 2.0 ** -10, -(2.0 ** -10), 3 * 2.0 ** -11, 460.0, 1e6, -1e6,
+                  np.inf, 1.0 / 3.0, 0.0], np.float32)
+    want = [0x38, 0x3A, 0x00, 0x80, 0x01, 0x7E, 0x7E, 0xFE, 0x7E, 0x2B, 0x00]
+    assert orc.e4m3_encode(x).tolist() == want
+    # every midpoint between neighbouring codes goes to the even one
+    v = orc.e4m3_decode(np.arange(0x7F, dtype=np.uint8))
+    mid = ((v[:-1] + v[1:]) / 2).astype(np.float32)
+    assert np.array_equal(mid.astype(np.float64), (v[:-1] + v[1:]) / 2)   # exact in float32
+    got = orc.e4m3_encode(mid).astype(int)
+    lo = np.arange(0x7E)
+    assert np.array_equal(got, np.where(lo % 2 == 0, lo, lo + 1))
+    # off the midpoints the code is the nearest value (brute force over the grid)
+    r = gen.uniform(gen.stream_seed(5, "e4m3"), 4000)
+    x = (np.where(r[:2000] < 0.5, -1.0, 1.0) * 2.0 ** (r[2000:] * 22 - 12)).astype(np.float32)
+    c = orc.e4m3_encode(x)
+    dist = np.abs(np.abs(x.astype(np.float64))[:, None] - v[None, :])
+    assert np.array_equal(c & 0x7F, np.argmin(dist, axis=1).astype(np.uint8))
+    assert np.array_equal(c >> 7, (x < 0).astype(np.uint8))
+
+
+def _mma_b_fragment(lane: int, i: int):
+    """Row k and column n of element i (0..3) of the B fragment that thread
+    `lane` holds in mma.m16n8k16 with 16-bit operands (PTX ISA, the figure of
+    the B fragment layout for .f16/.bf16): groupID = lane / 4,
+    threadID_in_group = lane % 4, k = threadID_in_group * 2 + (i % 2) + 8 * (i >= 2),
+    n = groupID."""
+    return (lane % 4) * 2 + (i % 2) + (8 if i >= 2 else 0), lane // 4
+
+
+def fp8_tile_map(D: int):
+    """(token, dim) of every byte of an FP8 K tile and V tile, from the
+    fragment table: the K tile is the B operand of Q K^T (k = dim, n = token;
+    per 64 dims two halves of 8 tokens, each lane's 16 bytes = its fragments
+    of the four 16-dim steps), the V tile that of P V (k = token, n = dim;
+    per 32 dims each lane's 16 bytes = its fragments of the four 8-dim steps)."""
+    kt, kd, vt, vd = (np.full(16 * D, -1) for _ in range(4))
+    for lane in range(32):
+        for s in range(4):
+            for i in range(4):
+                k, n = _mma_b_fragment(lane, i)
+                for grp in range(D // 64):
+                    for half in range(2):
+                        o = grp * 1024 + half * 512 + lane * 16 + s * 4 + i
+                        kt[o], kd[o] = half * 8 + n, grp * 64 + s * 16 + k
+                for grp in range(D // 32):
+                    o = grp * 512 + lane * 16 + s * 4 + i
+                    vt[o], vd[o] = k, grp * 32 + s * 8 + n
+    return kt, kd, vt, vd
+
+
+def fp8_dequantized(orc, pool: np.ndarray, scale, D: int, is_v: bool) -> np.ndarray:
+    """An FP8 pool's values as float64 [nb, Hkv, 16, D] (code value * scale)."""
+    kt, kd, vt, vd = fp8_tile_map(D)
+    t, d = (vt, vd) if is_v else (kt, kd)
+    vals = orc.e4m3_decode(pool) * float(scale)
+    out = np.empty(pool.shape[:2] + (16, D))
+    out[:, :, t, d] = vals
+    return out
+
+
+def pin_fp8_tile_layout(orc):
+    # one token at a time into a fresh pool: the code of value 0x20 + d marks
+    # where (t, d) lands
+    for D in (64, 128):
+        kt, kd, vt, vd = fp8_tile_map(D)
+        assert sorted(zip(kt, kd)) == [(t, d) for t in range(16) for d in range(D)]
+        assert sorted(zip(vt, vd)) == [(t, d) for t in range(16) for d in range(D)]
+        codes = (0x20 + np.arange(D) % 64).astype(np.uint8)
+        row = gen.bf16_bits(orc.e4m3_decode(codes).astype(np.float32)).reshape(1, 1, D)
+        for t in range(16):
+            kp = np.full((1, 1, 16 * D), 0x7F, np.uint8)
+            vp = kp.copy()
+            orc.append(kp, vp, "fp8", np.array([t], np.int32), row, row, 1.0, 1.0)
+            for pool, (tt, dd) in ((kp, (kt, kd)), (vp, (vt, vd))):
+                mine = tt == t
+                assert np.array_equal(pool[0, 0, mine], codes[dd[mine]]), (D, t)
+                assert (pool[0, 0, ~mine] == 0x7F).all()
+
+
+def pin_fp8_append_quantizes(orc):
+    w = small_decode(seed=37, dtype="bf16", hq=4, hkv=2, d=64, ctx=(5, 30), bs=16)
+    kp, vp = gen.fp8_empty_pools(w)
+    slots = oracle_slots(orc, w)
+    ks, vs = gen.FP8_K_SCALE, gen.FP8_V_SCALE
+    orc.append(kp, vp, "fp8", slots, w.k_new, w.v_new, ks, vs)
+    kt, kd, vt, vd = fp8_tile_map(64)
+    for i, s in enumerate(slots):
+        b, t = divmod(int(s), 16)
+        for pool, new, sc, (tt, dd) in ((kp, w.k_new, ks, (kt, kd)), (vp, w.v_new, vs, (vt, vd))):
+            mine = tt == t
+            q = gen.bf16_to_f32(new[i]) / np.float32(sc)         # float32 quotient
+            assert q.dtype == np.float32
+            assert np.array_equal(pool[b][:, mine], orc.e4m3_encode(q)[:, dd[mine]])
+    touched = np.zeros(kp.shape[0], bool)
+    touched[slots // 16] = True
+    assert (kp[~touched] == 0x7F).all() and (vp[~touched] == 0x7F).all()
+
+
+def _fp8_context(orc, w):
+    kp, vp = gen.fp8_empty_pools(w)
+    ks, vs = gen.FP8_K_SCALE, gen.FP8_V_SCALE
+    s, kr, vr = gen.live_slots(w)
+    orc.append(kp, vp, "fp8", s, kr, vr, ks, vs)
+    orc.append(kp, vp, "fp8", oracle_slots(orc, w), w.k_new, w.v_new, ks, vs)
+    return kp, vp
+
+
+def pin_fp8_decode_equals_dense(orc):
+    for seed, ctx, window, prefix in ((41, (1, 17, 40, 77), 0, 0), (43, (33, 64, 90), 20, 32)):
+        w = small_decode(seed=seed, dtype="bf16", hq=8, hkv=2, d=64, ctx=ctx, bs=16,
+                         window=window, prefix=prefix)
+        kp, vp = _fp8_context(orc, w)
+        out = orc.decode(w.q, kp, vp, "fp8", w.block_tables, w.seq_lens, w.window, w.scale,
+                         k_scale=gen.FP8_K_SCALE, v_scale=gen.FP8_V_SCALE)
+        K = fp8_dequantized(orc, kp, gen.FP8_K_SCALE, 64, False)
+        V = fp8_dequantized(orc, vp, gen.FP8_V_SCALE, 64, True)
+        q = f64(w.q, "bf16")
+        for r in range(w.batch):
+            L = int(w.seq_lens[r])
+            lo = max(0, L - w.window) if w.window > 0 else 0
+            for h in range(w.num_q_heads):
+                g = h // 4
+                ref = dense_attention(q[r, h], gather_row(K, w.block_tables, r, g, lo, L, 16),
+                                      gather_row(V, w.block_tables, r, g, lo, L, 16), w.scale)
+                assert np.allclose(out[r, h], ref, rtol=1e-12, atol=1e-12), (seed, r, h)
+
+
+def pin_fp8_prefill_equals_dense_causal(orc):
+    w = gen.prefill_workload(seed=47, dtype="bf16", num_q_heads=4, num_kv_heads=2, head_dim=64,
+                             prefix_lens=[0, 21, 40], chunk_lens=[9, 16, 3])
+    kp, vp = _fp8_context(orc, w)
+    out = orc.prefill(w.q, w.cu_q_lens, kp, vp, "fp8", w.block_tables, w.seq_lens, 0, w.scale,
+                      k_scale=gen.FP8_K_SCALE, v_scale=gen.FP8_V_SCALE)
+    K = fp8_dequantized(orc, kp, gen.FP8_K_SCALE, 64, False)
+    V = fp8_dequantized(orc, vp, gen.FP8_V_SCALE, 64, True)
+    q = f64(w.q, "bf16")
+    for r in range(w.batch):
+        c0, c1, L = int(w.cu_q_lens[r]), int(w.cu_q_lens[r + 1]), int(w.seq_lens[r])
+        for i in range(c1 - c0):
+            p = L - (c1 - c0) + i
+            for h in range(4):
+                ref = dense_attention(q[c0 + i, h], gather_row(K, w.block_tables, r, h // 2, 0, p + 1, 16),
+                                      gather_row(V, w.block_tables, r, h // 2, 0, p + 1, 16), w.scale)
+                assert np.allclose(out[c0 + i, h], ref, rtol=1e-12, atol=1e-12), (r, i, h)
+
+
 ALL_PINS = [
     pin_slot_mapping_hand_worked,
     pin_slot_mapping_inverse,
@@ -387,4 +575,11 @@ ALL_PINS = [
     pin_prefill_row_equals_decode,
     pin_prefix_groups_pages_example,
     pin_prefix_groups_properties,
+    pin_e4m3_published_values,
+    pin_e4m3_grid_and_round_trip,
+    pin_e4m3_rounding,
+    pin_fp8_tile_layout,
+    pin_fp8_append_quantizes,
+    pin_fp8_decode_equals_dense,
+    pin_fp8_prefill_equals_dense_causal,
 ]

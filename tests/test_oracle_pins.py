@@ -4,7 +4,8 @@ import pytest
 import _pins
 
 PLANTS = ["PLANT_TRANSPOSE", "PLANT_SLOT", "PLANT_APPEND_HEAD", "PLANT_OFFSET", "PLANT_NO_SCALE",
-          "PLANT_DROP_LAST_V", "PLANT_GQA", "PLANT_WINDOW", "PLANT_CAUSAL", "PLANT_PREFIX_CAP"]
+          "PLANT_DROP_LAST_V", "PLANT_GQA", "PLANT_WINDOW", "PLANT_CAUSAL", "PLANT_PREFIX_CAP",
+          "PLANT_E4M3_TIES", "PLANT_FP8_VPERM"]
 
 
 @pytest.mark.parametrize("pin", _pins.ALL_PINS, ids=lambda f: f.__name__)
