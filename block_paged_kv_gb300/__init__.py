@@ -26,8 +26,9 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libpkv.so")
 
 PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA, PKV_ERR_WORKSPACE, PKV_ERR_OUT_OF_BLOCKS = range(6)
-PKV_F32, PKV_BF16 = 0, 1
+PKV_F32, PKV_BF16, PKV_FP8_E4M3 = 0, 1, 2
 DEV_BAD_BLOCK, DEV_BAD_SLOT, DEV_BAD_LEN, DEV_BAD_PREFIX, DEV_TIMEOUT = 1, 2, 4, 8, 16
+DEV_Q_RANGE = 32
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"{LIB_PATH} is missing: build it first "
@@ -38,7 +39,8 @@ _lib = ctypes.CDLL(LIB_PATH)
 class _Pool(ctypes.Structure):
     _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("num_blocks", ctypes.c_int32),
                 ("block_size", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
-                ("head_dim", ctypes.c_int32), ("dtype", ctypes.c_int)]
+                ("head_dim", ctypes.c_int32), ("dtype", ctypes.c_int),
+                ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float)]
 
 
 class _Prefix(ctypes.Structure):
@@ -139,7 +141,25 @@ def _dtype_code(t: torch.dtype) -> int:
         return PKV_F32
     if t == torch.bfloat16:
         return PKV_BF16
-    raise TypeError(f"unsupported dtype {t}: the pools hold float32 or bfloat16")
+    if t == torch.uint8:
+        return PKV_FP8_E4M3
+    raise TypeError(f"unsupported dtype {t}: the pools hold float32, bfloat16 or FP8 (uint8) codes")
+
+
+def _act_dtype(pool_dtype: torch.dtype) -> torch.dtype:
+    """dtype of queries, outputs and new rows for a pool: bf16 beside FP8 pools."""
+    return torch.bfloat16 if pool_dtype == torch.uint8 else pool_dtype
+
+
+FP8_BLOCK_SIZE = 16
+
+
+def fp8_pools(num_blocks: int, num_kv_heads: int, head_dim: int, device) -> Tuple[torch.Tensor, torch.Tensor]:
+    """A pair of FP8 (E4M3) pools: uint8 tile bytes [num_blocks, num_kv_heads,
+    16 * head_dim] (block size 16, tile bytes in the library's fragment order)."""
+    shape = (num_blocks, num_kv_heads, FP8_BLOCK_SIZE * head_dim)
+    return (torch.zeros(shape, dtype=torch.uint8, device=device),
+            torch.zeros(shape, dtype=torch.uint8, device=device))
 
 
 def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
@@ -155,14 +175,23 @@ def _require(cond: bool, msg: str) -> None:
         raise ValueError(msg)
 
 
-def _pool(k_pool: torch.Tensor, v_pool: torch.Tensor) -> _Pool:
-    _require(k_pool.dim() == 4 and k_pool.shape == v_pool.shape,
-             "pools are [num_blocks, num_kv_heads, block_size, head_dim] and K/V match")
-    _require(k_pool.dtype == v_pool.dtype, "K and V pools share a dtype")
+def _pool(k_pool: torch.Tensor, v_pool: torch.Tensor, k_scale: Optional[float] = None,
+          v_scale: Optional[float] = None) -> _Pool:
+    _require(k_pool.dtype == v_pool.dtype and k_pool.shape == v_pool.shape,
+             "K and V pools share a dtype and a shape")
     _require(k_pool.is_cuda and v_pool.is_cuda, "pools live on the GPU")
     _require(k_pool.is_contiguous() and v_pool.is_contiguous(), "pools are contiguous")
+    if k_pool.dtype == torch.uint8:
+        _require(k_pool.dim() == 3 and k_pool.shape[2] % FP8_BLOCK_SIZE == 0,
+                 "FP8 pools are [num_blocks, num_kv_heads, 16 * head_dim] uint8")
+        _require(k_scale is not None and v_scale is not None, "FP8 pools need k_scale and v_scale")
+        nb, hkv, n = k_pool.shape
+        return _Pool(k_pool.data_ptr(), v_pool.data_ptr(), nb, FP8_BLOCK_SIZE, hkv,
+                     n // FP8_BLOCK_SIZE, PKV_FP8_E4M3, float(k_scale), float(v_scale))
+    _require(k_pool.dim() == 4, "pools are [num_blocks, num_kv_heads, block_size, head_dim]")
     nb, hkv, bs, d = k_pool.shape
-    return _Pool(k_pool.data_ptr(), v_pool.data_ptr(), nb, bs, hkv, d, _dtype_code(k_pool.dtype))
+    return _Pool(k_pool.data_ptr(), v_pool.data_ptr(), nb, bs, hkv, d, _dtype_code(k_pool.dtype),
+                 0.0, 0.0)
 
 
 def _i32_dev(t: torch.Tensor, name: str, device) -> torch.Tensor:
@@ -227,15 +256,18 @@ def slot_mapping_host(block_tables: np.ndarray, num_blocks: int, rows: np.ndarra
 
 def paged_kv_append(k_pool: torch.Tensor, v_pool: torch.Tensor, slot_mapping: torch.Tensor,
                     k_new: torch.Tensor, v_new: torch.Tensor,
-                    status: Optional[torch.Tensor] = None) -> None:
-    """Write ``k_new``/``v_new`` [T, Hkv, D] into the pools at ``slot_mapping`` [T]."""
-    pool = _pool(k_pool, v_pool)
+                    status: Optional[torch.Tensor] = None, k_scale: Optional[float] = None,
+                    v_scale: Optional[float] = None) -> None:
+    """Write ``k_new``/``v_new`` [T, Hkv, D] into the pools at ``slot_mapping`` [T]
+    (quantized with ``k_scale``/``v_scale`` into FP8 pools)."""
+    pool = _pool(k_pool, v_pool, k_scale, v_scale)
     dev = k_pool.device
     _i32_dev(slot_mapping, "slot_mapping", dev)
     _require(k_new.shape == v_new.shape and k_new.dim() == 3 and
              k_new.shape[1:] == (pool.num_kv_heads, pool.head_dim),
              "k_new/v_new are [T, num_kv_heads, head_dim]")
-    _require(k_new.dtype == k_pool.dtype and v_new.dtype == k_pool.dtype, "new rows match the pool dtype")
+    act = _act_dtype(k_pool.dtype)
+    _require(k_new.dtype == act and v_new.dtype == act, "new rows match the pool dtype (bf16 for FP8)")
     _require(k_new.is_contiguous() and v_new.is_contiguous(), "new rows are contiguous")
     _require(slot_mapping.shape[0] == k_new.shape[0], "one slot per new token")
     _check("paged_kv_append", _lib.paged_kv_append(
@@ -262,15 +294,18 @@ def paged_decode_attention(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.
                            workspace: Optional[torch.Tensor] = None,
                            max_seq_len: Optional[int] = None,
                            prefix: Optional[PrefixDesc] = None,
-                           status: Optional[torch.Tensor] = None) -> torch.Tensor:
+                           status: Optional[torch.Tensor] = None,
+                           k_scale: Optional[float] = None,
+                           v_scale: Optional[float] = None) -> torch.Tensor:
     """Batched paged decode attention; returns ``out`` [B, Hq, D].
 
     ``max_seq_len`` is a host bound on ``seq_lens`` (default: the block-table
     capacity); ``workspace`` defaults to a fresh buffer of the queried size.
+    FP8 pools (uint8) take bf16 queries and their ``k_scale``/``v_scale``.
     """
-    pool = _pool(k_pool, v_pool)
+    pool = _pool(k_pool, v_pool, k_scale, v_scale)
     dev = k_pool.device
-    _require(q.dim() == 3 and q.shape[2] == pool.head_dim and q.dtype == k_pool.dtype and
+    _require(q.dim() == 3 and q.shape[2] == pool.head_dim and q.dtype == _act_dtype(k_pool.dtype) and
              q.is_contiguous() and q.device == dev, "q is [B, Hq, D], contiguous, pool dtype")
     B, hq, D = q.shape
     _i32_dev(block_tables, "block_tables", dev)
@@ -308,11 +343,13 @@ def paged_prefill_chunk_attention(q: torch.Tensor, cu_q_lens: torch.Tensor, k_po
                                   scale: float, out: Optional[torch.Tensor] = None,
                                   workspace: Optional[torch.Tensor] = None,
                                   max_seq_len: Optional[int] = None,
-                                  status: Optional[torch.Tensor] = None) -> torch.Tensor:
+                                  status: Optional[torch.Tensor] = None,
+                                  k_scale: Optional[float] = None,
+                                  v_scale: Optional[float] = None) -> torch.Tensor:
     """Chunked prefill against the paged prefix; returns ``out`` [sum C, Hq, D]."""
-    pool = _pool(k_pool, v_pool)
+    pool = _pool(k_pool, v_pool, k_scale, v_scale)
     dev = k_pool.device
-    _require(q.dim() == 3 and q.shape[2] == pool.head_dim and q.dtype == k_pool.dtype and
+    _require(q.dim() == 3 and q.shape[2] == pool.head_dim and q.dtype == _act_dtype(k_pool.dtype) and
              q.is_contiguous() and q.device == dev, "q is [sum C, Hq, D], contiguous, pool dtype")
     _i32_dev(cu_q_lens, "cu_q_lens", dev)
     _i32_dev(block_tables, "block_tables", dev)
@@ -390,7 +427,9 @@ def paged_decode_attention_no_alloc(q: torch.Tensor, k_pool: torch.Tensor, v_poo
                                     window: int, scale: float, out: torch.Tensor,
                                     max_seq_len: Optional[int] = None,
                                     prefix: Optional[PrefixDesc] = None,
-                                    status: Optional[torch.Tensor] = None) -> torch.Tensor:
+                                    status: Optional[torch.Tensor] = None,
+                                    k_scale: Optional[float] = None,
+                                    v_scale: Optional[float] = None) -> torch.Tensor:
     """paged_decode_attention for callers that cannot allocate device memory.
 
     No workspace is passed and nothing is allocated: the library's fixed
@@ -399,9 +438,9 @@ def paged_decode_attention_no_alloc(q: torch.Tensor, k_pool: torch.Tensor, v_poo
     overlap on the GPU must be ordered.  Sizes that need more scratch raise
     PkvError with PKV_ERR_WORKSPACE.
     """
-    pool = _pool(k_pool, v_pool)
+    pool = _pool(k_pool, v_pool, k_scale, v_scale)
     dev = k_pool.device
-    _require(q.dim() == 3 and q.shape[2] == pool.head_dim and q.dtype == k_pool.dtype and
+    _require(q.dim() == 3 and q.shape[2] == pool.head_dim and q.dtype == _act_dtype(k_pool.dtype) and
              q.is_contiguous() and q.device == dev, "q is [B, Hq, D], contiguous, pool dtype")
     B, hq, _ = q.shape
     _i32_dev(block_tables, "block_tables", dev)

@@ -68,17 +68,33 @@ bool valid_pool(const pkv_pool *pool)
     if (pool->num_blocks <= 0 || pool->block_size <= 0 || pool->num_kv_heads <= 0 ||
         pool->head_dim <= 0)
         return false;
-    if (pool->dtype != PKV_F32 && pool->dtype != PKV_BF16) return false;
+    if (pool->dtype != PKV_F32 && pool->dtype != PKV_BF16 && pool->dtype != PKV_FP8_E4M3)
+        return false;
+    if (pool->dtype == PKV_FP8_E4M3 &&
+        (!(std::isfinite(pool->k_scale) && pool->k_scale > 0.f) ||
+         !(std::isfinite(pool->v_scale) && pool->v_scale > 0.f)))
+        return false;
     return aligned16(pool->k) && aligned16(pool->v);
 }
 
-int elem_bytes(pkv_dtype t) { return t == PKV_BF16 ? 2 : 4; }
+// FP8 pools have one tile layout: 16-token blocks, head_dim a multiple of 64
+bool fp8_shape_built(const pkv_pool *pool)
+{
+    return pool->block_size == 16 &&
+           (pool->head_dim == 64 || pool->head_dim == 128 || pool->head_dim == 256);
+}
+
+// Element type of queries and outputs: bf16 beside FP8 pools, else the pool's own.
+pkv_dtype out_dtype(pkv_dtype t) { return t == PKV_FP8_E4M3 ? PKV_BF16 : t; }
+
+int elem_bytes(pkv_dtype t) { return t == PKV_FP8_E4M3 ? 1 : (t == PKV_BF16 ? 2 : 4); }
 
 // Which decode shapes are built.
 bool decode_shape_built(pkv_dtype dtype, int32_t D, int32_t bs, int32_t G)
 {
     if (G < 1 || G > 16) return false;
-    if (dtype == PKV_BF16) return bs == 16 && (D == 64 || D == 128 || D == 256);
+    if (dtype == PKV_BF16 || dtype == PKV_FP8_E4M3)
+        return bs == 16 && (D == 64 || D == 128 || D == 256);
     return (D == 32 || D == 64 || D == 128 || D == 256) && bs <= 64 && bs * D <= 4096;
 }
 
@@ -125,7 +141,7 @@ DecodePlan make_plan(int32_t batch, int32_t hq, int32_t hkv, int32_t D, int32_t 
                                     prefix->num_groups * chunks_bf16,
                                 std::max(num_sms, 1));
         Cp = std::min<int64_t>(std::max<int64_t>(Cp, 4), 64);
-        const int64_t chunks = dtype == PKV_BF16 ? chunks_bf16 : ceil_div64(rows_pairs, kF32Rows);
+        const int64_t chunks = dtype != PKV_F32 ? chunks_bf16 : ceil_div64(rows_pairs, kF32Rows);
         pl.prefix_split_blocks = static_cast<int32_t>(Cp);
         pl.n_prefix_splits = static_cast<int32_t>(ceil_div64(prefix->max_prefix_blocks, Cp));
         pl.prefix_chunks = static_cast<int32_t>(chunks);
@@ -318,6 +334,28 @@ pkv_status paged_kv_append(const pkv_pool *pool, const int32_t *slot_mapping, in
     if (num_tokens == 0) return PKV_OK;
     if (slot_mapping == nullptr || k_new == nullptr || v_new == nullptr) return PKV_ERR_INVALID_ARG;
     if (!aligned16(k_new) || !aligned16(v_new)) return PKV_ERR_INVALID_ARG;
+    if (pool->dtype == PKV_FP8_E4M3) {
+        if (!fp8_shape_built(pool)) return PKV_ERR_UNSUPPORTED;
+        if (static_cast<int64_t>(pool->num_blocks) * pool->block_size > INT32_MAX)
+            return PKV_ERR_UNSUPPORTED;
+        AppendParams p{};
+        p.k_pool = pool->k;
+        p.v_pool = pool->v;
+        p.k_new = k_new;
+        p.v_new = v_new;
+        p.slot_mapping = slot_mapping;
+        p.status = dev_status;
+        p.num_tokens = num_tokens;
+        p.hkv = pool->num_kv_heads;
+        p.block_size = pool->block_size;
+        p.num_slots = pool->num_blocks * pool->block_size;
+        p.head_dim = pool->head_dim;
+        p.k_scale = pool->k_scale;
+        p.v_scale = pool->v_scale;
+        return launch_append_fp8(p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+                   ? PKV_OK
+                   : PKV_ERR_CUDA;
+    }
     const int64_t row_bytes = static_cast<int64_t>(pool->head_dim) * elem_bytes(pool->dtype);
     if (row_bytes % 16 != 0) return PKV_ERR_UNSUPPORTED;
     if (static_cast<int64_t>(pool->num_blocks) * pool->block_size > INT32_MAX)
@@ -425,11 +463,18 @@ pkv_status paged_decode_attention(const void *q, int32_t num_q_heads, const pkv_
     p.max_len = max_len;
     p.window = window;
     p.scale_log2 = scale * 1.4426950408889634f;
+    p.v_scale = 1.f;
+    if (pool->dtype == PKV_FP8_E4M3) {
+        p.scale_log2 *= pool->k_scale;
+        p.v_scale = pool->v_scale;
+    }
     p.plan = pl;
 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t err;
-    if (pool->dtype == PKV_BF16) {
+    if (pool->dtype == PKV_FP8_E4M3) {
+        err = launch_decode_fp8(p, st);
+    } else if (pool->dtype == PKV_BF16) {
         if (!encode_fn_ready()) return PKV_ERR_CUDA;
         CUtensorMap kmap, vmap;
         if (!encode_pool_map_tile(&kmap, pool->k, *pool) ||
@@ -440,7 +485,7 @@ pkv_status paged_decode_attention(const void *q, int32_t num_q_heads, const pkv_
         err = launch_decode_f32(p, st);
     }
     if (err != cudaSuccess) return PKV_ERR_CUDA;
-    err = launch_decode_combine(p, pool->dtype, st);
+    err = launch_decode_combine(p, out_dtype(pool->dtype), st);
     return err == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
@@ -507,7 +552,7 @@ pkv_status paged_prefill_chunk_attention(const void *q, const int32_t *cu_q_lens
         return PKV_ERR_INVALID_ARG;
     const int32_t G = num_q_heads / pool->num_kv_heads;
     const int64_t cap = static_cast<int64_t>(max_blocks_per_seq) * pool->block_size;
-    if (pool->dtype == PKV_BF16 &&
+    if (pool->dtype != PKV_F32 &&
         verify_on_decode(G, pool->head_dim, pool->block_size, max_q_len)) {
         // a few queries per row: the split-KV decode kernel with (query, head)
         // M-rows, then its merge
@@ -547,15 +592,23 @@ pkv_status paged_prefill_chunk_attention(const void *q, const int32_t *cu_q_lens
         d.max_len = max_len;
         d.window = window;
         d.scale_log2 = scale * 1.4426950408889634f;
+        d.v_scale = 1.f;
         d.plan = pl;
-        if (!encode_fn_ready()) return PKV_ERR_CUDA;
-        CUtensorMap kmap, vmap;
-        if (!encode_pool_map_tile(&kmap, pool->k, *pool) ||
-            !encode_pool_map_tile(&vmap, pool->v, *pool))
-            return PKV_ERR_UNSUPPORTED;
         cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-        cudaError_t err = launch_decode_bf16(d, kmap, vmap, st);
-        if (err == cudaSuccess) err = launch_decode_combine(d, pool->dtype, st);
+        cudaError_t err;
+        if (pool->dtype == PKV_FP8_E4M3) {
+            d.scale_log2 *= pool->k_scale;
+            d.v_scale = pool->v_scale;
+            err = launch_decode_fp8(d, st);
+        } else {
+            if (!encode_fn_ready()) return PKV_ERR_CUDA;
+            CUtensorMap kmap, vmap;
+            if (!encode_pool_map_tile(&kmap, pool->k, *pool) ||
+                !encode_pool_map_tile(&vmap, pool->v, *pool))
+                return PKV_ERR_UNSUPPORTED;
+            err = launch_decode_bf16(d, kmap, vmap, st);
+        }
+        if (err == cudaSuccess) err = launch_decode_combine(d, out_dtype(pool->dtype), st);
         return err == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
     }
     if (!prefill_shape_built(pool->dtype, pool->head_dim, pool->block_size, G))

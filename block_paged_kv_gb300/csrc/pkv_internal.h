@@ -22,8 +22,10 @@ struct AppendParams {
     int32_t num_tokens;
     int32_t hkv;
     int32_t block_size;
-    int32_t vecs_per_row;  // head_dim * elem_bytes / 16
+    int32_t vecs_per_row;  // head_dim * elem_bytes / 16 (bf16/f32 pools)
     int32_t num_slots;     // num_blocks * block_size
+    int32_t head_dim;      // FP8 pools: bf16 rows are quantized with these scales
+    float k_scale, v_scale;
 };
 
 // Split plan of one decode call.  A row's key range [lo, L) covers the blocks
@@ -46,7 +48,7 @@ struct DecodePlan {
 struct DecodeParams {
     const void *q;
     void *out;
-    const void *k_pool;  // used by the CUDA-core (f32) kernel; the bf16 kernel reads via TMA
+    const void *k_pool;  // read directly by the f32 and FP8 kernels; bf16 goes through TMA maps
     const void *v_pool;
     const int32_t *tables;
     const int32_t *seq_lens;
@@ -64,7 +66,8 @@ struct DecodeParams {
     int32_t max_len;   // min(max_seq_len, width * block_size): lengths are clamped to it
     int32_t window;
     int32_t num_groups;
-    float scale_log2;  // scale * log2(e): scores are kept in base-2 units
+    float scale_log2;  // scale * log2(e) (* k_scale for FP8): scores are kept in base-2 units
+    float v_scale;     // FP8: applied to each partial's weighted values
     DecodePlan plan;
 };
 
@@ -118,6 +121,7 @@ struct PrefillParams {
 };
 
 cudaError_t launch_append(const AppendParams &p, cudaStream_t stream);
+cudaError_t launch_append_fp8(const AppendParams &p, cudaStream_t stream);
 bool prefill_shape_built(pkv_dtype dtype, int32_t D, int32_t bs, int32_t G);
 int32_t prefill_queries_per_cta(pkv_dtype dtype, int32_t G);
 // Key-range split of the bf16 prefill for short chunks (all of a row's
@@ -140,6 +144,7 @@ cudaError_t launch_decode_bf16(const DecodeParams &p, const CUtensorMap &kmap,
                                const CUtensorMap &vmap, cudaStream_t stream);
 // f32 pools: CUDA-core kernel.
 cudaError_t launch_decode_f32(const DecodeParams &p, cudaStream_t stream);
+cudaError_t launch_decode_fp8(const DecodeParams &p, cudaStream_t stream);
 // merge of the split partials into out (dtype of q)
 cudaError_t launch_decode_combine(const DecodeParams &p, pkv_dtype dtype, cudaStream_t stream);
 

@@ -706,6 +706,7 @@ bool prefill_shape_built(pkv_dtype dtype, int32_t D, int32_t bs, int32_t G)
 {
     if (G < 1 || G > 16) return false;
     if (dtype == PKV_BF16) return D == pf::kD && bs == 16 && (pf::kRows % G) == 0;
+    if (dtype != PKV_F32) return false;  // FP8: short chunks only, on the decode kernel
     return (D == 32 || D == 64 || D == 128 || D == 256) && bs <= 64 && bs * D <= 4096 &&
            (kPf32Pairs % G) == 0;
 }

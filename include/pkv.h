@@ -60,7 +60,22 @@ typedef enum {
     PKV_ERR_OUT_OF_BLOCKS = 5 /* block allocator: the pool (at its maximum) cannot hold the request */
 } pkv_status;
 
-typedef enum { PKV_F32 = 0, PKV_BF16 = 1 } pkv_dtype;
+/*
+ * Element type of a pool.  PKV_FP8_E4M3: the FP8 KV cache with per-layer
+ * scales of "perf.md" (quantisation scheme table, FP8 KV cache row).  Each
+ * element is one E4M3 code c ("FP8 Formats for Deep Learning", E4M3: bias 7,
+ * 3 mantissa bits, max 448, S.1111.111 = NaN) holding e4m3(c) * scale, with
+ * pool.k_scale for the K pool and pool.v_scale for the V pool.  Queries,
+ * outputs and appended rows of an FP8 pool are bf16.  An FP8 pool has
+ * block_size 16 and head_dim 64, 128 or 256; its (block, kv head) tiles are
+ * 16 * head_dim bytes in the operand order of the m16n8k16 tensor-core
+ * product (so each thread's operands are 16 consecutive bytes):
+ *   K byte of (token t, dim d):  (d/64)*1024 + (t/8)*512 + ((t%8)*4 + c)*16 + ((d%64)/16)*4 + j
+ *       with k = d%16, c = (k%8)/2, j = k%2 + 2*(k/8);
+ *   V byte of (token t, dim d):  (d/32)*512 + ((d%8)*4 + c)*16 + ((d%32)/8)*4 + j
+ *       with c = (t%8)/2, j = t%2 + 2*(t/8).
+ */
+typedef enum { PKV_F32 = 0, PKV_BF16 = 1, PKV_FP8_E4M3 = 2 } pkv_dtype;
 
 /* Bits OR-ed into *dev_status by the kernels. */
 #define PKV_DEV_BAD_BLOCK 1  /* a table entry inside a row's key range is < 0 or >= num_blocks:
@@ -72,6 +87,8 @@ typedef enum { PKV_F32 = 0, PKV_BF16 = 1 } pkv_dtype;
                                 prefix blocks, or is shorter than the prefix */
 #define PKV_DEV_TIMEOUT 16   /* a pipeline wait gave up after its time limit; the outputs of
                                 that call are not valid */
+#define PKV_DEV_Q_RANGE 32   /* FP8 pools: a query element's magnitude is past 65504, the f16
+                                range the FP8 path computes q . k in; outputs not valid */
 
 /* One layer's K/V block pool (device pointers, 16-byte aligned). */
 typedef struct {
@@ -82,6 +99,8 @@ typedef struct {
     int32_t num_kv_heads;
     int32_t head_dim;
     pkv_dtype dtype;
+    float k_scale;  /* PKV_FP8_E4M3 only (finite, > 0): the layer's K and V scales */
+    float v_scale;
 } pkv_pool;
 
 /*
@@ -103,9 +122,12 @@ typedef struct {
  * Append ("perf.md", paged knob table, MLX_PAGED_NATIVE_KV_WRITE: new K/V rows
  * are written into their pool slots).  For token t with slot s >= 0:
  *   pool.k[s / bs][h][s % bs][:] = k_new[t][h][:]   for every kv head h (same for v).
- * k_new, v_new: device [num_tokens][num_kv_heads][head_dim] of pool.dtype.
- * slot_mapping: device int32 [num_tokens].  Bit-exact copy.  Two tokens naming
- * one slot race (the caller must not do that).
+ * k_new, v_new: device [num_tokens][num_kv_heads][head_dim] of pool.dtype (bf16
+ * for an FP8 pool).  slot_mapping: device int32 [num_tokens].  Bit-exact copy;
+ * into an FP8 pool each element x is stored as the E4M3 code nearest to the
+ * float32 quotient x / scale (ties to the even code, magnitudes past 448
+ * saturate to +-448), at its byte of the tile.  Two tokens naming one slot
+ * race (the caller must not do that).
  */
 pkv_status paged_kv_append(const pkv_pool *pool, const int32_t *slot_mapping, int32_t num_tokens,
                            const void *k_new, const void *v_new, int32_t *dev_status,
@@ -127,7 +149,7 @@ size_t paged_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t n
  *   out[r][h][:] = softmax_p(scale * q[r][h] . K_p) . V_p
  * over the positions p of row r in its key range (see the conventions above),
  * K_p/V_p read through block_tables from kv head h / (Hq / Hkv).
- *   q, out:        device [batch][num_q_heads][head_dim], pool.dtype
+ *   q, out:        device [batch][num_q_heads][head_dim], pool.dtype (bf16 for FP8)
  *   block_tables:  device int32 [batch][max_blocks_per_seq]
  *   seq_lens:      device int32 [batch]
  *   max_seq_len:   host upper bound on seq_lens (sizes the split plan)
@@ -136,8 +158,12 @@ size_t paged_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t n
  * Split-KV: each row's key range is cut into fixed-size runs of blocks; every
  * run yields fp32 (max, sum, weighted values) partials that a second kernel
  * merges.  The cut depends only on the sizes and the SM count, so a call is
- * bit-reproducible.  Built: f32 and bf16; block_size 16 for bf16 (any
- * block_size <= 64 for f32); head_dim 64, 128, 256; Hq / Hkv <= 16.
+ * bit-reproducible.  Built: f32, bf16 and FP8; block_size 16 for bf16 and FP8
+ * (any block_size <= 64 for f32); head_dim 64, 128, 256; Hq / Hkv <= 16.  FP8
+ * pools: q . k is computed with q converted to f16 (exact for bf16 values of
+ * magnitude 2^-14 .. 65504; smaller ones round to f16 subnormals, larger ones
+ * set PKV_DEV_Q_RANGE) against the exact code values, the scales applied in
+ * fp32; probabilities enter P.V as f16.
  */
 pkv_status paged_decode_attention(const void *q, int32_t num_q_heads, const pkv_pool *pool,
                                   const int32_t *block_tables, int32_t max_blocks_per_seq,
@@ -195,6 +221,7 @@ size_t paged_prefill_workspace_size(int32_t batch, int32_t num_q_heads, int32_t 
  * max(0, p - W + 1) .. p (W = 0: 0 .. p), i.e. the whole prefix and the chunk
  * causally.
  *   q, out:      device [cu_q_lens[batch]][num_q_heads][head_dim], pool.dtype
+ *                (bf16 for FP8)
  *   cu_q_lens:   device int32 [batch + 1], non-decreasing, cu_q_lens[0] = 0
  *   max_q_len:   host upper bound on C_r;  max_seq_len: host bound on seq_lens
  *   workspace:   device, >= paged_prefill_workspace_size(...) bytes, 256-byte
@@ -204,7 +231,8 @@ size_t paged_prefill_workspace_size(int32_t batch, int32_t num_q_heads, int32_t 
  * product as bf16 hi + lo terms); f32 pools run a CUDA-core kernel.  bf16
  * chunks with max_q_len * (Hq / Hkv) <= 16 (a speculative-verify step) run on
  * the split-KV decode kernel instead, one M-row per (query, head) pair, for
- * head_dim 64, 128 or 256.
+ * head_dim 64, 128 or 256; FP8 pools are built for such chunks only (longer
+ * ones return PKV_ERR_UNSUPPORTED).
  */
 pkv_status paged_prefill_chunk_attention(const void *q, const int32_t *cu_q_lens,
                                          int32_t num_q_heads, const pkv_pool *pool,

@@ -86,27 +86,41 @@ static double e4m3_value(uint8_t c)
     return (c & 0x80) ? -v : v;
 }
 
-/* Nearest finite E4M3 code to x by search over every positive code; a tie
- * between two neighbours goes to the one with an even code (mantissa lsb 0).
- * 448 is the nearest finite value to anything larger, so the search itself
- * saturates.  The sign bit is x's own (so -0.0 and negative values that
- * round to zero give 0x80).  NaN gives 0x7F. */
+/* Nearest finite E4M3 code to x: a search of the positive codes, whose
+ * values increase with the code; a tie between two neighbours goes to the
+ * one with an even code (mantissa lsb 0).  448 is the nearest finite value to
+ * anything larger, so the search itself saturates.  The sign bit is x's own
+ * (so -0.0 and negative values that round to zero give 0x80).  NaN gives
+ * 0x7F. */
+static double e4m3_grid[0x7F]; /* values of the codes 0x00 .. 0x7E */
+static int e4m3_grid_ready;
+
 static uint8_t e4m3_encode(float x)
 {
     if (isnan(x)) return 0x7F;
+    if (!e4m3_grid_ready) {
+        for (int c = 0; c <= 0x7E; ++c) e4m3_grid[c] = e4m3_value((uint8_t)c);
+        e4m3_grid_ready = 1;
+    }
     double a = fabs((double)x);
-    int best = 0;
-    double bd = INFINITY;
-    for (int c = 0; c <= 0x7E; ++c) {
-        double d = fabs(e4m3_value((uint8_t)c) - a);
-#ifdef PLANT_E4M3_TIES
-        if (d < bd || (d == bd && 0)) { /* wrong: ties go to the smaller magnitude */
-#else
-        if (d < bd || (d == bd && (c & 1) == 0)) {
-#endif
-            bd = d;
-            best = c;
+    /* lo = the largest code whose value is <= a (bisection on the grid) */
+    int lo = 0, hi = 0x7E;
+    if (a >= e4m3_grid[0x7E]) {
+        lo = 0x7E;
+    } else {
+        while (hi - lo > 1) {
+            int mid = (lo + hi) / 2;
+            if (e4m3_grid[mid] <= a) lo = mid; else hi = mid;
         }
+    }
+    int best = lo;
+    if (lo < 0x7E) {
+        double dl = a - e4m3_grid[lo], dh = e4m3_grid[lo + 1] - a;
+#ifdef PLANT_E4M3_TIES
+        if (dh < dl) best = lo + 1; /* wrong: ties go to the smaller magnitude */
+#else
+        if (dh < dl || (dh == dl && ((lo + 1) & 1) == 0)) best = lo + 1;
+#endif
     }
     return (uint8_t)(signbit(x) ? (best | 0x80) : best);
 }

@@ -1,0 +1,229 @@
+"""GPU parity of the FP8 (E4M3) KV pools against the oracle (through the C ABI).
+
+The pools start as the poison code everywhere; the context of a workload is
+written by appending its live rows (bf16) and then the step's new rows, on the
+GPU by the library and on the CPU by the oracle, from the same arrays.  The
+pool bytes must agree exactly (the code of every element is decided by the
+same float32 quotient on both sides); attention outputs within the bf16
+tolerance |gpu - ref| <= 2e-3 + 1e-2 |ref| (the oracle attends the exact code
+values in float64).
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+
+import pkv_inputs as gen
+from gpu_util import assert_close, to_f64, to_torch
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+KS, VS = float(gen.FP8_K_SCALE), float(gen.FP8_V_SCALE)
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import block_paged_kv_gb300 as m
+    return m
+
+
+def _rows_only(w, rows):
+    """live slots of the blocks that the given rows' tables reach"""
+    s, kr, vr = gen.live_slots(w)
+    t = w.block_tables[np.asarray(rows)]
+    keep = np.isin(s // 16, t[t >= 0])
+    return s[keep], kr[keep], vr[keep]
+
+
+class Fp8Step:
+    """One workload on FP8 pools: context + new rows appended on both sides."""
+
+    def __init__(self, pkv, orc, w, rows=None, check_pool=True):
+        assert w.dtype == "bf16"
+        dev = torch.device("cuda")
+        self.w = w
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        kp, vp = gen.fp8_empty_pools(w)
+        self.k_pool = torch.from_numpy(kp).to(dev)
+        self.v_pool = torch.from_numpy(vp).to(dev)
+        ctx = gen.live_slots(w) if rows is None else _rows_only(w, rows)
+        new_slots = pkv.slot_mapping_host(w.block_tables, w.num_blocks, w.new_rows, w.new_pos, 16)
+        or_slots, bad = orc.slot_mapping(w.block_tables, w.num_blocks, w.new_rows, w.new_pos, 16)
+        assert bad == 0 and np.array_equal(new_slots, or_slots)
+        for s, kr, vr in (ctx, (new_slots, w.k_new, w.v_new)):
+            if s.shape[0] == 0:
+                continue
+            pkv.paged_kv_append(self.k_pool, self.v_pool, torch.from_numpy(s).to(dev),
+                                to_torch(kr, "bf16"), to_torch(vr, "bf16"), status=self.status,
+                                k_scale=KS, v_scale=VS)
+            orc.append(kp, vp, "fp8", s, kr, vr, KS, VS)
+        self.kp, self.vp = kp, vp
+        self.q = to_torch(w.q, "bf16")
+        self.tables = torch.from_numpy(w.block_tables).to(dev)
+        self.seq_lens = torch.from_numpy(w.seq_lens).to(dev)
+        self.cu = torch.from_numpy(w.cu_q_lens).to(dev) if w.cu_q_lens is not None else None
+        torch.cuda.synchronize()
+        assert int(self.status.item()) == 0
+        if check_pool:
+            assert np.array_equal(self.k_pool.cpu().numpy(), kp), "K pool bytes differ"
+            assert np.array_equal(self.v_pool.cpu().numpy(), vp), "V pool bytes differ"
+
+    def decode(self, pkv, prefix=False):
+        w = self.w
+        desc = pkv.make_prefix_desc(w.block_tables, w.seq_lens, 16, self.k_pool.device) \
+            if prefix else None
+        out = pkv.paged_decode_attention(self.q, self.k_pool, self.v_pool, self.tables,
+                                         self.seq_lens, w.window, w.scale,
+                                         max_seq_len=int(w.seq_lens.max()), prefix=desc,
+                                         status=self.status, k_scale=KS, v_scale=VS)
+        torch.cuda.synchronize()
+        assert int(self.status.item()) == 0
+        return to_f64(out)
+
+    def oracle_decode(self, orc, pairs=None):
+        w = self.w
+        return orc.decode(w.q, self.kp, self.vp, "fp8", w.block_tables, w.seq_lens, w.window,
+                          w.scale, pairs=pairs, k_scale=KS, v_scale=VS)
+
+
+# ---------------------------------------------------------------------------
+# append
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("d,hkv", [(64, 1), (128, 8), (256, 2)])
+def test_append_codes_bit_exact(pkv, orc, d, hkv):
+    w = gen.decode_workload(seed=300 + d + hkv, dtype="bf16", num_q_heads=hkv * 2,
+                            num_kv_heads=hkv, head_dim=d, context_lens=[0, 1, 15, 16, 17, 70, 333])
+    Fp8Step(pkv, orc, w)
+
+
+def test_append_saturates_and_keeps_tiny_values(pkv, orc):
+    # rows scaled to reach past +-448 * scale and down into the subnormal codes,
+    # with zeros of both signs
+    w = gen.decode_workload(seed=310, dtype="bf16", num_q_heads=4, num_kv_heads=2, head_dim=128,
+                            context_lens=[40, 5])
+    f = gen.bf16_to_f32(w.k_new)
+    mags = np.array([1e3, 30.0, 1.0, 1e-4, 3e-6], np.float32)
+    k = f * mags[np.arange(f.size) % mags.size].reshape(f.shape)
+    k.reshape(-1)[:4] = [0.0, -0.0, 448 * KS * 1.0001, -1e30]
+    w = dataclasses.replace(w, k_new=gen.bf16_bits(k), v_new=gen.bf16_bits(k[::-1].copy()))
+    s = Fp8Step(pkv, orc, w)
+    codes = s.k_pool.cpu().numpy()
+    assert (codes == 0x7E).any() and (codes == 0xFE).any(), "saturated codes present"
+    assert ((codes & 0x78) == 0).sum() > 0, "subnormal or zero codes present"
+
+
+def test_append_negative_slots_skipped(pkv, orc):
+    w = gen.decode_workload(seed=311, dtype="bf16", num_q_heads=4, num_kv_heads=2, head_dim=64,
+                            context_lens=[20, 40])
+    dev = torch.device("cuda")
+    k, v = pkv.fp8_pools(w.num_blocks, 2, 64, dev)
+    before = k.clone()
+    pkv.paged_kv_append(k, v, torch.full((2,), -1, dtype=torch.int32, device=dev),
+                        to_torch(w.k_new, "bf16"), to_torch(w.v_new, "bf16"), k_scale=KS, v_scale=VS)
+    torch.cuda.synchronize()
+    assert torch.equal(k, before)
+
+
+# ---------------------------------------------------------------------------
+# decode
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("d,hq,hkv", [(64, 4, 4), (128, 8, 2), (128, 32, 8), (256, 8, 1),
+                                      (64, 16, 1), (128, 6, 2)])
+@pytest.mark.parametrize("window", [0, 1, 37, 200])
+def test_decode_shapes_windows_ragged(pkv, orc, d, hq, hkv, window):
+    ctx = [0, 1, 15, 16, 17, 100, 333, 700]
+    w = gen.decode_workload(seed=320 + d + hq + window, dtype="bf16", num_q_heads=hq,
+                            num_kv_heads=hkv, head_dim=d, context_lens=ctx, window=window)
+    s = Fp8Step(pkv, orc, w)
+    assert_close(s.decode(pkv), s.oracle_decode(orc), "bf16", f"fp8 d{d} {hq}/{hkv} w{window}")
+
+
+@pytest.mark.parametrize("scale", [-0.3, 0.0])
+def test_decode_scale_sign_and_zero(pkv, orc, scale):
+    w = gen.decode_workload(seed=330, dtype="bf16", num_q_heads=8, num_kv_heads=2, head_dim=128,
+                            context_lens=[3, 90, 513])
+    s = Fp8Step(pkv, orc, dataclasses.replace(w, scale=scale))
+    assert_close(s.decode(pkv), s.oracle_decode(orc), "bf16", f"fp8 scale {scale}")
+
+
+@pytest.mark.parametrize("prefix", [False, True])
+def test_decode_shared_prefix(pkv, orc, prefix):
+    w = gen.decode_workload(seed=340, dtype="bf16", num_q_heads=32, num_kv_heads=8, head_dim=128,
+                            context_lens=[256 + x for x in (0, 5, 17, 300, 1000, 64)],
+                            shared_prefix_tokens=256)
+    s = Fp8Step(pkv, orc, w)
+    assert_close(s.decode(pkv, prefix=prefix), s.oracle_decode(orc), "bf16",
+                 f"fp8 shared prefix (prefix path {prefix})")
+
+
+def test_decode_sliding_null_sentinel(pkv, orc):
+    w = gen.decode_workload(seed=350, dtype="bf16", num_q_heads=8, num_kv_heads=1, head_dim=256,
+                            context_lens=[600, 1000, 50], window=128, sliding_live_only=True)
+    s = Fp8Step(pkv, orc, w)
+    assert_close(s.decode(pkv), s.oracle_decode(orc), "bf16", "fp8 sliding group")
+
+
+def test_decode_shared_prefix_b32_full_size(pkv, orc):
+    # the shared-prefix batch at full size on FP8 pools; the oracle fills and
+    # reads only the sampled rows
+    w = gen.shared_prefix_b32()
+    rows = [0, 7, 13, 31]
+    s = Fp8Step(pkv, orc, w, rows=rows, check_pool=False)
+    pairs = np.array([(r, h) for r in rows for h in (0, 5, 17, 31)], dtype=np.int32)
+    for prefix in (False, True):
+        got = s.decode(pkv, prefix=prefix)[pairs[:, 0], pairs[:, 1]]
+        assert_close(got, s.oracle_decode(orc, pairs=pairs), "bf16",
+                     f"fp8 shared prefix b32 (prefix path {prefix})")
+
+
+def test_query_out_of_f16_range_flagged(pkv, orc):
+    w = gen.decode_workload(seed=360, dtype="bf16", num_q_heads=4, num_kv_heads=1, head_dim=64,
+                            context_lens=[30])
+    s = Fp8Step(pkv, orc, w)
+    q = s.q.clone()
+    q[0, 2, 5] = 1e5
+    pkv.paged_decode_attention(q, s.k_pool, s.v_pool, s.tables, s.seq_lens, 0, w.scale,
+                               status=s.status, k_scale=KS, v_scale=VS)
+    torch.cuda.synchronize()
+    assert int(s.status.item()) == pkv.DEV_Q_RANGE
+
+
+# ---------------------------------------------------------------------------
+# verify steps (a few queries per row) and the unsupported long chunk
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("d,hq,hkv,chunks", [
+    (128, 32, 8, [4, 4, 2, 1, 3]),
+    (64, 8, 2, [4, 2, 4, 1, 3]),
+    (256, 8, 1, [2, 1, 2, 2, 1]),
+])
+@pytest.mark.parametrize("window", [0, 40])
+def test_verify_steps(pkv, orc, d, hq, hkv, chunks, window):
+    w = gen.prefill_workload(seed=370 + d + hq + window, dtype="bf16", num_q_heads=hq,
+                             num_kv_heads=hkv, head_dim=d,
+                             prefix_lens=[100, 1000, 3000, 17, 0], chunk_lens=chunks,
+                             window=window)
+    s = Fp8Step(pkv, orc, w)
+    out = pkv.paged_prefill_chunk_attention(s.q, s.cu, s.k_pool, s.v_pool, s.tables, s.seq_lens,
+                                            max(chunks), window, w.scale, status=s.status,
+                                            k_scale=KS, v_scale=VS)
+    torch.cuda.synchronize()
+    assert int(s.status.item()) == 0
+    ref = orc.prefill(w.q, w.cu_q_lens, s.kp, s.vp, "fp8", w.block_tables, w.seq_lens, window,
+                      w.scale, k_scale=KS, v_scale=VS)
+    assert_close(to_f64(out), ref, "bf16", f"fp8 verify d{d} {hq}/{hkv} w{window}")
+
+
+def test_long_chunk_unsupported(pkv, orc):
+    w = gen.prefill_workload(seed=380, dtype="bf16", num_q_heads=8, num_kv_heads=2, head_dim=128,
+                             prefix_lens=[16], chunk_lens=[64])
+    s = Fp8Step(pkv, orc, w, check_pool=False)
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.paged_prefill_chunk_attention(s.q, s.cu, s.k_pool, s.v_pool, s.tables, s.seq_lens,
+                                          64, 0, w.scale, k_scale=KS, v_scale=VS)
+    assert e.value.code == pkv.PKV_ERR_UNSUPPORTED
