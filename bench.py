@@ -128,7 +128,7 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 def kernel_source_sha():
     h = hashlib.sha256()
-    for f in ("decode_bf16.cu", "decode_common.cuh", "pkv_device.cuh"):
+    for f in ("decode_kernel.cuh", "decode_bf16.cu", "decode_common.cuh", "pkv_device.cuh"):
         with open(os.path.join(ROOT, "block_paged_kv_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -305,7 +305,7 @@ def run_pkv(args, rank, world, local):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms / e2e_steps, 5)},
         "gpu_launches": int(launches),
-        "roofline": {"kernel": "decode_bf16_kernel<128> (shared-prefix + split-KV decode, one launch)",
+        "roofline": {"kernel": "decode_split_kernel<128, bf16> (shared-prefix + split-KV decode, one launch)",
                      "bound": "hbm",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 3), "peak_source": f"{peak_kind} hbm_gbs",
@@ -335,6 +335,67 @@ def time_loop(torch, fn, steps, warmup, flush=None):
         torch.cuda.synchronize()
         total += e0.elapsed_time(e1)
     return total / steps / 1e3
+
+
+def fp8_b32_setup(pkv, torch, dev):
+    """The batch-32 shared-prefix workload on FP8 (E4M3) pools: its context is
+    appended (quantized) once; returns (workload, step = append one token per
+    row + shared-prefix decode, decode alone, K/V bytes a decode reads, status)."""
+    w = gen.shared_prefix_b32()
+    ks, vs = float(gen.FP8_K_SCALE), float(gen.FP8_V_SCALE)
+
+    def up(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    kp, vp = pkv.fp8_pools(w.num_blocks, w.num_kv_heads, w.head_dim, dev)
+    cs, ckr, cvr = gen.live_slots(w)
+    pkv.paged_kv_append(kp, vp, torch.from_numpy(cs).to(dev), up(ckr), up(cvr),
+                        k_scale=ks, v_scale=vs)
+    del ckr, cvr
+    q, kn, vn = up(w.q), up(w.k_new), up(w.v_new)
+    t = torch.from_numpy(w.block_tables).to(dev)
+    sl = torch.from_numpy(w.seq_lens).to(dev)
+    slots = torch.from_numpy(pkv.slot_mapping_host(w.block_tables, w.num_blocks, w.new_rows,
+                                                   w.new_pos, 16)).to(dev)
+    desc = pkv.make_prefix_desc(w.block_tables, w.seq_lens, 16, dev)
+    ml = int(w.seq_lens.max())
+    ws = pkv.alloc_workspace(pkv.decode_workspace_size(w.batch, w.num_q_heads, w.num_kv_heads,
+                                                       w.head_dim, 16, ml, 0, desc), dev)
+    out = torch.empty_like(q)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def decode():
+        pkv.paged_decode_attention(q, kp, vp, t, sl, 0, w.scale, out=out, workspace=ws,
+                                   max_seq_len=ml, prefix=desc, status=st, k_scale=ks, v_scale=vs)
+
+    def step():
+        pkv.paged_kv_append(kp, vp, slots, kn, vn, status=st, k_scale=ks, v_scale=vs)
+        decode()
+
+    return w, step, decode, workload_bytes(w)[0] // 2, st
+
+
+def run_fp8_case(args, local):
+    """The FP8 decode of the batch-32 shared-prefix workload timed alone (for profiling)."""
+    import torch
+    import block_paged_kv_gb300 as pkv
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w, _, decode, b, st = fp8_b32_setup(pkv, torch, dev)
+    for _ in range(args.warmup):
+        decode()
+    torch.cuda.synchronize()
+    pkv.profile_enable([pkv.KERNEL_DECODE_SPLIT])
+    for _ in range(args.steps):
+        decode()
+    torch.cuda.synchronize()
+    n, t = pkv.profile_read(pkv.KERNEL_DECODE_SPLIT)
+    pkv.profile_enable([])
+    assert int(st.item()) == 0, f"device status {int(st.item())}"
+    s = t / max(n, 1) / 1e3
+    print(json.dumps({"case": "fp8_decode", "workload": w.name.replace("bf16", "fp8"),
+                      "split_kernel_us": round(s * 1e6, 2), "GB/s": round(b / s / 1e9, 1),
+                      "frac_of_hbm_peak": round(b / s / 1e9 / peaks()[0], 3)}), flush=True)
 
 
 def secondary_measurements(args, pkv, torch, dev):
@@ -452,6 +513,40 @@ def secondary_measurements(args, pkv, torch, dev):
                               "tokens_per_batch": int(sum(len(x) for x in prompts)),
                               "pool_blocks": alloc.stats()[0],
                               "note": "host, single thread, via the Python binding"}
+    # FP8 (E4M3) pools: the batch-32 shared-prefix step with the K/V cache in
+    # FP8 (per-layer scales), timed like the contract line: steps back to
+    # back, the split kernel's own duration from events on sampled steps
+    w, fp8_step, fp8_decode, b, st = fp8_b32_setup(pkv, torch, dev)
+    steps = 400
+    for _ in range(10):
+        fp8_step()
+    torch.cuda.synchronize()
+    pkv.profile_enable([])
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(steps):
+        if i % PROF_EVERY == 0:
+            pkv.profile_mask([pkv.KERNEL_DECODE_SPLIT])
+        fp8_step()
+        if i % PROF_EVERY == 0:
+            pkv.profile_mask([])
+    e1.record()
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0, f"device status {int(st.item())}"
+    s_step = e0.elapsed_time(e1) / steps / 1e3
+    nsp, tsp = pkv.profile_read(pkv.KERNEL_DECODE_SPLIT)
+    s_split = tsp / max(nsp, 1) / 1e3
+    peak = peaks()[0]
+    res["fp8_decode_b32"] = {"workload": w.name.replace("bf16", "fp8"), "step_us": round(s_step * 1e6, 2),
+                             "tok_per_s": round(w.batch / s_step, 1),
+                             "step_GB/s": round(b / s_step / 1e9, 1),
+                             "split_kernel_us": round(s_split * 1e6, 2),
+                             "split_kernel_GB/s": round(b / s_split / 1e9, 1),
+                             "split_kernel_frac_of_hbm_peak": round(b / s_split / 1e9 / peak, 3),
+                             "kv_bytes": b, "scales": [float(gen.FP8_K_SCALE), float(gen.FP8_V_SCALE)],
+                             "step": "append 1 token/row (quantized) + shared-prefix paged decode",
+                             "l2": "no flush: 0.26 GB of K/V per step exceeds the 129 MB L2"}
+    del fp8_step, fp8_decode
     # bulk append: every token of the batch-32 workload's private suffixes
     w = gen.shared_prefix_b32()
     n = int(np.sum(w.seq_lens - 1024))
@@ -466,6 +561,14 @@ def secondary_measurements(args, pkv, torch, dev):
     b = 2 * 2 * n * 8 * 128 * 2 + 4 * n
     res["bulk_append"] = {"tokens": n, "us": round(s * 1e6, 2), "GB/s": round(b / s / 1e9, 1),
                           "bytes": b}
+    del kp, vp
+    kp, vp = pkv.fp8_pools(w.num_blocks, 8, 128, dev)
+    ks, vs = float(gen.FP8_K_SCALE), float(gen.FP8_V_SCALE)
+    s = time_loop(torch, lambda: pkv.paged_kv_append(kp, vp, slots, kn, vn, k_scale=ks, v_scale=vs),
+                  50, 5)
+    b = 2 * n * 8 * 128 * (2 + 1) + 4 * n   # bf16 rows in, E4M3 codes out
+    res["bulk_append_fp8"] = {"tokens": n, "us": round(s * 1e6, 2), "GB/s": round(b / s / 1e9, 1),
+                              "bytes": b}
     return res
 
 
@@ -579,9 +682,9 @@ def main():
     ap.add_argument("--no-secondary", dest="secondary", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--case", choices=["step", "prefill"], default="step",
-                    help="step: the decode step (the contract line); prefill: time the chunked "
-                         "prefill kernel alone (for profiling)")
+    ap.add_argument("--case", choices=["step", "prefill", "fp8_decode"], default="step",
+                    help="step: the decode step (the contract line); prefill / fp8_decode: time "
+                         "the chunked prefill or the FP8 decode alone (for profiling)")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -592,6 +695,8 @@ def main():
         run_reference(args, rank, world)
     elif args.case == "prefill":
         run_prefill_case(args, local)
+    elif args.case == "fp8_decode":
+        run_fp8_case(args, local)
     else:
         run_pkv(args, rank, world, local)
 

@@ -10,15 +10,20 @@ cudaError_t launch_decode_fp8(const DecodeParams &p, cudaStream_t stream)
 {
     const CUtensorMap none{};  // unused by the FP8 instantiations
     const bool mq = p.cu_q_lens != nullptr;
+    // query n-tiles: the rows of a split item (G, or G x max_q for a verify step)
+    const bool two = fp8_query_ntiles(static_cast<int64_t>(p.group) * (mq ? p.max_q : 1)) == 2;
+#define PKV_FP8_LAUNCH(DIM)                                                               \
+    return mq ? (two ? launch_split<DIM, true, true, 2>(p, none, none, stream)             \
+                     : launch_split<DIM, true, true, 1>(p, none, none, stream))            \
+              : (two ? launch_split<DIM, false, true, 2>(p, none, none, stream)            \
+                     : launch_split<DIM, false, true, 1>(p, none, none, stream))
     switch (p.head_dim) {
-    case 64: return mq ? launch_split<64, true, true>(p, none, none, stream)
-                       : launch_split<64, false, true>(p, none, none, stream);
-    case 128: return mq ? launch_split<128, true, true>(p, none, none, stream)
-                        : launch_split<128, false, true>(p, none, none, stream);
-    case 256: return mq ? launch_split<256, true, true>(p, none, none, stream)
-                        : launch_split<256, false, true>(p, none, none, stream);
+    case 64: PKV_FP8_LAUNCH(64);
+    case 128: PKV_FP8_LAUNCH(128);
+    case 256: PKV_FP8_LAUNCH(256);
     default: return cudaErrorInvalidValue;
     }
+#undef PKV_FP8_LAUNCH
 }
 
 }  // namespace pkv

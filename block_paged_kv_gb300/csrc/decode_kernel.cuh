@@ -44,14 +44,22 @@ struct KvCfg {
     static constexpr int kTok = 16;                       // block_size
     static constexpr int kElem = kF8 ? 1 : 2;             // bytes per K/V element
     static constexpr int kTileBytes = kTok * D * kElem;   // one (block, kv head) tile of K or V
-    static constexpr int kStageBytes = 2 * kTileBytes;    // K + V
+    // blocks per pipeline stage: an FP8 stage at head_dim <= 128 holds two
+    // blocks, so that each pass of the online softmax covers 32 tokens and
+    // the per-pass costs (waits, reductions, rescale, refill) are paid once
+    // per 32 tokens
+    static constexpr int kBps = (kF8 && D <= 128) ? 2 : 1;
+    static constexpr int kStageBytes = kBps * 2 * kTileBytes;  // K + V of each block
     // query fragments stay in registers for head_dim <= 128; there the query
     // tiles are staged through the ring before the first load, otherwise they
     // keep a region of their own
     static constexpr bool kQInRegs = D <= 128;
     static constexpr int kTiles = 4;                      // query tiles of a prefix item
-    // ring sized so that two CTAs fit on an SM
-    static constexpr int kRingBytes = (D == 256 ? 64 : 96) * 1024;
+    // ring sized so that kCtasPerSm CTAs fit on an SM
+    static constexpr int kRingBytes = (D == 256 ? 64 : (kF8 ? 64 : 96)) * 1024;
+    // resident CTAs per SM the ring is sized for (FP8 tiles need half the
+    // bytes per token, so a third CTA fits and hides more latency)
+    static constexpr int kCtasPerSm = (kF8 && D <= 128) ? 3 : 2;
     static constexpr int kStages = kRingBytes / kStageBytes;
     static constexpr int kStagesPerWarp = kStages / kDecodeWarps;  // split items
     static_assert(kStages % kDecodeWarps == 0, "split items give each warp the same stages");
@@ -71,7 +79,7 @@ struct KvSmem {
     static constexpr int kBarOff =
         C::kQInRegs ? C::kRingBytes : C::kRingBytes + C::kTiles * C::kQTileBytes;
     static constexpr int kOkOff = kBarOff + 2 * C::kStages * 8;
-    static constexpr int kPairOff = kOkOff + C::kStages * 4;
+    static constexpr int kPairOff = kOkOff + C::kStages * C::kBps * 4;
     static constexpr int kMiscOff = kPairOff + 3 * C::kTiles * 16 * 4;
     static constexpr int kBytes = kMiscOff + 16;
     static constexpr int kLaunchBytes = kBytes + 1024;  // room to align the base to 1024
@@ -124,8 +132,8 @@ struct BlockIds {
     }
 };
 
-template <int D, bool kMQ, bool kF8>
-__global__ void __launch_bounds__(kDecodeWarps * 32, 2)
+template <int D, bool kMQ, bool kF8, int NQ>
+__global__ void __launch_bounds__(kDecodeWarps * 32, KvCfg<D, kF8>::kCtasPerSm)
     decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, const DecodeParams p)
 {
@@ -134,6 +142,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
     constexpr int NW = kDecodeWarps;
     constexpr int STAGES = C::kStages;
     constexpr int SPW = C::kStagesPerWarp;
+    // query rows per warp tile of a prefix item: 16 (bf16: the M side of the
+    // products), 8 * NQ (FP8: the N side, NQ n-tiles of 8)
+    constexpr int TR = kF8 ? 8 * NQ : 16;
+    static_assert(kF8 || NQ == 1, "bf16 tiles are 16 query rows on M");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -144,7 +156,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
     uint64_t *empty = full + STAGES;
     int32_t *stage_ok = reinterpret_cast<int32_t *>(smem + SM::kOkOff);
     int32_t *pair_row = reinterpret_cast<int32_t *>(smem + SM::kPairOff);
-    int32_t *pair_head = pair_row + C::kTiles * 16;
+    int32_t *pair_head = pair_row + C::kTiles * 16;  // capacity for TR <= 16
     int32_t *pair_len = pair_head + C::kTiles * 16;
     int32_t *misc = reinterpret_cast<int32_t *>(smem + SM::kMiscOff);
 
@@ -203,11 +215,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
         if (b0 >= b1) return;
         nblk = b1 - b0;
         slot = s;
-        for (int i = threadIdx.x; i < tiles * 16; i += blockDim.x) pair_row[i] = -1;
+        for (int i = threadIdx.x; i < tiles * TR; i += blockDim.x) pair_row[i] = -1;
         __syncthreads();
         if (warp == 0) {
             // rows of the group in ascending order; pair k = rank * G + j
-            const int32_t per_cta = tiles * 16;
+            const int32_t per_cta = tiles * TR;
             const int32_t kbase = chunk * per_cta;
             int32_t cnt = 0, leader = -1, hmax = 0;
             for (int32_t base = 0; base < p.batch; base += 32) {
@@ -247,7 +259,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
         lo_all = 0;
         hi_all = misc[1];
         // every row of the chunk must hold the leader's blocks in this range
-        for (int i = threadIdx.x; i < tiles * 16 * nblk; i += blockDim.x) {
+        for (int i = threadIdx.x; i < tiles * TR * nblk; i += blockDim.x) {
             const int k = i / nblk, b = b0 + i % nblk;
             const int32_t pr = pair_row[k];
             if (pr >= 0 && (k % G) == 0 &&
@@ -260,7 +272,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
     // ------------------------------------------------- query tiles + barriers
     {
         constexpr int kVec = D / 8;  // 16-byte vectors per row
-        for (int i = threadIdx.x; i < tiles * 16 * kVec; i += blockDim.x) {
+        const int qrows = prefix_item ? tiles * TR : 16;
+        for (int i = threadIdx.x; i < qrows * kVec; i += blockDim.x) {
             const int row = i / kVec, v = i % kVec;
             int32_t qr = -1, qh = 0;
             if (!prefix_item) {
@@ -294,8 +307,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
                 if (bad) report(p.status, PKV_DEV_Q_RANGE);
                 val = make_uint4(w[0], w[1], w[2], w[3]);
             }
-            *reinterpret_cast<uint4 *>(q_mem + (row / 16) * C::kQTileBytes +
-                                       (row % 16) * C::kQStride + v * 16) = val;
+            const int qt = prefix_item ? row / TR : 0, qr_in = prefix_item ? row % TR : row;
+            *reinterpret_cast<uint4 *>(q_mem + qt * C::kQTileBytes + qr_in * C::kQStride + v * 16) =
+                val;
         }
         if (threadIdx.x == 0) {
             for (int s = 0; s < STAGES; ++s) {
@@ -312,11 +326,28 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
     const int tile = prefix_item ? warp : 0;
     const uint32_t q_lane = smem_u32(q_mem + tile * C::kQTileBytes) +
                             (((lane >> 3) & 1) * 8 + (lane & 7)) * C::kQStride + (lane >> 4) * 16;
-    uint32_t qf[C::kQInRegs ? C::kKS : 1][4];
+    // bf16: A fragments of Q (query rows on M).  FP8: B fragments of Q^T
+    // (query rows on N, NQ n-tiles of 8): b0 = Q[row 8n + lane/4][16kk + 2(lane%4), +1],
+    // b1 = the same 8 dims further
+    const uint32_t qb_lane = smem_u32(q_mem + tile * C::kQTileBytes) + (lane >> 2) * C::kQStride +
+                             (lane & 3) * 4;
+    uint32_t qf[C::kQInRegs && !kF8 ? C::kKS : 1][4];
+    uint32_t qb[C::kQInRegs && kF8 ? C::kKS : 1][NQ][2];
     if constexpr (C::kQInRegs) {
+        if constexpr (kF8) {
 #pragma unroll
-        for (int kk = 0; kk < C::kKS; ++kk)
-            ldsm_x4(q_lane + kk * 32, qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3]);
+            for (int kk = 0; kk < C::kKS; ++kk)
+#pragma unroll
+                for (int n = 0; n < NQ; ++n) {
+                    const uint32_t a = qb_lane + n * 8 * C::kQStride + kk * 32;
+                    qb[kk][n][0] = lds32(a);
+                    qb[kk][n][1] = lds32(a + 16);
+                }
+        } else {
+#pragma unroll
+            for (int kk = 0; kk < C::kKS; ++kk)
+                ldsm_x4(q_lane + kk * 32, qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3]);
+        }
         // the ring is about to be overwritten by TMA (async proxy) after these
         // generic-proxy reads and writes of the staged query tiles
         fence_proxy_async_smem();
@@ -324,41 +355,58 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
     }
 
     // ------------------------------------------------------------- loads
-    // split item: warp w's blocks are b0 + w + NW*k (k = 0 .. nk-1); its use k
-    // goes to stage w*SPW + k % SPW.  prefix item: block k to stage k % STAGES,
-    // loads issued by warp 0.
+    // A stage holds BPS blocks; pass k of the loop below consumes one stage.
+    // split item: warp w's blocks are b0 + w + NW*j (j = 0 .. nb-1); its pass
+    //   k covers j = BPS*k .. BPS*k + BPS-1 and goes to stage w*SPW + k % SPW.
+    // prefix item: block j of the run, pass k covers j = BPS*k ..; stage
+    //   k % STAGES; loads issued by warp 0.
+    constexpr int BPS = C::kBps;
     const uint64_t policy = l2_evict_first_policy();
     const int32_t *table_row = p.tables + static_cast<int64_t>(tab_row) * p.width + b0;
-    const int32_t nk = prefix_item ? nblk : (nblk > warp ? (nblk - warp + NW - 1) / NW : 0);
+    const int32_t nb = prefix_item ? nblk : (nblk > warp ? (nblk - warp + NW - 1) / NW : 0);
+    const int32_t nk = (nb + BPS - 1) / BPS;
     const bool issuer = !prefix_item || warp == 0;
     BlockIds ids;
-    if (issuer) ids.init(table_row, prefix_item ? 0 : warp, prefix_item ? 1 : NW, nk, lane);
+    if (issuer) ids.init(table_row, prefix_item ? 0 : warp, prefix_item ? 1 : NW, nb, lane);
     auto stage_of = [&](int32_t k) { return prefix_item ? k % STAGES : warp * SPW + k % SPW; };
     auto issue = [&](int32_t k) {  // whole warp; lane 0 issues
-        const int32_t bj = ids.next(k, lane);
+        int32_t bj[BPS];
+#pragma unroll
+        for (int i = 0; i < BPS; ++i) bj[i] = ids.next(k * BPS + i, lane);  // -1 past the run
         if (lane == 0) {
             const int st = stage_of(k);
-            const bool ok = static_cast<uint32_t>(bj) < static_cast<uint32_t>(p.num_blocks);
-            stage_ok[st] = ok ? 1 : 0;
-            if (ok) {
-                mbar_arrive_expect_tx(&full[st], C::kStageBytes);
-                uint8_t *kdst = stage_mem + st * C::kStageBytes;
-                uint8_t *vdst = kdst + C::kTileBytes;
-                if constexpr (kF8) {
-                    // the tile is one contiguous run of the pool
-                    const int64_t off = (static_cast<int64_t>(bj) * p.hkv + g) * C::kTileBytes;
-                    bulk_load(kdst, static_cast<const uint8_t *>(p.k_pool) + off, C::kTileBytes,
-                              &full[st], policy);
-                    bulk_load(vdst, static_cast<const uint8_t *>(p.v_pool) + off, C::kTileBytes,
-                              &full[st], policy);
-                } else {
-                    // one box per (block, kv head) tile: every 64-dim region at once
-                    tma_load_5d(kdst, &kmap, &full[st], 0, 0, 0, g, bj, policy);
-                    tma_load_5d(vdst, &vmap, &full[st], 0, 0, 0, g, bj, policy);
-                }
-            } else {
-                report(p.status, PKV_DEV_BAD_BLOCK);
+            bool okv[BPS];
+            uint32_t bytes = 0;
+#pragma unroll
+            for (int i = 0; i < BPS; ++i) {
+                const bool exists = k * BPS + i < nb;
+                okv[i] = exists && static_cast<uint32_t>(bj[i]) < static_cast<uint32_t>(p.num_blocks);
+                if (exists && !okv[i]) report(p.status, PKV_DEV_BAD_BLOCK);
+                stage_ok[st * BPS + i] = okv[i] ? 1 : 0;
+                bytes += okv[i] ? 2 * C::kTileBytes : 0;
+            }
+            if (bytes == 0) {
                 mbar_arrive(&full[st]);
+            } else {
+                mbar_arrive_expect_tx(&full[st], bytes);
+#pragma unroll
+                for (int i = 0; i < BPS; ++i) {
+                    if (!okv[i]) continue;
+                    uint8_t *kdst = stage_mem + st * C::kStageBytes + i * 2 * C::kTileBytes;
+                    uint8_t *vdst = kdst + C::kTileBytes;
+                    if constexpr (kF8) {
+                        // the tile is one contiguous run of the pool
+                        const int64_t off = (static_cast<int64_t>(bj[i]) * p.hkv + g) * C::kTileBytes;
+                        bulk_load(kdst, static_cast<const uint8_t *>(p.k_pool) + off, C::kTileBytes,
+                                  &full[st], policy);
+                        bulk_load(vdst, static_cast<const uint8_t *>(p.v_pool) + off, C::kTileBytes,
+                                  &full[st], policy);
+                    } else {
+                        // one box per (block, kv head) tile: every 64-dim region at once
+                        tma_load_5d(kdst, &kmap, &full[st], 0, 0, 0, g, bj[i], policy);
+                        tma_load_5d(vdst, &vmap, &full[st], 0, 0, 0, g, bj[i], policy);
+                    }
+                }
             }
         }
     };
@@ -367,181 +415,495 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
         for (int32_t k = 0; k < min(depth, nk); ++k) issue(k);
 
     // ---------------------------------------------------------------- compute
-    const int qd = lane >> 2;        // fragment rows qd and qd + 8
-    const int c2 = 2 * (lane & 3);   // fragment columns c2, c2 + 1
-    int lo0, hi0, lo1, hi1;
-    if (!prefix_item) {
-        if constexpr (kMQ) {
-            // query t of the row sits at L - C + t: causal limit hi, window start lo
-            auto limits = [&](int row, int &lo, int &hi) {
-                const int t = row / G;
-                hi = (row < R && t < row_C) ? hi_all - row_C + t + 1 : 0;
-                lo = (p.window > 0 && hi > 0) ? max(0, hi - p.window) : 0;
-            };
-            limits(qd, lo0, hi0);
-            limits(qd + 8, lo1, hi1);
-        } else {
-            lo0 = lo1 = lo_all;
-            hi0 = hi1 = hi_all;
+    // split item: the four warps' partials of the one tile meet in the ring
+    // (free once every warp is past its last block)
+    float *mbuf = reinterpret_cast<float *>(stage_mem);  // [NW][R][D]
+    float *mlbuf = mbuf + NW * 16 * D;                    // [NW][R][2], R <= 16
+    if constexpr (kF8) {
+        // FP8: transposed products, so that tokens (S^T = K Q^T) and dims
+        // (O^T = V^T P^T) fill the 16-row M side of m16n8k16 and the query
+        // rows sit on N (NQ n-tiles of 8).  The tile bytes are already in A
+        // fragment order for both K and V^T.
+        const int g8 = lane >> 2;  // A rows g8, g8 + 8; B / C column g8 (B), 2cc (C)
+        const int cc = lane & 3;
+        // key range of this lane's C columns: query rows 8n + 2cc + e
+        int clo[NQ][2], chi[NQ][2];
+#pragma unroll
+        for (int n = 0; n < NQ; ++n)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int row = 8 * n + 2 * cc + e;
+                int lo = 0, hi = 0;
+                if (prefix_item) {
+                    const int kq = tile * TR + row;
+                    hi = pair_row[kq] >= 0 ? pair_len[kq] : 0;
+                } else if constexpr (kMQ) {
+                    const int t = row / G;
+                    hi = (row < R && t < row_C) ? hi_all - row_C + t + 1 : 0;
+                    lo = (p.window > 0 && hi > 0) ? max(0, hi - p.window) : 0;
+                } else if (row < R) {
+                    lo = lo_all;
+                    hi = hi_all;
+                }
+                clo[n][e] = lo;
+                chi[n][e] = hi;
+            }
+        float oT[C::kNT / 2][NQ][4];  // [16-dim m-tile][n-tile][C fragment]
+#pragma unroll
+        for (int mt = 0; mt < C::kNT / 2; ++mt)
+#pragma unroll
+            for (int n = 0; n < NQ; ++n) oT[mt][n][0] = oT[mt][n][1] = oT[mt][n][2] = oT[mt][n][3] = 0.f;
+        float mc[NQ][2], lc[NQ][2];
+#pragma unroll
+        for (int n = 0; n < NQ; ++n) {
+            mc[n][0] = mc[n][1] = -INFINITY;
+            lc[n][0] = lc[n][1] = 0.f;
         }
-    } else {
-        lo0 = lo1 = 0;
-        const int k0 = tile * 16 + qd;
-        hi0 = pair_row[k0] >= 0 ? pair_len[k0] : 0;
-        hi1 = pair_row[k0 + 8] >= 0 ? pair_len[k0 + 8] : 0;
-    }
 
-    float o[C::kNT][4];
+        for (int32_t k = 0; k < nk; ++k) {
+            const int st = stage_of(k);
+            const int32_t use = prefix_item ? k / STAGES : k / SPW;
+            const bool got = mbar_wait(&full[st], use & 1);
+            if (__any_sync(0xffffffffu, !got)) {
+                if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
+                break;
+            }
+            const uint32_t stile = smem_u32(stage_mem + st * C::kStageBytes);
+            bool okb[BPS];
+            int base_tok[BPS];
 #pragma unroll
-    for (int nt = 0; nt < C::kNT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+            for (int i = 0; i < BPS; ++i) {
+                okb[i] = stage_ok[st * BPS + i] != 0;
+                const int32_t j = k * BPS + i;
+                base_tok[i] = (b0 + (prefix_item ? j : warp + NW * j)) * bs;
+            }
 
-    // lane-constant parts of the ldmatrix addresses
-    const int k_tok = (lane >> 4) * 8 + (lane & 7);
-    const int k_dof = ((lane >> 3) & 1) * 8;
-    const int v_tok = ((lane >> 3) & 1) * 8 + (lane & 7);
-    const int v_dof = (lane >> 4) * 8;
-
-    for (int32_t k = 0; k < nk; ++k) {
-        const int st = stage_of(k);
-        const int32_t use = prefix_item ? k / STAGES : k / SPW;
-        const bool got = mbar_wait(&full[st], use & 1);
-        if (__any_sync(0xffffffffu, !got)) {
-            if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
-            break;
-        }
-        const bool ok = stage_ok[st] != 0;
-        const uint32_t kt = smem_u32(stage_mem + st * C::kStageBytes);
-        const uint32_t vt = kt + C::kTileBytes;
-        const int base_tok = (b0 + (prefix_item ? k : warp + NW * k)) * bs;
-
-        // S = Q K^T  (16 rows x 16 tokens)
-        float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        if constexpr (kF8) {
-            // lane's 16 bytes of a (64-dim group, token half) hold its B
-            // fragments of the group's four 16-dim steps
+            // S^T = K Q^T: rows = the block's tokens g8 (first half) and
+            // g8 + 8 (second half); even and odd 16-dim steps in two chains
+            float sT[BPS][NQ][4];
 #pragma unroll
-            for (int grp = 0; grp < D / 64; ++grp)
+            for (int i = 0; i < BPS; ++i) {
+                const uint32_t kt = stile + i * 2 * C::kTileBytes;
+                float sa[2][NQ][4] = {};
 #pragma unroll
-                for (int jt = 0; jt < 2; ++jt) {
-                    const uint4 kw = lds128(kt + grp * 1024 + jt * 512 + lane * 16);
-                    const uint32_t w4[4] = {kw.x, kw.y, kw.z, kw.w};
+                for (int grp = 0; grp < D / 64; ++grp) {
+                    const uint4 h0 = lds128(kt + grp * 1024 + lane * 16);
+                    const uint4 h1 = lds128(kt + grp * 1024 + 512 + lane * 16);
+                    const uint32_t w0[4] = {h0.x, h0.y, h0.z, h0.w};
+                    const uint32_t w1[4] = {h1.x, h1.y, h1.z, h1.w};
 #pragma unroll
                     for (int s4 = 0; s4 < 4; ++s4) {
                         const int kk = grp * 4 + s4;
                         uint32_t a[4];
-                        if constexpr (C::kQInRegs) {
-                            a[0] = qf[kk][0]; a[1] = qf[kk][1]; a[2] = qf[kk][2]; a[3] = qf[kk][3];
-                        } else {
-                            ldsm_x4(q_lane + kk * 32, a[0], a[1], a[2], a[3]);
+                        e4m3x4_to_f16x2x2(w0[s4], a[0], a[2]);  // token g8
+                        e4m3x4_to_f16x2x2(w1[s4], a[1], a[3]);  // token g8 + 8
+#pragma unroll
+                        for (int n = 0; n < NQ; ++n) {
+                            uint32_t b0, b1;
+                            if constexpr (C::kQInRegs) {
+                                b0 = qb[kk][n][0];
+                                b1 = qb[kk][n][1];
+                            } else {
+                                const uint32_t qa = qb_lane + n * 8 * C::kQStride + kk * 32;
+                                b0 = lds32(qa);
+                                b1 = lds32(qa + 16);
+                            }
+                            mma_16816_f16(sa[s4 & 1][n], a, b0, b1);
                         }
-                        uint32_t b0, b1;
-                        e4m3x4_to_f16x2x2(w4[s4], b0, b1);
-                        mma_16816_f16(sacc[jt], a, b0, b1);
                     }
                 }
-        } else {
 #pragma unroll
-            for (int kk = 0; kk < C::kKS; ++kk) {
-                uint32_t a[4];
-                if constexpr (C::kQInRegs) {
-                    a[0] = qf[kk][0]; a[1] = qf[kk][1]; a[2] = qf[kk][2]; a[3] = qf[kk][3];
-                } else {
-                    ldsm_x4(q_lane + kk * 32, a[0], a[1], a[2], a[3]);
+                for (int n = 0; n < NQ; ++n)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) sT[i][n][e] = sa[0][n][e] + sa[1][n][e];
+            }
+
+            // mask, scale to log2 units; element e of C is (token g8 + 8(e/2),
+            // column 2cc + e%2)
+            float sv[BPS][NQ][4];
+            bool inside = true;
+#pragma unroll
+            for (int i = 0; i < BPS; ++i) {
+                bool in = okb[i];
+#pragma unroll
+                for (int n = 0; n < NQ; ++n)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e)
+                        in = in && (chi[n][e] == 0 ||
+                                    (base_tok[i] >= clo[n][e] && base_tok[i] + bs <= chi[n][e]));
+                inside = inside && in;
+            }
+            if (__all_sync(0xffffffffu, inside)) {
+#pragma unroll
+                for (int i = 0; i < BPS; ++i)
+#pragma unroll
+                    for (int n = 0; n < NQ; ++n)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) sv[i][n][e] = sT[i][n][e] * p.scale_log2;
+            } else {
+#pragma unroll
+                for (int i = 0; i < BPS; ++i)
+#pragma unroll
+                    for (int n = 0; n < NQ; ++n)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int pos = base_tok[i] + g8 + 8 * (e >> 1);
+                            const int lo = clo[n][e & 1], hi = chi[n][e & 1];
+                            sv[i][n][e] = (okb[i] && pos >= lo && pos < hi)
+                                              ? sT[i][n][e] * p.scale_log2
+                                              : -INFINITY;
+                        }
+            }
+            // column maxima: this lane's tokens, then the 8 lanes sharing cc
+            float mu[NQ][2], al[NQ][2];
+            bool grew = false;
+#pragma unroll
+            for (int n = 0; n < NQ; ++n)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    float mx = -INFINITY;
+#pragma unroll
+                    for (int i = 0; i < BPS; ++i) mx = fmaxf(mx, fmaxf(sv[i][n][e], sv[i][n][e + 2]));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                    const float mn = fmaxf(mc[n][e], mx);
+                    mu[n][e] = mn == -INFINITY ? 0.f : mn;
+                    al[n][e] = fast_exp2(mc[n][e] - mu[n][e]);
+                    grew = grew || mn != mc[n][e];
+                    mc[n][e] = mn;
                 }
-                uint32_t k0, k1, k2, k3;
-                ldsm_x4(kv_chunk_addr<D>(kt, k_tok, kk * 16 + k_dof), k0, k1, k2, k3);
-                mma_16816(sacc[0], a, k0, k1);
-                mma_16816(sacc[1], a, k2, k3);
+            grew = __any_sync(0xffffffffu, grew);
+            float pv[BPS][NQ][4];
+#pragma unroll
+            for (int n = 0; n < NQ; ++n)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    float sum = 0.f;
+#pragma unroll
+                    for (int i = 0; i < BPS; ++i) {
+                        pv[i][n][e] = fast_exp2(sv[i][n][e] - mu[n][e]);
+                        pv[i][n][e + 2] = fast_exp2(sv[i][n][e + 2] - mu[n][e]);
+                        sum += pv[i][n][e] + pv[i][n][e + 2];
+                    }
+                    lc[n][e] = lc[n][e] * al[n][e] + sum;
+                }
+            if (grew) {
+#pragma unroll
+                for (int mt = 0; mt < C::kNT / 2; ++mt)
+#pragma unroll
+                    for (int n = 0; n < NQ; ++n) {
+                        oT[mt][n][0] *= al[n][0];
+                        oT[mt][n][1] *= al[n][1];
+                        oT[mt][n][2] *= al[n][0];
+                        oT[mt][n][3] *= al[n][1];
+                    }
             }
-        }
 
-        // mask, scale to log2 units, online softmax over the quad's row
-        float s[2][4];
+            // O^T += V^T P^T per block.  P as f16 pairs (token g8: columns
+            // 2cc, 2cc+1) is row g8 of an 8x8 (tokens x columns) matrix;
+            // movmatrix.trans hands each lane the (column g8: tokens 2cc,
+            // 2cc+1) pair of the B fragment (one f16 term: 2^-11 relative).
+            // Values of tokens outside every row's range are zeroed: stale
+            // slots may hold anything, including NaN.
 #pragma unroll
-        for (int j = 0; j < 2; ++j)
+            for (int i = 0; i < BPS; ++i) {
+                if (!okb[i]) continue;
+                const uint32_t vt = stile + i * 2 * C::kTileBytes + C::kTileBytes;
+                uint32_t pb[NQ][2];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int pos = base_tok + j * 8 + c2 + (e & 1);
-                const int lo = e < 2 ? lo0 : lo1, hi = e < 2 ? hi0 : hi1;
-                s[j][e] = (ok && pos >= lo && pos < hi) ? sacc[j][e] * p.scale_log2 : -INFINITY;
-            }
-        float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
-        float mx1 = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
-        const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
-        const float al0 = fast_exp2(m0 - mu0), al1 = fast_exp2(m1 - mu1);
-        m0 = mn0;
-        m1 = mn1;
-        // P = 2^(s - m) as a bf16 pair hi + lo (lo = bf16(P - hi)): the P.V
-        // product then carries P to about 2^-17 relative instead of the 2^-9
-        // of a single bf16 rounding
-        float pf[2][4];
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            pf[j][0] = fast_exp2(s[j][0] - mu0);
-            pf[j][1] = fast_exp2(s[j][1] - mu0);
-            pf[j][2] = fast_exp2(s[j][2] - mu1);
-            pf[j][3] = fast_exp2(s[j][3] - mu1);
-        }
-        uint32_t pa[4], pl[4];
-        if constexpr (kF8) {
-            pa[0] = pack_f16x2(pf[0][0], pf[0][1]);
-            pa[1] = pack_f16x2(pf[0][2], pf[0][3]);
-            pa[2] = pack_f16x2(pf[1][0], pf[1][1]);
-            pa[3] = pack_f16x2(pf[1][2], pf[1][3]);
-        } else {
-            pa[0] = pack_bf16x2(pf[0][0], pf[0][1]);
-            pa[1] = pack_bf16x2(pf[0][2], pf[0][3]);
-            pa[2] = pack_bf16x2(pf[1][0], pf[1][1]);
-            pa[3] = pack_bf16x2(pf[1][2], pf[1][3]);
-            pl[0] = pack_bf16x2(pf[0][0] - bf16lo_to_f32(pa[0]), pf[0][1] - bf16hi_to_f32(pa[0]));
-            pl[1] = pack_bf16x2(pf[0][2] - bf16lo_to_f32(pa[1]), pf[0][3] - bf16hi_to_f32(pa[1]));
-            pl[2] = pack_bf16x2(pf[1][0] - bf16lo_to_f32(pa[2]), pf[1][1] - bf16hi_to_f32(pa[2]));
-            pl[3] = pack_bf16x2(pf[1][2] - bf16lo_to_f32(pa[3]), pf[1][3] - bf16hi_to_f32(pa[3]));
-        }
-        l0 = l0 * al0 + ((pf[0][0] + pf[0][1]) + (pf[1][0] + pf[1][1]));
-        l1 = l1 * al1 + ((pf[0][2] + pf[0][3]) + (pf[1][2] + pf[1][3]));
-#pragma unroll
-        for (int nt = 0; nt < C::kNT; ++nt) {
-            o[nt][0] *= al0;
-            o[nt][1] *= al0;
-            o[nt][2] *= al1;
-            o[nt][3] *= al1;
-        }
-
-        // O += P V  (values of tokens outside every row's range are zeroed:
-        // stale slots may hold anything, including NaN)
-        if (ok) {
-            uint32_t mk0 = 0xffffffffu, mk1 = 0xffffffffu;
-            if (base_tok < lo_all || base_tok + bs > hi_all) {
-                auto live = [&](int t) {
-                    return base_tok + t >= lo_all && base_tok + t < hi_all;
-                };
-                mk0 = (live(c2) ? 0x0000ffffu : 0u) | (live(c2 + 1) ? 0xffff0000u : 0u);
-                mk1 = (live(c2 + 8) ? 0x0000ffffu : 0u) | (live(c2 + 9) ? 0xffff0000u : 0u);
-            }
-            if constexpr (kF8) {
-                // lane's 16 bytes of a 32-dim group hold its B fragments of
-                // the group's four 8-dim n-tiles
+                for (int n = 0; n < NQ; ++n) {
+                    pb[n][0] = movmatrix_trans(pack_f16x2(pv[i][n][0], pv[i][n][1]));
+                    pb[n][1] = movmatrix_trans(pack_f16x2(pv[i][n][2], pv[i][n][3]));
+                }
+                uint32_t mk0 = 0xffffffffu, mk1 = 0xffffffffu;
+                const int bt = base_tok[i];
+                if (bt < lo_all || bt + bs > hi_all) {
+                    auto live = [&](int t) { return bt + t >= lo_all && bt + t < hi_all; };
+                    mk0 = (live(2 * cc) ? 0x0000ffffu : 0u) | (live(2 * cc + 1) ? 0xffff0000u : 0u);
+                    mk1 = (live(2 * cc + 8) ? 0x0000ffffu : 0u) | (live(2 * cc + 9) ? 0xffff0000u : 0u);
+                }
 #pragma unroll
                 for (int grp = 0; grp < D / 32; ++grp) {
                     const uint4 vw = lds128(vt + grp * 512 + lane * 16);
                     const uint32_t w4[4] = {vw.x, vw.y, vw.z, vw.w};
 #pragma unroll
-                    for (int jn = 0; jn < 4; ++jn) {
-                        uint32_t b0, b1;
-                        e4m3x4_to_f16x2x2(w4[jn], b0, b1);
-                        mma_16816_f16(o[grp * 4 + jn], pa, b0 & mk0, b1 & mk1);
+                    for (int half = 0; half < 2; ++half) {
+                        // m-tile 2grp + half: dims 16mt + g8 (word 2half) and
+                        // 16mt + 8 + g8 (word 2half + 1)
+                        uint32_t a[4];
+                        e4m3x4_to_f16x2x2(w4[2 * half], a[0], a[2]);
+                        e4m3x4_to_f16x2x2(w4[2 * half + 1], a[1], a[3]);
+                        a[0] &= mk0;
+                        a[1] &= mk0;
+                        a[2] &= mk1;
+                        a[3] &= mk1;
+#pragma unroll
+                        for (int n = 0; n < NQ; ++n)
+                            mma_16816_f16(oT[2 * grp + half][n], a, pb[n][0], pb[n][1]);
                     }
                 }
+            }
+
+            // release the stage: its generic-proxy reads come before the next
+            // async-proxy write into it
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (!prefix_item) {
+                if (k + SPW < nk) issue(k + SPW);
             } else {
+                if (lane == 0) mbar_arrive(&empty[st]);
+                if (warp == 0 && k + STAGES < nk) {
+                    // every warp has released this stage before it is refilled
+                    bool freed = true;
+                    if (lane == 0) freed = mbar_wait(&empty[st], use & 1);
+                    if (!__shfl_sync(0xffffffffu, freed, 0)) {
+                        if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
+                    } else {
+                        issue(k + STAGES);
+                    }
+                }
+            }
+        }
+
+        // column sums over the 8 lanes sharing cc; the V scale on the values
 #pragma unroll
+        for (int n = 0; n < NQ; ++n)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                lc[n][e] += __shfl_xor_sync(0xffffffffu, lc[n][e], 4);
+                lc[n][e] += __shfl_xor_sync(0xffffffffu, lc[n][e], 8);
+                lc[n][e] += __shfl_xor_sync(0xffffffffu, lc[n][e], 16);
+            }
+#pragma unroll
+        for (int mt = 0; mt < C::kNT / 2; ++mt)
+#pragma unroll
+            for (int n = 0; n < NQ; ++n)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) oT[mt][n][e] *= p.v_scale;
+
+        // element e of oT[mt][n]: dim 16mt + g8 + 8(e/2), query row 8n + 2cc + e%2
+        if (prefix_item) {
+            // each warp owns its tile: write its rows directly
+#pragma unroll
+            for (int n = 0; n < NQ; ++n)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int kq = tile * TR + 8 * n + 2 * cc + e;
+                    const int32_t pr = pair_row[kq];
+                    if (pr < 0) continue;
+                    const size_t pi = partial_index(p, pr, pair_head[kq], slot);
+                    float *dst = p.ws_o + pi * D + g8;
+#pragma unroll
+                    for (int mt = 0; mt < C::kNT / 2; ++mt) {
+                        dst[16 * mt] = oT[mt][n][e];
+                        dst[16 * mt + 8] = oT[mt][n][e + 2];
+                    }
+                    if (g8 == 0)
+                        *reinterpret_cast<float2 *>(p.ws_ml + pi * 2) = make_float2(mc[n][e], lc[n][e]);
+                }
+            return;
+        }
+        // split item: this warp's rows of the one tile into the merge buffers
+        __syncthreads();
+#pragma unroll
+        for (int n = 0; n < NQ; ++n)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int row = 8 * n + 2 * cc + e;
+                if (row >= R) continue;
+                float *dst = mbuf + (warp * R + row) * D + g8;
+#pragma unroll
+                for (int mt = 0; mt < C::kNT / 2; ++mt) {
+                    dst[16 * mt] = oT[mt][n][e];
+                    dst[16 * mt + 8] = oT[mt][n][e + 2];
+                }
+                if (g8 == 0)
+                    *reinterpret_cast<float2 *>(mlbuf + (warp * R + row) * 2) =
+                        make_float2(mc[n][e], lc[n][e]);
+            }
+    } else {
+        const int qd = lane >> 2;        // fragment rows qd and qd + 8
+        const int c2 = 2 * (lane & 3);   // fragment columns c2, c2 + 1
+        int lo0, hi0, lo1, hi1;
+        if (!prefix_item) {
+            if constexpr (kMQ) {
+                // query t of the row sits at L - C + t: causal limit hi, window start lo
+                auto limits = [&](int row, int &lo, int &hi) {
+                    const int t = row / G;
+                    hi = (row < R && t < row_C) ? hi_all - row_C + t + 1 : 0;
+                    lo = (p.window > 0 && hi > 0) ? max(0, hi - p.window) : 0;
+                };
+                limits(qd, lo0, hi0);
+                limits(qd + 8, lo1, hi1);
+            } else {
+                lo0 = lo1 = lo_all;
+                hi0 = hi1 = hi_all;
+            }
+        } else {
+            lo0 = lo1 = 0;
+            const int k0 = tile * 16 + qd;
+            hi0 = pair_row[k0] >= 0 ? pair_len[k0] : 0;
+            hi1 = pair_row[k0 + 8] >= 0 ? pair_len[k0 + 8] : 0;
+        }
+
+        float o[C::kNT][4];
+    #pragma unroll
+        for (int nt = 0; nt < C::kNT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+        // lane-constant parts of the ldmatrix addresses
+        const int k_tok = (lane >> 4) * 8 + (lane & 7);
+        const int k_dof = ((lane >> 3) & 1) * 8;
+        const int v_tok = ((lane >> 3) & 1) * 8 + (lane & 7);
+        const int v_dof = (lane >> 4) * 8;
+
+        for (int32_t k = 0; k < nk; ++k) {
+            const int st = stage_of(k);
+            const int32_t use = prefix_item ? k / STAGES : k / SPW;
+            const bool got = mbar_wait(&full[st], use & 1);
+            if (__any_sync(0xffffffffu, !got)) {
+                if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
+                break;
+            }
+            const uint32_t stile = smem_u32(stage_mem + st * C::kStageBytes);
+            bool okb[BPS];
+            int base_tok[BPS];
+    #pragma unroll
+            for (int i = 0; i < BPS; ++i) {
+                okb[i] = stage_ok[st * BPS + i] != 0;
+                const int32_t j = k * BPS + i;
+                base_tok[i] = (b0 + (prefix_item ? j : warp + NW * j)) * bs;
+            }
+
+            // S = Q K^T  (16 rows x 16 tokens per block; n-tile 2i + h holds
+            // tokens 8h .. 8h+7 of block i), even and odd 16-dim steps in two
+            // accumulator chains (half the dependent-MMA latency)
+            float sacc[2 * BPS][4];
+    #pragma unroll
+            for (int i = 0; i < BPS; ++i) {
+                const uint32_t kt = stile + i * 2 * C::kTileBytes;
+                float sa[2][2][4] = {};
+    #pragma unroll
+                for (int kk = 0; kk < C::kKS; ++kk) {
+                    uint32_t a[4];
+                    if constexpr (C::kQInRegs) {
+                        a[0] = qf[kk][0]; a[1] = qf[kk][1]; a[2] = qf[kk][2]; a[3] = qf[kk][3];
+                    } else {
+                        ldsm_x4(q_lane + kk * 32, a[0], a[1], a[2], a[3]);
+                    }
+                    uint32_t k0, k1, k2, k3;
+                    ldsm_x4(kv_chunk_addr<D>(kt, k_tok, kk * 16 + k_dof), k0, k1, k2, k3);
+                    mma_16816(sa[kk & 1][0], a, k0, k1);
+                    mma_16816(sa[kk & 1][1], a, k2, k3);
+                }
+    #pragma unroll
+                for (int h = 0; h < 2; ++h)
+    #pragma unroll
+                    for (int e = 0; e < 4; ++e) sacc[2 * i + h][e] = sa[0][h][e] + sa[1][h][e];
+            }
+
+            // mask, scale to log2 units, online softmax over the quad's row
+            float s[2 * BPS][4];
+            // blocks inside the range of every live row (the common case) need
+            // no mask; rows with hi = 0 hold no query and are never written out
+            bool inside = true;
+    #pragma unroll
+            for (int i = 0; i < BPS; ++i) {
+                auto in_row = [&](int lo, int hi) {
+                    return hi == 0 || (base_tok[i] >= lo && base_tok[i] + bs <= hi);
+                };
+                inside = inside && okb[i] && in_row(lo0, hi0) && in_row(lo1, hi1);
+            }
+            if (__all_sync(0xffffffffu, inside)) {
+    #pragma unroll
+                for (int j = 0; j < 2 * BPS; ++j)
+    #pragma unroll
+                    for (int e = 0; e < 4; ++e) s[j][e] = sacc[j][e] * p.scale_log2;
+            } else {
+    #pragma unroll
+                for (int j = 0; j < 2 * BPS; ++j)
+    #pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int pos = base_tok[j >> 1] + (j & 1) * 8 + c2 + (e & 1);
+                        const int lo = e < 2 ? lo0 : lo1, hi = e < 2 ? hi0 : hi1;
+                        s[j][e] = (okb[j >> 1] && pos >= lo && pos < hi) ? sacc[j][e] * p.scale_log2
+                                                                          : -INFINITY;
+                    }
+            }
+            float mx0 = fmaxf(s[0][0], s[0][1]), mx1 = fmaxf(s[0][2], s[0][3]);
+    #pragma unroll
+            for (int j = 1; j < 2 * BPS; ++j) {
+                mx0 = fmaxf(mx0, fmaxf(s[j][0], s[j][1]));
+                mx1 = fmaxf(mx1, fmaxf(s[j][2], s[j][3]));
+            }
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+            const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
+            const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
+            const float al0 = fast_exp2(m0 - mu0), al1 = fast_exp2(m1 - mu1);
+            // once the running maxima settle the rescale factor is exactly 1
+            const bool grew = __any_sync(0xffffffffu, mn0 != m0 || mn1 != m1);
+            m0 = mn0;
+            m1 = mn1;
+            float pf[2 * BPS][4];
+    #pragma unroll
+            for (int j = 0; j < 2 * BPS; ++j) {
+                pf[j][0] = fast_exp2(s[j][0] - mu0);
+                pf[j][1] = fast_exp2(s[j][1] - mu0);
+                pf[j][2] = fast_exp2(s[j][2] - mu1);
+                pf[j][3] = fast_exp2(s[j][3] - mu1);
+            }
+            float ps0 = 0.f, ps1 = 0.f;
+    #pragma unroll
+            for (int j = 0; j < 2 * BPS; ++j) {
+                ps0 += pf[j][0] + pf[j][1];
+                ps1 += pf[j][2] + pf[j][3];
+            }
+            l0 = l0 * al0 + ps0;
+            l1 = l1 * al1 + ps1;
+            if (grew) {
+    #pragma unroll
+                for (int nt = 0; nt < C::kNT; ++nt) {
+                    o[nt][0] *= al0;
+                    o[nt][1] *= al0;
+                    o[nt][2] *= al1;
+                    o[nt][3] *= al1;
+                }
+            }
+
+            // O += P V per block  (values of tokens outside every row's range are
+            // zeroed: stale slots may hold anything, including NaN)
+    #pragma unroll
+            for (int i = 0; i < BPS; ++i) {
+                if (!okb[i]) continue;
+                const uint32_t vt = stile + i * 2 * C::kTileBytes + C::kTileBytes;
+                // P of block i as the A fragment of a 16-token k-step
+                uint32_t pa[4], pl[4];
+                const float(&p0)[4] = pf[2 * i];
+                const float(&p1)[4] = pf[2 * i + 1];
+                // a bf16 pair hi + lo (lo = bf16(P - hi)): the P.V product then
+                // carries P to about 2^-17 relative instead of the 2^-9 of a
+                // single bf16 rounding
+                pa[0] = pack_bf16x2(p0[0], p0[1]);
+                pa[1] = pack_bf16x2(p0[2], p0[3]);
+                pa[2] = pack_bf16x2(p1[0], p1[1]);
+                pa[3] = pack_bf16x2(p1[2], p1[3]);
+                pl[0] = pack_bf16x2(p0[0] - bf16lo_to_f32(pa[0]), p0[1] - bf16hi_to_f32(pa[0]));
+                pl[1] = pack_bf16x2(p0[2] - bf16lo_to_f32(pa[1]), p0[3] - bf16hi_to_f32(pa[1]));
+                pl[2] = pack_bf16x2(p1[0] - bf16lo_to_f32(pa[2]), p1[1] - bf16hi_to_f32(pa[2]));
+                pl[3] = pack_bf16x2(p1[2] - bf16lo_to_f32(pa[3]), p1[3] - bf16hi_to_f32(pa[3]));
+                uint32_t mk0 = 0xffffffffu, mk1 = 0xffffffffu;
+                const int bt = base_tok[i];
+                if (bt < lo_all || bt + bs > hi_all) {
+                    auto live = [&](int t) { return bt + t >= lo_all && bt + t < hi_all; };
+                    mk0 = (live(c2) ? 0x0000ffffu : 0u) | (live(c2 + 1) ? 0xffff0000u : 0u);
+                    mk1 = (live(c2 + 8) ? 0x0000ffffu : 0u) | (live(c2 + 9) ? 0xffff0000u : 0u);
+                }
+    #pragma unroll
                 for (int np = 0; np < C::kNT / 2; ++np) {
                     uint32_t v0, v1, v2, v3;
                     ldsm_x4_trans(kv_chunk_addr<D>(vt, v_tok, np * 16 + v_dof), v0, v1, v2, v3);
@@ -552,82 +914,69 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
                     mma_16816(o[2 * np + 1], pl, v2, v3);
                 }
             }
-        }
 
-        // release the stage: its generic-proxy reads come before the next
-        // TMA write into it
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (!prefix_item) {
-            if (k + SPW < nk) issue(k + SPW);
-        } else {
-            if (lane == 0) mbar_arrive(&empty[st]);
-            if (warp == 0 && k + STAGES < nk) {
-                // every warp has released this stage before it is refilled
-                bool freed = true;
-                if (lane == 0) freed = mbar_wait(&empty[st], use & 1);
-                if (!__shfl_sync(0xffffffffu, freed, 0)) {
-                    if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
-                } else {
-                    issue(k + STAGES);
+            // release the stage: its generic-proxy reads come before the next
+            // TMA write into it
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (!prefix_item) {
+                if (k + SPW < nk) issue(k + SPW);
+            } else {
+                if (lane == 0) mbar_arrive(&empty[st]);
+                if (warp == 0 && k + STAGES < nk) {
+                    // every warp has released this stage before it is refilled
+                    bool freed = true;
+                    if (lane == 0) freed = mbar_wait(&empty[st], use & 1);
+                    if (!__shfl_sync(0xffffffffu, freed, 0)) {
+                        if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
+                    } else {
+                        issue(k + STAGES);
+                    }
                 }
             }
         }
-    }
 
-    if constexpr (kF8) {
-#pragma unroll
-        for (int nt = 0; nt < C::kNT; ++nt) {
-            o[nt][0] *= p.v_scale;
-            o[nt][1] *= p.v_scale;
-            o[nt][2] *= p.v_scale;
-            o[nt][3] *= p.v_scale;
+        // row sums: the quad's four partial sums
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+
+        if (prefix_item) {
+            // each warp owns its tile: write its rows directly
+    #pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const int k = tile * 16 + qd + half * 8;
+                const int32_t pr = pair_row[k];
+                if (pr < 0) continue;
+                const size_t pi = partial_index(p, pr, pair_head[k], slot);
+                float *dst = p.ws_o + pi * D;
+    #pragma unroll
+                for (int nt = 0; nt < C::kNT; ++nt)
+                    *reinterpret_cast<float2 *>(dst + nt * 8 + c2) =
+                        make_float2(o[nt][2 * half], o[nt][2 * half + 1]);
+                if ((lane & 3) == 0)
+                    *reinterpret_cast<float2 *>(p.ws_ml + pi * 2) =
+                        make_float2(half ? m1 : m0, half ? l1 : l0);
+            }
+            return;
         }
-    }
 
-    // row sums: the quad's four partial sums
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-
-    if (prefix_item) {
-        // each warp owns its tile: write its rows directly
-#pragma unroll
+        // split item: this warp's rows of the one tile into the merge buffers
+        __syncthreads();
+    #pragma unroll
         for (int half = 0; half < 2; ++half) {
-            const int k = tile * 16 + qd + half * 8;
-            const int32_t pr = pair_row[k];
-            if (pr < 0) continue;
-            const size_t pi = partial_index(p, pr, pair_head[k], slot);
-            float *dst = p.ws_o + pi * D;
-#pragma unroll
+            const int row = qd + half * 8;
+            if (row >= R) continue;
+            float *dst = mbuf + (warp * R + row) * D;
+    #pragma unroll
             for (int nt = 0; nt < C::kNT; ++nt)
                 *reinterpret_cast<float2 *>(dst + nt * 8 + c2) =
                     make_float2(o[nt][2 * half], o[nt][2 * half + 1]);
             if ((lane & 3) == 0)
-                *reinterpret_cast<float2 *>(p.ws_ml + pi * 2) =
+                *reinterpret_cast<float2 *>(mlbuf + (warp * R + row) * 2) =
                     make_float2(half ? m1 : m0, half ? l1 : l0);
         }
-        return;
-    }
-
-    // split item: merge the four warps' partials of the one tile through
-    // shared memory (the ring is free once every warp is past its last block)
-    float *mbuf = reinterpret_cast<float *>(stage_mem);  // [NW][R][D]
-    float *mlbuf = mbuf + NW * 16 * D;                    // [NW][R][2], R <= 16
-    __syncthreads();
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-        const int row = qd + half * 8;
-        if (row >= R) continue;
-        float *dst = mbuf + (warp * R + row) * D;
-#pragma unroll
-        for (int nt = 0; nt < C::kNT; ++nt)
-            *reinterpret_cast<float2 *>(dst + nt * 8 + c2) =
-                make_float2(o[nt][2 * half], o[nt][2 * half + 1]);
-        if ((lane & 3) == 0)
-            *reinterpret_cast<float2 *>(mlbuf + (warp * R + row) * 2) =
-                make_float2(half ? m1 : m0, half ? l1 : l0);
     }
     __syncthreads();
     for (int idx = threadIdx.x; idx < R * D; idx += NW * 32) {
@@ -652,13 +1001,13 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
     }
 }
 
-template <int D, bool kMQ, bool kF8>
+template <int D, bool kMQ, bool kF8, int NQ = 1>
 static cudaError_t launch_split(const DecodeParams &p, const CUtensorMap &kmap,
                                 const CUtensorMap &vmap, cudaStream_t stream)
 {
     const int64_t ctas = p.plan.n_prefix_ctas + p.plan.n_suffix_ctas;
     if (ctas == 0) return cudaSuccess;
-    auto kern = decode_split_kernel<D, kMQ, kF8>;
+    auto kern = decode_split_kernel<D, kMQ, kF8, NQ>;
     const int smem = KvSmem<D, kF8>::kLaunchBytes;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;

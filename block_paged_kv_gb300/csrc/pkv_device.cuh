@@ -233,6 +233,24 @@ __device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi)
     return r;
 }
 
+// 4-byte shared-memory load
+__device__ __forceinline__ uint32_t lds32(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
+// Transpose of an 8x8 matrix of 16-bit elements held one 32-bit pair per lane
+// (lane l: row l/4, columns 2(l%4), 2(l%4)+1): lane l receives row l/4 of the
+// transpose, i.e. the pair (row 2(l%4), column l/4), (row 2(l%4)+1, column l/4).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x)
+{
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
 // 16-byte shared-memory load
 __device__ __forceinline__ uint4 lds128(uint32_t addr)
 {

@@ -154,6 +154,12 @@ cudaError_t launch_decode_combine(const DecodeParams &p, pkv_dtype dtype, cudaSt
 // head_dim <= 128, 32 for 256), each read by NW / tiles warps.
 constexpr int kDecodeWarps = 4;
 constexpr int kPrefixPairsPerCta = 64;  // head_dim <= 128 (32 for head_dim 256)
+
+// FP8 decode: query rows sit on the N side of the products in n-tiles of 8;
+// a split item's rows (the G heads, or G x queries of a verify step) need
+// this many, and so does each warp's tile of a prefix item (8 x that many
+// (row, head) pairs per warp)
+inline int fp8_query_ntiles(int64_t rows) { return rows > 8 ? 2 : 1; }
 // query rows per CTA of the f32 kernel
 constexpr int kF32Rows = 16;
 
