@@ -261,18 +261,14 @@ struct view {
     double k_scale, v_scale; /* FP8 pools only */
 };
 
-/* The query's element type: bf16 beside FP8 pools, else the pools' own. */
-static int q_dtype(int32_t dtype) { return dtype == OR_FP8 ? OR_BF16 : dtype; }
-
-/* K (is_v = 0) or V (is_v = 1) element (block b, kv head g, slot t, dim d). */
+/* K (is_v = 0) or V (is_v = 1) element (block b, kv head g, slot t, dim d)
+ * of an FP8 pool: the code at its byte of the tile, times the pool's scale. */
 static double kv_ld(const struct view *w, int is_v, int32_t b, int32_t g, int32_t t, int32_t d)
 {
-    const void *pool = is_v ? w->v_pool : w->k_pool;
-    if (w->dtype != OR_FP8)
-        return ld(pool, w->dtype, pool_index(w->hkv, w->bs, w->dim, b, g, t, d));
+    const uint8_t *pool = (const uint8_t *)(is_v ? w->v_pool : w->k_pool);
     size_t tile = ((size_t)b * w->hkv + g) * (size_t)(w->bs * w->dim);
     size_t off = is_v ? fp8_v_byte(t, d) : fp8_k_byte(t, d);
-    return e4m3_value(((const uint8_t *)pool)[tile + off]) * (is_v ? w->v_scale : w->k_scale);
+    return e4m3_value(pool[tile + off]) * (is_v ? w->v_scale : w->k_scale);
 }
 
 static int attend(const struct view *w, const void *q, size_t qoff, int32_t r, int32_t g,
@@ -300,8 +296,14 @@ static int attend(const struct view *w, const void *q, size_t qoff, int32_t r, i
         int32_t t = p % w->bs;
 #endif
         double acc = 0.0;
-        for (int32_t d = 0; d < dim; ++d)
-            acc += ld(q, q_dtype(w->dtype), qoff + d) * kv_ld(w, 0, blk[j], g, t, d);
+        if (w->dtype == OR_FP8) {
+            for (int32_t d = 0; d < dim; ++d)
+                acc += ld(q, OR_BF16, qoff + d) * kv_ld(w, 0, blk[j], g, t, d);
+        } else {
+            for (int32_t d = 0; d < dim; ++d)
+                acc += ld(q, w->dtype, qoff + d) *
+                       ld(w->k_pool, w->dtype, pool_index(w->hkv, w->bs, dim, blk[j], g, t, d));
+        }
 #ifdef PLANT_NO_SCALE
         s[j] = acc;
 #else
@@ -317,8 +319,12 @@ static int attend(const struct view *w, const void *q, size_t qoff, int32_t r, i
 #ifdef PLANT_DROP_LAST_V
         if (j == n - 1 && n > 1) continue; /* wrong: last value never accumulated */
 #endif
-        for (int32_t d = 0; d < dim; ++d)
-            out[d] += e * kv_ld(w, 1, blk[j], g, t, d);
+        if (w->dtype == OR_FP8) {
+            for (int32_t d = 0; d < dim; ++d) out[d] += e * kv_ld(w, 1, blk[j], g, t, d);
+        } else {
+            for (int32_t d = 0; d < dim; ++d)
+                out[d] += e * ld(w->v_pool, w->dtype, pool_index(w->hkv, w->bs, dim, blk[j], g, t, d));
+        }
     }
     for (int32_t d = 0; d < dim; ++d) out[d] /= l;
     free(s);
