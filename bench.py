@@ -444,6 +444,35 @@ def secondary_measurements(args, pkv, torch, dev):
             b = workload_bytes(w)[0]
         res[name] = {"us": round(s * 1e6, 2), "GB/s": round(b / s / 1e9, 1), "kv_bytes": b}
         del kp, vp
+    # the same two groups in one fused launch (split + merge), against the two
+    # calls one after the other
+    gdev = []
+    for w in (full, sliding):
+        kp, vp, q = up(w, w.k_pool), up(w, w.v_pool), up(w, w.q)
+        gdev.append((w, kp, vp, q, torch.from_numpy(w.block_tables).to(dev),
+                     torch.from_numpy(w.seq_lens).to(dev), torch.empty_like(q)))
+    groups = [pkv.DecodeGroup(q, kp, vp, t, sl, w.window, w.scale, out=o,
+                              max_seq_len=int(w.seq_lens.max()))
+              for w, kp, vp, q, t, sl, o in gdev]
+    gws = pkv.alloc_workspace(pkv.decode_groups_workspace_size(groups), dev)
+    sws = [pkv.alloc_workspace(pkv.decode_workspace_size(w.batch, w.num_q_heads, w.num_kv_heads,
+                                                         w.head_dim, 16, int(w.seq_lens.max()),
+                                                         w.window), dev) for w, *_ in gdev]
+
+    def two_calls():
+        for (w, kp, vp, q, t, sl, o), wsx in zip(gdev, sws):
+            pkv.paged_decode_attention(q, kp, vp, t, sl, w.window, w.scale, out=o, workspace=wsx,
+                                       max_seq_len=int(w.seq_lens.max()))
+
+    s_two = time_loop(torch, two_calls, 100, 5, flush)
+    s_fused = time_loop(torch, lambda: pkv.paged_decode_attention_groups(groups, workspace=gws),
+                        100, 5, flush)
+    b = workload_bytes(full)[0] + full.batch * sliding.window * 2 * sliding.num_kv_heads * sliding.head_dim * 2
+    res["long_two_groups_fused"] = {"us": round(s_fused * 1e6, 2), "GB/s": round(b / s_fused / 1e9, 1),
+                                    "two_calls_us": round(s_two * 1e6, 2), "kv_bytes": b,
+                                    "note": "full + sliding group of the long-context workload, one split "
+                                            "launch and one merge launch; host launch time inside both"}
+    del gdev, groups
     # chunked prefill: 4 rows x 512 queries against a 16384-token paged prefix
     w = gen.chunked_prefill()
     kp, vp, q = up(w, w.k_pool), up(w, w.v_pool), up(w, w.q)

@@ -49,8 +49,18 @@ class _Prefix(ctypes.Structure):
                 ("prefix_blocks", ctypes.c_void_p)]
 
 
+class _Group(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("out", ctypes.c_void_p), ("pool", _Pool),
+                ("block_tables", ctypes.c_void_p), ("max_blocks_per_seq", ctypes.c_int32),
+                ("seq_lens", ctypes.c_void_p), ("max_seq_len", ctypes.c_int32),
+                ("window", ctypes.c_int32), ("scale", ctypes.c_float)]
+
+
+MAX_DECODE_GROUPS = 4
+
 _vp, _i32, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
 _PP, _XP = ctypes.POINTER(_Pool), ctypes.POINTER(_Prefix)
+_GP = ctypes.POINTER(_Group)
 
 _lib.paged_kv_append.argtypes = [_PP, _vp, _i32, _vp, _vp, _vp, _vp]
 _lib.paged_kv_append.restype = ctypes.c_int
@@ -59,6 +69,10 @@ _lib.paged_decode_workspace_size.restype = _sz
 _lib.paged_decode_attention.argtypes = [_vp, _i32, _PP, _vp, _i32, _vp, _i32, _i32, _i32,
                                         ctypes.c_float, _vp, _vp, _sz, _XP, _vp, _vp]
 _lib.paged_decode_attention.restype = ctypes.c_int
+_lib.paged_decode_groups_workspace_size.argtypes = [_GP, _i32, _i32, _i32]
+_lib.paged_decode_groups_workspace_size.restype = _sz
+_lib.paged_decode_attention_groups.argtypes = [_GP, _i32, _i32, _i32, _vp, _sz, _vp, _vp]
+_lib.paged_decode_attention_groups.restype = ctypes.c_int
 _lib.paged_prefill_workspace_size.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32]
 _lib.paged_prefill_workspace_size.restype = _sz
 _lib.paged_prefill_chunk_attention.argtypes = [_vp, _vp, _i32, _PP, _vp, _i32, _vp, _i32, _i32,
@@ -118,7 +132,8 @@ EXPORTED = ["paged_kv_append", "paged_decode_workspace_size", "paged_decode_atte
             "paged_prefill_workspace_size", "paged_prefill_chunk_attention", "pkv_status_string",
             "pkv_slot_mapping_host", "pkv_prefix_groups_host", "pkv_set_decode_split_blocks",
             "pkv_decode_plan", "pkv_version", "pkv_profile_enable", "pkv_profile_mask", "pkv_profile_read",
-            "pkv_launch_count", "paged_decode_attention_no_alloc", "pkv_allocator_create",
+            "pkv_launch_count", "paged_decode_attention_no_alloc", "paged_decode_groups_workspace_size",
+            "paged_decode_attention_groups", "pkv_allocator_create",
             "pkv_allocator_destroy", "pkv_allocator_begin", "pkv_allocator_find_cached_prefix",
             "pkv_allocator_reserve", "pkv_allocator_publish", "pkv_allocator_expire",
             "pkv_allocator_release",
@@ -420,6 +435,72 @@ def profile_read(kind: int) -> Tuple[int, float]:
 def launch_count() -> int:
     """Kernels launched through the library by this process."""
     return int(_lib.pkv_launch_count())
+
+
+@dataclass
+class DecodeGroup:
+    """One group of a fused decode: a paged_decode_attention call's own
+    arguments (q [B, Hq, D], pools, tables, lengths, window, scale)."""
+    q: torch.Tensor
+    k_pool: torch.Tensor
+    v_pool: torch.Tensor
+    block_tables: torch.Tensor
+    seq_lens: torch.Tensor
+    window: int
+    scale: float
+    out: Optional[torch.Tensor] = None
+    max_seq_len: Optional[int] = None
+    k_scale: Optional[float] = None
+    v_scale: Optional[float] = None
+
+
+def _group_c(g: DecodeGroup) -> _Group:
+    pool = _pool(g.k_pool, g.v_pool, g.k_scale, g.v_scale)
+    dev = g.k_pool.device
+    _require(g.q.dim() == 3 and g.q.shape[2] == pool.head_dim and
+             g.q.dtype == _act_dtype(g.k_pool.dtype) and g.q.is_contiguous() and g.q.device == dev,
+             "q is [B, Hq, D], contiguous, pool dtype")
+    B = g.q.shape[0]
+    _i32_dev(g.block_tables, "block_tables", dev)
+    _i32_dev(g.seq_lens, "seq_lens", dev)
+    _require(g.block_tables.dim() == 2 and g.block_tables.shape[0] == B and g.seq_lens.shape == (B,),
+             "block_tables [B, max_blocks], seq_lens [B]")
+    if g.out is None:
+        g.out = torch.empty_like(g.q)
+    _require(g.out.shape == g.q.shape and g.out.dtype == g.q.dtype and g.out.is_contiguous(),
+             "out matches q")
+    width = g.block_tables.shape[1]
+    msl = g.max_seq_len if g.max_seq_len is not None else width * pool.block_size
+    return _Group(g.q.data_ptr(), g.out.data_ptr(), pool, g.block_tables.data_ptr(), width,
+                  g.seq_lens.data_ptr(), msl, int(g.window), float(g.scale))
+
+
+def paged_decode_attention_groups(groups, workspace: Optional[torch.Tensor] = None,
+                                  status: Optional[torch.Tensor] = None):
+    """Several decode calls (groups of layers sharing the head shape: a full
+    group and a sliding group, say) in one split launch and one merge launch.
+    Returns the groups' outputs; each equals its own paged_decode_attention
+    call bit for bit."""
+    groups = list(groups)
+    _require(1 <= len(groups) <= MAX_DECODE_GROUPS, f"1 .. {MAX_DECODE_GROUPS} groups")
+    arr = (_Group * len(groups))(*[_group_c(g) for g in groups])
+    B, hq = groups[0].q.shape[0], groups[0].q.shape[1]
+    _require(all(g.q.shape[:2] == (B, hq) for g in groups), "every group has the same batch and q heads")
+    dev = groups[0].k_pool.device
+    need = int(_lib.paged_decode_groups_workspace_size(arr, len(groups), B, hq))
+    if workspace is None:
+        workspace = alloc_workspace(need, dev)
+    _check("paged_decode_attention_groups", _lib.paged_decode_attention_groups(
+        arr, len(groups), B, hq, workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+        _ptr(status), _stream(dev)))
+    return [g.out for g in groups]
+
+
+def decode_groups_workspace_size(groups) -> int:
+    groups = list(groups)
+    arr = (_Group * len(groups))(*[_group_c(g) for g in groups])
+    return int(_lib.paged_decode_groups_workspace_size(arr, len(groups), groups[0].q.shape[0],
+                                                       groups[0].q.shape[1]))
 
 
 def paged_decode_attention_no_alloc(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,

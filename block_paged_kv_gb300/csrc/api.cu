@@ -231,6 +231,90 @@ bool encode_pool_map_tile(CUtensorMap *map, void *base, const pkv_pool &pool)
     return r == CUDA_SUCCESS;
 }
 
+// Validation and parameters of one decode call (no launch).  batch == 0
+// returns PKV_OK with nothing filled.
+pkv_status decode_setup(const void *q, int32_t num_q_heads, const pkv_pool *pool,
+                        const int32_t *block_tables, int32_t max_blocks_per_seq,
+                        const int32_t *seq_lens, int32_t batch, int32_t max_seq_len,
+                        int32_t window, float scale, void *out, void *workspace, size_t ws_bytes,
+                        const pkv_prefix_desc *prefix, int32_t *dev_status, DecodeParams *pp)
+{
+    if (!valid_pool(pool) || batch < 0 || num_q_heads <= 0 || max_seq_len < 0 || window < 0 ||
+        !std::isfinite(scale))
+        return PKV_ERR_INVALID_ARG;
+    if (num_q_heads % pool->num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+    if (batch == 0) return PKV_OK;
+    if (q == nullptr || out == nullptr || block_tables == nullptr || seq_lens == nullptr ||
+        max_blocks_per_seq <= 0 || !aligned16(q) || !aligned16(out))
+        return PKV_ERR_INVALID_ARG;
+    if (!valid_prefix(prefix, batch, max_blocks_per_seq)) return PKV_ERR_INVALID_ARG;
+    const bool use_prefix = prefix != nullptr && prefix->num_groups > 0;
+    if (use_prefix && window != 0) return PKV_ERR_UNSUPPORTED;
+    const int32_t G = num_q_heads / pool->num_kv_heads;
+    if (!decode_shape_built(pool->dtype, pool->head_dim, pool->block_size, G))
+        return PKV_ERR_UNSUPPORTED;
+    const int64_t cap = static_cast<int64_t>(max_blocks_per_seq) * pool->block_size;
+    const int32_t max_len = static_cast<int32_t>(std::min<int64_t>(max_seq_len, cap));
+
+    const DecodePlan pl = make_plan(batch, num_q_heads, pool->num_kv_heads, pool->head_dim,
+                                    pool->block_size, max_len, window,
+                                    use_prefix ? prefix : nullptr, pool->dtype, num_sms_current());
+    if (pl.n_suffix_ctas > INT32_MAX || pl.n_prefix_ctas > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+    const size_t need = ws_total_bytes(batch, num_q_heads, pool->head_dim, pl);
+    if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+        ws_bytes < need)
+        return PKV_ERR_WORKSPACE;
+
+    DecodeParams &p = *pp;
+    p = DecodeParams{};
+    p.q = q;
+    p.out = out;
+    p.k_pool = pool->k;
+    p.v_pool = pool->v;
+    p.tables = block_tables;
+    p.seq_lens = seq_lens;
+    p.group_of_row = use_prefix ? prefix->group_of_row : nullptr;
+    p.prefix_blocks = use_prefix ? prefix->prefix_blocks : nullptr;
+    p.num_groups = use_prefix ? prefix->num_groups : 0;
+    p.ws_o = static_cast<float *>(workspace);
+    p.ws_ml = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                        ws_o_bytes(batch, num_q_heads, pool->head_dim, pl));
+    p.status = dev_status;
+    p.cu_q_lens = nullptr;  // one query per row
+    p.max_q = 1;
+    p.batch = batch;
+    p.hq = num_q_heads;
+    p.hkv = pool->num_kv_heads;
+    p.group = G;
+    p.head_dim = pool->head_dim;
+    p.block_size = pool->block_size;
+    p.width = max_blocks_per_seq;
+    p.num_blocks = pool->num_blocks;
+    p.max_len = max_len;
+    p.window = window;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.v_scale = 1.f;
+    if (pool->dtype == PKV_FP8_E4M3) {
+        p.scale_log2 *= pool->k_scale;
+        p.v_scale = pool->v_scale;
+    }
+    p.plan = pl;
+    return PKV_OK;
+}
+
+// Groups of one fused call must share what fixes the kernel instantiation.
+bool groups_compatible(const pkv_decode_group *groups, int32_t n)
+{
+    const pkv_pool &p0 = groups[0].pool;
+    for (int32_t i = 1; i < n; ++i) {
+        const pkv_pool &pi = groups[i].pool;
+        if (pi.dtype != p0.dtype || pi.head_dim != p0.head_dim || pi.block_size != p0.block_size ||
+            pi.num_kv_heads != p0.num_kv_heads)
+            return false;
+    }
+    return true;
+}
+
 }  // namespace
 
 namespace pkv {
@@ -413,65 +497,11 @@ pkv_status paged_decode_attention(const void *q, int32_t num_q_heads, const pkv_
                                   size_t ws_bytes, const pkv_prefix_desc *prefix,
                                   int32_t *dev_status, pkv_stream_t stream)
 {
-    if (!valid_pool(pool) || batch < 0 || num_q_heads <= 0 || max_seq_len < 0 || window < 0 ||
-        !std::isfinite(scale))
-        return PKV_ERR_INVALID_ARG;
-    if (num_q_heads % pool->num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
-    if (batch == 0) return PKV_OK;
-    if (q == nullptr || out == nullptr || block_tables == nullptr || seq_lens == nullptr ||
-        max_blocks_per_seq <= 0 || !aligned16(q) || !aligned16(out))
-        return PKV_ERR_INVALID_ARG;
-    if (!valid_prefix(prefix, batch, max_blocks_per_seq)) return PKV_ERR_INVALID_ARG;
-    const bool use_prefix = prefix != nullptr && prefix->num_groups > 0;
-    if (use_prefix && window != 0) return PKV_ERR_UNSUPPORTED;
-    const int32_t G = num_q_heads / pool->num_kv_heads;
-    if (!decode_shape_built(pool->dtype, pool->head_dim, pool->block_size, G))
-        return PKV_ERR_UNSUPPORTED;
-    const int64_t cap = static_cast<int64_t>(max_blocks_per_seq) * pool->block_size;
-    const int32_t max_len = static_cast<int32_t>(std::min<int64_t>(max_seq_len, cap));
-
-    const DecodePlan pl = make_plan(batch, num_q_heads, pool->num_kv_heads, pool->head_dim,
-                                    pool->block_size, max_len, window,
-                                    use_prefix ? prefix : nullptr, pool->dtype, num_sms_current());
-    if (pl.n_suffix_ctas > INT32_MAX || pl.n_prefix_ctas > INT32_MAX) return PKV_ERR_UNSUPPORTED;
-    const size_t need = ws_total_bytes(batch, num_q_heads, pool->head_dim, pl);
-    if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
-        ws_bytes < need)
-        return PKV_ERR_WORKSPACE;
-
     DecodeParams p{};
-    p.q = q;
-    p.out = out;
-    p.k_pool = pool->k;
-    p.v_pool = pool->v;
-    p.tables = block_tables;
-    p.seq_lens = seq_lens;
-    p.group_of_row = use_prefix ? prefix->group_of_row : nullptr;
-    p.prefix_blocks = use_prefix ? prefix->prefix_blocks : nullptr;
-    p.num_groups = use_prefix ? prefix->num_groups : 0;
-    p.ws_o = static_cast<float *>(workspace);
-    p.ws_ml = reinterpret_cast<float *>(static_cast<char *>(workspace) +
-                                        ws_o_bytes(batch, num_q_heads, pool->head_dim, pl));
-    p.status = dev_status;
-    p.cu_q_lens = nullptr;  // one query per row
-    p.max_q = 1;
-    p.batch = batch;
-    p.hq = num_q_heads;
-    p.hkv = pool->num_kv_heads;
-    p.group = G;
-    p.head_dim = pool->head_dim;
-    p.block_size = pool->block_size;
-    p.width = max_blocks_per_seq;
-    p.num_blocks = pool->num_blocks;
-    p.max_len = max_len;
-    p.window = window;
-    p.scale_log2 = scale * 1.4426950408889634f;
-    p.v_scale = 1.f;
-    if (pool->dtype == PKV_FP8_E4M3) {
-        p.scale_log2 *= pool->k_scale;
-        p.v_scale = pool->v_scale;
-    }
-    p.plan = pl;
+    const pkv_status stt = decode_setup(q, num_q_heads, pool, block_tables, max_blocks_per_seq,
+                                        seq_lens, batch, max_seq_len, window, scale, out,
+                                        workspace, ws_bytes, prefix, dev_status, &p);
+    if (stt != PKV_OK || batch == 0) return stt;
 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t err;
@@ -489,6 +519,72 @@ pkv_status paged_decode_attention(const void *q, int32_t num_q_heads, const pkv_
     }
     if (err != cudaSuccess) return PKV_ERR_CUDA;
     err = launch_decode_combine(p, out_dtype(pool->dtype), st);
+    return err == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+size_t paged_decode_groups_workspace_size(const pkv_decode_group *groups, int32_t n_groups,
+                                          int32_t batch, int32_t num_q_heads)
+{
+    if (groups == nullptr || n_groups < 1 || n_groups > PKV_MAX_DECODE_GROUPS || batch < 0)
+        return 0;
+    size_t total = 0;
+    for (int32_t i = 0; i < n_groups; ++i) {
+        const pkv_decode_group &g = groups[i];
+        const size_t one = paged_decode_workspace_size(
+            batch, num_q_heads, g.pool.num_kv_heads, g.pool.head_dim, g.pool.block_size,
+            g.max_seq_len, g.window, nullptr);
+        if (one == 0) return 0;
+        total += (one + 255) & ~static_cast<size_t>(255);
+    }
+    return total;
+}
+
+pkv_status paged_decode_attention_groups(const pkv_decode_group *groups, int32_t n_groups,
+                                         int32_t batch, int32_t num_q_heads, void *workspace,
+                                         size_t ws_bytes, int32_t *dev_status, pkv_stream_t stream)
+{
+    if (groups == nullptr || n_groups < 1 || n_groups > PKV_MAX_DECODE_GROUPS || batch < 0 ||
+        num_q_heads <= 0)
+        return PKV_ERR_INVALID_ARG;
+    for (int32_t i = 0; i < n_groups; ++i)
+        if (!valid_pool(&groups[i].pool)) return PKV_ERR_INVALID_ARG;
+    if (!groups_compatible(groups, n_groups)) return PKV_ERR_INVALID_ARG;
+    const pkv_dtype dt = groups[0].pool.dtype;
+    if (dt == PKV_F32) return PKV_ERR_UNSUPPORTED;  // the CUDA-core f32 kernel runs per call
+    if (batch == 0) return PKV_OK;
+    if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+        ws_bytes < paged_decode_groups_workspace_size(groups, n_groups, batch, num_q_heads))
+        return PKV_ERR_WORKSPACE;
+    if (dt == PKV_BF16 && !encode_fn_ready()) return PKV_ERR_CUDA;
+
+    GroupedDecode gd{};
+    gd.n = n_groups;
+    char *ws = static_cast<char *>(workspace);
+    size_t left = ws_bytes;
+    int64_t ctas = 0;
+    for (int32_t i = 0; i < n_groups; ++i) {
+        const pkv_decode_group &g = groups[i];
+        const pkv_status stt = decode_setup(g.q, num_q_heads, &g.pool, g.block_tables,
+                                            g.max_blocks_per_seq, g.seq_lens, batch, g.max_seq_len,
+                                            g.window, g.scale, g.out, ws, left, nullptr,
+                                            dev_status, &gd.g[i]);
+        if (stt != PKV_OK) return stt;
+        const size_t used = (ws_total_bytes(batch, num_q_heads, g.pool.head_dim, gd.g[i].plan) + 255) &
+                            ~static_cast<size_t>(255);
+        ws += used;
+        left -= used;
+        ctas += gd.g[i].plan.n_prefix_ctas + gd.g[i].plan.n_suffix_ctas;
+        gd.cta_end[i] = ctas;
+        if (dt == PKV_BF16 && (!encode_pool_map_tile(&gd.kmap[i], g.pool.k, g.pool) ||
+                               !encode_pool_map_tile(&gd.vmap[i], g.pool.v, g.pool)))
+            return PKV_ERR_UNSUPPORTED;
+    }
+    if (ctas > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t err = dt == PKV_FP8_E4M3 ? launch_decode_fp8_grouped(gd, st)
+                                         : launch_decode_bf16_grouped(gd, st);
+    if (err != cudaSuccess) return PKV_ERR_CUDA;
+    err = launch_decode_combine_grouped(gd, out_dtype(dt), st);
     return err == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

@@ -249,7 +249,7 @@ __device__ __forceinline__ __nv_bfloat16 to_out<__nv_bfloat16>(float x) { return
 constexpr int kCombineWarps = 8;
 
 template <typename OutT, int D, int W>
-__global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(const DecodeParams p)
+__device__ __forceinline__ void decode_combine_body(const DecodeParams &p, const int64_t cta)
 {
     constexpr int CH = (W == 1 || D < 64) ? D : 64;  // dims per item
     constexpr int PER = CH / 32;                     // dims per lane
@@ -259,7 +259,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
     __shared__ float sm_acc[kCombineWarps][CH];
     const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int warp = wid % W, sub = wid / W;  // warp within the item, item within the CTA
-    const int64_t item = static_cast<int64_t>(blockIdx.x) * IPC + sub;
+    const int64_t item = cta * IPC + sub;
     bool live = item < static_cast<int64_t>(p.batch) * p.max_q * p.hq * NCH;
     const int64_t idx = live ? item / NCH : 0;  // ((row, query), q head)
     const int ch = static_cast<int>(item % NCH);
@@ -341,6 +341,69 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
             static_cast<OutT *>(p.out)[(out_row * p.hq + h) * D + ch * CH + threadIdx.x] = to_out<OutT>(o * inv);
         }
     }
+}
+
+template <typename OutT, int D, int W>
+__global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(const DecodeParams p)
+{
+    decode_combine_body<OutT, D, W>(p, blockIdx.x);
+}
+
+// The merges of several decode calls in one launch: CTAs
+// [item_end[i-1], item_end[i]) merge group i.
+template <typename OutT, int D, int W>
+__global__ void __launch_bounds__(kCombineWarps * 32)
+    decode_combine_grouped_kernel(const __grid_constant__ GroupedDecode gd)
+{
+    int i = 0;
+    const int64_t b = blockIdx.x;
+    while (i + 1 < gd.n && b >= gd.item_end[i]) ++i;
+    const int64_t first = i > 0 ? gd.item_end[i - 1] : 0;
+    decode_combine_body<OutT, D, W>(gd.g[i], b - first);
+}
+
+// merge CTAs of one call
+template <int W>
+static int64_t combine_ctas(const DecodeParams &p)
+{
+    const int64_t chunks = (W == 1 || p.head_dim < 64) ? 1 : p.head_dim / 64;
+    const int64_t items = static_cast<int64_t>(p.batch) * p.max_q * p.hq * chunks;
+    const int64_t ipc = kCombineWarps / W;
+    return (items + ipc - 1) / ipc;
+}
+
+template <typename OutT, int W>
+static cudaError_t launch_combine_grouped_w(GroupedDecode &gd, cudaStream_t stream)
+{
+    int64_t total = 0;
+    for (int i = 0; i < gd.n; ++i) {
+        total += combine_ctas<W>(gd.g[i]);
+        gd.item_end[i] = total;
+    }
+    if (total == 0) return cudaSuccess;
+    const dim3 grid(static_cast<unsigned>(total)), block(kCombineWarps * 32);
+    switch (gd.g[0].head_dim) {
+    case 64: return launch_pdl(decode_combine_grouped_kernel<OutT, 64, W>, grid, block, 0, stream, gd);
+    case 128: return launch_pdl(decode_combine_grouped_kernel<OutT, 128, W>, grid, block, 0, stream, gd);
+    case 256: return launch_pdl(decode_combine_grouped_kernel<OutT, 256, W>, grid, block, 0, stream, gd);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_decode_combine_grouped(GroupedDecode &gd, pkv_dtype out_dtype, cudaStream_t stream)
+{
+    bool many = false;  // eight warps per item when any group's rows have many partials
+    for (int i = 0; i < gd.n; ++i) many = many || gd.g[i].plan.nslot > 16;
+    prof_begin(PKV_KERNEL_DECODE_COMBINE, stream);
+    cudaError_t err;
+    if (out_dtype == PKV_BF16)
+        err = many ? launch_combine_grouped_w<__nv_bfloat16, kCombineWarps>(gd, stream)
+                   : launch_combine_grouped_w<__nv_bfloat16, 1>(gd, stream);
+    else
+        err = many ? launch_combine_grouped_w<float, kCombineWarps>(gd, stream)
+                   : launch_combine_grouped_w<float, 1>(gd, stream);
+    prof_end(PKV_KERNEL_DECODE_COMBINE, stream);
+    return err;
 }
 
 template <typename OutT, int W>

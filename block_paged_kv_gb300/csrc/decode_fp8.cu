@@ -26,4 +26,15 @@ cudaError_t launch_decode_fp8(const DecodeParams &p, cudaStream_t stream)
 #undef PKV_FP8_LAUNCH
 }
 
+cudaError_t launch_decode_fp8_grouped(const GroupedDecode &gd, cudaStream_t stream)
+{
+    const bool two = fp8_query_ntiles(gd.g[0].group) == 2;
+    switch (gd.g[0].head_dim) {
+    case 64: return two ? launch_split_grouped<64, true, 2>(gd, stream) : launch_split_grouped<64, true, 1>(gd, stream);
+    case 128: return two ? launch_split_grouped<128, true, 2>(gd, stream) : launch_split_grouped<128, true, 1>(gd, stream);
+    case 256: return two ? launch_split_grouped<256, true, 2>(gd, stream) : launch_split_grouped<256, true, 1>(gd, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
 }  // namespace pkv

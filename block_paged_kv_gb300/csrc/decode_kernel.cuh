@@ -132,10 +132,11 @@ struct BlockIds {
     }
 };
 
+// The work of CTA `cta` of one decode call (p), its K/V tensor maps (bf16)
+// given by reference to kernel-parameter memory.
 template <int D, bool kMQ, bool kF8, int NQ>
-__global__ void __launch_bounds__(kDecodeWarps * 32, KvCfg<D, kF8>::kCtasPerSm)
-    decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
-                        const __grid_constant__ CUtensorMap vmap, const DecodeParams p)
+__device__ __forceinline__ void decode_split_body(const CUtensorMap &kmap, const CUtensorMap &vmap,
+                                                  const DecodeParams &p, const int64_t cta)
 {
     using C = KvCfg<D, kF8>;
     using SM = KvSmem<D, kF8>;
@@ -173,7 +174,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, KvCfg<D, kF8>::kCtasPerSm)
     pdl_trigger();  // the merge kernel may be scheduled now; it waits for us
 
     // ---------------------------------------------------------------- work item
-    const bool prefix_item = static_cast<int64_t>(blockIdx.x) < p.plan.n_prefix_ctas;
+    const bool prefix_item = cta < p.plan.n_prefix_ctas;
     int32_t b0, nblk, slot, tab_row, g, lo_all, hi_all, tiles;
     // split item only: the row, its query count and first packed query
     int32_t row_r = 0, row_C = 1, row_q0 = 0;
@@ -181,7 +182,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, KvCfg<D, kF8>::kCtasPerSm)
     // head) pairs of a row's few queries (kMQ: a verify step)
     const int R = kMQ ? G * p.max_q : G;
     if (!prefix_item) {
-        int64_t bid = static_cast<int64_t>(blockIdx.x) - p.plan.n_prefix_ctas;
+        int64_t bid = cta - p.plan.n_prefix_ctas;
         const int32_t s = static_cast<int32_t>(bid % p.plan.n_suffix_splits);
         bid /= p.plan.n_suffix_splits;
         g = static_cast<int32_t>(bid % p.hkv);
@@ -200,7 +201,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, KvCfg<D, kF8>::kCtasPerSm)
         tiles = 1;
     } else {
         tiles = C::kTiles;
-        int64_t bid = blockIdx.x;
+        int64_t bid = cta;
         const int32_t s = static_cast<int32_t>(bid % p.plan.n_prefix_splits);
         bid /= p.plan.n_prefix_splits;
         g = static_cast<int32_t>(bid % p.hkv);
@@ -999,6 +1000,46 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, KvCfg<D, kF8>::kCtasPerSm)
         p.ws_o[pi * D + d] = acc;
         if (d == 0) *reinterpret_cast<float2 *>(p.ws_ml + pi * 2) = make_float2(M, lsum);
     }
+}
+
+template <int D, bool kMQ, bool kF8, int NQ>
+__global__ void __launch_bounds__(kDecodeWarps * 32, KvCfg<D, kF8>::kCtasPerSm)
+    decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
+                        const __grid_constant__ CUtensorMap vmap, const DecodeParams p)
+{
+    decode_split_body<D, kMQ, kF8, NQ>(kmap, vmap, p, blockIdx.x);
+}
+
+// Several decode calls in one launch (groups of a model's layers that share
+// the head shape, e.g. a full-attention group and a sliding group): CTAs
+// [cta_end[i-1], cta_end[i]) do group i's work.
+template <int D, bool kF8, int NQ>
+__global__ void __launch_bounds__(kDecodeWarps * 32, KvCfg<D, kF8>::kCtasPerSm)
+    decode_split_grouped_kernel(const __grid_constant__ GroupedDecode gd)
+{
+    int i = 0;
+    const int64_t b = blockIdx.x;
+    while (i + 1 < gd.n && b >= gd.cta_end[i]) ++i;
+    const int64_t first = i > 0 ? gd.cta_end[i - 1] : 0;
+    decode_split_body<D, false, kF8, NQ>(gd.kmap[i], gd.vmap[i], gd.g[i], b - first);
+}
+
+template <int D, bool kF8, int NQ = 1>
+static cudaError_t launch_split_grouped(const GroupedDecode &gd, cudaStream_t stream)
+{
+    const int64_t ctas = gd.cta_end[gd.n - 1];
+    if (ctas == 0) return cudaSuccess;
+    auto kern = decode_split_grouped_kernel<D, kF8, NQ>;
+    const int smem = KvSmem<D, kF8>::kLaunchBytes;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return err;
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared);
+    if (err != cudaSuccess) return err;
+    prof_begin(PKV_KERNEL_DECODE_SPLIT, stream);
+    err = launch_pdl(kern, dim3(static_cast<unsigned>(ctas)), dim3(kDecodeWarps * 32), smem, stream, gd);
+    prof_end(PKV_KERNEL_DECODE_SPLIT, stream);
+    return err;
 }
 
 template <int D, bool kMQ, bool kF8, int NQ = 1>

@@ -71,6 +71,17 @@ struct DecodeParams {
     DecodePlan plan;
 };
 
+// Several decode calls fused into one split launch and one merge launch.
+constexpr int kMaxDecodeGroups = 4;
+struct GroupedDecode {
+    CUtensorMap kmap[kMaxDecodeGroups];  // bf16 pools (unused for FP8)
+    CUtensorMap vmap[kMaxDecodeGroups];
+    DecodeParams g[kMaxDecodeGroups];
+    int64_t cta_end[kMaxDecodeGroups];   // split CTAs of groups 0..i (cumulative)
+    int64_t item_end[kMaxDecodeGroups];  // merge CTAs of groups 0..i (cumulative)
+    int32_t n;
+};
+
 // Launch with programmatic stream serialization (PDL): the kernel may be
 // scheduled while the previous kernel on the stream drains; it calls
 // pdl_wait() before touching global memory.
@@ -145,6 +156,11 @@ cudaError_t launch_decode_bf16(const DecodeParams &p, const CUtensorMap &kmap,
 // f32 pools: CUDA-core kernel.
 cudaError_t launch_decode_f32(const DecodeParams &p, cudaStream_t stream);
 cudaError_t launch_decode_fp8(const DecodeParams &p, cudaStream_t stream);
+// grouped launches (decode only: one query per row, no prefix path); the
+// merge covers every group with the same kernel shape
+cudaError_t launch_decode_bf16_grouped(const GroupedDecode &gd, cudaStream_t stream);
+cudaError_t launch_decode_fp8_grouped(const GroupedDecode &gd, cudaStream_t stream);
+cudaError_t launch_decode_combine_grouped(GroupedDecode &gd, pkv_dtype out_dtype, cudaStream_t stream);
 // merge of the split partials into out (dtype of q)
 cudaError_t launch_decode_combine(const DecodeParams &p, pkv_dtype dtype, cudaStream_t stream);
 

@@ -173,6 +173,46 @@ pkv_status paged_decode_attention(const void *q, int32_t num_q_heads, const pkv_
                                   int32_t *dev_status, pkv_stream_t stream);
 
 /*
+ * Fused decode over several groups of a model's layers ("paged-cache.md",
+ * Gemma4 grouped-coordinator passage: full-attention and sliding-window groups
+ * keep pools and block tables of their own and advance together; "perf.md",
+ * paged knob table: a sliding group's decode reads from its first live block).
+ * Each group is one paged_decode_attention call (prefix = NULL) over the same
+ * batch and q heads: its own q, out, pool, tables, lengths, window and scale.
+ * All groups run in one split launch and one merge launch, so a small group
+ * (a sliding window) fills the gaps of a large one instead of running after
+ * it.  The groups' pools must share dtype (bf16 or FP8; f32 returns
+ * PKV_ERR_UNSUPPORTED), head_dim, block_size and num_kv_heads, else
+ * PKV_ERR_INVALID_ARG.  Every group's output equals, bit for bit, that of its
+ * own paged_decode_attention call.
+ *   groups:    host array of n_groups (1 .. PKV_MAX_DECODE_GROUPS) descriptors
+ *   workspace: device, >= paged_decode_groups_workspace_size(...) bytes,
+ *              256-byte aligned
+ */
+#define PKV_MAX_DECODE_GROUPS 4
+
+typedef struct {
+    const void *q;                /* device [batch][num_q_heads][head_dim] */
+    void *out;                    /* device [batch][num_q_heads][head_dim] */
+    pkv_pool pool;                /* the group's pool (by value) */
+    const int32_t *block_tables;  /* device int32 [batch][max_blocks_per_seq] */
+    int32_t max_blocks_per_seq;
+    const int32_t *seq_lens;      /* device int32 [batch] */
+    int32_t max_seq_len;          /* host bound on seq_lens */
+    int32_t window;               /* 0 = full attention */
+    float scale;
+} pkv_decode_group;
+
+/* Bytes of workspace for paged_decode_attention_groups (0 for invalid sizes). */
+size_t paged_decode_groups_workspace_size(const pkv_decode_group *groups, int32_t n_groups,
+                                          int32_t batch, int32_t num_q_heads);
+
+pkv_status paged_decode_attention_groups(const pkv_decode_group *groups, int32_t n_groups,
+                                         int32_t batch, int32_t num_q_heads, void *workspace,
+                                         size_t ws_bytes, int32_t *dev_status,
+                                         pkv_stream_t stream);
+
+/*
  * Allocation-free decode.  The pages have no counterpart: this entry point
  * exists for callers that cannot allocate device memory where they call the
  * library (a plug-in inside a framework that owns all device memory, a serving
