@@ -398,6 +398,30 @@ def run_fp8_case(args, local):
                       "frac_of_hbm_peak": round(b / s / 1e9 / peaks()[0], 3)}), flush=True)
 
 
+def run_fp8_append_case(args, local):
+    """The bulk append into FP8 pools (every private-suffix token of the
+    batch-32 workload) timed alone (for profiling)."""
+    import torch
+    import block_paged_kv_gb300 as pkv
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = gen.shared_prefix_b32()
+    n = int(np.sum(w.seq_lens - 1024))
+    rows = np.repeat(np.arange(w.batch), w.seq_lens - 1024).astype(np.int32)
+    pos = np.concatenate([np.arange(1024, L) for L in w.seq_lens]).astype(np.int32)
+    slots = torch.from_numpy(pkv.slot_mapping_host(w.block_tables, w.num_blocks, rows, pos, 16)).to(dev)
+    kn = torch.randn((n, 8, 128), dtype=torch.bfloat16, device=dev)
+    vn = torch.randn_like(kn)
+    kp, vp = pkv.fp8_pools(w.num_blocks, 8, 128, dev)
+    ks, vs = float(gen.FP8_K_SCALE), float(gen.FP8_V_SCALE)
+    s = time_loop(torch, lambda: pkv.paged_kv_append(kp, vp, slots, kn, vn, k_scale=ks, v_scale=vs),
+                  args.steps, args.warmup)
+    b = 2 * n * 8 * 128 * (2 + 1) + 4 * n
+    print(json.dumps({"case": "fp8_append", "tokens": n, "us": round(s * 1e6, 2),
+                      "GB/s": round(b / s / 1e9, 1), "frac_of_hbm_peak": round(b / s / 1e9 / peaks()[0], 3)}),
+          flush=True)
+
+
 def secondary_measurements(args, pkv, torch, dev):
     """The other workloads, shorter runs: dense decode (L2 flushed), long
     context full + sliding, bulk append of a whole context."""
@@ -711,9 +735,10 @@ def main():
     ap.add_argument("--no-secondary", dest="secondary", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--case", choices=["step", "prefill", "fp8_decode"], default="step",
-                    help="step: the decode step (the contract line); prefill / fp8_decode: time "
-                         "the chunked prefill or the FP8 decode alone (for profiling)")
+    ap.add_argument("--case", choices=["step", "prefill", "fp8_decode", "fp8_append"], default="step",
+                    help="step: the decode step (the contract line); prefill / fp8_decode / "
+                         "fp8_append: time the chunked prefill, the FP8 decode or the bulk FP8 "
+                         "append alone (for profiling)")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -726,6 +751,8 @@ def main():
         run_prefill_case(args, local)
     elif args.case == "fp8_decode":
         run_fp8_case(args, local)
+    elif args.case == "fp8_append":
+        run_fp8_append_case(args, local)
     else:
         run_pkv(args, rank, world, local)
 

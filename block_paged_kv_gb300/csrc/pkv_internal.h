@@ -26,6 +26,7 @@ struct AppendParams {
     int32_t num_slots;     // num_blocks * block_size
     int32_t head_dim;      // FP8 pools: bf16 rows are quantized with these scales
     float k_scale, v_scale;
+    int32_t heads_per_warp;  // FP8: kv heads one warp quantizes for a token (divides hkv)
 };
 
 // Split plan of one decode call.  A row's key range [lo, L) covers the blocks

@@ -116,6 +116,72 @@ def test_append_saturates_and_keeps_tiny_values(pkv, orc):
     assert ((codes & 0x78) == 0).sum() > 0, "subnormal or zero codes present"
 
 
+@pytest.mark.parametrize("d,hkv", [(64, 2), (128, 8), (256, 1)])
+@pytest.mark.parametrize("shuffle", [False, True])
+def test_append_chunks_whole_blocks_and_ragged_ends(pkv, orc, d, hkv, shuffle):
+    # chunks that start mid-block: whole blocks inside (written as tiles when
+    # their 16 tokens come in order) and ragged ends (written token by token);
+    # shuffled, no block has its tokens in order
+    w = gen.prefill_workload(seed=315 + d, dtype="bf16", num_q_heads=hkv, num_kv_heads=hkv,
+                             head_dim=d, prefix_lens=[0, 13, 64, 250], chunk_lens=[5, 77, 16, 300])
+    slots = pkv.slot_mapping_host(w.block_tables, w.num_blocks, w.new_rows, w.new_pos, 16)
+    order = np.arange(slots.shape[0])
+    if shuffle:
+        order = gen.permutation(316, "order", slots.shape[0]).astype(np.int64)
+    s, kr, vr = slots[order], w.k_new[order], w.v_new[order]
+    kp, vp = gen.fp8_empty_pools(w)
+    k_d, v_d = torch.from_numpy(kp).cuda(), torch.from_numpy(vp).cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv.paged_kv_append(k_d, v_d, torch.from_numpy(np.ascontiguousarray(s)).cuda(),
+                        to_torch(np.ascontiguousarray(kr), "bf16"),
+                        to_torch(np.ascontiguousarray(vr), "bf16"), status=status,
+                        k_scale=KS, v_scale=VS)
+    orc.append(kp, vp, "fp8", np.ascontiguousarray(s), np.ascontiguousarray(kr),
+               np.ascontiguousarray(vr), KS, VS)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert np.array_equal(k_d.cpu().numpy(), kp) and np.array_equal(v_d.cpu().numpy(), vp)
+
+
+# a scale that puts 1.0 / scale 3 float32 ulps above the midpoint 1.0625
+# between the E4M3 values 1.0 and 1.125 (and 2^k / scale above 1.0625 * 2^k)
+_NEAR_TIE_SCALE = float(np.float32(1.0 / (1.0625 * (1 + 3 * 2.0 ** -24))))
+
+
+@pytest.mark.parametrize("whole_blocks", [False, True])
+@pytest.mark.parametrize("scale", [KS, 0.25, _NEAR_TIE_SCALE])
+def test_append_codes_at_rounding_boundaries(pkv, orc, whole_blocks, scale):
+    # rows whose quotients x / scale sit on and next to the midpoints between
+    # neighbouring E4M3 values, both signs, normal and subnormal codes, 448:
+    # with a power-of-two scale the quotients are exact ties; the crafted
+    # scale puts powers of two a few ulps off a tie
+    v = orc.e4m3_decode(np.arange(0x7F, dtype=np.uint8))
+    mids = np.concatenate([(v[:-1] + v[1:]) / 2, [448.0, 464.0]])
+    b = gen.bf16_bits((mids * scale).astype(np.float32)).astype(np.int32)
+    near = np.concatenate([b + k for k in (-2, -1, 0, 1, 2)] +
+                          [gen.bf16_bits(np.float32(2.0) ** np.arange(-6, 8, dtype=np.float32))])
+    near = near.astype(np.uint16)
+    vals = np.concatenate([near, near | np.uint16(0x8000)])
+    D, hkv = 128, 2
+    T = 16 * (len(vals) // (D * hkv * 16) + 1)   # whole blocks of tokens
+    kn = np.resize(vals, T * hkv * D).reshape(T, hkv, D).astype(np.uint16)
+    vn = np.resize(vals[::-1], T * hkv * D).reshape(T, hkv, D).astype(np.uint16)
+    if whole_blocks:
+        slots = np.arange(16, 16 + T, dtype=np.int32)        # blocks 1.. in order
+        nb = T // 16 + 1
+    else:
+        slots = np.arange(T, dtype=np.int32) * 16 + 3        # one token per block
+        nb = T + 1
+    shape = (nb, hkv, 16 * D)
+    kp, vp = np.full(shape, 0x7F, np.uint8), np.full(shape, 0x7F, np.uint8)
+    k_d, v_d = torch.from_numpy(kp).cuda(), torch.from_numpy(vp).cuda()
+    pkv.paged_kv_append(k_d, v_d, torch.from_numpy(slots).cuda(), to_torch(kn, "bf16"),
+                        to_torch(vn, "bf16"), k_scale=scale, v_scale=scale)
+    orc.append(kp, vp, "fp8", slots, kn, vn, scale, scale)
+    torch.cuda.synchronize()
+    assert np.array_equal(k_d.cpu().numpy(), kp) and np.array_equal(v_d.cpu().numpy(), vp)
+
+
 def test_append_negative_slots_skipped(pkv, orc):
     w = gen.decode_workload(seed=311, dtype="bf16", num_q_heads=4, num_kv_heads=2, head_dim=64,
                             context_lens=[20, 40])
