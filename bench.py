@@ -375,6 +375,50 @@ def fp8_b32_setup(pkv, torch, dev):
     return w, step, decode, workload_bytes(w)[0] // 2, st
 
 
+def fp8_prefill_measure(pkv, torch, dev, steps, warmup, flush=None):
+    """The chunked-prefill workload (4 x 512 queries vs a 16384-token prefix)
+    with its K/V in FP8 pools."""
+    w = gen.chunked_prefill()
+    ks, vs = float(gen.FP8_K_SCALE), float(gen.FP8_V_SCALE)
+
+    def up(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    kp, vp = pkv.fp8_pools(w.num_blocks, w.num_kv_heads, w.head_dim, dev)
+    cs, ckr, cvr = gen.live_slots(w)
+    pkv.paged_kv_append(kp, vp, torch.from_numpy(cs).to(dev), up(ckr), up(cvr), k_scale=ks, v_scale=vs)
+    slots = pkv.slot_mapping_host(w.block_tables, w.num_blocks, w.new_rows, w.new_pos, 16)
+    pkv.paged_kv_append(kp, vp, torch.from_numpy(slots).to(dev), up(w.k_new), up(w.v_new),
+                        k_scale=ks, v_scale=vs)
+    q = up(w.q)
+    t = torch.from_numpy(w.block_tables).to(dev)
+    sl = torch.from_numpy(w.seq_lens).to(dev)
+    cu = torch.from_numpy(w.cu_q_lens).to(dev)
+    out = torch.empty_like(q)
+    C = int(w.cu_q_lens[1] - w.cu_q_lens[0])
+    ml = int(w.seq_lens.max())
+    s = time_loop(torch, lambda: pkv.paged_prefill_chunk_attention(q, cu, kp, vp, t, sl, C, 0, w.scale,
+                                                                   out=out, max_seq_len=ml,
+                                                                   k_scale=ks, v_scale=vs),
+                  steps, warmup, flush)
+    keys = sum(int(L) - C + i + 1 for L in w.seq_lens for i in range(C))
+    flops = 4 * w.head_dim * keys * w.num_q_heads
+    return {"us": round(s * 1e6, 2), "TFLOP/s": round(flops / s / 1e12, 1), "flop": flops,
+            "frac_of_bf16_peak": round(flops / s / 1e12 / bf16_peak(), 3),
+            "peak": "measured bf16_tflops (burst): the products are f16, whose dense rate is bf16's",
+            "l2": "flushed before each call" if flush else "not flushed"}
+
+
+def run_fp8_prefill_case(args, local):
+    """The chunked prefill on FP8 pools timed alone (for profiling)."""
+    import torch
+    import block_paged_kv_gb300 as pkv
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    r = fp8_prefill_measure(pkv, torch, dev, args.steps, args.warmup)
+    print(json.dumps(dict(case="fp8_prefill", **r)), flush=True)
+
+
 def run_fp8_case(args, local):
     """The FP8 decode of the batch-32 shared-prefix workload timed alone (for profiling)."""
     import torch
@@ -519,6 +563,8 @@ def secondary_measurements(args, pkv, torch, dev):
                               "flop": flops, "frac_of_bf16_peak": round(flops / s / 1e12 / bf16_peak(), 3),
                               "peak": "measured bf16_tflops (burst)", "l2": "flushed before each call"}
     del kp, vp
+    # the same chunked prefill on FP8 pools (context appended quantized)
+    res["chunked_prefill_fp8"] = fp8_prefill_measure(pkv, torch, dev, 30, 5, flush)
     # speculative verify: 32 rows x 4 queries over 1024..8192-token contexts
     w = gen.verify_steps()
     kp, vp, q = up(w, w.k_pool), up(w, w.v_pool), up(w, w.q)
@@ -735,10 +781,11 @@ def main():
     ap.add_argument("--no-secondary", dest="secondary", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--case", choices=["step", "prefill", "fp8_decode", "fp8_append"], default="step",
+    ap.add_argument("--case", choices=["step", "prefill", "fp8_decode", "fp8_append", "fp8_prefill"],
+                    default="step",
                     help="step: the decode step (the contract line); prefill / fp8_decode / "
-                         "fp8_append: time the chunked prefill, the FP8 decode or the bulk FP8 "
-                         "append alone (for profiling)")
+                         "fp8_append / fp8_prefill: time the chunked prefill, the FP8 decode, the "
+                         "bulk FP8 append or the FP8 chunked prefill alone (for profiling)")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -753,6 +800,8 @@ def main():
         run_fp8_case(args, local)
     elif args.case == "fp8_append":
         run_fp8_append_case(args, local)
+    elif args.case == "fp8_prefill":
+        run_fp8_prefill_case(args, local)
     else:
         run_pkv(args, rank, world, local)
 

@@ -736,7 +736,7 @@ pkv_status paged_prefill_chunk_attention(const void *q, const int32_t *cu_q_lens
     p.q_tiles = static_cast<int32_t>(ceil_div64(max_q_len, qpt));
     p.kv_splits = 1;
     p.split_tiles = 0;
-    if (pool->dtype == PKV_BF16) {
+    if (pool->dtype != PKV_F32) {
         const PrefillSplit sp = prefill_split_plan(batch, num_q_heads, pool->num_kv_heads,
                                                    pool->head_dim, pool->block_size, max_q_len,
                                                    p.max_len, window, num_sms_current());
@@ -755,11 +755,18 @@ pkv_status paged_prefill_chunk_attention(const void *q, const int32_t *cu_q_lens
         }
     }
     p.scale_log2 = scale * 1.4426950408889634f;
+    p.v_scale = 1.f;
+    if (pool->dtype == PKV_FP8_E4M3) {
+        p.scale_log2 *= pool->k_scale;
+        p.v_scale = pool->v_scale;
+    }
     if (static_cast<int64_t>(batch) * p.hkv * p.q_tiles * p.kv_splits > INT32_MAX)
         return PKV_ERR_UNSUPPORTED;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t err;
-    if (pool->dtype == PKV_BF16) {
+    if (pool->dtype == PKV_FP8_E4M3) {
+        err = launch_prefill_fp8(p, st);
+    } else if (pool->dtype == PKV_BF16) {
         if (!encode_fn_ready()) return PKV_ERR_CUDA;
         CUtensorMap kmap, vmap;
         if (!encode_pool_map(&kmap, pool->k, *pool) || !encode_pool_map(&vmap, pool->v, *pool))

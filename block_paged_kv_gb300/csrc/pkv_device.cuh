@@ -233,6 +233,35 @@ __device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi)
     return r;
 }
 
+// f16 halves of a packed pair as floats (exact)
+__device__ __forceinline__ float f16lo_to_f32(uint32_t v)
+{
+    float f;
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.f32.f16 %0, l;\n\t}" : "=f"(f) : "r"(v));
+    return f;
+}
+__device__ __forceinline__ float f16hi_to_f32(uint32_t v)
+{
+    float f;
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.f32.f16 %0, h;\n\t}" : "=f"(f) : "r"(v));
+    return f;
+}
+
+// bf16 pair -> f16 pair (exact inside the f16 range); `bad` is set when a
+// magnitude is past 65504
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v, bool &bad)
+{
+    const float lo = __uint_as_float(v << 16), hi = __uint_as_float(v & 0xFFFF0000u);
+    bad = bad || fabsf(lo) > 65504.f || fabsf(hi) > 65504.f;
+    return pack_f16x2(lo, hi);
+}
+
+// 4-byte shared-memory store
+__device__ __forceinline__ void sts32(uint32_t addr, uint32_t v)
+{
+    asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
 // 4-byte shared-memory load
 __device__ __forceinline__ uint32_t lds32(uint32_t addr)
 {

@@ -129,7 +129,8 @@ struct PrefillParams {
     int32_t split_tiles;
     float *ws_o;   // [batch][max_q_len][hq][kv_splits][128] unnormalised weighted values
     float *ws_ml;  // [batch][max_q_len][hq][kv_splits][2]: reference max (log2 units), weight sum
-    float scale_log2;
+    float scale_log2;  // scale * log2(e) (* k_scale for FP8 pools)
+    float v_scale;     // FP8 pools: applied to the weighted values
 };
 
 cudaError_t launch_append(const AppendParams &p, cudaStream_t stream);
@@ -149,6 +150,7 @@ size_t prefill_split_ws_bytes(int32_t batch, int32_t hq, int32_t max_q_len, cons
 cudaError_t launch_prefill_bf16(const PrefillParams &p, const CUtensorMap &kmap,
                                 const CUtensorMap &vmap, cudaStream_t stream);
 cudaError_t launch_prefill_f32(const PrefillParams &p, cudaStream_t stream);
+cudaError_t launch_prefill_fp8(const PrefillParams &p, cudaStream_t stream);
 
 // bf16 pools: TMA + mbarrier pipeline, mma.sync tiles.  kmap/vmap: 5-D tensor
 // maps (64 dims, slot, 64-dim region, kv head, block), whole-tile boxes, 128B swizzle.

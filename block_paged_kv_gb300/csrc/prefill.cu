@@ -50,14 +50,24 @@ constexpr int kStages = 4;                // K ring and V ring depth
 constexpr int kQOff = 0;
 constexpr int kKOff = kQOff + kQTiles * kQBytes;
 constexpr int kVOff = kKOff + kStages * kTileBytes;
-constexpr int kBarOff = kVOff + kStages * kTileBytes;
-// barriers: k_full[4], k_empty[4], v_full[4], v_empty[4], s_full[tile][buf],
-// p_full[tile][buf], pv_done[tile]
-constexpr int kNumBars = 4 * kStages + 4 + 4 + 2;
-constexpr int kMaskOff = kBarOff + kNumBars * 8;
-constexpr int kTmemOff = kMaskOff + kStages * 4;
-constexpr int kBytes = kTmemOff + 16;
-constexpr int kLaunchBytes = kBytes + 1024;
+// FP8 pools: the producers stage each tile's E4M3 bytes (4 blocks x 2 KiB)
+// by bulk copy, two tiles deep, and widen them into the ring
+constexpr int kF8BlockBytes = 16 * kD;                 // one (block, kv head) E4M3 tile
+constexpr int kF8StageTile = kBlocks * kF8BlockBytes;  // 8 KiB
+template <bool kF8>
+struct Layout {
+    static constexpr int kStagingOff = kVOff + kStages * kTileBytes;
+    static constexpr int kStagingBytes = kF8 ? 2 * 2 * kF8StageTile : 0;  // K and V, 2 deep
+    static constexpr int kBarOff = kStagingOff + kStagingBytes;
+    // barriers: k_full[4], k_empty[4], v_full[4], v_empty[4], s_full[tile][buf],
+    // p_full[tile][buf], pv_done[tile], FP8: staged[K/V][2]
+    static constexpr int kNumBars = 4 * kStages + 4 + 4 + 2 + (kF8 ? 4 : 0);
+    static constexpr int kMaskOff = kBarOff + kNumBars * 8;
+    static constexpr int kTmemOff = kMaskOff + kStages * 4;
+    static constexpr int kBytes = kTmemOff + 16;
+    static constexpr int kLaunchBytes = kBytes + 1024;
+    static_assert(kLaunchBytes <= 227 * 1024, "shared memory of one CTA");
+};
 // warps: 0 K producer, 1 MMA issue for tile A, 2 V producer, 3 MMA issue for
 // tile B;
 // 4-7 softmax of query tile A, 8-11 of tile B (one M-row per thread)
@@ -66,7 +76,6 @@ constexpr int kThreads = 384;
 // tensor memory: S_x[buf] (64 columns each) at 128x + 64buf, O_x at 256 + 128x
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kRescaleLog2 = 8;      // O is rescaled only when the max grows past 2^8
-static_assert(kLaunchBytes <= 227 * 1024, "shared memory of one CTA");
 }  // namespace pf
 
 struct PrefillRowInfo {
@@ -117,30 +126,33 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, int la
 // ---------------------------------------------------------------------------
 // bf16, tcgen05
 // ---------------------------------------------------------------------------
+template <bool kF8>
 __global__ void __launch_bounds__(pf::kThreads, 1)
-    prefill_bf16_kernel(const __grid_constant__ CUtensorMap kmap,
-                        const __grid_constant__ CUtensorMap vmap, const PrefillParams p)
+    prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                   const PrefillParams p)
 {
     using namespace pf;
+    using L = Layout<kF8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t *q_s = smem + kQOff;
     uint8_t *k_s = smem + kKOff;
     uint8_t *v_s = smem + kVOff;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kBarOff);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBarOff);
     uint64_t *k_full = bars, *k_empty = bars + kStages, *v_full = bars + 2 * kStages,
              *v_empty = bars + 3 * kStages;
     uint64_t *s_full = bars + 4 * kStages;      // [tile * 2 + buf]
     uint64_t *p_full = bars + 4 * kStages + 4;  // [tile * 2 + buf]
     uint64_t *pv_done = bars + 4 * kStages + 8; // [tile]
-    uint32_t *kmask = reinterpret_cast<uint32_t *>(smem + kMaskOff);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kTmemOff);
+    uint64_t *staged = bars + 4 * kStages + 10;  // FP8: [K/V * 2 + buffer]
+    uint32_t *kmask = reinterpret_cast<uint32_t *>(smem + L::kMaskOff);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kTmemOff);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = p.group;
     const int qpt = kRows / G;  // queries per query tile
 
-    if (threadIdx.x == 0) {
+    if (!kF8 && threadIdx.x == 0) {
         tma_prefetch_desc(&kmap);
         tma_prefetch_desc(&vmap);
     }
@@ -189,6 +201,8 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         }
         mbar_init(&pv_done[0], 1);
         mbar_init(&pv_done[1], 1);
+        if (kF8)
+            for (int i = 0; i < 4; ++i) mbar_init(&staged[i], 1);
         fence_mbar_init();
     }
     if (warp == 1) tc::alloc(tmem_slot, kTmemCols);
@@ -207,9 +221,17 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         // a negative scale: stage -q (sign bits flipped, exact), so that the
         // scores the tensor cores produce always take a positive factor
         const uint32_t flip = p.scale_log2 < 0.f ? 0x80008000u : 0u;
+        bool qbad = false;
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
             uint4 v = valid ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+            if constexpr (kF8) {
+                // FP8 pools: the products are f16 x f16 (exact inside the f16 range)
+                v.x = bf16x2_to_f16x2(v.x, qbad);
+                v.y = bf16x2_to_f16x2(v.y, qbad);
+                v.z = bf16x2_to_f16x2(v.z, qbad);
+                v.w = bf16x2_to_f16x2(v.w, qbad);
+            }
             v.x ^= flip;
             v.y ^= flip;
             v.z ^= flip;
@@ -217,6 +239,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             *reinterpret_cast<uint4 *>(qt_s + (c >> 3) * (kRows * 128) + i * 128 +
                                        (((c & 7) ^ (i & 7)) << 4)) = v;
         }
+        if (qbad) report(p.status, PKV_DEV_Q_RANGE);
         fence_proxy_async_smem();  // read by the tensor cores (async proxy)
     }
     tc::fence_before();
@@ -229,37 +252,158 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
     if (warp == 0 || warp == 2) {
         // ------------------------------------------ K (warp 0) / V (warp 2) producer
         const bool is_k = warp == 0;
-        const CUtensorMap *map = is_k ? &kmap : &vmap;
         uint8_t *ring = is_k ? k_s : v_s;
         uint64_t *full = is_k ? k_full : v_full;
         uint64_t *empty = is_k ? k_empty : v_empty;
-        const uint64_t policy = l2_evict_last_policy();  // re-read by the row's other CTAs
         const int32_t *trow = p.tables + static_cast<int64_t>(w.r) * p.width;
-        for (int32_t jj = 0; jj < ntile; ++jj) {
-            const int st = jj % kStages;
-            if (jj >= kStages && !warp_wait(&empty[st], ((jj / kStages) + 1) & 1, lane, p.status)) break;
-            const int32_t kb = (jt0 + jj) * kBlocks + lane;  // logical block of lane < kBlocks
-            const bool in_range = lane < kBlocks && kb < p.width && kb * 16 < w.kv_hi &&
-                                  (kb + 1) * 16 > w.kv_lo;
-            const int32_t id = in_range ? __ldg(trow + kb) : -1;
-            const bool good = in_range && static_cast<uint32_t>(id) < static_cast<uint32_t>(p.num_blocks);
-            if (is_k && in_range && !good) report(p.status, PKV_DEV_BAD_BLOCK);
-            const uint32_t mask = __ballot_sync(0xffffffffu, good) & ((1u << kBlocks) - 1u);
-            if (lane == 0) {
-                if (is_k) kmask[st] = mask;
-                if (mask == 0)
-                    mbar_arrive(&full[st]);
-                else
-                    mbar_arrive_expect_tx(&full[st], __popc(mask) * 2 * 2048);
-            }
-            __syncwarp();
-            uint8_t *dst = ring + st * kTileBytes;
+        if constexpr (kF8) {
+            // FP8: tile jj's E4M3 blocks are bulk-copied into staging buffer
+            // jj % 2 (two tiles ahead of the ring), then widened to f16 into
+            // the ring stage: K as the bf16 path lays it out (key rows, 64-dim
+            // 128-byte-swizzled regions), V transposed (dim rows of the tile's
+            // 64 keys, 128-byte swizzled), so that a pair of codes becomes
+            // one 4-byte store.  Value columns of keys outside [kv_lo, kv_hi)
+            // or of blocks not loaded are written as zeros (stale slots may
+            // hold NaN codes).
+            const uint64_t policy = l2_evict_last_policy();  // re-read by the row's other CTAs
+            const uint8_t *pool = static_cast<const uint8_t *>(is_k ? p.k_pool : p.v_pool);
+            uint8_t *stg = smem + L::kStagingOff + (is_k ? 0 : 2) * kF8StageTile;
+            uint64_t *stg_bar = staged + (is_k ? 0 : 2);
+            auto fetch = [&](int32_t jj) {  // whole warp; returns the mask of loaded blocks
+                const int32_t kb = (jt0 + jj) * kBlocks + lane;
+                const bool in_range = lane < kBlocks && kb < p.width && kb * 16 < w.kv_hi &&
+                                      (kb + 1) * 16 > w.kv_lo;
+                const int32_t id = in_range ? __ldg(trow + kb) : -1;
+                const bool good = in_range && static_cast<uint32_t>(id) < static_cast<uint32_t>(p.num_blocks);
+                if (is_k && in_range && !good) report(p.status, PKV_DEV_BAD_BLOCK);
+                const uint32_t mask = __ballot_sync(0xffffffffu, good) & ((1u << kBlocks) - 1u);
+                const int sb = jj & 1;
+                if (lane == 0) {
+                    if (mask == 0)
+                        mbar_arrive(&stg_bar[sb]);
+                    else
+                        mbar_arrive_expect_tx(&stg_bar[sb], __popc(mask) * kF8BlockBytes);
+                }
+                __syncwarp();
 #pragma unroll
-            for (int b = 0; b < kBlocks; ++b) {
-                const int32_t bid = __shfl_sync(0xffffffffu, id, b);
-                if (((mask >> b) & 1u) && elect_one()) {
-                    tma_load_4d(dst + b * 2048, map, &full[st], 0, 0, w.g, bid, policy);
-                    tma_load_4d(dst + kKVRegion + b * 2048, map, &full[st], 64, 0, w.g, bid, policy);
+                for (int b = 0; b < kBlocks; ++b) {
+                    const int32_t bid = __shfl_sync(0xffffffffu, id, b);
+                    if (((mask >> b) & 1u) && elect_one())
+                        bulk_load(stg + sb * kF8StageTile + b * kF8BlockBytes,
+                                  pool + (static_cast<int64_t>(bid) * p.hkv + w.g) * kF8BlockBytes,
+                                  kF8BlockBytes, &stg_bar[sb], policy);
+                }
+                __syncwarp();
+                return mask;
+            };
+            uint32_t smask[2] = {0u, 0u};
+            smask[0] = fetch(0);
+            if (ntile > 1) smask[1] = fetch(1);
+            for (int32_t jj = 0; jj < ntile; ++jj) {
+                const int st = jj % kStages, sb = jj & 1;
+                if (jj >= kStages && !warp_wait(&empty[st], ((jj / kStages) + 1) & 1, lane, p.status)) break;
+                if (!warp_wait(&stg_bar[sb], (jj >> 1) & 1, lane, p.status)) break;
+                const uint32_t mask = smask[sb];
+                if (is_k && lane == 0) kmask[st] = mask;
+                const uint32_t src = smem_u32(stg + sb * kF8StageTile);
+                const uint32_t dst = smem_u32(ring + st * kTileBytes);
+                const int32_t tbase = (jt0 + jj) * kKeys;
+                const bool edge = tbase < w.kv_lo || tbase + kKeys > w.kv_hi;
+#pragma unroll
+                for (int b = 0; b < kBlocks; ++b) {
+                    const bool loaded = (mask >> b) & 1u;
+                    if (is_k) {
+                        // the scores of keys not loaded are masked by the softmax
+                        if (!loaded) continue;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            // chunk ch: 64-dim group ch/64, token half (ch/32)%2,
+                            // token 8 half + (ch%32)/4, pair class c = ch%4
+                            const int ch = lane + 32 * i;
+                            const int grp = ch >> 6, half = (ch >> 5) & 1, c = ch & 3;
+                            const int row = b * 16 + half * 8 + ((ch & 31) >> 2);
+                            const uint4 q4 = lds128(src + b * kF8BlockBytes + ch * 16);
+                            const uint32_t wv[4] = {q4.x, q4.y, q4.z, q4.w};
+                            const uint32_t base = dst + grp * kKVRegion + row * 128 + 4 * c;
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk) {
+                                uint32_t lo, hi;  // dims 16kk + 2c, +1 | 16kk + 2c + 8, +9
+                                e4m3x4_to_f16x2x2(wv[kk], lo, hi);
+                                sts32(base + (((2 * kk) ^ (row & 7)) << 4), lo);
+                                sts32(base + (((2 * kk + 1) ^ (row & 7)) << 4), hi);
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            // chunk ch: 32-dim group ch/32, dim class n = (ch%32)/4,
+                            // token pairs c = ch%4: words jn = dim 32g + 8jn + n,
+                            // keys 16b + {2c, 2c+1} (low half) and + 8 (high half)
+                            const int ch = lane + 32 * i;
+                            const int g32 = ch >> 5, n = (ch & 31) >> 2, c = ch & 3;
+                            uint32_t wv[4] = {0u, 0u, 0u, 0u};
+                            if (loaded) {
+                                const uint4 q4 = lds128(src + b * kF8BlockBytes + ch * 16);
+                                wv[0] = q4.x; wv[1] = q4.y; wv[2] = q4.z; wv[3] = q4.w;
+                            }
+                            uint32_t mk0 = 0xffffffffu, mk1 = 0xffffffffu;
+                            if (edge) {
+                                auto live = [&](int k) {
+                                    const int32_t kp = tbase + b * 16 + k;
+                                    return kp >= w.kv_lo && kp < w.kv_hi;
+                                };
+                                mk0 = (live(2 * c) ? 0x0000ffffu : 0u) | (live(2 * c + 1) ? 0xffff0000u : 0u);
+                                mk1 = (live(2 * c + 8) ? 0x0000ffffu : 0u) | (live(2 * c + 9) ? 0xffff0000u : 0u);
+                            }
+#pragma unroll
+                            for (int jn = 0; jn < 4; ++jn) {
+                                const int d = g32 * 32 + jn * 8 + n;
+                                uint32_t lo = 0u, hi = 0u;
+                                if (loaded) e4m3x4_to_f16x2x2(wv[jn], lo, hi);
+                                const uint32_t rowb = dst + d * 128 + 4 * c;
+                                sts32(rowb + (((2 * b) ^ (d & 7)) << 4), lo & mk0);
+                                sts32(rowb + (((2 * b + 1) ^ (d & 7)) << 4), hi & mk1);
+                            }
+                        }
+                    }
+                }
+                // the ring stage is read by the tensor cores (async proxy) and
+                // the staging buffer is refilled by bulk copies after these
+                // generic-proxy accesses
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&full[st]);
+                if (jj + 2 < ntile) smask[sb] = fetch(jj + 2);
+            }
+        } else {
+            const CUtensorMap *map = is_k ? &kmap : &vmap;
+            const uint64_t policy = l2_evict_last_policy();  // re-read by the row's other CTAs
+            for (int32_t jj = 0; jj < ntile; ++jj) {
+                const int st = jj % kStages;
+                if (jj >= kStages && !warp_wait(&empty[st], ((jj / kStages) + 1) & 1, lane, p.status)) break;
+                const int32_t kb = (jt0 + jj) * kBlocks + lane;  // logical block of lane < kBlocks
+                const bool in_range = lane < kBlocks && kb < p.width && kb * 16 < w.kv_hi &&
+                                      (kb + 1) * 16 > w.kv_lo;
+                const int32_t id = in_range ? __ldg(trow + kb) : -1;
+                const bool good = in_range && static_cast<uint32_t>(id) < static_cast<uint32_t>(p.num_blocks);
+                if (is_k && in_range && !good) report(p.status, PKV_DEV_BAD_BLOCK);
+                const uint32_t mask = __ballot_sync(0xffffffffu, good) & ((1u << kBlocks) - 1u);
+                if (lane == 0) {
+                    if (is_k) kmask[st] = mask;
+                    if (mask == 0)
+                        mbar_arrive(&full[st]);
+                    else
+                        mbar_arrive_expect_tx(&full[st], __popc(mask) * 2 * 2048);
+                }
+                __syncwarp();
+                uint8_t *dst = ring + st * kTileBytes;
+#pragma unroll
+                for (int b = 0; b < kBlocks; ++b) {
+                    const int32_t bid = __shfl_sync(0xffffffffu, id, b);
+                    if (((mask >> b) & 1u) && elect_one()) {
+                        tma_load_4d(dst + b * 2048, map, &full[st], 0, 0, w.g, bid, policy);
+                        tma_load_4d(dst + kKVRegion + b * 2048, map, &full[st], 64, 0, w.g, bid, policy);
+                    }
                 }
             }
         }
@@ -271,14 +415,19 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         // finishes P(j).  One thread's products execute in issue order, so a
         // product never overtakes an earlier read of the same columns.
         const int x = warp >> 1;
-        constexpr uint32_t idS = tc::idesc_bf16(kRows, kKeys, 0, 0);
-        constexpr uint32_t idO = tc::idesc_bf16(kRows, kD, 0, 1);
+        // bf16: V is MN-major (key rows); FP8: V^T is K-major (dim rows of keys)
+        constexpr uint32_t idS = kF8 ? tc::idesc_f16(kRows, kKeys, 0, 0) : tc::idesc_bf16(kRows, kKeys, 0, 0);
+        constexpr uint32_t idO = kF8 ? tc::idesc_f16(kRows, kD, 0, 0) : tc::idesc_bf16(kRows, kD, 0, 1);
         // Descriptors are built once; moving along K (or to the next 16 keys
         // of V) adds the byte offset / 16 to the start-address field, which
         // cannot carry out of it inside shared memory.
         const uint64_t dq = tc::smem_desc(smem_u32(q_s + x * kQBytes), 16, 1024);
         const uint64_t dk = tc::smem_desc(smem_u32(k_s), 16, 1024);
-        const uint64_t dv = tc::smem_desc(smem_u32(v_s), kKVRegion, 1024);
+        const uint64_t dv = kF8 ? tc::smem_desc(smem_u32(v_s), 16, 1024)
+                                : tc::smem_desc(smem_u32(v_s), kKVRegion, 1024);
+        // the B operand of the keys 16kk .. 16kk+15: bf16 key rows 16kk.. (2 KiB
+        // on); FP8 32 bytes along each dim row
+        constexpr uint64_t kVStep = kF8 ? (32 >> 4) : (2048 >> 4);
         constexpr uint64_t kStageStep = kTileBytes >> 4;
         const uint32_t tO_x = tO(x);
         // The whole warp runs these; one elected lane issues a group's
@@ -306,15 +455,14 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             const uint32_t a = tS(x, jj & 1);
             const uint32_t first = jj > 0 ? 1u : 0u;
             // keys 16g..16g+15 hold P hi in S columns 16g..16g+7 and P lo in
-            // 16g+8..16g+15 (bf16 pairs)
+            // 16g+8..16g+15 (bf16 pairs; f16 for FP8 pools)
             if (elect_one()) {
 #pragma unroll
                 for (int part = 0; part < 2; ++part)
 #pragma unroll
                     for (int kk = 0; kk < kBlocks; ++kk)
-                        tc::mma_ts(tO_x, a + 16 * kk + 8 * part,
-                                   vd + static_cast<uint64_t>(kk * 2048 >> 4), idO,
-                                   (part > 0 || kk > 0) ? 1u : first);
+                        tc::mma_ts(tO_x, a + 16 * kk + 8 * part, vd + kVStep * static_cast<uint64_t>(kk),
+                                   idO, (part > 0 || kk > 0) ? 1u : first);
                 tc::commit(&pv_done[x]);
                 tc::commit(&v_empty[jj % kStages]);
             }
@@ -443,9 +591,15 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
                         const float a = fast_exp2(fmaf(s[16 * g + 2 * e], sl, nmu));
                         const float b = fast_exp2(fmaf(s[16 * g + 2 * e + 1], sl, nmu));
                         ls[e & 3] += a + b;
-                        const uint32_t hi = pack_bf16x2(a, b);
-                        pk[e] = hi;
-                        pk[8 + e] = pack_bf16x2(a - bf16lo_to_f32(hi), b - bf16hi_to_f32(hi));
+                        if constexpr (kF8) {
+                            const uint32_t hi = pack_f16x2(a, b);
+                            pk[e] = hi;
+                            pk[8 + e] = pack_f16x2(a - f16lo_to_f32(hi), b - f16hi_to_f32(hi));
+                        } else {
+                            const uint32_t hi = pack_bf16x2(a, b);
+                            pk[e] = hi;
+                            pk[8 + e] = pack_bf16x2(a - bf16lo_to_f32(hi), b - bf16hi_to_f32(hi));
+                        }
                     }
                     tc::st16(sx + 16 * g, pk);
                 }
@@ -462,7 +616,9 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
                 abort = true;
                 break;
             }
-            const bool edge = mask != (1u << kBlocks) - 1u || tbase < w.kv_lo || tbase + kKeys > w.kv_hi;
+            // (FP8: the V producer wrote those columns as zeros)
+            const bool edge = !kF8 && (mask != (1u << kBlocks) - 1u || tbase < w.kv_lo ||
+                                       tbase + kKeys > w.kv_hi);
             if (edge) {
                 // thread row r < 64 zeroes key row r's first 64 dims, r >= 64
                 // the second 64 dims of key row r - 64
@@ -502,16 +658,17 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
                     tc::ld32(ox + c * 32, r32);
                     tc::wait_ld();
                     if (valid_row) {
+                        const float vs = kF8 ? p.v_scale : 1.f;
 #pragma unroll
                         for (int v = 0; v < 8; ++v)
-                            dst[c * 8 + v] = make_float4(__uint_as_float(r32[4 * v]), __uint_as_float(r32[4 * v + 1]),
-                                                         __uint_as_float(r32[4 * v + 2]), __uint_as_float(r32[4 * v + 3]));
+                            dst[c * 8 + v] = make_float4(__uint_as_float(r32[4 * v]) * vs, __uint_as_float(r32[4 * v + 1]) * vs,
+                                                         __uint_as_float(r32[4 * v + 2]) * vs, __uint_as_float(r32[4 * v + 3]) * vs);
                     }
                 }
                 if (valid_row) *reinterpret_cast<float2 *>(p.ws_ml + pi * 2) = make_float2(m_ref, l);
             } else {
                 tc::fence_after();
-                const float inv = l > 0.f ? 1.f / l : 0.f;
+                const float inv = (l > 0.f ? 1.f / l : 0.f) * (kF8 ? p.v_scale : 1.f);
                 const int h = row % G;
                 uint4 *dst = reinterpret_cast<uint4 *>(p.out) +
                              ((static_cast<int64_t>(__ldg(p.cu_q_lens + w.r)) + w.i0 + t) * p.hq +
@@ -705,15 +862,14 @@ __global__ void __launch_bounds__(kMergeWarps * 32) prefill_merge_kernel(const P
 bool prefill_shape_built(pkv_dtype dtype, int32_t D, int32_t bs, int32_t G)
 {
     if (G < 1 || G > 16) return false;
-    if (dtype == PKV_BF16) return D == pf::kD && bs == 16 && (pf::kRows % G) == 0;
-    if (dtype != PKV_F32) return false;  // FP8: short chunks only, on the decode kernel
+    if (dtype == PKV_BF16 || dtype == PKV_FP8_E4M3) return D == pf::kD && bs == 16 && (pf::kRows % G) == 0;
     return (D == 32 || D == 64 || D == 128 || D == 256) && bs <= 64 && bs * D <= 4096 &&
            (kPf32Pairs % G) == 0;
 }
 
 int32_t prefill_queries_per_cta(pkv_dtype dtype, int32_t G)
 {
-    return dtype == PKV_BF16 ? pf::kQTiles * (pf::kRows / G) : kPf32Pairs / G;
+    return dtype != PKV_F32 ? pf::kQTiles * (pf::kRows / G) : kPf32Pairs / G;
 }
 
 PrefillSplit prefill_split_plan(int32_t batch, int32_t hq, int32_t hkv, int32_t D, int32_t bs,
@@ -747,18 +903,19 @@ size_t prefill_split_ws_bytes(int32_t batch, int32_t hq, int32_t max_q_len, cons
     return o + n * 2 * sizeof(float);
 }
 
-cudaError_t launch_prefill_bf16(const PrefillParams &p, const CUtensorMap &kmap,
-                                const CUtensorMap &vmap, cudaStream_t stream)
+template <bool kF8>
+static cudaError_t launch_prefill_tc(const PrefillParams &p, const CUtensorMap &kmap,
+                                    const CUtensorMap &vmap, cudaStream_t stream)
 {
     const int64_t ctas = static_cast<int64_t>(p.batch) * p.hkv * p.q_tiles * p.kv_splits;
     if (ctas == 0) return cudaSuccess;
-    cudaError_t err = cudaFuncSetAttribute(prefill_bf16_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           pf::kLaunchBytes);
+    constexpr int smem = pf::Layout<kF8>::kLaunchBytes;
+    cudaError_t err = cudaFuncSetAttribute(prefill_kernel<kF8>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
     prof_begin(PKV_KERNEL_PREFILL, stream);
-    err = launch_pdl(prefill_bf16_kernel, dim3(static_cast<unsigned>(ctas)), dim3(pf::kThreads),
-                     pf::kLaunchBytes, stream, kmap, vmap, p);
+    err = launch_pdl(prefill_kernel<kF8>, dim3(static_cast<unsigned>(ctas)), dim3(pf::kThreads), smem,
+                     stream, kmap, vmap, p);
     if (err == cudaSuccess && p.kv_splits > 1) {
         const int64_t items = static_cast<int64_t>(p.batch) * p.max_q_len * p.hq;
         err = launch_pdl(prefill_merge_kernel,
@@ -767,6 +924,18 @@ cudaError_t launch_prefill_bf16(const PrefillParams &p, const CUtensorMap &kmap,
     }
     prof_end(PKV_KERNEL_PREFILL, stream);
     return err;
+}
+
+cudaError_t launch_prefill_bf16(const PrefillParams &p, const CUtensorMap &kmap,
+                                const CUtensorMap &vmap, cudaStream_t stream)
+{
+    return launch_prefill_tc<false>(p, kmap, vmap, stream);
+}
+
+cudaError_t launch_prefill_fp8(const PrefillParams &p, cudaStream_t stream)
+{
+    const CUtensorMap none{};  // the FP8 producers read the pools by bulk copy
+    return launch_prefill_tc<true>(p, none, none, stream);
 }
 
 cudaError_t launch_prefill_f32(const PrefillParams &p, cudaStream_t stream)

@@ -32,6 +32,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_
            (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// The same with f16 A and B (FP8 pools widened to f16 in shared memory).
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int a_mn, int b_mn)
+{
+    return (1u << 4) | (static_cast<uint32_t>(a_mn) << 15) | (static_cast<uint32_t>(b_mn) << 16) |
+           (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
 // D[tmem] (+)= A[smem] * B[smem]
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                        uint32_t idesc, uint32_t accumulate)

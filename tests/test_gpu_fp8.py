@@ -260,7 +260,7 @@ def test_query_out_of_f16_range_flagged(pkv, orc):
 
 
 # ---------------------------------------------------------------------------
-# verify steps (a few queries per row) and the unsupported long chunk
+# verify steps (a few queries per row) and longer chunks (tensor-core prefill)
 # ---------------------------------------------------------------------------
 
 @pytest.mark.parametrize("d,hq,hkv,chunks", [
@@ -285,11 +285,60 @@ def test_verify_steps(pkv, orc, d, hq, hkv, chunks, window):
     assert_close(to_f64(out), ref, "bf16", f"fp8 verify d{d} {hq}/{hkv} w{window}")
 
 
-def test_long_chunk_unsupported(pkv, orc):
-    w = gen.prefill_workload(seed=380, dtype="bf16", num_q_heads=8, num_kv_heads=2, head_dim=128,
+def _prefill(pkv, s, w, window):
+    out = pkv.paged_prefill_chunk_attention(s.q, s.cu, s.k_pool, s.v_pool, s.tables, s.seq_lens,
+                                            int(np.max(np.diff(w.cu_q_lens))), window, w.scale,
+                                            status=s.status, k_scale=KS, v_scale=VS)
+    torch.cuda.synchronize()
+    assert int(s.status.item()) == 0
+    return to_f64(out)
+
+
+@pytest.mark.parametrize("hq,hkv,window", [(8, 2, 0), (32, 8, 0), (16, 16, 64), (8, 1, 200)])
+def test_prefill_chunks(pkv, orc, hq, hkv, window):
+    # chunks past 16 (query, head) pairs run on the tensor-core prefill kernel,
+    # its producers widening the E4M3 tiles to f16 in shared memory
+    w = gen.prefill_workload(seed=390 + hq + window, dtype="bf16", num_q_heads=hq,
+                             num_kv_heads=hkv, head_dim=128, prefix_lens=[0, 90, 300, 1000],
+                             chunk_lens=[37, 64, 130, 300], window=window)
+    s = Fp8Step(pkv, orc, w)
+    ref = orc.prefill(w.q, w.cu_q_lens, s.kp, s.vp, "fp8", w.block_tables, w.seq_lens, window,
+                      w.scale, k_scale=KS, v_scale=VS)
+    assert_close(_prefill(pkv, s, w, window), ref, "bf16", f"fp8 prefill {hq}/{hkv} w{window}")
+
+
+@pytest.mark.parametrize("scale", [-0.3, 0.0])
+def test_prefill_scale_sign_and_zero(pkv, orc, scale):
+    w = gen.prefill_workload(seed=395, dtype="bf16", num_q_heads=8, num_kv_heads=2, head_dim=128,
+                             prefix_lens=[0, 90, 300], chunk_lens=[37, 64, 130])
+    w = dataclasses.replace(w, scale=scale)
+    s = Fp8Step(pkv, orc, w)
+    ref = orc.prefill(w.q, w.cu_q_lens, s.kp, s.vp, "fp8", w.block_tables, w.seq_lens, 0, w.scale,
+                      k_scale=KS, v_scale=VS)
+    assert_close(_prefill(pkv, s, w, 0), ref, "bf16", f"fp8 prefill scale {scale}")
+
+
+def test_prefill_full_size(pkv, orc):
+    # the chunked-prefill workload (4 x 512 queries after 16384 cached tokens)
+    # on FP8 pools, sampled outputs
+    w = gen.chunked_prefill()
+    s = Fp8Step(pkv, orc, w, check_pool=False)
+    got = _prefill(pkv, s, w, 0)
+    u = gen.uniform_ints(396, "samples", 3 * 64, 0, 1 << 30)
+    samples = np.array([(int(u[3 * k]) % w.batch, int(u[3 * k + 1]) % 512, int(u[3 * k + 2]) % 32)
+                        for k in range(64)] + [(r, 511, 0) for r in range(w.batch)], dtype=np.int32)
+    ref = orc.prefill(w.q, w.cu_q_lens, s.kp, s.vp, "fp8", w.block_tables, w.seq_lens, 0, w.scale,
+                      samples=samples, k_scale=KS, v_scale=VS)
+    rows = w.cu_q_lens[samples[:, 0]] + samples[:, 1]
+    assert_close(got[rows, samples[:, 2]], ref, "bf16", "fp8 chunked prefill full size")
+
+
+def test_prefill_query_range_flagged(pkv, orc):
+    w = gen.prefill_workload(seed=397, dtype="bf16", num_q_heads=8, num_kv_heads=2, head_dim=128,
                              prefix_lens=[16], chunk_lens=[64])
     s = Fp8Step(pkv, orc, w, check_pool=False)
-    with pytest.raises(pkv.PkvError) as e:
-        pkv.paged_prefill_chunk_attention(s.q, s.cu, s.k_pool, s.v_pool, s.tables, s.seq_lens,
-                                          64, 0, w.scale, k_scale=KS, v_scale=VS)
-    assert e.value.code == pkv.PKV_ERR_UNSUPPORTED
+    s.q[3, 1, 7] = 1e5
+    pkv.paged_prefill_chunk_attention(s.q, s.cu, s.k_pool, s.v_pool, s.tables, s.seq_lens, 64, 0,
+                                      w.scale, status=s.status, k_scale=KS, v_scale=VS)
+    torch.cuda.synchronize()
+    assert int(s.status.item()) == pkv.DEV_Q_RANGE
