@@ -269,11 +269,16 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             const uint8_t *pool = static_cast<const uint8_t *>(is_k ? p.k_pool : p.v_pool);
             uint8_t *stg = smem + L::kStagingOff + (is_k ? 0 : 2) * kF8StageTile;
             uint64_t *stg_bar = staged + (is_k ? 0 : 2);
-            auto fetch = [&](int32_t jj) {  // whole warp; returns the mask of loaded blocks
+            // block ids of tile jj (lane < kBlocks), read one tile before use
+            auto in_range_of = [&](int32_t jj) {
                 const int32_t kb = (jt0 + jj) * kBlocks + lane;
-                const bool in_range = lane < kBlocks && kb < p.width && kb * 16 < w.kv_hi &&
-                                      (kb + 1) * 16 > w.kv_lo;
-                const int32_t id = in_range ? __ldg(trow + kb) : -1;
+                return lane < kBlocks && kb < p.width && kb * 16 < w.kv_hi && (kb + 1) * 16 > w.kv_lo;
+            };
+            auto load_id = [&](int32_t jj) {
+                return in_range_of(jj) ? __ldg(trow + (jt0 + jj) * kBlocks + lane) : -1;
+            };
+            auto fetch = [&](int32_t jj, int32_t id) {  // whole warp; returns the mask of loaded blocks
+                const bool in_range = in_range_of(jj);
                 const bool good = in_range && static_cast<uint32_t>(id) < static_cast<uint32_t>(p.num_blocks);
                 if (is_k && in_range && !good) report(p.status, PKV_DEV_BAD_BLOCK);
                 const uint32_t mask = __ballot_sync(0xffffffffu, good) & ((1u << kBlocks) - 1u);
@@ -297,8 +302,9 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
                 return mask;
             };
             uint32_t smask[2] = {0u, 0u};
-            smask[0] = fetch(0);
-            if (ntile > 1) smask[1] = fetch(1);
+            smask[0] = fetch(0, load_id(0));
+            if (ntile > 1) smask[1] = fetch(1, load_id(1));
+            int32_t id_ahead = ntile > 2 ? load_id(2) : -1;
             for (int32_t jj = 0; jj < ntile; ++jj) {
                 const int st = jj % kStages, sb = jj & 1;
                 if (jj >= kStages && !warp_wait(&empty[st], ((jj / kStages) + 1) & 1, lane, p.status)) break;
@@ -373,7 +379,10 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&full[st]);
-                if (jj + 2 < ntile) smask[sb] = fetch(jj + 2);
+                if (jj + 2 < ntile) {
+                    smask[sb] = fetch(jj + 2, id_ahead);
+                    id_ahead = jj + 3 < ntile ? load_id(jj + 3) : -1;
+                }
             }
         } else {
             const CUtensorMap *map = is_k ? &kmap : &vmap;
