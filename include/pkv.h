@@ -266,13 +266,14 @@ size_t paged_prefill_workspace_size(int32_t batch, int32_t num_q_heads, int32_t 
  *   max_q_len:   host upper bound on C_r;  max_seq_len: host bound on seq_lens
  *   workspace:   device, >= paged_prefill_workspace_size(...) bytes, 256-byte
  *                aligned (NULL when that size is 0)
- * Built: bf16, block_size 16, head_dim 128, Hq / Hkv <= 16 (tcgen05 tensor
+ * Built: bf16 and FP8, block_size 16, head_dim 128, Hq / Hkv <= 16 (tcgen05 tensor
  * cores, fp32 accumulation in tensor memory; probabilities enter the P.V
  * product as bf16 hi + lo terms); f32 pools run a CUDA-core kernel.  bf16
  * chunks with max_q_len * (Hq / Hkv) <= 16 (a speculative-verify step) run on
  * the split-KV decode kernel instead, one M-row per (query, head) pair, for
- * head_dim 64, 128 or 256; FP8 pools are built for such chunks only (longer
- * ones return PKV_ERR_UNSUPPORTED).
+ * head_dim 64, 128 or 256.  FP8 pools: the tensor-core kernel widens the E4M3
+ * tiles to f16 in shared memory and multiplies f16 x f16 (the query converted
+ * to f16, PKV_DEV_Q_RANGE past 65504), P as f16 hi + lo terms.
  */
 pkv_status paged_prefill_chunk_attention(const void *q, const int32_t *cu_q_lens,
                                          int32_t num_q_heads, const pkv_pool *pool,
