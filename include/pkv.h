@@ -243,8 +243,8 @@ pkv_status paged_decode_attention_no_alloc(const void *q, int32_t num_q_heads,
                                            int32_t *dev_status, pkv_stream_t stream);
 
 /* Bytes of device workspace paged_prefill_chunk_attention needs on the
- * current device: 0, except for short bf16 chunks (every C_r <= 128 / (Hq /
- * Hkv), a speculative-verify step, say) on grids too small to fill the GPU,
+ * current device: 0, except for short bf16 or FP8 chunks (every C_r <= 128 /
+ * (Hq / Hkv), a speculative-verify step, say) on grids too small to fill the GPU,
  * whose key ranges are then cut into runs whose fp32 partials a second kernel
  * merges.  The cut depends only on the sizes and the SM count. */
 size_t paged_prefill_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
