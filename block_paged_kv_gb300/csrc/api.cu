@@ -142,9 +142,8 @@ DecodePlan make_plan(int32_t batch, int32_t hq, int32_t hkv, int32_t D, int32_t 
                                 std::max(num_sms, 1));
         Cp = std::min<int64_t>(std::max<int64_t>(Cp, 4), 64);
         int64_t chunks = ceil_div64(rows_pairs, kF32Rows);
-        if (dtype == PKV_BF16) chunks = chunks_bf16;
-        if (dtype == PKV_FP8_E4M3)
-            chunks = ceil_div64(rows_pairs, static_cast<int64_t>(kDecodeWarps) * 8 * fp8_query_ntiles(G));
+        if (dtype != PKV_F32)
+            chunks = ceil_div64(rows_pairs, static_cast<int64_t>(kDecodeWarps) * 8 * query_ntiles(G));
         pl.prefix_split_blocks = static_cast<int32_t>(Cp);
         pl.n_prefix_splits = static_cast<int32_t>(ceil_div64(prefix->max_prefix_blocks, Cp));
         pl.prefix_chunks = static_cast<int32_t>(chunks);

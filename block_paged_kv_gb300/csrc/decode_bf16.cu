@@ -10,23 +10,29 @@ cudaError_t launch_decode_bf16(const DecodeParams &p, const CUtensorMap &kmap,
                                const CUtensorMap &vmap, cudaStream_t stream)
 {
     const bool mq = p.cu_q_lens != nullptr;  // several queries per row
+    // query n-tiles: the rows of a split item (G, or G x max_q for a verify step)
+    const bool two = query_ntiles(static_cast<int64_t>(p.group) * (mq ? p.max_q : 1)) == 2;
+#define PKV_BF16_LAUNCH(DIM)                                                             \
+    return mq ? (two ? launch_split<DIM, true, false, 2>(p, kmap, vmap, stream)           \
+                     : launch_split<DIM, true, false, 1>(p, kmap, vmap, stream))          \
+              : (two ? launch_split<DIM, false, false, 2>(p, kmap, vmap, stream)          \
+                     : launch_split<DIM, false, false, 1>(p, kmap, vmap, stream))
     switch (p.head_dim) {
-    case 64: return mq ? launch_split<64, true, false>(p, kmap, vmap, stream)
-                       : launch_split<64, false, false>(p, kmap, vmap, stream);
-    case 128: return mq ? launch_split<128, true, false>(p, kmap, vmap, stream)
-                        : launch_split<128, false, false>(p, kmap, vmap, stream);
-    case 256: return mq ? launch_split<256, true, false>(p, kmap, vmap, stream)
-                        : launch_split<256, false, false>(p, kmap, vmap, stream);
+    case 64: PKV_BF16_LAUNCH(64);
+    case 128: PKV_BF16_LAUNCH(128);
+    case 256: PKV_BF16_LAUNCH(256);
     default: return cudaErrorInvalidValue;
     }
+#undef PKV_BF16_LAUNCH
 }
 
 cudaError_t launch_decode_bf16_grouped(const GroupedDecode &gd, cudaStream_t stream)
 {
+    const bool two = query_ntiles(gd.g[0].group) == 2;
     switch (gd.g[0].head_dim) {
-    case 64: return launch_split_grouped<64, false>(gd, stream);
-    case 128: return launch_split_grouped<128, false>(gd, stream);
-    case 256: return launch_split_grouped<256, false>(gd, stream);
+    case 64: return two ? launch_split_grouped<64, false, 2>(gd, stream) : launch_split_grouped<64, false, 1>(gd, stream);
+    case 128: return two ? launch_split_grouped<128, false, 2>(gd, stream) : launch_split_grouped<128, false, 1>(gd, stream);
+    case 256: return two ? launch_split_grouped<256, false, 2>(gd, stream) : launch_split_grouped<256, false, 1>(gd, stream);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -11,7 +11,7 @@ cudaError_t launch_decode_fp8(const DecodeParams &p, cudaStream_t stream)
     const CUtensorMap none{};  // unused by the FP8 instantiations
     const bool mq = p.cu_q_lens != nullptr;
     // query n-tiles: the rows of a split item (G, or G x max_q for a verify step)
-    const bool two = fp8_query_ntiles(static_cast<int64_t>(p.group) * (mq ? p.max_q : 1)) == 2;
+    const bool two = query_ntiles(static_cast<int64_t>(p.group) * (mq ? p.max_q : 1)) == 2;
 #define PKV_FP8_LAUNCH(DIM)                                                               \
     return mq ? (two ? launch_split<DIM, true, true, 2>(p, none, none, stream)             \
                      : launch_split<DIM, true, true, 1>(p, none, none, stream))            \
@@ -28,7 +28,7 @@ cudaError_t launch_decode_fp8(const DecodeParams &p, cudaStream_t stream)
 
 cudaError_t launch_decode_fp8_grouped(const GroupedDecode &gd, cudaStream_t stream)
 {
-    const bool two = fp8_query_ntiles(gd.g[0].group) == 2;
+    const bool two = query_ntiles(gd.g[0].group) == 2;
     switch (gd.g[0].head_dim) {
     case 64: return two ? launch_split_grouped<64, true, 2>(gd, stream) : launch_split_grouped<64, true, 1>(gd, stream);
     case 128: return two ? launch_split_grouped<128, true, 2>(gd, stream) : launch_split_grouped<128, true, 1>(gd, stream);

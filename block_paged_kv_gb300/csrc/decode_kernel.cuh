@@ -9,7 +9,8 @@
 //       (row, head) pairs of the group's rows, so every shared block is read
 //       once for all of them;
 //   split item: row r, kv head g, split s -> blocks b_first + s*C .. ; its one
-//       16-row query tile holds the G q heads of (r, g).
+//       query tile holds the G q heads of (r, g) (a verify step: the G heads
+//       of each of the row's few queries).
 // K and V (block, kv head) tiles are brought into shared memory with one TMA
 // tensor load each (5-D maps viewing [block][kv head][slot][dim] as
 // (64 dims, slot, 64-dim region, kv head, block), 128-byte swizzle, so a tile
@@ -19,13 +20,19 @@
 //       itself as it frees a stage, so no warp ever waits behind another;
 //   prefix item: the four warps share one ring (each owns a query tile and
 //       reads every block); warp 0 refills a stage once all four released it.
-// Warps compute S = Q K^T and O += P V with mma.sync m16n8k16 (fp32
-// accumulate): M = 16 query rows, N = 8 tokens or 8 dims.  The online softmax
-// runs on the accumulator fragments with quad shuffles.  Each tile's partial
-// (max in log2 units, sum, unnormalised O) goes to the workspace.
-//   bf16 pools: bf16 operands; P enters the P.V product as two bf16 terms
-//       (hi + lo) so that its rounding stays far below the output's own bf16
-//       rounding.
+// Warps compute the transposed products S^T = K Q^T and O^T = V^T P^T with
+// mma.sync m16n8k16 (fp32 accumulate), so that a block's 16 tokens (S^T) and
+// 16-dim slices of the head (O^T) fill the 16-row M side and the query rows
+// (the G q heads of a GQA group, G <= 8 in one n-tile of 8, or two n-tiles)
+// sit on N: a decode step of G <= 8 heads wastes no M rows, and the query's
+// fragments are small enough to stay in registers.  The online softmax runs
+// on the accumulator fragments, a column per query row, with shuffles across
+// the 8 lanes that share it.  Each tile's partial (max in log2 units, sum,
+// unnormalised O) goes to the workspace.
+//   bf16 pools: K rows and V^T columns come out of the swizzled tiles with
+//       ldmatrix (plain for K, transposing for V); P enters the P.V product
+//       as two bf16 terms (hi + lo) so that its rounding stays far below the
+//       output's own bf16 rounding.
 //   FP8 pools ("perf.md", quantisation scheme table: FP8 KV cache with
 //       per-layer scales): a (block, kv head) tile is one contiguous run of
 //       16 * D bytes, brought in with one bulk copy; its bytes are already in
@@ -39,7 +46,7 @@
 
 namespace pkv {
 
-template <int D, bool kF8>
+template <int D, bool kF8, int NQ>
 struct KvCfg {
     static constexpr int kTok = 16;                       // block_size
     static constexpr int kElem = kF8 ? 1 : 2;             // bytes per K/V element
@@ -50,52 +57,54 @@ struct KvCfg {
     // per 32 tokens
     static constexpr int kBps = (kF8 && D <= 128) ? 2 : 1;
     static constexpr int kStageBytes = kBps * 2 * kTileBytes;  // K + V of each block
-    // query fragments stay in registers for head_dim <= 128; there the query
-    // tiles are staged through the ring before the first load, otherwise they
-    // keep a region of their own
-    static constexpr bool kQInRegs = D <= 128;
+    static constexpr int kTR = 8 * NQ;                    // query rows of a warp tile (N side)
+    // the query's B fragments stay in registers (D/16 k-steps x NQ n-tiles x
+    // 2 words) unless that is 64 words or more; in registers, the query tiles
+    // are staged through the ring before the first load, otherwise they keep
+    // a region of their own
+    static constexpr bool kQInRegs = D * NQ <= 256;
     static constexpr int kTiles = 4;                      // query tiles of a prefix item
-    // ring sized so that kCtasPerSm CTAs fit on an SM: three at head_dim <=
-    // 128 (a CTA's start - lengths, tables, query, first loads - then
-    // overlaps two others' streaming; measured 6 % faster than two CTAs with
-    // a 96 KB ring), two at 256 (its query tiles need their own region)
+    // ring sized so that kCtasPerSm CTAs fit on an SM: three when the query
+    // lives in registers (a CTA's start - lengths, tables, query, first loads
+    // - then overlaps two others' streaming; measured 6 % faster than two
+    // CTAs with a 96 KB ring at head_dim 128), otherwise two (the query tiles
+    // need their own region)
     static constexpr int kRingBytes = 64 * 1024;
-    static constexpr int kCtasPerSm = D <= 128 ? 3 : 2;
+    static constexpr int kCtasPerSm = kQInRegs ? 3 : 2;
     static constexpr int kStages = kRingBytes / kStageBytes;
     static constexpr int kStagesPerWarp = kStages / kDecodeWarps;  // split items
     static_assert(kStages % kDecodeWarps == 0, "split items give each warp the same stages");
     static constexpr int kRegions = D / 64;               // 64-dim swizzled regions per tile
     static constexpr int kRegionBytes = kTok * 128;
     static constexpr int kQStride = (D + 8) * 2;          // padded query row (bytes)
-    static constexpr int kQTileBytes = 16 * kQStride;
-    static constexpr int kNT = D / 8;                     // 8-dim output n-tiles
-    static constexpr int kKS = D / 16;                    // 16-dim k-steps of Q K^T
+    static constexpr int kQTileBytes = kTR * kQStride;
+    static constexpr int kMT = D / 16;                    // 16-dim m-tiles of O^T
+    static constexpr int kKS = D / 16;                    // 16-dim k-steps of K Q^T
 };
 
-template <int D, bool kF8>
+template <int D, bool kF8, int NQ>
 struct KvSmem {
-    using C = KvCfg<D, kF8>;
+    using C = KvCfg<D, kF8, NQ>;
     static constexpr int kStageOff = 0;
     static constexpr int kQOff = C::kQInRegs ? 0 : C::kRingBytes;
     static constexpr int kBarOff =
         C::kQInRegs ? C::kRingBytes : C::kRingBytes + C::kTiles * C::kQTileBytes;
     static constexpr int kOkOff = kBarOff + 2 * C::kStages * 8;
     static constexpr int kPairOff = kOkOff + C::kStages * C::kBps * 4;
-    static constexpr int kMiscOff = kPairOff + 3 * C::kTiles * 16 * 4;
+    static constexpr int kMiscOff = kPairOff + 3 * C::kTiles * C::kTR * 4;
     static constexpr int kBytes = kMiscOff + 16;
     static constexpr int kLaunchBytes = kBytes + 1024;  // room to align the base to 1024
     static_assert(C::kTiles * C::kQTileBytes <= C::kRingBytes || !C::kQInRegs,
                   "query tiles staged through the ring fit in it");
-    static_assert(kDecodeWarps * 16 * D * 4 + kDecodeWarps * 16 * 8 <= kBarOff,
+    static_assert(kDecodeWarps * C::kTR * D * 4 + kDecodeWarps * C::kTR * 8 <= kBarOff,
                   "the merge buffers fit below the barriers");
 };
 
 // Swizzled shared address of the 16-byte chunk holding dims d0..d0+7 of token
 // `tok` in a K/V tile (TMA SWIZZLE_128B: chunk index XOR (line % 8)).
-template <int D>
 __device__ __forceinline__ uint32_t kv_chunk_addr(uint32_t tile, int tok, int d0)
 {
-    return tile + (d0 >> 6) * KvCfg<D, false>::kRegionBytes + tok * 128 +
+    return tile + (d0 >> 6) * (16 * 128) + tok * 128 +
            ((((d0 & 63) >> 3) ^ (tok & 7)) << 4);
 }
 
@@ -139,15 +148,12 @@ template <int D, bool kMQ, bool kF8, int NQ>
 __device__ __forceinline__ void decode_split_body(const CUtensorMap &kmap, const CUtensorMap &vmap,
                                                   const DecodeParams &p, const int64_t cta)
 {
-    using C = KvCfg<D, kF8>;
-    using SM = KvSmem<D, kF8>;
+    using C = KvCfg<D, kF8, NQ>;
+    using SM = KvSmem<D, kF8, NQ>;
     constexpr int NW = kDecodeWarps;
     constexpr int STAGES = C::kStages;
     constexpr int SPW = C::kStagesPerWarp;
-    // query rows per warp tile of a prefix item: 16 (bf16: the M side of the
-    // products), 8 * NQ (FP8: the N side, NQ n-tiles of 8)
-    constexpr int TR = kF8 ? 8 * NQ : 16;
-    static_assert(kF8 || NQ == 1, "bf16 tiles are 16 query rows on M");
+    constexpr int TR = C::kTR;  // query rows per warp tile: the N side, NQ n-tiles of 8
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -158,8 +164,8 @@ __device__ __forceinline__ void decode_split_body(const CUtensorMap &kmap, const
     uint64_t *empty = full + STAGES;
     int32_t *stage_ok = reinterpret_cast<int32_t *>(smem + SM::kOkOff);
     int32_t *pair_row = reinterpret_cast<int32_t *>(smem + SM::kPairOff);
-    int32_t *pair_head = pair_row + C::kTiles * 16;  // capacity for TR <= 16
-    int32_t *pair_len = pair_head + C::kTiles * 16;
+    int32_t *pair_head = pair_row + C::kTiles * TR;
+    int32_t *pair_len = pair_head + C::kTiles * TR;
     int32_t *misc = reinterpret_cast<int32_t *>(smem + SM::kMiscOff);
 
     const int warp = threadIdx.x >> 5;
@@ -179,8 +185,9 @@ __device__ __forceinline__ void decode_split_body(const CUtensorMap &kmap, const
     int32_t b0, nblk, slot, tab_row, g, lo_all, hi_all, tiles;
     // split item only: the row, its query count and first packed query
     int32_t row_r = 0, row_C = 1, row_q0 = 0;
-    // M-rows of a split item: the G heads of one query (decode), or (query,
-    // head) pairs of a row's few queries (kMQ: a verify step)
+    // query rows of a split item: the G heads of one query (decode), or
+    // (query, head) pairs of a row's few queries (kMQ: a verify step); the
+    // launch takes NQ so that R <= TR
     const int R = kMQ ? G * p.max_q : G;
     if (!prefix_item) {
         int64_t bid = cta - p.plan.n_prefix_ctas;
@@ -274,7 +281,7 @@ __device__ __forceinline__ void decode_split_body(const CUtensorMap &kmap, const
     // ------------------------------------------------- query tiles + barriers
     {
         constexpr int kVec = D / 8;  // 16-byte vectors per row
-        const int qrows = prefix_item ? tiles * TR : 16;
+        const int qrows = prefix_item ? tiles * TR : TR;
         for (int i = threadIdx.x; i < qrows * kVec; i += blockDim.x) {
             const int row = i / kVec, v = i % kVec;
             int32_t qr = -1, qh = 0;
@@ -326,30 +333,20 @@ __device__ __forceinline__ void decode_split_body(const CUtensorMap &kmap, const
     // a split item's warps all read query tile 0; a prefix item's warp w owns
     // tile w
     const int tile = prefix_item ? warp : 0;
-    const uint32_t q_lane = smem_u32(q_mem + tile * C::kQTileBytes) +
-                            (((lane >> 3) & 1) * 8 + (lane & 7)) * C::kQStride + (lane >> 4) * 16;
-    // bf16: A fragments of Q (query rows on M).  FP8: B fragments of Q^T
-    // (query rows on N, NQ n-tiles of 8): b0 = Q[row 8n + lane/4][16kk + 2(lane%4), +1],
-    // b1 = the same 8 dims further
+    // B fragments of Q^T (query rows on N, NQ n-tiles of 8):
+    // b0 = Q[row 8n + lane/4][16kk + 2(lane%4), +1], b1 = the same 8 dims further
     const uint32_t qb_lane = smem_u32(q_mem + tile * C::kQTileBytes) + (lane >> 2) * C::kQStride +
                              (lane & 3) * 4;
-    uint32_t qf[C::kQInRegs && !kF8 ? C::kKS : 1][4];
-    uint32_t qb[C::kQInRegs && kF8 ? C::kKS : 1][NQ][2];
+    uint32_t qb[C::kQInRegs ? C::kKS : 1][NQ][2];
     if constexpr (C::kQInRegs) {
-        if constexpr (kF8) {
 #pragma unroll
-            for (int kk = 0; kk < C::kKS; ++kk)
+        for (int kk = 0; kk < C::kKS; ++kk)
 #pragma unroll
-                for (int n = 0; n < NQ; ++n) {
-                    const uint32_t a = qb_lane + n * 8 * C::kQStride + kk * 32;
-                    qb[kk][n][0] = lds32(a);
-                    qb[kk][n][1] = lds32(a + 16);
-                }
-        } else {
-#pragma unroll
-            for (int kk = 0; kk < C::kKS; ++kk)
-                ldsm_x4(q_lane + kk * 32, qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3]);
-        }
+            for (int n = 0; n < NQ; ++n) {
+                const uint32_t a = qb_lane + n * 8 * C::kQStride + kk * 32;
+                qb[kk][n][0] = lds32(a);
+                qb[kk][n][1] = lds32(a + 16);
+            }
         // the ring is about to be overwritten by TMA (async proxy) after these
         // generic-proxy reads and writes of the staged query tiles
         fence_proxy_async_smem();
@@ -420,73 +417,84 @@ __device__ __forceinline__ void decode_split_body(const CUtensorMap &kmap, const
     // split item: the four warps' partials of the one tile meet in the ring
     // (free once every warp is past its last block)
     float *mbuf = reinterpret_cast<float *>(stage_mem);  // [NW][R][D]
-    float *mlbuf = mbuf + NW * 16 * D;                    // [NW][R][2], R <= 16
-    if constexpr (kF8) {
-        // FP8: transposed products, so that tokens (S^T = K Q^T) and dims
-        // (O^T = V^T P^T) fill the 16-row M side of m16n8k16 and the query
-        // rows sit on N (NQ n-tiles of 8).  The tile bytes are already in A
-        // fragment order for both K and V^T.
-        const int g8 = lane >> 2;  // A rows g8, g8 + 8; B / C column g8 (B), 2cc (C)
-        const int cc = lane & 3;
-        // key range of this lane's C columns: query rows 8n + 2cc + e
-        int clo[NQ][2], chi[NQ][2];
+    float *mlbuf = mbuf + NW * TR * D;                    // [NW][R][2], R <= TR
+    const int g8 = lane >> 2;  // A rows g8, g8 + 8; B / C column g8 (B), 2cc (C)
+    const int cc = lane & 3;
+    // bf16 ldmatrix rows of this lane (matrix lane/8, row lane%8): K as the A
+    // operand of S^T (tokens 0-7 / 8-15 at dims +0 / +8: plain), V as that of
+    // O^T (the same, transposed on the way: dims +0 / +8 at tokens 0-7 / 8-15)
+    const int ka_tok = ((lane >> 3) & 1) * 8 + (lane & 7), ka_dof = (lane >> 4) * 8;
+    const int va_tok = (lane >> 4) * 8 + (lane & 7), va_dof = ((lane >> 3) & 1) * 8;
+    // key range of this lane's C columns: query rows 8n + 2cc + e
+    int clo[NQ][2], chi[NQ][2];
 #pragma unroll
-        for (int n = 0; n < NQ; ++n)
+    for (int n = 0; n < NQ; ++n)
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int row = 8 * n + 2 * cc + e;
-                int lo = 0, hi = 0;
-                if (prefix_item) {
-                    const int kq = tile * TR + row;
-                    hi = pair_row[kq] >= 0 ? pair_len[kq] : 0;
-                } else if constexpr (kMQ) {
-                    const int t = row / G;
-                    hi = (row < R && t < row_C) ? hi_all - row_C + t + 1 : 0;
-                    lo = (p.window > 0 && hi > 0) ? max(0, hi - p.window) : 0;
-                } else if (row < R) {
-                    lo = lo_all;
-                    hi = hi_all;
-                }
-                clo[n][e] = lo;
-                chi[n][e] = hi;
+        for (int e = 0; e < 2; ++e) {
+            const int row = 8 * n + 2 * cc + e;
+            int lo = 0, hi = 0;
+            if (prefix_item) {
+                const int kq = tile * TR + row;
+                hi = pair_row[kq] >= 0 ? pair_len[kq] : 0;
+            } else if constexpr (kMQ) {
+                const int t = row / G;
+                hi = (row < R && t < row_C) ? hi_all - row_C + t + 1 : 0;
+                lo = (p.window > 0 && hi > 0) ? max(0, hi - p.window) : 0;
+            } else if (row < R) {
+                lo = lo_all;
+                hi = hi_all;
             }
-        float oT[C::kNT / 2][NQ][4];  // [16-dim m-tile][n-tile][C fragment]
+            clo[n][e] = lo;
+            chi[n][e] = hi;
+        }
+    float oT[C::kMT][NQ][4];  // [16-dim m-tile][n-tile][C fragment]
 #pragma unroll
-        for (int mt = 0; mt < C::kNT / 2; ++mt)
+    for (int mt = 0; mt < C::kMT; ++mt)
 #pragma unroll
-            for (int n = 0; n < NQ; ++n) oT[mt][n][0] = oT[mt][n][1] = oT[mt][n][2] = oT[mt][n][3] = 0.f;
-        float mc[NQ][2], lc[NQ][2];
+        for (int n = 0; n < NQ; ++n) oT[mt][n][0] = oT[mt][n][1] = oT[mt][n][2] = oT[mt][n][3] = 0.f;
+    float mc[NQ][2], lc[NQ][2];
 #pragma unroll
-        for (int n = 0; n < NQ; ++n) {
-            mc[n][0] = mc[n][1] = -INFINITY;
-            lc[n][0] = lc[n][1] = 0.f;
+    for (int n = 0; n < NQ; ++n) {
+        mc[n][0] = mc[n][1] = -INFINITY;
+        lc[n][0] = lc[n][1] = 0.f;
+    }
+
+    for (int32_t k = 0; k < nk; ++k) {
+        const int st = stage_of(k);
+        const int32_t use = prefix_item ? k / STAGES : k / SPW;
+        const bool got = mbar_wait(&full[st], use & 1);
+        if (__any_sync(0xffffffffu, !got)) {
+            if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
+            break;
+        }
+        const uint32_t stile = smem_u32(stage_mem + st * C::kStageBytes);
+        bool okb[BPS];
+        int base_tok[BPS];
+#pragma unroll
+        for (int i = 0; i < BPS; ++i) {
+            okb[i] = stage_ok[st * BPS + i] != 0;
+            const int32_t j = k * BPS + i;
+            base_tok[i] = (b0 + (prefix_item ? j : warp + NW * j)) * bs;
         }
 
-        for (int32_t k = 0; k < nk; ++k) {
-            const int st = stage_of(k);
-            const int32_t use = prefix_item ? k / STAGES : k / SPW;
-            const bool got = mbar_wait(&full[st], use & 1);
-            if (__any_sync(0xffffffffu, !got)) {
-                if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
-                break;
-            }
-            const uint32_t stile = smem_u32(stage_mem + st * C::kStageBytes);
-            bool okb[BPS];
-            int base_tok[BPS];
+        // S^T = K Q^T: rows = the block's tokens g8 (first half) and
+        // g8 + 8 (second half); even and odd 16-dim steps in two chains
+        float sT[BPS][NQ][4];
 #pragma unroll
-            for (int i = 0; i < BPS; ++i) {
-                okb[i] = stage_ok[st * BPS + i] != 0;
-                const int32_t j = k * BPS + i;
-                base_tok[i] = (b0 + (prefix_item ? j : warp + NW * j)) * bs;
-            }
-
-            // S^T = K Q^T: rows = the block's tokens g8 (first half) and
-            // g8 + 8 (second half); even and odd 16-dim steps in two chains
-            float sT[BPS][NQ][4];
-#pragma unroll
-            for (int i = 0; i < BPS; ++i) {
-                const uint32_t kt = stile + i * 2 * C::kTileBytes;
-                float sa[2][NQ][4] = {};
+        for (int i = 0; i < BPS; ++i) {
+            const uint32_t kt = stile + i * 2 * C::kTileBytes;
+            float sa[2][NQ][4] = {};
+            auto q_frag = [&](int kk, int n, uint32_t &b0, uint32_t &b1) {
+                if constexpr (C::kQInRegs) {
+                    b0 = qb[kk][n][0];
+                    b1 = qb[kk][n][1];
+                } else {
+                    const uint32_t qa = qb_lane + n * 8 * C::kQStride + kk * 32;
+                    b0 = lds32(qa);
+                    b1 = lds32(qa + 16);
+                }
+            };
+            if constexpr (kF8) {
 #pragma unroll
                 for (int grp = 0; grp < D / 64; ++grp) {
                     const uint4 h0 = lds128(kt + grp * 1024 + lane * 16);
@@ -502,129 +510,151 @@ __device__ __forceinline__ void decode_split_body(const CUtensorMap &kmap, const
 #pragma unroll
                         for (int n = 0; n < NQ; ++n) {
                             uint32_t b0, b1;
-                            if constexpr (C::kQInRegs) {
-                                b0 = qb[kk][n][0];
-                                b1 = qb[kk][n][1];
-                            } else {
-                                const uint32_t qa = qb_lane + n * 8 * C::kQStride + kk * 32;
-                                b0 = lds32(qa);
-                                b1 = lds32(qa + 16);
-                            }
+                            q_frag(kk, n, b0, b1);
                             mma_16816_f16(sa[s4 & 1][n], a, b0, b1);
                         }
                     }
                 }
-#pragma unroll
-                for (int n = 0; n < NQ; ++n)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) sT[i][n][e] = sa[0][n][e] + sa[1][n][e];
-            }
-
-            // mask, scale to log2 units; element e of C is (token g8 + 8(e/2),
-            // column 2cc + e%2)
-            float sv[BPS][NQ][4];
-            bool inside = true;
-#pragma unroll
-            for (int i = 0; i < BPS; ++i) {
-                bool in = okb[i];
-#pragma unroll
-                for (int n = 0; n < NQ; ++n)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e)
-                        in = in && (chi[n][e] == 0 ||
-                                    (base_tok[i] >= clo[n][e] && base_tok[i] + bs <= chi[n][e]));
-                inside = inside && in;
-            }
-            if (__all_sync(0xffffffffu, inside)) {
-#pragma unroll
-                for (int i = 0; i < BPS; ++i)
-#pragma unroll
-                    for (int n = 0; n < NQ; ++n)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) sv[i][n][e] = sT[i][n][e] * p.scale_log2;
             } else {
 #pragma unroll
-                for (int i = 0; i < BPS; ++i)
-#pragma unroll
-                    for (int n = 0; n < NQ; ++n)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int pos = base_tok[i] + g8 + 8 * (e >> 1);
-                            const int lo = clo[n][e & 1], hi = chi[n][e & 1];
-                            sv[i][n][e] = (okb[i] && pos >= lo && pos < hi)
-                                              ? sT[i][n][e] * p.scale_log2
-                                              : -INFINITY;
-                        }
-            }
-            // column maxima: this lane's tokens, then the 8 lanes sharing cc
-            float mu[NQ][2], al[NQ][2];
-            bool grew = false;
-#pragma unroll
-            for (int n = 0; n < NQ; ++n)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    float mx = -INFINITY;
-#pragma unroll
-                    for (int i = 0; i < BPS; ++i) mx = fmaxf(mx, fmaxf(sv[i][n][e], sv[i][n][e + 2]));
-                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-                    const float mn = fmaxf(mc[n][e], mx);
-                    mu[n][e] = mn == -INFINITY ? 0.f : mn;
-                    al[n][e] = fast_exp2(mc[n][e] - mu[n][e]);
-                    grew = grew || mn != mc[n][e];
-                    mc[n][e] = mn;
-                }
-            grew = __any_sync(0xffffffffu, grew);
-            float pv[BPS][NQ][4];
-#pragma unroll
-            for (int n = 0; n < NQ; ++n)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    float sum = 0.f;
-#pragma unroll
-                    for (int i = 0; i < BPS; ++i) {
-                        pv[i][n][e] = fast_exp2(sv[i][n][e] - mu[n][e]);
-                        pv[i][n][e + 2] = fast_exp2(sv[i][n][e + 2] - mu[n][e]);
-                        sum += pv[i][n][e] + pv[i][n][e + 2];
-                    }
-                    lc[n][e] = lc[n][e] * al[n][e] + sum;
-                }
-            if (grew) {
-#pragma unroll
-                for (int mt = 0; mt < C::kNT / 2; ++mt)
+                for (int kk = 0; kk < C::kKS; ++kk) {
+                    uint32_t a[4];
+                    ldsm_x4(kv_chunk_addr(kt, ka_tok, kk * 16 + ka_dof), a[0], a[1], a[2], a[3]);
 #pragma unroll
                     for (int n = 0; n < NQ; ++n) {
-                        oT[mt][n][0] *= al[n][0];
-                        oT[mt][n][1] *= al[n][1];
-                        oT[mt][n][2] *= al[n][0];
-                        oT[mt][n][3] *= al[n][1];
+                        uint32_t b0, b1;
+                        q_frag(kk, n, b0, b1);
+                        mma_16816(sa[kk & 1][n], a, b0, b1);
                     }
+                }
             }
-
-            // O^T += V^T P^T per block.  P as f16 pairs (token g8: columns
-            // 2cc, 2cc+1) is row g8 of an 8x8 (tokens x columns) matrix;
-            // movmatrix.trans hands each lane the (column g8: tokens 2cc,
-            // 2cc+1) pair of the B fragment (one f16 term: 2^-11 relative).
-            // Values of tokens outside every row's range are zeroed: stale
-            // slots may hold anything, including NaN.
 #pragma unroll
-            for (int i = 0; i < BPS; ++i) {
-                if (!okb[i]) continue;
-                const uint32_t vt = stile + i * 2 * C::kTileBytes + C::kTileBytes;
-                uint32_t pb[NQ][2];
+            for (int n = 0; n < NQ; ++n)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sT[i][n][e] = sa[0][n][e] + sa[1][n][e];
+        }
+
+        // mask, scale to log2 units; element e of C is (token g8 + 8(e/2),
+        // column 2cc + e%2)
+        float sv[BPS][NQ][4];
+        bool inside = true;
+#pragma unroll
+        for (int i = 0; i < BPS; ++i) {
+            bool in = okb[i];
+#pragma unroll
+            for (int n = 0; n < NQ; ++n)
+#pragma unroll
+                for (int e = 0; e < 2; ++e)
+                    in = in && (chi[n][e] == 0 ||
+                                (base_tok[i] >= clo[n][e] && base_tok[i] + bs <= chi[n][e]));
+            inside = inside && in;
+        }
+        if (__all_sync(0xffffffffu, inside)) {
+#pragma unroll
+            for (int i = 0; i < BPS; ++i)
+#pragma unroll
+                for (int n = 0; n < NQ; ++n)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) sv[i][n][e] = sT[i][n][e] * p.scale_log2;
+        } else {
+#pragma unroll
+            for (int i = 0; i < BPS; ++i)
+#pragma unroll
+                for (int n = 0; n < NQ; ++n)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int pos = base_tok[i] + g8 + 8 * (e >> 1);
+                        const int lo = clo[n][e & 1], hi = chi[n][e & 1];
+                        sv[i][n][e] = (okb[i] && pos >= lo && pos < hi)
+                                          ? sT[i][n][e] * p.scale_log2
+                                          : -INFINITY;
+                    }
+        }
+        // column maxima: this lane's tokens, then the 8 lanes sharing cc
+        float mu[NQ][2], al[NQ][2];
+        bool grew = false;
+#pragma unroll
+        for (int n = 0; n < NQ; ++n)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                float mx = -INFINITY;
+#pragma unroll
+                for (int i = 0; i < BPS; ++i) mx = fmaxf(mx, fmaxf(sv[i][n][e], sv[i][n][e + 2]));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                const float mn = fmaxf(mc[n][e], mx);
+                mu[n][e] = mn == -INFINITY ? 0.f : mn;
+                al[n][e] = fast_exp2(mc[n][e] - mu[n][e]);
+                grew = grew || mn != mc[n][e];
+                mc[n][e] = mn;
+            }
+        grew = __any_sync(0xffffffffu, grew);
+        float pv[BPS][NQ][4];
+#pragma unroll
+        for (int n = 0; n < NQ; ++n)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                float sum = 0.f;
+#pragma unroll
+                for (int i = 0; i < BPS; ++i) {
+                    pv[i][n][e] = fast_exp2(sv[i][n][e] - mu[n][e]);
+                    pv[i][n][e + 2] = fast_exp2(sv[i][n][e + 2] - mu[n][e]);
+                    sum += pv[i][n][e] + pv[i][n][e + 2];
+                }
+                lc[n][e] = lc[n][e] * al[n][e] + sum;
+            }
+        if (grew) {
+#pragma unroll
+            for (int mt = 0; mt < C::kMT; ++mt)
 #pragma unroll
                 for (int n = 0; n < NQ; ++n) {
+                    oT[mt][n][0] *= al[n][0];
+                    oT[mt][n][1] *= al[n][1];
+                    oT[mt][n][2] *= al[n][0];
+                    oT[mt][n][3] *= al[n][1];
+                }
+        }
+
+        // O^T += V^T P^T per block.  P as 16-bit pairs (token g8: columns
+        // 2cc, 2cc+1) is row g8 of an 8x8 (tokens x columns) matrix;
+        // movmatrix.trans hands each lane the (column g8: tokens 2cc, 2cc+1)
+        // pair of the B fragment.  FP8: one f16 term (2^-11 relative).  bf16:
+        // a bf16 pair hi + lo (lo = bf16(P - hi)), two products, so that P is
+        // carried to about 2^-17 relative instead of the 2^-9 of one bf16
+        // rounding.  Values of tokens outside every row's range are zeroed:
+        // stale slots may hold anything, including NaN.
+#pragma unroll
+        for (int i = 0; i < BPS; ++i) {
+            if (!okb[i]) continue;
+            const uint32_t vt = stile + i * 2 * C::kTileBytes + C::kTileBytes;
+            uint32_t pb[NQ][2], pl[NQ][2];
+#pragma unroll
+            for (int n = 0; n < NQ; ++n) {
+                if constexpr (kF8) {
                     pb[n][0] = movmatrix_trans(pack_f16x2(pv[i][n][0], pv[i][n][1]));
                     pb[n][1] = movmatrix_trans(pack_f16x2(pv[i][n][2], pv[i][n][3]));
+                } else {
+                    const uint32_t h0 = pack_bf16x2(pv[i][n][0], pv[i][n][1]);
+                    const uint32_t h1 = pack_bf16x2(pv[i][n][2], pv[i][n][3]);
+                    const uint32_t l0 = pack_bf16x2(pv[i][n][0] - bf16lo_to_f32(h0),
+                                                    pv[i][n][1] - bf16hi_to_f32(h0));
+                    const uint32_t l1 = pack_bf16x2(pv[i][n][2] - bf16lo_to_f32(h1),
+                                                    pv[i][n][3] - bf16hi_to_f32(h1));
+                    pb[n][0] = movmatrix_trans(h0);
+                    pb[n][1] = movmatrix_trans(h1);
+                    pl[n][0] = movmatrix_trans(l0);
+                    pl[n][1] = movmatrix_trans(l1);
                 }
-                uint32_t mk0 = 0xffffffffu, mk1 = 0xffffffffu;
-                const int bt = base_tok[i];
-                if (bt < lo_all || bt + bs > hi_all) {
-                    auto live = [&](int t) { return bt + t >= lo_all && bt + t < hi_all; };
-                    mk0 = (live(2 * cc) ? 0x0000ffffu : 0u) | (live(2 * cc + 1) ? 0xffff0000u : 0u);
-                    mk1 = (live(2 * cc + 8) ? 0x0000ffffu : 0u) | (live(2 * cc + 9) ? 0xffff0000u : 0u);
-                }
+            }
+            uint32_t mk0 = 0xffffffffu, mk1 = 0xffffffffu;
+            const int bt = base_tok[i];
+            if (bt < lo_all || bt + bs > hi_all) {
+                auto live = [&](int t) { return bt + t >= lo_all && bt + t < hi_all; };
+                mk0 = (live(2 * cc) ? 0x0000ffffu : 0u) | (live(2 * cc + 1) ? 0xffff0000u : 0u);
+                mk1 = (live(2 * cc + 8) ? 0x0000ffffu : 0u) | (live(2 * cc + 9) ? 0xffff0000u : 0u);
+            }
+            if constexpr (kF8) {
 #pragma unroll
                 for (int grp = 0; grp < D / 32; ++grp) {
                     const uint4 vw = lds128(vt + grp * 512 + lane * 16);
@@ -645,341 +675,105 @@ __device__ __forceinline__ void decode_split_body(const CUtensorMap &kmap, const
                             mma_16816_f16(oT[2 * grp + half][n], a, pb[n][0], pb[n][1]);
                     }
                 }
-            }
-
-            // release the stage: its generic-proxy reads come before the next
-            // async-proxy write into it
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (!prefix_item) {
-                if (k + SPW < nk) issue(k + SPW);
             } else {
-                if (lane == 0) mbar_arrive(&empty[st]);
-                if (warp == 0 && k + STAGES < nk) {
-                    // every warp has released this stage before it is refilled
-                    bool freed = true;
-                    if (lane == 0) freed = mbar_wait(&empty[st], use & 1);
-                    if (!__shfl_sync(0xffffffffu, freed, 0)) {
-                        if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
-                    } else {
-                        issue(k + STAGES);
+#pragma unroll
+                for (int mt = 0; mt < C::kMT; ++mt) {
+                    // a[0] (dim 16mt + g8, tokens 2cc, +1), a[1] (dim + 8),
+                    // a[2], a[3]: the same for tokens 2cc + 8, +9
+                    uint32_t a[4];
+                    ldsm_x4_trans(kv_chunk_addr(vt, va_tok, mt * 16 + va_dof), a[0], a[1], a[2], a[3]);
+                    a[0] &= mk0;
+                    a[1] &= mk0;
+                    a[2] &= mk1;
+                    a[3] &= mk1;
+#pragma unroll
+                    for (int n = 0; n < NQ; ++n) {
+                        mma_16816(oT[mt][n], a, pb[n][0], pb[n][1]);
+                        mma_16816(oT[mt][n], a, pl[n][0], pl[n][1]);
                     }
                 }
             }
         }
 
-        // column sums over the 8 lanes sharing cc; the V scale on the values
-#pragma unroll
-        for (int n = 0; n < NQ; ++n)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                lc[n][e] += __shfl_xor_sync(0xffffffffu, lc[n][e], 4);
-                lc[n][e] += __shfl_xor_sync(0xffffffffu, lc[n][e], 8);
-                lc[n][e] += __shfl_xor_sync(0xffffffffu, lc[n][e], 16);
+        // release the stage: its generic-proxy reads come before the next
+        // async-proxy write into it
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (!prefix_item) {
+            if (k + SPW < nk) issue(k + SPW);
+        } else {
+            if (lane == 0) mbar_arrive(&empty[st]);
+            if (warp == 0 && k + STAGES < nk) {
+                // every warp has released this stage before it is refilled
+                bool freed = true;
+                if (lane == 0) freed = mbar_wait(&empty[st], use & 1);
+                if (!__shfl_sync(0xffffffffu, freed, 0)) {
+                    if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
+                } else {
+                    issue(k + STAGES);
+                }
             }
+        }
+    }
+
+    // column sums over the 8 lanes sharing cc; FP8: the V scale on the values
 #pragma unroll
-        for (int mt = 0; mt < C::kNT / 2; ++mt)
+    for (int n = 0; n < NQ; ++n)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            lc[n][e] += __shfl_xor_sync(0xffffffffu, lc[n][e], 4);
+            lc[n][e] += __shfl_xor_sync(0xffffffffu, lc[n][e], 8);
+            lc[n][e] += __shfl_xor_sync(0xffffffffu, lc[n][e], 16);
+        }
+    if constexpr (kF8) {
+#pragma unroll
+        for (int mt = 0; mt < C::kMT; ++mt)
 #pragma unroll
             for (int n = 0; n < NQ; ++n)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) oT[mt][n][e] *= p.v_scale;
+    }
 
-        // element e of oT[mt][n]: dim 16mt + g8 + 8(e/2), query row 8n + 2cc + e%2
-        if (prefix_item) {
-            // each warp owns its tile: write its rows directly
-#pragma unroll
-            for (int n = 0; n < NQ; ++n)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int kq = tile * TR + 8 * n + 2 * cc + e;
-                    const int32_t pr = pair_row[kq];
-                    if (pr < 0) continue;
-                    const size_t pi = partial_index(p, pr, pair_head[kq], slot);
-                    float *dst = p.ws_o + pi * D + g8;
-#pragma unroll
-                    for (int mt = 0; mt < C::kNT / 2; ++mt) {
-                        dst[16 * mt] = oT[mt][n][e];
-                        dst[16 * mt + 8] = oT[mt][n][e + 2];
-                    }
-                    if (g8 == 0)
-                        *reinterpret_cast<float2 *>(p.ws_ml + pi * 2) = make_float2(mc[n][e], lc[n][e]);
-                }
-            return;
-        }
-        // split item: this warp's rows of the one tile into the merge buffers
-        __syncthreads();
+    // element e of oT[mt][n]: dim 16mt + g8 + 8(e/2), query row 8n + 2cc + e%2
+    if (prefix_item) {
+        // each warp owns its tile: write its rows directly
 #pragma unroll
         for (int n = 0; n < NQ; ++n)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-                const int row = 8 * n + 2 * cc + e;
-                if (row >= R) continue;
-                float *dst = mbuf + (warp * R + row) * D + g8;
+                const int kq = tile * TR + 8 * n + 2 * cc + e;
+                const int32_t pr = pair_row[kq];
+                if (pr < 0) continue;
+                const size_t pi = partial_index(p, pr, pair_head[kq], slot);
+                float *dst = p.ws_o + pi * D + g8;
 #pragma unroll
-                for (int mt = 0; mt < C::kNT / 2; ++mt) {
+                for (int mt = 0; mt < C::kMT; ++mt) {
                     dst[16 * mt] = oT[mt][n][e];
                     dst[16 * mt + 8] = oT[mt][n][e + 2];
                 }
                 if (g8 == 0)
-                    *reinterpret_cast<float2 *>(mlbuf + (warp * R + row) * 2) =
-                        make_float2(mc[n][e], lc[n][e]);
+                    *reinterpret_cast<float2 *>(p.ws_ml + pi * 2) = make_float2(mc[n][e], lc[n][e]);
             }
-    } else {
-        const int qd = lane >> 2;        // fragment rows qd and qd + 8
-        const int c2 = 2 * (lane & 3);   // fragment columns c2, c2 + 1
-        int lo0, hi0, lo1, hi1;
-        if (!prefix_item) {
-            if constexpr (kMQ) {
-                // query t of the row sits at L - C + t: causal limit hi, window start lo
-                auto limits = [&](int row, int &lo, int &hi) {
-                    const int t = row / G;
-                    hi = (row < R && t < row_C) ? hi_all - row_C + t + 1 : 0;
-                    lo = (p.window > 0 && hi > 0) ? max(0, hi - p.window) : 0;
-                };
-                limits(qd, lo0, hi0);
-                limits(qd + 8, lo1, hi1);
-            } else {
-                lo0 = lo1 = lo_all;
-                hi0 = hi1 = hi_all;
-            }
-        } else {
-            lo0 = lo1 = 0;
-            const int k0 = tile * 16 + qd;
-            hi0 = pair_row[k0] >= 0 ? pair_len[k0] : 0;
-            hi1 = pair_row[k0 + 8] >= 0 ? pair_len[k0 + 8] : 0;
-        }
-
-        float o[C::kNT][4];
-    #pragma unroll
-        for (int nt = 0; nt < C::kNT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
-        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-
-        // lane-constant parts of the ldmatrix addresses
-        const int k_tok = (lane >> 4) * 8 + (lane & 7);
-        const int k_dof = ((lane >> 3) & 1) * 8;
-        const int v_tok = ((lane >> 3) & 1) * 8 + (lane & 7);
-        const int v_dof = (lane >> 4) * 8;
-
-        for (int32_t k = 0; k < nk; ++k) {
-            const int st = stage_of(k);
-            const int32_t use = prefix_item ? k / STAGES : k / SPW;
-            const bool got = mbar_wait(&full[st], use & 1);
-            if (__any_sync(0xffffffffu, !got)) {
-                if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
-                break;
-            }
-            const uint32_t stile = smem_u32(stage_mem + st * C::kStageBytes);
-            bool okb[BPS];
-            int base_tok[BPS];
-    #pragma unroll
-            for (int i = 0; i < BPS; ++i) {
-                okb[i] = stage_ok[st * BPS + i] != 0;
-                const int32_t j = k * BPS + i;
-                base_tok[i] = (b0 + (prefix_item ? j : warp + NW * j)) * bs;
-            }
-
-            // S = Q K^T  (16 rows x 16 tokens per block; n-tile 2i + h holds
-            // tokens 8h .. 8h+7 of block i), even and odd 16-dim steps in two
-            // accumulator chains (half the dependent-MMA latency)
-            float sacc[2 * BPS][4];
-    #pragma unroll
-            for (int i = 0; i < BPS; ++i) {
-                const uint32_t kt = stile + i * 2 * C::kTileBytes;
-                float sa[2][2][4] = {};
-    #pragma unroll
-                for (int kk = 0; kk < C::kKS; ++kk) {
-                    uint32_t a[4];
-                    if constexpr (C::kQInRegs) {
-                        a[0] = qf[kk][0]; a[1] = qf[kk][1]; a[2] = qf[kk][2]; a[3] = qf[kk][3];
-                    } else {
-                        ldsm_x4(q_lane + kk * 32, a[0], a[1], a[2], a[3]);
-                    }
-                    uint32_t k0, k1, k2, k3;
-                    ldsm_x4(kv_chunk_addr<D>(kt, k_tok, kk * 16 + k_dof), k0, k1, k2, k3);
-                    mma_16816(sa[kk & 1][0], a, k0, k1);
-                    mma_16816(sa[kk & 1][1], a, k2, k3);
-                }
-    #pragma unroll
-                for (int h = 0; h < 2; ++h)
-    #pragma unroll
-                    for (int e = 0; e < 4; ++e) sacc[2 * i + h][e] = sa[0][h][e] + sa[1][h][e];
-            }
-
-            // mask, scale to log2 units, online softmax over the quad's row
-            float s[2 * BPS][4];
-            // blocks inside the range of every live row (the common case) need
-            // no mask; rows with hi = 0 hold no query and are never written out
-            bool inside = true;
-    #pragma unroll
-            for (int i = 0; i < BPS; ++i) {
-                auto in_row = [&](int lo, int hi) {
-                    return hi == 0 || (base_tok[i] >= lo && base_tok[i] + bs <= hi);
-                };
-                inside = inside && okb[i] && in_row(lo0, hi0) && in_row(lo1, hi1);
-            }
-            if (__all_sync(0xffffffffu, inside)) {
-    #pragma unroll
-                for (int j = 0; j < 2 * BPS; ++j)
-    #pragma unroll
-                    for (int e = 0; e < 4; ++e) s[j][e] = sacc[j][e] * p.scale_log2;
-            } else {
-    #pragma unroll
-                for (int j = 0; j < 2 * BPS; ++j)
-    #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int pos = base_tok[j >> 1] + (j & 1) * 8 + c2 + (e & 1);
-                        const int lo = e < 2 ? lo0 : lo1, hi = e < 2 ? hi0 : hi1;
-                        s[j][e] = (okb[j >> 1] && pos >= lo && pos < hi) ? sacc[j][e] * p.scale_log2
-                                                                          : -INFINITY;
-                    }
-            }
-            float mx0 = fmaxf(s[0][0], s[0][1]), mx1 = fmaxf(s[0][2], s[0][3]);
-    #pragma unroll
-            for (int j = 1; j < 2 * BPS; ++j) {
-                mx0 = fmaxf(mx0, fmaxf(s[j][0], s[j][1]));
-                mx1 = fmaxf(mx1, fmaxf(s[j][2], s[j][3]));
-            }
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-            const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
-            const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
-            const float al0 = fast_exp2(m0 - mu0), al1 = fast_exp2(m1 - mu1);
-            // once the running maxima settle the rescale factor is exactly 1
-            const bool grew = __any_sync(0xffffffffu, mn0 != m0 || mn1 != m1);
-            m0 = mn0;
-            m1 = mn1;
-            float pf[2 * BPS][4];
-    #pragma unroll
-            for (int j = 0; j < 2 * BPS; ++j) {
-                pf[j][0] = fast_exp2(s[j][0] - mu0);
-                pf[j][1] = fast_exp2(s[j][1] - mu0);
-                pf[j][2] = fast_exp2(s[j][2] - mu1);
-                pf[j][3] = fast_exp2(s[j][3] - mu1);
-            }
-            float ps0 = 0.f, ps1 = 0.f;
-    #pragma unroll
-            for (int j = 0; j < 2 * BPS; ++j) {
-                ps0 += pf[j][0] + pf[j][1];
-                ps1 += pf[j][2] + pf[j][3];
-            }
-            l0 = l0 * al0 + ps0;
-            l1 = l1 * al1 + ps1;
-            if (grew) {
-    #pragma unroll
-                for (int nt = 0; nt < C::kNT; ++nt) {
-                    o[nt][0] *= al0;
-                    o[nt][1] *= al0;
-                    o[nt][2] *= al1;
-                    o[nt][3] *= al1;
-                }
-            }
-
-            // O += P V per block  (values of tokens outside every row's range are
-            // zeroed: stale slots may hold anything, including NaN)
-    #pragma unroll
-            for (int i = 0; i < BPS; ++i) {
-                if (!okb[i]) continue;
-                const uint32_t vt = stile + i * 2 * C::kTileBytes + C::kTileBytes;
-                // P of block i as the A fragment of a 16-token k-step
-                uint32_t pa[4], pl[4];
-                const float(&p0)[4] = pf[2 * i];
-                const float(&p1)[4] = pf[2 * i + 1];
-                // a bf16 pair hi + lo (lo = bf16(P - hi)): the P.V product then
-                // carries P to about 2^-17 relative instead of the 2^-9 of a
-                // single bf16 rounding
-                pa[0] = pack_bf16x2(p0[0], p0[1]);
-                pa[1] = pack_bf16x2(p0[2], p0[3]);
-                pa[2] = pack_bf16x2(p1[0], p1[1]);
-                pa[3] = pack_bf16x2(p1[2], p1[3]);
-                pl[0] = pack_bf16x2(p0[0] - bf16lo_to_f32(pa[0]), p0[1] - bf16hi_to_f32(pa[0]));
-                pl[1] = pack_bf16x2(p0[2] - bf16lo_to_f32(pa[1]), p0[3] - bf16hi_to_f32(pa[1]));
-                pl[2] = pack_bf16x2(p1[0] - bf16lo_to_f32(pa[2]), p1[1] - bf16hi_to_f32(pa[2]));
-                pl[3] = pack_bf16x2(p1[2] - bf16lo_to_f32(pa[3]), p1[3] - bf16hi_to_f32(pa[3]));
-                uint32_t mk0 = 0xffffffffu, mk1 = 0xffffffffu;
-                const int bt = base_tok[i];
-                if (bt < lo_all || bt + bs > hi_all) {
-                    auto live = [&](int t) { return bt + t >= lo_all && bt + t < hi_all; };
-                    mk0 = (live(c2) ? 0x0000ffffu : 0u) | (live(c2 + 1) ? 0xffff0000u : 0u);
-                    mk1 = (live(c2 + 8) ? 0x0000ffffu : 0u) | (live(c2 + 9) ? 0xffff0000u : 0u);
-                }
-    #pragma unroll
-                for (int np = 0; np < C::kNT / 2; ++np) {
-                    uint32_t v0, v1, v2, v3;
-                    ldsm_x4_trans(kv_chunk_addr<D>(vt, v_tok, np * 16 + v_dof), v0, v1, v2, v3);
-                    v0 &= mk0; v1 &= mk1; v2 &= mk0; v3 &= mk1;
-                    mma_16816(o[2 * np], pa, v0, v1);
-                    mma_16816(o[2 * np + 1], pa, v2, v3);
-                    mma_16816(o[2 * np], pl, v0, v1);
-                    mma_16816(o[2 * np + 1], pl, v2, v3);
-                }
-            }
-
-            // release the stage: its generic-proxy reads come before the next
-            // TMA write into it
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (!prefix_item) {
-                if (k + SPW < nk) issue(k + SPW);
-            } else {
-                if (lane == 0) mbar_arrive(&empty[st]);
-                if (warp == 0 && k + STAGES < nk) {
-                    // every warp has released this stage before it is refilled
-                    bool freed = true;
-                    if (lane == 0) freed = mbar_wait(&empty[st], use & 1);
-                    if (!__shfl_sync(0xffffffffu, freed, 0)) {
-                        if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
-                    } else {
-                        issue(k + STAGES);
-                    }
-                }
-            }
-        }
-
-        // row sums: the quad's four partial sums
-        l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-        l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-
-        if (prefix_item) {
-            // each warp owns its tile: write its rows directly
-    #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                const int k = tile * 16 + qd + half * 8;
-                const int32_t pr = pair_row[k];
-                if (pr < 0) continue;
-                const size_t pi = partial_index(p, pr, pair_head[k], slot);
-                float *dst = p.ws_o + pi * D;
-    #pragma unroll
-                for (int nt = 0; nt < C::kNT; ++nt)
-                    *reinterpret_cast<float2 *>(dst + nt * 8 + c2) =
-                        make_float2(o[nt][2 * half], o[nt][2 * half + 1]);
-                if ((lane & 3) == 0)
-                    *reinterpret_cast<float2 *>(p.ws_ml + pi * 2) =
-                        make_float2(half ? m1 : m0, half ? l1 : l0);
-            }
-            return;
-        }
-
-        // split item: this warp's rows of the one tile into the merge buffers
-        __syncthreads();
-    #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            const int row = qd + half * 8;
-            if (row >= R) continue;
-            float *dst = mbuf + (warp * R + row) * D;
-    #pragma unroll
-            for (int nt = 0; nt < C::kNT; ++nt)
-                *reinterpret_cast<float2 *>(dst + nt * 8 + c2) =
-                    make_float2(o[nt][2 * half], o[nt][2 * half + 1]);
-            if ((lane & 3) == 0)
-                *reinterpret_cast<float2 *>(mlbuf + (warp * R + row) * 2) =
-                    make_float2(half ? m1 : m0, half ? l1 : l0);
-        }
+        return;
     }
+    // split item: this warp's rows of the one tile into the merge buffers
+    __syncthreads();
+#pragma unroll
+    for (int n = 0; n < NQ; ++n)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int row = 8 * n + 2 * cc + e;
+            if (row >= R) continue;
+            float *dst = mbuf + (warp * R + row) * D + g8;
+#pragma unroll
+            for (int mt = 0; mt < C::kMT; ++mt) {
+                dst[16 * mt] = oT[mt][n][e];
+                dst[16 * mt + 8] = oT[mt][n][e + 2];
+            }
+            if (g8 == 0)
+                *reinterpret_cast<float2 *>(mlbuf + (warp * R + row) * 2) =
+                    make_float2(mc[n][e], lc[n][e]);
+        }
     __syncthreads();
     for (int idx = threadIdx.x; idx < R * D; idx += NW * 32) {
         const int row = idx / D, d = idx % D;
@@ -1004,7 +798,7 @@ __device__ __forceinline__ void decode_split_body(const CUtensorMap &kmap, const
 }
 
 template <int D, bool kMQ, bool kF8, int NQ>
-__global__ void __launch_bounds__(kDecodeWarps * 32, KvCfg<D, kF8>::kCtasPerSm)
+__global__ void __launch_bounds__(kDecodeWarps * 32, KvCfg<D, kF8, NQ>::kCtasPerSm)
     decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, const DecodeParams p)
 {
@@ -1015,7 +809,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, KvCfg<D, kF8>::kCtasPerSm)
 // the head shape, e.g. a full-attention group and a sliding group): CTAs
 // [cta_end[i-1], cta_end[i]) do group i's work.
 template <int D, bool kF8, int NQ>
-__global__ void __launch_bounds__(kDecodeWarps * 32, KvCfg<D, kF8>::kCtasPerSm)
+__global__ void __launch_bounds__(kDecodeWarps * 32, KvCfg<D, kF8, NQ>::kCtasPerSm)
     decode_split_grouped_kernel(const __grid_constant__ GroupedDecode gd)
 {
     int i = 0;
@@ -1031,7 +825,7 @@ static cudaError_t launch_split_grouped(const GroupedDecode &gd, cudaStream_t st
     const int64_t ctas = gd.cta_end[gd.n - 1];
     if (ctas == 0) return cudaSuccess;
     auto kern = decode_split_grouped_kernel<D, kF8, NQ>;
-    const int smem = KvSmem<D, kF8>::kLaunchBytes;
+    const int smem = KvSmem<D, kF8, NQ>::kLaunchBytes;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
     err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -1050,7 +844,7 @@ static cudaError_t launch_split(const DecodeParams &p, const CUtensorMap &kmap,
     const int64_t ctas = p.plan.n_prefix_ctas + p.plan.n_suffix_ctas;
     if (ctas == 0) return cudaSuccess;
     auto kern = decode_split_kernel<D, kMQ, kF8, NQ>;
-    const int smem = KvSmem<D, kF8>::kLaunchBytes;
+    const int smem = KvSmem<D, kF8, NQ>::kLaunchBytes;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
     // the largest shared-memory carveout, so that kCtasPerSm CTAs are resident per SM

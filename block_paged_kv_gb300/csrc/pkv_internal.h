@@ -167,18 +167,19 @@ cudaError_t launch_decode_combine_grouped(GroupedDecode &gd, pkv_dtype out_dtype
 // merge of the split partials into out (dtype of q)
 cudaError_t launch_decode_combine(const DecodeParams &p, pkv_dtype dtype, cudaStream_t stream);
 
-// Consumer warps per decode CTA (plus one producer warp for bf16): a split
-// CTA's warps share one 16-row query tile and take its blocks in turn; a
-// shared-prefix CTA holds several tiles of (row, head) pairs (64 pairs for
-// head_dim <= 128, 32 for 256), each read by NW / tiles warps.
+// Warps per decode CTA: a split CTA's warps share one query tile and take its
+// blocks in turn; a shared-prefix CTA holds one tile of (row, head) pairs per
+// warp.  The prefix cut (the prefix blocks per split) is sized as if a CTA
+// held 64 pairs (32 at head_dim 256), whatever the dtype, so that the
+// workspace size does not depend on it.
 constexpr int kDecodeWarps = 4;
 constexpr int kPrefixPairsPerCta = 64;  // head_dim <= 128 (32 for head_dim 256)
 
-// FP8 decode: query rows sit on the N side of the products in n-tiles of 8;
-// a split item's rows (the G heads, or G x queries of a verify step) need
-// this many, and so does each warp's tile of a prefix item (8 x that many
-// (row, head) pairs per warp)
-inline int fp8_query_ntiles(int64_t rows) { return rows > 8 ? 2 : 1; }
+// bf16 / FP8 decode: query rows sit on the N side of the products in n-tiles
+// of 8; a split item's rows (the G heads, or G x queries of a verify step)
+// need this many, and so does each warp's tile of a prefix item (8 x that
+// many (row, head) pairs per warp)
+inline int query_ntiles(int64_t rows) { return rows > 8 ? 2 : 1; }
 // query rows per CTA of the f32 kernel
 constexpr int kF32Rows = 16;
 
