@@ -110,14 +110,15 @@ DecodePlan make_plan(int32_t batch, int32_t hq, int32_t hkv, int32_t D, int32_t 
     nblk_max = std::max<int64_t>(nblk_max, 1);
     const int64_t tiles_ub = static_cast<int64_t>(batch) * nblk_max * hkv;
     // Split size over the upper bound of (block, kv head) tiles, a multiple of
-    // the consumer warp count.  Many (row, kv head) pairs: about four waves of
-    // two resident CTAs per SM, so that rows of unequal length even out, and
-    // at least 8 blocks per split.  Fewer pairs than SMs (a few long rows):
-    // about one wave, since each CTA pays a fixed start-up cost and the merge
-    // reads every partial; at least 4 blocks per split.
+    // the consumer warp count.  Many (row, kv head) pairs: about twelve CTAs
+    // per SM (four waves of three resident CTAs), so that rows of unequal
+    // length even out, and at least 8 blocks per split.  Fewer pairs than SMs
+    // (a few long rows): two CTAs per SM, one wave, since each CTA pays a
+    // fixed start-up cost and the merge reads every partial; at least 4
+    // blocks per split.
     const int64_t pairs = static_cast<int64_t>(batch) * hkv;
     const bool few = pairs < num_sms;
-    const int64_t target = static_cast<int64_t>(std::max(num_sms, 1)) * 2 * (few ? 1 : 4);
+    const int64_t target = static_cast<int64_t>(std::max(num_sms, 1)) * (few ? 2 : 12);
     int64_t C = ceil_div64(tiles_ub, target);
     C = std::max<int64_t>(C, few ? 4 : 8);
     C = ceil_div64(C, kDecodeWarps) * kDecodeWarps;

@@ -189,12 +189,55 @@ __device__ __forceinline__ void decode_split_body(const CUtensorMap &kmap, const
     // (query, head) pairs of a row's few queries (kMQ: a verify step); the
     // launch takes NQ so that R <= TR
     const int R = kMQ ? G * p.max_q : G;
+    // the block ids of the run (this warp's share of a split item; the whole
+    // run for a prefix item, fetched by warp 0)
+    BlockIds ids;
+    // B fragments of Q^T (query rows on N, NQ n-tiles of 8):
+    // b0 = Q[row 8n + lane/4][16kk + 2(lane%4), +1], b1 = the same 8 dims further.
+    // A split item whose query fits in registers loads them straight from
+    // global memory (no shared-memory staging, no wait before its first
+    // block loads); other items stage the query tiles in shared memory.
+    uint32_t qb[C::kQInRegs ? C::kKS : 1][NQ][2];
+    const bool q_direct = C::kQInRegs && !prefix_item;
+    auto load_q_direct = [&]() {
+#pragma unroll
+        for (int n = 0; n < NQ; ++n) {
+            const int row = 8 * n + (lane >> 2);
+            int32_t qr = -1, qh = 0;
+            if constexpr (kMQ) {
+                if (row < R && row / G < row_C) {
+                    qr = row_q0 + row / G;
+                    qh = g * G + row % G;
+                }
+            } else if (row < G) {
+                qr = row_r;
+                qh = g * G + row;
+            }
+            const uint32_t *src = reinterpret_cast<const uint32_t *>(p.q) +
+                                  (static_cast<int64_t>(qr < 0 ? 0 : qr) * p.hq + qh) * (D / 2) + (lane & 3);
+#pragma unroll
+            for (int kk = 0; kk < C::kKS; ++kk) {
+                qb[kk][n][0] = qr >= 0 ? __ldg(src + 8 * kk) : 0u;
+                qb[kk][n][1] = qr >= 0 ? __ldg(src + 8 * kk + 4) : 0u;
+            }
+        }
+    };
     if (!prefix_item) {
         int64_t bid = cta - p.plan.n_prefix_ctas;
         const int32_t s = static_cast<int32_t>(bid % p.plan.n_suffix_splits);
         bid /= p.plan.n_suffix_splits;
         g = static_cast<int32_t>(bid % p.hkv);
         row_r = static_cast<int32_t>(bid / p.hkv);
+        const int32_t *table_row = p.tables + static_cast<int64_t>(row_r) * p.width;
+        // This warp's block ids are fetched before the row's length is known,
+        // on the guess that the row's own splits start at block 0 (full
+        // attention, no shared prefix), so that the two fetches overlap; a
+        // decode step's query loads go out with them.
+        const int32_t b_guess = s * p.plan.split_blocks;
+        const int32_t n_guess =
+            max(0, (min(p.plan.split_blocks, p.width - b_guess) - warp + NW - 1) / NW);
+        ids.init(table_row + (n_guess > 0 ? b_guess : 0), warp, NW, n_guess, lane);
+        if constexpr (C::kQInRegs && !kMQ) load_q_direct();
         const RowRange rr = row_range(p, row_r, s == 0 && g == 0);
         b0 = rr.b_first + s * p.plan.split_blocks;
         const int32_t b1 = min(b0 + p.plan.split_blocks, rr.b_end);
@@ -207,6 +250,12 @@ __device__ __forceinline__ void decode_split_body(const CUtensorMap &kmap, const
         row_C = rr.C;
         row_q0 = rr.q0;
         tiles = 1;
+        if constexpr (C::kQInRegs && kMQ) load_q_direct();
+        const int32_t nbw = nblk > warp ? (nblk - warp + NW - 1) / NW : 0;
+        if (rr.b_first != 0)
+            ids.init(table_row + b0, warp, NW, nbw, lane);  // the guess was wrong
+        else
+            ids.n = nbw;  // fetched ids past the run are never used
     } else {
         tiles = C::kTiles;
         int64_t bid = cta;
@@ -281,7 +330,7 @@ __device__ __forceinline__ void decode_split_body(const CUtensorMap &kmap, const
     // ------------------------------------------------- query tiles + barriers
     {
         constexpr int kVec = D / 8;  // 16-byte vectors per row
-        const int qrows = prefix_item ? tiles * TR : TR;
+        const int qrows = q_direct ? 0 : (prefix_item ? tiles * TR : TR);
         for (int i = threadIdx.x; i < qrows * kVec; i += blockDim.x) {
             const int row = i / kVec, v = i % kVec;
             int32_t qr = -1, qh = 0;
@@ -333,24 +382,24 @@ __device__ __forceinline__ void decode_split_body(const CUtensorMap &kmap, const
     // a split item's warps all read query tile 0; a prefix item's warp w owns
     // tile w
     const int tile = prefix_item ? warp : 0;
-    // B fragments of Q^T (query rows on N, NQ n-tiles of 8):
-    // b0 = Q[row 8n + lane/4][16kk + 2(lane%4), +1], b1 = the same 8 dims further
     const uint32_t qb_lane = smem_u32(q_mem + tile * C::kQTileBytes) + (lane >> 2) * C::kQStride +
                              (lane & 3) * 4;
-    uint32_t qb[C::kQInRegs ? C::kKS : 1][NQ][2];
     if constexpr (C::kQInRegs) {
+        if (!q_direct) {
+            // a prefix item's tiles, staged through the ring
 #pragma unroll
-        for (int kk = 0; kk < C::kKS; ++kk)
+            for (int kk = 0; kk < C::kKS; ++kk)
 #pragma unroll
-            for (int n = 0; n < NQ; ++n) {
-                const uint32_t a = qb_lane + n * 8 * C::kQStride + kk * 32;
-                qb[kk][n][0] = lds32(a);
-                qb[kk][n][1] = lds32(a + 16);
-            }
-        // the ring is about to be overwritten by TMA (async proxy) after these
-        // generic-proxy reads and writes of the staged query tiles
-        fence_proxy_async_smem();
-        __syncthreads();
+                for (int n = 0; n < NQ; ++n) {
+                    const uint32_t a = qb_lane + n * 8 * C::kQStride + kk * 32;
+                    qb[kk][n][0] = lds32(a);
+                    qb[kk][n][1] = lds32(a + 16);
+                }
+            // the ring is about to be overwritten by TMA (async proxy) after
+            // these generic-proxy reads and writes of the staged query tiles
+            fence_proxy_async_smem();
+            __syncthreads();
+        }
     }
 
     // ------------------------------------------------------------- loads
@@ -361,12 +410,11 @@ __device__ __forceinline__ void decode_split_body(const CUtensorMap &kmap, const
     //   k % STAGES; loads issued by warp 0.
     constexpr int BPS = C::kBps;
     const uint64_t policy = l2_evict_first_policy();
-    const int32_t *table_row = p.tables + static_cast<int64_t>(tab_row) * p.width + b0;
     const int32_t nb = prefix_item ? nblk : (nblk > warp ? (nblk - warp + NW - 1) / NW : 0);
     const int32_t nk = (nb + BPS - 1) / BPS;
     const bool issuer = !prefix_item || warp == 0;
-    BlockIds ids;
-    if (issuer) ids.init(table_row, prefix_item ? 0 : warp, prefix_item ? 1 : NW, nb, lane);
+    if (prefix_item && warp == 0)
+        ids.init(p.tables + static_cast<int64_t>(tab_row) * p.width + b0, 0, 1, nb, lane);
     auto stage_of = [&](int32_t k) { return prefix_item ? k % STAGES : warp * SPW + k % SPW; };
     auto issue = [&](int32_t k) {  // whole warp; lane 0 issues
         int32_t bj[BPS];
@@ -412,6 +460,21 @@ __device__ __forceinline__ void decode_split_body(const CUtensorMap &kmap, const
     const int32_t depth = prefix_item ? STAGES : SPW;
     if (issuer)
         for (int32_t k = 0; k < min(depth, nk); ++k) issue(k);
+    if constexpr (kF8 && C::kQInRegs) {
+        if (q_direct) {
+            // bf16 -> f16 (exact inside the f16 range; NaN stays NaN), while
+            // the first loads are in flight
+            bool bad = false;
+#pragma unroll
+            for (int kk = 0; kk < C::kKS; ++kk)
+#pragma unroll
+                for (int n = 0; n < NQ; ++n) {
+                    qb[kk][n][0] = bf16x2_to_f16x2(qb[kk][n][0], bad);
+                    qb[kk][n][1] = bf16x2_to_f16x2(qb[kk][n][1], bad);
+                }
+            if (bad) report(p.status, PKV_DEV_Q_RANGE);
+        }
+    }
 
     // ---------------------------------------------------------------- compute
     // split item: the four warps' partials of the one tile meet in the ring
