@@ -248,7 +248,7 @@ __device__ __forceinline__ __nv_bfloat16 to_out<__nv_bfloat16>(float x) { return
 
 constexpr int kCombineWarps = 8;
 
-template <typename OutT, int D, int W>
+template <typename OutT, int D, int W, int KB>
 __device__ __forceinline__ void decode_combine_body(const DecodeParams &p, const int64_t cta)
 {
     constexpr int CH = (W == 1 || D < 64) ? D : 64;  // dims per item
@@ -277,36 +277,61 @@ __device__ __forceinline__ void decode_combine_body(const DecodeParams &p, const
     const size_t base = partial_index(p, r, h, 0, t);
     auto slot_of = [&](int32_t k) { return k < npre ? k : p.plan.n_prefix_splits + (k - npre); };
 
-    // this warp's maximum over its partials k = warp + W * i
-    float Mw = -INFINITY;
-    for (int32_t k = warp + W * lane; k < n; k += W * 32)
-        Mw = fmaxf(Mw, p.ws_ml[(base + slot_of(k)) * 2]);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) Mw = fmaxf(Mw, __shfl_xor_sync(0xffffffffu, Mw, off));
+    // this warp's partials k = warp + W * i, in batches of kB: every load of
+    // a batch is issued before any of them is used (one memory round trip per
+    // batch), and each batch is folded into the running (max, sum, values)
+    // with the usual rescale (a factor of exactly 0 while nothing has been
+    // seen).  The launch sizes KB to the row's partials, so that one batch
+    // usually covers them, without more registers (fewer resident CTAs) than
+    // that needs.
+    constexpr int kB = (W == 1 && PER > 4) ? KB / 2 : KB;
+    float Mw = -INFINITY, lw = 0.f;
     float acc[PER];
 #pragma unroll
     for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-    float lw = 0.f;
-    if (Mw != -INFINITY) {
-        // the partials' loads are independent: unrolling keeps several in flight
-#pragma unroll 8
-        for (int32_t k = warp; k < n; k += W) {
-            const size_t slot = base + slot_of(k);
-            const float2 ml = *reinterpret_cast<const float2 *>(p.ws_ml + slot * 2);
-            const float wgt = fast_exp2(ml.x - Mw);  // 0 for an empty partial
-            lw = fmaf(wgt, ml.y, lw);
-            const float *src = p.ws_o + slot * D + ch * CH + (W == 1 ? lane : lane * PER);
-            if constexpr (W == 1) {
-                // lane owns dims lane + 32 e: each load instruction is coalesced
+    for (int32_t k0 = warp; k0 < n; k0 += W * kB) {
+        float2 ml[kB];
+        float v[kB][PER];
 #pragma unroll
-                for (int e = 0; e < PER; ++e) acc[e] = fmaf(wgt, src[32 * e], acc[e]);
-            } else if constexpr (PER == 2) {
-                const float2 v = *reinterpret_cast<const float2 *>(src);
-                acc[0] = fmaf(wgt, v.x, acc[0]);
-                acc[1] = fmaf(wgt, v.y, acc[1]);
+        for (int i = 0; i < kB; ++i) {
+            const int32_t k = k0 + W * i;
+            if (k < n) {
+                const size_t slot = base + slot_of(k);
+                ml[i] = *reinterpret_cast<const float2 *>(p.ws_ml + slot * 2);
+                const float *src = p.ws_o + slot * D + ch * CH + (W == 1 ? lane : lane * PER);
+                if constexpr (W == 1) {
+                    // lane owns dims lane + 32 e: each load instruction is coalesced
+#pragma unroll
+                    for (int e = 0; e < PER; ++e) v[i][e] = src[32 * e];
+                } else if constexpr (PER == 2) {
+                    const float2 t = *reinterpret_cast<const float2 *>(src);
+                    v[i][0] = t.x;
+                    v[i][1] = t.y;
+                } else {
+                    v[i][0] = src[0];
+                }
             } else {
-                acc[0] = fmaf(wgt, src[0], acc[0]);
+                ml[i] = make_float2(-INFINITY, 0.f);
+#pragma unroll
+                for (int e = 0; e < PER; ++e) v[i][e] = 0.f;
             }
+        }
+        float bm = Mw;
+#pragma unroll
+        for (int i = 0; i < kB; ++i) bm = fmaxf(bm, ml[i].x);
+        if (bm != -INFINITY) {
+            const float a = fast_exp2(Mw - bm);
+            lw *= a;
+#pragma unroll
+            for (int e = 0; e < PER; ++e) acc[e] *= a;
+#pragma unroll
+            for (int i = 0; i < kB; ++i) {
+                const float wgt = fast_exp2(ml[i].x - bm);  // 0 for an empty partial
+                lw = fmaf(wgt, ml[i].y, lw);
+#pragma unroll
+                for (int e = 0; e < PER; ++e) acc[e] = fmaf(wgt, v[i][e], acc[e]);
+            }
+            Mw = bm;
         }
     }
     if constexpr (W == 1) {
@@ -343,15 +368,15 @@ __device__ __forceinline__ void decode_combine_body(const DecodeParams &p, const
     }
 }
 
-template <typename OutT, int D, int W>
+template <typename OutT, int D, int W, int KB>
 __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(const DecodeParams p)
 {
-    decode_combine_body<OutT, D, W>(p, blockIdx.x);
+    decode_combine_body<OutT, D, W, KB>(p, blockIdx.x);
 }
 
 // The merges of several decode calls in one launch: CTAs
 // [item_end[i-1], item_end[i]) merge group i.
-template <typename OutT, int D, int W>
+template <typename OutT, int D, int W, int KB>
 __global__ void __launch_bounds__(kCombineWarps * 32)
     decode_combine_grouped_kernel(const __grid_constant__ GroupedDecode gd)
 {
@@ -359,7 +384,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
     const int64_t b = blockIdx.x;
     while (i + 1 < gd.n && b >= gd.item_end[i]) ++i;
     const int64_t first = i > 0 ? gd.item_end[i - 1] : 0;
-    decode_combine_body<OutT, D, W>(gd.g[i], b - first);
+    decode_combine_body<OutT, D, W, KB>(gd.g[i], b - first);
 }
 
 // merge CTAs of one call
@@ -372,7 +397,7 @@ static int64_t combine_ctas(const DecodeParams &p)
     return (items + ipc - 1) / ipc;
 }
 
-template <typename OutT, int W>
+template <typename OutT, int W, int KB>
 static cudaError_t launch_combine_grouped_w(GroupedDecode &gd, cudaStream_t stream)
 {
     int64_t total = 0;
@@ -383,30 +408,32 @@ static cudaError_t launch_combine_grouped_w(GroupedDecode &gd, cudaStream_t stre
     if (total == 0) return cudaSuccess;
     const dim3 grid(static_cast<unsigned>(total)), block(kCombineWarps * 32);
     switch (gd.g[0].head_dim) {
-    case 64: return launch_pdl(decode_combine_grouped_kernel<OutT, 64, W>, grid, block, 0, stream, gd);
-    case 128: return launch_pdl(decode_combine_grouped_kernel<OutT, 128, W>, grid, block, 0, stream, gd);
-    case 256: return launch_pdl(decode_combine_grouped_kernel<OutT, 256, W>, grid, block, 0, stream, gd);
+    case 64: return launch_pdl(decode_combine_grouped_kernel<OutT, 64, W, KB>, grid, block, 0, stream, gd);
+    case 128: return launch_pdl(decode_combine_grouped_kernel<OutT, 128, W, KB>, grid, block, 0, stream, gd);
+    case 256: return launch_pdl(decode_combine_grouped_kernel<OutT, 256, W, KB>, grid, block, 0, stream, gd);
     default: return cudaErrorInvalidValue;
     }
 }
 
 cudaError_t launch_decode_combine_grouped(GroupedDecode &gd, pkv_dtype out_dtype, cudaStream_t stream)
 {
-    bool many = false;  // eight warps per item when any group's rows have many partials
-    for (int i = 0; i < gd.n; ++i) many = many || gd.g[i].plan.nslot > 16;
+    int32_t nslot = 0;  // the shape follows the group with the most partials per row
+    for (int i = 0; i < gd.n; ++i) nslot = std::max(nslot, gd.g[i].plan.nslot);
     prof_begin(PKV_KERNEL_DECODE_COMBINE, stream);
     cudaError_t err;
     if (out_dtype == PKV_BF16)
-        err = many ? launch_combine_grouped_w<__nv_bfloat16, kCombineWarps>(gd, stream)
-                   : launch_combine_grouped_w<__nv_bfloat16, 1>(gd, stream);
+        err = nslot <= 16 ? launch_combine_grouped_w<__nv_bfloat16, 1, 8>(gd, stream)
+              : nslot <= 32 ? launch_combine_grouped_w<__nv_bfloat16, kCombineWarps, 4>(gd, stream)
+                            : launch_combine_grouped_w<__nv_bfloat16, kCombineWarps, 16>(gd, stream);
     else
-        err = many ? launch_combine_grouped_w<float, kCombineWarps>(gd, stream)
-                   : launch_combine_grouped_w<float, 1>(gd, stream);
+        err = nslot <= 16 ? launch_combine_grouped_w<float, 1, 8>(gd, stream)
+              : nslot <= 32 ? launch_combine_grouped_w<float, kCombineWarps, 4>(gd, stream)
+                            : launch_combine_grouped_w<float, kCombineWarps, 16>(gd, stream);
     prof_end(PKV_KERNEL_DECODE_COMBINE, stream);
     return err;
 }
 
-template <typename OutT, int W>
+template <typename OutT, int W, int KB>
 static cudaError_t launch_combine_w(const DecodeParams &p, cudaStream_t stream)
 {
     const int64_t chunks = (W == 1 || p.head_dim < 64) ? 1 : p.head_dim / 64;
@@ -414,10 +441,10 @@ static cudaError_t launch_combine_w(const DecodeParams &p, cudaStream_t stream)
     const int64_t ipc = kCombineWarps / W;
     const dim3 grid(static_cast<unsigned>((items + ipc - 1) / ipc)), block(kCombineWarps * 32);
     switch (p.head_dim) {
-    case 32: return launch_pdl(decode_combine_kernel<OutT, 32, W>, grid, block, 0, stream, p);
-    case 64: return launch_pdl(decode_combine_kernel<OutT, 64, W>, grid, block, 0, stream, p);
-    case 128: return launch_pdl(decode_combine_kernel<OutT, 128, W>, grid, block, 0, stream, p);
-    case 256: return launch_pdl(decode_combine_kernel<OutT, 256, W>, grid, block, 0, stream, p);
+    case 32: return launch_pdl(decode_combine_kernel<OutT, 32, W, KB>, grid, block, 0, stream, p);
+    case 64: return launch_pdl(decode_combine_kernel<OutT, 64, W, KB>, grid, block, 0, stream, p);
+    case 128: return launch_pdl(decode_combine_kernel<OutT, 128, W, KB>, grid, block, 0, stream, p);
+    case 256: return launch_pdl(decode_combine_kernel<OutT, 256, W, KB>, grid, block, 0, stream, p);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -427,9 +454,14 @@ static cudaError_t launch_combine_t(const DecodeParams &p, cudaStream_t stream)
 {
     if (static_cast<int64_t>(p.batch) * p.hq == 0) return cudaSuccess;
     prof_begin(PKV_KERNEL_DECODE_COMBINE, stream);
-    // a warp per item while rows have few partials, eight when they have many
-    const cudaError_t err = p.plan.nslot > 16 ? launch_combine_w<OutT, kCombineWarps>(p, stream)
-                                             : launch_combine_w<OutT, 1>(p, stream);
+    // a warp per item while rows have few partials (one batch of 4, or two
+    // of 8 at most), eight when they have many: one batch of 4 per warp up to 32
+    // partials (few registers, many resident CTAs), else batches of 16
+    const int32_t n = p.plan.nslot;
+    const cudaError_t err = n <= 4    ? launch_combine_w<OutT, 1, 4>(p, stream)
+                            : n <= 16 ? launch_combine_w<OutT, 1, 8>(p, stream)
+                            : n <= 32 ? launch_combine_w<OutT, kCombineWarps, 4>(p, stream)
+                                      : launch_combine_w<OutT, kCombineWarps, 16>(p, stream);
     prof_end(PKV_KERNEL_DECODE_COMBINE, stream);
     return err;
 }
