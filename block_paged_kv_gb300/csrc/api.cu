@@ -48,13 +48,17 @@ cudaEvent_t take_event()
 
 int num_sms_current()
 {
-    static int cache[64] = {0};
+    // per-device cache; host threads may call concurrently
+    static std::atomic<int> cache[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+    if (dev >= 0 && dev < 64) {
+        const int c = cache[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    if (dev >= 0 && dev < 64) cache[dev] = n;
+    if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
     return n;
 }
 
@@ -110,15 +114,16 @@ DecodePlan make_plan(int32_t batch, int32_t hq, int32_t hkv, int32_t D, int32_t 
     nblk_max = std::max<int64_t>(nblk_max, 1);
     const int64_t tiles_ub = static_cast<int64_t>(batch) * nblk_max * hkv;
     // Split size over the upper bound of (block, kv head) tiles, a multiple of
-    // the consumer warp count.  Many (row, kv head) pairs: about twelve CTAs
-    // per SM (four waves of three resident CTAs), so that rows of unequal
-    // length even out, and at least 8 blocks per split.  Fewer pairs than SMs
-    // (a few long rows): two CTAs per SM, one wave, since each CTA pays a
-    // fixed start-up cost and the merge reads every partial; at least 4
-    // blocks per split.
+    // the consumer warp count.  Many (row, kv head) pairs: about nine CTAs
+    // per SM (three waves of three resident CTAs), so that rows of unequal
+    // length even out, and at least 8 blocks per split (measured on 32 rows of
+    // 1-8k tokens: 96 blocks per split beat 64, 72, 80, 108 and 128, for one
+    // query per row and for four).  Fewer pairs than SMs (a few long rows):
+    // two CTAs per SM, one wave, since each CTA pays a fixed start-up cost
+    // and the merge reads every partial; at least 4 blocks per split.
     const int64_t pairs = static_cast<int64_t>(batch) * hkv;
     const bool few = pairs < num_sms;
-    const int64_t target = static_cast<int64_t>(std::max(num_sms, 1)) * (few ? 2 : 12);
+    const int64_t target = static_cast<int64_t>(std::max(num_sms, 1)) * (few ? 2 : 9);
     int64_t C = ceil_div64(tiles_ub, target);
     C = std::max<int64_t>(C, few ? 4 : 8);
     C = ceil_div64(C, kDecodeWarps) * kDecodeWarps;
