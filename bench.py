@@ -532,9 +532,10 @@ def run_long_case(args, local):
                       "split_frac_of_hbm_peak": round(b / s / 1e9 / peaks()[0], 3)}), flush=True)
 
 
-def run_fp8_append_case(args, local):
-    """The bulk append into FP8 pools (every private-suffix token of the
-    batch-32 workload) timed alone (for profiling)."""
+def run_append_case(args, local, fp8=False):
+    """The bulk append of every private-suffix token of the batch-32 workload
+    (124,682 tokens) into bf16 pools, or quantized into FP8 pools, timed alone
+    (for profiling)."""
     import torch
     import block_paged_kv_gb300 as pkv
     dev = torch.device("cuda", local)
@@ -546,12 +547,18 @@ def run_fp8_append_case(args, local):
     slots = torch.from_numpy(pkv.slot_mapping_host(w.block_tables, w.num_blocks, rows, pos, 16)).to(dev)
     kn = torch.randn((n, 8, 128), dtype=torch.bfloat16, device=dev)
     vn = torch.randn_like(kn)
-    kp, vp = pkv.fp8_pools(w.num_blocks, 8, 128, dev)
-    ks, vs = float(gen.FP8_K_SCALE), float(gen.FP8_V_SCALE)
-    s = time_loop(torch, lambda: pkv.paged_kv_append(kp, vp, slots, kn, vn, k_scale=ks, v_scale=vs),
-                  args.steps, args.warmup)
-    b = 2 * n * 8 * 128 * (2 + 1) + 4 * n
-    print(json.dumps({"case": "fp8_append", "tokens": n, "us": round(s * 1e6, 2),
+    if fp8:
+        kp, vp = pkv.fp8_pools(w.num_blocks, 8, 128, dev)
+        ks, vs = float(gen.FP8_K_SCALE), float(gen.FP8_V_SCALE)
+        fn = lambda: pkv.paged_kv_append(kp, vp, slots, kn, vn, k_scale=ks, v_scale=vs)  # noqa: E731
+        b = 2 * n * 8 * 128 * (2 + 1) + 4 * n   # bf16 rows in, E4M3 codes out
+    else:
+        kp = torch.empty((w.num_blocks, 8, 16, 128), dtype=torch.bfloat16, device=dev)
+        vp = torch.empty_like(kp)
+        fn = lambda: pkv.paged_kv_append(kp, vp, slots, kn, vn)  # noqa: E731
+        b = 2 * 2 * n * 8 * 128 * 2 + 4 * n     # rows read and written, K and V
+    s = time_loop(torch, fn, args.steps, args.warmup)
+    print(json.dumps({"case": "fp8_append" if fp8 else "append", "tokens": n, "us": round(s * 1e6, 2),
                       "GB/s": round(b / s / 1e9, 1), "frac_of_hbm_peak": round(b / s / 1e9 / peaks()[0], 3)}),
           flush=True)
 
@@ -878,13 +885,13 @@ def main():
     ap.add_argument("--no-secondary", dest="secondary", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--case", choices=["step", "prefill", "fp8_decode", "fp8_append", "fp8_prefill",
-                                       "long_decode"],
+    ap.add_argument("--case", choices=["step", "prefill", "fp8_decode", "append", "fp8_append",
+                                       "fp8_prefill", "long_decode"],
                     default="step",
-                    help="step: the decode step (the contract line); prefill / fp8_decode / "
+                    help="step: the decode step (the contract line); prefill / fp8_decode / append / "
                          "fp8_append / fp8_prefill / long_decode: time the chunked prefill, the FP8 "
-                         "decode, the bulk FP8 append, the FP8 chunked prefill or the long-context "
-                         "full-attention decode alone (for profiling)")
+                         "decode, the bulk append into bf16 or FP8 pools, the FP8 chunked prefill "
+                         "or the long-context full-attention decode alone (for profiling)")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -898,7 +905,9 @@ def main():
     elif args.case == "fp8_decode":
         run_fp8_case(args, local)
     elif args.case == "fp8_append":
-        run_fp8_append_case(args, local)
+        run_append_case(args, local, fp8=True)
+    elif args.case == "append":
+        run_append_case(args, local)
     elif args.case == "fp8_prefill":
         run_fp8_prefill_case(args, local)
     elif args.case == "long_decode":
