@@ -487,15 +487,16 @@ def run_fp8_case(args, local):
                       "frac_of_hbm_peak": round(b / s / 1e9 / peaks()[0], 3)}), flush=True)
 
 
-def run_long_case(args, local):
-    """The full-attention group of the long-context workload (4 rows x 32768
-    tokens, 8 q / 1 kv head, head_dim 256) decoded alone, its split and merge
-    kernels timed by their own events (for profiling)."""
+def run_long_case(args, local, sliding=False):
+    """One group of the long-context workload (4 rows x 32768 tokens, 8 q / 1
+    kv head, head_dim 256) decoded alone: the full-attention group, or the
+    sliding-window group (window 512, expired blocks as -1 sentinels); its
+    split and merge kernels timed by their own events (for profiling)."""
     import torch
     import block_paged_kv_gb300 as pkv
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    w, _ = gen.long_two_groups()
+    w = gen.long_two_groups()[1 if sliding else 0]
 
     def up(a):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
@@ -507,10 +508,10 @@ def run_long_case(args, local):
     st = torch.zeros(1, dtype=torch.int32, device=dev)
     ml = int(w.seq_lens.max())
     ws = pkv.alloc_workspace(pkv.decode_workspace_size(w.batch, w.num_q_heads, w.num_kv_heads,
-                                                       w.head_dim, 16, ml, 0), dev)
+                                                       w.head_dim, 16, ml, w.window), dev)
 
     def decode():
-        pkv.paged_decode_attention(q, kp, vp, t, sl, 0, w.scale, out=out, workspace=ws,
+        pkv.paged_decode_attention(q, kp, vp, t, sl, w.window, w.scale, out=out, workspace=ws,
                                    max_seq_len=ml, status=st)
 
     for _ in range(args.warmup):
@@ -524,9 +525,13 @@ def run_long_case(args, local):
     n2, tc = pkv.profile_read(pkv.KERNEL_DECODE_COMBINE)
     pkv.profile_enable([])
     assert int(st.item()) == 0, f"device status {int(st.item())}"
-    b = workload_bytes(w)[0]
+    if w.window:
+        b = w.batch * min(w.window, ml) * 2 * w.num_kv_heads * w.head_dim * 2
+    else:
+        b = workload_bytes(w)[0]
     s = ts / max(n, 1) / 1e3
-    print(json.dumps({"case": "long_decode", "workload": w.name, "split_kernel_us": round(s * 1e6, 2),
+    print(json.dumps({"case": "sliding_decode" if sliding else "long_decode", "workload": w.name,
+                      "split_kernel_us": round(s * 1e6, 2),
                       "merge_kernel_us": round(tc / max(n2, 1) * 1e3, 2),
                       "split_GB/s": round(b / s / 1e9, 1),
                       "split_frac_of_hbm_peak": round(b / s / 1e9 / peaks()[0], 3)}), flush=True)
@@ -886,12 +891,13 @@ def main():
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--case", choices=["step", "prefill", "fp8_decode", "append", "fp8_append",
-                                       "fp8_prefill", "long_decode"],
+                                       "fp8_prefill", "long_decode", "sliding_decode"],
                     default="step",
                     help="step: the decode step (the contract line); prefill / fp8_decode / append / "
                          "fp8_append / fp8_prefill / long_decode: time the chunked prefill, the FP8 "
                          "decode, the bulk append into bf16 or FP8 pools, the FP8 chunked prefill "
-                         "or the long-context full-attention decode alone (for profiling)")
+                         "or the long-context full-attention or sliding-window decode alone (for "
+                         "profiling)")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -912,6 +918,8 @@ def main():
         run_fp8_prefill_case(args, local)
     elif args.case == "long_decode":
         run_long_case(args, local)
+    elif args.case == "sliding_decode":
+        run_long_case(args, local, sliding=True)
     else:
         run_pkv(args, rank, world, local)
 
