@@ -209,6 +209,20 @@ def _pool(k_pool: torch.Tensor, v_pool: torch.Tensor, k_scale: Optional[float] =
                  0.0, 0.0)
 
 
+def _on_device(t: Optional[torch.Tensor], name: str, device) -> None:
+    """Buffers the kernels read or write must live on the pools' GPU: the
+    pointer of a host tensor, or of another GPU's, would be dereferenced by
+    the kernel."""
+    if t is not None:
+        _require(t.is_cuda and t.device == device, f"{name} lives on {device}")
+
+
+def _status_ok(status: Optional[torch.Tensor], device) -> None:
+    if status is not None:
+        _on_device(status, "status", device)
+        _require(status.dtype == torch.int32 and status.numel() >= 1, "status is an int32 word")
+
+
 def _i32_dev(t: torch.Tensor, name: str, device) -> torch.Tensor:
     _require(t.dtype == torch.int32 and t.is_contiguous() and t.device == device,
              f"{name} is a contiguous int32 tensor on {device}")
@@ -227,6 +241,12 @@ class PrefixDesc:
     def _c(self) -> _Prefix:
         return _Prefix(self.num_groups, self.max_group_rows, self.max_prefix_blocks,
                        self.group_of_row.data_ptr(), self.prefix_blocks.data_ptr())
+
+
+def _prefix_ok(prefix: Optional[PrefixDesc], device) -> None:
+    if prefix is not None:
+        _i32_dev(prefix.group_of_row, "prefix.group_of_row", device)
+        _i32_dev(prefix.prefix_blocks, "prefix.prefix_blocks", device)
 
 
 def prefix_groups_host(block_tables: np.ndarray, seq_lens: np.ndarray,
@@ -284,7 +304,11 @@ def paged_kv_append(k_pool: torch.Tensor, v_pool: torch.Tensor, slot_mapping: to
     act = _act_dtype(k_pool.dtype)
     _require(k_new.dtype == act and v_new.dtype == act, "new rows match the pool dtype (bf16 for FP8)")
     _require(k_new.is_contiguous() and v_new.is_contiguous(), "new rows are contiguous")
-    _require(slot_mapping.shape[0] == k_new.shape[0], "one slot per new token")
+    _require(slot_mapping.dim() == 1 and slot_mapping.shape[0] == k_new.shape[0],
+             "one slot per new token")
+    _on_device(k_new, "k_new", dev)
+    _on_device(v_new, "v_new", dev)
+    _status_ok(status, dev)
     _check("paged_kv_append", _lib.paged_kv_append(
         ctypes.byref(pool), slot_mapping.data_ptr(), k_new.shape[0], k_new.data_ptr(),
         v_new.data_ptr(), _ptr(status), _stream(dev)))
@@ -333,6 +357,10 @@ def paged_decode_attention(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.
     if out is None:
         out = torch.empty_like(q)
     _require(out.shape == q.shape and out.dtype == q.dtype and out.is_contiguous(), "out matches q")
+    _on_device(out, "out", dev)
+    _on_device(workspace, "workspace", dev)
+    _status_ok(status, dev)
+    _prefix_ok(prefix, dev)
     need = decode_workspace_size(B, hq, pool.num_kv_heads, D, pool.block_size, max_seq_len, window,
                                  prefix)
     if workspace is None:
@@ -377,6 +405,10 @@ def paged_prefill_chunk_attention(q: torch.Tensor, cu_q_lens: torch.Tensor, k_po
         max_seq_len = width * pool.block_size
     if out is None:
         out = torch.empty_like(q)
+    _require(out.shape == q.shape and out.dtype == q.dtype and out.is_contiguous(), "out matches q")
+    _on_device(out, "out", dev)
+    _on_device(workspace, "workspace", dev)
+    _status_ok(status, dev)
     hq = q.shape[1]
     need = prefill_workspace_size(B, hq, pool.num_kv_heads, pool.head_dim, pool.block_size,
                                   max_q_len, max_seq_len, window)
@@ -469,6 +501,7 @@ def _group_c(g: DecodeGroup) -> _Group:
         g.out = torch.empty_like(g.q)
     _require(g.out.shape == g.q.shape and g.out.dtype == g.q.dtype and g.out.is_contiguous(),
              "out matches q")
+    _on_device(g.out, "out", dev)
     width = g.block_tables.shape[1]
     msl = g.max_seq_len if g.max_seq_len is not None else width * pool.block_size
     return _Group(g.q.data_ptr(), g.out.data_ptr(), pool, g.block_tables.data_ptr(), width,
@@ -487,6 +520,9 @@ def paged_decode_attention_groups(groups, workspace: Optional[torch.Tensor] = No
     B, hq = groups[0].q.shape[0], groups[0].q.shape[1]
     _require(all(g.q.shape[:2] == (B, hq) for g in groups), "every group has the same batch and q heads")
     dev = groups[0].k_pool.device
+    _require(all(g.k_pool.device == dev for g in groups), "every group's pools on one GPU")
+    _on_device(workspace, "workspace", dev)
+    _status_ok(status, dev)
     need = int(_lib.paged_decode_groups_workspace_size(arr, len(groups), B, hq))
     if workspace is None:
         workspace = alloc_workspace(need, dev)
@@ -529,6 +565,9 @@ def paged_decode_attention_no_alloc(q: torch.Tensor, k_pool: torch.Tensor, v_poo
     _require(block_tables.dim() == 2 and block_tables.shape[0] == B and seq_lens.shape == (B,),
              "block_tables [B, max_blocks], seq_lens [B]")
     _require(out.shape == q.shape and out.dtype == q.dtype and out.is_contiguous(), "out matches q")
+    _on_device(out, "out", dev)
+    _status_ok(status, dev)
+    _prefix_ok(prefix, dev)
     width = block_tables.shape[1]
     if max_seq_len is None:
         max_seq_len = width * pool.block_size

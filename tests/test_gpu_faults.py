@@ -92,3 +92,26 @@ def test_host_errors(pkv):
         pkv.paged_decode_attention(d.q, d.k_pool, d.v_pool, d.tables, d.seq_lens, 16, w.scale,
                                    prefix=desc)
     assert e.value.code == pkv.PKV_ERR_UNSUPPORTED
+
+
+def test_buffers_off_the_gpu_rejected_before_launch(pkv):
+    # a host tensor's pointer handed to a kernel would be dereferenced on the
+    # device: the binding refuses such buffers before anything is enqueued
+    w = gen.decode_workload(seed=25, dtype="bf16", num_q_heads=4, num_kv_heads=2, head_dim=128,
+                            context_lens=[30])
+    d = Dev(w)
+    n0 = pkv.launch_count()
+    for kw in ({"workspace": torch.empty(1 << 20, dtype=torch.uint8)},
+               {"out": torch.empty(tuple(d.q.shape), dtype=d.q.dtype)},
+               {"status": torch.zeros(1, dtype=torch.int32)},
+               {"status": torch.zeros(1, dtype=torch.int64, device="cuda")}):
+        with pytest.raises(ValueError):
+            pkv.paged_decode_attention(d.q, d.k_pool, d.v_pool, d.tables, d.seq_lens, 0, w.scale,
+                                       **kw)
+    slots = torch.zeros(w.k_new.shape[0], dtype=torch.int32, device="cuda")
+    with pytest.raises(ValueError):
+        pkv.paged_kv_append(d.k_pool, d.v_pool, slots, d.k_new.cpu(), d.v_new)
+    with pytest.raises(ValueError):
+        pkv.paged_decode_attention_no_alloc(d.q, d.k_pool, d.v_pool, d.tables, d.seq_lens, 0,
+                                            w.scale, torch.empty(tuple(d.q.shape), dtype=d.q.dtype))
+    assert pkv.launch_count() == n0
