@@ -136,10 +136,13 @@ DecodePlan make_plan(int32_t batch, int32_t hq, int32_t hkv, int32_t D, int32_t 
     pl.prefix_chunks = 0;
     pl.n_prefix_ctas = 0;
     if (prefix != nullptr && prefix->num_groups > 0 && prefix->max_prefix_blocks > 0) {
-        // The prefix cut aims at about one CTA per SM for the bf16 kernel (64
-        // (row, head) pairs per CTA, 32 at head_dim 256); it does not depend
-        // on the dtype, so the workspace size does not either.  The f32 kernel
-        // takes 16 pairs per CTA.
+        // The prefix cut (blocks per prefix split) is sized for a nominal 64
+        // (row, head) pairs per CTA (32 at head_dim 256), about one CTA per SM
+        // at that size, whatever the dtype, so that the workspace size does
+        // not depend on the dtype.  The row chunks then follow the kernel: the
+        // bf16 and FP8 kernels take four warp tiles of 8 pairs (G <= 8) or 16
+        // per CTA, so at G <= 8 the prefix CTAs come to about two per SM; the
+        // f32 kernel takes 16 pairs per CTA.
         const int64_t rows_pairs = static_cast<int64_t>(prefix->max_group_rows) * G;
         const int64_t pairs_bf16 = D == 256 ? kPrefixPairsPerCta / 2 : kPrefixPairsPerCta;
         const int64_t chunks_bf16 = ceil_div64(rows_pairs, pairs_bf16);
