@@ -90,3 +90,24 @@ def test_argument_checks_before_launch(pkv):
     assert lib.paged_decode_attention(16, 4, ctypes.byref(pool32), 16, 4, 16, 1, 64, 0, 1.0, 16,
                                       256, 1 << 20, None, None, None) == pkv.PKV_ERR_UNSUPPORTED
     assert lib.pkv_status_string(pkv.PKV_ERR_WORKSPACE).decode() == "workspace too small or misaligned"
+
+
+def test_plain_c_caller(pkv, tmp_path):
+    """include/pkv.h compiles as C99 and a C program linked against the library
+    runs its host-side entry points (tests/c_abi_host.c) without torch."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not found")
+    libdir = os.path.dirname(pkv.LIB_PATH)
+    exe = str(tmp_path / "c_abi_host")
+    build = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror",
+                            "-I", os.path.join(ROOT, "include"),
+                            os.path.join(ROOT, "tests", "c_abi_host.c"),
+                            "-L", libdir, "-lpkv", f"-Wl,-rpath,{libdir}", "-o", exe],
+                           capture_output=True, text=True)
+    assert build.returncode == 0, build.stderr
+    run = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert run.returncode == 0, run.stderr
+    assert "c_abi_host: ok" in run.stdout
