@@ -103,6 +103,8 @@ _lib.paged_decode_attention_no_alloc.restype = ctypes.c_int
 NO_ALLOC_SCRATCH_BYTES = 16 << 20
 _u64p = ctypes.POINTER(ctypes.c_uint64)
 _i32p = ctypes.POINTER(ctypes.c_int32)
+_lib.pkv_slot_mapping_check_host.argtypes = [_vp, _i32, _i32, _i32, _i32p]
+_lib.pkv_slot_mapping_check_host.restype = ctypes.c_int
 _lib.pkv_allocator_create.argtypes = [_i32, _i32, _i32]
 _lib.pkv_allocator_create.restype = _vp
 _lib.pkv_allocator_destroy.argtypes = [_vp]
@@ -130,7 +132,8 @@ KERNEL_APPEND, KERNEL_DECODE_PREFIX, KERNEL_DECODE_SPLIT, KERNEL_DECODE_COMBINE,
 
 EXPORTED = ["paged_kv_append", "paged_decode_workspace_size", "paged_decode_attention",
             "paged_prefill_workspace_size", "paged_prefill_chunk_attention", "pkv_status_string",
-            "pkv_slot_mapping_host", "pkv_prefix_groups_host", "pkv_set_decode_split_blocks",
+            "pkv_slot_mapping_host", "pkv_slot_mapping_check_host", "pkv_prefix_groups_host",
+            "pkv_set_decode_split_blocks",
             "pkv_decode_plan", "pkv_version", "pkv_profile_enable", "pkv_profile_mask", "pkv_profile_read",
             "pkv_launch_count", "paged_decode_attention_no_alloc", "paged_decode_groups_workspace_size",
             "paged_decode_attention_groups", "pkv_allocator_create",
@@ -287,6 +290,22 @@ def slot_mapping_host(block_tables: np.ndarray, num_blocks: int, rows: np.ndarra
                                       out.ctypes.data)
     _check("pkv_slot_mapping_host", code)
     return out
+
+
+def check_slot_mapping(slots: np.ndarray, num_blocks: int, block_size: int) -> None:
+    """Debug check before an append (library helper, host arrays): every slot
+    >= 0 inside the pool and no slot named by two tokens (their stores would
+    race).  Raises ValueError naming the first token at fault."""
+    s = np.ascontiguousarray(slots, dtype=np.int32)
+    bad = ctypes.c_int32(-1)
+    code = _lib.pkv_slot_mapping_check_host(s.ctypes.data, s.shape[0], num_blocks, block_size,
+                                            ctypes.byref(bad))
+    if code != PKV_OK:
+        if bad.value < 0:
+            raise ValueError("check_slot_mapping: invalid arguments")
+        slot = int(s[bad.value])
+        what = "lies past the pool" if slot >= num_blocks * block_size else "repeats an earlier token's"
+        raise ValueError(f"check_slot_mapping: token {bad.value}'s slot {slot} {what}")
 
 
 def paged_kv_append(k_pool: torch.Tensor, v_pool: torch.Tensor, slot_mapping: torch.Tensor,

@@ -1,7 +1,8 @@
-// Host helpers of the C ABI: slot mapping and shared-prefix group derivation
-// from block tables.  Plain C++ on host arrays.
+// Host helpers of the C ABI: slot mapping, its debug check and shared-prefix
+// group derivation from block tables.  Plain C++ on host arrays.
 #include <algorithm>
 #include <unordered_map>
+#include <unordered_set>
 #include <vector>
 
 #include "pkv.h"
@@ -33,6 +34,27 @@ extern "C" pkv_status pkv_slot_mapping_host(const int32_t *block_tables, int32_t
         all_ok = all_ok && slot >= 0;
     }
     return all_ok ? PKV_OK : PKV_ERR_INVALID_ARG;
+}
+
+extern "C" pkv_status pkv_slot_mapping_check_host(const int32_t *slots, int32_t n,
+                                                  int32_t num_blocks, int32_t block_size,
+                                                  int32_t *first_bad)
+{
+    if (first_bad != nullptr) *first_bad = -1;
+    if (n < 0 || num_blocks <= 0 || block_size <= 0 || (n > 0 && slots == nullptr))
+        return PKV_ERR_INVALID_ARG;
+    const int64_t cap = static_cast<int64_t>(num_blocks) * block_size;
+    std::unordered_set<int32_t> seen;
+    seen.reserve(static_cast<size_t>(n));
+    for (int32_t i = 0; i < n; ++i) {
+        const int32_t s = slots[i];
+        if (s < 0) continue;  // skipped by the append
+        if (static_cast<int64_t>(s) >= cap || !seen.insert(s).second) {
+            if (first_bad != nullptr) *first_bad = i;
+            return PKV_ERR_INVALID_ARG;
+        }
+    }
+    return PKV_OK;
 }
 
 extern "C" int32_t pkv_prefix_groups_host(const int32_t *block_tables, int32_t max_blocks_per_seq,

@@ -298,6 +298,21 @@ pkv_status pkv_slot_mapping_host(const int32_t *block_tables, int32_t max_blocks
                                  int32_t *slots_out);
 
 /*
+ * Host helper, a debug check of a slot mapping before an append: every slot
+ * >= 0 of slots[0 .. n-1] lies inside the pool (< num_blocks * block_size)
+ * and no two tokens name the same slot.  Two tokens written to one slot would
+ * leave whichever store lands last, a race that breaks the run-to-run
+ * determinism the mlx-bun notes require of the batched kernels (section
+ * "Risks": no atomics, deterministic).  The append itself does not look for
+ * repeats.  Returns PKV_OK, or PKV_ERR_INVALID_ARG with *first_bad (may be
+ * NULL) the index of the first token at fault in order (for a repeat, the later
+ * token of the pair); *first_bad is -1 when the arguments themselves are
+ * invalid or nothing is wrong.  Host arrays; allocates host scratch.
+ */
+pkv_status pkv_slot_mapping_check_host(const int32_t *slots, int32_t n, int32_t num_blocks,
+                                       int32_t block_size, int32_t *first_bad);
+
+/*
  * Host helper: shared-prefix groups read off the block tables (host arrays).
  * Rows whose first entry is the same physical block form a group when there
  * are at least two of them; the group's prefix is the longest run of leading

@@ -31,6 +31,14 @@ static void slot_mapping(void)
           PKV_ERR_INVALID_ARG);
     CHECK(slots[0] == 7 * 16 + 4 && slots[1] == 5 * 16 + 3 && slots[2] == 3 * 16 && slots[3] == -1);
     CHECK(pkv_slot_mapping_host(&tables[0][0], 2, 2, 8, rows, pos, 3, 16, slots) == PKV_OK);
+    {
+        /* the debug check: slots 116, 83, 48 are distinct and inside the pool */
+        int32_t bad = 7;
+        const int32_t twice[3] = {48, -1, 48};
+        CHECK(pkv_slot_mapping_check_host(slots, 3, 8, 16, &bad) == PKV_OK && bad == -1);
+        CHECK(pkv_slot_mapping_check_host(twice, 3, 8, 16, &bad) == PKV_ERR_INVALID_ARG &&
+              bad == 2);
+    }
 }
 
 static void prefix_groups(void)

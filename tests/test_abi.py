@@ -111,3 +111,41 @@ def test_plain_c_caller(pkv, tmp_path):
     run = subprocess.run([exe], capture_output=True, text=True, timeout=60)
     assert run.returncode == 0, run.stderr
     assert "c_abi_host: ok" in run.stdout
+
+
+def _first_fault(slots, cap):
+    seen = set()
+    for i, s in enumerate(int(x) for x in slots):
+        if s < 0:
+            continue
+        if s >= cap or s in seen:
+            return i
+        seen.add(s)
+    return None
+
+
+def test_slot_mapping_check(pkv):
+    # the appends of the workloads: slots inside the pool, none repeated
+    for w in _workloads():
+        slots = pkv.slot_mapping_host(w.block_tables, w.num_blocks, w.new_rows, w.new_pos,
+                                      w.block_size)
+        pkv.check_slot_mapping(slots, w.num_blocks, w.block_size)
+    # seeded slot arrays with planted repeats and out-of-pool slots: the first
+    # token at fault, in order, is the one named
+    nb, bs = 8, 16
+    for seed in range(40):
+        s = gen.uniform_ints(700 + seed, "slots", 24, -2, nb * bs + 3).astype(np.int32)
+        want = _first_fault(s, nb * bs)
+        if want is None:
+            pkv.check_slot_mapping(s, nb, bs)
+            continue
+        with pytest.raises(ValueError, match=f"token {want}'s slot {int(s[want])} "):
+            pkv.check_slot_mapping(s, nb, bs)
+    # negative slots are skipped by the append, so they may repeat
+    pkv.check_slot_mapping(np.array([-1, 5, -1, 6], np.int32), nb, bs)
+    with pytest.raises(ValueError, match="token 2's slot 5 repeats"):
+        pkv.check_slot_mapping(np.array([5, 7, 5], np.int32), nb, bs)
+    with pytest.raises(ValueError, match="past the pool"):
+        pkv.check_slot_mapping(np.array([3, nb * bs], np.int32), nb, bs)
+    with pytest.raises(ValueError, match="invalid arguments"):
+        pkv.check_slot_mapping(np.array([3], np.int32), 0, bs)
