@@ -145,7 +145,8 @@ def committed_traffic(sha):
     return d.get("dram_bytes_per_launch_full_workload")
 
 
-PROF_EVERY = 16  # decode launches timed by events: one step in this many
+PROF_EVERY = 4     # roofline loop: one decode launch in this many carries events
+ROOF_SAMPLES = 64  # roofline loop: timed decode launches (the median is reported)
 
 
 def barrier(world):
@@ -220,28 +221,36 @@ def run_pkv(args, rank, world, local):
         clocks.start()
     stream = torch.cuda.current_stream(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    pkv.profile_enable([])  # clear the records
     n0 = pkv.launch_count()
     barrier(world)
     torch.cuda.synchronize()
     e0.record(stream)
-    # the decode kernel's own duration is sampled on every PROF_EVERY-th step:
-    # the events around a launch cost that step its overlap with the kernels
-    # before and after it (programmatic dependent launch), so timing every
-    # launch would slow the step being measured
-    for i in range(args.steps):
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    launches = pkv.launch_count() - n0
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+
+    # the decode kernel's own duration, for the roofline: a loop of its own
+    # right after the timed steps, of ROOF_SAMPLES timed launches (whatever
+    # --steps is), each the decode launch of one step among unsampled ones.
+    # The events around a launch cost it its overlap with its neighbours
+    # (programmatic dependent launch), so only one step in PROF_EVERY carries
+    # them; the median launch is reported
+    pkv.profile_enable([])  # clear the records
+    for i in range(ROOF_SAMPLES * PROF_EVERY):
         sample = i % PROF_EVERY == 0
         if sample:
             pkv.profile_mask([pkv.KERNEL_DECODE_SPLIT])
         step()
         if sample:
             pkv.profile_mask([])
-    e1.record(stream)
     torch.cuda.synchronize()
-    barrier(world)
-    launches = pkv.launch_count() - n0
-    ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
-    nsplit, split_ms = pkv.profile_read(pkv.KERNEL_DECODE_SPLIT)
+    split_times = pkv.profile_times(pkv.KERNEL_DECODE_SPLIT)
+    nsplit = len(split_times)
+    split_med_ms = statistics.median(split_times)
     clk = clocks.stop() if rank == 0 else None
     assert int(status.item()) == 0, f"device status {int(status.item())}"
 
@@ -273,7 +282,9 @@ def run_pkv(args, rank, world, local):
     bufs = [(*input_views(raw), torch.empty_like(out)) for raw in raws]
     h2d = total
     d2h = out_h[0].numel() * out_h[0].element_size()
-    e2e_steps = max(1, min(args.steps, 1000))
+    # at least 200 end-to-end steps (about 20 ms), so that the pipeline's
+    # fill and drain do not weigh on a short --steps run
+    e2e_steps = max(200, min(args.steps, 1000))
     cs = torch.cuda.Stream(dev)
     ev_in = [torch.cuda.Event() for _ in range(2)]
     ev_done = [torch.cuda.Event() for _ in range(2)]
@@ -322,7 +333,7 @@ def run_pkv(args, rank, world, local):
     peak, peak_kind = peaks()
     t_step = ms / args.steps / 1e3
     value = job_rate(bytes_step, world, ms, args.steps) / 1e9
-    split_avg_s = split_ms / max(nsplit, 1) / 1e3
+    split_avg_s = split_med_ms / 1e3
     achieved = bytes_step / split_avg_s / 1e9
     sha = kernel_source_sha()
     line = {
@@ -330,12 +341,7 @@ def run_pkv(args, rank, world, local):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) cast to bf16; shuffled block ids)",
-        "config": {"workload": w.name, "batch": w.batch, "q_heads": w.num_q_heads,
-                   "kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
-                   "shared_prefix_tokens": w.shared_prefix_tokens, "suffix_tokens": "uniform 0..7168",
-                   "step": "append 1 token/row + shared-prefix paged decode",
-                   "kv_bytes_per_step": bytes_step, "parallelism": f"replicas x{world} (rows shard)",
-                   "l2": "no flush: 0.47 GB of K/V per step exceeds the 129 MB L2"},
+        "config": contract_config(w, world),
         "pct_of_8TBps": round(100 * value / world / NOMINAL_HBM_GBS, 1),
         "tok_per_s": round(job_rate(w.batch, world, ms, args.steps), 1),
         "clocks": clk,
@@ -350,7 +356,11 @@ def run_pkv(args, rank, world, local):
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 3), "peak_source": f"{peak_kind} hbm_gbs",
                      "traffic": committed_traffic(sha), "algorithmic_bytes_per_launch": bytes_step,
-                     "avg_launch_us": round(split_avg_s * 1e6, 2), "launches_timed": nsplit,
+                     "avg_launch_us": round(split_avg_s * 1e6, 2),
+                     "launch_us_stat": "median of the timed launches", "launches_timed": nsplit,
+                     "launch_us_mean": round(1e3 * statistics.mean(split_times), 2),
+                     "launch_us_min": round(1e3 * min(split_times), 2),
+                     "launch_us_max": round(1e3 * max(split_times), 2),
                      "source_sha": sha},
     }
     if secondary is not None:
@@ -735,13 +745,13 @@ def secondary_measurements(args, pkv, torch, dev):
     torch.cuda.synchronize()
     assert int(st.item()) == 0, f"device status {int(st.item())}"
     s_step = e0.elapsed_time(e1) / steps / 1e3
-    nsp, tsp = pkv.profile_read(pkv.KERNEL_DECODE_SPLIT)
-    s_split = tsp / max(nsp, 1) / 1e3
+    s_split = statistics.median(pkv.profile_times(pkv.KERNEL_DECODE_SPLIT)) / 1e3
     peak = peaks()[0]
     res["fp8_decode_b32"] = {"workload": w.name.replace("bf16", "fp8"), "step_us": round(s_step * 1e6, 2),
                              "tok_per_s": round(w.batch / s_step, 1),
                              "step_GB/s": round(b / s_step / 1e9, 1),
                              "split_kernel_us": round(s_split * 1e6, 2),
+                             "split_kernel_us_stat": f"median of {steps // PROF_EVERY} timed launches",
                              "split_kernel_GB/s": round(b / s_split / 1e9, 1),
                              "split_kernel_frac_of_hbm_peak": round(b / s_split / 1e9 / peak, 3),
                              "kv_bytes": b, "scales": [float(gen.FP8_K_SCALE), float(gen.FP8_V_SCALE)],
@@ -785,53 +795,113 @@ def _oracle_setup(w):
     return orc, kp, vp
 
 
-def _oracle_rate(w, orc, kp, vp, budget_s, rows_order):
-    """Oracle time for sampled rows (all q heads each) until about budget_s;
-    the full step's time is extrapolated by attended keys."""
+def host_cpu():
+    """(logical cores, CPU model string) of this host."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if model is None:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for line in f:
+                    if line.lower().startswith(("model name", "cpu part")):
+                        model = line.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    return os.cpu_count() or 1, model or "unknown"
+
+
+def _oracle_rate(w, orc, kp, vp, budget_s, rows_order, threads=1):
+    """Oracle rate for whole rows (all q heads each) taken in the given order,
+    again from the start when every row is done, until about budget_s of wall
+    time; the full step's time is extrapolated by attended keys.  With
+    threads > 1 that many host threads each decode whole rows at once (the
+    oracle's C calls release the interpreter lock), one row per call."""
+    import threading
     bytes_step, _ = workload_bytes(w)
     full_keys = float(np.sum(w.seq_lens.astype(np.int64))) * w.num_q_heads
-    # whole rows in the given order, again from the start when every row is
-    # done (a fast host finishes the whole step inside the budget)
-    done_keys, spent, rows = 0.0, 0.0, []
-    while spent < budget_s:
-        for r in rows_order:
+    lock = threading.Lock()
+    state = {"next": 0, "keys": 0.0, "rows": []}
+    t_start = time.perf_counter()
+
+    def worker():
+        while True:
+            with lock:
+                if time.perf_counter() - t_start >= budget_s:
+                    return
+                r = int(rows_order[state["next"] % len(rows_order)])
+                state["next"] += 1
             pairs = np.array([[r, h] for h in range(w.num_q_heads)], dtype=np.int32)
-            t0 = time.perf_counter()
             orc.decode(w.q, kp, vp, w.dtype, w.block_tables, w.seq_lens, w.window, w.scale,
                        pairs=pairs)
-            spent += time.perf_counter() - t0
-            done_keys += float(w.seq_lens[r]) * w.num_q_heads
-            rows.append(int(r))
-            if spent >= budget_s:
-                break
-    t_full = spent * full_keys / done_keys
-    return bytes_step / t_full / 1e9, rows, spent
+            with lock:
+                state["keys"] += float(w.seq_lens[r]) * w.num_q_heads
+                state["rows"].append(r)
+
+    if threads == 1:
+        worker()
+    else:
+        pool = [threading.Thread(target=worker) for _ in range(threads)]
+        for t in pool:
+            t.start()
+        for t in pool:
+            t.join()
+    spent = time.perf_counter() - t_start
+    t_full = spent * full_keys / state["keys"]
+    return bytes_step / t_full / 1e9, state["rows"], spent
 
 
 def cpu_baseline(w, budget_s=10.0):
+    """The oracle timed on this host: one thread, then every logical core."""
     orc, kp, vp = _oracle_setup(w)
     order = gen.permutation(77, "cpu_rows", w.batch)
+    nproc, model = host_cpu()
     value, rows, spent = _oracle_rate(w, orc, kp, vp, budget_s, order)
+    value_all, rows_all, spent_all = _oracle_rate(w, orc, kp, vp, budget_s, order, threads=nproc)
     passes = len(rows) / w.batch
     return {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"decode of {len(rows)} whole rows ({passes:.2f} passes over the "
                       f"{w.batch} rows in the order {[int(r) for r in order]}; all "
                       f"{w.num_q_heads} q heads each; {spent:.1f} s single-threaded); "
-                      "full-step time extrapolated by attended keys"}
+                      "full-step time extrapolated by attended keys",
+            "value_all_cores": round(value_all, 4), "cores_all": nproc,
+            "sample_all_cores": f"{len(rows_all)} whole rows in the same order on {nproc} threads "
+                                f"(one row per oracle call), {spent_all:.1f} s of wall time",
+            "nproc": nproc, "cpu_model": model}
+
+
+def contract_config(w, world):
+    """The workload description both arms print (the same keys and values)."""
+    return {"workload": w.name, "batch": w.batch, "q_heads": w.num_q_heads,
+            "kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
+            "shared_prefix_tokens": w.shared_prefix_tokens, "suffix_tokens": "uniform 0..7168",
+            "step": "append 1 token/row + shared-prefix paged decode",
+            "kv_bytes_per_step": workload_bytes(w)[0], "parallelism": f"replicas x{world} (rows shard)",
+            "l2": "no flush: 0.47 GB of K/V per step exceeds the 129 MB L2"}
 
 
 def run_reference(args, rank, world):
+    """The oracle as the reference arm: every host core decodes whole rows of
+    the batch-32 workload for a bounded time per step."""
     if rank != 0:
         return
     w = gen.shared_prefix_b32()
     orc, kp, vp = _oracle_setup(w)
     order = gen.permutation(77, "cpu_rows", w.batch)
+    nproc, model = host_cpu()
     total_steps = args.steps + args.warmup
     per_step = max(0.05, min(5.0, 120.0 / max(total_steps, 1)))
     vals = []
     for i in range(total_steps):
         rot = np.roll(order, -i)
-        v, rows, spent = _oracle_rate(w, orc, kp, vp, per_step, rot)
+        v, rows, spent = _oracle_rate(w, orc, kp, vp, per_step, rot, threads=nproc)
         if i >= args.warmup:
             vals.append((v, spent, rows))
     value = statistics.median(v for v, _, _ in vals)
@@ -840,12 +910,12 @@ def run_reference(args, rank, world):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(ms_step, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "batch": w.batch, "q_heads": w.num_q_heads,
-                       "kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
-                       "step": "oracle decode (CPU, IEEE double), bounded sample per step"},
-            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": f"each step: whole rows (all q heads) for about {per_step:.2f} s; "
-                                       "full-step time extrapolated by attended keys"},
+            "config": contract_config(w, world),
+            "arm": "the CPU oracle (IEEE double), bounded sample of whole rows per step",
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": nproc, "kind": "oracle",
+                             "cpu_model": model,
+                             "sample": f"each step: whole rows (all q heads) on {nproc} threads for about "
+                                       f"{per_step:.2f} s; full-step time extrapolated by attended keys"},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)

@@ -14,6 +14,7 @@ tokens appended this step.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 from dataclasses import dataclass
@@ -86,6 +87,8 @@ _lib.pkv_prefix_groups_host.argtypes = [_vp, _i32, _vp, _i32, _i32, _vp, _vp]
 _lib.pkv_prefix_groups_host.restype = _i32
 _lib.pkv_set_decode_split_blocks.argtypes = [_i32]
 _lib.pkv_set_decode_split_blocks.restype = _i32
+_lib.pkv_set_wait_drill.argtypes = [ctypes.c_uint64, ctypes.c_uint32]
+_lib.pkv_set_wait_drill.restype = ctypes.c_int
 _lib.pkv_decode_plan.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32, _i32,
                                  ctypes.POINTER(_i32)]
 _lib.pkv_decode_plan.restype = _i32
@@ -96,6 +99,8 @@ _lib.pkv_profile_mask.argtypes = [ctypes.c_uint32]
 _lib.pkv_profile_mask.restype = ctypes.c_int
 _lib.pkv_profile_read.argtypes = [_i32, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_double)]
 _lib.pkv_profile_read.restype = ctypes.c_int
+_lib.pkv_profile_times.argtypes = [_i32, _vp, ctypes.c_int64, ctypes.POINTER(ctypes.c_int64)]
+_lib.pkv_profile_times.restype = ctypes.c_int
 _lib.pkv_launch_count.restype = ctypes.c_int64
 _lib.paged_decode_attention_no_alloc.argtypes = [_vp, _i32, _PP, _vp, _i32, _vp, _i32, _i32, _i32,
                                                  ctypes.c_float, _vp, _XP, _vp, _vp]
@@ -133,8 +138,8 @@ KERNEL_APPEND, KERNEL_DECODE_PREFIX, KERNEL_DECODE_SPLIT, KERNEL_DECODE_COMBINE,
 EXPORTED = ["paged_kv_append", "paged_decode_workspace_size", "paged_decode_attention",
             "paged_prefill_workspace_size", "paged_prefill_chunk_attention", "pkv_status_string",
             "pkv_slot_mapping_host", "pkv_slot_mapping_check_host", "pkv_prefix_groups_host",
-            "pkv_set_decode_split_blocks",
-            "pkv_decode_plan", "pkv_version", "pkv_profile_enable", "pkv_profile_mask", "pkv_profile_read",
+            "pkv_set_decode_split_blocks", "pkv_set_wait_drill",
+            "pkv_decode_plan", "pkv_version", "pkv_profile_enable", "pkv_profile_mask", "pkv_profile_read", "pkv_profile_times",
             "pkv_launch_count", "paged_decode_attention_no_alloc", "paged_decode_groups_workspace_size",
             "paged_decode_attention_groups", "pkv_allocator_create",
             "pkv_allocator_destroy", "pkv_allocator_begin", "pkv_allocator_find_cached_prefix",
@@ -186,6 +191,14 @@ def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
 
 def _stream(device: torch.device) -> int:
     return torch.cuda.current_stream(device).cuda_stream
+
+
+def _on(device: torch.device):
+    """Make `device` current for a library call (the library plans for, and
+    takes scratch from, the current device); a no-op when it already is."""
+    if device.index is None or torch.cuda.current_device() == device.index:
+        return contextlib.nullcontext()
+    return torch.cuda.device(device)
 
 
 def _require(cond: bool, msg: str) -> None:
@@ -328,9 +341,10 @@ def paged_kv_append(k_pool: torch.Tensor, v_pool: torch.Tensor, slot_mapping: to
     _on_device(k_new, "k_new", dev)
     _on_device(v_new, "v_new", dev)
     _status_ok(status, dev)
-    _check("paged_kv_append", _lib.paged_kv_append(
-        ctypes.byref(pool), slot_mapping.data_ptr(), k_new.shape[0], k_new.data_ptr(),
-        v_new.data_ptr(), _ptr(status), _stream(dev)))
+    with _on(dev):
+        _check("paged_kv_append", _lib.paged_kv_append(
+            ctypes.byref(pool), slot_mapping.data_ptr(), k_new.shape[0], k_new.data_ptr(),
+            v_new.data_ptr(), _ptr(status), _stream(dev)))
 
 
 def decode_workspace_size(batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
@@ -380,15 +394,17 @@ def paged_decode_attention(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.
     _on_device(workspace, "workspace", dev)
     _status_ok(status, dev)
     _prefix_ok(prefix, dev)
-    need = decode_workspace_size(B, hq, pool.num_kv_heads, D, pool.block_size, max_seq_len, window,
-                                 prefix)
-    if workspace is None:
-        workspace = alloc_workspace(need, dev)
-    px = ctypes.byref(prefix._c()) if prefix is not None else None
-    _check("paged_decode_attention", _lib.paged_decode_attention(
-        q.data_ptr(), hq, ctypes.byref(pool), block_tables.data_ptr(), width, seq_lens.data_ptr(),
-        B, max_seq_len, window, float(scale), out.data_ptr(), workspace.data_ptr(),
-        workspace.numel() * workspace.element_size(), px, _ptr(status), _stream(dev)))
+    with _on(dev):  # the plan reads the SM count of the current device
+        need = decode_workspace_size(B, hq, pool.num_kv_heads, D, pool.block_size, max_seq_len,
+                                     window, prefix)
+        if workspace is None:
+            workspace = alloc_workspace(need, dev)
+        px = ctypes.byref(prefix._c()) if prefix is not None else None
+        _check("paged_decode_attention", _lib.paged_decode_attention(
+            q.data_ptr(), hq, ctypes.byref(pool), block_tables.data_ptr(), width,
+            seq_lens.data_ptr(), B, max_seq_len, window, float(scale), out.data_ptr(),
+            workspace.data_ptr(), workspace.numel() * workspace.element_size(), px, _ptr(status),
+            _stream(dev)))
     return out
 
 
@@ -429,15 +445,16 @@ def paged_prefill_chunk_attention(q: torch.Tensor, cu_q_lens: torch.Tensor, k_po
     _on_device(workspace, "workspace", dev)
     _status_ok(status, dev)
     hq = q.shape[1]
-    need = prefill_workspace_size(B, hq, pool.num_kv_heads, pool.head_dim, pool.block_size,
-                                  max_q_len, max_seq_len, window)
-    if workspace is None:
-        workspace = alloc_workspace(need, dev)
-    _check("paged_prefill_chunk_attention", _lib.paged_prefill_chunk_attention(
-        q.data_ptr(), cu_q_lens.data_ptr(), hq, ctypes.byref(pool), block_tables.data_ptr(),
-        width, seq_lens.data_ptr(), B, max_q_len, max_seq_len, window, float(scale),
-        out.data_ptr(), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-        _ptr(status), _stream(dev)))
+    with _on(dev):  # the plan reads the SM count of the current device
+        need = prefill_workspace_size(B, hq, pool.num_kv_heads, pool.head_dim, pool.block_size,
+                                      max_q_len, max_seq_len, window)
+        if workspace is None:
+            workspace = alloc_workspace(need, dev)
+        _check("paged_prefill_chunk_attention", _lib.paged_prefill_chunk_attention(
+            q.data_ptr(), cu_q_lens.data_ptr(), hq, ctypes.byref(pool), block_tables.data_ptr(),
+            width, seq_lens.data_ptr(), B, max_q_len, max_seq_len, window, float(scale),
+            out.data_ptr(), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+            _ptr(status), _stream(dev)))
     return out
 
 
@@ -481,6 +498,26 @@ def profile_read(kind: int) -> Tuple[int, float]:
     ms = ctypes.c_double(0.0)
     _check("pkv_profile_read", _lib.pkv_profile_read(kind, ctypes.byref(n), ctypes.byref(ms)))
     return int(n.value), float(ms.value)
+
+
+def profile_times(kind: int) -> list:
+    """Device milliseconds of every recorded launch of a kernel kind, in launch order."""
+    n = ctypes.c_int64(0)
+    _check("pkv_profile_times", _lib.pkv_profile_times(kind, None, 0, ctypes.byref(n)))
+    buf = (ctypes.c_float * max(int(n.value), 1))()
+    _check("pkv_profile_times", _lib.pkv_profile_times(kind, buf, int(n.value), ctypes.byref(n)))
+    return [float(buf[i]) for i in range(int(n.value))]
+
+
+DRILL_WITHHOLD_FIRST_LOAD = 1
+
+
+def set_wait_drill(wait_limit_ns: int = 0, flags: int = 0) -> None:
+    """Diagnostic fail-closed drill for the launches that follow: the limit of
+    each pipeline data wait (0 = the 2 s default) and, with
+    DRILL_WITHHOLD_FIRST_LOAD, every pipeline's first load left unissued so
+    that the wait for it runs out.  set_wait_drill() restores normal operation."""
+    _check("pkv_set_wait_drill", _lib.pkv_set_wait_drill(int(wait_limit_ns), int(flags)))
 
 
 def launch_count() -> int:
@@ -542,12 +579,13 @@ def paged_decode_attention_groups(groups, workspace: Optional[torch.Tensor] = No
     _require(all(g.k_pool.device == dev for g in groups), "every group's pools on one GPU")
     _on_device(workspace, "workspace", dev)
     _status_ok(status, dev)
-    need = int(_lib.paged_decode_groups_workspace_size(arr, len(groups), B, hq))
-    if workspace is None:
-        workspace = alloc_workspace(need, dev)
-    _check("paged_decode_attention_groups", _lib.paged_decode_attention_groups(
-        arr, len(groups), B, hq, workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-        _ptr(status), _stream(dev)))
+    with _on(dev):  # the plan reads the SM count of the current device
+        need = int(_lib.paged_decode_groups_workspace_size(arr, len(groups), B, hq))
+        if workspace is None:
+            workspace = alloc_workspace(need, dev)
+        _check("paged_decode_attention_groups", _lib.paged_decode_attention_groups(
+            arr, len(groups), B, hq, workspace.data_ptr(),
+            workspace.numel() * workspace.element_size(), _ptr(status), _stream(dev)))
     return [g.out for g in groups]
 
 
@@ -591,9 +629,13 @@ def paged_decode_attention_no_alloc(q: torch.Tensor, k_pool: torch.Tensor, v_poo
     if max_seq_len is None:
         max_seq_len = width * pool.block_size
     px = ctypes.byref(prefix._c()) if prefix is not None else None
-    code = _lib.paged_decode_attention_no_alloc(
-        q.data_ptr(), hq, ctypes.byref(pool), block_tables.data_ptr(), width, seq_lens.data_ptr(),
-        B, max_seq_len, window, float(scale), out.data_ptr(), px, _ptr(status), _stream(dev))
+    # the pools' GPU is made current for the call: the library takes the
+    # scratch of the current device and launches on this device's stream
+    with _on(dev):
+        code = _lib.paged_decode_attention_no_alloc(
+            q.data_ptr(), hq, ctypes.byref(pool), block_tables.data_ptr(), width,
+            seq_lens.data_ptr(), B, max_seq_len, window, float(scale), out.data_ptr(), px,
+            _ptr(status), _stream(dev))
     if code == PKV_ERR_WORKSPACE:
         raise PkvError("paged_decode_attention_no_alloc (request exceeds the "
                        f"{NO_ALLOC_SCRATCH_BYTES >> 20} MiB static scratch)", code)

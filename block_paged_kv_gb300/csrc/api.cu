@@ -18,6 +18,9 @@ using namespace pkv;
 namespace {
 
 std::atomic<int32_t> g_split_override{0};
+// diagnostic drill (pkv_set_wait_drill): data-wait limit and flags
+std::atomic<uint64_t> g_drill_wait_ns{kWaitLimitNs};
+std::atomic<uint32_t> g_drill_flags{0};
 
 // ---------------------------------------------------------------------------
 // launch counting and optional per-kind event timing
@@ -130,6 +133,7 @@ DecodePlan make_plan(int32_t batch, int32_t hq, int32_t hkv, int32_t D, int32_t 
     const int32_t ov = g_split_override.load();
     if (ov > 0) C = ov;
     pl.split_blocks = static_cast<int32_t>(C);
+    pl.few = few ? 1 : 0;
     pl.n_suffix_splits = static_cast<int32_t>(ceil_div64(nblk_max, C));
     pl.prefix_split_blocks = 8;
     pl.n_prefix_splits = 0;
@@ -306,6 +310,7 @@ pkv_status decode_setup(const void *q, int32_t num_q_heads, const pkv_pool *pool
         p.scale_log2 *= pool->k_scale;
         p.v_scale = pool->v_scale;
     }
+    drill_settings(&p.wait_ns, &p.drill);
     p.plan = pl;
     return PKV_OK;
 }
@@ -326,6 +331,12 @@ bool groups_compatible(const pkv_decode_group *groups, int32_t n)
 }  // namespace
 
 namespace pkv {
+
+void drill_settings(uint64_t *wait_ns, uint32_t *flags)
+{
+    *wait_ns = g_drill_wait_ns.load();
+    *flags = g_drill_flags.load();
+}
 
 void prof_begin(int kind, cudaStream_t stream)
 {
@@ -354,6 +365,16 @@ void prof_end(int kind, cudaStream_t stream)
 }  // namespace pkv
 
 extern "C" {
+
+pkv_status pkv_set_wait_drill(uint64_t wait_limit_ns, uint32_t flags)
+{
+    if ((flags & ~static_cast<uint32_t>(PKV_DRILL_WITHHOLD_FIRST_LOAD)) != 0)
+        return PKV_ERR_INVALID_ARG;
+    g_drill_wait_ns.store(wait_limit_ns == 0 ? kWaitLimitNs
+                                             : std::min<uint64_t>(wait_limit_ns, kWaitLimitNs));
+    g_drill_flags.store(flags);
+    return PKV_OK;
+}
 
 pkv_status pkv_profile_enable(uint32_t kind_mask)
 {
@@ -395,6 +416,26 @@ pkv_status pkv_profile_read(int32_t kind, int64_t *launches, double *total_ms)
     }
     *launches = n;
     *total_ms = ms;
+    return PKV_OK;
+}
+
+pkv_status pkv_profile_times(int32_t kind, float *ms_out, int64_t cap, int64_t *launches)
+{
+    if (kind < 0 || kind >= PKV_KERNEL_KINDS || launches == nullptr || cap < 0 ||
+        (cap > 0 && ms_out == nullptr))
+        return PKV_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    int64_t n = 0;
+    for (const auto &r : g_prof_records) {
+        if (r.kind != kind) continue;
+        float t = 0.f;
+        if (cudaEventSynchronize(r.stop) != cudaSuccess ||
+            cudaEventElapsedTime(&t, r.start, r.stop) != cudaSuccess)
+            return PKV_ERR_CUDA;
+        if (n < cap) ms_out[n] = t;
+        ++n;
+    }
+    *launches = n;
     return PKV_OK;
 }
 
@@ -491,8 +532,9 @@ size_t paged_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t n
     if (batch < 0 || num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads != 0 ||
         head_dim <= 0 || block_size <= 0 || max_seq_len < 0 || window < 0)
         return 0;
-    // the f32 and bf16 plans differ only in how many CTAs cover a group's
-    // rows, which does not change the slot count
+    // the f32, bf16 and FP8 plans differ only in how many CTAs cover a
+    // prefix group's rows, which does not change the slot count: the size
+    // holds for every pool dtype
     const DecodePlan pl = make_plan(batch, num_q_heads, num_kv_heads, head_dim, block_size,
                                     max_seq_len, window, prefix, PKV_BF16, num_sms_current());
     return ws_total_bytes(batch, num_q_heads, head_dim, pl);
@@ -700,6 +742,7 @@ pkv_status paged_prefill_chunk_attention(const void *q, const int32_t *cu_q_lens
         d.window = window;
         d.scale_log2 = scale * 1.4426950408889634f;
         d.v_scale = 1.f;
+        drill_settings(&d.wait_ns, &d.drill);
         d.plan = pl;
         cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
         cudaError_t err;
@@ -768,6 +811,7 @@ pkv_status paged_prefill_chunk_attention(const void *q, const int32_t *cu_q_lens
         p.scale_log2 *= pool->k_scale;
         p.v_scale = pool->v_scale;
     }
+    drill_settings(&p.wait_ns, &p.drill);
     if (static_cast<int64_t>(batch) * p.hkv * p.q_tiles * p.kv_splits > INT32_MAX)
         return PKV_ERR_UNSUPPORTED;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

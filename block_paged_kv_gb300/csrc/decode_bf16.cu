@@ -2,13 +2,26 @@
 // decode_kernel.cuh for each head_dim, one query per row (decode) or a few
 // (a speculative-verify step), and of the grouped kernel (several decode
 // calls in one launch).
+#include "decode_coop.cuh"
 #include "decode_kernel.cuh"
 
 namespace pkv {
 
+// A few long rows (rows x kv heads below the SM count), one query per row, no
+// shared-prefix items and one query n-tile: the cooperative kernel, whose
+// warps share every block (decode_coop.cuh).
+static bool coop_fits(const DecodeParams &p)
+{
+    return p.plan.few && p.cu_q_lens == nullptr && p.plan.n_prefix_ctas == 0 && p.group <= 8 &&
+           (p.head_dim == 128 || p.head_dim == 256);
+}
+
 cudaError_t launch_decode_bf16(const DecodeParams &p, const CUtensorMap &kmap,
                                const CUtensorMap &vmap, cudaStream_t stream)
 {
+    if (coop_fits(p))
+        return p.head_dim == 128 ? launch_coop<128>(p, kmap, vmap, stream)
+                                 : launch_coop<256>(p, kmap, vmap, stream);
     const bool mq = p.cu_q_lens != nullptr;  // several queries per row
     // query n-tiles: the rows of a split item (G, or G x max_q for a verify step)
     const bool two = query_ntiles(static_cast<int64_t>(p.group) * (mq ? p.max_q : 1)) == 2;
@@ -28,6 +41,11 @@ cudaError_t launch_decode_bf16(const DecodeParams &p, const CUtensorMap &kmap,
 
 cudaError_t launch_decode_bf16_grouped(const GroupedDecode &gd, cudaStream_t stream)
 {
+    bool coop = true;
+    for (int i = 0; i < gd.n; ++i) coop = coop && coop_fits(gd.g[i]);
+    if (coop)
+        return gd.g[0].head_dim == 128 ? launch_coop_grouped<128>(gd, stream)
+                                       : launch_coop_grouped<256>(gd, stream);
     const bool two = query_ntiles(gd.g[0].group) == 2;
     switch (gd.g[0].head_dim) {
     case 64: return two ? launch_split_grouped<64, false, 2>(gd, stream) : launch_split_grouped<64, false, 1>(gd, stream);

@@ -416,11 +416,13 @@ __device__ __forceinline__ void decode_split_body(const CUtensorMap &kmap, const
     if (prefix_item && warp == 0)
         ids.init(p.tables + static_cast<int64_t>(tab_row) * p.width + b0, 0, 1, nb, lane);
     auto stage_of = [&](int32_t k) { return prefix_item ? k % STAGES : warp * SPW + k % SPW; };
+    // diagnostic drill: pass 0's loads are never issued (its wait runs out)
+    auto withheld = [&](int32_t k) { return (p.drill & kDrillWithholdFirst) != 0 && k == 0; };
     auto issue = [&](int32_t k) {  // whole warp; lane 0 issues
         int32_t bj[BPS];
 #pragma unroll
         for (int i = 0; i < BPS; ++i) bj[i] = ids.next(k * BPS + i, lane);  // -1 past the run
-        if (lane == 0) {
+        if (lane == 0 && !withheld(k)) {
             const int st = stage_of(k);
             bool okv[BPS];
             uint32_t bytes = 0;
@@ -460,6 +462,16 @@ __device__ __forceinline__ void decode_split_body(const CUtensorMap &kmap, const
     const int32_t depth = prefix_item ? STAGES : SPW;
     if (issuer)
         for (int32_t k = 0; k < min(depth, nk); ++k) issue(k);
+    // wind-down after a wait ran out: the loads this warp issued and nobody
+    // consumed, passes k0 .. k_end-1, land before it leaves (their stages are
+    // then quiet when the ring is reused or the CTA exits).  While pass k
+    // is awaited, the passes below min(k + depth, nk) have been issued.
+    auto drain = [&](int32_t k0, int32_t k_end) {
+        if (issuer && lane == 0)
+            for (int32_t j = k0; j < min(k_end, nk); ++j)
+                if (!withheld(j)) mbar_wait(&full[stage_of(j)], (j / depth) & 1);
+        __syncwarp();
+    };
     if constexpr (kF8 && C::kQInRegs) {
         if (q_direct) {
             // bf16 -> f16 (exact inside the f16 range; NaN stays NaN), while
@@ -525,9 +537,10 @@ __device__ __forceinline__ void decode_split_body(const CUtensorMap &kmap, const
     for (int32_t k = 0; k < nk; ++k) {
         const int st = stage_of(k);
         const int32_t use = prefix_item ? k / STAGES : k / SPW;
-        const bool got = mbar_wait(&full[st], use & 1);
+        const bool got = mbar_wait(&full[st], use & 1, p.wait_ns);
         if (__any_sync(0xffffffffu, !got)) {
             if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
+            drain(k, k + depth);
             break;
         }
         const uint32_t stile = smem_u32(stage_mem + st * C::kStageBytes);
@@ -769,12 +782,15 @@ __device__ __forceinline__ void decode_split_body(const CUtensorMap &kmap, const
             if (warp == 0 && k + STAGES < nk) {
                 // every warp has released this stage before it is refilled
                 bool freed = true;
-                if (lane == 0) freed = mbar_wait(&empty[st], use & 1);
+                if (lane == 0) freed = mbar_wait(&empty[st], use & 1, p.wait_ns);
                 if (!__shfl_sync(0xffffffffu, freed, 0)) {
+                    // stop issuing: the passes after k still in flight land,
+                    // then this warp leaves (the others run out of passes)
                     if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
-                } else {
-                    issue(k + STAGES);
+                    drain(k + 1, k + STAGES);
+                    break;
                 }
+                issue(k + STAGES);
             }
         }
     }

@@ -9,12 +9,10 @@
 #include <stdint.h>
 
 #include "pkv.h"
+#include "pkv_internal.h"
 
 namespace pkv {
 
-// Upper bound on any pipeline wait; a wait that runs past it reports
-// PKV_DEV_TIMEOUT and the kernel winds down instead of spinning on.
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
 {
@@ -104,14 +102,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
 }
 
 // Wait for the phase with the given parity to complete.  Bounded: false after
-// kWaitLimitNs (or an iteration cap) without completion.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
+// limit_ns (or an iteration cap) without completion.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
+                                          unsigned long long limit_ns = kWaitLimitNs)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();
     for (uint32_t it = 1; it < (1u << 26); ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 127u) == 0 && globaltimer() - t0 > kWaitLimitNs) return false;
+        if ((it & 127u) == 0 && globaltimer() - t0 > limit_ns) return false;
     }
     return false;
 }

@@ -12,6 +12,18 @@
 
 namespace pkv {
 
+// Upper bound on any pipeline wait; a wait that runs past it reports
+// PKV_DEV_TIMEOUT and the kernel winds down instead of spinning on.  The
+// kernels' data waits take their limit from the launch parameters (this value
+// unless a diagnostic drill shortens it); the waits of a wind-down, for copies
+// a CTA issued itself, always take this one.
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+// Diagnostic drill flag carried by the launch parameters (pkv_set_wait_drill):
+// the first load of every pipeline is never issued, so that the wait for it
+// runs out with nothing in flight on its barrier.
+constexpr uint32_t kDrillWithholdFirst = PKV_DRILL_WITHHOLD_FIRST_LOAD;
+
 struct AppendParams {
     void *k_pool;
     void *v_pool;
@@ -42,6 +54,7 @@ struct DecodePlan {
     int32_t nslot;                // partial slots per (row, q head) = n_prefix + n_suffix
     int32_t prefix_chunks;        // CTAs per (group, kv head, prefix split) over its rows
     int32_t prefix_max;           // prefix lengths are clamped to this (<= table width)
+    int32_t few;                  // rows x kv heads < SMs: a few long rows, about two CTAs per SM
     int64_t n_prefix_ctas;
     int64_t n_suffix_ctas;
 };
@@ -69,6 +82,8 @@ struct DecodeParams {
     int32_t num_groups;
     float scale_log2;  // scale * log2(e) (* k_scale for FP8): scores are kept in base-2 units
     float v_scale;     // FP8: applied to each partial's weighted values
+    uint64_t wait_ns;  // limit of the pipeline's data waits (kWaitLimitNs unless a drill)
+    uint32_t drill;    // diagnostic drill flags (kDrillWithholdFirst); 0 normally
     DecodePlan plan;
 };
 
@@ -131,7 +146,13 @@ struct PrefillParams {
     float *ws_ml;  // [batch][max_q_len][hq][kv_splits][2]: reference max (log2 units), weight sum
     float scale_log2;  // scale * log2(e) (* k_scale for FP8 pools)
     float v_scale;     // FP8 pools: applied to the weighted values
+    uint64_t wait_ns;  // limit of the pipeline's data waits (kWaitLimitNs unless a drill)
+    uint32_t drill;    // diagnostic drill flags (kDrillWithholdFirst); 0 normally
 };
+
+// The current diagnostic drill (pkv_set_wait_drill): the data-wait limit and
+// the flags every decode / prefill launch carries.
+void drill_settings(uint64_t *wait_ns, uint32_t *flags);
 
 cudaError_t launch_append(const AppendParams &p, cudaStream_t stream);
 cudaError_t launch_append_fp8(const AppendParams &p, cudaStream_t stream);

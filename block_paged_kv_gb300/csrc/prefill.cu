@@ -60,8 +60,8 @@ struct Layout {
     static constexpr int kStagingBytes = kF8 ? 2 * 2 * kF8StageTile : 0;  // K and V, 2 deep
     static constexpr int kBarOff = kStagingOff + kStagingBytes;
     // barriers: k_full[4], k_empty[4], v_full[4], v_empty[4], s_full[tile][buf],
-    // p_full[tile][buf], pv_done[tile], FP8: staged[K/V][2]
-    static constexpr int kNumBars = 4 * kStages + 4 + 4 + 2 + (kF8 ? 4 : 0);
+    // p_full[tile][buf], pv_done[tile], mma_drain[tile], FP8: staged[K/V][2]
+    static constexpr int kNumBars = 4 * kStages + 4 + 4 + 2 + 2 + (kF8 ? 4 : 0);
     static constexpr int kMaskOff = kBarOff + kNumBars * 8;
     static constexpr int kTmemOff = kMaskOff + kStages * 4;
     static constexpr int kBytes = kTmemOff + 16;
@@ -116,9 +116,10 @@ __device__ __forceinline__ bool prefill_item(const PrefillParams &p, int64_t bid
 
 // Wait by every lane of the warp (false in all lanes if any gave up); reports
 // a timeout.
-__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, int lane, int32_t *status)
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, int lane, int32_t *status,
+                                          unsigned long long limit_ns)
 {
-    const bool ok = __all_sync(0xffffffffu, mbar_wait(bar, parity));
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(bar, parity, limit_ns));
     if (!ok && lane == 0) report(status, PKV_DEV_TIMEOUT);
     return ok;
 }
@@ -145,7 +146,8 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
     uint64_t *s_full = bars + 4 * kStages;      // [tile * 2 + buf]
     uint64_t *p_full = bars + 4 * kStages + 4;  // [tile * 2 + buf]
     uint64_t *pv_done = bars + 4 * kStages + 8; // [tile]
-    uint64_t *staged = bars + 4 * kStages + 10;  // FP8: [K/V * 2 + buffer]
+    uint64_t *mma_drain = bars + 4 * kStages + 10;  // [tile]: the issuer's last products
+    uint64_t *staged = bars + 4 * kStages + 12;  // FP8: [K/V * 2 + buffer]
     uint32_t *kmask = reinterpret_cast<uint32_t *>(smem + L::kMaskOff);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kTmemOff);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -201,6 +203,8 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         }
         mbar_init(&pv_done[0], 1);
         mbar_init(&pv_done[1], 1);
+        mbar_init(&mma_drain[0], 1);
+        mbar_init(&mma_drain[1], 1);
         if (kF8)
             for (int i = 0; i < 4; ++i) mbar_init(&staged[i], 1);
         fence_mbar_init();
@@ -252,6 +256,8 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
     if (warp == 0 || warp == 2) {
         // ------------------------------------------ K (warp 0) / V (warp 2) producer
         const bool is_k = warp == 0;
+        // diagnostic drill: tile 0's loads are never issued (its waits run out)
+        auto withheld = [&](int32_t jj) { return (p.drill & kDrillWithholdFirst) != 0 && jj == 0; };
         uint8_t *ring = is_k ? k_s : v_s;
         uint64_t *full = is_k ? k_full : v_full;
         uint64_t *empty = is_k ? k_empty : v_empty;
@@ -277,12 +283,15 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             auto load_id = [&](int32_t jj) {
                 return in_range_of(jj) ? __ldg(trow + (jt0 + jj) * kBlocks + lane) : -1;
             };
+            int32_t nf = 0;  // tiles 0 .. nf-1 fetched into the staging buffers
             auto fetch = [&](int32_t jj, int32_t id) {  // whole warp; returns the mask of loaded blocks
                 const bool in_range = in_range_of(jj);
                 const bool good = in_range && static_cast<uint32_t>(id) < static_cast<uint32_t>(p.num_blocks);
                 if (is_k && in_range && !good) report(p.status, PKV_DEV_BAD_BLOCK);
                 const uint32_t mask = __ballot_sync(0xffffffffu, good) & ((1u << kBlocks) - 1u);
                 const int sb = jj & 1;
+                nf = jj + 1;
+                if (withheld(jj)) return mask;  // diagnostic drill: never issued
                 if (lane == 0) {
                     if (mask == 0)
                         mbar_arrive(&stg_bar[sb]);
@@ -305,10 +314,11 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             smask[0] = fetch(0, load_id(0));
             if (ntile > 1) smask[1] = fetch(1, load_id(1));
             int32_t id_ahead = ntile > 2 ? load_id(2) : -1;
-            for (int32_t jj = 0; jj < ntile; ++jj) {
+            int32_t jj = 0;
+            for (; jj < ntile; ++jj) {
                 const int st = jj % kStages, sb = jj & 1;
-                if (jj >= kStages && !warp_wait(&empty[st], ((jj / kStages) + 1) & 1, lane, p.status)) break;
-                if (!warp_wait(&stg_bar[sb], (jj >> 1) & 1, lane, p.status)) break;
+                if (jj >= kStages && !warp_wait(&empty[st], ((jj / kStages) + 1) & 1, lane, p.status, p.wait_ns)) break;
+                if (!warp_wait(&stg_bar[sb], (jj >> 1) & 1, lane, p.status, p.wait_ns)) break;
                 const uint32_t mask = smask[sb];
                 if (is_k && lane == 0) kmask[st] = mask;
                 const uint32_t src = smem_u32(stg + sb * kF8StageTile);
@@ -384,12 +394,19 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
                     id_ahead = jj + 3 < ntile ? load_id(jj + 3) : -1;
                 }
             }
+            // wind-down (a wait ran out): the staged copies issued but not yet
+            // consumed land before the warp leaves
+            if (lane == 0)
+                for (int32_t t = jj; t < nf; ++t)
+                    if (!withheld(t)) mbar_wait(&stg_bar[t & 1], (t >> 1) & 1);
+            __syncwarp();
         } else {
             const CUtensorMap *map = is_k ? &kmap : &vmap;
             const uint64_t policy = l2_evict_last_policy();  // re-read by the row's other CTAs
-            for (int32_t jj = 0; jj < ntile; ++jj) {
+            int32_t jj = 0;
+            for (; jj < ntile; ++jj) {
                 const int st = jj % kStages;
-                if (jj >= kStages && !warp_wait(&empty[st], ((jj / kStages) + 1) & 1, lane, p.status)) break;
+                if (jj >= kStages && !warp_wait(&empty[st], ((jj / kStages) + 1) & 1, lane, p.status, p.wait_ns)) break;
                 const int32_t kb = (jt0 + jj) * kBlocks + lane;  // logical block of lane < kBlocks
                 const bool in_range = lane < kBlocks && kb < p.width && kb * 16 < w.kv_hi &&
                                       (kb + 1) * 16 > w.kv_lo;
@@ -397,8 +414,9 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
                 const bool good = in_range && static_cast<uint32_t>(id) < static_cast<uint32_t>(p.num_blocks);
                 if (is_k && in_range && !good) report(p.status, PKV_DEV_BAD_BLOCK);
                 const uint32_t mask = __ballot_sync(0xffffffffu, good) & ((1u << kBlocks) - 1u);
+                if (is_k && lane == 0) kmask[st] = mask;
+                if (withheld(jj)) continue;  // diagnostic drill: never issued
                 if (lane == 0) {
-                    if (is_k) kmask[st] = mask;
                     if (mask == 0)
                         mbar_arrive(&full[st]);
                     else
@@ -415,6 +433,13 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
                     }
                 }
             }
+            // wind-down (a wait ran out) and normal exit alike: the loads of
+            // the last ring's worth of tiles have landed before the warp
+            // leaves (at a normal exit their consumers saw them land already)
+            if (lane == 0)
+                for (int32_t t = max(0, jj - kStages); t < jj; ++t)
+                    if (!withheld(t)) mbar_wait(&full[t % kStages], (t / kStages) & 1);
+            __syncwarp();
         }
     } else if (warp == 1 || (warp == 3 && nqt == 2)) {
         // ------------------------------------------------------------ MMA issue
@@ -442,7 +467,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         // The whole warp runs these; one elected lane issues a group's
         // products and commits from one straight-line block.
         auto s_mma = [&](int32_t jj) {  // once K(jj) has landed
-            if (!warp_wait(&k_full[jj % kStages], (jj / kStages) & 1, lane, p.status)) return false;
+            if (!warp_wait(&k_full[jj % kStages], (jj / kStages) & 1, lane, p.status, p.wait_ns)) return false;
             tc::fence_after();
             const uint64_t kd = dk + static_cast<uint64_t>(jj % kStages) * kStageStep;
             const uint32_t d = tS(x, jj & 1);
@@ -479,12 +504,18 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         };
         bool ok = s_mma(0) && (ntile < 2 || s_mma(1));
         for (int32_t jj = 0; jj < ntile && ok; ++jj) {
-            ok = warp_wait(&p_full[x * 2 + (jj & 1)], (jj >> 1) & 1, lane, p.status);
+            ok = warp_wait(&p_full[x * 2 + (jj & 1)], (jj >> 1) & 1, lane, p.status, p.wait_ns);
             if (!ok) break;
             tc::fence_after();
             pv_mma(jj);
             if (jj + 2 < ntile) ok = s_mma(jj + 2);
         }
+        // every product this warp issued has completed before the CTA frees
+        // tensor memory (after a wait ran out, some may still be running)
+        if (elect_one()) tc::commit(&mma_drain[x]);
+        __syncwarp();
+        mbar_wait(&mma_drain[x], 0);
+        __syncwarp();
     } else if (warp >= 4 && (warp < 8 || nqt == 2)) {
         // ------------------------------------------------------------ softmax
         // warpgroup x (warps 4-7: tile A, 8-11: tile B), one M-row per thread:
@@ -507,8 +538,8 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             const int ks = jj % kStages, buf = jj & 1;
             const int32_t tbase = (jt0 + jj) * kKeys;
             const uint32_t sx = tS(x, buf) + lane_base;
-            bool got = mbar_wait(&s_full[x * 2 + buf], (jj >> 1) & 1);
-            got = got && mbar_wait(&k_full[ks], (jj / kStages) & 1);  // for kmask
+            bool got = mbar_wait(&s_full[x * 2 + buf], (jj >> 1) & 1, p.wait_ns);
+            got = got && mbar_wait(&k_full[ks], (jj / kStages) & 1, p.wait_ns);  // for kmask
             if (__any_sync(0xffffffffu, !got)) {
                 if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
                 abort = true;
@@ -568,7 +599,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
                 if (__any_sync(0xffffffffu, resc)) {
                     // O_x holds P.V up to tile jj-1 once that product completes
                     if (jj > 0) {
-                        const bool done = mbar_wait(&pv_done[x], (jj - 1) & 1);
+                        const bool done = mbar_wait(&pv_done[x], (jj - 1) & 1, p.wait_ns);
                         if (__any_sync(0xffffffffu, !done)) {
                             if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
                             abort = true;
@@ -619,7 +650,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             // stale slots (possibly NaN): each warpgroup zeroes them before its
             // own P.V reads them (both write the same zeros, so whichever
             // product runs first reads zeros)
-            const bool landed = mbar_wait(&v_full[ks], (jj / kStages) & 1);
+            const bool landed = mbar_wait(&v_full[ks], (jj / kStages) & 1, p.wait_ns);
             if (__any_sync(0xffffffffu, !landed)) {
                 if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
                 abort = true;
@@ -651,8 +682,8 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         // P(ntile-3).V), so wait for ntile - 2 first: a parity names one phase
         // only when the one before it has completed
         if (!abort) {
-            bool done = ntile < 2 || mbar_wait(&pv_done[x], (ntile - 2) & 1);
-            done = done && mbar_wait(&pv_done[x], (ntile - 1) & 1);
+            bool done = ntile < 2 || mbar_wait(&pv_done[x], (ntile - 2) & 1, p.wait_ns);
+            done = done && mbar_wait(&pv_done[x], (ntile - 1) & 1, p.wait_ns);
             if (__any_sync(0xffffffffu, !done)) {
                 if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
             } else if (split) {

@@ -136,7 +136,10 @@ pkv_status paged_kv_append(const pkv_pool *pool, const int32_t *slot_mapping, in
 /*
  * Bytes of device workspace paged_decode_attention needs for these sizes on the
  * current device (the split plan depends on its SM count).  prefix may be NULL.
- * Returns 0 for invalid sizes.
+ * The size does not depend on the pool's dtype: f32, bf16 and FP8 pools of
+ * the same sizes take the same workspace (the plan's partial slots per row do
+ * not change with the dtype; only how many CTAs share a prefix group's rows
+ * does).  Returns 0 for invalid sizes.
  */
 size_t paged_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                    int32_t head_dim, int32_t block_size, int32_t max_seq_len,
@@ -222,9 +225,13 @@ pkv_status paged_decode_attention_groups(const pkv_decode_group *groups, int32_t
  * that loads the library holds until the process exits.
  *   - It allocates nothing: no cudaMalloc, no cudaFree, no allocating library
  *     routine.
- *   - The first call on a device, with that device current, looks up the
- *     array's device address (cudaGetSymbolAddress) and keeps it; make that
- *     first call before any stream capture.
+ *   - The scratch is that of the CURRENT device: make the device that holds
+ *     the pools and buffers current (cudaSetDevice) before the call.  The
+ *     first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) and keeps it for the life of the process; make
+ *     that first call before any stream capture.  After cudaDeviceReset the
+ *     kept address is stale: do not call this entry point on that device
+ *     again in the same process.
  *   - Sizes whose workspace (paged_decode_workspace_size) exceeds
  *     PKV_NO_ALLOC_SCRATCH_BYTES return PKV_ERR_WORKSPACE, nothing enqueued.
  *   - Every call on a device shares the one array and leaves its contents
@@ -334,6 +341,27 @@ int32_t pkv_prefix_groups_host(const int32_t *block_tables, int32_t max_blocks_p
  */
 int32_t pkv_set_decode_split_blocks(int32_t blocks_per_split);
 
+/*
+ * Diagnostic fail-closed drill for the device-side wait timeout (the pages
+ * require the paged path to fail closed rather than degrade silently:
+ * "paged-cache.md", fail-closed gates of the grouped coordinator;
+ * "perf.md", paged knob table, MLX_PAGED_NATIVE_KV_WRITE row, where batched
+ * decode hard-errors instead of falling back).  Process-wide, for the
+ * launches that follow (bf16 and FP8 decode, tensor-core prefill):
+ *   wait_limit_ns: limit of each pipeline data wait, 0 = the default
+ *                  (2 s); values above the default are cut to it;
+ *   flags:         0, or PKV_DRILL_WITHHOLD_FIRST_LOAD: every pipeline
+ *                  leaves its first load unissued, so that the wait for it
+ *                  runs out after wait_limit_ns.
+ * A wait that runs out sets PKV_DEV_TIMEOUT in the status word; the CTA then
+ * waits (with the 2 s default limit) for every copy it did issue to land
+ * and for its tensor-core products to finish, and exits.  The call's output
+ * is then undefined.  pkv_set_wait_drill(0, 0) restores normal operation.
+ * Returns PKV_ERR_INVALID_ARG for unknown flags.
+ */
+#define PKV_DRILL_WITHHOLD_FIRST_LOAD 1u
+pkv_status pkv_set_wait_drill(uint64_t wait_limit_ns, uint32_t flags);
+
 /* Number of splits per row and blocks per split the automatic plan picks for
  * these sizes on the current device (diagnostic; -1 on invalid sizes). */
 int32_t pkv_decode_plan(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
@@ -366,6 +394,11 @@ pkv_status pkv_profile_mask(uint32_t kind_mask);
 /* Launches recorded for a kind and their summed device time in milliseconds.
  * Waits for the recorded events. */
 pkv_status pkv_profile_read(int32_t kind, int64_t *launches, double *total_ms);
+
+/* The device times (milliseconds) of the recorded launches of a kind, in
+ * launch order: up to `cap` of them go to ms_out (host array), *launches
+ * receives how many were recorded in all.  Waits for the recorded events. */
+pkv_status pkv_profile_times(int32_t kind, float *ms_out, int64_t cap, int64_t *launches);
 
 /* Number of kernels this process has launched through the library. */
 int64_t pkv_launch_count(void);
