@@ -82,3 +82,34 @@ def sample_pairs(w: gen.Workload, n: int, seed: int = 0) -> np.ndarray:
     for i in range(n):
         pairs.add((int(u[2 * i]) % w.batch, int(u[2 * i + 1]) % w.num_q_heads))
     return np.array(sorted(pairs), dtype=np.int32)
+
+
+def assert_appended_blocks_equal(d: Dev, slots: np.ndarray, kp: np.ndarray, vp: np.ndarray):
+    """Every pool block that received a token of the append, K and V, equals
+    the oracle's byte for byte (the new rows and the untouched rows beside
+    them): the pool check of workloads too large to copy back whole."""
+    bs = d.w.block_size
+    blocks = np.unique(slots[slots >= 0] // bs)
+    idx = torch.from_numpy(blocks.astype(np.int64)).to(d.k_pool.device)
+    for got, ref, name in ((d.k_pool, kp, "K"), (d.v_pool, vp, "V")):
+        g = got.index_select(0, idx).contiguous().view(torch.uint8).cpu().numpy().tobytes()
+        r = np.ascontiguousarray(ref[blocks]).tobytes()
+        assert g == r, f"{name} pool blocks of the appended tokens differ from the oracle's"
+
+
+def oracle_decode_rows(orc, q, kp, vp, dtype, tables, seq_lens, window, scale, num_q_heads,
+                       threads=None, **kw):
+    """The oracle's full [B, Hq, D] decode output, one row per oracle call on
+    a pool of host threads (the oracle's C calls release the interpreter
+    lock); the same arithmetic as one call over the whole batch."""
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+    batch = tables.shape[0]
+
+    def one(r):
+        pairs = np.array([[r, h] for h in range(num_q_heads)], dtype=np.int32)
+        return orc.decode(q, kp, vp, dtype, tables, seq_lens, window, scale, pairs=pairs, **kw)
+
+    with ThreadPoolExecutor(max_workers=threads or os.cpu_count() or 1) as ex:
+        rows = list(ex.map(one, range(batch)))
+    return np.stack(rows)

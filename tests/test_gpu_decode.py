@@ -7,7 +7,8 @@ import numpy as np
 import pytest
 
 import pkv_inputs as gen
-from gpu_util import Dev, append, assert_close, oracle_pools, sample_pairs, storage_bytes, to_f64
+from gpu_util import (Dev, append, assert_appended_blocks_equal, assert_close, oracle_pools,
+                      sample_pairs, storage_bytes, to_f64)
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -29,6 +30,8 @@ def run_step(pkv, orc, w, prefix=False, pairs=None, check_pool=True):
     assert np.array_equal(slots, or_slots)
     if check_pool:
         assert storage_bytes(d.k_pool) == kp.tobytes() and storage_bytes(d.v_pool) == vp.tobytes()
+    else:
+        assert_appended_blocks_equal(d, slots, kp, vp)
     desc = pkv.make_prefix_desc(w.block_tables, w.seq_lens, w.block_size, d.k_pool.device) \
         if prefix else None
     out = pkv.paged_decode_attention(d.q, d.k_pool, d.v_pool, d.tables, d.seq_lens, w.window,
@@ -64,17 +67,20 @@ def test_dense_bf16(pkv, orc):
 
 @pytest.mark.parametrize("prefix", [False, True])
 def test_shared_prefix_b32_full_size(pkv, orc, prefix):
+    # every output element of the batch-32 step; the pools' appended blocks
+    # byte for byte (the whole pools are too large to copy back)
     w = gen.shared_prefix_b32()
-    pairs = sample_pairs(w, 96, seed=3)
-    got, ref, _ = run_step(pkv, orc, w, prefix=prefix, pairs=pairs, check_pool=False)
+    got, ref, _ = run_step(pkv, orc, w, prefix=prefix, check_pool=False)
+    assert got.shape == ref.shape == (w.batch, w.num_q_heads, w.head_dim)
     assert_close(got, ref, "bf16", f"shared prefix b32 (prefix path {prefix})")
 
 
 def test_long_two_groups_full_size(pkv, orc):
+    # both groups of the long-context workload, every output element
     full, sliding = gen.long_two_groups()
     for w in (full, sliding):
-        pairs = sample_pairs(w, 16, seed=4)
-        got, ref, _ = run_step(pkv, orc, w, pairs=pairs, check_pool=False)
+        got, ref, _ = run_step(pkv, orc, w, check_pool=False)
+        assert got.shape == ref.shape == (w.batch, w.num_q_heads, w.head_dim)
         assert_close(got, ref, "bf16", w.name)
 
 

@@ -20,9 +20,9 @@ def pkv():
     return m
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_bad_block_id_sets_status(pkv, dtype):
-    w = gen.decode_workload(seed=20, dtype=dtype, num_q_heads=4, num_kv_heads=2, head_dim=64,
+@pytest.mark.parametrize("dtype,d", [("f32", 64), ("bf16", 64), ("bf16", 128), ("bf16", 256)])
+def test_bad_block_id_sets_status(pkv, dtype, d):
+    w = gen.decode_workload(seed=20, dtype=dtype, num_q_heads=4, num_kv_heads=2, head_dim=d,
                             context_lens=[100, 100])
     d = Dev(w)
     append(pkv, d)
@@ -115,3 +115,116 @@ def test_buffers_off_the_gpu_rejected_before_launch(pkv):
         pkv.paged_decode_attention_no_alloc(d.q, d.k_pool, d.v_pool, d.tables, d.seq_lens, 0,
                                             w.scale, torch.empty(tuple(d.q.shape), dtype=d.q.dtype))
     assert pkv.launch_count() == n0
+
+
+# ---------------------------------------------------------------------------
+# fail-closed drill: a pipeline wait that runs out.  The drill leaves every
+# pipeline's first load unissued and shortens the data-wait limit to 1 ms, so
+# the wait for that load runs out with nothing in flight on its barrier; the
+# CTA then lets the copies it did issue land and exits.  The status word must
+# carry PKV_DEV_TIMEOUT, the call must return, and the next call (drill off)
+# must be clean and match the oracle.
+# ---------------------------------------------------------------------------
+DRILL_NS = 1_000_000
+
+
+def _drill(pkv, fn):
+    pkv.set_wait_drill(DRILL_NS, pkv.DRILL_WITHHOLD_FIRST_LOAD)
+    try:
+        fn()
+        torch.cuda.synchronize()
+    finally:
+        pkv.set_wait_drill()
+
+
+@pytest.mark.parametrize("prefix", [False, True])
+def test_wait_timeout_drill_decode_bf16(pkv, orc, prefix):
+    from gpu_util import assert_close, oracle_pools, to_f64
+    w = gen.decode_workload(seed=25, dtype="bf16", num_q_heads=8, num_kv_heads=2, head_dim=128,
+                            context_lens=[300, 700, 64], shared_prefix_tokens=64 if prefix else 0)
+    d = Dev(w)
+    append(pkv, d)
+    desc = pkv.make_prefix_desc(w.block_tables, w.seq_lens, 16, d.k_pool.device) if prefix else None
+
+    def call():
+        return pkv.paged_decode_attention(d.q, d.k_pool, d.v_pool, d.tables, d.seq_lens, 0, w.scale,
+                                          prefix=desc, status=d.status)
+
+    _drill(pkv, call)
+    assert int(d.status.item()) & pkv.DEV_TIMEOUT
+    d.status.zero_()
+    out = call()
+    torch.cuda.synchronize()
+    assert int(d.status.item()) == 0
+    _, kp, vp = oracle_pools(orc, w)
+    ref = orc.decode(w.q, kp, vp, "bf16", w.block_tables, w.seq_lens, 0, w.scale)
+    assert_close(to_f64(out), ref, "bf16", "decode after the drill")
+
+
+def test_wait_timeout_drill_decode_fp8(pkv):
+    w = gen.decode_workload(seed=26, dtype="bf16", num_q_heads=8, num_kv_heads=1, head_dim=256,
+                            context_lens=[200, 900])
+    d = Dev(w)
+    kp, vp = pkv.fp8_pools(w.num_blocks, 1, 256, "cuda")
+    slots, kr, vr = gen.live_slots(w)
+    ks, vs = float(gen.FP8_K_SCALE), float(gen.FP8_V_SCALE)
+    from gpu_util import to_torch
+    pkv.paged_kv_append(kp, vp, torch.from_numpy(slots).cuda(), to_torch(kr, "bf16"),
+                        to_torch(vr, "bf16"), status=d.status, k_scale=ks, v_scale=vs)
+
+    def call():
+        return pkv.paged_decode_attention(d.q, kp, vp, d.tables, d.seq_lens, 0, w.scale,
+                                          status=d.status, k_scale=ks, v_scale=vs)
+
+    torch.cuda.synchronize()
+    assert int(d.status.item()) == 0
+    ref = call().clone()
+    _drill(pkv, call)
+    assert int(d.status.item()) & pkv.DEV_TIMEOUT
+    d.status.zero_()
+    out = call()
+    torch.cuda.synchronize()
+    assert int(d.status.item()) == 0
+    assert torch.equal(out, ref)
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_wait_timeout_drill_prefill(pkv, fp8):
+    w = gen.prefill_workload(seed=27, dtype="bf16", num_q_heads=8, num_kv_heads=2, head_dim=128,
+                             prefix_lens=[640, 100], chunk_lens=[200, 130])
+    d = Dev(w)
+    kw = {}
+    if fp8:
+        kp, vp = pkv.fp8_pools(w.num_blocks, 2, 128, "cuda")
+        from gpu_util import to_torch
+        ks, vs = float(gen.FP8_K_SCALE), float(gen.FP8_V_SCALE)
+        slots, kr, vr = gen.live_slots(w)
+        pkv.paged_kv_append(kp, vp, torch.from_numpy(slots).cuda(), to_torch(kr, "bf16"),
+                            to_torch(vr, "bf16"), status=d.status, k_scale=ks, v_scale=vs)
+        kw = {"k_scale": ks, "v_scale": vs}
+    else:
+        kp, vp = d.k_pool, d.v_pool
+    new = torch.from_numpy(pkv.slot_mapping_host(w.block_tables, w.num_blocks, w.new_rows,
+                                                 w.new_pos, 16)).cuda()
+    pkv.paged_kv_append(kp, vp, new, d.k_new, d.v_new, status=d.status, **kw)
+    C = int(np.max(np.diff(w.cu_q_lens)))
+
+    def call():
+        return pkv.paged_prefill_chunk_attention(d.q, d.cu, kp, vp, d.tables, d.seq_lens, C, 0,
+                                                 w.scale, status=d.status, **kw)
+
+    ref = call().clone()
+    torch.cuda.synchronize()
+    assert int(d.status.item()) == 0
+    _drill(pkv, call)
+    assert int(d.status.item()) & pkv.DEV_TIMEOUT
+    d.status.zero_()
+    out = call()
+    torch.cuda.synchronize()
+    assert int(d.status.item()) == 0
+    assert torch.equal(out, ref)
+
+
+def test_wait_drill_rejects_unknown_flags(pkv):
+    with pytest.raises(pkv.PkvError):
+        pkv.set_wait_drill(0, 2)

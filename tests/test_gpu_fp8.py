@@ -14,7 +14,7 @@ import numpy as np
 import pytest
 
 import pkv_inputs as gen
-from gpu_util import assert_close, to_f64, to_torch
+from gpu_util import assert_close, oracle_decode_rows, to_f64, to_torch
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -70,6 +70,12 @@ class Fp8Step:
         if check_pool:
             assert np.array_equal(self.k_pool.cpu().numpy(), kp), "K pool bytes differ"
             assert np.array_equal(self.v_pool.cpu().numpy(), vp), "V pool bytes differ"
+        else:
+            # the blocks that received the step's new tokens, byte for byte
+            blocks = np.unique(new_slots[new_slots >= 0] // 16)
+            idx = torch.from_numpy(blocks.astype(np.int64)).to(dev)
+            assert np.array_equal(self.k_pool.index_select(0, idx).cpu().numpy(), kp[blocks])
+            assert np.array_equal(self.v_pool.index_select(0, idx).cpu().numpy(), vp[blocks])
 
     def decode(self, pkv, prefix=False):
         w = self.w
@@ -235,16 +241,16 @@ def test_decode_sliding_null_sentinel(pkv, orc):
 
 
 def test_decode_shared_prefix_b32_full_size(pkv, orc):
-    # the shared-prefix batch at full size on FP8 pools; the oracle fills and
-    # reads only the sampled rows
+    # the shared-prefix batch at full size on FP8 pools, every output element
+    # of every row, both prefix paths
     w = gen.shared_prefix_b32()
-    rows = [0, 7, 13, 31]
-    s = Fp8Step(pkv, orc, w, rows=rows, check_pool=False)
-    pairs = np.array([(r, h) for r in rows for h in (0, 5, 17, 31)], dtype=np.int32)
+    s = Fp8Step(pkv, orc, w, check_pool=False)
+    ref = oracle_decode_rows(orc, w.q, s.kp, s.vp, "fp8", w.block_tables, w.seq_lens, w.window,
+                             w.scale, w.num_q_heads, k_scale=KS, v_scale=VS)
     for prefix in (False, True):
-        got = s.decode(pkv, prefix=prefix)[pairs[:, 0], pairs[:, 1]]
-        assert_close(got, s.oracle_decode(orc, pairs=pairs), "bf16",
-                     f"fp8 shared prefix b32 (prefix path {prefix})")
+        got = s.decode(pkv, prefix=prefix)
+        assert got.shape == ref.shape
+        assert_close(got, ref, "bf16", f"fp8 shared prefix b32 (prefix path {prefix})")
 
 
 def test_query_out_of_f16_range_flagged(pkv, orc):

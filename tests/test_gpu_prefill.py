@@ -8,7 +8,8 @@ import numpy as np
 import pytest
 
 import pkv_inputs as gen
-from gpu_util import Dev, append, assert_close, oracle_pools, storage_bytes, to_f64
+from gpu_util import (Dev, append, assert_appended_blocks_equal, assert_close, oracle_pools,
+                      storage_bytes, to_f64)
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -29,6 +30,8 @@ def run_prefill(pkv, orc, w, samples=None, check_pool=True):
     assert np.array_equal(slots, or_slots)
     if check_pool:
         assert storage_bytes(d.k_pool) == kp.tobytes() and storage_bytes(d.v_pool) == vp.tobytes()
+    else:
+        assert_appended_blocks_equal(d, slots, kp, vp)
     max_q = int(np.max(np.diff(w.cu_q_lens)))
     out = pkv.paged_prefill_chunk_attention(d.q, d.cu, d.k_pool, d.v_pool, d.tables, d.seq_lens,
                                             max_q, w.window, w.scale,
@@ -40,18 +43,38 @@ def run_prefill(pkv, orc, w, samples=None, check_pool=True):
         ref = orc.prefill(w.q, w.cu_q_lens, kp, vp, w.dtype, w.block_tables, w.seq_lens, w.window,
                           w.scale)
         return got, ref, d
-    ref = orc.prefill(w.q, w.cu_q_lens, kp, vp, w.dtype, w.block_tables, w.seq_lens, w.window,
-                      w.scale, samples=samples)
+    ref = _oracle_samples(orc, w, kp, vp, samples)
     rows = w.cu_q_lens[samples[:, 0]] + samples[:, 1]
     return got[rows, samples[:, 2]], ref, d
 
 
+def _oracle_samples(orc, w, kp, vp, samples, chunk=64):
+    """The oracle at (row, query, head) samples, chunks of them on a pool of
+    host threads (the oracle's C calls release the interpreter lock)."""
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+
+    def one(i):
+        return orc.prefill(w.q, w.cu_q_lens, kp, vp, w.dtype, w.block_tables, w.seq_lens,
+                           w.window, w.scale, samples=samples[i:i + chunk])
+
+    with ThreadPoolExecutor(max_workers=os.cpu_count() or 1) as ex:
+        parts = list(ex.map(one, range(0, samples.shape[0], chunk)))
+    return np.concatenate(parts)
+
+
 def test_chunked_prefill_full_size(pkv, orc):
+    # the oracle costs 5.6e11 FLOP over the whole call, so the outputs are
+    # sampled: every query index of row 0 for one q head of each kv head
+    # (a different head offset per kv head), the chunk's ends of every row,
+    # and seeded (row, query, head) triples
     w = gen.chunked_prefill()
     u = gen.uniform_ints(5, "samples", 3 * 160, 0, 1 << 30)
     C = int(w.cu_q_lens[1] - w.cu_q_lens[0])
-    samples = [[r, i, h] for r in range(w.batch) for i in (0, 1, 31, 32, C - 1)
-               for h in (0, w.num_q_heads - 1)]
+    G = w.num_q_heads // w.num_kv_heads
+    samples = [[0, i, g * G + g % G] for g in range(w.num_kv_heads) for i in range(C)]
+    samples += [[r, i, h] for r in range(w.batch) for i in (0, 1, 31, 32, C - 1)
+                for h in (0, w.num_q_heads - 1)]
     samples += [[int(u[3 * k]) % w.batch, int(u[3 * k + 1]) % C, int(u[3 * k + 2]) % w.num_q_heads]
                 for k in range(160)]
     samples = np.array(samples, dtype=np.int32)
