@@ -1,27 +1,26 @@
-// Split-KV paged decode for a few long rows, bf16 pools: the four warps of a
-// CTA work on every block of the run together, each on a quarter of the head
-// dimension ("perf.md": above some context length the pages switch decode to
-// grouped, partitioned kernels; this is the layout of such a kernel for a
-// grid of one or two CTAs per SM).
+// Split-KV paged decode for a few long rows, bf16 pools: the four compute
+// warps of a CTA work on every block of the run together, each on a quarter
+// of the head dimension ("perf.md": above some context length the pages switch
+// decode to grouped, partitioned kernels; this is the layout of such a kernel
+// for a grid of about two CTAs per SM).
 //
 // Why a second layout.  When rows x kv heads are fewer than the SMs, each CTA
 // streams one long run of blocks.  If each warp took every fourth block (the
 // many-row kernel in decode_kernel.cuh), a warp would keep at most its own
 // ring share in flight (one 16 KB block at head_dim 256) and the warps of a
-// CTA would drift apart, the CTA then waiting for its slowest one.  Here the
-// CTA keeps one shared ring of kStages blocks (96 KB) that one thread
-// refills, so that kStages - 1 blocks are in flight while one is computed,
-// and every warp finishes with the last block.
+// CTA would drift apart, the CTA then waiting for its slowest one.  Here a
+// fifth warp keeps one shared ring of kStages blocks (96 KB) full: it refills
+// a stage as soon as the four compute warps have released it, so the ring's
+// other blocks stay in flight while two are computed, and every compute warp
+// finishes with the last block.
 //
-// Per block (16 tokens), warp w:
+// Per pass (two blocks, 32 tokens), compute warp w:
 //   S^T partial = K[:, dims of w] Q^T[dims of w, :]   (mma.sync m16n8k16, fp32)
 //   the four partials meet in shared memory (one named barrier, which also
-//   votes on whether any warp's wait for the block ran out), every warp adds
+//   votes on whether any warp's wait for the blocks ran out), every warp adds
 //   them in the same order, so all hold the same scores and the same online
 //   softmax state;
 //   O^T[dims of w, :] += V^T[dims of w, :] P^T        (P as bf16 hi + lo)
-// The named barrier of block j also tells the refilling thread that every
-// warp is done with block j-1, whose stage then takes block j-1 + kStages.
 // At the end each warp writes its dims of the partial (unnormalised O, the
 // running max in log2 units and the weight sum) to the workspace; the merge
 // kernel is the one of the other decode kernels.
@@ -38,21 +37,24 @@ struct CoopCfg {
     static constexpr int kStageBytes = 2 * kTileBytes;      // K + V of one block
     static constexpr int kRingBytes = 96 * 1024;
     static constexpr int kStages = kRingBytes / kStageBytes;
+    static constexpr int kBpp = 2;                          // blocks per pass
     static constexpr int kKS = D / 16 / kDecodeWarps;       // 16-dim k-steps of a warp's S part
     static constexpr int kMT = D / 16 / kDecodeWarps;       // 16-dim m-tiles of a warp's O part
-    static constexpr int kSbufOff = kRingBytes;             // [2][warps][32 lanes] float4
-    static constexpr int kSbufBytes = 2 * kDecodeWarps * 32 * 16;
-    static constexpr int kBarOff = kSbufOff + kSbufBytes;
-    static constexpr int kOkOff = kBarOff + kStages * 8;     // [kStages] int32: block loaded
+    static constexpr int kThreads = (kDecodeWarps + 1) * 32;  // + the producer warp
+    static constexpr int kSbufOff = kRingBytes;             // [2][warps][kBpp][32 lanes] float4
+    static constexpr int kSbufBytes = 2 * kDecodeWarps * kBpp * 32 * 16;
+    static constexpr int kBarOff = kSbufOff + kSbufBytes;   // full[kStages], empty[kStages]
+    static constexpr int kOkOff = kBarOff + 2 * kStages * 8;  // [kStages] int32: block loaded
     static constexpr int kBytes = kOkOff + kStages * 4;
     static constexpr int kLaunchBytes = kBytes + 1024;      // room to align the base to 1024
     static constexpr int kCtasPerSm = 2;
-    static_assert(kStages >= 3, "at least two blocks in flight while one is computed");
+    static_assert(kStages >= 2 * kBpp, "a pass's blocks plus the next pass's in flight");
     static_assert(kKS >= 1 && D % (16 * kDecodeWarps) == 0, "head_dim splits into four warps");
     static_assert(kCtasPerSm * kLaunchBytes <= 227 * 1024, "two CTAs per SM");
 };
 
-// Named barrier 1 over the CTA's warps; returns whether any thread passed `pred`.
+// Named barrier 1 over the CTA's compute warps; returns whether any thread
+// passed `pred`.
 __device__ __forceinline__ bool coop_barrier_any(bool pred)
 {
     uint32_t r;
@@ -73,15 +75,18 @@ __device__ __forceinline__ void decode_coop_body(const CUtensorMap &kmap, const 
 {
     using C = CoopCfg<D>;
     constexpr int S = C::kStages;
+    constexpr int BPP = C::kBpp;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     float4 *sbuf = reinterpret_cast<float4 *>(smem + C::kSbufOff);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kBarOff);
+    uint64_t *empty = full + S;
     int32_t *stage_ok = reinterpret_cast<int32_t *>(smem + C::kOkOff);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const bool producer = warp == kDecodeWarps;
     const int G = p.group;
     const int bs = C::kTok;
 
@@ -99,17 +104,18 @@ __device__ __forceinline__ void decode_coop_body(const CUtensorMap &kmap, const 
     const int32_t g = static_cast<int32_t>(bid % p.hkv);
     const int32_t r = static_cast<int32_t>(bid / p.hkv);
     const int32_t *table_row = p.tables + static_cast<int64_t>(r) * p.width;
-    // warp 0 fetches the run's block ids before the row's length is known, on
-    // the guess that the row's splits start at block 0 (full attention)
+    // the producer fetches the run's block ids before the row's length is
+    // known, on the guess that the row's splits start at block 0 (full
+    // attention); the compute warps load their query fragments meanwhile
     BlockIds ids;
     const int32_t b_guess = s * p.plan.split_blocks;
-    if (warp == 0)
+    if (producer)
         ids.init(table_row + min(b_guess, p.width), 0, 1,
                  max(0, min(p.plan.split_blocks, p.width - b_guess)), lane);
-    // this warp's B fragments of Q^T: the G heads of (r, g) on N (one n-tile),
-    // its own k-steps kk = w * kKS + i on K
+    // B fragments of Q^T: the G heads of (r, g) on N (one n-tile), this
+    // warp's k-steps kk = w * kKS + i on K
     uint32_t qb[C::kKS][2];
-    {
+    if (!producer) {
         const int row = lane >> 2;
         const bool live = row < G;
         const uint32_t *src = reinterpret_cast<const uint32_t *>(p.q) +
@@ -128,42 +134,61 @@ __device__ __forceinline__ void decode_coop_body(const CUtensorMap &kmap, const 
     if (b0 >= b1) return;  // uniform over the CTA
     const int32_t nblk = b1 - b0;
     const int32_t lo_all = rr.lo, hi_all = rr.L;
-    if (warp == 0) {
-        if (rr.b_first != 0)
-            ids.init(table_row + b0, 0, 1, nblk, lane);  // the guess was wrong
-        else
-            ids.n = nblk;  // fetched ids past the run are never used
-    }
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < S; ++i) mbar_init(&full[i], 1);
+        for (int i = 0; i < S; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kDecodeWarps);  // lane 0 of every compute warp
+        }
         fence_mbar_init();
     }
     __syncthreads();
 
-    // ------------------------------------------------------------- loads
-    // block j of the run goes to stage j % S; warp 0 issues (lane 0 copies)
-    const uint64_t policy = l2_evict_first_policy();
     auto withheld = [&](int32_t j) { return (p.drill & kDrillWithholdFirst) != 0 && j == 0; };
-    auto issue = [&](int32_t j) {  // warp 0, whole warp
-        const int32_t id = ids.next(j, lane);
-        if (lane == 0 && !withheld(j)) {
+    if (producer) {
+        // ------------------------------------------------------------- loads
+        // block j of the run goes to stage j % S once the compute warps have
+        // released block j - S
+        if (rr.b_first != 0)
+            ids.init(table_row + b0, 0, 1, nblk, lane);  // the guess was wrong
+        else
+            ids.n = nblk;  // fetched ids past the run are never used
+        const uint64_t policy = l2_evict_first_policy();
+        int32_t j = 0;
+        for (; j < nblk; ++j) {
             const int st = j % S;
-            const bool ok = static_cast<uint32_t>(id) < static_cast<uint32_t>(p.num_blocks);
-            stage_ok[st] = ok ? 1 : 0;  // published by the arrive (release)
-            if (ok) {
-                mbar_arrive_expect_tx(&full[st], 2 * C::kTileBytes);
-                uint8_t *kdst = smem + st * C::kStageBytes;
-                tma_load_5d(kdst, &kmap, &full[st], 0, 0, 0, g, id, policy);
-                tma_load_5d(kdst + C::kTileBytes, &vmap, &full[st], 0, 0, 0, g, id, policy);
-            } else {
-                report(p.status, PKV_DEV_BAD_BLOCK);
-                mbar_arrive(&full[st]);  // an empty stage: its tokens are masked, its values unread
+            if (j >= S) {
+                bool freed = true;
+                if (lane == 0) freed = mbar_wait(&empty[st], ((j / S) - 1) & 1, p.wait_ns);
+                if (!__shfl_sync(0xffffffffu, freed, 0)) {
+                    if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
+                    break;
+                }
+            }
+            const int32_t id = ids.next(j, lane);
+            if (lane == 0 && !withheld(j)) {
+                const bool ok = static_cast<uint32_t>(id) < static_cast<uint32_t>(p.num_blocks);
+                stage_ok[st] = ok ? 1 : 0;  // published by the arrive (release)
+                if (ok) {
+                    mbar_arrive_expect_tx(&full[st], 2 * C::kTileBytes);
+                    uint8_t *kdst = smem + st * C::kStageBytes;
+                    tma_load_5d(kdst, &kmap, &full[st], 0, 0, 0, g, id, policy);
+                    tma_load_5d(kdst + C::kTileBytes, &vmap, &full[st], 0, 0, 0, g, id, policy);
+                } else {
+                    report(p.status, PKV_DEV_BAD_BLOCK);
+                    mbar_arrive(&full[st]);  // an empty stage: tokens masked, values unread
+                }
             }
         }
-    };
-    if (warp == 0)
-        for (int32_t j = 0; j < min(S, nblk); ++j) issue(j);
+        // every copy this warp issued has landed before it leaves (at a
+        // normal end the compute warps wait for them anyway; after a wait
+        // ran out they may have left already)
+        if (lane == 0)
+            for (int32_t t = max(0, j - S); t < j; ++t)
+                if (!withheld(t)) mbar_wait(&full[t % S], (t / S) & 1);
+        __syncwarp();
+        return;
+    }
 
     // ---------------------------------------------------------------- compute
     const int g8 = lane >> 2;  // C rows g8, g8 + 8 (tokens / dims); B column g8
@@ -174,60 +199,80 @@ __device__ __forceinline__ void decode_coop_body(const CUtensorMap &kmap, const 
 #pragma unroll
     for (int i = 0; i < C::kMT; ++i) oT[i][0] = oT[i][1] = oT[i][2] = oT[i][3] = 0.f;
     float mc[2] = {-INFINITY, -INFINITY}, lc[2] = {0.f, 0.f};
-    int32_t j = 0;
-    bool failed = false;
-    for (; j < nblk; ++j) {
-        const int st = j % S;
-        const bool got = mbar_wait(&full[st], (j / S) & 1, p.wait_ns);
-        const uint32_t kt = smem_u32(smem + st * C::kStageBytes);
-        const uint32_t vt = kt + C::kTileBytes;
-        const bool okb = got && stage_ok[st] != 0;
-        // this warp's part of S^T = K Q^T: tokens on M, the G heads on N
-        float sa[4] = {0.f, 0.f, 0.f, 0.f};
-        if (okb) {
+    const int32_t npass = (nblk + BPP - 1) / BPP;
+    for (int32_t k = 0; k < npass; ++k) {
+        bool got = true, okb[BPP], have[BPP];
+        uint32_t kt[BPP];
+        int bt[BPP];
 #pragma unroll
-            for (int i = 0; i < C::kKS; ++i) {
-                uint32_t a[4];
-                ldsm_x4(kv_chunk_addr(kt, ka_tok, (warp * C::kKS + i) * 16 + ka_dof), a[0], a[1], a[2],
-                        a[3]);
-                mma_16816(sa, a, qb[i][0], qb[i][1]);
+        for (int b = 0; b < BPP; ++b) {
+            const int32_t j = k * BPP + b;
+            const int st = j % S;
+            have[b] = j < nblk;
+            if (have[b]) got = got && mbar_wait(&full[st], (j / S) & 1, p.wait_ns);
+            okb[b] = have[b] && got && stage_ok[st] != 0;
+            kt[b] = smem_u32(smem + st * C::kStageBytes);
+            bt[b] = (b0 + j) * bs;
+        }
+        // this warp's part of S^T = K Q^T for each block: tokens on M, the G
+        // heads on N
+        float sa[BPP][4];
+#pragma unroll
+        for (int b = 0; b < BPP; ++b) {
+            sa[b][0] = sa[b][1] = sa[b][2] = sa[b][3] = 0.f;
+            if (okb[b]) {
+#pragma unroll
+                for (int i = 0; i < C::kKS; ++i) {
+                    uint32_t a[4];
+                    ldsm_x4(kv_chunk_addr(kt[b], ka_tok, (warp * C::kKS + i) * 16 + ka_dof), a[0], a[1],
+                            a[2], a[3]);
+                    mma_16816(sa[b], a, qb[i][0], qb[i][1]);
+                }
             }
         }
-        float4 *slot = sbuf + (j & 1) * (kDecodeWarps * 32);
-        slot[warp * 32 + lane] = make_float4(sa[0], sa[1], sa[2], sa[3]);
-        // every warp is past block j-1 (and has written its part for block j)
-        failed = coop_barrier_any(!got);
-        if (failed) break;
-        if (warp == 0 && j >= 1 && j - 1 + S < nblk) issue(j - 1 + S);
-        float sT[4] = {0.f, 0.f, 0.f, 0.f};
+        float4 *slot = sbuf + (k & 1) * (kDecodeWarps * BPP * 32);
 #pragma unroll
-        for (int w = 0; w < kDecodeWarps; ++w) {
-            const float4 v = slot[w * 32 + lane];
-            sT[0] += v.x;
-            sT[1] += v.y;
-            sT[2] += v.z;
-            sT[3] += v.w;
+        for (int b = 0; b < BPP; ++b)
+            slot[(warp * BPP + b) * 32 + lane] = make_float4(sa[b][0], sa[b][1], sa[b][2], sa[b][3]);
+        if (coop_barrier_any(!got)) {
+            // a wait ran out (every compute warp sees it here); the producer
+            // lets its copies land before it leaves
+            if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
+            return;
         }
-        // mask, scale to log2 units; element e: token g8 + 8(e/2), column 2cc + e%2
-        const int bt = (b0 + j) * bs;
-        const bool inside = bt >= lo_all && bt + bs <= hi_all;
-        float sv[4];
-        if (inside && okb) {
+        // the whole S^T of each block, mask, scale to log2 units; element e:
+        // token g8 + 8(e/2), column 2cc + e%2
+        float sv[BPP][4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) sv[e] = sT[e] * p.scale_log2;
-        } else {
+        for (int b = 0; b < BPP; ++b) {
+            float sT[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int pos = bt + g8 + 8 * (e >> 1);
-                sv[e] = (okb && pos >= lo_all && pos < hi_all) ? sT[e] * p.scale_log2 : -INFINITY;
+            for (int w = 0; w < kDecodeWarps; ++w) {
+                const float4 v = slot[(w * BPP + b) * 32 + lane];
+                sT[0] += v.x;
+                sT[1] += v.y;
+                sT[2] += v.z;
+                sT[3] += v.w;
+            }
+            if (okb[b] && bt[b] >= lo_all && bt[b] + bs <= hi_all) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sv[b][e] = sT[e] * p.scale_log2;
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int pos = bt[b] + g8 + 8 * (e >> 1);
+                    sv[b][e] = (okb[b] && pos >= lo_all && pos < hi_all) ? sT[e] * p.scale_log2 : -INFINITY;
+                }
             }
         }
-        // column maxima over the 16 tokens: this lane's two, then the 8 lanes of cc
+        // column maxima over the pass's tokens: this lane's, then the 8 lanes of cc
         float mu[2], al[2];
         bool grew = false;
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-            float mx = fmaxf(sv[e], sv[e + 2]);
+            float mx = -INFINITY;
+#pragma unroll
+            for (int b = 0; b < BPP; ++b) mx = fmaxf(mx, fmaxf(sv[b][e], sv[b][e + 2]));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
@@ -237,12 +282,17 @@ __device__ __forceinline__ void decode_coop_body(const CUtensorMap &kmap, const 
             grew = grew || mn != mc[e];
             mc[e] = mn;
         }
-        float pv[4];
+        float pv[BPP][4];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-            pv[e] = fast_exp2(sv[e] - mu[e]);
-            pv[e + 2] = fast_exp2(sv[e + 2] - mu[e]);
-            lc[e] = lc[e] * al[e] + (pv[e] + pv[e + 2]);
+            float sum = 0.f;
+#pragma unroll
+            for (int b = 0; b < BPP; ++b) {
+                pv[b][e] = fast_exp2(sv[b][e] - mu[e]);
+                pv[b][e + 2] = fast_exp2(sv[b][e + 2] - mu[e]);
+                sum += pv[b][e] + pv[b][e + 2];
+            }
+            lc[e] = lc[e] * al[e] + sum;
         }
         if (__any_sync(0xffffffffu, grew)) {
 #pragma unroll
@@ -253,48 +303,47 @@ __device__ __forceinline__ void decode_coop_body(const CUtensorMap &kmap, const 
                 oT[i][3] *= al[1];
             }
         }
-        // O^T += V^T P^T: P as a bf16 pair hi + lo (B fragment through
-        // movmatrix.trans), values of tokens outside the range zeroed (stale
-        // slots may hold NaN)
-        const uint32_t h0 = pack_bf16x2(pv[0], pv[1]);
-        const uint32_t h1 = pack_bf16x2(pv[2], pv[3]);
-        const uint32_t l0 = pack_bf16x2(pv[0] - bf16lo_to_f32(h0), pv[1] - bf16hi_to_f32(h0));
-        const uint32_t l1 = pack_bf16x2(pv[2] - bf16lo_to_f32(h1), pv[3] - bf16hi_to_f32(h1));
-        const uint32_t pb0 = movmatrix_trans(h0), pb1 = movmatrix_trans(h1);
-        const uint32_t pl0 = movmatrix_trans(l0), pl1 = movmatrix_trans(l1);
-        uint32_t mk0 = 0xffffffffu, mk1 = 0xffffffffu;
-        if (!inside || !okb) {
-            auto live = [&](int t) { return okb && bt + t >= lo_all && bt + t < hi_all; };
-            mk0 = (live(2 * cc) ? 0x0000ffffu : 0u) | (live(2 * cc + 1) ? 0xffff0000u : 0u);
-            mk1 = (live(2 * cc + 8) ? 0x0000ffffu : 0u) | (live(2 * cc + 9) ? 0xffff0000u : 0u);
-        }
+        // O^T += V^T P^T per block: P as a bf16 pair hi + lo (B fragment
+        // through movmatrix.trans), values of tokens outside the range zeroed
+        // (stale slots may hold NaN)
 #pragma unroll
-        for (int i = 0; i < C::kMT; ++i) {
-            uint32_t a[4];
-            ldsm_x4_trans(kv_chunk_addr(vt, va_tok, (warp * C::kMT + i) * 16 + va_dof), a[0], a[1], a[2],
-                          a[3]);
-            a[0] &= mk0;
-            a[1] &= mk0;
-            a[2] &= mk1;
-            a[3] &= mk1;
-            mma_16816(oT[i], a, pb0, pb1);
-            mma_16816(oT[i], a, pl0, pl1);
+        for (int b = 0; b < BPP; ++b) {
+            if (!okb[b]) continue;
+            const uint32_t vt = kt[b] + C::kTileBytes;
+            const uint32_t h0 = pack_bf16x2(pv[b][0], pv[b][1]);
+            const uint32_t h1 = pack_bf16x2(pv[b][2], pv[b][3]);
+            const uint32_t l0 = pack_bf16x2(pv[b][0] - bf16lo_to_f32(h0), pv[b][1] - bf16hi_to_f32(h0));
+            const uint32_t l1 = pack_bf16x2(pv[b][2] - bf16lo_to_f32(h1), pv[b][3] - bf16hi_to_f32(h1));
+            const uint32_t pb0 = movmatrix_trans(h0), pb1 = movmatrix_trans(h1);
+            const uint32_t pl0 = movmatrix_trans(l0), pl1 = movmatrix_trans(l1);
+            uint32_t mk0 = 0xffffffffu, mk1 = 0xffffffffu;
+            if (bt[b] < lo_all || bt[b] + bs > hi_all) {
+                const int t0 = bt[b];
+                auto live = [&](int t) { return t0 + t >= lo_all && t0 + t < hi_all; };
+                mk0 = (live(2 * cc) ? 0x0000ffffu : 0u) | (live(2 * cc + 1) ? 0xffff0000u : 0u);
+                mk1 = (live(2 * cc + 8) ? 0x0000ffffu : 0u) | (live(2 * cc + 9) ? 0xffff0000u : 0u);
+            }
+#pragma unroll
+            for (int i = 0; i < C::kMT; ++i) {
+                uint32_t a[4];
+                ldsm_x4_trans(kv_chunk_addr(vt, va_tok, (warp * C::kMT + i) * 16 + va_dof), a[0], a[1],
+                              a[2], a[3]);
+                a[0] &= mk0;
+                a[1] &= mk0;
+                a[2] &= mk1;
+                a[3] &= mk1;
+                mma_16816(oT[i], a, pb0, pb1);
+                mma_16816(oT[i], a, pl0, pl1);
+            }
         }
-        // this block's generic-proxy reads of the stage come before the
-        // async-proxy refill that the next barrier lets warp 0 issue
+        // release the pass's stages: these generic-proxy reads come before
+        // the producer's async-proxy refill
         fence_proxy_async_smem();
-    }
-    if (failed) {
-        // a wait ran out (every warp saw it at the same barrier): the blocks
-        // warp 0 issued and nobody consumed land before the CTA leaves.  While
-        // block j was awaited, blocks below j + S - 1 (S at j = 0) were issued.
-        if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
-        if (warp == 0 && lane == 0) {
-            const int32_t end = min(nblk, j + S - (j > 0 ? 1 : 0));
-            for (int32_t t = j; t < end; ++t)
-                if (!withheld(t)) mbar_wait(&full[t % S], (t / S) & 1);
-        }
-        return;
+        __syncwarp();
+        if (lane == 0)
+#pragma unroll
+            for (int b = 0; b < BPP; ++b)
+                if (have[b]) mbar_arrive(&empty[(k * BPP + b) % S]);
     }
 
     // column sums over the 8 lanes sharing cc
@@ -323,7 +372,7 @@ __device__ __forceinline__ void decode_coop_body(const CUtensorMap &kmap, const 
 }
 
 template <int D>
-__global__ void __launch_bounds__(kDecodeWarps * 32, CoopCfg<D>::kCtasPerSm)
+__global__ void __launch_bounds__(CoopCfg<D>::kThreads, CoopCfg<D>::kCtasPerSm)
     decode_coop_kernel(const __grid_constant__ CUtensorMap kmap,
                        const __grid_constant__ CUtensorMap vmap, const DecodeParams p)
 {
@@ -331,7 +380,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, CoopCfg<D>::kCtasPerSm)
 }
 
 template <int D>
-__global__ void __launch_bounds__(kDecodeWarps * 32, CoopCfg<D>::kCtasPerSm)
+__global__ void __launch_bounds__(CoopCfg<D>::kThreads, CoopCfg<D>::kCtasPerSm)
     decode_coop_grouped_kernel(const __grid_constant__ GroupedDecode gd)
 {
     int i = 0;
@@ -355,8 +404,8 @@ static cudaError_t launch_coop(const DecodeParams &p, const CUtensorMap &kmap,
                                cudaSharedmemCarveoutMaxShared);
     if (err != cudaSuccess) return err;
     prof_begin(PKV_KERNEL_DECODE_SPLIT, stream);
-    err = launch_pdl(kern, dim3(static_cast<unsigned>(ctas)), dim3(kDecodeWarps * 32), smem, stream,
-                     kmap, vmap, p);
+    err = launch_pdl(kern, dim3(static_cast<unsigned>(ctas)), dim3(CoopCfg<D>::kThreads), smem,
+                     stream, kmap, vmap, p);
     prof_end(PKV_KERNEL_DECODE_SPLIT, stream);
     return err;
 }
@@ -374,7 +423,8 @@ static cudaError_t launch_coop_grouped(const GroupedDecode &gd, cudaStream_t str
                                cudaSharedmemCarveoutMaxShared);
     if (err != cudaSuccess) return err;
     prof_begin(PKV_KERNEL_DECODE_SPLIT, stream);
-    err = launch_pdl(kern, dim3(static_cast<unsigned>(ctas)), dim3(kDecodeWarps * 32), smem, stream, gd);
+    err = launch_pdl(kern, dim3(static_cast<unsigned>(ctas)), dim3(CoopCfg<D>::kThreads), smem, stream,
+                     gd);
     prof_end(PKV_KERNEL_DECODE_SPLIT, stream);
     return err;
 }
