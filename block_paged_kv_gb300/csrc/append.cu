@@ -140,7 +140,8 @@ constexpr int kAppendMaxHeadsPerWarp = 8;
 // Token t of the call, kv heads h0 .. h0 + nh - 1, by one warp
 template <int D>
 __device__ __forceinline__ void append_fp8_token(const AppendParams &p, const int32_t t,
-                                                 const int32_t h0, const int32_t nh, const int lane)
+                                                 const int32_t h0, const int32_t nh, const int lane,
+                                                 const bool skip_whole = false)
 {
     constexpr int kPerHead = D / 4;                          // 4-byte words per head and tensor
     constexpr int kPerLane = (kPerHead + 31) / 32;
@@ -159,6 +160,7 @@ __device__ __forceinline__ void append_fp8_token(const AppendParams &p, const in
         mine = u >= 0 && u < p.num_tokens && __ldg(p.slot_mapping + u) == slot - off + lane;
     }
     const bool whole = __all_sync(0xffffffffu, mine);
+    if (whole && skip_whole) return;  // the block's tile is written whole elsewhere
     const int64_t tok_stride = static_cast<int64_t>(p.hkv) * D;  // elements per token row set
     const uint16_t *knew = static_cast<const uint16_t *>(p.k_new);
     const uint16_t *vnew = static_cast<const uint16_t *>(p.v_new);
@@ -256,12 +258,156 @@ __global__ void __launch_bounds__(256) append_fp8_kernel(AppendParams p)
                             static_cast<int32_t>(i % groups) * p.heads_per_warp, p.heads_per_warp, lane);
 }
 
+// Bulk FP8 append: one CTA per window of 16 tokens of the call.  A block
+// whose 16 tokens come in order from the call (its lead token, the one at
+// slot offset 0, lies in the window) is written as whole tiles: for each run
+// of HG kv heads, the 16 tokens' bf16 K and V rows are staged in shared memory
+// (16-byte asynchronous copies, rows padded to 2D + 16 bytes so that the
+// reads below hit distinct banks), then every thread forms whole 16-byte
+// chunks of the tiles in the tiles' byte order (a K chunk: one token, the 16
+// dims of one pair class over four 16-dim steps; a V chunk: one dim of four
+// tokens over four 8-dim steps) and stores them with coalesced 16-byte stores.
+// Tokens of blocks that are not whole (ragged chunk ends) are then written
+// by the per-token path, one warp per token.  At most one lead lies in a
+// window (a whole block spans 16 tokens of the call).
+constexpr int kAppendWindow = 16;
+
+template <int D>
+struct AppendWin {
+    static constexpr int kHG = 512 / D;          // kv heads per staging round
+    static constexpr int kRowB = 2 * D + 16;     // padded bytes of one (head, token) row
+    static constexpr int kTensorB = kHG * kAppendWindow * kRowB;
+    static constexpr int kSmem = 2 * kTensorB;   // K and V
+};
+
+template <int D>
+__global__ void __launch_bounds__(256) append_fp8_window_kernel(AppendParams p)
+{
+    using W = AppendWin<D>;
+    constexpr int HG = W::kHG;
+    extern __shared__ __align__(16) uint8_t sm[];
+    __shared__ int32_t s_lead;
+    pdl_wait();
+    pdl_trigger();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int32_t t0 = blockIdx.x * kAppendWindow;
+    // the window's lead of a whole block, if any: thread k checks token
+    // t0 + k/16 against the slot of token t0 + k/16 + k%16
+    if (threadIdx.x == 0) s_lead = -1;
+    __syncthreads();
+    {
+        const int32_t tw = t0 + (threadIdx.x >> 4), i = threadIdx.x & 15;
+        bool ok = false;
+        if (tw < p.num_tokens && tw + i < p.num_tokens) {
+            const int32_t s0 = __ldg(p.slot_mapping + tw);
+            ok = s0 >= 0 && s0 < p.num_slots && (s0 & 15) == 0 && __ldg(p.slot_mapping + tw + i) == s0 + i;
+        }
+        const uint32_t m = __ballot_sync(0xffffffffu, ok);
+        const uint32_t mine = (m >> (lane & 16)) & 0xFFFFu;
+        if (i == 0 && mine == 0xFFFFu) s_lead = tw;
+    }
+    __syncthreads();
+    const int32_t lead = s_lead;
+    if (lead >= 0) {
+        const int32_t blk = __ldg(p.slot_mapping + lead) >> 4;
+        const float ks = p.k_scale, vs = p.v_scale;
+        const float kr = __frcp_rn(ks), vr = __frcp_rn(vs);
+        for (int32_t h0 = 0; h0 < p.hkv; h0 += HG) {
+            const int nh = min(HG, p.hkv - h0);
+            // stage: tensor x (head, token) rows of D/8 16-byte chunks
+            constexpr int kRowChunks = D / 8;
+            constexpr int kChunks = 2 * HG * kAppendWindow * kRowChunks;
+            for (int q = threadIdx.x; q < kChunks; q += blockDim.x) {
+                const int tensor = q / (HG * kAppendWindow * kRowChunks);
+                const int rr = q % (HG * kAppendWindow * kRowChunks);
+                const int row = rr / kRowChunks, col = rr % kRowChunks;
+                const int hh = row / kAppendWindow, tok = row % kAppendWindow;
+                if (hh >= nh) continue;
+                const uint8_t *src = static_cast<const uint8_t *>(tensor ? p.v_new : p.k_new) +
+                                     ((static_cast<int64_t>(lead + tok) * p.hkv + h0 + hh) * D) * 2 +
+                                     col * 16;
+                const uint32_t dst = smem_u32(sm + tensor * W::kTensorB + row * W::kRowB + col * 16);
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+            }
+            asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+            __syncthreads();
+            // chunks: per head D of K then D of V, 16 bytes each
+            for (int q = threadIdx.x; q < nh * 2 * D; q += blockDim.x) {
+                const int hh = q / (2 * D), r = q % (2 * D);
+                const bool is_v = r >= D;
+                const int c = is_v ? r - D : r;
+                const uint8_t *base = sm + (is_v ? W::kTensorB : 0) + hh * kAppendWindow * W::kRowB;
+                uint32_t w4[4];
+                if (!is_v) {
+                    // byte 16c of the K tile: c = grp*64 + half*32 + t8*4 + cc; token
+                    // half*8 + t8, words kk: dims grp*64 + 16kk + 2cc + {0, 1, 8, 9}
+                    const int grp = c >> 6, tok = ((c >> 5) & 1) * 8 + ((c >> 2) & 7), cc = c & 3;
+                    const uint8_t *rowp = base + tok * W::kRowB;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const int d0 = grp * 64 + kk * 16 + 2 * cc;
+                        const uint32_t a = *reinterpret_cast<const uint32_t *>(rowp + d0 * 2);
+                        const uint32_t b = *reinterpret_cast<const uint32_t *>(rowp + (d0 + 8) * 2);
+                        w4[kk] = quant4(a, b, ks, kr);
+                    }
+                } else {
+                    // byte 16c of the V tile: c = g32*32 + n*4 + cq; words jn: dim
+                    // g32*32 + 8jn + n of tokens 2cq, 2cq + 1, 2cq + 8, 2cq + 9
+                    const int g32 = c >> 5, n = (c >> 2) & 7, cq = c & 3;
+                    const uint16_t *r0 = reinterpret_cast<const uint16_t *>(base + (2 * cq) * W::kRowB);
+                    const uint16_t *r1 = reinterpret_cast<const uint16_t *>(base + (2 * cq + 1) * W::kRowB);
+                    const uint16_t *r8 = reinterpret_cast<const uint16_t *>(base + (2 * cq + 8) * W::kRowB);
+                    const uint16_t *r9 = reinterpret_cast<const uint16_t *>(base + (2 * cq + 9) * W::kRowB);
+#pragma unroll
+                    for (int jn = 0; jn < 4; ++jn) {
+                        const int d = g32 * 32 + jn * 8 + n;
+                        const uint32_t a = static_cast<uint32_t>(r0[d]) | (static_cast<uint32_t>(r1[d]) << 16);
+                        const uint32_t b = static_cast<uint32_t>(r8[d]) | (static_cast<uint32_t>(r9[d]) << 16);
+                        w4[jn] = quant4(a, b, vs, vr);
+                    }
+                }
+                uint8_t *tile = static_cast<uint8_t *>(is_v ? p.v_pool : p.k_pool) +
+                                (static_cast<int64_t>(blk) * p.hkv + h0 + hh) * (16 * D);
+                __stcs(reinterpret_cast<uint4 *>(tile) + c, make_uint4(w4[0], w4[1], w4[2], w4[3]));
+            }
+            __syncthreads();  // the staging rows are refilled by the next round
+        }
+    }
+    // tokens of the window whose block is not whole: one warp per token
+    for (int32_t i = warp; i < kAppendWindow; i += blockDim.x >> 5) {
+        const int32_t t = t0 + i;
+        if (t >= p.num_tokens) break;
+        for (int32_t h0 = 0; h0 < p.hkv; h0 += kAppendMaxHeadsPerWarp)
+            append_fp8_token<D>(p, t, h0, min(kAppendMaxHeadsPerWarp, p.hkv - h0), lane, true);
+    }
+}
+
 cudaError_t launch_append_fp8(const AppendParams &p, cudaStream_t stream)
 {
     if (p.num_tokens == 0 || p.hkv == 0) return cudaSuccess;
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) == cudaSuccess)
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (p.head_dim != 64 && p.head_dim != 128 && p.head_dim != 256) return cudaErrorInvalidValue;
+    // bulk appends (a prefill chunk, a whole context): whole-tile windows
+    if (static_cast<int64_t>(p.num_tokens) >= 8ll * sms) {
+        const unsigned grid = static_cast<unsigned>((p.num_tokens + kAppendWindow - 1) / kAppendWindow);
+        cudaError_t err;
+        prof_begin(PKV_KERNEL_APPEND, stream);
+        switch (p.head_dim) {
+        case 64:
+            err = launch_pdl(append_fp8_window_kernel<64>, dim3(grid), dim3(256), AppendWin<64>::kSmem, stream, p);
+            break;
+        case 128:
+            err = launch_pdl(append_fp8_window_kernel<128>, dim3(grid), dim3(256), AppendWin<128>::kSmem, stream, p);
+            break;
+        default:
+            err = launch_pdl(append_fp8_window_kernel<256>, dim3(grid), dim3(256), AppendWin<256>::kSmem, stream, p);
+            break;
+        }
+        prof_end(PKV_KERNEL_APPEND, stream);
+        return err;
+    }
     // a warp takes all kv heads of a token (the slot checks once per token)
     // unless that leaves fewer than 32 warps per SM (a decode step's few
     // tokens): then fewer heads per warp, down to one
@@ -278,7 +424,6 @@ cudaError_t launch_append_fp8(const AppendParams &p, cudaStream_t stream)
     const int64_t blocks = std::min<int64_t>((warps + 7) / 8, static_cast<int64_t>(sms) * 8);
     auto kern = p.head_dim == 64 ? append_fp8_kernel<64>
                                  : (p.head_dim == 128 ? append_fp8_kernel<128> : append_fp8_kernel<256>);
-    if (p.head_dim != 64 && p.head_dim != 128 && p.head_dim != 256) return cudaErrorInvalidValue;
     prof_begin(PKV_KERNEL_APPEND, stream);
     const cudaError_t err = launch_pdl(kern, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, q);
     prof_end(PKV_KERNEL_APPEND, stream);

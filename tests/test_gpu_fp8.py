@@ -149,14 +149,41 @@ def test_append_chunks_whole_blocks_and_ragged_ends(pkv, orc, d, hkv, shuffle):
     assert np.array_equal(k_d.cpu().numpy(), kp) and np.array_equal(v_d.cpu().numpy(), vp)
 
 
+@pytest.mark.parametrize("d,hkv", [(64, 8), (64, 9), (128, 8), (128, 3), (256, 2), (256, 5)])
+@pytest.mark.parametrize("shuffle", [False, True])
+def test_append_bulk_windows_bit_exact(pkv, orc, d, hkv, shuffle):
+    # a bulk append (2000+ tokens, the windowed kernel: whole blocks as tiles
+    # staged a few kv heads at a time, ragged chunk ends token by token; the
+    # head counts leave partial staging rounds), every pool byte against the
+    # oracle; shuffled, no block is whole
+    w = gen.prefill_workload(seed=317 + d + hkv, dtype="bf16", num_q_heads=hkv, num_kv_heads=hkv,
+                             head_dim=d, prefix_lens=[0, 13, 250, 7], chunk_lens=[700, 333, 500, 611])
+    slots = pkv.slot_mapping_host(w.block_tables, w.num_blocks, w.new_rows, w.new_pos, 16)
+    assert slots.shape[0] >= 2048
+    order = np.arange(slots.shape[0])
+    if shuffle:
+        order = gen.permutation(318, "order", slots.shape[0]).astype(np.int64)
+    s, kr, vr = (np.ascontiguousarray(a[order]) for a in (slots, w.k_new, w.v_new))
+    kp, vp = gen.fp8_empty_pools(w)
+    k_d, v_d = torch.from_numpy(kp).cuda(), torch.from_numpy(vp).cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv.paged_kv_append(k_d, v_d, torch.from_numpy(s).cuda(), to_torch(kr, "bf16"),
+                        to_torch(vr, "bf16"), status=status, k_scale=KS, v_scale=VS)
+    orc.append(kp, vp, "fp8", s, kr, vr, KS, VS)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert np.array_equal(k_d.cpu().numpy(), kp) and np.array_equal(v_d.cpu().numpy(), vp)
+
+
 # a scale that puts 1.0 / scale 3 float32 ulps above the midpoint 1.0625
 # between the E4M3 values 1.0 and 1.125 (and 2^k / scale above 1.0625 * 2^k)
 _NEAR_TIE_SCALE = float(np.float32(1.0 / (1.0625 * (1 + 3 * 2.0 ** -24))))
 
 
+@pytest.mark.parametrize("bulk", [False, True])
 @pytest.mark.parametrize("whole_blocks", [False, True])
 @pytest.mark.parametrize("scale", [KS, 0.25, _NEAR_TIE_SCALE])
-def test_append_codes_at_rounding_boundaries(pkv, orc, whole_blocks, scale):
+def test_append_codes_at_rounding_boundaries(pkv, orc, whole_blocks, scale, bulk):
     # rows whose quotients x / scale sit on and next to the midpoints between
     # neighbouring E4M3 values, both signs, normal and subnormal codes, 448:
     # with a power-of-two scale the quotients are exact ties; the crafted
@@ -170,6 +197,8 @@ def test_append_codes_at_rounding_boundaries(pkv, orc, whole_blocks, scale):
     vals = np.concatenate([near, near | np.uint16(0x8000)])
     D, hkv = 128, 2
     T = 16 * (len(vals) // (D * hkv * 16) + 1)   # whole blocks of tokens
+    if bulk:
+        T = 2048  # the windowed bulk kernel
     kn = np.resize(vals, T * hkv * D).reshape(T, hkv, D).astype(np.uint16)
     vn = np.resize(vals[::-1], T * hkv * D).reshape(T, hkv, D).astype(np.uint16)
     if whole_blocks:
