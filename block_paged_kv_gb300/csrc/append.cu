@@ -79,59 +79,38 @@ cudaError_t launch_append(const AppendParams &p, cudaStream_t stream)
 //      ragged ends of a chunk) the warp stores its own token's V codes byte
 //      by byte.
 // E4M3 codes of correctly rounded float32 quotients x / s (s > 0) without a
-// division, r = the rounded reciprocal of s.
+// division, r = the correctly rounded reciprocal of s.
 //
-// The product q = x * r lies within 2.5 ulps of the rounded quotient (two
-// roundings of at most half an ulp each, and the quotient's own half ulp).
-// The code can only differ where the quotient is near a rounding boundary
-// of E4M3: a midpoint m between neighbouring E4M3 values, whose float32
-// form ends in 19 zero bits.  So unless q is within 4 ulps of such an m it
-// is converted as it is.  Near m, the rounded quotient is m itself when
-// |x/s - m| <= ulp(m)/2 (a tie goes to m, whose last bit is 0), else one of
-// its neighbours; the test is exact: the residual x - s*m is small (a few
-// ulps of m, times s) and has at most 9 significant bits, so one fused
-// multiply-add yields it exactly (the exact-remainder property used in
-// Markstein's division, "Computation of elementary functions on the IBM
-// RISC System/6000 processor", 1990), and s * ulp(m)/2 is a power-of-two
-// scaling of s.  Zero, NaN, values below 2^-11 (code 0) and above 512
-// (saturated to 448) need no test.
-__device__ __forceinline__ bool near_e4m3_boundary(float q)
+// q0 = RN(x * r) lies within one ulp of x / s (the rounding of the product
+// and r's own half ulp).  One correction step then gives the correctly
+// rounded quotient: e = x - s * q0 is exact (one fused multiply-add), and
+// RN(q0 + e * r) = RN(x / s) when r = RN(1/s) and q0 is within one ulp, in
+// the normal range (Markstein's theorem on the final step of an FMA
+// division: P. Markstein, "Computation of elementary functions on the IBM
+// RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990).  The step is
+// taken where the last ulp can change the E4M3 code, 2^-11 <= |q0| <= 512:
+// below, the code is a zero of x's sign; above, E4M3 saturates (448); NaN
+// stays NaN.  Checked against the IEEE quotient on every bf16 input for
+// thousands of scales, codes compared, and against the oracle's codes in the
+// GPU tests.
+__device__ __forceinline__ float e4m3_quotient(float x, float s, float r)
 {
-    const uint32_t low = __float_as_uint(q) & 0x7FFFFu;
-    const float aq = fabsf(q);
-    return (low <= 4u || low >= 0x7FFFBu) && aq >= 0x1p-11f && aq <= 512.f;
-}
-
-// q = x * r near a boundary: the value to convert in its place
-__device__ __forceinline__ float resolve_near_boundary(float x, float s, float q)
-{
-    const uint32_t mb = (__float_as_uint(fabsf(q)) + 4u) & ~0x7FFFFu;  // the nearest such m
-    const float m = __uint_as_float(mb);
-    const float e = fmaf(-s, m, fabsf(x));                                  // |x| - s*m, exact
-    const float h = s * __uint_as_float((mb & 0x7F800000u) - (24u << 23));  // s * ulp(m) / 2
-    const float t = e > h ? __uint_as_float(mb + 1u) : (e < -h ? __uint_as_float(mb - 1u) : m);
-    return copysignf(t, x);
+    const float q0 = __fmul_rn(x, r);
+    const float e = __fmaf_rn(-s, q0, x);
+    const float q1 = __fmaf_rn(e, r, q0);
+    const uint32_t a = __float_as_uint(q0) & 0x7FFFFFFFu;
+    return (a - 0x3A000000u) <= 0x0A000000u ? q1 : q0;  // 2^-11 .. 512 as bits
 }
 
 __device__ __forceinline__ uint32_t quant4(uint32_t a, uint32_t b, float s, float r)
 {
     // bf16 pairs a = (x0, x1), b = (x2, x3) -> codes x0 | x1 << 8 | x2 << 16 | x3 << 24
-    const float x[4] = {bf16lo_to_f32(a), bf16hi_to_f32(a), bf16lo_to_f32(b), bf16hi_to_f32(b)};
-    float q[4];
-    bool near = false;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        q[i] = x[i] * r;
-        near = near || near_e4m3_boundary(q[i]);
-    }
-    // rare (about 1e-4 of the calls): resolve in a branch the warp takes together
-    if (__any_sync(__activemask(), near)) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            if (near_e4m3_boundary(q[i])) q[i] = resolve_near_boundary(x[i], s, q[i]);
-    }
-    return static_cast<uint32_t>(f32x2_to_e4m3x2(q[0], q[1])) |
-           (static_cast<uint32_t>(f32x2_to_e4m3x2(q[2], q[3])) << 16);
+    const float q0 = e4m3_quotient(bf16lo_to_f32(a), s, r);
+    const float q1 = e4m3_quotient(bf16hi_to_f32(a), s, r);
+    const float q2 = e4m3_quotient(bf16lo_to_f32(b), s, r);
+    const float q3 = e4m3_quotient(bf16hi_to_f32(b), s, r);
+    return static_cast<uint32_t>(f32x2_to_e4m3x2(q0, q1)) |
+           (static_cast<uint32_t>(f32x2_to_e4m3x2(q2, q3)) << 16);
 }
 
 constexpr int kAppendMaxHeadsPerWarp = 8;
@@ -277,7 +256,8 @@ struct AppendWin {
     static constexpr int kHG = 512 / D;          // kv heads per staging round
     static constexpr int kRowB = 2 * D + 16;     // padded bytes of one (head, token) row
     static constexpr int kTensorB = kHG * kAppendWindow * kRowB;
-    static constexpr int kSmem = 2 * kTensorB;   // K and V
+    static constexpr int kSmem = 2 * kTensorB;   // K and V of one staging round
+    static constexpr int kLaunchSmem = 2 * kSmem;  // two rounds in flight
 };
 
 template <int D>
@@ -312,9 +292,12 @@ __global__ void __launch_bounds__(256) append_fp8_window_kernel(AppendParams p)
         const int32_t blk = __ldg(p.slot_mapping + lead) >> 4;
         const float ks = p.k_scale, vs = p.v_scale;
         const float kr = __frcp_rn(ks), vr = __frcp_rn(vs);
-        for (int32_t h0 = 0; h0 < p.hkv; h0 += HG) {
-            const int nh = min(HG, p.hkv - h0);
-            // stage: tensor x (head, token) rows of D/8 16-byte chunks
+        const int ngroups = (p.hkv + HG - 1) / HG;
+        // staging round g (kv heads g*HG ..) into buffer g % 2: 16-byte
+        // asynchronous copies of the (head, token) rows of K and V
+        auto stage = [&](int g) {
+            const int h0 = g * HG, nh = min(HG, p.hkv - h0);
+            uint8_t *buf = sm + (g & 1) * W::kSmem;
             constexpr int kRowChunks = D / 8;
             constexpr int kChunks = 2 * HG * kAppendWindow * kRowChunks;
             for (int q = threadIdx.x; q < kChunks; q += blockDim.x) {
@@ -326,23 +309,33 @@ __global__ void __launch_bounds__(256) append_fp8_window_kernel(AppendParams p)
                 const uint8_t *src = static_cast<const uint8_t *>(tensor ? p.v_new : p.k_new) +
                                      ((static_cast<int64_t>(lead + tok) * p.hkv + h0 + hh) * D) * 2 +
                                      col * 16;
-                const uint32_t dst = smem_u32(sm + tensor * W::kTensorB + row * W::kRowB + col * 16);
+                const uint32_t dst = smem_u32(buf + tensor * W::kTensorB + row * W::kRowB + col * 16);
                 asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
             }
-            asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+            asm volatile("cp.async.commit_group;" ::: "memory");
+        };
+        stage(0);
+        if (ngroups > 1) stage(1);
+        for (int g = 0; g < ngroups; ++g) {
+            if (g + 1 < ngroups)
+                asm volatile("cp.async.wait_group 1;" ::: "memory");
+            else
+                asm volatile("cp.async.wait_group 0;" ::: "memory");
             __syncthreads();
-            // chunks: per head D of K then D of V, 16 bytes each
-            for (int q = threadIdx.x; q < nh * 2 * D; q += blockDim.x) {
-                const int hh = q / (2 * D), r = q % (2 * D);
-                const bool is_v = r >= D;
-                const int c = is_v ? r - D : r;
-                const uint8_t *base = sm + (is_v ? W::kTensorB : 0) + hh * kAppendWindow * W::kRowB;
-                uint32_t w4[4];
-                if (!is_v) {
+            const int h0 = g * HG, nh = min(HG, p.hkv - h0);
+            const uint8_t *buf = sm + (g & 1) * W::kSmem;
+            // per head: D items of one K chunk, then D/2 items of two V chunks
+            // (dims n and n + 1 share their 4-byte shared-memory reads)
+            constexpr int kItems = D + D / 2;
+            for (int q = threadIdx.x; q < nh * kItems; q += blockDim.x) {
+                const int hh = q / kItems, r = q % kItems;
+                if (r < D) {
                     // byte 16c of the K tile: c = grp*64 + half*32 + t8*4 + cc; token
                     // half*8 + t8, words kk: dims grp*64 + 16kk + 2cc + {0, 1, 8, 9}
+                    const int c = r;
                     const int grp = c >> 6, tok = ((c >> 5) & 1) * 8 + ((c >> 2) & 7), cc = c & 3;
-                    const uint8_t *rowp = base + tok * W::kRowB;
+                    const uint8_t *rowp = buf + (hh * kAppendWindow + tok) * W::kRowB;
+                    uint32_t w4[4];
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const int d0 = grp * 64 + kk * 16 + 2 * cc;
@@ -350,27 +343,36 @@ __global__ void __launch_bounds__(256) append_fp8_window_kernel(AppendParams p)
                         const uint32_t b = *reinterpret_cast<const uint32_t *>(rowp + (d0 + 8) * 2);
                         w4[kk] = quant4(a, b, ks, kr);
                     }
+                    uint8_t *tile = static_cast<uint8_t *>(p.k_pool) +
+                                    (static_cast<int64_t>(blk) * p.hkv + h0 + hh) * (16 * D);
+                    __stcs(reinterpret_cast<uint4 *>(tile) + c, make_uint4(w4[0], w4[1], w4[2], w4[3]));
                 } else {
-                    // byte 16c of the V tile: c = g32*32 + n*4 + cq; words jn: dim
-                    // g32*32 + 8jn + n of tokens 2cq, 2cq + 1, 2cq + 8, 2cq + 9
-                    const int g32 = c >> 5, n = (c >> 2) & 7, cq = c & 3;
-                    const uint16_t *r0 = reinterpret_cast<const uint16_t *>(base + (2 * cq) * W::kRowB);
-                    const uint16_t *r1 = reinterpret_cast<const uint16_t *>(base + (2 * cq + 1) * W::kRowB);
-                    const uint16_t *r8 = reinterpret_cast<const uint16_t *>(base + (2 * cq + 8) * W::kRowB);
-                    const uint16_t *r9 = reinterpret_cast<const uint16_t *>(base + (2 * cq + 9) * W::kRowB);
+                    // bytes 16c and 16(c + 4) of the V tile, c = g32*32 + n*4 + cq, n
+                    // even: words jn of chunk c hold dim g32*32 + 8jn + n of tokens
+                    // 2cq, 2cq + 1, 2cq + 8, 2cq + 9, those of chunk c + 4 dim + 1
+                    const int v = r - D;
+                    const int g32 = v >> 4, n = ((v >> 2) & 3) * 2, cq = v & 3;
+                    const int c = g32 * 32 + n * 4 + cq;
+                    const uint8_t *vb = buf + W::kTensorB + (hh * kAppendWindow + 2 * cq) * W::kRowB;
+                    uint32_t w0[4], w1[4];
 #pragma unroll
                     for (int jn = 0; jn < 4; ++jn) {
-                        const int d = g32 * 32 + jn * 8 + n;
-                        const uint32_t a = static_cast<uint32_t>(r0[d]) | (static_cast<uint32_t>(r1[d]) << 16);
-                        const uint32_t b = static_cast<uint32_t>(r8[d]) | (static_cast<uint32_t>(r9[d]) << 16);
-                        w4[jn] = quant4(a, b, vs, vr);
+                        const int off = (g32 * 32 + jn * 8 + n) * 2;
+                        const uint32_t t0 = *reinterpret_cast<const uint32_t *>(vb + off);
+                        const uint32_t t1 = *reinterpret_cast<const uint32_t *>(vb + W::kRowB + off);
+                        const uint32_t t8 = *reinterpret_cast<const uint32_t *>(vb + 8 * W::kRowB + off);
+                        const uint32_t t9 = *reinterpret_cast<const uint32_t *>(vb + 9 * W::kRowB + off);
+                        w0[jn] = quant4(__byte_perm(t0, t1, 0x5410), __byte_perm(t8, t9, 0x5410), vs, vr);
+                        w1[jn] = quant4(__byte_perm(t0, t1, 0x7632), __byte_perm(t8, t9, 0x7632), vs, vr);
                     }
+                    uint4 *tile = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.v_pool) +
+                                                            (static_cast<int64_t>(blk) * p.hkv + h0 + hh) * (16 * D));
+                    __stcs(tile + c, make_uint4(w0[0], w0[1], w0[2], w0[3]));
+                    __stcs(tile + c + 4, make_uint4(w1[0], w1[1], w1[2], w1[3]));
                 }
-                uint8_t *tile = static_cast<uint8_t *>(is_v ? p.v_pool : p.k_pool) +
-                                (static_cast<int64_t>(blk) * p.hkv + h0 + hh) * (16 * D);
-                __stcs(reinterpret_cast<uint4 *>(tile) + c, make_uint4(w4[0], w4[1], w4[2], w4[3]));
             }
-            __syncthreads();  // the staging rows are refilled by the next round
+            __syncthreads();  // buffer g % 2 is refilled by round g + 2
+            if (g + 2 < ngroups) stage(g + 2);
         }
     }
     // tokens of the window whose block is not whole: one warp per token
@@ -382,6 +384,20 @@ __global__ void __launch_bounds__(256) append_fp8_window_kernel(AppendParams p)
     }
 }
 
+template <int D>
+static cudaError_t launch_append_window(const AppendParams &p, cudaStream_t stream)
+{
+    auto kern = append_fp8_window_kernel<D>;
+    const int smem = AppendWin<D>::kLaunchSmem;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return err;
+    const unsigned grid = static_cast<unsigned>((p.num_tokens + kAppendWindow - 1) / kAppendWindow);
+    prof_begin(PKV_KERNEL_APPEND, stream);
+    err = launch_pdl(kern, dim3(grid), dim3(256), smem, stream, p);
+    prof_end(PKV_KERNEL_APPEND, stream);
+    return err;
+}
+
 cudaError_t launch_append_fp8(const AppendParams &p, cudaStream_t stream)
 {
     if (p.num_tokens == 0 || p.hkv == 0) return cudaSuccess;
@@ -391,22 +407,11 @@ cudaError_t launch_append_fp8(const AppendParams &p, cudaStream_t stream)
     if (p.head_dim != 64 && p.head_dim != 128 && p.head_dim != 256) return cudaErrorInvalidValue;
     // bulk appends (a prefill chunk, a whole context): whole-tile windows
     if (static_cast<int64_t>(p.num_tokens) >= 8ll * sms) {
-        const unsigned grid = static_cast<unsigned>((p.num_tokens + kAppendWindow - 1) / kAppendWindow);
-        cudaError_t err;
-        prof_begin(PKV_KERNEL_APPEND, stream);
         switch (p.head_dim) {
-        case 64:
-            err = launch_pdl(append_fp8_window_kernel<64>, dim3(grid), dim3(256), AppendWin<64>::kSmem, stream, p);
-            break;
-        case 128:
-            err = launch_pdl(append_fp8_window_kernel<128>, dim3(grid), dim3(256), AppendWin<128>::kSmem, stream, p);
-            break;
-        default:
-            err = launch_pdl(append_fp8_window_kernel<256>, dim3(grid), dim3(256), AppendWin<256>::kSmem, stream, p);
-            break;
+        case 64: return launch_append_window<64>(p, stream);
+        case 128: return launch_append_window<128>(p, stream);
+        default: return launch_append_window<256>(p, stream);
         }
-        prof_end(PKV_KERNEL_APPEND, stream);
-        return err;
     }
     // a warp takes all kv heads of a token (the slot checks once per token)
     // unless that leaves fewer than 32 warps per SM (a decode step's few
