@@ -128,7 +128,8 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 def kernel_source_sha():
     h = hashlib.sha256()
-    for f in ("decode_kernel.cuh", "decode_bf16.cu", "decode_common.cuh", "pkv_device.cuh"):
+    for f in ("decode_kernel.cuh", "decode_coop.cuh", "decode_bf16.cu", "decode_common.cuh", "pkv_device.cuh",
+              "pkv_internal.h"):
         with open(os.path.join(ROOT, "block_paged_kv_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
