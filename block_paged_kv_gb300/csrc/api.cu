@@ -165,6 +165,12 @@ DecodePlan make_plan(int32_t batch, int32_t hq, int32_t hkv, int32_t D, int32_t 
     }
     pl.nslot = pl.n_prefix_splits + pl.n_suffix_splits;
     pl.n_suffix_ctas = static_cast<int64_t>(pl.n_suffix_splits) * hkv * batch;
+    // The cooperative kernel (its warps share every block) for long runs, or
+    // for a grid under half the SMs; runs of 16 blocks over a full grid
+    // (4 rows x 2048 tokens) were faster on the many-row kernel (17.4 against
+    // 18.9 us per call), runs of 28 (4 rows x 32768) and the 4-block runs of a
+    // 512-token window slower (35.9 against 33.4, 15.4 against 12.6 us).
+    pl.coop = few && (C >= 24 || 2 * pl.n_suffix_ctas < num_sms) ? 1 : 0;
     return pl;
 }
 

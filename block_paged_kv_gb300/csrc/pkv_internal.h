@@ -55,6 +55,8 @@ struct DecodePlan {
     int32_t prefix_chunks;        // CTAs per (group, kv head, prefix split) over its rows
     int32_t prefix_max;           // prefix lengths are clamped to this (<= table width)
     int32_t few;                  // rows x kv heads < SMs: a few long rows, about two CTAs per SM
+    int32_t coop;                 // few, and runs long enough (or a grid small enough) for the
+                                  // cooperative kernel (bf16, one query per row, G <= 8)
     int64_t n_prefix_ctas;
     int64_t n_suffix_ctas;
 };

@@ -180,14 +180,14 @@ def test_append_bulk_windows_bit_exact(pkv, orc, d, hkv, shuffle):
 _NEAR_TIE_SCALE = float(np.float32(1.0 / (1.0625 * (1 + 3 * 2.0 ** -24))))
 
 
-@pytest.mark.parametrize("bulk", [False, True])
-@pytest.mark.parametrize("whole_blocks", [False, True])
 # a scale at which x = 3 gives a quotient just above a midpoint that the
 # plain product x * RN(1/s) would land on (the quantizer's correction step
 # must restore the quotient's code)
 _PRODUCT_ON_MIDPOINT_SCALE = 11.294116973876953
 
 
+@pytest.mark.parametrize("bulk", [False, True])
+@pytest.mark.parametrize("whole_blocks", [False, True])
 @pytest.mark.parametrize("scale", [KS, 0.25, _NEAR_TIE_SCALE, _PRODUCT_ON_MIDPOINT_SCALE])
 def test_append_codes_at_rounding_boundaries(pkv, orc, whole_blocks, scale, bulk):
     # rows whose quotients x / scale sit on and next to the midpoints between
