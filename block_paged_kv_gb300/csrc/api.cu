@@ -656,6 +656,15 @@ bool verify_on_decode(int32_t G, int32_t D, int32_t bs, int32_t max_q_len)
            decode_shape_built(PKV_BF16, D, bs, G);
 }
 
+// Items of the tensor-core prefill: (row, kv head, query-tile pair).
+int32_t prefill_items(int32_t batch, int32_t hq, int32_t hkv, int32_t max_q_len)
+{
+    if (hkv <= 0 || hq % hkv != 0) return 0;
+    const int32_t qpc = prefill_queries_per_cta(PKV_BF16, hq / hkv);
+    const int64_t n = static_cast<int64_t>(batch) * hkv * ((max_q_len + qpc - 1) / qpc);
+    return n > INT32_MAX ? 0 : static_cast<int32_t>(n);
+}
+
 // The decode plan for a verify step: the key range of a row spans its
 // queries' windows.
 DecodePlan verify_plan(int32_t batch, int32_t hq, int32_t hkv, int32_t D, int32_t bs,
@@ -684,9 +693,13 @@ size_t paged_prefill_workspace_size(int32_t batch, int32_t num_q_heads, int32_t 
                                           max_seq_len, window, max_q_len);
         return ws_total_bytes(batch * max_q_len, num_q_heads, head_dim, pl);
     }
+    const int sms = num_sms_current();
     const PrefillSplit sp = prefill_split_plan(batch, num_q_heads, num_kv_heads, head_dim, block_size,
-                                               max_q_len, max_seq_len, window, num_sms_current());
-    return prefill_split_ws_bytes(batch, num_q_heads, max_q_len, sp);
+                                               max_q_len, max_seq_len, window, sms);
+    const int32_t sk = prefill_sk_ctas(PKV_BF16, batch, num_q_heads, num_kv_heads, head_dim, block_size,
+                                       max_q_len, sms);
+    return std::max(prefill_split_ws_bytes(batch, num_q_heads, max_q_len, sp),
+                    prefill_sk_ws_bytes(prefill_items(batch, num_q_heads, num_kv_heads, max_q_len), sk));
 }
 
 pkv_status paged_prefill_chunk_attention(const void *q, const int32_t *cu_q_lens,
@@ -818,6 +831,29 @@ pkv_status paged_prefill_chunk_attention(const void *q, const int32_t *cu_q_lens
         p.v_scale = pool->v_scale;
     }
     drill_settings(&p.wait_ns, &p.drill);
+    p.sk_ctas = 0;
+    p.sk_items = 0;
+    if (pool->dtype != PKV_F32 && p.kv_splits == 1) {
+        const int32_t sk = prefill_sk_ctas(pool->dtype, batch, num_q_heads, pool->num_kv_heads,
+                                           pool->head_dim, pool->block_size, max_q_len, num_sms_current());
+        if (sk > 0) {
+            const int32_t items = prefill_items(batch, num_q_heads, pool->num_kv_heads, max_q_len);
+            if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+                ws_bytes < prefill_sk_ws_bytes(items, sk))
+                return PKV_ERR_WORKSPACE;
+            p.sk_ctas = sk;
+            p.sk_items = items;
+            char *ws = static_cast<char *>(workspace);
+            p.sk_prefix = reinterpret_cast<int32_t *>(ws);
+            ws += (static_cast<size_t>(items + 1) * sizeof(int32_t) + 255) & ~static_cast<size_t>(255);
+            p.sk_count = reinterpret_cast<int32_t *>(ws);
+            ws += (static_cast<size_t>(sk) * 8 * sizeof(int32_t) + 255) & ~static_cast<size_t>(255);
+            p.sk_o = reinterpret_cast<float *>(ws);
+            const size_t rows = static_cast<size_t>(sk) * 2 * 256;
+            ws += (rows * 128 * sizeof(float) + 255) & ~static_cast<size_t>(255);
+            p.sk_ml = reinterpret_cast<float *>(ws);
+        }
+    }
     if (static_cast<int64_t>(batch) * p.hkv * p.q_tiles * p.kv_splits > INT32_MAX)
         return PKV_ERR_UNSUPPORTED;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

@@ -146,6 +146,16 @@ struct PrefillParams {
     int32_t split_tiles;
     float *ws_o;   // [batch][max_q_len][hq][kv_splits][128] unnormalised weighted values
     float *ws_ml;  // [batch][max_q_len][hq][kv_splits][2]: reference max (log2 units), weight sum
+    // persistent balanced schedule ("stream-K"; 0 = off): sk_ctas CTAs take
+    // equal runs of the (item, 64-key tile) sequence of the sk_items items
+    // (row, kv head, query-tile pair); a run that cuts an item writes a
+    // partial to one of its CTA's two slots
+    int32_t sk_ctas, sk_items;
+    int32_t *sk_prefix;  // [sk_items + 1]: tiles of items 0 .. u-1 (written by the plan kernel)
+    int32_t *sk_count;   // [sk_ctas][2 query tiles][4 warps]: pieces done of the item cut
+                         // after the CTA's first tile (zeroed by the plan kernel)
+    float *sk_o;         // [sk_ctas][2][256 rows][128] unnormalised weighted values
+    float *sk_ml;        // [sk_ctas][2][256 rows][2]: reference max (log2 units), weight sum
     float scale_log2;  // scale * log2(e) (* k_scale for FP8 pools)
     float v_scale;     // FP8 pools: applied to the weighted values
     uint64_t wait_ns;  // limit of the pipeline's data waits (kWaitLimitNs unless a drill)
@@ -170,6 +180,11 @@ PrefillSplit prefill_split_plan(int32_t batch, int32_t hq, int32_t hkv, int32_t 
                                 int32_t max_q_len, int32_t max_seq_len, int32_t window,
                                 int num_sms);
 size_t prefill_split_ws_bytes(int32_t batch, int32_t hq, int32_t max_q_len, const PrefillSplit &sp);
+// The persistent balanced schedule of the tensor-core prefill: the CTA count
+// (0 = off: the grid then holds one CTA per item) and its workspace.
+int32_t prefill_sk_ctas(pkv_dtype dtype, int32_t batch, int32_t hq, int32_t hkv, int32_t D,
+                        int32_t bs, int32_t max_q_len, int num_sms);
+size_t prefill_sk_ws_bytes(int32_t items, int32_t ctas);
 cudaError_t launch_prefill_bf16(const PrefillParams &p, const CUtensorMap &kmap,
                                 const CUtensorMap &vmap, cudaStream_t stream);
 cudaError_t launch_prefill_f32(const PrefillParams &p, cudaStream_t stream);

@@ -54,24 +54,25 @@ constexpr int kVOff = kKOff + kStages * kTileBytes;
 // by bulk copy, two tiles deep, and widen them into the ring
 constexpr int kF8BlockBytes = 16 * kD;                 // one (block, kv head) E4M3 tile
 constexpr int kF8StageTile = kBlocks * kF8BlockBytes;  // 8 KiB
+constexpr int kSoftmaxWarps = 8;  // 4-7 softmax of query tile A, 8-11 of tile B
 template <bool kF8>
 struct Layout {
     static constexpr int kStagingOff = kVOff + kStages * kTileBytes;
     static constexpr int kStagingBytes = kF8 ? 2 * 2 * kF8StageTile : 0;  // K and V, 2 deep
     static constexpr int kBarOff = kStagingOff + kStagingBytes;
     // barriers: k_full[4], k_empty[4], v_full[4], v_empty[4], s_full[tile][buf],
-    // p_full[tile][buf], pv_done[tile], mma_drain[tile], FP8: staged[K/V][2]
-    static constexpr int kNumBars = 4 * kStages + 4 + 4 + 2 + 2 + (kF8 ? 4 : 0);
+    // p_full[tile][buf], pv_done[tile], mma_drain[tile], q_full[tile], FP8: staged[K/V][2]
+    static constexpr int kNumBars = 4 * kStages + 4 + 4 + 2 + 2 + 2 + (kF8 ? 4 : 0);
     static constexpr int kMaskOff = kBarOff + kNumBars * 8;
     static constexpr int kTmemOff = kMaskOff + kStages * 4;
-    static constexpr int kBytes = kTmemOff + 16;
+    static constexpr int kSegOff = kTmemOff + 16;  // per softmax warp: its segment walk
+    static constexpr int kBytes = kSegOff + kSoftmaxWarps * 96;
     static constexpr int kLaunchBytes = kBytes + 1024;
     static_assert(kLaunchBytes <= 227 * 1024, "shared memory of one CTA");
 };
 // warps: 0 K producer, 1 MMA issue for tile A, 2 V producer, 3 MMA issue for
 // tile B;
 // 4-7 softmax of query tile A, 8-11 of tile B (one M-row per thread)
-constexpr int kSoftmaxWarps = 8;
 constexpr int kThreads = 384;
 // tensor memory: S_x[buf] (64 columns each) at 128x + 64buf, O_x at 256 + 128x
 constexpr uint32_t kTmemCols = 512;
@@ -125,6 +126,182 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, int la
 }
 
 // ---------------------------------------------------------------------------
+// Segments: the (item, key-tile range) pieces a CTA works through.  An item
+// is a (row, kv head, query-tile pair); its key tiles are the 64-key tiles of
+// its key range [kv_lo, kv_hi).
+//   one CTA per item (sk_ctas == 0): one segment, the item's whole range or,
+//     for the key-range runs of a short chunk, one run of it;
+//   persistent balanced schedule (sk_ctas > 0): the items' tiles in item
+//     order form one sequence of W tiles (sk_prefix, written by
+//     prefill_sk_plan_kernel); CTA c takes tiles [c W / n, (c + 1) W / n),
+//     item by item.  Only its first and its last segment can cut an item;
+//     a cut segment writes a partial to slot 0 (first) or 1 (last) of the
+//     CTA, and prefill_sk_merge_kernel combines an item's pieces.
+// ---------------------------------------------------------------------------
+struct Seg {
+    PrefillRowInfo w;
+    int32_t item;
+    int32_t jt0;    // first key tile of the segment (in 64-key units)
+    int32_t ntile;  // tiles of the segment
+    bool whole;     // the item's whole key range
+    int32_t slot;   // persistent schedule: partial slot of a cut segment
+};
+
+struct SegWalk {
+    int32_t pos, end;  // persistent schedule: tiles of the CTA's run still ahead
+    int32_t u;         // the item holding tile pos
+    int32_t k;         // segments returned so far
+};
+
+__device__ __forceinline__ int32_t sk_run_start(const PrefillParams &p, int32_t c)
+{
+    const int64_t W = __ldg(p.sk_prefix + p.sk_items);
+    return static_cast<int32_t>(static_cast<int64_t>(c) * W / p.sk_ctas);
+}
+
+// the item holding tile pos: the largest u with prefix[u] <= pos
+__device__ __forceinline__ int32_t sk_item_of(const PrefillParams &p, int32_t pos)
+{
+    int32_t lo = 0, hi = p.sk_items;
+    while (hi - lo > 1) {
+        const int32_t mid = (lo + hi) >> 1;
+        if (__ldg(p.sk_prefix + mid) <= pos) lo = mid; else hi = mid;
+    }
+    return lo;
+}
+
+// the CTA whose run holds tile pos
+__device__ __forceinline__ int32_t sk_cta_of(const PrefillParams &p, int32_t pos)
+{
+    const int64_t W = __ldg(p.sk_prefix + p.sk_items);
+    int32_t c = W > 0 ? static_cast<int32_t>(static_cast<int64_t>(pos) * p.sk_ctas / W) : 0;
+    c = min(max(c, 0), p.sk_ctas - 1);
+    while (c + 1 < p.sk_ctas && sk_run_start(p, c + 1) <= pos) ++c;
+    while (c > 0 && sk_run_start(p, c) > pos) --c;
+    return c;
+}
+
+// Next segment of a persistent CTA's run (false at its end).
+__device__ __forceinline__ bool sk_next(const PrefillParams &p, int qpc, SegWalk &sw, Seg &sg)
+{
+    if (sw.pos >= sw.end) return false;
+    const int32_t u = sw.u;
+    const int32_t lo = __ldg(p.sk_prefix + u), hi = __ldg(p.sk_prefix + u + 1);
+    const int32_t seg_end = min(hi, sw.end);
+    prefill_item(p, u, qpc, sg.w);  // an item with tiles has queries
+    sg.item = u;
+    sg.jt0 = sg.w.kv_lo / pf::kKeys + (sw.pos - lo);
+    sg.ntile = seg_end - sw.pos;
+    sg.whole = sw.pos == lo && seg_end == hi;
+    sg.slot = sw.k == 0 ? 0 : 1;
+    ++sw.k;
+    sw.pos = seg_end;
+    if (seg_end == hi) {
+        int32_t v = u + 1;  // skip items without tiles (no queries)
+        while (v < p.sk_items && __ldg(p.sk_prefix + v + 1) == __ldg(p.sk_prefix + v)) ++v;
+        sw.u = v;
+    }
+    return true;
+}
+
+// First segment of CTA `cta` (false: nothing to do).  One CTA per item: the
+// item (or its key-range run; an empty run sets ntile <= 0).
+__device__ __forceinline__ bool seg_first(const PrefillParams &p, int qpc, int64_t cta, SegWalk &sw,
+                                          Seg &sg)
+{
+    if (p.sk_ctas > 0) {
+        sw.pos = sk_run_start(p, static_cast<int32_t>(cta));
+        sw.end = sk_run_start(p, static_cast<int32_t>(cta) + 1);
+        sw.k = 0;
+        if (sw.pos >= sw.end) return false;
+        sw.u = sk_item_of(p, sw.pos);
+        return sk_next(p, qpc, sw, sg);
+    }
+    if (!prefill_item(p, cta, qpc, sg.w)) return false;
+    sg.item = static_cast<int32_t>(cta);
+    sg.jt0 = sg.w.kv_lo / pf::kKeys;
+    sg.ntile = (sg.w.kv_hi - 1) / pf::kKeys - sg.jt0 + 1;
+    sg.whole = p.kv_splits <= 1;
+    sg.slot = 0;
+    if (!sg.whole) {
+        const int32_t tb = sg.w.s * p.split_tiles;
+        sg.ntile = min(sg.ntile, tb + p.split_tiles) - tb;
+        sg.jt0 += tb;
+    }
+    sw.pos = sw.end = 0;  // no further segment
+    return true;
+}
+
+__device__ __forceinline__ bool seg_next(const PrefillParams &p, int qpc, SegWalk &sw, Seg &sg)
+{
+    return p.sk_ctas > 0 && sk_next(p, qpc, sw, sg);
+}
+
+// The key tiles of a CTA in order, over its segments (producers).
+struct TileCursor {
+    SegWalk sw;
+    Seg sg;
+    int32_t j;  // tile within the segment
+    bool valid;
+    __device__ __forceinline__ void start(const PrefillParams &p, int qpc, const SegWalk &w0, const Seg &s0)
+    {
+        sw = w0;
+        sg = s0;
+        j = 0;
+        valid = s0.ntile > 0;
+        (void)p;
+        (void)qpc;
+    }
+    __device__ __forceinline__ void advance(const PrefillParams &p, int qpc)
+    {
+        if (!valid) return;
+        if (++j < sg.ntile) return;
+        j = 0;
+        valid = seg_next(p, qpc, sw, sg);
+    }
+    __device__ __forceinline__ int32_t kt() const { return sg.jt0 + j; }  // absolute key tile
+};
+
+// One row of a query tile into shared memory (softmax thread ii = 0 .. 255:
+// tile ii / 128, row i = ii % 128 = (query x*qpt + i/G, head i%G)), 128-byte
+// swizzled for the tensor cores.  FP8 pools take f16 products (bf16 -> f16 is
+// exact inside the f16 range; a magnitude past 65504 sets PKV_DEV_Q_RANGE); a
+// negative scale is staged as -q (`flip` toggles the sign bits), so that the
+// scores the tensor cores produce always take a positive factor.  Not inlined:
+// a segment's staging then leaves the registers of the softmax loop around
+// it alone.
+template <bool kF8>
+__device__ __noinline__ void stage_q_row(const uint4 *q, const int32_t *cu_q_lens, int32_t hq, int G,
+                                         int qpt, int32_t r, int32_t i0, int32_t nq, int32_t g,
+                                         uint32_t flip, int32_t *status, uint8_t *q_s, int ii)
+{
+    constexpr int kD = pf::kD, kRows = pf::kRows;
+    const int x = ii / kRows, i = ii % kRows;
+    const int t = x * qpt + i / G, h = i % G;
+    const bool valid = i < qpt * G && t < nq;
+    const uint4 *src = q + ((static_cast<int64_t>(__ldg(cu_q_lens + r)) + i0 + t) * hq + g * G + h) * (kD / 8);
+    uint8_t *qt_s = q_s + x * pf::kQBytes;
+    bool qbad = false;
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+        uint4 v = valid ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+        if constexpr (kF8) {
+            v.x = bf16x2_to_f16x2(v.x, qbad);
+            v.y = bf16x2_to_f16x2(v.y, qbad);
+            v.z = bf16x2_to_f16x2(v.z, qbad);
+            v.w = bf16x2_to_f16x2(v.w, qbad);
+        }
+        v.x ^= flip;
+        v.y ^= flip;
+        v.z ^= flip;
+        v.w ^= flip;
+        *reinterpret_cast<uint4 *>(qt_s + (c >> 3) * (kRows * 128) + i * 128 + (((c & 7) ^ (i & 7)) << 4)) = v;
+    }
+    if (qbad) report(status, PKV_DEV_Q_RANGE);
+    fence_proxy_async_smem();  // read by the tensor cores (async proxy)
+}
+
+// ---------------------------------------------------------------------------
 // bf16, tcgen05
 // ---------------------------------------------------------------------------
 template <bool kF8>
@@ -147,7 +324,8 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
     uint64_t *p_full = bars + 4 * kStages + 4;  // [tile * 2 + buf]
     uint64_t *pv_done = bars + 4 * kStages + 8; // [tile]
     uint64_t *mma_drain = bars + 4 * kStages + 10;  // [tile]: the issuer's last products
-    uint64_t *staged = bars + 4 * kStages + 12;  // FP8: [K/V * 2 + buffer]
+    uint64_t *q_full = bars + 4 * kStages + 12;     // [tile]: a segment's query tile staged
+    uint64_t *staged = bars + 4 * kStages + 14;  // FP8: [K/V * 2 + buffer]
     uint32_t *kmask = reinterpret_cast<uint32_t *>(smem + L::kMaskOff);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kTmemOff);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -161,33 +339,29 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
     pdl_wait();
     pdl_trigger();
 
-    PrefillRowInfo w;
-    if (!prefill_item(p, blockIdx.x, kQTiles * qpt, w)) return;
-    int32_t jt0 = w.kv_lo / kKeys;
-    int32_t ntile = (w.kv_hi - 1) / kKeys - jt0 + 1;
-    const bool split = p.kv_splits > 1;
-    if (split) {
-        // this CTA's run of the key range
-        const int32_t tb = w.s * p.split_tiles;
-        ntile = min(ntile, tb + p.split_tiles) - tb;
-        jt0 += tb;
-        if (ntile <= 0) {
-            // an empty run: an empty partial (no weight) for every live row
-            if (warp >= 4) {
-                const int x = (warp >> 2) - 1, row = 32 * (warp & 3) + lane;
-                const int t = x * qpt + row / G;
-                if (row < qpt * G && t < w.nq) {
-                    const size_t pi = ((static_cast<size_t>(w.r) * p.max_q_len + w.i0 + t) * p.hq +
-                                       w.g * G + row % G) * p.kv_splits + w.s;
-                    *reinterpret_cast<float2 *>(p.ws_ml + pi * 2) = make_float2(-INFINITY, 0.f);
-                }
+    const int qpc = kQTiles * qpt;  // queries per item
+    SegWalk sw0;
+    Seg seg0;
+    if (!seg_first(p, qpc, blockIdx.x, sw0, seg0)) return;
+    const bool split = p.kv_splits > 1;  // one CTA per key-range run of a short chunk
+    if (split && seg0.ntile <= 0) {
+        // an empty run: an empty partial (no weight) for every live row
+        const PrefillRowInfo &w = seg0.w;
+        if (warp >= 4) {
+            const int x = (warp >> 2) - 1, row = 32 * (warp & 3) + lane;
+            const int t = x * qpt + row / G;
+            if (row < qpt * G && t < w.nq) {
+                const size_t pi = ((static_cast<size_t>(w.r) * p.max_q_len + w.i0 + t) * p.hq +
+                                   w.g * G + row % G) * p.kv_splits + w.s;
+                *reinterpret_cast<float2 *>(p.ws_ml + pi * 2) = make_float2(-INFINITY, 0.f);
             }
-            return;
         }
+        return;
     }
     // query tiles with queries in them: a short chunk (a verify step of a few
-    // queries) fills tile A only, and tile B's warps then stay idle
-    const int nqt = w.nq > qpt ? 2 : 1;
+    // queries) fills tile A only, and tile B's warps then stay idle; the
+    // persistent schedule runs both (its segments' items differ)
+    const int nqt = (p.sk_ctas > 0 || seg0.w.nq > qpt) ? 2 : 1;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
@@ -205,6 +379,8 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         mbar_init(&pv_done[1], 1);
         mbar_init(&mma_drain[0], 1);
         mbar_init(&mma_drain[1], 1);
+        mbar_init(&q_full[0], kSoftmaxWarps / kQTiles);
+        mbar_init(&q_full[1], kSoftmaxWarps / kQTiles);
         if (kF8)
             for (int i = 0; i < 4; ++i) mbar_init(&staged[i], 1);
         fence_mbar_init();
@@ -212,40 +388,16 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
     if (warp == 1) tc::alloc(tmem_slot, kTmemCols);
 
     // query tiles: tile x row i = (query t = x * qpt + i / G, head h = i % G);
-    // the 256 softmax threads load one row each
-    if (warp >= 4) {
-        const int ii = threadIdx.x - 128;
-        const int x = ii / kRows, i = ii % kRows;
-        const int t = x * qpt + i / G, h = i % G;
-        const bool valid = i < qpt * G && t < w.nq;
-        const uint4 *src = reinterpret_cast<const uint4 *>(p.q) +
-                           ((static_cast<int64_t>(__ldg(p.cu_q_lens + w.r)) + w.i0 + t) * p.hq +
-                            w.g * G + h) * (kD / 8);
-        uint8_t *qt_s = q_s + x * kQBytes;
-        // a negative scale: stage -q (sign bits flipped, exact), so that the
-        // scores the tensor cores produce always take a positive factor
-        const uint32_t flip = p.scale_log2 < 0.f ? 0x80008000u : 0u;
-        bool qbad = false;
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-            uint4 v = valid ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
-            if constexpr (kF8) {
-                // FP8 pools: the products are f16 x f16 (exact inside the f16 range)
-                v.x = bf16x2_to_f16x2(v.x, qbad);
-                v.y = bf16x2_to_f16x2(v.y, qbad);
-                v.z = bf16x2_to_f16x2(v.z, qbad);
-                v.w = bf16x2_to_f16x2(v.w, qbad);
-            }
-            v.x ^= flip;
-            v.y ^= flip;
-            v.z ^= flip;
-            v.w ^= flip;
-            *reinterpret_cast<uint4 *>(qt_s + (c >> 3) * (kRows * 128) + i * 128 +
-                                       (((c & 7) ^ (i & 7)) << 4)) = v;
-        }
-        if (qbad) report(p.status, PKV_DEV_Q_RANGE);
-        fence_proxy_async_smem();  // read by the tensor cores (async proxy)
-    }
+    // the 256 softmax threads load one row each (the first segment's here,
+    // the next segments' after each epilogue)
+    // a negative scale: stage -q (sign bits flipped, exact), so that the
+    // scores the tensor cores produce always take a positive factor
+    const uint32_t flip = p.scale_log2 < 0.f ? 0x80008000u : 0u;
+    auto load_q_row = [&](const PrefillRowInfo &w) {
+        stage_q_row<kF8>(static_cast<const uint4 *>(p.q), p.cu_q_lens, p.hq, G, qpt, w.r, w.i0, w.nq,
+                         w.g, flip, p.status, q_s, threadIdx.x - 128);
+    };
+    if (warp >= 4) load_q_row(seg0.w);
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
@@ -255,16 +407,29 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
 
     if (warp == 0 || warp == 2) {
         // ------------------------------------------ K (warp 0) / V (warp 2) producer
+        // The CTA's key tiles in order over its segments; tile T (a running
+        // count) goes to ring stage T % kStages.
         const bool is_k = warp == 0;
         // diagnostic drill: tile 0's loads are never issued (its waits run out)
-        auto withheld = [&](int32_t jj) { return (p.drill & kDrillWithholdFirst) != 0 && jj == 0; };
+        auto withheld = [&](int32_t T) { return (p.drill & kDrillWithholdFirst) != 0 && T == 0; };
         uint8_t *ring = is_k ? k_s : v_s;
         uint64_t *full = is_k ? k_full : v_full;
         uint64_t *empty = is_k ? k_empty : v_empty;
-        const int32_t *trow = p.tables + static_cast<int64_t>(w.r) * p.width;
+        // lane < kBlocks: logical block kt * kBlocks + lane of the cursor's
+        // tile, inside the table and the item's key range
+        auto in_range_of = [&](const TileCursor &c) {
+            const int32_t kb = c.kt() * kBlocks + lane;
+            return c.valid && lane < kBlocks && kb < p.width && kb * 16 < c.sg.w.kv_hi &&
+                   (kb + 1) * 16 > c.sg.w.kv_lo;
+        };
+        auto load_id = [&](const TileCursor &c) {
+            return in_range_of(c) ? __ldg(p.tables + static_cast<int64_t>(c.sg.w.r) * p.width +
+                                          c.kt() * kBlocks + lane)
+                                  : -1;
+        };
         if constexpr (kF8) {
-            // FP8: tile jj's E4M3 blocks are bulk-copied into staging buffer
-            // jj % 2 (two tiles ahead of the ring), then widened to f16 into
+            // FP8: tile T's E4M3 blocks are bulk-copied into staging buffer
+            // T % 2 (two tiles ahead of the ring), then widened to f16 into
             // the ring stage: K as the bf16 path lays it out (key rows, 64-dim
             // 128-byte-swizzled regions), V transposed (dim rows of the tile's
             // 64 keys, 128-byte swizzled), so that a pair of codes becomes
@@ -275,23 +440,17 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             const uint8_t *pool = static_cast<const uint8_t *>(is_k ? p.k_pool : p.v_pool);
             uint8_t *stg = smem + L::kStagingOff + (is_k ? 0 : 2) * kF8StageTile;
             uint64_t *stg_bar = staged + (is_k ? 0 : 2);
-            // block ids of tile jj (lane < kBlocks), read one tile before use
-            auto in_range_of = [&](int32_t jj) {
-                const int32_t kb = (jt0 + jj) * kBlocks + lane;
-                return lane < kBlocks && kb < p.width && kb * 16 < w.kv_hi && (kb + 1) * 16 > w.kv_lo;
-            };
-            auto load_id = [&](int32_t jj) {
-                return in_range_of(jj) ? __ldg(trow + (jt0 + jj) * kBlocks + lane) : -1;
-            };
             int32_t nf = 0;  // tiles 0 .. nf-1 fetched into the staging buffers
-            auto fetch = [&](int32_t jj, int32_t id) {  // whole warp; returns the mask of loaded blocks
-                const bool in_range = in_range_of(jj);
+            // fetch tile nf at cursor c (block ids read one tile before);
+            // whole warp; returns the mask of loaded blocks
+            auto fetch = [&](const TileCursor &c, int32_t id) {
+                const bool in_range = in_range_of(c);
                 const bool good = in_range && static_cast<uint32_t>(id) < static_cast<uint32_t>(p.num_blocks);
                 if (is_k && in_range && !good) report(p.status, PKV_DEV_BAD_BLOCK);
                 const uint32_t mask = __ballot_sync(0xffffffffu, good) & ((1u << kBlocks) - 1u);
-                const int sb = jj & 1;
-                nf = jj + 1;
-                if (withheld(jj)) return mask;  // diagnostic drill: never issued
+                const int32_t tile = nf++;
+                const int sb = tile & 1;
+                if (withheld(tile)) return mask;  // diagnostic drill: never issued
                 if (lane == 0) {
                     if (mask == 0)
                         mbar_arrive(&stg_bar[sb]);
@@ -304,26 +463,36 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
                     const int32_t bid = __shfl_sync(0xffffffffu, id, b);
                     if (((mask >> b) & 1u) && elect_one())
                         bulk_load(stg + sb * kF8StageTile + b * kF8BlockBytes,
-                                  pool + (static_cast<int64_t>(bid) * p.hkv + w.g) * kF8BlockBytes,
+                                  pool + (static_cast<int64_t>(bid) * p.hkv + c.sg.w.g) * kF8BlockBytes,
                                   kF8BlockBytes, &stg_bar[sb], policy);
                 }
                 __syncwarp();
                 return mask;
             };
+            TileCursor cw, cf, ci;  // the tile widened, the next fetched, the next id read
+            cw.start(p, qpc, sw0, seg0);
+            cf = cw;
+            ci = cw;
+            int32_t id_next = load_id(ci);
+            ci.advance(p, qpc);
             uint32_t smask[2] = {0u, 0u};
-            smask[0] = fetch(0, load_id(0));
-            if (ntile > 1) smask[1] = fetch(1, load_id(1));
-            int32_t id_ahead = ntile > 2 ? load_id(2) : -1;
-            int32_t jj = 0;
-            for (; jj < ntile; ++jj) {
-                const int st = jj % kStages, sb = jj & 1;
-                if (jj >= kStages && !warp_wait(&empty[st], ((jj / kStages) + 1) & 1, lane, p.status, p.wait_ns)) break;
-                if (!warp_wait(&stg_bar[sb], (jj >> 1) & 1, lane, p.status, p.wait_ns)) break;
+            for (int i = 0; i < 2 && cf.valid; ++i) {
+                smask[i] = fetch(cf, id_next);
+                cf.advance(p, qpc);
+                id_next = load_id(ci);
+                ci.advance(p, qpc);
+            }
+            int32_t T = 0;
+            for (; cw.valid; ++T, cw.advance(p, qpc)) {
+                const int st = T % kStages, sb = T & 1;
+                if (T >= kStages && !warp_wait(&empty[st], ((T / kStages) + 1) & 1, lane, p.status, p.wait_ns)) break;
+                if (!warp_wait(&stg_bar[sb], (T >> 1) & 1, lane, p.status, p.wait_ns)) break;
+                const PrefillRowInfo &w = cw.sg.w;
                 const uint32_t mask = smask[sb];
                 if (is_k && lane == 0) kmask[st] = mask;
                 const uint32_t src = smem_u32(stg + sb * kF8StageTile);
                 const uint32_t dst = smem_u32(ring + st * kTileBytes);
-                const int32_t tbase = (jt0 + jj) * kKeys;
+                const int32_t tbase = cw.kt() * kKeys;
                 const bool edge = tbase < w.kv_lo || tbase + kKeys > w.kv_hi;
 #pragma unroll
                 for (int b = 0; b < kBlocks; ++b) {
@@ -389,33 +558,35 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&full[st]);
-                if (jj + 2 < ntile) {
-                    smask[sb] = fetch(jj + 2, id_ahead);
-                    id_ahead = jj + 3 < ntile ? load_id(jj + 3) : -1;
+                if (cf.valid) {
+                    smask[sb] = fetch(cf, id_next);  // tile T + 2 into buffer sb
+                    cf.advance(p, qpc);
+                    id_next = load_id(ci);
+                    ci.advance(p, qpc);
                 }
             }
             // wind-down (a wait ran out): the staged copies issued but not yet
             // consumed land before the warp leaves
             if (lane == 0)
-                for (int32_t t = jj; t < nf; ++t)
+                for (int32_t t = T; t < nf; ++t)
                     if (!withheld(t)) mbar_wait(&stg_bar[t & 1], (t >> 1) & 1);
             __syncwarp();
         } else {
             const CUtensorMap *map = is_k ? &kmap : &vmap;
             const uint64_t policy = l2_evict_last_policy();  // re-read by the row's other CTAs
-            int32_t jj = 0;
-            for (; jj < ntile; ++jj) {
-                const int st = jj % kStages;
-                if (jj >= kStages && !warp_wait(&empty[st], ((jj / kStages) + 1) & 1, lane, p.status, p.wait_ns)) break;
-                const int32_t kb = (jt0 + jj) * kBlocks + lane;  // logical block of lane < kBlocks
-                const bool in_range = lane < kBlocks && kb < p.width && kb * 16 < w.kv_hi &&
-                                      (kb + 1) * 16 > w.kv_lo;
-                const int32_t id = in_range ? __ldg(trow + kb) : -1;
+            TileCursor cur;
+            cur.start(p, qpc, sw0, seg0);
+            int32_t T = 0;
+            for (; cur.valid; ++T, cur.advance(p, qpc)) {
+                const int st = T % kStages;
+                if (T >= kStages && !warp_wait(&empty[st], ((T / kStages) + 1) & 1, lane, p.status, p.wait_ns)) break;
+                const bool in_range = in_range_of(cur);
+                const int32_t id = load_id(cur);
                 const bool good = in_range && static_cast<uint32_t>(id) < static_cast<uint32_t>(p.num_blocks);
                 if (is_k && in_range && !good) report(p.status, PKV_DEV_BAD_BLOCK);
                 const uint32_t mask = __ballot_sync(0xffffffffu, good) & ((1u << kBlocks) - 1u);
                 if (is_k && lane == 0) kmask[st] = mask;
-                if (withheld(jj)) continue;  // diagnostic drill: never issued
+                if (withheld(T)) continue;  // diagnostic drill: never issued
                 if (lane == 0) {
                     if (mask == 0)
                         mbar_arrive(&full[st]);
@@ -424,12 +595,13 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
                 }
                 __syncwarp();
                 uint8_t *dst = ring + st * kTileBytes;
+                const int32_t g = cur.sg.w.g;
 #pragma unroll
                 for (int b = 0; b < kBlocks; ++b) {
                     const int32_t bid = __shfl_sync(0xffffffffu, id, b);
                     if (((mask >> b) & 1u) && elect_one()) {
-                        tma_load_4d(dst + b * 2048, map, &full[st], 0, 0, w.g, bid, policy);
-                        tma_load_4d(dst + kKVRegion + b * 2048, map, &full[st], 64, 0, w.g, bid, policy);
+                        tma_load_4d(dst + b * 2048, map, &full[st], 0, 0, g, bid, policy);
+                        tma_load_4d(dst + kKVRegion + b * 2048, map, &full[st], 64, 0, g, bid, policy);
                     }
                 }
             }
@@ -437,7 +609,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             // the last ring's worth of tiles have landed before the warp
             // leaves (at a normal exit their consumers saw them land already)
             if (lane == 0)
-                for (int32_t t = max(0, jj - kStages); t < jj; ++t)
+                for (int32_t t = max(0, T - kStages); t < T; ++t)
                     if (!withheld(t)) mbar_wait(&full[t % kStages], (t / kStages) & 1);
             __syncwarp();
         }
@@ -466,11 +638,11 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         const uint32_t tO_x = tO(x);
         // The whole warp runs these; one elected lane issues a group's
         // products and commits from one straight-line block.
-        auto s_mma = [&](int32_t jj) {  // once K(jj) has landed
-            if (!warp_wait(&k_full[jj % kStages], (jj / kStages) & 1, lane, p.status, p.wait_ns)) return false;
+        auto s_mma = [&](int32_t T) {  // once K(T) has landed (T: the CTA's running tile count)
+            if (!warp_wait(&k_full[T % kStages], (T / kStages) & 1, lane, p.status, p.wait_ns)) return false;
             tc::fence_after();
-            const uint64_t kd = dk + static_cast<uint64_t>(jj % kStages) * kStageStep;
-            const uint32_t d = tS(x, jj & 1);
+            const uint64_t kd = dk + static_cast<uint64_t>(T % kStages) * kStageStep;
+            const uint32_t d = tS(x, T & 1);
             if (elect_one()) {
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
@@ -478,16 +650,18 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
                     const uint64_t ko = static_cast<uint64_t>(((kk >> 2) * kKVRegion + (kk & 3) * 32) >> 4);
                     tc::mma_ss(d, dq + qo, kd + ko, idS, kk > 0 ? 1u : 0u);
                 }
-                tc::commit(&s_full[x * 2 + (jj & 1)]);
-                tc::commit(&k_empty[jj % kStages]);
+                tc::commit(&s_full[x * 2 + (T & 1)]);
+                tc::commit(&k_empty[T % kStages]);
             }
             __syncwarp();
             return true;
         };
-        auto pv_mma = [&](int32_t jj) {  // V(jj) has landed: the warpgroup checked it
-            const uint64_t vd = dv + static_cast<uint64_t>(jj % kStages) * kStageStep;
-            const uint32_t a = tS(x, jj & 1);
-            const uint32_t first = jj > 0 ? 1u : 0u;
+        // V(T) has landed: the warpgroup checked it; a segment's first tile
+        // starts O afresh
+        auto pv_mma = [&](int32_t T, bool seg_start) {
+            const uint64_t vd = dv + static_cast<uint64_t>(T % kStages) * kStageStep;
+            const uint32_t a = tS(x, T & 1);
+            const uint32_t first = seg_start ? 0u : 1u;
             // keys 16g..16g+15 hold P hi in S columns 16g..16g+7 and P lo in
             // 16g+8..16g+15 (bf16 pairs; f16 for FP8 pools)
             if (elect_one()) {
@@ -498,17 +672,33 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
                         tc::mma_ts(tO_x, a + 16 * kk + 8 * part, vd + kVStep * static_cast<uint64_t>(kk),
                                    idO, (part > 0 || kk > 0) ? 1u : first);
                 tc::commit(&pv_done[x]);
-                tc::commit(&v_empty[jj % kStages]);
+                tc::commit(&v_empty[T % kStages]);
             }
             __syncwarp();
         };
-        bool ok = s_mma(0) && (ntile < 2 || s_mma(1));
-        for (int32_t jj = 0; jj < ntile && ok; ++jj) {
-            ok = warp_wait(&p_full[x * 2 + (jj & 1)], (jj >> 1) & 1, lane, p.status, p.wait_ns);
+        SegWalk sw = sw0;
+        Seg sg = seg0;
+        int32_t T0 = 0;  // the segment's first tile in the running count
+        for (int32_t k = 0;; ++k) {
+            const int32_t n = sg.ntile;
+            // the segment's query tile is staged (the previous segment's
+            // products, which read the old one, completed before its epilogue)
+            bool ok = warp_wait(&q_full[x], k & 1, lane, p.status, p.wait_ns);
+            if (ok) {
+                tc::fence_after();
+                ok = s_mma(T0) && (n < 2 || s_mma(T0 + 1));
+            }
+            for (int32_t j = 0; j < n && ok; ++j) {
+                const int32_t T = T0 + j;
+                ok = warp_wait(&p_full[x * 2 + (T & 1)], (T >> 1) & 1, lane, p.status, p.wait_ns);
+                if (!ok) break;
+                tc::fence_after();
+                pv_mma(T, j == 0);
+                if (j + 2 < n) ok = s_mma(T + 2);
+            }
             if (!ok) break;
-            tc::fence_after();
-            pv_mma(jj);
-            if (jj + 2 < ntile) ok = s_mma(jj + 2);
+            T0 += n;
+            if (!seg_next(p, qpc, sw, sg)) break;
         }
         // every product this warp issued has completed before the CTA frees
         // tensor memory (after a wait ran out, some may still be running)
@@ -524,22 +714,45 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
         const int row = 32 * (warp & 3) + lane;
         const int t = x * qpt + row / G;
-        const bool valid_row = row < qpt * G && t < w.nq;
-        const int32_t qpos = w.L - w.C + w.i0 + t;
-        const int32_t qlo = p.window > 0 ? max(0, qpos - p.window + 1) : 0;
         const uint32_t ox = tO(x) + lane_base;
         // |scale| * log2(e) (q was staged negated for a negative scale), kept
         // away from 0 so that a masked score (-inf) never meets a zero factor
         const float sl = fmaxf(fabsf(p.scale_log2), 1e-30f);
-        float m_ref = -INFINITY, l = 0.f;
         bool abort = false;
+        // this warp's segment walk and current segment live in shared memory
+        // (lane 0 writes them): the tile loop keeps its registers
+        struct SegSmem {
+            SegWalk sw;
+            Seg sg;
+        };
+        static_assert(sizeof(SegSmem) <= 96, "the per-warp segment slot");
+        SegSmem *ss = reinterpret_cast<SegSmem *>(smem + L::kSegOff) + (warp - 4);
+        if (lane == 0) {
+            ss->sw = sw0;
+            ss->sg = seg0;
+        }
+        __syncwarp();
+        int32_t T0 = 0;  // the segment's first tile in the running count
+        for (int32_t k = 0;; ++k) {
+        const int32_t ntile = ss->sg.ntile, jt0 = ss->sg.jt0;
+        const int32_t kv_lo = ss->sg.w.kv_lo, kv_hi = ss->sg.w.kv_hi;
+        // the segment's query tile: staged (the first in the prologue), then
+        // handed to the MMA-issue warp
+        if (k > 0) load_q_row(ss->sg.w);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&q_full[x]);
+        const bool valid_row = row < qpt * G && t < ss->sg.w.nq;
+        const int32_t qpos = ss->sg.w.L - ss->sg.w.C + ss->sg.w.i0 + t;
+        const int32_t qlo = p.window > 0 ? max(0, qpos - p.window + 1) : 0;
+        float m_ref = -INFINITY, l = 0.f;
         const bool warp_live = __any_sync(0xffffffffu, valid_row);
         for (int32_t jj = 0; jj < ntile; ++jj) {
-            const int ks = jj % kStages, buf = jj & 1;
+            const int32_t T = T0 + jj;
+            const int ks = T % kStages, buf = T & 1;
             const int32_t tbase = (jt0 + jj) * kKeys;
             const uint32_t sx = tS(x, buf) + lane_base;
-            bool got = mbar_wait(&s_full[x * 2 + buf], (jj >> 1) & 1, p.wait_ns);
-            got = got && mbar_wait(&k_full[ks], (jj / kStages) & 1, p.wait_ns);  // for kmask
+            bool got = mbar_wait(&s_full[x * 2 + buf], (T >> 1) & 1, p.wait_ns);
+            got = got && mbar_wait(&k_full[ks], (T / kStages) & 1, p.wait_ns);  // for kmask
             if (__any_sync(0xffffffffu, !got)) {
                 if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
                 abort = true;
@@ -599,7 +812,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
                 if (__any_sync(0xffffffffu, resc)) {
                     // O_x holds P.V up to tile jj-1 once that product completes
                     if (jj > 0) {
-                        const bool done = mbar_wait(&pv_done[x], (jj - 1) & 1, p.wait_ns);
+                        const bool done = mbar_wait(&pv_done[x], (T - 1) & 1, p.wait_ns);
                         if (__any_sync(0xffffffffu, !done)) {
                             if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
                             abort = true;
@@ -650,21 +863,21 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             // stale slots (possibly NaN): each warpgroup zeroes them before its
             // own P.V reads them (both write the same zeros, so whichever
             // product runs first reads zeros)
-            const bool landed = mbar_wait(&v_full[ks], (jj / kStages) & 1, p.wait_ns);
+            const bool landed = mbar_wait(&v_full[ks], (T / kStages) & 1, p.wait_ns);
             if (__any_sync(0xffffffffu, !landed)) {
                 if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
                 abort = true;
                 break;
             }
             // (FP8: the V producer wrote those columns as zeros)
-            const bool edge = !kF8 && (mask != (1u << kBlocks) - 1u || tbase < w.kv_lo ||
-                                       tbase + kKeys > w.kv_hi);
+            const bool edge = !kF8 && (mask != (1u << kBlocks) - 1u || tbase < kv_lo ||
+                                       tbase + kKeys > kv_hi);
             if (edge) {
                 // thread row r < 64 zeroes key row r's first 64 dims, r >= 64
                 // the second 64 dims of key row r - 64
                 const int kr = row & (kKeys - 1), half = row >> 6;
                 const int32_t kp = tbase + kr;
-                if (!(kp >= w.kv_lo && kp < w.kv_hi && ((mask >> (kr >> 4)) & 1u))) {
+                if (!(kp >= kv_lo && kp < kv_hi && ((mask >> (kr >> 4)) & 1u))) {
                     uint8_t *vs = v_s + ks * kTileBytes + half * kKVRegion + kr * 128;
 #pragma unroll
                     for (int c = 0; c < 8; ++c)
@@ -677,15 +890,106 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&p_full[x * 2 + buf]);
         }
-        // epilogue: O / l once the tile's last P.V product is in.  Phases up
-        // to ntile - 3 are known complete here (S(ntile-1) was issued after
-        // P(ntile-3).V), so wait for ntile - 2 first: a parity names one phase
-        // only when the one before it has completed
-        if (!abort) {
-            bool done = ntile < 2 || mbar_wait(&pv_done[x], (ntile - 2) & 1, p.wait_ns);
-            done = done && mbar_wait(&pv_done[x], (ntile - 1) & 1, p.wait_ns);
+        if (abort) break;
+        const PrefillRowInfo &w = ss->sg.w;
+        // epilogue: O / l once the segment's last P.V product is in.  Phases
+        // up to its last tile - 3 are known complete here (S of its last tile
+        // was issued after P.V of the tile two before), and those of earlier
+        // segments too, so wait for the last tile - 1 first: a parity names
+        // one phase only when the one before it has completed
+        {
+            const int32_t Tl = T0 + ntile - 1;
+            bool done = ntile < 2 || mbar_wait(&pv_done[x], (Tl - 1) & 1, p.wait_ns);
+            done = done && mbar_wait(&pv_done[x], Tl & 1, p.wait_ns);
             if (__any_sync(0xffffffffu, !done)) {
                 if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
+                break;
+            } else if (p.sk_ctas > 0 && !ss->sg.whole) {
+                // a piece of an item cut by this CTA's run: a partial in the
+                // CTA's slot (first or last segment), merged afterwards
+                tc::fence_after();
+                const size_t pr = (static_cast<size_t>(blockIdx.x) * 2 + ss->sg.slot) * (kQTiles * kRows) +
+                                  x * kRows + row;
+                float4 *dst = reinterpret_cast<float4 *>(p.sk_o + pr * kD);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t r32[32];
+                    tc::ld32(ox + c * 32, r32);
+                    tc::wait_ld();
+                    if (valid_row) {
+                        const float vs = kF8 ? p.v_scale : 1.f;
+#pragma unroll
+                        for (int v = 0; v < 8; ++v)
+                            dst[c * 8 + v] = make_float4(__uint_as_float(r32[4 * v]) * vs, __uint_as_float(r32[4 * v + 1]) * vs,
+                                                         __uint_as_float(r32[4 * v + 2]) * vs, __uint_as_float(r32[4 * v + 3]) * vs);
+                    }
+                }
+                if (valid_row) *reinterpret_cast<float2 *>(p.sk_ml + pr * 2) = make_float2(m_ref, l);
+                // the item's pieces: CTAs cf .. cl; per (query tile, warp) the
+                // warp whose piece completes last merges their 32 rows (no
+                // waiting: the others published theirs before counting)
+                __syncwarp();
+                const int32_t u = ss->sg.item;
+                const int32_t lo = __ldg(p.sk_prefix + u), hi = __ldg(p.sk_prefix + u + 1);
+                const int32_t cf = sk_cta_of(p, lo), cl = sk_cta_of(p, hi - 1);
+                int last = 0;
+                if (lane == 0) {
+                    __threadfence();
+                    const int old = atomicAdd(p.sk_count + (cf * 2 + x) * 4 + (warp & 3), 1);
+                    last = old == cl - cf;
+                    if (last) __threadfence();
+                }
+                last = __shfl_sync(0xffffffffu, last, 0);
+                if (last && valid_row) {
+                    auto piece = [&](int32_t c) {  // slot 1: the item is not c's first segment
+                        const int32_t slot = (c == cf && sk_run_start(p, c) < lo) ? 1 : 0;
+                        return (static_cast<size_t>(c) * 2 + slot) * (kQTiles * kRows) + x * kRows + row;
+                    };
+                    float M = -INFINITY, lsum = 0.f;
+                    for (int32_t c = cf; c <= cl; ++c) M = fmaxf(M, __ldcg(p.sk_ml + piece(c) * 2));
+                    if (M != -INFINITY)
+                        for (int32_t c = cf; c <= cl; ++c) {
+                            const size_t pc = piece(c);
+                            const float mc = __ldcg(p.sk_ml + pc * 2);
+                            if (mc != -INFINITY) lsum = fmaf(fast_exp2(mc - M), __ldcg(p.sk_ml + pc * 2 + 1), lsum);
+                        }
+                    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.out) +
+                                 ((static_cast<int64_t>(__ldg(p.cu_q_lens + w.r)) + w.i0 + t) * p.hq +
+                                  w.g * G + row % G) * (kD / 8);
+                    // 32 dims at a time
+#pragma unroll 1
+                    for (int d0 = 0; d0 < kD; d0 += 32) {
+                        float acc[32];
+#pragma unroll
+                        for (int d = 0; d < 32; ++d) acc[d] = 0.f;
+                        if (M != -INFINITY)
+                            for (int32_t c = cf; c <= cl; ++c) {
+                                const size_t pc = piece(c);
+                                const float mc = __ldcg(p.sk_ml + pc * 2);
+                                if (mc == -INFINITY) continue;
+                                const float wgt = fast_exp2(mc - M);
+                                const float4 *src = reinterpret_cast<const float4 *>(p.sk_o + pc * kD + d0);
+#pragma unroll
+                                for (int v = 0; v < 8; ++v) {
+                                    const float4 o4 = __ldcg(src + v);
+                                    acc[4 * v] = fmaf(wgt, o4.x, acc[4 * v]);
+                                    acc[4 * v + 1] = fmaf(wgt, o4.y, acc[4 * v + 1]);
+                                    acc[4 * v + 2] = fmaf(wgt, o4.z, acc[4 * v + 2]);
+                                    acc[4 * v + 3] = fmaf(wgt, o4.w, acc[4 * v + 3]);
+                                }
+                            }
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            uint4 o;
+                            o.x = pack_bf16x2(acc[8 * v + 0] * inv, acc[8 * v + 1] * inv);
+                            o.y = pack_bf16x2(acc[8 * v + 2] * inv, acc[8 * v + 3] * inv);
+                            o.z = pack_bf16x2(acc[8 * v + 4] * inv, acc[8 * v + 5] * inv);
+                            o.w = pack_bf16x2(acc[8 * v + 6] * inv, acc[8 * v + 7] * inv);
+                            dst[d0 / 8 + v] = o;
+                        }
+                    }
+                }
             } else if (split) {
                 // a partial: O unnormalised with its reference max and sum
                 tc::fence_after();
@@ -731,6 +1035,24 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
                     }
                 }
             }
+        }
+        // the next segment: its query tile replaces this one once every
+        // product that read it has completed (the waits above)
+        tc::fence_before();
+        T0 += ntile;
+        bool more = false;
+        if (lane == 0) {
+            SegWalk sw = ss->sw;
+            Seg sg;
+            more = seg_next(p, qpc, sw, sg);
+            if (more) {
+                ss->sw = sw;
+                ss->sg = sg;
+            }
+        }
+        more = __shfl_sync(0xffffffffu, more, 0);
+        __syncwarp();
+        if (!more) break;
         }
     }
     tc::fence_before();
@@ -897,6 +1219,59 @@ __global__ void __launch_bounds__(kMergeWarps * 32) prefill_merge_kernel(const P
 }
 
 // ---------------------------------------------------------------------------
+// persistent balanced schedule: the plan (tile prefix sums of the items; the
+// cut items' arrival counters zeroed)
+// ---------------------------------------------------------------------------
+constexpr int kSkPlanThreads = 1024;
+
+__global__ void __launch_bounds__(kSkPlanThreads) prefill_sk_plan_kernel(const PrefillParams p)
+{
+    __shared__ int32_t warp_sum[kSkPlanThreads / 32];
+    __shared__ int32_t carry;
+    pdl_wait();  // lengths may come from the previous kernel on the stream
+    pdl_trigger();
+    const int qpc = pf::kQTiles * (pf::kRows / p.group);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) {
+        carry = 0;
+        p.sk_prefix[0] = 0;
+    }
+    for (int32_t i = threadIdx.x; i < p.sk_ctas * 8; i += kSkPlanThreads) p.sk_count[i] = 0;
+    __syncthreads();
+    for (int32_t base = 0; base < p.sk_items; base += kSkPlanThreads) {
+        const int32_t u = base + threadIdx.x;
+        int32_t n = 0;
+        PrefillRowInfo w;
+        if (u < p.sk_items && prefill_item(p, u, qpc, w))
+            n = (w.kv_hi - 1) / pf::kKeys - w.kv_lo / pf::kKeys + 1;
+        // inclusive scan: within the warp, then over the warps' sums
+        int32_t v = n;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int32_t o = __shfl_up_sync(0xffffffffu, v, d);
+            if (lane >= d) v += o;
+        }
+        if (lane == 31) warp_sum[warp] = v;
+        __syncthreads();
+        if (warp == 0) {
+            int32_t ws = warp_sum[lane];
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int32_t o = __shfl_up_sync(0xffffffffu, ws, d);
+                if (lane >= d) ws += o;
+            }
+            warp_sum[lane] = ws;  // inclusive over the warps
+        }
+        __syncthreads();
+        const int32_t incl = v + (warp > 0 ? warp_sum[warp - 1] : 0) + carry;
+        if (u < p.sk_items) p.sk_prefix[u + 1] = incl;
+        __syncthreads();
+        if (threadIdx.x == kSkPlanThreads - 1) carry = incl;
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
 bool prefill_shape_built(pkv_dtype dtype, int32_t D, int32_t bs, int32_t G)
@@ -935,6 +1310,32 @@ PrefillSplit prefill_split_plan(int32_t batch, int32_t hq, int32_t hkv, int32_t 
     return sp;
 }
 
+int32_t prefill_sk_ctas(pkv_dtype dtype, int32_t batch, int32_t hq, int32_t hkv, int32_t D, int32_t bs,
+                        int32_t max_q_len, int num_sms)
+{
+    if (dtype == PKV_F32 || hkv <= 0 || hq % hkv != 0 || batch <= 0 || max_q_len <= 0 || num_sms <= 0)
+        return 0;
+    const int32_t G = hq / hkv;
+    if (D != pf::kD || bs != 16 || G < 1 || pf::kRows % G != 0) return 0;
+    if (max_q_len <= pf::kRows / G) return 0;  // one query tile: the key-range runs serve it
+    const int64_t qpc = static_cast<int64_t>(pf::kQTiles) * (pf::kRows / G);
+    const int64_t items = static_cast<int64_t>(batch) * hkv * ((max_q_len + qpc - 1) / qpc);
+    // more items than SMs (else one wave of one CTA per item already fits),
+    // and a plan the one-CTA plan kernel scans quickly
+    if (items <= num_sms || items > 65536) return 0;
+    return num_sms;
+}
+
+size_t prefill_sk_ws_bytes(int32_t items, int32_t ctas)
+{
+    if (ctas <= 0) return 0;
+    const size_t pre = ((static_cast<size_t>(items + 1) * sizeof(int32_t) + 255) & ~static_cast<size_t>(255)) +
+                       ((static_cast<size_t>(ctas) * 8 * sizeof(int32_t) + 255) & ~static_cast<size_t>(255));
+    const size_t rows = static_cast<size_t>(ctas) * 2 * pf::kQTiles * pf::kRows;
+    const size_t o = (rows * pf::kD * sizeof(float) + 255) & ~static_cast<size_t>(255);
+    return pre + o + rows * 2 * sizeof(float);
+}
+
 size_t prefill_split_ws_bytes(int32_t batch, int32_t hq, int32_t max_q_len, const PrefillSplit &sp)
 {
     if (sp.splits <= 1) return 0;
@@ -947,15 +1348,19 @@ template <bool kF8>
 static cudaError_t launch_prefill_tc(const PrefillParams &p, const CUtensorMap &kmap,
                                     const CUtensorMap &vmap, cudaStream_t stream)
 {
-    const int64_t ctas = static_cast<int64_t>(p.batch) * p.hkv * p.q_tiles * p.kv_splits;
+    const int64_t ctas = p.sk_ctas > 0 ? p.sk_ctas
+                                       : static_cast<int64_t>(p.batch) * p.hkv * p.q_tiles * p.kv_splits;
     if (ctas == 0) return cudaSuccess;
     constexpr int smem = pf::Layout<kF8>::kLaunchBytes;
     cudaError_t err = cudaFuncSetAttribute(prefill_kernel<kF8>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
     prof_begin(PKV_KERNEL_PREFILL, stream);
-    err = launch_pdl(prefill_kernel<kF8>, dim3(static_cast<unsigned>(ctas)), dim3(pf::kThreads), smem,
-                     stream, kmap, vmap, p);
+    if (p.sk_ctas > 0)
+        err = launch_pdl(prefill_sk_plan_kernel, dim3(1), dim3(kSkPlanThreads), 0, stream, p);
+    if (err == cudaSuccess)
+        err = launch_pdl(prefill_kernel<kF8>, dim3(static_cast<unsigned>(ctas)), dim3(pf::kThreads), smem,
+                         stream, kmap, vmap, p);
     if (err == cudaSuccess && p.kv_splits > 1) {
         const int64_t items = static_cast<int64_t>(p.batch) * p.max_q_len * p.hq;
         err = launch_pdl(prefill_merge_kernel,

@@ -250,10 +250,18 @@ pkv_status paged_decode_attention_no_alloc(const void *q, int32_t num_q_heads,
                                            int32_t *dev_status, pkv_stream_t stream);
 
 /* Bytes of device workspace paged_prefill_chunk_attention needs on the
- * current device: 0, except for short bf16 or FP8 chunks (every C_r <= 128 /
- * (Hq / Hkv), a speculative-verify step, say) on grids too small to fill the GPU,
- * whose key ranges are then cut into runs whose fp32 partials a second kernel
- * merges.  The cut depends only on the sizes and the SM count. */
+ * current device (0: none).  Two schedules use one, both for bf16 and FP8
+ * pools (the size covers either dtype; f32 pools need less):
+ *   - short chunks (every C_r <= 128 / (Hq / Hkv), a speculative-verify step,
+ *     say) on grids too small to fill the GPU: their key ranges are cut into
+ *     runs whose fp32 partials a second kernel merges;
+ *   - longer chunks with more (row, kv head, 256-row query tile pair) items
+ *     than SMs: one persistent CTA per SM takes an equal share of the items'
+ *     64-key tiles (computed on the device from the actual lengths by a
+ *     one-CTA plan kernel); an item cut by a CTA boundary is computed in
+ *     pieces whose fp32 partials a merge kernel combines.
+ * Both cuts depend only on the sizes, the lengths and the SM count, so a call
+ * is bit-reproducible. */
 size_t paged_prefill_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                     int32_t head_dim, int32_t block_size, int32_t max_q_len,
                                     int32_t max_seq_len, int32_t window);

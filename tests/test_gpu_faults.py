@@ -225,6 +225,41 @@ def test_wait_timeout_drill_prefill(pkv, fp8):
     assert torch.equal(out, ref)
 
 
+@pytest.mark.parametrize("fp8", [False, True])
+def test_wait_timeout_drill_prefill_balanced_schedule(pkv, fp8):
+    # more (row, kv head, query-tile pair) items than SMs: the persistent
+    # balanced schedule, every CTA's first load withheld
+    w = gen.prefill_workload(seed=28, dtype="bf16", num_q_heads=16, num_kv_heads=4, head_dim=128,
+                             prefix_lens=[0] * 40, chunk_lens=[70] * 40)
+    assert w.batch * w.num_kv_heads * 2 > torch.cuda.get_device_properties(0).multi_processor_count
+    d = Dev(w)
+    kw = {}
+    if fp8:
+        kp, vp = pkv.fp8_pools(w.num_blocks, 4, 128, "cuda")
+        ks, vs = float(gen.FP8_K_SCALE), float(gen.FP8_V_SCALE)
+        kw = {"k_scale": ks, "v_scale": vs}
+    else:
+        kp, vp = d.k_pool, d.v_pool
+    new = torch.from_numpy(pkv.slot_mapping_host(w.block_tables, w.num_blocks, w.new_rows,
+                                                 w.new_pos, 16)).cuda()
+    pkv.paged_kv_append(kp, vp, new, d.k_new, d.v_new, status=d.status, **kw)
+
+    def call():
+        return pkv.paged_prefill_chunk_attention(d.q, d.cu, kp, vp, d.tables, d.seq_lens, 70, 0,
+                                                 w.scale, status=d.status, **kw)
+
+    ref = call().clone()
+    torch.cuda.synchronize()
+    assert int(d.status.item()) == 0
+    _drill(pkv, call)
+    assert int(d.status.item()) & pkv.DEV_TIMEOUT
+    d.status.zero_()
+    out = call()
+    torch.cuda.synchronize()
+    assert int(d.status.item()) == 0
+    assert torch.equal(out, ref)
+
+
 def test_wait_drill_rejects_unknown_flags(pkv):
     with pytest.raises(pkv.PkvError):
         pkv.set_wait_drill(0, 2)

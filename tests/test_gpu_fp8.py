@@ -359,6 +359,19 @@ def test_prefill_scale_sign_and_zero(pkv, orc, scale):
     assert_close(_prefill(pkv, s, w, 0), ref, "bf16", f"fp8 prefill scale {scale}")
 
 
+def test_prefill_balanced_schedule(pkv, orc):
+    # more (row, kv head, query-tile pair) items than SMs: the persistent
+    # balanced schedule with FP8 widening producers, ragged rows, a window
+    w = gen.prefill_workload(seed=398, dtype="bf16", num_q_heads=16, num_kv_heads=4, head_dim=128,
+                             prefix_lens=[0, 5, 130, 300, 1000, 17, 64, 900],
+                             chunk_lens=[600, 1, 64, 65, 300, 129, 512, 33], window=200)
+    assert w.batch * w.num_kv_heads * 10 > torch.cuda.get_device_properties(0).multi_processor_count
+    s = Fp8Step(pkv, orc, w)
+    ref = orc.prefill(w.q, w.cu_q_lens, s.kp, s.vp, "fp8", w.block_tables, w.seq_lens, 200, w.scale,
+                      k_scale=KS, v_scale=VS)
+    assert_close(_prefill(pkv, s, w, 200), ref, "bf16", "fp8 prefill, balanced schedule")
+
+
 def test_prefill_full_size(pkv, orc):
     # the chunked-prefill workload (4 x 512 queries after 16384 cached tokens)
     # on FP8 pools, sampled outputs

@@ -199,3 +199,53 @@ def test_verify_steps_on_decode_kernel(pkv, orc, d, hq, hkv, chunks, window):
                              window=window)
     got, ref, _ = run_prefill(pkv, orc, w)
     assert_close(got, ref, "bf16", f"verify on decode d{d} {hq}/{hkv} w{window}")
+
+
+# ---------------------------------------------------------------------------
+# the persistent balanced schedule: more (row, kv head, query-tile pair)
+# items than SMs; every CTA takes an equal share of the items' 64-key tiles,
+# items cut by a CTA boundary are computed in pieces and merged
+# ---------------------------------------------------------------------------
+
+def _sk_on(pkv, w):
+    """The call runs the balanced schedule (its workspace is the schedule's)."""
+    import torch as _t
+    C = int(np.max(np.diff(w.cu_q_lens)))
+    G = w.num_q_heads // w.num_kv_heads
+    items = w.batch * w.num_kv_heads * -(-C // (2 * (128 // G)))
+    return items > _t.cuda.get_device_properties(0).multi_processor_count
+
+
+@pytest.mark.parametrize("window", [0, 300])
+def test_balanced_schedule_ragged(pkv, orc, window):
+    # 8 ragged rows, 16 q / 4 kv heads: 320 items, short and long key ranges
+    w = gen.prefill_workload(seed=75 + window, dtype="bf16", num_q_heads=16, num_kv_heads=4,
+                             head_dim=128, prefix_lens=[0, 5, 130, 300, 1000, 17, 64, 2000],
+                             chunk_lens=[600, 1, 64, 65, 300, 129, 512, 33], window=window)
+    assert _sk_on(pkv, w)
+    got, ref, _ = run_prefill(pkv, orc, w)
+    assert_close(got, ref, "bf16", f"balanced schedule, window {window}")
+
+
+def test_balanced_schedule_many_tiny_items(pkv, orc):
+    # 40 rows of 70 queries with no prefix: items of one or two tiles, so a
+    # CTA's share runs through many items and most boundaries cut one
+    w = gen.prefill_workload(seed=77, dtype="bf16", num_q_heads=16, num_kv_heads=4, head_dim=128,
+                             prefix_lens=[0] * 40, chunk_lens=[70] * 40)
+    assert _sk_on(pkv, w)
+    got, ref, _ = run_prefill(pkv, orc, w)
+    assert_close(got, ref, "bf16", "balanced schedule, tiny items")
+
+
+def test_balanced_schedule_deterministic(pkv):
+    w = gen.prefill_workload(seed=78, dtype="bf16", num_q_heads=32, num_kv_heads=8, head_dim=128,
+                             prefix_lens=[3000, 700, 50, 1200], chunk_lens=[512, 300, 600, 77])
+    assert _sk_on(pkv, w)
+    d = Dev(w)
+    append(pkv, d)
+    a = pkv.paged_prefill_chunk_attention(d.q, d.cu, d.k_pool, d.v_pool, d.tables, d.seq_lens, 600,
+                                          0, w.scale).clone()
+    b = pkv.paged_prefill_chunk_attention(d.q, d.cu, d.k_pool, d.v_pool, d.tables, d.seq_lens, 600,
+                                          0, w.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b) and int(d.status.item()) == 0
