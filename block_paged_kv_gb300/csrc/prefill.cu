@@ -61,10 +61,12 @@ struct Layout {
     static constexpr int kStagingBytes = kF8 ? 2 * 2 * kF8StageTile : 0;  // K and V, 2 deep
     static constexpr int kBarOff = kStagingOff + kStagingBytes;
     // barriers: k_full[4], k_empty[4], v_full[4], v_empty[4], s_full[tile][buf],
-    // p_full[tile][buf], pv_done[tile], mma_drain[tile], q_full[tile], FP8: staged[K/V][2]
-    static constexpr int kNumBars = 4 * kStages + 4 + 4 + 2 + 2 + 2 + (kF8 ? 4 : 0);
+    // p_full[tile][buf], pv_done[tile], mma_drain[tile], q_full[tile],
+    // FP8: staged[K/V][2], stg_free[K/V][2]
+    static constexpr int kNumBars = 4 * kStages + 4 + 4 + 2 + 2 + 2 + (kF8 ? 8 : 0);
+    // kmask[kStages], FP8: smask[K/V][2] (blocks loaded of each staging buffer)
     static constexpr int kMaskOff = kBarOff + kNumBars * 8;
-    static constexpr int kTmemOff = kMaskOff + kStages * 4;
+    static constexpr int kTmemOff = kMaskOff + (kStages + 4) * 4;
     static constexpr int kSegOff = kTmemOff + 16;  // per softmax warp: its segment walk
     static constexpr int kBytes = kSegOff + kSoftmaxWarps * 96;
     static constexpr int kLaunchBytes = kBytes + 1024;
@@ -326,7 +328,9 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
     uint64_t *mma_drain = bars + 4 * kStages + 10;  // [tile]: the issuer's last products
     uint64_t *q_full = bars + 4 * kStages + 12;     // [tile]: a segment's query tile staged
     uint64_t *staged = bars + 4 * kStages + 14;  // FP8: [K/V * 2 + buffer]
+    uint64_t *stg_free = bars + 4 * kStages + 18;  // FP8: [K/V * 2 + buffer] widened by the softmax warps
     uint32_t *kmask = reinterpret_cast<uint32_t *>(smem + L::kMaskOff);
+    uint32_t *smask = kmask + kStages;  // FP8: [K/V * 2 + buffer] blocks loaded of a staging buffer
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kTmemOff);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = p.group;
@@ -365,10 +369,12 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
-            mbar_init(&k_full[i], 1);
             // the S products of the live tiles + their warpgroups' kmask reads
             mbar_init(&k_empty[i], nqt + nqt * (kSoftmaxWarps / kQTiles));
-            mbar_init(&v_full[i], 1);
+            // FP8: the softmax warps widen K and V into the stages; bf16: one
+            // TMA arrival
+            mbar_init(&k_full[i], kF8 ? nqt * (kSoftmaxWarps / kQTiles) : 1);
+            mbar_init(&v_full[i], kF8 ? nqt * (kSoftmaxWarps / kQTiles) : 1);
             mbar_init(&v_empty[i], nqt);  // the live tiles' P.V products
         }
         for (int i = 0; i < 4; ++i) {
@@ -381,8 +387,10 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         mbar_init(&mma_drain[1], 1);
         mbar_init(&q_full[0], kSoftmaxWarps / kQTiles);
         mbar_init(&q_full[1], kSoftmaxWarps / kQTiles);
-        if (kF8)
+        if (kF8) {
             for (int i = 0; i < 4; ++i) mbar_init(&staged[i], 1);
+            for (int i = 0; i < 4; ++i) mbar_init(&stg_free[i], nqt * (kSoftmaxWarps / kQTiles));
+        }
         fence_mbar_init();
     }
     if (warp == 1) tc::alloc(tmem_slot, kTmemCols);
@@ -450,6 +458,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
                 const uint32_t mask = __ballot_sync(0xffffffffu, good) & ((1u << kBlocks) - 1u);
                 const int32_t tile = nf++;
                 const int sb = tile & 1;
+                if (lane == 0) smask[(is_k ? 0 : 2) + sb] = mask;  // published by the arrival below
                 if (withheld(tile)) return mask;  // diagnostic drill: never issued
                 if (lane == 0) {
                     if (mask == 0)
@@ -469,106 +478,26 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
                 __syncwarp();
                 return mask;
             };
-            TileCursor cw, cf, ci;  // the tile widened, the next fetched, the next id read
-            cw.start(p, qpc, sw0, seg0);
-            cf = cw;
-            ci = cw;
+            // bulk copies only, two tiles ahead; the softmax warps widen each
+            // tile into the ring and release the staging buffer
+            TileCursor cf, ci;
+            cf.start(p, qpc, sw0, seg0);
+            ci = cf;
             int32_t id_next = load_id(ci);
             ci.advance(p, qpc);
-            uint32_t smask[2] = {0u, 0u};
-            for (int i = 0; i < 2 && cf.valid; ++i) {
-                smask[i] = fetch(cf, id_next);
-                cf.advance(p, qpc);
+            int32_t T = 0;
+            for (; cf.valid; ++T, cf.advance(p, qpc)) {
+                const int sb = T & 1;
+                if (T >= 2 && !warp_wait(&stg_free[(is_k ? 0 : 2) + sb], ((T >> 1) + 1) & 1, lane, p.status,
+                                         p.wait_ns))
+                    break;
+                fetch(cf, id_next);
                 id_next = load_id(ci);
                 ci.advance(p, qpc);
             }
-            int32_t T = 0;
-            for (; cw.valid; ++T, cw.advance(p, qpc)) {
-                const int st = T % kStages, sb = T & 1;
-                if (T >= kStages && !warp_wait(&empty[st], ((T / kStages) + 1) & 1, lane, p.status, p.wait_ns)) break;
-                if (!warp_wait(&stg_bar[sb], (T >> 1) & 1, lane, p.status, p.wait_ns)) break;
-                const PrefillRowInfo &w = cw.sg.w;
-                const uint32_t mask = smask[sb];
-                if (is_k && lane == 0) kmask[st] = mask;
-                const uint32_t src = smem_u32(stg + sb * kF8StageTile);
-                const uint32_t dst = smem_u32(ring + st * kTileBytes);
-                const int32_t tbase = cw.kt() * kKeys;
-                const bool edge = tbase < w.kv_lo || tbase + kKeys > w.kv_hi;
-#pragma unroll
-                for (int b = 0; b < kBlocks; ++b) {
-                    const bool loaded = (mask >> b) & 1u;
-                    if (is_k) {
-                        // the scores of keys not loaded are masked by the softmax
-                        if (!loaded) continue;
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            // chunk ch: 64-dim group ch/64, token half (ch/32)%2,
-                            // token 8 half + (ch%32)/4, pair class c = ch%4
-                            const int ch = lane + 32 * i;
-                            const int grp = ch >> 6, half = (ch >> 5) & 1, c = ch & 3;
-                            const int row = b * 16 + half * 8 + ((ch & 31) >> 2);
-                            const uint4 q4 = lds128(src + b * kF8BlockBytes + ch * 16);
-                            const uint32_t wv[4] = {q4.x, q4.y, q4.z, q4.w};
-                            const uint32_t base = dst + grp * kKVRegion + row * 128 + 4 * c;
-#pragma unroll
-                            for (int kk = 0; kk < 4; ++kk) {
-                                uint32_t lo, hi;  // dims 16kk + 2c, +1 | 16kk + 2c + 8, +9
-                                e4m3x4_to_f16x2x2(wv[kk], lo, hi);
-                                sts32(base + (((2 * kk) ^ (row & 7)) << 4), lo);
-                                sts32(base + (((2 * kk + 1) ^ (row & 7)) << 4), hi);
-                            }
-                        }
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            // chunk ch: 32-dim group ch/32, dim class n = (ch%32)/4,
-                            // token pairs c = ch%4: words jn = dim 32g + 8jn + n,
-                            // keys 16b + {2c, 2c+1} (low half) and + 8 (high half)
-                            const int ch = lane + 32 * i;
-                            const int g32 = ch >> 5, n = (ch & 31) >> 2, c = ch & 3;
-                            uint32_t wv[4] = {0u, 0u, 0u, 0u};
-                            if (loaded) {
-                                const uint4 q4 = lds128(src + b * kF8BlockBytes + ch * 16);
-                                wv[0] = q4.x; wv[1] = q4.y; wv[2] = q4.z; wv[3] = q4.w;
-                            }
-                            uint32_t mk0 = 0xffffffffu, mk1 = 0xffffffffu;
-                            if (edge) {
-                                auto live = [&](int k) {
-                                    const int32_t kp = tbase + b * 16 + k;
-                                    return kp >= w.kv_lo && kp < w.kv_hi;
-                                };
-                                mk0 = (live(2 * c) ? 0x0000ffffu : 0u) | (live(2 * c + 1) ? 0xffff0000u : 0u);
-                                mk1 = (live(2 * c + 8) ? 0x0000ffffu : 0u) | (live(2 * c + 9) ? 0xffff0000u : 0u);
-                            }
-#pragma unroll
-                            for (int jn = 0; jn < 4; ++jn) {
-                                const int d = g32 * 32 + jn * 8 + n;
-                                uint32_t lo = 0u, hi = 0u;
-                                if (loaded) e4m3x4_to_f16x2x2(wv[jn], lo, hi);
-                                const uint32_t rowb = dst + d * 128 + 4 * c;
-                                sts32(rowb + (((2 * b) ^ (d & 7)) << 4), lo & mk0);
-                                sts32(rowb + (((2 * b + 1) ^ (d & 7)) << 4), hi & mk1);
-                            }
-                        }
-                    }
-                }
-                // the ring stage is read by the tensor cores (async proxy) and
-                // the staging buffer is refilled by bulk copies after these
-                // generic-proxy accesses
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&full[st]);
-                if (cf.valid) {
-                    smask[sb] = fetch(cf, id_next);  // tile T + 2 into buffer sb
-                    cf.advance(p, qpc);
-                    id_next = load_id(ci);
-                    ci.advance(p, qpc);
-                }
-            }
-            // wind-down (a wait ran out): the staged copies issued but not yet
-            // consumed land before the warp leaves
+            // the copies this warp issued have landed before it leaves
             if (lane == 0)
-                for (int32_t t = T; t < nf; ++t)
+                for (int32_t t = max(0, T - 2); t < T; ++t)
                     if (!withheld(t)) mbar_wait(&stg_bar[t & 1], (t >> 1) & 1);
             __syncwarp();
         } else {
@@ -719,6 +648,59 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         // away from 0 so that a masked score (-inf) never meets a zero factor
         const float sl = fmaxf(fabsf(p.scale_log2), 1e-30f);
         bool abort = false;
+        // FP8: K(Tk)'s staged E4M3 chunks, this thread's share, widened to f16
+        // into ring stage Tk % kStages (key rows, 64-dim 128-byte-swizzled
+        // regions, as the bf16 path lays them out); keys of blocks not loaded
+        // are left as they are (their scores are masked).  The stage is free
+        // once tile Tk - kStages's S products and mask reads are done.
+        const int nthr = nqt * kRows;  // the softmax threads that run
+        auto widen_k = [&](int32_t Tk) {
+            const int sb = Tk & 1, st = Tk % kStages;
+            bool okw = mbar_wait(&staged[sb], (Tk >> 1) & 1, p.wait_ns);
+            if (Tk >= kStages) okw = okw && mbar_wait(&k_empty[st], ((Tk / kStages) + 1) & 1, p.wait_ns);
+            if (__any_sync(0xffffffffu, !okw)) return false;
+            const uint32_t km = smask[sb];
+            if (threadIdx.x == 128) kmask[st] = km;  // for the score masks of tile Tk
+            const uint32_t src = smem_u32(smem + L::kStagingOff + sb * kF8StageTile);
+            const uint32_t dst = smem_u32(k_s + st * kTileBytes);
+            for (int q = threadIdx.x - 128; q < kBlocks * 128; q += nthr) {
+                const int b = q >> 7, ch = q & 127;
+                if (!((km >> b) & 1u)) continue;
+                // chunk ch: 64-dim group ch/64, token half (ch/32)%2, token 8
+                // half + (ch%32)/4, pair class c = ch%4
+                const int grp = ch >> 6, half = (ch >> 5) & 1, c = ch & 3;
+                const int krow = b * 16 + half * 8 + ((ch & 31) >> 2);
+                const uint4 q4 = lds128(src + b * kF8BlockBytes + ch * 16);
+                const uint32_t wv[4] = {q4.x, q4.y, q4.z, q4.w};
+                const uint32_t base = dst + grp * kKVRegion + krow * 128 + 4 * c;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    uint32_t lo, hi;  // dims 16kk + 2c, +1 | 16kk + 2c + 8, +9
+                    e4m3x4_to_f16x2x2(wv[kk], lo, hi);
+                    sts32(base + (((2 * kk) ^ (krow & 7)) << 4), lo);
+                    sts32(base + (((2 * kk + 1) ^ (krow & 7)) << 4), hi);
+                }
+            }
+            // read by the tensor cores (async proxy); the staging buffer is
+            // refilled by bulk copies after these generic-proxy reads
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&k_full[st]);
+                mbar_arrive(&stg_free[sb]);
+            }
+            return true;
+        };
+        // the CTA's tiles over all its segments
+        const int32_t T_total = p.sk_ctas > 0 ? sk_run_start(p, blockIdx.x + 1) - sk_run_start(p, blockIdx.x)
+                                              : seg0.ntile;
+        if constexpr (kF8) {
+            for (int32_t Tk = 0; Tk < min(2, T_total) && !abort; ++Tk)
+                if (!widen_k(Tk)) {
+                    if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
+                    abort = true;
+                }
+        }
         // this warp's segment walk and current segment live in shared memory
         // (lane 0 writes them): the tile loop keeps its registers
         struct SegSmem {
@@ -733,7 +715,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         }
         __syncwarp();
         int32_t T0 = 0;  // the segment's first tile in the running count
-        for (int32_t k = 0;; ++k) {
+        for (int32_t k = 0; !abort; ++k) {
         const int32_t ntile = ss->sg.ntile, jt0 = ss->sg.jt0;
         const int32_t kv_lo = ss->sg.w.kv_lo, kv_hi = ss->sg.w.kv_hi;
         // the segment's query tile: staged (the first in the prologue), then
@@ -751,6 +733,71 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             const int ks = T % kStages, buf = T & 1;
             const int32_t tbase = (jt0 + jj) * kKeys;
             const uint32_t sx = tS(x, buf) + lane_base;
+            if constexpr (kF8) {
+                if (T + 2 < T_total && !widen_k(T + 2)) {
+                    if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
+                    abort = true;
+                    break;
+                }
+            }
+            if constexpr (kF8) {
+                // V(T): this thread's share of the staged E4M3 chunks widened to
+                // f16 into ring stage T % kStages, transposed (dim rows of the
+                // tile's 64 keys, 128-byte swizzled); value columns of keys
+                // outside [kv_lo, kv_hi) or of blocks not loaded as zeros.  The
+                // stage is free once both tiles' P.V(T - kStages) completed.
+                const int sb = T & 1;
+                bool okw = mbar_wait(&staged[2 + sb], (T >> 1) & 1, p.wait_ns);
+                if (T >= kStages) okw = okw && mbar_wait(&v_empty[ks], ((T / kStages) + 1) & 1, p.wait_ns);
+                if (__any_sync(0xffffffffu, !okw)) {
+                    if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
+                    abort = true;
+                    break;
+                }
+                const uint32_t vm = smask[2 + sb];
+                const uint32_t src = smem_u32(smem + L::kStagingOff + 2 * kF8StageTile + sb * kF8StageTile);
+                const uint32_t dst = smem_u32(v_s + ks * kTileBytes);
+                const bool vedge = tbase < kv_lo || tbase + kKeys > kv_hi;
+                for (int q = threadIdx.x - 128; q < kBlocks * 128; q += nthr) {
+                    const int b = q >> 7, ch = q & 127;
+                    // chunk ch: 32-dim group ch/32, dim class n = (ch%32)/4, token
+                    // pairs c = ch%4: words jn = dim 32g + 8jn + n, keys 16b +
+                    // {2c, 2c+1} (low half) and + 8 (high half)
+                    const int g32 = ch >> 5, n = (ch & 31) >> 2, c = ch & 3;
+                    const bool loaded = (vm >> b) & 1u;
+                    uint32_t wv[4] = {0u, 0u, 0u, 0u};
+                    if (loaded) {
+                        const uint4 q4 = lds128(src + b * kF8BlockBytes + ch * 16);
+                        wv[0] = q4.x; wv[1] = q4.y; wv[2] = q4.z; wv[3] = q4.w;
+                    }
+                    uint32_t mk0 = 0xffffffffu, mk1 = 0xffffffffu;
+                    if (vedge) {
+                        auto live = [&](int k) {
+                            const int32_t kp = tbase + b * 16 + k;
+                            return kp >= kv_lo && kp < kv_hi;
+                        };
+                        mk0 = (live(2 * c) ? 0x0000ffffu : 0u) | (live(2 * c + 1) ? 0xffff0000u : 0u);
+                        mk1 = (live(2 * c + 8) ? 0x0000ffffu : 0u) | (live(2 * c + 9) ? 0xffff0000u : 0u);
+                    }
+#pragma unroll
+                    for (int jn = 0; jn < 4; ++jn) {
+                        const int d = g32 * 32 + jn * 8 + n;
+                        uint32_t lo = 0u, hi = 0u;
+                        if (loaded) e4m3x4_to_f16x2x2(wv[jn], lo, hi);
+                        const uint32_t rowb = dst + d * 128 + 4 * c;
+                        sts32(rowb + (((2 * b) ^ (d & 7)) << 4), lo & mk0);
+                        sts32(rowb + (((2 * b + 1) ^ (d & 7)) << 4), hi & mk1);
+                    }
+                }
+                // read by the tensor cores (async proxy); the staging buffer is
+                // refilled by bulk copies after these generic-proxy reads
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&v_full[ks]);
+                    mbar_arrive(&stg_free[2 + sb]);
+                }
+            }
             bool got = mbar_wait(&s_full[x * 2 + buf], (T >> 1) & 1, p.wait_ns);
             got = got && mbar_wait(&k_full[ks], (T / kStages) & 1, p.wait_ns);  // for kmask
             if (__any_sync(0xffffffffu, !got)) {
