@@ -591,15 +591,16 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             const uint64_t vd = dv + static_cast<uint64_t>(T % kStages) * kStageStep;
             const uint32_t a = tS(x, T & 1);
             const uint32_t first = seg_start ? 0u : 1u;
-            // keys 16g..16g+15 hold P hi in S columns 16g..16g+7 and P lo in
-            // 16g+8..16g+15 (bf16 pairs; f16 for FP8 pools)
+            // bf16: keys 16g..16g+15 hold P hi in S columns 16g..16g+7 and P
+            // lo in 16g+8..16g+15 (bf16 pairs); FP8 pools: one f16 term, keys
+            // 16g..16g+15 in columns 8g..8g+7
             if (elect_one()) {
 #pragma unroll
-                for (int part = 0; part < 2; ++part)
+                for (int part = 0; part < (kF8 ? 1 : 2); ++part)
 #pragma unroll
                     for (int kk = 0; kk < kBlocks; ++kk)
-                        tc::mma_ts(tO_x, a + 16 * kk + 8 * part, vd + kVStep * static_cast<uint64_t>(kk),
-                                   idO, (part > 0 || kk > 0) ? 1u : first);
+                        tc::mma_ts(tO_x, a + (kF8 ? 8 : 16) * kk + 8 * part,
+                                   vd + kVStep * static_cast<uint64_t>(kk), idO, (part > 0 || kk > 0) ? 1u : first);
                 tc::commit(&pv_done[x]);
                 tc::commit(&v_empty[T % kStages]);
             }
@@ -844,13 +845,13 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
                 {
                     float m8[8];
     #pragma unroll
-                    for (int e = 0; e < 8; ++e) m8[e] = fmaxf(s[e], s[8 + e]);
-    #pragma unroll
-                    for (int c = 2; c < 8; ++c)
-    #pragma unroll
-                        for (int e = 0; e < 8; ++e) m8[e] = fmaxf(m8[e], s[8 * c + e]);
-                    mt = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * sl;
+                    for (int e = 0; e < 8; ++e) {
+                        m8[e] = fmax3(s[e], s[8 + e], s[16 + e]);
+                        m8[e] = fmax3(m8[e], s[24 + e], s[32 + e]);
+                        m8[e] = fmax3(m8[e], s[40 + e], s[48 + e]);
+                        m8[e] = fmaxf(m8[e], s[56 + e]);
+                    }
+                    mt = fmaxf(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], fmax3(m8[5], m8[6], m8[7]))) * sl;
                 }
                 // keep the reference max within 2^8 of the running max
                 const float new_ref = (mt > m_ref + static_cast<float>(kRescaleLog2)) ? mt : m_ref;
@@ -881,29 +882,53 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
                 }
                 m_ref = new_ref;
                 const float nmu = new_ref == -INFINITY ? 0.f : -new_ref;
-                float ls[4] = {0.f, 0.f, 0.f, 0.f};
-                // group g (16 keys) -> 8 columns of P hi then 8 of P lo, in place
+                // key pairs in paired fp32 arithmetic: 2^(s * sl - m), the
+                // row sum in two paired accumulators
+                const uint64_t sl2 = f2_pack(sl, sl), nmu2 = f2_pack(nmu, nmu);
+                uint64_t ls2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+                auto p_pair = [&](int k, float &a, float &b) {
+                    f2_unpack(f2_fma(f2_pack(s[k], s[k + 1]), sl2, nmu2), a, b);
+                    a = fast_exp2(a);
+                    b = fast_exp2(b);
+                };
+                if constexpr (kF8) {
+                    // one f16 term: keys 2c, 2c+1 -> column c, in place
     #pragma unroll
-                for (int g = 0; g < kBlocks; ++g) {
-                    uint32_t pk[16];
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t pk[16];
     #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float a = fast_exp2(fmaf(s[16 * g + 2 * e], sl, nmu));
-                        const float b = fast_exp2(fmaf(s[16 * g + 2 * e + 1], sl, nmu));
-                        ls[e & 3] += a + b;
-                        if constexpr (kF8) {
-                            const uint32_t hi = pack_f16x2(a, b);
-                            pk[e] = hi;
-                            pk[8 + e] = pack_f16x2(a - f16lo_to_f32(hi), b - f16hi_to_f32(hi));
-                        } else {
+                        for (int e = 0; e < 16; ++e) {
+                            float a, b;
+                            p_pair(32 * h + 2 * e, a, b);
+                            ls2[e & 1] = f2_add(ls2[e & 1], f2_pack(a, b));
+                            pk[e] = pack_f16x2(a, b);
+                        }
+                        tc::st16(sx + 16 * h, pk);
+                    }
+                } else {
+                    // group g (16 keys) -> 8 columns of P hi then 8 of P lo
+    #pragma unroll
+                    for (int g = 0; g < kBlocks; ++g) {
+                        uint32_t pk[16];
+    #pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            float a, b;
+                            p_pair(16 * g + 2 * e, a, b);
+                            const uint64_t ab = f2_pack(a, b);
+                            ls2[e & 1] = f2_add(ls2[e & 1], ab);
                             const uint32_t hi = pack_bf16x2(a, b);
                             pk[e] = hi;
-                            pk[8 + e] = pack_bf16x2(a - bf16lo_to_f32(hi), b - bf16hi_to_f32(hi));
+                            float ra, rb;
+                            f2_unpack(f2_sub(ab, f2_pack(bf16lo_to_f32(hi), bf16hi_to_f32(hi))), ra, rb);
+                            pk[8 + e] = pack_bf16x2(ra, rb);
                         }
+                        tc::st16(sx + 16 * g, pk);
                     }
-                    tc::st16(sx + 16 * g, pk);
                 }
-                l = l * (resc ? alpha : 1.f) + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
+                float l0, l1, l2, l3;
+                f2_unpack(ls2[0], l0, l1);
+                f2_unpack(ls2[1], l2, l3);
+                l = l * (resc ? alpha : 1.f) + ((l0 + l1) + (l2 + l3));
             }
             // V(jj) must have landed before this tile's P.V is issued.  Value
             // rows of keys outside [kv_lo, kv_hi) or of blocks not loaded hold
