@@ -565,46 +565,40 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         constexpr uint64_t kVStep = kF8 ? (32 >> 4) : (2048 >> 4);
         constexpr uint64_t kStageStep = kTileBytes >> 4;
         const uint32_t tO_x = tO(x);
-        // The whole warp runs these; one elected lane issues a group's
-        // products and commits from one straight-line block.
-        auto s_mma = [&](int32_t T) {  // once K(T) has landed (T: the CTA's running tile count)
-            if (!warp_wait(&k_full[T % kStages], (T / kStages) & 1, lane, p.status, p.wait_ns)) return false;
-            tc::fence_after();
+        // The whole warp waits; one elected lane issues a step's products and
+        // commits from one straight-line block.
+        auto k_landed = [&](int32_t T) {  // K(T) landed (T: the CTA's running tile count)
+            return warp_wait(&k_full[T % kStages], (T / kStages) & 1, lane, p.status, p.wait_ns);
+        };
+        auto s_issue = [&](int32_t T) {  // S(T) = Q K(T)^T
             const uint64_t kd = dk + static_cast<uint64_t>(T % kStages) * kStageStep;
             const uint32_t d = tS(x, T & 1);
-            if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t qo = static_cast<uint64_t>(((kk >> 2) * (kRows * 128) + (kk & 3) * 32) >> 4);
-                    const uint64_t ko = static_cast<uint64_t>(((kk >> 2) * kKVRegion + (kk & 3) * 32) >> 4);
-                    tc::mma_ss(d, dq + qo, kd + ko, idS, kk > 0 ? 1u : 0u);
-                }
-                tc::commit(&s_full[x * 2 + (T & 1)]);
-                tc::commit(&k_empty[T % kStages]);
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint64_t qo = static_cast<uint64_t>(((kk >> 2) * (kRows * 128) + (kk & 3) * 32) >> 4);
+                const uint64_t ko = static_cast<uint64_t>(((kk >> 2) * kKVRegion + (kk & 3) * 32) >> 4);
+                tc::mma_ss(d, dq + qo, kd + ko, idS, kk > 0 ? 1u : 0u);
             }
-            __syncwarp();
-            return true;
+            tc::commit(&s_full[x * 2 + (T & 1)]);
+            tc::commit(&k_empty[T % kStages]);
         };
-        // V(T) has landed: the warpgroup checked it; a segment's first tile
-        // starts O afresh
-        auto pv_mma = [&](int32_t T, bool seg_start) {
+        // O += P(T) V(T); V(T) has landed (the warpgroup checked it before
+        // handing P over); a segment's first tile starts O afresh
+        auto pv_issue = [&](int32_t T, bool seg_start) {
             const uint64_t vd = dv + static_cast<uint64_t>(T % kStages) * kStageStep;
             const uint32_t a = tS(x, T & 1);
             const uint32_t first = seg_start ? 0u : 1u;
             // bf16: keys 16g..16g+15 hold P hi in S columns 16g..16g+7 and P
             // lo in 16g+8..16g+15 (bf16 pairs); FP8 pools: one f16 term, keys
             // 16g..16g+15 in columns 8g..8g+7
-            if (elect_one()) {
 #pragma unroll
-                for (int part = 0; part < (kF8 ? 1 : 2); ++part)
+            for (int part = 0; part < (kF8 ? 1 : 2); ++part)
 #pragma unroll
-                    for (int kk = 0; kk < kBlocks; ++kk)
-                        tc::mma_ts(tO_x, a + (kF8 ? 8 : 16) * kk + 8 * part,
-                                   vd + kVStep * static_cast<uint64_t>(kk), idO, (part > 0 || kk > 0) ? 1u : first);
-                tc::commit(&pv_done[x]);
-                tc::commit(&v_empty[T % kStages]);
-            }
-            __syncwarp();
+                for (int kk = 0; kk < kBlocks; ++kk)
+                    tc::mma_ts(tO_x, a + (kF8 ? 8 : 16) * kk + 8 * part, vd + kVStep * static_cast<uint64_t>(kk),
+                               idO, (part > 0 || kk > 0) ? 1u : first);
+            tc::commit(&pv_done[x]);
+            tc::commit(&v_empty[T % kStages]);
         };
         SegWalk sw = sw0;
         Seg sg = seg0;
@@ -614,17 +608,30 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             // the segment's query tile is staged (the previous segment's
             // products, which read the old one, completed before its epilogue)
             bool ok = warp_wait(&q_full[x], k & 1, lane, p.status, p.wait_ns);
+            ok = ok && k_landed(T0) && (n < 2 || k_landed(T0 + 1));
             if (ok) {
                 tc::fence_after();
-                ok = s_mma(T0) && (n < 2 || s_mma(T0 + 1));
+                if (elect_one()) {
+                    s_issue(T0);
+                    if (n >= 2) s_issue(T0 + 1);
+                }
+                __syncwarp();
             }
+            // per tile: K(T+2) is waited for first (it landed, or was widened,
+            // long before P(T) is ready), so that P(T).V(T) and S(T+2) leave
+            // in one block as soon as P(T) is
             for (int32_t j = 0; j < n && ok; ++j) {
                 const int32_t T = T0 + j;
-                ok = warp_wait(&p_full[x * 2 + (T & 1)], (T >> 1) & 1, lane, p.status, p.wait_ns);
+                const bool more = j + 2 < n;
+                if (more) ok = k_landed(T + 2);
+                ok = ok && warp_wait(&p_full[x * 2 + (T & 1)], (T >> 1) & 1, lane, p.status, p.wait_ns);
                 if (!ok) break;
                 tc::fence_after();
-                pv_mma(T, j == 0);
-                if (j + 2 < n) ok = s_mma(T + 2);
+                if (elect_one()) {
+                    pv_issue(T, j == 0);
+                    if (more) s_issue(T + 2);
+                }
+                __syncwarp();
             }
             if (!ok) break;
             T0 += n;
