@@ -279,6 +279,17 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x)
     return y;
 }
 
+// Four 8x8 matrices of 16-bit elements to shared memory, each held as one
+// 32-bit pair per lane (lane l: row l/4, columns 2(l%4), 2(l%4)+1): matrix j
+// from register j; lane 8j + i gives the address of matrix j's row i (16
+// bytes, 16-byte aligned).
+__device__ __forceinline__ void stsm_x4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b),
+                 "r"(c), "r"(d)
+                 : "memory");
+}
+
 // 16-byte shared-memory load
 __device__ __forceinline__ uint4 lds128(uint32_t addr)
 {

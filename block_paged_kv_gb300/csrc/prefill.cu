@@ -671,23 +671,27 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             if (threadIdx.x == 128) kmask[st] = km;  // for the score masks of tile Tk
             const uint32_t src = smem_u32(smem + L::kStagingOff + sb * kF8StageTile);
             const uint32_t dst = smem_u32(k_s + st * kTileBytes);
+            // A warp takes 32 chunks of one (block, 64-dim group, token half):
+            // lane l holds key 8 half + l/4, dims 16kk + 2(l%4) + {0, 1, 8, 9}
+            // (kk = 0..3), i.e. the 8x8 matrices (keys) x (dims 16kk + 8h ..
+            // + 7) in the fragment order that stmatrix stores as 16-byte rows.
+            // Matrix 2kk + h is 16-byte chunk 2kk + h of each key's 128-byte
+            // row, swizzled by the key row.
+            const int mr = lane & 7, mm = lane >> 3;  // this lane's row address: row mr of matrix mm
             for (int q = threadIdx.x - 128; q < kBlocks * 128; q += nthr) {
-                const int b = q >> 7, ch = q & 127;
+                const int b = q >> 7, ch = q & 127;  // warp-uniform but for ch % 32
                 if (!((km >> b) & 1u)) continue;
-                // chunk ch: 64-dim group ch/64, token half (ch/32)%2, token 8
-                // half + (ch%32)/4, pair class c = ch%4
-                const int grp = ch >> 6, half = (ch >> 5) & 1, c = ch & 3;
-                const int krow = b * 16 + half * 8 + ((ch & 31) >> 2);
+                const int grp = ch >> 6, half = (ch >> 5) & 1;
                 const uint4 q4 = lds128(src + b * kF8BlockBytes + ch * 16);
-                const uint32_t wv[4] = {q4.x, q4.y, q4.z, q4.w};
-                const uint32_t base = dst + grp * kKVRegion + krow * 128 + 4 * c;
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    uint32_t lo, hi;  // dims 16kk + 2c, +1 | 16kk + 2c + 8, +9
-                    e4m3x4_to_f16x2x2(wv[kk], lo, hi);
-                    sts32(base + (((2 * kk) ^ (krow & 7)) << 4), lo);
-                    sts32(base + (((2 * kk + 1) ^ (krow & 7)) << 4), hi);
-                }
+                uint32_t f[8];  // f[2kk + h]: matrix (kk, h)
+                e4m3x4_to_f16x2x2(q4.x, f[0], f[1]);
+                e4m3x4_to_f16x2x2(q4.y, f[2], f[3]);
+                e4m3x4_to_f16x2x2(q4.z, f[4], f[5]);
+                e4m3x4_to_f16x2x2(q4.w, f[6], f[7]);
+                const int krow = b * 16 + half * 8 + mr;
+                const uint32_t rowa = dst + grp * kKVRegion + krow * 128;
+                stsm_x4(rowa + ((mm ^ mr) << 4), f[0], f[1], f[2], f[3]);
+                stsm_x4(rowa + (((4 + mm) ^ mr) << 4), f[4], f[5], f[6], f[7]);
             }
             // read by the tensor cores (async proxy); the staging buffer is
             // refilled by bulk copies after these generic-proxy reads
@@ -766,36 +770,42 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
                 const uint32_t src = smem_u32(smem + L::kStagingOff + 2 * kF8StageTile + sb * kF8StageTile);
                 const uint32_t dst = smem_u32(v_s + ks * kTileBytes);
                 const bool vedge = tbase < kv_lo || tbase + kKeys > kv_hi;
+                // A warp takes the 32 chunks of one (block, 32-dim group): lane
+                // l holds dim 32g + 8jn + l/4 (jn = 0..3) for keys 16b + 2(l%4)
+                // + {0, 1, 8, 9}, i.e. the 8x8 matrices (dims 32g + 8jn .. + 7)
+                // x (keys 16b + 8h .. + 7) in stmatrix fragment order.  Matrix
+                // (jn, h) is 16-byte chunk 2b + h of each dim row, swizzled by
+                // the dim row.
+                const int mr = lane & 7, mm = lane >> 3, c = lane & 3;
                 for (int q = threadIdx.x - 128; q < kBlocks * 128; q += nthr) {
-                    const int b = q >> 7, ch = q & 127;
-                    // chunk ch: 32-dim group ch/32, dim class n = (ch%32)/4, token
-                    // pairs c = ch%4: words jn = dim 32g + 8jn + n, keys 16b +
-                    // {2c, 2c+1} (low half) and + 8 (high half)
-                    const int g32 = ch >> 5, n = (ch & 31) >> 2, c = ch & 3;
-                    const bool loaded = (vm >> b) & 1u;
-                    uint32_t wv[4] = {0u, 0u, 0u, 0u};
-                    if (loaded) {
+                    const int b = q >> 7, ch = q & 127;  // warp-uniform but for ch % 32
+                    const int g32 = ch >> 5;
+                    uint32_t f[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};  // f[2jn + h]: matrix (jn, h)
+                    if ((vm >> b) & 1u) {
                         const uint4 q4 = lds128(src + b * kF8BlockBytes + ch * 16);
-                        wv[0] = q4.x; wv[1] = q4.y; wv[2] = q4.z; wv[3] = q4.w;
-                    }
-                    uint32_t mk0 = 0xffffffffu, mk1 = 0xffffffffu;
-                    if (vedge) {
-                        auto live = [&](int k) {
-                            const int32_t kp = tbase + b * 16 + k;
-                            return kp >= kv_lo && kp < kv_hi;
-                        };
-                        mk0 = (live(2 * c) ? 0x0000ffffu : 0u) | (live(2 * c + 1) ? 0xffff0000u : 0u);
-                        mk1 = (live(2 * c + 8) ? 0x0000ffffu : 0u) | (live(2 * c + 9) ? 0xffff0000u : 0u);
-                    }
+                        e4m3x4_to_f16x2x2(q4.x, f[0], f[1]);
+                        e4m3x4_to_f16x2x2(q4.y, f[2], f[3]);
+                        e4m3x4_to_f16x2x2(q4.z, f[4], f[5]);
+                        e4m3x4_to_f16x2x2(q4.w, f[6], f[7]);
+                        if (vedge) {
+                            auto live = [&](int k) {
+                                const int32_t kp = tbase + b * 16 + k;
+                                return kp >= kv_lo && kp < kv_hi;
+                            };
+                            const uint32_t mk0 = (live(2 * c) ? 0x0000ffffu : 0u) | (live(2 * c + 1) ? 0xffff0000u : 0u);
+                            const uint32_t mk1 = (live(2 * c + 8) ? 0x0000ffffu : 0u) | (live(2 * c + 9) ? 0xffff0000u : 0u);
 #pragma unroll
-                    for (int jn = 0; jn < 4; ++jn) {
-                        const int d = g32 * 32 + jn * 8 + n;
-                        uint32_t lo = 0u, hi = 0u;
-                        if (loaded) e4m3x4_to_f16x2x2(wv[jn], lo, hi);
-                        const uint32_t rowb = dst + d * 128 + 4 * c;
-                        sts32(rowb + (((2 * b) ^ (d & 7)) << 4), lo & mk0);
-                        sts32(rowb + (((2 * b + 1) ^ (d & 7)) << 4), hi & mk1);
+                            for (int jn = 0; jn < 4; ++jn) {
+                                f[2 * jn] &= mk0;
+                                f[2 * jn + 1] &= mk1;
+                            }
+                        }
                     }
+                    // row mr of matrix mm: dim 32g + 8(jn0 + mm/2) + mr, chunk 2b + mm%2
+                    const uint32_t rowa = dst + (g32 * 32 + (mm >> 1) * 8 + mr) * 128;
+                    const uint32_t cx = static_cast<uint32_t>(((2 * b + (mm & 1)) ^ mr) << 4);
+                    stsm_x4(rowa + cx, f[0], f[1], f[2], f[3]);
+                    stsm_x4(rowa + 16 * 128 + cx, f[4], f[5], f[6], f[7]);
                 }
                 // read by the tensor cores (async proxy); the staging buffer is
                 // refilled by bulk copies after these generic-proxy reads
