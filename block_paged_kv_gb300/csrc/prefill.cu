@@ -371,10 +371,10 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         for (int i = 0; i < kStages; ++i) {
             // the S products of the live tiles + their warpgroups' kmask reads
             mbar_init(&k_empty[i], nqt + nqt * (kSoftmaxWarps / kQTiles));
-            // FP8: the softmax warps widen K and V into the stages; bf16: one
-            // TMA arrival
-            mbar_init(&k_full[i], kF8 ? nqt * (kSoftmaxWarps / kQTiles) : 1);
-            mbar_init(&v_full[i], kF8 ? nqt * (kSoftmaxWarps / kQTiles) : 1);
+            // FP8: one softmax warpgroup widens K into the stages, the other
+            // V (tile A's both when it runs alone); bf16: one TMA arrival
+            mbar_init(&k_full[i], kF8 ? kSoftmaxWarps / kQTiles : 1);
+            mbar_init(&v_full[i], kF8 ? kSoftmaxWarps / kQTiles : 1);
             mbar_init(&v_empty[i], nqt);  // the live tiles' P.V products
         }
         for (int i = 0; i < 4; ++i) {
@@ -389,7 +389,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         mbar_init(&q_full[1], kSoftmaxWarps / kQTiles);
         if (kF8) {
             for (int i = 0; i < 4; ++i) mbar_init(&staged[i], 1);
-            for (int i = 0; i < 4; ++i) mbar_init(&stg_free[i], nqt * (kSoftmaxWarps / kQTiles));
+            for (int i = 0; i < 4; ++i) mbar_init(&stg_free[i], kSoftmaxWarps / kQTiles);
         }
         fence_mbar_init();
     }
@@ -656,12 +656,18 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         // away from 0 so that a masked score (-inf) never meets a zero factor
         const float sl = fmaxf(fabsf(p.scale_log2), 1e-30f);
         bool abort = false;
-        // FP8: K(Tk)'s staged E4M3 chunks, this thread's share, widened to f16
+        // FP8: tile A's warpgroup widens K, tile B's V (tile A's both when it
+        // runs alone), each 128 threads over a tile's 512 staged chunks: a
+        // warp then waits for one staging and one ring barrier per tile, and
+        // the two warpgroups need not run in step.
+        // K(Tk)'s staged E4M3 chunks, this thread's share, widened to f16
         // into ring stage Tk % kStages (key rows, 64-dim 128-byte-swizzled
         // regions, as the bf16 path lays them out); keys of blocks not loaded
         // are left as they are (their scores are masked).  The stage is free
         // once tile Tk - kStages's S products and mask reads are done.
-        const int nthr = nqt * kRows;  // the softmax threads that run
+        const int nthr = kRows;
+        const bool do_k = nqt == 1 || x == 0, do_v = nqt == 1 || x == 1;
+        const int wq0 = (threadIdx.x - 128) & (kRows - 1);  // this thread's first chunk
         auto widen_k = [&](int32_t Tk) {
             const int sb = Tk & 1, st = Tk % kStages;
             bool okw = mbar_wait(&staged[sb], (Tk >> 1) & 1, p.wait_ns);
@@ -678,7 +684,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             // Matrix 2kk + h is 16-byte chunk 2kk + h of each key's 128-byte
             // row, swizzled by the key row.
             const int mr = lane & 7, mm = lane >> 3;  // this lane's row address: row mr of matrix mm
-            for (int q = threadIdx.x - 128; q < kBlocks * 128; q += nthr) {
+            for (int q = wq0; q < kBlocks * 128; q += nthr) {
                 const int b = q >> 7, ch = q & 127;  // warp-uniform but for ch % 32
                 if (!((km >> b) & 1u)) continue;
                 const int grp = ch >> 6, half = (ch >> 5) & 1;
@@ -707,7 +713,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         const int32_t T_total = p.sk_ctas > 0 ? sk_run_start(p, blockIdx.x + 1) - sk_run_start(p, blockIdx.x)
                                               : seg0.ntile;
         if constexpr (kF8) {
-            for (int32_t Tk = 0; Tk < min(2, T_total) && !abort; ++Tk)
+            for (int32_t Tk = 0; do_k && Tk < min(2, T_total) && !abort; ++Tk)
                 if (!widen_k(Tk)) {
                     if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
                     abort = true;
@@ -746,13 +752,13 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             const int32_t tbase = (jt0 + jj) * kKeys;
             const uint32_t sx = tS(x, buf) + lane_base;
             if constexpr (kF8) {
-                if (T + 2 < T_total && !widen_k(T + 2)) {
+                if (do_k && T + 2 < T_total && !widen_k(T + 2)) {
                     if (lane == 0) report(p.status, PKV_DEV_TIMEOUT);
                     abort = true;
                     break;
                 }
             }
-            if constexpr (kF8) {
+            if (kF8 && do_v) {
                 // V(T): this thread's share of the staged E4M3 chunks widened to
                 // f16 into ring stage T % kStages, transposed (dim rows of the
                 // tile's 64 keys, 128-byte swizzled); value columns of keys
@@ -777,7 +783,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
                 // (jn, h) is 16-byte chunk 2b + h of each dim row, swizzled by
                 // the dim row.
                 const int mr = lane & 7, mm = lane >> 3, c = lane & 3;
-                for (int q = threadIdx.x - 128; q < kBlocks * 128; q += nthr) {
+                for (int q = wq0; q < kBlocks * 128; q += nthr) {
                     const int b = q >> 7, ch = q & 127;  // warp-uniform but for ch % 32
                     const int g32 = ch >> 5;
                     uint32_t f[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};  // f[2jn + h]: matrix (jn, h)
