@@ -288,7 +288,8 @@ size_t paged_prefill_workspace_size(int32_t batch, int32_t num_q_heads, int32_t 
  * the split-KV decode kernel instead, one M-row per (query, head) pair, for
  * head_dim 64, 128 or 256.  FP8 pools: the tensor-core kernel widens the E4M3
  * tiles to f16 in shared memory and multiplies f16 x f16 (the query converted
- * to f16, PKV_DEV_Q_RANGE past 65504), P as f16 hi + lo terms.
+ * to f16, PKV_DEV_Q_RANGE past 65504), P as one f16 term (2^-11 relative, as
+ * in the FP8 decode).
  */
 pkv_status paged_prefill_chunk_attention(const void *q, const int32_t *cu_q_lens,
                                          int32_t num_q_heads, const pkv_pool *pool,
