@@ -133,12 +133,15 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, int la
 // its key range [kv_lo, kv_hi).
 //   one CTA per item (sk_ctas == 0): one segment, the item's whole range or,
 //     for the key-range runs of a short chunk, one run of it;
-//   persistent balanced schedule (sk_ctas > 0): the items' tiles in item
-//     order form one sequence of W tiles (sk_prefix, written by
-//     prefill_sk_plan_kernel); CTA c takes tiles [c W / n, (c + 1) W / n),
-//     item by item.  Only its first and its last segment can cut an item;
-//     a cut segment writes a partial to slot 0 (first) or 1 (last) of the
-//     CTA, and prefill_sk_merge_kernel combines an item's pieces.
+//   persistent balanced schedule (sk_ctas = n > 0, fewer than the items):
+//     the items' tiles in item order form one sequence of W tiles
+//     (sk_prefix, written by prefill_sk_plan_kernel).  CTA c first runs item
+//     c whole (the CTAs of one (row, kv head) then start together and share
+//     its K/V through L2), then takes the tiles [B + c R / n, B + (c + 1) R
+//     / n) of the rest (B = the first n items' tiles, R = W - B), item by
+//     item.  Only the first and the last segment of that run can cut an
+//     item; a cut segment writes a partial to slot 0 (first) or 1 (last) of
+//     the CTA, and the warp that completes an item's pieces merges them.
 // ---------------------------------------------------------------------------
 struct Seg {
     PrefillRowInfo w;
@@ -155,10 +158,11 @@ struct SegWalk {
     int32_t k;         // segments returned so far
 };
 
+// start of CTA c's balanced run (c = n: the end of the sequence)
 __device__ __forceinline__ int32_t sk_run_start(const PrefillParams &p, int32_t c)
 {
-    const int64_t W = __ldg(p.sk_prefix + p.sk_items);
-    return static_cast<int32_t>(static_cast<int64_t>(c) * W / p.sk_ctas);
+    const int64_t B = __ldg(p.sk_prefix + p.sk_ctas), W = __ldg(p.sk_prefix + p.sk_items);
+    return static_cast<int32_t>(B + static_cast<int64_t>(c) * (W - B) / p.sk_ctas);
 }
 
 // the item holding tile pos: the largest u with prefix[u] <= pos
@@ -172,11 +176,11 @@ __device__ __forceinline__ int32_t sk_item_of(const PrefillParams &p, int32_t po
     return lo;
 }
 
-// the CTA whose run holds tile pos
+// the CTA whose balanced run holds tile pos (pos past the first n items)
 __device__ __forceinline__ int32_t sk_cta_of(const PrefillParams &p, int32_t pos)
 {
-    const int64_t W = __ldg(p.sk_prefix + p.sk_items);
-    int32_t c = W > 0 ? static_cast<int32_t>(static_cast<int64_t>(pos) * p.sk_ctas / W) : 0;
+    const int64_t B = __ldg(p.sk_prefix + p.sk_ctas), W = __ldg(p.sk_prefix + p.sk_items);
+    int32_t c = W > B ? static_cast<int32_t>((pos - B) * static_cast<int64_t>(p.sk_ctas) / (W - B)) : 0;
     c = min(max(c, 0), p.sk_ctas - 1);
     while (c + 1 < p.sk_ctas && sk_run_start(p, c + 1) <= pos) ++c;
     while (c > 0 && sk_run_start(p, c) > pos) --c;
@@ -212,11 +216,21 @@ __device__ __forceinline__ bool seg_first(const PrefillParams &p, int qpc, int64
                                           Seg &sg)
 {
     if (p.sk_ctas > 0) {
-        sw.pos = sk_run_start(p, static_cast<int32_t>(cta));
-        sw.end = sk_run_start(p, static_cast<int32_t>(cta) + 1);
+        const int32_t c = static_cast<int32_t>(cta);
+        sw.pos = sk_run_start(p, c);
+        sw.end = sk_run_start(p, c + 1);
         sw.k = 0;
-        if (sw.pos >= sw.end) return false;
-        sw.u = sk_item_of(p, sw.pos);
+        sw.u = sw.pos < sw.end ? sk_item_of(p, sw.pos) : 0;
+        const int32_t lo = __ldg(p.sk_prefix + c), hi = __ldg(p.sk_prefix + c + 1);
+        if (hi > lo) {  // item c, whole
+            prefill_item(p, c, qpc, sg.w);  // an item with tiles has queries
+            sg.item = c;
+            sg.jt0 = sg.w.kv_lo / pf::kKeys;
+            sg.ntile = hi - lo;
+            sg.whole = true;
+            sg.slot = 0;
+            return true;
+        }
         return sk_next(p, qpc, sw, sg);
     }
     if (!prefill_item(p, cta, qpc, sg.w)) return false;
@@ -710,8 +724,10 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             return true;
         };
         // the CTA's tiles over all its segments
-        const int32_t T_total = p.sk_ctas > 0 ? sk_run_start(p, blockIdx.x + 1) - sk_run_start(p, blockIdx.x)
-                                              : seg0.ntile;
+        const int32_t T_total =
+            p.sk_ctas > 0 ? __ldg(p.sk_prefix + blockIdx.x + 1) - __ldg(p.sk_prefix + blockIdx.x) +
+                                sk_run_start(p, blockIdx.x + 1) - sk_run_start(p, blockIdx.x)
+                          : seg0.ntile;
         if constexpr (kF8) {
             for (int32_t Tk = 0; do_k && Tk < min(2, T_total) && !abort; ++Tk)
                 if (!widen_k(Tk)) {
