@@ -237,6 +237,19 @@ def test_balanced_schedule_many_tiny_items(pkv, orc):
     assert_close(got, ref, "bf16", "balanced schedule, tiny items")
 
 
+def test_balanced_schedule_items_just_past_sms(pkv, orc):
+    # a few items more than SMs: each CTA runs one item whole, then the few
+    # remaining items' tiles are shared by all CTAs, so each of them is cut
+    # into about twenty pieces that one warp merges
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    rows = -(-(n_sm + 8) // 32)  # 8 kv heads x 4 query-tile pairs per row
+    w = gen.prefill_workload(seed=79, dtype="bf16", num_q_heads=32, num_kv_heads=8, head_dim=128,
+                             prefix_lens=[1500 - 37 * r for r in range(rows)], chunk_lens=[256] * rows)
+    assert _sk_on(pkv, w)
+    got, ref, _ = run_prefill(pkv, orc, w)
+    assert_close(got, ref, "bf16", "balanced schedule, items just past the SMs")
+
+
 def test_balanced_schedule_deterministic(pkv):
     w = gen.prefill_workload(seed=78, dtype="bf16", num_q_heads=32, num_kv_heads=8, head_dim=128,
                              prefix_lens=[3000, 700, 50, 1200], chunk_lens=[512, 300, 600, 77])
