@@ -4,30 +4,36 @@
 // row's chunk sits at absolute position p = L - C + i and attends positions
 // max(0, p - W + 1) .. p: the whole prefix and the chunk causally.
 //
-// bf16 kernel, one CTA per (row, kv head, two tiles of 128/G queries).  A
-// tile's 128 M-rows are (query, head) pairs of all G q heads of the kv head,
-// and both tiles share every K/V tile, so K/V are loaded once per 256 query
-// rows.  QK^T and PV are dense contractions and run on the 5th-generation
-// tensor cores:
-//   warps 0/2 TMA producers: K and V tiles of 64 keys (4 paged blocks, two
-//             64-dim boxes each) into 4-stage rings; a K stage is freed once
-//             both S products are computed and the key masks read, a V stage
-//             once both P.V products are;
+// Tensor-core kernel (bf16 pools; FP8 pools the same kernel with widening),
+// work item = (row, kv head, two tiles of 128/G queries).  A tile's 128 M-rows
+// are (query, head) pairs of all G q heads of the kv head, and both tiles
+// share every K/V tile, so K/V are loaded once per 256 query rows.  QK^T and
+// PV are dense contractions and run on the 5th-generation tensor cores:
+//   warps 0/2 producers: K and V tiles of 64 keys (4 paged blocks) into
+//             4-stage rings (bf16: two 64-dim TMA boxes a block; FP8: bulk
+//             copies of the E4M3 blocks into a two-deep staging buffer); a K
+//             stage is freed once both S products are computed and the key
+//             masks read, a V stage once both P.V products are;
 //   warps 1/3 issue tile A's / tile B's tcgen05.mma from one elected lane:
 //             S = Q K^T into one of the tile's two S buffers in tensor memory
 //             (both operands K-major, 128-byte swizzle), O += P V with P read
-//             from tensor memory (V MN-major); per K/V tile j: P(j).V, then
-//             S(j+2) into the buffer that product just read.  Warp 1 also
-//             allocates the 512 tensor-memory columns;
+//             from tensor memory; per K/V tile j, once K(j+2) has landed and
+//             P(j) is stored: P(j).V, then S(j+2) into the buffer that product
+//             reads.  Warp 1 also allocates the 512 tensor-memory columns;
 //   warps 4-7 / 8-11  softmax of tile A / tile B, concurrently, one M-row per
 //             thread: S from tensor memory, causal / window / range mask,
 //             running max kept within 2^8 of the true maximum (O is rescaled
 //             in tensor memory only when it moves further), P written back
-//             over S as bf16 hi + lo terms, 8 columns each per 16 keys (P.V
-//             then carries P to ~2^-17 relative), and the epilogue O / l.
-// A short chunk fills tile A only (tile B's warps stay idle, warps whose rows
-// hold no query skip the softmax work); on a grid too small for the GPU its
-// key range is cut into runs whose fp32 partials prefill_merge_kernel merges.
+//             over S (bf16: hi + lo terms, 8 columns each per 16 keys, so
+//             that P.V carries P to ~2^-17 relative; FP8 pools: one f16
+//             term), and the epilogue O / l.  FP8 pools: tile A's warps also
+//             widen the staged K tiles to f16, tile B's the V tiles.
+// Schedules: one CTA per item while the items fit one wave; more items than
+// SMs: one persistent CTA per SM (a whole item, then an equal run of the
+// remaining items' tiles, cut pieces merged in the kernel).  A short chunk
+// fills tile A only (tile B's warps stay idle, warps whose rows hold no query
+// skip the softmax work); on a grid too small for the GPU its key range is
+// cut into runs whose fp32 partials prefill_merge_kernel merges.
 // f32 kernel: CUDA cores, the same work split with 16 (query, head) pairs per
 // CTA, for the fp32 pools.
 #include <algorithm>
