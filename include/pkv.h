@@ -282,8 +282,9 @@ size_t paged_prefill_workspace_size(int32_t batch, int32_t num_q_heads, int32_t 
  *   workspace:   device, >= paged_prefill_workspace_size(...) bytes, 256-byte
  *                aligned (NULL when that size is 0)
  * Built: bf16 and FP8, block_size 16, head_dim 128, Hq / Hkv <= 16 (tcgen05 tensor
- * cores, fp32 accumulation in tensor memory; probabilities enter the P.V
- * product as bf16 hi + lo terms); f32 pools run a CUDA-core kernel.  bf16
+ * cores, fp32 accumulation in tensor memory; for bf16 pools probabilities
+ * enter the P.V product as bf16 hi + lo terms); f32 pools run a CUDA-core
+ * kernel.  bf16
  * chunks with max_q_len * (Hq / Hkv) <= 16 (a speculative-verify step) run on
  * the split-KV decode kernel instead, one M-row per (query, head) pair, for
  * head_dim 64, 128 or 256.  FP8 pools: the tensor-core kernel widens the E4M3

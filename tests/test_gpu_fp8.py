@@ -338,7 +338,7 @@ def _prefill(pkv, s, w, window):
 @pytest.mark.parametrize("hq,hkv,window", [(8, 2, 0), (32, 8, 0), (16, 16, 64), (8, 1, 200)])
 def test_prefill_chunks(pkv, orc, hq, hkv, window):
     # chunks past 16 (query, head) pairs run on the tensor-core prefill kernel,
-    # its producers widening the E4M3 tiles to f16 in shared memory
+    # its softmax warpgroups widening the E4M3 tiles to f16 in shared memory
     w = gen.prefill_workload(seed=390 + hq + window, dtype="bf16", num_q_heads=hq,
                              num_kv_heads=hkv, head_dim=128, prefix_lens=[0, 90, 300, 1000],
                              chunk_lens=[37, 64, 130, 300], window=window)
@@ -361,7 +361,7 @@ def test_prefill_scale_sign_and_zero(pkv, orc, scale):
 
 def test_prefill_balanced_schedule(pkv, orc):
     # more (row, kv head, query-tile pair) items than SMs: the persistent
-    # balanced schedule with FP8 widening producers, ragged rows, a window
+    # balanced schedule with FP8 widening, ragged rows, a window
     w = gen.prefill_workload(seed=398, dtype="bf16", num_q_heads=16, num_kv_heads=4, head_dim=128,
                              prefix_lens=[0, 5, 130, 300, 1000, 17, 64, 900],
                              chunk_lens=[600, 1, 64, 65, 300, 129, 512, 33], window=200)
