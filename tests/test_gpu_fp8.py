@@ -372,6 +372,19 @@ def test_prefill_balanced_schedule(pkv, orc):
     assert_close(_prefill(pkv, s, w, 200), ref, "bf16", "fp8 prefill, balanced schedule")
 
 
+def test_prefill_items_just_past_sms(pkv, orc):
+    # a few items more than SMs on FP8 pools: one whole item per CTA, then
+    # the few remaining items cut into many pieces merged in the kernel
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    rows = -(-(n_sm + 8) // 32)  # 8 kv heads x 4 query-tile pairs per row
+    w = gen.prefill_workload(seed=399, dtype="bf16", num_q_heads=32, num_kv_heads=8, head_dim=128,
+                             prefix_lens=[1500 - 41 * r for r in range(rows)], chunk_lens=[256] * rows)
+    s = Fp8Step(pkv, orc, w)
+    ref = orc.prefill(w.q, w.cu_q_lens, s.kp, s.vp, "fp8", w.block_tables, w.seq_lens, 0, w.scale,
+                      k_scale=KS, v_scale=VS)
+    assert_close(_prefill(pkv, s, w, 0), ref, "bf16", "fp8 prefill, items just past the SMs")
+
+
 def test_prefill_full_size(pkv, orc):
     # the chunked-prefill workload (4 x 512 queries after 16384 cached tokens)
     # on FP8 pools, sampled outputs
