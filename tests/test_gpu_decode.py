@@ -131,6 +131,24 @@ def test_prefix_groups_mixed(pkv, orc, dtype):
     assert_close(got2, ref, dtype, "no prefix path")
 
 
+def test_prefix_with_window_is_refused(pkv, orc):
+    # the shared-prefix path serves full attention only: a window with a
+    # prefix descriptor is refused before any launch, the output untouched
+    w = gen.decode_workload(seed=8, dtype="bf16", num_q_heads=8, num_kv_heads=2, head_dim=128,
+                            context_lens=[80, 81, 95, 96, 300, 1000], shared_prefix_tokens=80)
+    d = Dev(w)
+    append(pkv, d)
+    desc = pkv.make_prefix_desc(w.block_tables, w.seq_lens, w.block_size, d.k_pool.device)
+    out = torch.full_like(d.q, 7.0)
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.paged_decode_attention(d.q, d.k_pool, d.v_pool, d.tables, d.seq_lens, 64, w.scale,
+                                   max_seq_len=int(w.seq_lens.max()), prefix=desc, out=out,
+                                   status=d.status)
+    assert e.value.code == pkv.PKV_ERR_UNSUPPORTED
+    torch.cuda.synchronize()
+    assert bool((out == 7.0).all()) and int(d.status.item()) == 0
+
+
 def test_prefix_many_rows_two_chunks(pkv, orc):
     # 40 rows x 4 heads = 160 pairs: two row chunks of the prefix CTAs
     suf = [int(x) for x in gen.uniform_ints(9, "s", 40, 0, 300)]
